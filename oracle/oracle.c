@@ -1,0 +1,217 @@
+/*
+ * CPU oracle for the batched speculative-verify causal depthwise conv1d update.
+ *
+ * TEST INFRASTRUCTURE ONLY.  The tests, the package's smoke check and the bench's CPU-baseline leg
+ * may call this file; the product path never does.  It shares no code, header, table or helper
+ * with the CUDA library: it is a plain, slow, single-threaded loop that states the definition.
+ *
+ * What it computes, with the passages it follows:
+ *
+ *   - Causal depthwise conv1d update over T draft tokens (sglang PR #46184, "Motivation": verify
+ *     calls causal_conv1d_update with an intermediate conv window; Atlas fn
+ *     gdn_verify_fused_conv_kn_batched: all K draft positions in one launch).  For one channel c the
+ *     sequence is full = [state[o .. o+W-2], x_0 .. x_{T-1}] (W-1 committed inputs, then the T new
+ *     ones) and token t sees the W inputs full[t .. t+W-1]:
+ *         acc_t = bias[c] + sum_{j=0}^{W-1} w[c][j] * full[t+j]
+ *     so w[c][W-1] multiplies the newest input x_t (the textbook causal convolution).  fp32
+ *     accumulate, bias first, taps in ascending j, every product rounded before its add (no fused
+ *     multiply-add: this file is built with -ffp-contract=off).
+ *   - SiLU fused into the conv (glm5next_kda mod.rs, module doc "conv1d + SiLU -> L2(q,k only)"):
+ *         y_t = acc_t / (1 + exp(-acc_t))            in fp32.
+ *   - L2 normalisation of the q|k channels only, per head_dim group, exactly once, V never
+ *     (mod.rs "Decode conv fuses L2 ... q/k are normalised exactly once; V never"), with the
+ *     eps inside the square root (mod.rs Glm5NextKdaConfig::l2_eps: "1/sqrt(sum + eps), not
+ *     max(norm, eps)"):
+ *         y_t[c] *= 1 / sqrt(sum_{c' in group(c)} y_t[c']^2 + eps)     for c < qk_channels.
+ *     The sum runs over the group's channels in ascending order.  The result is rounded once to
+ *     the output type (round to nearest even for bf16).
+ *   - Per-token rollback snapshots (Atlas fn gdn_verify_fused_conv_kn_batched: "every per-token
+ *     conv-state rollback snapshot written inline"; mod.rs decode_k: snapshot t is the state AFTER
+ *     row t).  Snapshot t of channel c is the committed window after token t, full[t+1 .. t+W-1],
+ *     copied as raw bits.  Dense layout: element (s, t, c, k) at
+ *         s*seq + t*step + c*ch + k*col.
+ *     Deduplicated layout (sglang PR #46184, "Motivation" and "Modifications"): one
+ *     [dim, T+W-2] row per sequence seen as an overlapping [T, dim, W-1] view whose step stride
+ *     equals its column stride, so element (s, t, c, k) lives at s*seq + (t+k)*col + c*ch.  The
+ *     oracle writes every (t, k) of the view one by one: this is the per-token store path, which
+ *     the PR shows to hit the same addresses with the same values as the row written once.
+ *   - The state is left holding the committed window after the last token, full[T .. T+W-2]
+ *     (Atlas fn doc: "conv_state is left holding the committed (post final-position) window"),
+ *     written to state columns [0, W-1).  Columns at and above W-1 are not touched.
+ *   - Padded sequences (cache index < 0) touch nothing (PR #46184: "Padded rows still exit before
+ *     any store").
+ *   - An optional per-sequence offset o into the state row says where the committed window is
+ *     read (PR #46184 test coverage: "a num_accept_tokens state offset").
+ *   - Commit: restore the state to the snapshot of the accepted prefix (PR #46184: the window
+ *     "lets the conv state of the accepted prefix be restored after verify"; mod.rs decode_k:
+ *     snapshot t is what a partial accept rewinds to).  With a accepted tokens (1 <= a <= T) the
+ *     state becomes snapshot a-1.
+ *
+ * Status codes written per sequence (same meaning as the library's): 1 = cache slot out of range,
+ * 2 = state offset out of range, 4 = accept count out of range.  A flagged sequence is untouched.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+typedef struct {
+    int32_t n_seq, T, dim, width, qk_channels, head_dim;
+    int32_t is_bf16; /* 0: fp32 elements, 1: bf16 elements (every buffer) */
+    float l2_eps;
+    const void *x;
+    int64_t x_seq, x_tok;
+    void *out;
+    int64_t out_seq, out_tok;
+    void *state;
+    int32_t n_slots, state_cols;
+    int64_t st_slot, st_ch;
+    const int32_t *cache_idx; /* NULL: sequence s uses slot s */
+    const int32_t *state_off; /* NULL: offset 0 */
+    const void *weight;       /* [dim][W] */
+    const void *bias;         /* [dim] or NULL */
+    void *window;
+    int32_t dedup;
+    int64_t w_seq, w_step, w_ch, w_col;
+    int32_t *status; /* [n_seq] or NULL */
+} oracle_verify_args;
+
+typedef struct {
+    int32_t n_seq, T, dim, width, is_bf16;
+    void *state;
+    int32_t n_slots;
+    int64_t st_slot, st_ch;
+    const int32_t *cache_idx;
+    const void *window;
+    int32_t dedup;
+    int64_t w_seq, w_step, w_ch, w_col;
+    const int32_t *accept_len;
+    int32_t *status;
+} oracle_commit_args;
+
+/* ---- element access: raw bits, so copies keep NaN payloads and signed zeros ---- */
+
+static uint32_t get_bits(const void *base, int is_bf16, int64_t i) {
+    if (is_bf16) return ((const uint16_t *)base)[i];
+    return ((const uint32_t *)base)[i];
+}
+
+static void put_bits(void *base, int is_bf16, int64_t i, uint32_t v) {
+    if (is_bf16)
+        ((uint16_t *)base)[i] = (uint16_t)v;
+    else
+        ((uint32_t *)base)[i] = v;
+}
+
+static float bits_to_float(uint32_t v, int is_bf16) {
+    /* bf16 is the upper half of an IEEE binary32: widening is exact. */
+    uint32_t u = is_bf16 ? (v << 16) : v;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return f;
+}
+
+static uint32_t float_to_bits(float f, int is_bf16) {
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    if (!is_bf16) return u;
+    if ((u & 0x7fffffffu) > 0x7f800000u) return 0x7fc0u; /* any NaN -> quiet NaN */
+    /* round to nearest, ties to even, on the 16 dropped bits */
+    uint32_t keep_lsb = (u >> 16) & 1u;
+    u += 0x7fffu + keep_lsb;
+    return u >> 16;
+}
+
+static int64_t win_index(const oracle_verify_args *a, int s, int t, int c, int k) {
+    int64_t step = a->dedup ? a->w_col : a->w_step;
+    return (int64_t)s * a->w_seq + (int64_t)t * step + (int64_t)c * a->w_ch + (int64_t)k * a->w_col;
+}
+
+/* Returns 0; per-sequence problems go to status[]. */
+int oracle_conv_verify(const oracle_verify_args *a) {
+    const int W = a->width, T = a->T, dim = a->dim, bf = a->is_bf16;
+    uint32_t full[1024]; /* W-1 + T raw elements of one channel */
+    if (W < 1 || T < 1 || dim < 1 || W - 1 + T > 1024) return -1;
+    /* y[t*dim + c]: post-SiLU fp32 values of one sequence, normalised in place below */
+    float *y = (float *)malloc(sizeof(float) * (size_t)T * (size_t)dim);
+    if (!y) return -2;
+
+    for (int s = 0; s < a->n_seq; ++s) {
+        const int slot = a->cache_idx ? a->cache_idx[s] : s;
+        const int o = a->state_off ? a->state_off[s] : 0;
+        int st = 0;
+        if (slot >= 0 && slot >= a->n_slots) st |= 1;
+        if (slot >= 0 && (o < 0 || o + W - 1 > a->state_cols)) st |= 2;
+        if (a->status) a->status[s] = st;
+        if (slot < 0 || st) continue;
+
+        for (int c = 0; c < dim; ++c) {
+            const int64_t srow = (int64_t)slot * a->st_slot + (int64_t)c * a->st_ch;
+            for (int k = 0; k < W - 1; ++k) full[k] = get_bits(a->state, bf, srow + o + k);
+            for (int t = 0; t < T; ++t)
+                full[W - 1 + t] = get_bits(a->x, bf, (int64_t)s * a->x_seq + (int64_t)t * a->x_tok + c);
+
+            for (int t = 0; t < T; ++t) {
+                float acc = a->bias ? bits_to_float(get_bits(a->bias, bf, c), bf) : 0.0f;
+                for (int j = 0; j < W; ++j) {
+                    const float wj = bits_to_float(get_bits(a->weight, bf, (int64_t)c * W + j), bf);
+                    const float prod = wj * bits_to_float(full[t + j], bf);
+                    acc = acc + prod;
+                }
+                y[(int64_t)t * dim + c] = acc / (1.0f + expf(-acc));
+            }
+
+            /* snapshot t = window after token t = full[t+1 .. t+W-1] */
+            for (int t = 0; t < T; ++t)
+                for (int k = 0; k < W - 1; ++k) put_bits(a->window, bf, win_index(a, s, t, c, k), full[t + 1 + k]);
+
+            /* committed window after the last token, written after every read of this row */
+            for (int k = 0; k < W - 1; ++k) put_bits(a->state, bf, srow + k, full[T + k]);
+        }
+
+        for (int t = 0; t < T; ++t) {
+            float *yt = y + (int64_t)t * dim;
+            if (a->qk_channels > 0) {
+                const int hd = a->head_dim;
+                for (int g = 0; g + hd <= a->qk_channels; g += hd) {
+                    float ss = 0.0f;
+                    for (int c = g; c < g + hd; ++c) {
+                        const float sq = yt[c] * yt[c];
+                        ss = ss + sq;
+                    }
+                    const float r = 1.0f / sqrtf(ss + a->l2_eps);
+                    for (int c = g; c < g + hd; ++c) yt[c] = yt[c] * r;
+                }
+            }
+            for (int c = 0; c < dim; ++c)
+                put_bits(a->out, bf, (int64_t)s * a->out_seq + (int64_t)t * a->out_tok + c, float_to_bits(yt[c], bf));
+        }
+    }
+    free(y);
+    return 0;
+}
+
+int oracle_conv_commit(const oracle_commit_args *a) {
+    const int W = a->width, bf = a->is_bf16;
+    for (int s = 0; s < a->n_seq; ++s) {
+        const int slot = a->cache_idx ? a->cache_idx[s] : s;
+        int st = 0;
+        if (slot >= 0 && slot >= a->n_slots) st |= 1;
+        const int acc = a->accept_len[s];
+        if (slot >= 0 && (acc < 1 || acc > a->T)) st |= 4;
+        if (a->status) a->status[s] = st;
+        if (slot < 0 || st) continue;
+        const int t = acc - 1;
+        const int64_t step = a->dedup ? a->w_col : a->w_step;
+        for (int c = 0; c < a->dim; ++c)
+            for (int k = 0; k < W - 1; ++k) {
+                const int64_t src = (int64_t)s * a->w_seq + (int64_t)t * step + (int64_t)c * a->w_ch + (int64_t)k * a->w_col;
+                const int64_t dst = (int64_t)slot * a->st_slot + (int64_t)c * a->st_ch + k;
+                put_bits(a->state, bf, dst, get_bits(a->window, bf, src));
+            }
+    }
+    return 0;
+}
+
+/* Exposed so the tests can pin the rounding against an independent library conversion. */
+uint32_t oracle_round_f32_to_bf16(float f) { return float_to_bits(f, 1); }

@@ -1,0 +1,175 @@
+"""Seeded synthetic inputs for the batched speculative-verify conv1d update.
+
+This module only draws random inputs and allocates output buffers filled with a sentinel bit
+pattern.  It holds none of the method's arithmetic, so both the CUDA library's tests and the CPU
+oracle's tests can take their inputs from it.
+
+The five named workloads follow the shapes the pages describe:
+  * the sglang PR #46184 benchmark ("Benchmarking and Profiling": GB300, dim 10240, conv width 4,
+    bf16, T 8, batch 128) with the deduplicated window layout of MambaPool ("Motivation");
+  * the Atlas batched verify (fn gdn_verify_fused_conv_kn_batched: K draft positions, strided
+    input/output rows, dense intermediates) with the q|k|v conv weights bound as
+    concat([q, k, v]) (glm5next_kda mod.rs, "The checkpoint SPLITS the conv");
+  * a width-3 conv without L2 groups and with a per-sequence accepted-token state offset (PR
+    #46184 coverage: "a num_accept_tokens state offset"; width-3 deduplicated windows are
+    named in its "Scope").
+Values: x, state ~ N(0, 1), weights ~ U(-0.5, 0.5), bias ~ N(0, 0.1); bf16 values are drawn in
+fp32 and converted by torch (round to nearest even).
+"""
+from __future__ import annotations
+
+import dataclasses
+from typing import Optional
+
+import numpy as np
+import torch
+
+# Sentinel bit patterns for buffers that must stay untouched (bf16: a finite negative number;
+# fp32: a finite negative number), so an untouched region compares bitwise.
+SENTINEL_BF16 = 0xDEAD
+SENTINEL_F32 = 0xDEADBEEF
+
+
+@dataclasses.dataclass(frozen=True)
+class VerifyWorkload:
+    name: str
+    n_seq: int
+    T: int
+    dim: int
+    width: int
+    qk_channels: int
+    head_dim: int
+    dtype: str  # "f32" or "bf16"
+    layout: str  # "dense" or "dedup"
+    bias: bool = False
+    l2_eps: float = 1e-6
+    n_pad: int = 0  # sequences whose cache index is -1
+    extra_slots: int = 0  # pool slots no sequence uses (must stay untouched)
+    x_row_stride: Optional[int] = None  # token stride of x when it is a slice of a wider buffer
+    qkv_split: Optional[tuple] = None  # (q, k, v) channel counts of separately drawn conv weights
+    state_offset: bool = False  # per-sequence offset = accept_len - 1 into a wider state row
+    seed: int = 0
+
+    @property
+    def n_slots(self) -> int:
+        return self.n_seq + self.extra_slots
+
+    @property
+    def state_cols(self) -> int:
+        return self.width - 1 + (self.T - 1 if self.state_offset else 0)
+
+    @property
+    def torch_dtype(self):
+        return torch.float32 if self.dtype == "f32" else torch.bfloat16
+
+    @property
+    def esize(self) -> int:
+        return 4 if self.dtype == "f32" else 2
+
+    def replace(self, **kw) -> "VerifyWorkload":
+        return dataclasses.replace(self, **kw)
+
+
+# The five workloads.  The first finishes in the oracle in milliseconds; the third is the
+# benchmark configuration of the PR's table.
+WORKLOADS = {
+    w.name: w
+    for w in [
+        VerifyWorkload("n1_t2_dim512_w4_f32_dense", n_seq=1, T=2, dim=512, width=4, qk_channels=256,
+                       head_dim=64, dtype="f32", layout="dense", seed=0),
+        VerifyWorkload("n4_t4_dim4096_w4_bf16_dedup_bias", n_seq=4, T=4, dim=4096, width=4,
+                       qk_channels=2048, head_dim=128, dtype="bf16", layout="dedup", bias=True, seed=1),
+        VerifyWorkload("n128_t8_dim10240_w4_bf16_dedup_pad13", n_seq=128, T=8, dim=10240, width=4,
+                       qk_channels=4096, head_dim=128, dtype="bf16", layout="dedup", n_pad=13,
+                       extra_slots=16, seed=2),
+        VerifyWorkload("n8_t17_dim8192_w4_bf16_dense_qkvsplit_xstride12288", n_seq=8, T=17, dim=8192,
+                       width=4, qk_channels=4096, head_dim=128, dtype="bf16", layout="dense",
+                       x_row_stride=12288, qkv_split=(2048, 2048, 4096), seed=3),
+        VerifyWorkload("n64_t8_dim6144_w3_bf16_dense_nol2_stateoff", n_seq=64, T=8, dim=6144, width=3,
+                       qk_channels=0, head_dim=128, dtype="bf16", layout="dense", state_offset=True,
+                       seed=4),
+    ]
+}
+WORKLOAD_ORDER = list(WORKLOADS)
+BENCH_WORKLOAD = "n128_t8_dim10240_w4_bf16_dedup_pad13"
+
+
+def _to_dtype(a: np.ndarray, dtype) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to(dtype)
+
+
+def sentinel_tensor(shape, dtype) -> torch.Tensor:
+    """A CPU tensor whose every element holds the sentinel bit pattern."""
+    if dtype == torch.bfloat16:
+        return torch.full(shape, SENTINEL_BF16 - 65536, dtype=torch.int16).view(torch.bfloat16)
+    return torch.full(shape, SENTINEL_F32 - 2**32, dtype=torch.int32).view(torch.float32)
+
+
+def window_shape(w: VerifyWorkload):
+    if w.layout == "dense":
+        return (w.n_seq, w.T, w.dim, w.width - 1)
+    return (w.n_seq, w.dim, w.T + w.width - 2)
+
+
+def make_inputs(w: VerifyWorkload, seed: Optional[int] = None) -> dict:
+    """CPU tensors for one verify + commit of workload ``w``.
+
+    Returns x [n_seq, T, dim] (a view with token stride ``x_row_stride`` when set), conv_state
+    [n_slots, dim, state_cols], weight [dim, W], bias [dim] or None, cache_idx int32 [n_seq]
+    (-1 = padded), state_off int32 [n_seq] or None, accept_len int32 [n_seq] in 1..T, and
+    sentinel-filled out [n_seq, T, dim] and window buffers (dense [n_seq, T, dim, W-1], dedup
+    [n_seq, dim, T+W-2]).
+    """
+    rng = np.random.default_rng(w.seed if seed is None else seed)
+    dt = w.torch_dtype
+    row = w.x_row_stride or w.dim
+    xw = rng.standard_normal((w.n_seq * w.T, row), dtype=np.float32)
+    x_wide = _to_dtype(xw, dt)
+    x = x_wide.view(w.n_seq, w.T, row)[:, :, : w.dim]
+    state = _to_dtype(rng.standard_normal((w.n_slots, w.dim, w.state_cols), dtype=np.float32), dt)
+    if w.qkv_split:
+        parts = [rng.uniform(-0.5, 0.5, size=(n, 1, w.width)).astype(np.float32) for n in w.qkv_split]
+        weight = _to_dtype(np.concatenate(parts, axis=0), dt).squeeze(1)
+        assert weight.shape == (w.dim, w.width)
+    else:
+        weight = _to_dtype(rng.uniform(-0.5, 0.5, size=(w.dim, w.width)).astype(np.float32), dt)
+    bias = _to_dtype(rng.normal(0.0, 0.1, size=(w.dim,)).astype(np.float32), dt) if w.bias else None
+    perm = rng.permutation(w.n_slots)[: w.n_seq].astype(np.int32)
+    if w.n_pad:
+        pad = rng.permutation(w.n_seq)[: w.n_pad]
+        perm[pad] = -1
+    cache_idx = torch.from_numpy(perm.copy())
+    accept = torch.from_numpy(rng.integers(1, w.T + 1, size=w.n_seq).astype(np.int32))
+    state_off = (accept - 1).to(torch.int32) if w.state_offset else None
+    out = sentinel_tensor((w.n_seq, w.T, w.dim), dt)
+    window = sentinel_tensor(window_shape(w), dt)
+    return dict(x=x, x_base=x_wide, conv_state=state, weight=weight, bias=bias, cache_idx=cache_idx,
+                state_off=state_off, accept_len=accept, out=out, window=window)
+
+
+def random_case(rng: np.random.Generator, **over) -> VerifyWorkload:
+    """A small random workload for sweeps (shapes drawn from the ranges the pages test)."""
+    W = int(over.pop("width", rng.integers(2, 5)))
+    T = int(over.pop("T", rng.choice([1, 2, 3, 4, 8, 9, 16, 17])))
+    hd = int(over.pop("head_dim", rng.choice([8, 16, 32, 64, 128])))
+    groups = int(rng.integers(0, 5))
+    qk = over.pop("qk_channels", groups * hd)
+    dim = int(over.pop("dim", qk + int(rng.integers(1, 300))))
+    return VerifyWorkload(
+        name=over.pop("name", "random"), n_seq=int(over.pop("n_seq", rng.integers(1, 6))), T=T, dim=dim,
+        width=W, qk_channels=int(qk), head_dim=hd, dtype=over.pop("dtype", str(rng.choice(["f32", "bf16"]))),
+        layout=over.pop("layout", str(rng.choice(["dense", "dedup"]))), bias=bool(over.pop("bias", rng.integers(0, 2))),
+        seed=int(over.pop("seed", rng.integers(0, 2**31))), **over)
+
+
+def algorithmic_bytes(w: VerifyWorkload, n_active: Optional[int] = None) -> dict:
+    """Bytes the verify and the commit must move (each element once), per the data movement of
+    the method: x read, committed window read, outputs written, snapshots written, state written;
+    weights and bias read once; the int32 index arrays once."""
+    e = w.esize
+    n = (w.n_seq - w.n_pad) if n_active is None else n_active
+    win_cols = (w.T + w.width - 2) if w.layout == "dedup" else w.T * (w.width - 1)
+    per_seq = (w.T * w.dim + (w.width - 1) * w.dim + w.T * w.dim + win_cols * w.dim + (w.width - 1) * w.dim) * e
+    shared = (w.dim * w.width + (w.dim if w.bias else 0)) * e + 4 * w.n_seq * (1 + (1 if w.state_offset else 0))
+    commit = n * 2 * (w.width - 1) * w.dim * e + 8 * w.n_seq
+    return dict(verify=n * per_seq + shared, commit=commit, per_seq=per_seq)

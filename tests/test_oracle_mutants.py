@@ -1,0 +1,64 @@
+"""The pins reject plausible mistakes: each test plants one mistake in a copy of the oracle (on the
+CPU), builds it, and checks that the named pin fails against it while the real oracle passes."""
+from __future__ import annotations
+
+import os
+import shutil
+import subprocess
+
+import pytest
+
+import oracle
+import test_oracle_pins as pins
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "oracle.c")
+
+# (id, text in oracle.c, planted replacement, pin that must fail).  Every planted mistake keeps all
+# accesses inside the test's buffers.
+MUTANTS = [
+    ("taps_reversed", "bits_to_float(full[t + j], bf)", "bits_to_float(full[t + W - 1 - j], bf)",
+     lambda: pins.test_p2_impulse_response()),
+    ("bias_dropped", "float acc = a->bias ? bits_to_float(get_bits(a->bias, bf, c), bf) : 0.0f;", "float acc = 0.0f;",
+     lambda: pins.test_p1_matches_float64_conv1d("f32", "dense", 4)),
+    ("silu_sign", "acc / (1.0f + expf(-acc))", "acc / (1.0f + expf(acc))",
+     lambda: pins.test_p1_matches_float64_conv1d("f32", "dense", 3)),
+    ("eps_as_norm_floor", "1.0f / sqrtf(ss + a->l2_eps)", "1.0f / fmaxf(sqrtf(ss), a->l2_eps)",
+     lambda: pins.test_p3_one_hot_taps_and_constant_group()),
+    ("snapshot_off_by_one", "full[t + 1 + k])", "full[t + k])",
+     lambda: pins.test_p4_sequential_equals_batched_in_T("dense", "f32")),
+    ("state_write_lags", "put_bits(a->state, bf, srow + k, full[T + k])", "put_bits(a->state, bf, srow + k, full[T - 1 + k])",
+     lambda: pins.test_p11_single_token_update()),
+    ("offset_ignored", "get_bits(a->state, bf, srow + o + k)", "get_bits(a->state, bf, srow + k)",
+     lambda: pins.test_p10_state_offset_equals_preshifted_state()),
+    ("commit_wrong_snapshot", "const int t = acc - 1;", "const int t = acc < a->T ? acc : acc - 1;",
+     lambda: pins.test_p9_commit_equals_shorter_verify("dedup")),
+    ("v_normalised", "g + hd <= a->qk_channels", "g + hd <= dim",
+     lambda: pins.test_p8_group_norms_and_v_passthrough()),
+    ("bf16_truncates", "u += 0x7fffu + keep_lsb;", "(void)keep_lsb;",
+     lambda: pins.test_bf16_rounding_matches_torch()),
+    ("dedup_step_uses_ch", "int64_t step = a->dedup ? a->w_col : a->w_step;", "int64_t step = a->dedup ? 0 : a->w_step;",
+     lambda: pins.test_p6_dedup_view_equals_dense(4)),
+    ("padded_row_written", "if (slot < 0 || st) continue;\n\n", "if (st) continue;\n        if (slot < 0) { if (a->out) put_bits(a->out, bf, (int64_t)s * a->out_seq, 0); continue; }\n\n",
+     lambda: pins.test_p7_padded_rows_untouched()),
+]
+
+
+@pytest.mark.parametrize("mid,old,new,pin", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_pin_rejects_planted_mistake(tmp_path, mid, old, new, pin):
+    if shutil.which("gcc") is None:
+        pytest.skip("gcc not available")
+    src = open(SRC).read()
+    assert src.count(old) >= 1, f"mutation site for {mid} not found"
+    mut = src.replace(old, new, 1)
+    c = tmp_path / f"{mid}.c"
+    so = tmp_path / f"{mid}.so"
+    c.write_text(mut)
+    subprocess.run(["gcc", "-O2", "-std=c99", "-ffp-contract=off", "-shared", "-fPIC", "-o", str(so), str(c), "-lm"],
+                   check=True)
+    pin()  # the real oracle passes this pin
+    prev = oracle.swap_library(str(so))
+    try:
+        with pytest.raises(AssertionError):
+            pin()
+    finally:
+        oracle.swap_library(prev)

@@ -1,0 +1,388 @@
+"""Pins of the CPU oracle against facts fixed by the pages and by mathematics (no GPU).
+
+Each test names the passage it pins.  None of them re-types the oracle's formula: they use a
+library special case (torch float64 conv1d), closed forms, the pages' invariants (sequential ==
+batched-in-T, batched over sequences == separate runs, deduplicated view == dense view, padded rows
+untouched, commit == shorter verify) and the pages' printed row layout (tests/golden).
+"""
+from __future__ import annotations
+
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+import torch.nn.functional as F
+
+import oracle
+from helpers import (assert_bits_equal, assert_out_close, bf16_ordinal, bits, clone_inputs, run_oracle_commit,
+                     run_oracle_verify)
+from spec_decode_verify_gb300 import workloads as wl
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def small(**kw) -> wl.VerifyWorkload:
+    base = dict(name="small", n_seq=3, T=5, dim=96, width=4, qk_channels=64, head_dim=16, dtype="f32",
+                layout="dense", bias=True, seed=11)
+    base.update(kw)
+    return wl.VerifyWorkload(**base)
+
+
+def float64_reference(w: wl.VerifyWorkload, inp: dict):
+    """Library special case: the causal depthwise conv is torch conv1d with groups=dim, 'valid'
+    padding, over [committed window, x]; SiLU and the per-group L2 in float64."""
+    outs, states, wins = {}, {}, {}
+    for s in range(w.n_seq):
+        slot = int(inp["cache_idx"][s])
+        if slot < 0:
+            continue
+        o = int(inp["state_off"][s]) if inp["state_off"] is not None else 0
+        win = inp["conv_state"][slot, :, o:o + w.width - 1].double()
+        xs = inp["x"][s].double().t()
+        full = torch.cat([win, xs], dim=1)
+        acc = F.conv1d(full[None], inp["weight"].double()[:, None, :],
+                       inp["bias"].double() if inp["bias"] is not None else None, groups=w.dim)[0]
+        assert acc.shape == (w.dim, w.T)
+        y = acc / (1.0 + torch.exp(-acc))
+        for g in range(0, w.qk_channels, w.head_dim):
+            blk = y[g:g + w.head_dim]
+            y[g:g + w.head_dim] = blk / torch.sqrt((blk * blk).sum(0, keepdim=True) + w.l2_eps)
+        outs[s] = y.t()
+        states[s] = full[:, w.T:w.T + w.width - 1]
+        wins[s] = full
+    return outs, states, wins
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("layout", ["dense", "dedup"])
+@pytest.mark.parametrize("width", [2, 3, 4])
+def test_p1_matches_float64_conv1d(dtype, layout, width):
+    """P-1: conv part == torch conv1d(groups=dim) in float64, then SiLU and L2 in float64."""
+    w = small(dtype=dtype, layout=layout, width=width, l2_eps=0.25, n_pad=1, extra_slots=2, seed=100 + width)
+    inp = wl.make_inputs(w)
+    r = run_oracle_verify(w, inp)
+    outs, states, _ = float64_reference(w, inp)
+    for s, ref in outs.items():
+        got = r["out"][s]
+        if dtype == "f32":
+            err = (got.double() - ref).abs()
+            assert (err <= 1e-5 * ref.abs() + 1e-6).all(), float(err.max())
+        else:
+            d = np.abs(bf16_ordinal(bits(got)) - bf16_ordinal(bits(ref.to(torch.bfloat16))))
+            assert d.max() <= 1, int(d.max())
+        slot = int(inp["cache_idx"][s])
+        assert torch.equal(r["conv_state"][slot, :, :width - 1].double(), states[s])
+
+
+def test_p2_impulse_response():
+    """P-2 (closed form): zero state, x = unit impulse at t = 0, no bias: acc[t] = w[c][W-1-t] for
+    t < W and 0 afterwards (the newest input meets the last tap)."""
+    w = small(T=7, width=4, qk_channels=0, bias=False)
+    inp = wl.make_inputs(w)
+    inp["conv_state"].zero_()
+    inp["x"].zero_()
+    inp["x"][:, 0, :] = 1.0
+    r = run_oracle_verify(w, inp)
+    for s in range(w.n_seq):
+        for t in range(w.T):
+            acc = inp["weight"][:, w.width - 1 - t].double() if t < w.width else torch.zeros(w.dim, dtype=torch.float64)
+            ref = acc / (1 + torch.exp(-acc))
+            assert torch.allclose(r["out"][s, t].double(), ref, rtol=1e-6, atol=1e-7)
+
+
+def test_p3_one_hot_taps_and_constant_group():
+    """P-3 (closed forms): one-hot weights w = e_j give acc[t] = full[t+j] exactly; a group whose
+    channels all carry the same value v normalises to v / sqrt(hd v^2 + eps)."""
+    w = small(T=4, width=4, qk_channels=0, bias=False, dtype="f32")
+    for j in range(4):
+        inp = wl.make_inputs(w)
+        inp["weight"].zero_()
+        inp["weight"][:, j] = 1.0
+        r = run_oracle_verify(w, inp)
+        for s in range(w.n_seq):
+            slot = int(inp["cache_idx"][s])
+            full = torch.cat([inp["conv_state"][slot, :, :3], inp["x"][s].t()], dim=1).double()
+            for t in range(w.T):
+                a = full[:, t + j]
+                assert torch.allclose(r["out"][s, t].double(), a / (1 + torch.exp(-a)), rtol=1e-6, atol=1e-7)
+    # constant group, eps large enough to tell sqrt(ss + eps) from max(norm, eps)
+    hd, eps = 16, 0.75
+    w = small(T=2, width=2, qk_channels=32, head_dim=hd, dim=48, bias=False, l2_eps=eps, n_seq=1)
+    inp = wl.make_inputs(w)
+    inp["weight"].zero_()
+    inp["weight"][:, 1] = 1.0
+    inp["x"][0, 0, :] = 0.5
+    inp["x"][0, 1, :] = -2.0
+    r = run_oracle_verify(w, inp)
+    for t, v in enumerate([0.5, -2.0]):
+        y = v / (1 + math.exp(-v))
+        want = y / math.sqrt(hd * y * y + eps)
+        assert torch.allclose(r["out"][0, t, :32].double(), torch.full((32,), want, dtype=torch.float64), rtol=1e-6)
+        assert torch.allclose(r["out"][0, t, 32:].double(), torch.full((16,), y, dtype=torch.float64), rtol=1e-6)
+
+
+@pytest.mark.parametrize("layout", ["dense", "dedup"])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_p4_sequential_equals_batched_in_T(layout, dtype):
+    """P-4: T single-token updates equal one T-token verify: outputs and state bit-exact, and
+    snapshot t equals the state after token t (Atlas: K positions in one launch replace K
+    per-token updates + K copies; the K=2 twin is bit-identical; mod.rs decode_k: snapshot t is
+    the state after row t)."""
+    w = small(T=6, dtype=dtype, layout=layout)
+    inp = wl.make_inputs(w)
+    full = run_oracle_verify(w, inp)
+    w1 = w.replace(T=1, layout="dense")
+    cur = clone_inputs(inp)
+    for t in range(w.T):
+        step = dict(cur)
+        step["x"] = inp["x"][:, t:t + 1, :]
+        step["out"] = wl.sentinel_tensor((w.n_seq, 1, w.dim), w.torch_dtype)
+        step["window"] = wl.sentinel_tensor(wl.window_shape(w1), w.torch_dtype)
+        r1 = run_oracle_verify(w1, step)
+        assert_bits_equal(r1["out"][:, 0], full["out"][:, t], f"out token {t}")
+        for s in range(w.n_seq):
+            slot = int(inp["cache_idx"][s])
+            snap = r1["conv_state"][slot, :, :w.width - 1]
+            if layout == "dense":
+                got = full["window"][s, t]
+            else:
+                got = full["window"][s, :, t:t + w.width - 1]
+            assert_bits_equal(got, snap, f"snapshot {t} seq {s}")
+        cur["conv_state"] = r1["conv_state"]
+    assert_bits_equal(full["conv_state"], cur["conv_state"], "final state")
+
+
+def test_p5_batched_equals_separate():
+    """P-5: a batched run equals n separate single-sequence runs bit for bit (Atlas batched doc:
+    bit-identical to n separate calls; only the base addresses differ)."""
+    w = small(n_seq=4, dtype="bf16", layout="dedup", n_pad=1, extra_slots=3)
+    inp = wl.make_inputs(w)
+    r = run_oracle_verify(w, inp)
+    for s in range(w.n_seq):
+        one = clone_inputs(inp)
+        ws = w.replace(n_seq=1, n_pad=0)
+        one["x"] = inp["x"][s:s + 1]
+        one["cache_idx"] = inp["cache_idx"][s:s + 1].clone()
+        one["out"] = wl.sentinel_tensor((1, w.T, w.dim), w.torch_dtype)
+        one["window"] = wl.sentinel_tensor(wl.window_shape(ws), w.torch_dtype)
+        r1 = run_oracle_verify(ws, one)
+        assert_bits_equal(r1["out"][0], r["out"][s], "out")
+        assert_bits_equal(r1["window"][0], r["window"][s], "window")
+        slot = int(inp["cache_idx"][s])
+        if slot >= 0:
+            assert_bits_equal(r1["conv_state"][slot], r["conv_state"][slot], "state")
+
+
+@pytest.mark.parametrize("width", [2, 3, 4])
+def test_p6_dedup_view_equals_dense(width):
+    """P-6: the deduplicated row read through its overlapping [T, dim, W-1] view gives the dense
+    snapshots bitwise (PR #46184: step stride == window stride makes both writes land on the
+    same addresses with the same values); also through the transposed row layout."""
+    w = small(width=width, dtype="bf16", T=8)
+    inp = wl.make_inputs(w)
+    dense = run_oracle_verify(w, inp)
+    wd = w.replace(layout="dedup")
+    inp_d = clone_inputs(inp)
+    inp_d["window"] = wl.sentinel_tensor(wl.window_shape(wd), w.torch_dtype)
+    dedup = run_oracle_verify(wd, inp_d)
+    row = dedup["window"]
+    view = row.as_strided((w.n_seq, w.T, w.dim, width - 1), (row.stride(0), row.stride(2), row.stride(1), row.stride(2)))
+    assert_bits_equal(view, dense["window"], "dedup view vs dense")
+    assert_bits_equal(dedup["out"], dense["out"], "out")
+    assert_bits_equal(dedup["conv_state"], dense["conv_state"], "state")
+    # transposed row layout ([n_seq, T+W-2, dim] storage seen as [n_seq, dim, T+W-2])
+    inp_t = clone_inputs(inp)
+    inp_t["window"] = wl.sentinel_tensor((w.n_seq, w.T + width - 2, w.dim), w.torch_dtype).transpose(1, 2)
+    tr = run_oracle_verify(wd, inp_t)
+    assert_bits_equal(tr["window"], row, "transposed row")
+
+
+def test_p7_padded_rows_untouched():
+    """P-7: padded sequences (cache index -1) leave their out rows, window rows and every unused
+    slot untouched (PR #46184: padded rows exit before any store)."""
+    w = small(n_seq=6, n_pad=3, extra_slots=4, dtype="bf16", layout="dedup")
+    inp = wl.make_inputs(w)
+    r = run_oracle_verify(w, inp)
+    used = {int(v) for v in inp["cache_idx"] if v >= 0}
+    for s in range(w.n_seq):
+        if int(inp["cache_idx"][s]) < 0:
+            assert_bits_equal(r["out"][s], inp["out"][s], "padded out")
+            assert_bits_equal(r["window"][s], inp["window"][s], "padded window")
+            assert int(r["status"][s]) == 0
+    for slot in range(w.n_slots):
+        if slot not in used:
+            assert_bits_equal(r["conv_state"][slot], inp["conv_state"][slot], f"unused slot {slot}")
+
+
+def test_p8_group_norms_and_v_passthrough():
+    """P-8: every q|k group of every token has norm sqrt(ss / (ss + eps)) = 1 to within the fp32
+    rounding of the sum; V channels equal a run without L2 bitwise (mod.rs: q/k normalised
+    exactly once, V never)."""
+    w = small(dim=160, qk_channels=128, head_dim=32, T=6, dtype="f32")
+    inp = wl.make_inputs(w)
+    r = run_oracle_verify(w, inp)
+    r0 = run_oracle_verify(w.replace(qk_channels=0), inp)
+    out = r["out"].double()
+    for g in range(0, 128, 32):
+        n = out[:, :, g:g + 32].pow(2).sum(-1).sqrt()
+        assert torch.allclose(n, torch.ones_like(n), atol=2e-6)
+    assert_bits_equal(r["out"][:, :, 128:], r0["out"][:, :, 128:], "V channels")
+    wb = w.replace(dtype="bf16")
+    rb = run_oracle_verify(wb, wl.make_inputs(wb))
+    ob = rb["out"].double()
+    for g in range(0, 128, 32):
+        n = ob[:, :, g:g + 32].pow(2).sum(-1).sqrt()
+        assert torch.allclose(n, torch.ones_like(n), atol=2 ** -8)
+
+
+@pytest.mark.parametrize("layout", ["dense", "dedup"])
+def test_p9_commit_equals_shorter_verify(layout):
+    """P-9: verify(T) then commit(a) leaves the state of verify over the first a tokens, bitwise
+    (the window lets the accepted prefix's state be restored)."""
+    w = small(n_seq=5, T=7, dtype="bf16", layout=layout, n_pad=1, extra_slots=2)
+    inp = wl.make_inputs(w)
+    r = run_oracle_verify(w, inp)
+    st = run_oracle_commit(w, r)
+    assert (st == 0).all()
+    for s in range(w.n_seq):
+        slot = int(inp["cache_idx"][s])
+        if slot < 0:
+            continue
+        a = int(inp["accept_len"][s])
+        wa = w.replace(T=a, n_seq=1, n_pad=0)
+        one = clone_inputs(inp)
+        one["x"] = inp["x"][s:s + 1, :a]
+        one["cache_idx"] = inp["cache_idx"][s:s + 1].clone()
+        one["out"] = wl.sentinel_tensor((1, a, w.dim), w.torch_dtype)
+        one["window"] = wl.sentinel_tensor(wl.window_shape(wa), w.torch_dtype)
+        ra = run_oracle_verify(wa, one)
+        assert_bits_equal(r["conv_state"][slot], ra["conv_state"][slot], f"seq {s} accept {a}")
+
+
+def test_p10_state_offset_equals_preshifted_state():
+    """P-10: reading the committed window at offset o equals reading a state pre-shifted to offset
+    0 (PR #46184 covers a num_accept_tokens state offset)."""
+    w = small(n_seq=4, T=5, width=3, state_offset=True, dtype="bf16", qk_channels=0)
+    inp = wl.make_inputs(w)
+    r = run_oracle_verify(w, inp)
+    for s in range(w.n_seq):
+        slot = int(inp["cache_idx"][s])
+        o = int(inp["state_off"][s])
+        one = clone_inputs(inp)
+        ws = w.replace(n_seq=1, state_offset=False)
+        shifted = inp["conv_state"][slot:slot + 1, :, o:o + w.width - 1].clone()
+        one["conv_state"] = shifted
+        one["x"] = inp["x"][s:s + 1]
+        one["cache_idx"] = torch.zeros(1, dtype=torch.int32)
+        one["state_off"] = None
+        one["out"] = wl.sentinel_tensor((1, w.T, w.dim), w.torch_dtype)
+        one["window"] = wl.sentinel_tensor(wl.window_shape(ws), w.torch_dtype)
+        r1 = run_oracle_verify(ws, one)
+        assert_bits_equal(r1["out"][0], r["out"][s], "out")
+        assert_bits_equal(r1["window"][0], r["window"][s], "window")
+        assert_bits_equal(r1["conv_state"][0], r["conv_state"][slot, :, :w.width - 1], "committed window")
+        # columns at and above W-1 are untouched
+        assert_bits_equal(r["conv_state"][slot, :, w.width - 1:], inp["conv_state"][slot, :, w.width - 1:], "tail")
+
+
+def test_p11_single_token_update():
+    """P-11: T = 1 is the standard single-token causal conv update: the state shifts left by one
+    and takes x; out = SiLU(sum_j w_j [state, x]_j + bias)."""
+    w = small(T=1, qk_channels=0, dtype="f32")
+    inp = wl.make_inputs(w)
+    r = run_oracle_verify(w, inp)
+    for s in range(w.n_seq):
+        slot = int(inp["cache_idx"][s])
+        st = inp["conv_state"][slot]
+        want_state = torch.cat([st[:, 1:], inp["x"][s, 0][:, None]], dim=1)
+        assert_bits_equal(r["conv_state"][slot], want_state, "shifted state")
+        full = torch.cat([st, inp["x"][s, 0][:, None]], dim=1).double()
+        acc = (full * inp["weight"].double()).sum(1) + inp["bias"].double()
+        assert torch.allclose(r["out"][s, 0].double(), acc / (1 + torch.exp(-acc)), rtol=1e-5, atol=1e-6)
+
+
+def test_bf16_rounding_matches_torch():
+    """The oracle's fp32 -> bf16 rounding (nearest, ties to even) equals torch's conversion on
+    random values, ties, subnormals, infinities and signed zeros."""
+    rng = np.random.default_rng(5)
+    vals = np.concatenate([
+        rng.standard_normal(20000).astype(np.float32) * np.float32(10.0) ** rng.integers(-40, 39, 20000),
+        np.array([0.0, -0.0, np.inf, -np.inf, 1e-45, -1e-45, 3.4e38, 1.0 + 2 ** -8, 1.0 + 3 * 2 ** -8,
+                  1.0 + 2 ** -8 + 2 ** -20, 1.17e-38, 5.9e-39], dtype=np.float32)])
+    ref = torch.from_numpy(vals).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    got = np.array([oracle.round_f32_to_bf16_bits(float(v)) for v in vals], dtype=np.uint16)
+    assert np.array_equal(got, ref)
+    assert oracle.round_f32_to_bf16_bits(float("nan")) & 0x7FFF > 0x7F80
+
+
+def _read_golden(name):
+    rows = []
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.split("#", 1)[0].strip()
+            if line:
+                rows.append(line)
+    return rows
+
+
+def test_golden_dedup_row_columns():
+    """The page's printed row layout (tests/golden/dedup_row_columns.txt): step t's window is columns
+    t..t+2 of [state[1], state[2], x_0, ..., x_{T-1}], T+2 columns, for the T values it tests."""
+    for line in _read_golden("dedup_row_columns.txt"):
+        T_s, cols = line.split(":")
+        T = int(T_s)
+        labels = cols.split()
+        assert len(labels) == T + 2
+        w = small(n_seq=1, T=T, dim=8, width=4, qk_channels=0, dtype="f32", layout="dedup", bias=False)
+        inp = wl.make_inputs(w)
+        slot = int(inp["cache_idx"][0])
+        # every input gets a distinct exactly representable tag
+        for k in range(3):
+            inp["conv_state"][slot, :, k] = 1000.0 + k
+        for t in range(T):
+            inp["x"][0, t, :] = 2000.0 + t
+        r = run_oracle_verify(w, inp)
+        tag = {f"state[{k}]": 1000.0 + k for k in range(3)}
+        tag.update({f"x_{t}": 2000.0 + t for t in range(T)})
+        want = torch.tensor([tag[l] for l in labels], dtype=torch.float32)
+        for c in range(w.dim):
+            assert torch.equal(r["window"][0, c], want)
+            for t in range(T):
+                assert torch.equal(r["window"][0, c, t:t + 3], want[t:t + 3])
+
+
+def test_status_codes_and_untouched():
+    """Out-of-range slot, state offset or accept count flags the sequence and touches nothing."""
+    w = small(n_seq=4, T=4, state_offset=True, dtype="bf16")
+    inp = wl.make_inputs(w)
+    inp["cache_idx"][0] = w.n_slots  # slot out of range
+    inp["state_off"][1] = w.state_cols - w.width + 2  # window would run past the row
+    inp["state_off"][2] = -1
+    r = run_oracle_verify(w, inp)
+    assert r["status"].tolist()[:3] == [1, 2, 2] and int(r["status"][3]) == 0
+    for s in range(3):
+        assert_bits_equal(r["out"][s], inp["out"][s], "flagged out")
+        assert_bits_equal(r["window"][s], inp["window"][s], "flagged window")
+    acc = inp["accept_len"].clone()
+    acc[3] = w.T + 1
+    before = r["conv_state"].clone()
+    st = run_oracle_commit(w, r, accept_len=acc)
+    assert int(st[3]) == 4 and int(st[0]) == 1
+    slot3 = int(inp["cache_idx"][3])
+    assert_bits_equal(r["conv_state"][slot3], before[slot3], "rejected commit")
+
+
+def test_nan_and_signed_zero_copies():
+    """Snapshots and state are raw copies: NaN payloads and -0 survive; outputs follow IEEE."""
+    w = small(n_seq=1, T=3, dtype="bf16", layout="dense", qk_channels=0)
+    inp = wl.make_inputs(w)
+    slot = int(inp["cache_idx"][0])
+    inp["conv_state"].view(torch.int16)[slot, 0, 1] = 0x7FA1  # NaN with a payload
+    inp["x"].view(torch.int16)[0, 0, 1] = -32768  # -0.0
+    r = run_oracle_verify(w, inp)
+    wb = bits(r["window"])
+    assert wb[0, 0, 0, 0] == 0x7FA1
+    assert wb[0, 0, 1, 2] == 0x8000 and wb[0, 1, 1, 1] == 0x8000 and wb[0, 2, 1, 0] == 0x8000
+    assert np.isnan(r["out"][0, :2, 0].float().numpy()).all()
