@@ -1,0 +1,388 @@
+"""Benchmark of the batched speculative-verify conv1d update (verify + commit) on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
+
+A step is one pass of the whole path over one batch: cv_conv_verify (conv + SiLU + L2, snapshots,
+committed window) followed by cv_conv_commit (restore the accepted prefix).  Default workload: 128
+sequences x 8 draft tokens, dim 10240 (q|k 4096, head_dim 128), conv width 4, bf16, deduplicated
+window rows, 13 padded sequences.  Inputs are synthetic and already resident in HBM when the
+timed region starts; every step uses the next of several rotating buffer sets whose total size is
+at least four times the L2, so each step reads and writes HBM, not L2.
+
+Prints ONE JSON line (rank 0).  Under torchrun every rank runs its own batch (weak scaling, no
+collective on the data path); the step time is the maximum over ranks.  ``--impl reference`` times
+the CPU oracle (plain C loop, one core) on the same workload and prints the same kind of line.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from spec_decode_verify_gb300 import workloads as wl  # noqa: E402
+
+METRIC = "verify-conv µs/step and achieved HBM GB/s (% of GB300 peak), 1 GPU"
+UNIT = "us/step"
+HBM_NOMINAL_GBS = 8000.0  # the metric's roofline: bytes moved / 8 TB/s
+PROFILE = os.path.join(ROOT, "profiles", "verify_kernel_n128_t8_dim10240_bf16_dedup.md")
+KERNEL_SRC = os.path.join(ROOT, "spec_decode_verify_gb300", "csrc", "cv_kernels.cuh")
+
+
+def kernel_sha() -> str:
+    with open(KERNEL_SRC, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def measured_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def profile_traffic():
+    """DRAM bytes per verify launch from the committed ncu summary, if it matches this kernel."""
+    try:
+        text = open(PROFILE).read()
+    except OSError:
+        return None, None
+    m = re.search(r"bench-traffic: dram_bytes_per_launch=(\d+) kernel_sha=([0-9a-f]+)", text)
+    if not m:
+        return None, None
+    if m.group(2) != kernel_sha():
+        return None, "stale"
+    return int(m.group(1)), "ncu"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason sampler (200 ms) around the loaded region."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{index}.csv") if os.path.isdir(
+            os.path.join(ROOT, "gpurun_out")) else f"/tmp/cv_clocks_{os.getpid()}.csv"
+
+    def start(self):
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.fh,
+                                         stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if not self.proc:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.fh.close()
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append(dict(sm=float(parts[1]), smax=float(parts[2]), power=float(parts[3]),
+                                 hw=parts[5], hwt=parts[6], swt=parts[7], pcap=parts[8]))
+            except ValueError:
+                continue
+        if not rows:
+            return None
+        reasons = set()
+        for r in rows:
+            for k, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"), ("swt", "sw_thermal_slowdown"),
+                            ("pcap", "sw_power_cap")):
+                if r[k].lower() in ("active", "1", "yes"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r["sm"] for r in rows), "sm_max_mhz": max(r["smax"] for r in rows),
+                "reasons": sorted(reasons), "samples": len(rows),
+                "power_w_max": max(r["power"] for r in rows)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+        return world, rank, local, dist
+    return 1, 0, 0, None
+
+
+def reduce_max(dist, value: float, device) -> float:
+    if dist is None:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device if dist.get_backend() == "nccl" else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(dist, device):
+    if dist is not None:
+        if dist.get_backend() == "nccl":
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+# ----------------------------------------------------------------------------- CPU oracle timing
+
+def oracle_step_times(w, reps_max: int, budget_s: float):
+    """Time oracle verify + commit on the whole workload (one core); returns per-step seconds."""
+    import oracle
+    inp = wl.make_inputs(w)
+    times = []
+    t_begin = time.perf_counter()
+    for _ in range(reps_max):
+        state = inp["conv_state"].clone()
+        out = inp["out"].clone()
+        win = inp["window"].clone()
+        t0 = time.perf_counter()
+        oracle.conv_verify(inp["x"], state, inp["weight"], inp["bias"], out, win, layout=w.layout,
+                           qk_channels=w.qk_channels, head_dim=w.head_dim, l2_eps=w.l2_eps,
+                           cache_idx=inp["cache_idx"], state_off=inp["state_off"])
+        oracle.conv_commit(state, win, inp["accept_len"], layout=w.layout, T=w.T, width=w.width,
+                           cache_idx=inp["cache_idx"])
+        times.append(time.perf_counter() - t0)
+        if time.perf_counter() - t_begin > budget_s and len(times) >= 3:
+            break
+    return times
+
+
+def run_reference(args, w, world, rank):
+    if rank != 0:
+        return 0
+    import oracle
+    oracle.build()
+    warm = oracle_step_times(w, max(args.warmup, 1), 1e9)
+    times = oracle_step_times(w, args.steps, 1e9)
+    us = statistics.mean(times) * 1e6
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(us, 3), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(us / 1e3, 6), "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+        "config": workload_config(w, None),
+        "cpu_baseline": {"value": round(us, 3), "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": f"whole workload ({w.n_seq} sequences) per step, {len(times)} steps after "
+                                   f"{len(warm)} warm-up; plain C loop, one thread"},
+        "e2e": {"value": round(us, 3), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def workload_config(w, l2_note):
+    c = {"workload": w.name, "n_seq": w.n_seq, "padded_seqs": w.n_pad, "T": w.T, "dim": w.dim, "width": w.width,
+         "qk_channels": w.qk_channels, "head_dim": w.head_dim, "layout": w.layout, "bias": w.bias,
+         "step": "cv_conv_verify + cv_conv_commit"}
+    if l2_note:
+        c["l2"] = l2_note
+    return c
+
+
+# ----------------------------------------------------------------------------- GPU arm
+
+def run_ours(args, w, world, rank, local, dist):
+    import spec_decode_verify_gb300 as cv
+    from spec_decode_verify_gb300 import build as cvbuild
+
+    cvbuild.build()
+    lib = cv.load_library()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    sp = stream.cuda_stream
+
+    inp = wl.make_inputs(w, seed=w.seed + 1009 * rank)
+    props = torch.cuda.get_device_properties(dev)
+    l2 = getattr(props, "L2_cache_size", 0) or 129 * 2 ** 20
+    per_set = sum(inp[k].numel() * inp[k].element_size()
+                  for k in ("x_base", "conv_state", "out", "window"))
+    n_sets = max(2, math.ceil(4 * l2 / per_set))
+    l2_note = f"rotating {n_sets} buffer sets, {n_sets * per_set / 2**20:.0f} MiB >= 4x L2 ({l2 / 2**20:.0f} MiB)"
+
+    weight = inp["weight"].to(dev)
+    bias = inp["bias"].to(dev) if inp["bias"] is not None else None
+    cache_idx = inp["cache_idx"].to(dev)
+    state_off = inp["state_off"].to(dev) if inp["state_off"] is not None else None
+    sets = []
+    for i in range(n_sets):
+        xb = inp["x_base"].to(dev)
+        x = xb.as_strided(inp["x"].shape, inp["x"].stride(), inp["x"].storage_offset())
+        s = dict(x_base=xb, x=x, conv_state=inp["conv_state"].to(dev), out=inp["out"].to(dev),
+                 window=inp["window"].to(dev), accept=inp["accept_len"].to(dev))
+        s["va"] = cv.make_verify_args(x, s["conv_state"], weight, bias, s["out"], s["window"], layout=w.layout,
+                                      qk_channels=w.qk_channels, head_dim=w.head_dim, l2_eps=w.l2_eps,
+                                      cache_idx=cache_idx, state_off=state_off)
+        s["ca"] = cv.make_commit_args(s["conv_state"], s["window"], s["accept"], layout=w.layout, T=w.T,
+                                      width=w.width, cache_idx=cache_idx)
+        sets.append(s)
+    verify_fn, commit_fn = lib.cv_conv_verify, lib.cv_conv_commit
+    vrefs = [ctypes.byref(s["va"]) for s in sets]
+    crefs = [ctypes.byref(s["ca"]) for s in sets]
+
+    def step(i):
+        rc = verify_fn(vrefs[i % n_sets], sp)
+        rc |= commit_fn(crefs[i % n_sets], sp)
+        return rc
+
+    for i in range(args.warmup):
+        if step(i) != 0:
+            raise RuntimeError("launch failed during warm-up")
+    torch.cuda.synchronize(dev)
+
+    # clocks: sample during a loaded stretch right before and through the timed region
+    sampler = ClockSampler(dev.index)
+    sampler.start()
+    t_end = time.perf_counter() + args.clock_probe_s
+    i = 0
+    while time.perf_counter() < t_end:
+        step(i)
+        i += 1
+        if i % 64 == 0:
+            torch.cuda.synchronize(dev)
+    torch.cuda.synchronize(dev)
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(dist, dev)
+    torch.cuda.synchronize(dev)
+    # keep the GPU busy while the host queues the K steps, so no launch waits on the host
+    torch.cuda._sleep(int(min(2e9, 60000 * K + 2e6)))
+    start.record(stream)
+    for i in range(K):
+        ev[i][0].record(stream)
+        verify_fn(vrefs[i % n_sets], sp)
+        ev[i][1].record(stream)
+        commit_fn(crefs[i % n_sets], sp)
+        ev[i][2].record(stream)
+    end.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(dist, dev)
+    clocks = sampler.stop()
+
+    step_us = start.elapsed_time(end) * 1e3 / K
+    verify_us = statistics.mean(ev[i][0].elapsed_time(ev[i][1]) for i in range(K)) * 1e3
+    commit_us = statistics.mean(ev[i][1].elapsed_time(ev[i][2]) for i in range(K)) * 1e3
+    step_us_max = reduce_max(dist, step_us, dev)
+    verify_us_max = reduce_max(dist, verify_us, dev)
+
+    # e2e: host buffers through the C ABI, copies inside the timed region
+    e2e = None
+    if not args.no_e2e:
+        s0 = sets[0]
+        x_host = inp["x_base"].clone().pin_memory()
+        acc_host = inp["accept_len"].clone().pin_memory()
+        out_host = torch.empty_like(s0["out"], device="cpu").pin_memory()
+        h2d = x_host.numel() * x_host.element_size() + acc_host.numel() * 4
+        d2h = out_host.numel() * out_host.element_size()
+        for _ in range(3):
+            s0["x_base"].copy_(x_host, non_blocking=True)
+            s0["accept"].copy_(acc_host, non_blocking=True)
+            step(0)
+            out_host.copy_(s0["out"], non_blocking=True)
+        torch.cuda.synchronize(dev)
+        barrier(dist, dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(K):
+            s0["x_base"].copy_(x_host, non_blocking=True)
+            s0["accept"].copy_(acc_host, non_blocking=True)
+            step(0)
+            out_host.copy_(s0["out"], non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier(dist, dev)
+        e2e_us = reduce_max(dist, e0.elapsed_time(e1) * 1e3 / K, dev)
+        e2e = {"value": round(e2e_us, 3), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+    if rank != 0:
+        return 0
+
+    nbytes = wl.algorithmic_bytes(w)
+    peak, peak_kind = measured_peak()
+    achieved = nbytes["verify"] / (verify_us_max * 1e-6) / 1e9
+    traffic, traffic_src = profile_traffic()
+    line = {
+        "metric": METRIC, "value": round(step_us_max, 3), "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": round(step_us_max / 1e3, 6), "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+        "config": workload_config(w, l2_note),
+        "verify_us": round(verify_us_max, 3), "commit_us": round(commit_us, 3),
+        "verify_gbs": round(achieved, 1), "verify_frac_of_8tbs": round(achieved / HBM_NOMINAL_GBS, 4),
+        "verify_algorithmic_bytes": nbytes["verify"], "commit_algorithmic_bytes": nbytes["commit"],
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "kernel": "verify_kernel", "peak_source": f"{peak_kind} hbm_gbs (copy)",
+                     "traffic_source": traffic_src},
+        "gpu_launches": 2 * K,
+        "clocks": clocks,
+        "e2e": e2e,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        times = oracle_step_times(w, 200, args.cpu_budget_s)
+        line["cpu_baseline"] = {"value": round(statistics.median(times) * 1e6, 1), "unit": UNIT, "cores": 1,
+                                "kind": "oracle",
+                                "sample": f"whole workload ({w.n_seq} sequences) per step, median of {len(times)} "
+                                          f"steps; plain C loop, one thread"}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=wl.BENCH_WORKLOAD, choices=wl.WORKLOAD_ORDER)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--clock-probe-s", type=float, default=1.5)
+    ap.add_argument("--cpu-budget-s", type=float, default=10.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    w = wl.WORKLOADS[args.workload]
+    world, rank, local, dist = dist_setup()
+    try:
+        if args.impl == "reference":
+            return run_reference(args, w, world, rank)
+        return run_ours(args, w, world, rank, local, dist)
+    finally:
+        if dist is not None:
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,210 @@
+/*
+ * convverify.h -- C ABI of the batched speculative-verify causal depthwise conv1d update.
+ *
+ * One verify call runs, for n_seq sequences of T draft tokens each, the conv update of a hybrid
+ * GDN/KDA/Mamba2 layer over all T positions in one launch, and writes every per-token rollback
+ * snapshot of the conv window; one commit call later restores the state of the accepted prefix.
+ *
+ * Sources (the pages this library follows):
+ *   [atlas-batched]  Atlas spark_model API doc, fn gdn_verify_fused_conv_kn_batched: all K draft
+ *                    positions in one launch, every per-token snapshot written inline to a strided
+ *                    intermediates array, conv_state left holding the committed window, batched
+ *                    over n_seq with per-sequence strides, bit-identical to n separate calls.
+ *   [sglang-46184]   sglang pull request #46184 (dedup conv window tile store), sections
+ *                    "Motivation" and "Modifications": the deduplicated [dim, T+K-2] window row
+ *                    seen as an overlapping [T, dim, K-1] view whose step stride equals its
+ *                    column stride; step t's window is columns t..t+2 of
+ *                    [state[1], state[2], x_0 .. x_{T-1}]; padded rows exit before any store; a
+ *                    num_accept_tokens state offset.
+ *   [kda-mod]        Atlas spark_model/layers/glm5next_kda/mod.rs: conv1d + SiLU, then L2 of the
+ *                    q|k channels only (V never), eps inside the square root; decode_k snapshot
+ *                    t = state after row t, which a partial accept rewinds to.
+ *
+ * Conventions for every entry point:
+ *   - Strides are in ELEMENTS and must be >= 0.  The channel stride of x, out and weight is 1, and
+ *     the column stride of conv_state is 1.
+ *   - Every data pointer is a DEVICE pointer (or managed memory) unless stated otherwise.  The
+ *     caller owns every buffer: the library allocates, frees and synchronises nothing, launches
+ *     asynchronously on `stream`, and keeps no pointer after it returns.
+ *   - `stream` is a cudaStream_t passed as void*; NULL means the legacy default stream.
+ *   - Invalid arguments are reported by a negative status before anything is launched; nothing is
+ *     written then.  Problems that only the device can see (a cache slot or state offset out of
+ *     range, an accept count out of range) are reported per sequence through the optional `err`
+ *     array, and that sequence is left untouched.  No kernel traps or waits on anything.
+ */
+#ifndef CONVVERIFY_H
+#define CONVVERIFY_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define CV_API __attribute__((visibility("default")))
+#else
+#define CV_API
+#endif
+
+#define CV_ABI_VERSION 1
+#define CV_MAX_T 128 /* draft tokens per verify call */
+
+typedef enum cv_dtype {
+    CV_F32 = 0,  /* IEEE binary32 */
+    CV_BF16 = 1  /* bfloat16; arithmetic in fp32, outputs rounded to nearest even */
+} cv_dtype;
+
+typedef enum cv_window_layout {
+    /* window element (s, t, c, k) at s*win_seq_stride + t*win_step_stride + c*win_ch_stride
+       + k*win_col_stride: the [n_seq, T, dim, W-1] intermediates of [atlas-batched]. */
+    CV_WINDOW_DENSE = 1,
+    /* the deduplicated row of [sglang-46184]: element (s, t, c, k) at s*win_seq_stride
+       + (t+k)*win_col_stride + c*win_ch_stride, i.e. one [dim, T+W-2] row per sequence whose
+       column q holds input q+1 of [committed window, x_0 .. x_{T-1}].  win_step_stride must
+       equal win_col_stride. */
+    CV_WINDOW_DEDUP = 2
+} cv_window_layout;
+
+/* Status codes returned by the entry points. */
+enum {
+    CV_OK = 0,
+    CV_ERR_NULL_ARGS = -1,    /* args pointer is NULL */
+    CV_ERR_NULL_POINTER = -2, /* a required buffer pointer is NULL */
+    CV_ERR_SHAPE = -3,        /* n_seq outside 0..65535, dim < 1, n_slots < 1, state_cols < W-1 */
+    CV_ERR_TOKENS = -4,       /* T outside 1..CV_MAX_T */
+    CV_ERR_WIDTH = -5,        /* conv width outside 2..4 */
+    CV_ERR_DTYPE = -6,        /* dtype not a cv_dtype */
+    CV_ERR_HEAD_DIM = -7,     /* qk_channels > 0 and head_dim not a power of two in 8..256, or
+                                 qk_channels not a multiple of head_dim, or qk_channels > dim */
+    CV_ERR_LAYOUT = -8,       /* unknown layout, or DEDUP with win_step_stride != win_col_stride */
+    CV_ERR_STRIDE = -9,       /* a negative stride, or state rows that overlap (state_ch_stride <
+                                 state_cols with dim > 1) */
+    CV_ERR_ALIAS = -10,       /* out or window has the same base address as x, conv_state or weight,
+                                 or out and window share a base address */
+    CV_ERR_LAUNCH = -11,      /* the CUDA launch failed (cudaGetLastError after the launch) */
+    CV_ERR_SMEM = -12         /* the tile does not fit in shared memory for any block size */
+};
+
+/* Per-sequence bits written to err[s] (0 = fine or padded). */
+#define CV_SEQ_BAD_SLOT 1   /* cache slot >= n_slots */
+#define CV_SEQ_BAD_OFFSET 2 /* state offset < 0 or offset + W-1 > state_cols */
+#define CV_SEQ_BAD_ACCEPT 4 /* accept count outside 1..T (commit only) */
+
+/*
+ * cv_conv_verify -- [atlas-batched] fused multi-token verify, batched over sequences.
+ *
+ * For every sequence s with slot = cache_idx ? cache_idx[s] : s and slot >= 0, and every channel
+ * c, let o = state_off ? state_off[s] : 0 and
+ *     full = [conv_state[slot][c][o .. o+W-2], x[s][0][c], ..., x[s][T-1][c]]     (W-1+T values)
+ * Then for every token t:
+ *     acc   = bias[c] (or 0) + sum_{j=0}^{W-1} weight[c][j] * full[t+j]   fp32, taps in order, each
+ *                                                                         product rounded, no FMA
+ *     y     = acc / (1 + exp(-acc))                                      SiLU [kda-mod]
+ *     for c < qk_channels: y *= 1/sqrt(sum over c's head_dim group of y^2 + l2_eps)   [kda-mod]
+ *     out[s][t][c] = y rounded once to dtype
+ *     snapshot (s, t, c, k) = full[t+1+k], k < W-1      raw bit copy, dense or dedup layout
+ * and finally conv_state[slot][c][0 .. W-2] = full[T .. T+W-2] (the committed window, equal to
+ * snapshot T-1); state columns >= W-1 are not touched.  A sequence with slot < 0 is padding: its
+ * out rows, window rows and every state slot are left untouched ([sglang-46184]).
+ *
+ * Arguments (all in cv_verify_args):
+ *   n_seq, T, dim      sequences (0 = nothing to do), draft tokens 1..CV_MAX_T, channels >= 1
+ *   width              conv width W in 2..4 (the window is held in registers)
+ *   qk_channels        leading channels that are L2-normalised (0 = none); multiple of head_dim
+ *   head_dim           L2 group size when qk_channels > 0: power of two, 8..256
+ *   dtype              cv_dtype of x, out, conv_state, window, weight and bias
+ *   l2_eps             added to the group's sum of squares inside the square root
+ *   x                  [n_seq][T][dim] read-only; element (s,t,c) at s*x_seq_stride + t*x_tok_stride + c
+ *                      (x may be a strided slice of a wider projection output)
+ *   out                [n_seq][T][dim] write-only; (s,t,c) at s*out_seq_stride + t*out_tok_stride + c
+ *   conv_state         [n_slots][dim][state_cols] read-modify-write in place;
+ *                      (slot,c,k) at slot*state_slot_stride + c*state_ch_stride + k
+ *   cache_idx          int32 [n_seq] device array or NULL (slot = s); negative = padded sequence
+ *   state_off          int32 [n_seq] device array or NULL (0): column where the committed window is
+ *                      read, the num_accept_tokens offset of [sglang-46184]
+ *   weight             [dim][W] contiguous, read-only; weight[c][W-1] multiplies the newest input
+ *   bias               [dim] read-only, or NULL
+ *   window             snapshot buffer, write-only, laid out as window_layout says
+ *   err                int32 [n_seq] device array or NULL: receives the CV_SEQ_* bits of each
+ *                      sequence (0 for fine and for padded sequences)
+ * Preconditions the library cannot check: distinct sequences use distinct slots; out and window do
+ * not overlap themselves, each other, x, conv_state or weight.
+ * Returns CV_OK after the launch is queued, or a negative CV_ERR_* code with nothing launched.
+ */
+typedef struct cv_verify_args {
+    int32_t n_seq, T, dim, width, qk_channels, head_dim;
+    int32_t dtype; /* cv_dtype */
+    float l2_eps;
+    const void *x;
+    int64_t x_seq_stride, x_tok_stride;
+    void *out;
+    int64_t out_seq_stride, out_tok_stride;
+    void *conv_state;
+    int32_t n_slots, state_cols;
+    int64_t state_slot_stride, state_ch_stride;
+    const int32_t *cache_idx;
+    const int32_t *state_off;
+    const void *weight;
+    const void *bias;
+    void *window;
+    int32_t window_layout; /* cv_window_layout */
+    int32_t reserved0;
+    int64_t win_seq_stride, win_step_stride, win_ch_stride, win_col_stride;
+    int32_t *err;
+} cv_verify_args;
+
+CV_API int cv_conv_verify(const cv_verify_args *args, void *stream);
+
+/*
+ * cv_conv_commit -- restore the state of the accepted prefix ([sglang-46184] "Motivation": the
+ * window lets the conv state of the accepted prefix be restored after verify; [kda-mod] decode_k:
+ * snapshot t is the state after row t, which a partial accept rewinds to).
+ *
+ * For every sequence s with slot = cache_idx ? cache_idx[s] : s, slot >= 0, and a = accept_len[s]
+ * read on the device (no host round trip), 1 <= a <= T:
+ *     conv_state[slot][c][k] = snapshot (s, a-1, c, k)      for every c < dim, k < W-1
+ * a = T rewrites the state with the value it already holds.  A sequence whose a is out of range
+ * gets CV_SEQ_BAD_ACCEPT in err[s] and is untouched.  The window must be the one the matching
+ * cv_conv_verify wrote (same layout and strides).
+ */
+typedef struct cv_commit_args {
+    int32_t n_seq, T, dim, width;
+    int32_t dtype; /* cv_dtype */
+    int32_t n_slots;
+    void *conv_state;
+    int64_t state_slot_stride, state_ch_stride;
+    int32_t state_cols;
+    int32_t window_layout; /* cv_window_layout */
+    const int32_t *cache_idx;
+    const void *window;
+    int64_t win_seq_stride, win_step_stride, win_ch_stride, win_col_stride;
+    const int32_t *accept_len; /* int32 [n_seq] device array, required */
+    int32_t *err;              /* int32 [n_seq] device array or NULL */
+} cv_commit_args;
+
+CV_API int cv_conv_commit(const cv_commit_args *args, void *stream);
+
+/*
+ * cv_verify_plan -- validate `args` exactly as cv_conv_verify does and report the launch it would
+ * make, without touching the GPU.  grid = (grid_x, grid_y), block = threads, dynamic shared
+ * memory = smem_bytes; each block owns channels_per_block channels of one sequence.  Host pointer
+ * `plan` must not be NULL.  Returns the same status cv_conv_verify would return before launching.
+ */
+typedef struct cv_launch_plan {
+    int32_t grid_x, grid_y, threads, smem_bytes, channels_per_block, reserved0;
+} cv_launch_plan;
+
+CV_API int cv_verify_plan(const cv_verify_args *args, cv_launch_plan *plan);
+
+/* cv_status_string -- a static, NUL-terminated description of a status code (never NULL). */
+CV_API const char *cv_status_string(int status);
+
+/* cv_abi_version -- CV_ABI_VERSION of the built library. */
+CV_API int cv_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CONVVERIFY_H */

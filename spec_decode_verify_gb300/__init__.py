@@ -1,1 +1,225 @@
-"""Placeholder; the binding is added with the CUDA library."""
+"""Batched speculative-verify causal depthwise conv1d update on GB300 (sm_103a).
+
+Thin Python binding over the C ABI in ``include/convverify.h`` (library built in-tree by
+``spec_decode_verify_gb300.build``).  This module only marshals torch tensors into pointers and
+element strides; every step of the computation runs in the library's CUDA kernels.  There is no
+CPU path: CPU tensors are rejected and a missing library raises.
+
+    conv_verify(x, conv_state, weight, bias, out, window, layout=..., qk_channels=..., head_dim=...)
+    conv_commit(conv_state, window, accept_len, layout=..., T=..., width=...)
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+__all__ = ["conv_verify", "conv_commit", "verify_plan", "status_string", "load_library", "library_path",
+           "CvError", "DENSE", "DEDUP", "SEQ_BAD_SLOT", "SEQ_BAD_OFFSET", "SEQ_BAD_ACCEPT"]
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+library_path = os.path.join(_PKG, "_build", "libconvverify.so")
+
+DENSE, DEDUP = 1, 2
+F32, BF16 = 0, 1
+SEQ_BAD_SLOT, SEQ_BAD_OFFSET, SEQ_BAD_ACCEPT = 1, 2, 4
+MAX_T = 128
+
+c_i32, c_i64, c_vp = ctypes.c_int32, ctypes.c_int64, ctypes.c_void_p
+
+
+class VerifyArgs(ctypes.Structure):
+    """Mirror of cv_verify_args."""
+    _fields_ = [
+        ("n_seq", c_i32), ("T", c_i32), ("dim", c_i32), ("width", c_i32), ("qk_channels", c_i32),
+        ("head_dim", c_i32), ("dtype", c_i32), ("l2_eps", ctypes.c_float),
+        ("x", c_vp), ("x_seq_stride", c_i64), ("x_tok_stride", c_i64),
+        ("out", c_vp), ("out_seq_stride", c_i64), ("out_tok_stride", c_i64),
+        ("conv_state", c_vp), ("n_slots", c_i32), ("state_cols", c_i32),
+        ("state_slot_stride", c_i64), ("state_ch_stride", c_i64),
+        ("cache_idx", c_vp), ("state_off", c_vp), ("weight", c_vp), ("bias", c_vp),
+        ("window", c_vp), ("window_layout", c_i32), ("reserved0", c_i32),
+        ("win_seq_stride", c_i64), ("win_step_stride", c_i64), ("win_ch_stride", c_i64), ("win_col_stride", c_i64),
+        ("err", c_vp),
+    ]
+
+
+class CommitArgs(ctypes.Structure):
+    """Mirror of cv_commit_args."""
+    _fields_ = [
+        ("n_seq", c_i32), ("T", c_i32), ("dim", c_i32), ("width", c_i32), ("dtype", c_i32), ("n_slots", c_i32),
+        ("conv_state", c_vp), ("state_slot_stride", c_i64), ("state_ch_stride", c_i64),
+        ("state_cols", c_i32), ("window_layout", c_i32), ("cache_idx", c_vp), ("window", c_vp),
+        ("win_seq_stride", c_i64), ("win_step_stride", c_i64), ("win_ch_stride", c_i64), ("win_col_stride", c_i64),
+        ("accept_len", c_vp), ("err", c_vp),
+    ]
+
+
+class LaunchPlan(ctypes.Structure):
+    """Mirror of cv_launch_plan."""
+    _fields_ = [("grid_x", c_i32), ("grid_y", c_i32), ("threads", c_i32), ("smem_bytes", c_i32),
+                ("channels_per_block", c_i32), ("reserved0", c_i32)]
+
+
+class CvError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__(f"{what}: {status_string(status)} (status {status})")
+        self.status = status
+
+
+_lib = None
+
+
+def load_library(path: Optional[str] = None):
+    """Load the CUDA library (raises if it has not been built: there is no fallback)."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or library_path
+    if not os.path.exists(p):
+        raise RuntimeError(f"CUDA library not built: {p} is missing (python -m spec_decode_verify_gb300.build)")
+    lib = ctypes.CDLL(p)
+    lib.cv_conv_verify.argtypes = [ctypes.POINTER(VerifyArgs), c_vp]
+    lib.cv_conv_verify.restype = c_i32
+    lib.cv_conv_commit.argtypes = [ctypes.POINTER(CommitArgs), c_vp]
+    lib.cv_conv_commit.restype = c_i32
+    lib.cv_verify_plan.argtypes = [ctypes.POINTER(VerifyArgs), ctypes.POINTER(LaunchPlan)]
+    lib.cv_verify_plan.restype = c_i32
+    lib.cv_status_string.argtypes = [c_i32]
+    lib.cv_status_string.restype = ctypes.c_char_p
+    lib.cv_abi_version.argtypes = []
+    lib.cv_abi_version.restype = c_i32
+    if path is None:
+        _lib = lib
+    return lib
+
+
+def status_string(status: int) -> str:
+    return load_library().cv_status_string(int(status)).decode()
+
+
+def _dtype_code(t) -> int:
+    import torch
+    if t.dtype == torch.bfloat16:
+        return BF16
+    if t.dtype == torch.float32:
+        return F32
+    raise TypeError(f"unsupported dtype {t.dtype}: expected bfloat16 or float32")
+
+
+def _dev_ptr(t, name, required=True):
+    if t is None:
+        if required:
+            raise ValueError(f"{name} is required")
+        return None
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor (there is no CPU path)")
+    return t.data_ptr()
+
+
+def _layout_code(layout) -> int:
+    if layout in (DENSE, "dense"):
+        return DENSE
+    if layout in (DEDUP, "dedup"):
+        return DEDUP
+    raise ValueError(f"unknown window layout {layout!r}")
+
+
+def _window_strides(window, layout: int):
+    s = window.stride()
+    if layout == DENSE:  # [n_seq, T, dim, W-1]
+        return s[0], s[1], s[2], s[3]
+    return s[0], s[2], s[1], s[2]  # dedup row [n_seq, dim, T+W-2]: step stride = column stride
+
+
+def _stream_ptr(stream) -> Optional[int]:
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def make_verify_args(x, conv_state, weight, bias, out, window, *, layout, qk_channels, head_dim,
+                     l2_eps=1e-6, cache_idx=None, state_off=None, err=None, check_device=True) -> VerifyArgs:
+    """Build cv_verify_args from tensors.
+
+    x [n_seq, T, dim] (channel stride 1, any seq/token strides), conv_state [n_slots, dim, S]
+    (column stride 1), weight [dim, W] contiguous, bias [dim] or None, out [n_seq, T, dim] (channel
+    stride 1), window dense [n_seq, T, dim, W-1] or dedup [n_seq, dim, T+W-2] (any strides),
+    cache_idx / state_off / err int32 [n_seq] or None."""
+    lay = _layout_code(layout)
+    ptr = _dev_ptr if check_device else (lambda t, n, required=True: None if t is None else t.data_ptr())
+    n_seq, T, dim = x.shape
+    W = weight.shape[1]
+    if x.stride(2) != 1 or out.stride(2) != 1 or conv_state.stride(2) != 1:
+        raise ValueError("x, out and conv_state need a unit innermost stride")
+    if not weight.is_contiguous() or (bias is not None and not bias.is_contiguous()):
+        raise ValueError("weight and bias must be contiguous")
+    ws = _window_strides(window, lay)
+    return VerifyArgs(
+        n_seq=n_seq, T=T, dim=dim, width=W, qk_channels=qk_channels, head_dim=head_dim, dtype=_dtype_code(x),
+        l2_eps=l2_eps, x=ptr(x, "x"), x_seq_stride=x.stride(0), x_tok_stride=x.stride(1),
+        out=ptr(out, "out"), out_seq_stride=out.stride(0), out_tok_stride=out.stride(1),
+        conv_state=ptr(conv_state, "conv_state"), n_slots=conv_state.shape[0], state_cols=conv_state.shape[2],
+        state_slot_stride=conv_state.stride(0), state_ch_stride=conv_state.stride(1),
+        cache_idx=ptr(cache_idx, "cache_idx", False), state_off=ptr(state_off, "state_off", False),
+        weight=ptr(weight, "weight"), bias=ptr(bias, "bias", False), window=ptr(window, "window"),
+        window_layout=lay, reserved0=0, win_seq_stride=ws[0], win_step_stride=ws[1], win_ch_stride=ws[2],
+        win_col_stride=ws[3], err=ptr(err, "err", False))
+
+
+def conv_verify(x, conv_state, weight, bias, out, window, *, layout, qk_channels, head_dim, l2_eps=1e-6,
+                cache_idx=None, state_off=None, err=None, stream=None) -> None:
+    """Queue one batched verify on ``stream`` (default: torch's current stream).
+
+    Writes out, window, conv_state (and err); raises CvError on an invalid argument."""
+    for t in (x, conv_state, weight, out, window):
+        if t.dtype != x.dtype:
+            raise TypeError("x, conv_state, weight, out and window must share one dtype")
+    if bias is not None and bias.dtype != x.dtype:
+        raise TypeError("bias must have the dtype of x")
+    a = make_verify_args(x, conv_state, weight, bias, out, window, layout=layout, qk_channels=qk_channels,
+                         head_dim=head_dim, l2_eps=l2_eps, cache_idx=cache_idx, state_off=state_off, err=err)
+    rc = load_library().cv_conv_verify(ctypes.byref(a), _stream_ptr(stream))
+    if rc != 0:
+        raise CvError(rc, "cv_conv_verify")
+
+
+def verify_plan(x, conv_state, weight, bias, out, window, *, layout, qk_channels, head_dim, l2_eps=1e-6,
+                cache_idx=None, state_off=None, err=None) -> LaunchPlan:
+    """The launch cv_conv_verify would make (validates without touching the GPU)."""
+    a = make_verify_args(x, conv_state, weight, bias, out, window, layout=layout, qk_channels=qk_channels,
+                         head_dim=head_dim, l2_eps=l2_eps, cache_idx=cache_idx, state_off=state_off, err=err,
+                         check_device=False)
+    pl = LaunchPlan()
+    rc = load_library().cv_verify_plan(ctypes.byref(a), ctypes.byref(pl))
+    if rc != 0:
+        raise CvError(rc, "cv_verify_plan")
+    return pl
+
+
+def make_commit_args(conv_state, window, accept_len, *, layout, T, width, cache_idx=None, err=None,
+                     check_device=True) -> CommitArgs:
+    lay = _layout_code(layout)
+    ptr = _dev_ptr if check_device else (lambda t, n, required=True: None if t is None else t.data_ptr())
+    ws = _window_strides(window, lay)
+    if conv_state.stride(2) != 1:
+        raise ValueError("conv_state needs a unit column stride")
+    return CommitArgs(
+        n_seq=accept_len.shape[0], T=T, dim=conv_state.shape[1], width=width, dtype=_dtype_code(conv_state),
+        n_slots=conv_state.shape[0], conv_state=ptr(conv_state, "conv_state"),
+        state_slot_stride=conv_state.stride(0), state_ch_stride=conv_state.stride(1),
+        state_cols=conv_state.shape[2], window_layout=lay, cache_idx=ptr(cache_idx, "cache_idx", False),
+        window=ptr(window, "window"), win_seq_stride=ws[0], win_step_stride=ws[1], win_ch_stride=ws[2],
+        win_col_stride=ws[3], accept_len=ptr(accept_len, "accept_len"), err=ptr(err, "err", False))
+
+
+def conv_commit(conv_state, window, accept_len, *, layout, T, width, cache_idx=None, err=None, stream=None) -> None:
+    """Queue the commit: conv_state[slot] <- snapshot accept_len[s]-1 of sequence s."""
+    if window.dtype != conv_state.dtype:
+        raise TypeError("window and conv_state must share one dtype")
+    a = make_commit_args(conv_state, window, accept_len, layout=layout, T=T, width=width, cache_idx=cache_idx,
+                         err=err)
+    rc = load_library().cv_conv_commit(ctypes.byref(a), _stream_ptr(stream))
+    if rc != 0:
+        raise CvError(rc, "cv_conv_commit")

@@ -1,0 +1,413 @@
+// Device code of the batched speculative-verify conv1d update (sm_103a).
+//
+// Verify: one CTA per (channel block, sequence), the launch shape of the Atlas batched verify
+// (fn gdn_verify_fused_conv_kn_batched: grid (ceil(dim/block), n_seq)).  Each thread owns 8
+// consecutive channels, so every global access of x, out, state and weights is a 16-byte vector
+// and a warp touches 512 contiguous bytes per instruction.  The block's inputs are staged once in
+// shared memory as a token-major tile
+//     tile[j][c] = full_c[j],  j in [0, W-1+T)   (rows 0..W-2: committed window, then x_0..x_{T-1})
+// and every snapshot layout is written from that tile in destination order: the deduplicated row
+// of the sglang tile store (PR #46184, "Modifications") becomes one contiguous, coalesced run of
+// channels*(T+W-2) elements per block instead of W-1 scattered stores per token, the dense
+// intermediates become one run per token, and the committed window one run for the state.  All
+// snapshot and state traffic moves raw bits, so NaN payloads and signed zeros survive.
+//
+// Arithmetic per channel and token, in fp32: acc = bias + sum_j w[j]*full[t+j] with each product
+// rounded before its add (explicit _rn intrinsics keep the compiler from fusing them), SiLU, then
+// for q|k channels an L2 normalisation over the head_dim group as a warp-shuffle reduction over
+// head_dim/8 lanes (glm5next_kda mod.rs: "conv1d + SiLU -> L2(q,k only)", eps inside the root).
+//
+// Commit: one thread per 16 bytes of the destination state rows; the accept count is read on the
+// device (memra Engine::ssm_conv_ring_rebuild_dc keeps the accept count on the device too).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace cvk {
+
+struct VerifyParams {
+    const void *x;
+    long long x_seq, x_tok;
+    void *out;
+    long long out_seq, out_tok;
+    void *state;
+    long long st_slot, st_ch;
+    const int *cache_idx;
+    const int *state_off;
+    const void *weight;
+    const void *bias;
+    void *win;
+    long long w_seq, w_step, w_ch, w_col;  // w_step already equals w_col for the dedup layout
+    int *err;
+    int n_seq, T, dim, n_slots, state_cols;
+    int qk_channels, head_dim, pitch;      // pitch: elements per shared-memory tile row
+    float eps;
+    int dedup;
+    int x_vec, out_vec, st_vec, w_vec, b_vec;  // 16-byte vector paths allowed (host-checked)
+};
+
+struct CommitParams {
+    void *state;
+    long long st_slot, st_ch;
+    const int *cache_idx;
+    const void *win;
+    long long w_seq, w_step, w_ch, w_col;
+    const int *accept_len;
+    int *err;
+    int n_seq, T, dim, n_slots;
+    int st_vec;
+};
+
+// ---------------------------------------------------------------- element helpers
+// B is the raw bit type of one element: uint16_t for bf16, uint32_t for fp32.
+
+template <typename B> __device__ __forceinline__ float widen(B b);
+template <> __device__ __forceinline__ float widen<uint16_t>(uint16_t b) { return __uint_as_float((uint32_t)b << 16); }
+template <> __device__ __forceinline__ float widen<uint32_t>(uint32_t b) { return __uint_as_float(b); }
+
+template <typename B> __device__ __forceinline__ B narrow(float f);
+template <> __device__ __forceinline__ uint16_t narrow<uint16_t>(float f) {
+    return __bfloat16_as_ushort(__float2bfloat16_rn(f));
+}
+template <> __device__ __forceinline__ uint32_t narrow<uint32_t>(float f) { return __float_as_uint(f); }
+
+// Eight consecutive elements as 16-byte words: one uint4 for bf16, two for fp32.
+template <typename B> struct Oct {
+    static constexpr int NV = (int)sizeof(B) / 2;  // uint4 vectors per 8 elements
+    uint4 v[NV];
+    __device__ __forceinline__ B get(int e) const {
+        const uint32_t *w = reinterpret_cast<const uint32_t *>(v);
+        if (sizeof(B) == 2) return (B)((w[e >> 1] >> ((e & 1) * 16)) & 0xffffu);
+        return (B)w[e];
+    }
+    __device__ __forceinline__ void set(int e, B b) {
+        uint32_t *w = reinterpret_cast<uint32_t *>(v);
+        if (sizeof(B) == 2) {
+            const int sh = (e & 1) * 16;
+            w[e >> 1] = (w[e >> 1] & ~(0xffffu << sh)) | ((uint32_t)b << sh);
+        } else {
+            w[e] = (uint32_t)b;
+        }
+    }
+};
+
+template <typename B> __device__ __forceinline__ void load_oct(Oct<B> &o, const B *p) {
+#pragma unroll
+    for (int i = 0; i < Oct<B>::NV; ++i) o.v[i] = *reinterpret_cast<const uint4 *>(p + i * (16 / sizeof(B)));
+}
+template <typename B> __device__ __forceinline__ void load_oct_nc(Oct<B> &o, const B *p) {
+#pragma unroll
+    for (int i = 0; i < Oct<B>::NV; ++i) o.v[i] = __ldg(reinterpret_cast<const uint4 *>(p + i * (16 / sizeof(B))));
+}
+template <typename B> __device__ __forceinline__ void store_oct(B *p, const Oct<B> &o) {
+#pragma unroll
+    for (int i = 0; i < Oct<B>::NV; ++i) *reinterpret_cast<uint4 *>(p + i * (16 / sizeof(B))) = o.v[i];
+}
+
+__device__ __forceinline__ void cp_async16(void *smem, const void *gmem) {
+    const unsigned s = (unsigned)__cvta_generic_to_shared(smem);
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(s), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit_wait_all() {
+    asm volatile("cp.async.commit_group;\n" ::: "memory");
+    asm volatile("cp.async.wait_group 0;\n" ::: "memory");
+}
+
+__device__ __forceinline__ float silu(float a) { return a / (1.0f + expf(-a)); }
+
+// Write one view of the tile: element (c, q) for c < nch, q < ncol is tile[(jofs+q)*pitch + c] and
+// goes to dst[c*ch_stride + q*col_stride].  Three shapes: channel-major contiguous (the dedup row
+// and the dense per-token chunks: one coalesced run of nch*ncol elements), channel-stride-1 (a
+// transposed row: one contiguous run of channels per column), and anything else element by element.
+template <typename B>
+__device__ __forceinline__ void write_view(const B *__restrict__ tile, int pitch, int jofs, int ncol, B *dst,
+                                           long long ch_stride, long long col_stride, int nch) {
+    constexpr int CH = 16 / (int)sizeof(B);
+    const int tid = threadIdx.x, NT = blockDim.x;
+    const int n = nch * ncol;
+    const bool aligned = ((reinterpret_cast<uintptr_t>(dst) & 15u) == 0);
+    if (ch_stride == ncol && col_stride == 1 && aligned) {
+        const int nchunks = (n + CH - 1) / CH;
+        for (int m = tid; m < nchunks; m += NT) {
+            const int pos = m * CH;
+            int c = pos / ncol;
+            int q = pos - c * ncol;
+            uint32_t wv[4];
+            B *vb = reinterpret_cast<B *>(wv);
+#pragma unroll
+            for (int e = 0; e < CH; ++e) {
+                vb[e] = (pos + e < n) ? tile[(jofs + q) * pitch + c] : (B)0;
+                if (++q == ncol) {
+                    q = 0;
+                    ++c;
+                }
+            }
+            if (pos + CH <= n) {
+                *reinterpret_cast<uint4 *>(dst + pos) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+            } else {
+                for (int e = 0; pos + e < n; ++e) dst[pos + e] = vb[e];
+            }
+        }
+    } else if (ch_stride == 1 && aligned && ((col_stride * (long long)sizeof(B)) & 15) == 0) {
+        const int nv = nch / CH;
+        for (int i = tid; i < ncol * nv; i += NT) {
+            const int q = i / nv, m = i - q * nv;
+            *reinterpret_cast<uint4 *>(dst + q * col_stride + m * CH) =
+                *reinterpret_cast<const uint4 *>(tile + (jofs + q) * pitch + m * CH);
+        }
+        const int rem = nch - nv * CH;
+        for (int i = tid; i < ncol * rem; i += NT) {
+            const int q = i / rem, c = nv * CH + (i - q * rem);
+            dst[q * col_stride + c] = tile[(jofs + q) * pitch + c];
+        }
+    } else {
+        for (int i = tid; i < n; i += NT) {
+            const int q = i / nch, c = i - q * nch;
+            dst[c * ch_stride + q * col_stride] = tile[(jofs + q) * pitch + c];
+        }
+    }
+}
+
+// ---------------------------------------------------------------- verify
+template <typename B, int W>
+__global__ void __launch_bounds__(256) verify_kernel(const __grid_constant__ VerifyParams p) {
+    constexpr int R = W - 1;  // committed window columns
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    B *tile = reinterpret_cast<B *>(smem_raw);
+
+    const int s = blockIdx.y;
+    const int tid = threadIdx.x;
+    const int BC = 8 * blockDim.x;
+    const int c0 = blockIdx.x * BC;
+    const int T = p.T, pitch = p.pitch;
+
+    const int slot = p.cache_idx ? p.cache_idx[s] : s;
+    const int off = p.state_off ? p.state_off[s] : 0;
+    int status = 0;
+    if (slot >= 0) {
+        if (slot >= p.n_slots) status |= 1;
+        if (off < 0 || off > p.state_cols - R) status |= 2;
+    }
+    if (p.err && blockIdx.x == 0 && tid == 0) p.err[s] = status;
+    if (slot < 0 || status) return;  // padded or rejected: touch nothing (uniform per block)
+
+    const int nch = min(BC, p.dim - c0);
+    const int cl = tid * 8;  // first block-local channel of this thread
+    const int my = max(0, min(8, nch - cl));
+    const bool full8 = (my == 8);
+
+    // (1) x_0..x_{T-1} -> tile rows R..R+T-1 (asynchronous 16-byte copies, no registers)
+    const B *xs = reinterpret_cast<const B *>(p.x) + (long long)s * p.x_seq + c0;
+    if (p.x_vec) {
+        if (full8) {
+            for (int t = 0; t < T; ++t) {
+#pragma unroll
+                for (int i = 0; i < Oct<B>::NV; ++i)
+                    cp_async16(tile + (R + t) * pitch + cl + i * (16 / sizeof(B)), xs + t * p.x_tok + cl + i * (16 / sizeof(B)));
+            }
+        } else {
+            for (int t = 0; t < T; ++t)
+                for (int e = 0; e < my; ++e) tile[(R + t) * pitch + cl + e] = xs[t * p.x_tok + cl + e];
+        }
+    } else {
+        for (int i = tid; i < T * nch; i += blockDim.x) {
+            const int t = i / nch, c = i - t * nch;
+            tile[(R + t) * pitch + c] = xs[t * p.x_tok + c];
+        }
+    }
+
+    // (2) committed window of this thread's channels -> registers and tile rows 0..R-1
+    float win[R][8];
+    {
+        B raw[R][8];
+        B *sp = reinterpret_cast<B *>(p.state) + (long long)slot * p.st_slot + (long long)(c0 + cl) * p.st_ch + off;
+        if (full8 && p.st_vec && off == 0) {
+            // 8 channels x R columns are contiguous: R 16-byte vectors (2R for fp32)
+            Oct<B> o[R];
+#pragma unroll
+            for (int k = 0; k < R; ++k) load_oct(o[k], sp + k * 8);
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+#pragma unroll
+                for (int k = 0; k < R; ++k) {
+                    const int lin = e * R + k;
+                    raw[k][e] = o[lin / 8].get(lin % 8);
+                }
+        } else {
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+#pragma unroll
+                for (int k = 0; k < R; ++k) raw[k][e] = (e < my) ? sp[e * p.st_ch + k] : (B)0;
+        }
+#pragma unroll
+        for (int k = 0; k < R; ++k) {
+            if (full8) {
+                Oct<B> o;
+#pragma unroll
+                for (int e = 0; e < 8; ++e) o.set(e, raw[k][e]);
+                store_oct(tile + k * pitch + cl, o);
+            } else {
+                for (int e = 0; e < my; ++e) tile[k * pitch + cl + e] = raw[k][e];
+            }
+#pragma unroll
+            for (int e = 0; e < 8; ++e) win[k][e] = widen<B>(raw[k][e]);
+        }
+    }
+
+    // (3) taps and bias of this thread's channels
+    float wt[8][W];
+    float bs[8];
+    {
+        const B *wp = reinterpret_cast<const B *>(p.weight) + (long long)(c0 + cl) * W;
+        if (full8 && p.w_vec) {
+            Oct<B> o[W];
+#pragma unroll
+            for (int i = 0; i < W; ++i) load_oct_nc(o[i], wp + i * 8);
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+#pragma unroll
+                for (int j = 0; j < W; ++j) {
+                    const int lin = e * W + j;
+                    wt[e][j] = widen<B>(o[lin / 8].get(lin % 8));
+                }
+        } else {
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+#pragma unroll
+                for (int j = 0; j < W; ++j) wt[e][j] = (e < my) ? widen<B>(wp[e * W + j]) : 0.0f;
+        }
+        const B *bp = reinterpret_cast<const B *>(p.bias);
+        if (bp && full8 && p.b_vec) {
+            Oct<B> o;
+            load_oct_nc(o, bp + c0 + cl);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) bs[e] = widen<B>(o.get(e));
+        } else {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) bs[e] = (bp && e < my) ? widen<B>(bp[c0 + cl + e]) : 0.0f;
+        }
+    }
+
+    if (p.x_vec) cp_async_commit_wait_all();
+    __syncthreads();
+
+    // (4) snapshots and committed window, written from the tile in destination order
+    {
+        B *wb = reinterpret_cast<B *>(p.win) + (long long)s * p.w_seq;
+        if (p.dedup) {
+            write_view<B>(tile, pitch, 1, T + R - 1, wb + (long long)c0 * p.w_ch, p.w_ch, p.w_col, nch);
+        } else {
+            for (int t = 0; t < T; ++t)
+                write_view<B>(tile, pitch, t + 1, R, wb + t * p.w_step + (long long)c0 * p.w_ch, p.w_ch, p.w_col, nch);
+        }
+        B *sb = reinterpret_cast<B *>(p.state) + (long long)slot * p.st_slot + (long long)c0 * p.st_ch;
+        write_view<B>(tile, pitch, T, R, sb, p.st_ch, 1, nch);
+    }
+
+    // (5) conv + SiLU (+ L2 over the head_dim group) for every token, outputs stored as vectors
+    const bool has_bias = (p.bias != nullptr);
+    const bool l2_block = (c0 < p.qk_channels);       // block-uniform
+    const bool l2_mine = (c0 + cl) < p.qk_channels;   // whole 8-channel group is q|k or V
+    const int lanes = p.head_dim >> 3;                // 1..32 threads per group
+    B *ob = reinterpret_cast<B *>(p.out) + (long long)s * p.out_seq + c0 + cl;
+    for (int t = 0; t < T; ++t) {
+        float xv[8];
+        if (full8) {
+            Oct<B> o;
+            load_oct(o, tile + (R + t) * pitch + cl);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) xv[e] = widen<B>(o.get(e));
+        } else {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) xv[e] = (e < my) ? widen<B>(tile[(R + t) * pitch + cl + e]) : 0.0f;
+        }
+        float y[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            float acc = has_bias ? bs[e] : 0.0f;
+#pragma unroll
+            for (int j = 0; j < R; ++j) acc = __fadd_rn(acc, __fmul_rn(wt[e][j], win[j][e]));
+            acc = __fadd_rn(acc, __fmul_rn(wt[e][R], xv[e]));
+            y[e] = silu(acc);
+        }
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+#pragma unroll
+            for (int j = 0; j + 1 < R; ++j) win[j][e] = win[j + 1][e];
+            win[R - 1][e] = xv[e];
+        }
+        if (l2_block) {
+            float ss = 0.0f;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) ss += y[e] * y[e];
+            for (int o = lanes >> 1; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+            if (l2_mine) {
+                const float r = rsqrtf(ss + p.eps);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) y[e] *= r;
+            }
+        }
+        B *op = ob + t * p.out_tok;
+        if (full8 && p.out_vec) {
+            Oct<B> o;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) o.set(e, narrow<B>(y[e]));
+            store_oct(op, o);
+        } else {
+            for (int e = 0; e < my; ++e) op[e] = narrow<B>(y[e]);
+        }
+    }
+}
+
+// ---------------------------------------------------------------- commit
+template <typename B, int W>
+__global__ void __launch_bounds__(256) commit_kernel(const __grid_constant__ CommitParams p) {
+    constexpr int R = W - 1;
+    constexpr int CH = 16 / (int)sizeof(B);
+    const int s = blockIdx.y;
+    const int slot = p.cache_idx ? p.cache_idx[s] : s;
+    const int a = p.accept_len[s];
+    int status = 0;
+    if (slot >= 0) {
+        if (slot >= p.n_slots) status |= 1;
+        if (a < 1 || a > p.T) status |= 4;
+    }
+    if (p.err && blockIdx.x == 0 && threadIdx.x == 0) p.err[s] = status;
+    if (slot < 0 || status) return;
+
+    const B *src = reinterpret_cast<const B *>(p.win) + (long long)s * p.w_seq + (long long)(a - 1) * p.w_step;
+    B *dst = reinterpret_cast<B *>(p.state) + (long long)slot * p.st_slot;
+    const long long n = (long long)p.dim * R;
+    const long long gtid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    const long long gstride = (long long)gridDim.x * blockDim.x;
+    if (p.st_vec) {
+        // destination rows are packed ([dim][R] contiguous): one 16-byte store per thread step
+        for (long long m = gtid; m * CH < n; m += gstride) {
+            const long long pos = m * CH;
+            uint32_t wv[4];
+            B *vb = reinterpret_cast<B *>(wv);
+#pragma unroll
+            for (int e = 0; e < CH; ++e) {
+                const long long q = pos + e;
+                const long long c = q / R;
+                const int k = (int)(q - c * R);
+                vb[e] = (q < n) ? src[c * p.w_ch + k * p.w_col] : (B)0;
+            }
+            if (pos + CH <= n) {
+                *reinterpret_cast<uint4 *>(dst + pos) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+            } else {
+                for (int e = 0; pos + e < n; ++e) dst[pos + e] = vb[e];
+            }
+        }
+    } else {
+        for (long long i = gtid; i < n; i += gstride) {
+            const long long c = i / R;
+            const int k = (int)(i - c * R);
+            dst[c * p.st_ch + k] = src[c * p.w_ch + k * p.w_col];
+        }
+    }
+}
+
+}  // namespace cvk

@@ -1,0 +1,154 @@
+"""Host-side checks of the C ABI (no GPU): the library loads, exports every function the header
+declares, and rejects invalid arguments with the documented status before launching anything."""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+import spec_decode_verify_gb300 as cv
+from spec_decode_verify_gb300 import build as cvbuild
+from spec_decode_verify_gb300 import workloads as wl
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "convverify.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    cvbuild.build()
+    return cv.load_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^CV_API\s[\w\s\*]*?\b(cv_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_exports_every_declared_function(lib):
+    names = declared_functions()
+    assert {"cv_conv_verify", "cv_conv_commit", "cv_verify_plan", "cv_status_string", "cv_abi_version"} <= set(names)
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in the header but not exported"
+    assert lib.cv_abi_version() == 1
+
+
+def test_exports_nothing_undeclared(lib):
+    """Only the declared C entry points are visible (the kernels and helpers are hidden)."""
+    import subprocess
+    r = subprocess.run(["nm", "-D", "--defined-only", cv.library_path], capture_output=True, text=True)
+    if r.returncode != 0:
+        pytest.skip("nm not available")
+    exported = {ln.split()[-1] for ln in r.stdout.splitlines() if " T " in ln}
+    ours = {n for n in exported if n.startswith("cv_")}
+    assert ours == set(declared_functions())
+
+
+def _args(w: wl.VerifyWorkload, **over):
+    inp = wl.make_inputs(w)
+    a = cv.make_verify_args(inp["x"], inp["conv_state"], inp["weight"], inp["bias"], inp["out"], inp["window"],
+                            layout=w.layout, qk_channels=w.qk_channels, head_dim=w.head_dim,
+                            cache_idx=inp["cache_idx"], check_device=False)
+    for k, v in over.items():
+        setattr(a, k, v)
+    return a
+
+
+def _plan(lib, a):
+    pl = cv.LaunchPlan()
+    return lib.cv_verify_plan(ctypes.byref(a), ctypes.byref(pl)), pl
+
+
+W3 = wl.WORKLOADS["n128_t8_dim10240_w4_bf16_dedup_pad13"]
+
+
+def test_plan_for_benchmark_workload(lib):
+    rc, pl = _plan(lib, _args(W3))
+    assert rc == 0
+    assert (pl.grid_x, pl.grid_y, pl.threads, pl.channels_per_block) == (10, 128, 128, 1024)
+    assert pl.smem_bytes == (8 + 3) * (1024 + 8) * 2
+    assert pl.channels_per_block % W3.head_dim == 0
+
+
+@pytest.mark.parametrize("field,value,status", [
+    ("dtype", 7, -6), ("width", 1, -5), ("width", 5, -5), ("T", 0, -4), ("T", 129, -4), ("n_seq", -1, -3),
+    ("n_seq", 65536, -3), ("dim", 0, -3), ("n_slots", 0, -3), ("state_cols", 2, -3), ("window_layout", 3, -8),
+    ("win_step_stride", 5, -8), ("qk_channels", 10240 + 128, -7), ("head_dim", 96, -7), ("head_dim", 4, -7),
+    ("head_dim", 512, -7), ("qk_channels", 4000, -7), ("x_tok_stride", -1, -9), ("state_ch_stride", 2, -9),
+    ("x", None, -2), ("weight", None, -2), ("window", None, -2),
+])
+def test_invalid_arguments_rejected(lib, field, value, status):
+    a = _args(W3, **{field: value})
+    assert _plan(lib, a)[0] == status
+    # the launching entry point returns the same code without touching the GPU
+    assert lib.cv_conv_verify(ctypes.byref(a), None) == status
+    assert cv.status_string(status) not in ("", "unknown status")
+
+
+def test_aliasing_rejected(lib):
+    a = _args(W3)
+    a.out = a.x
+    assert _plan(lib, a)[0] == -10
+    a = _args(W3)
+    a.window = a.conv_state
+    assert _plan(lib, a)[0] == -10
+    a = _args(W3)
+    a.window = a.out
+    assert _plan(lib, a)[0] == -10
+
+
+def test_null_args_and_plan(lib):
+    assert lib.cv_conv_verify(None, None) == -1
+    assert lib.cv_conv_commit(None, None) == -1
+    a = _args(W3)
+    assert lib.cv_verify_plan(ctypes.byref(a), None) == -2
+
+
+def test_zero_sequences_is_ok_without_gpu(lib):
+    a = _args(W3, n_seq=0, x=None, out=None)
+    assert lib.cv_conv_verify(ctypes.byref(a), None) == 0
+
+
+@pytest.mark.parametrize("T,dtype,threads", [(8, "bf16", 128), (17, "bf16", 128), (32, "bf16", 128),
+                                             (64, "f32", 32), (128, "f32", 32), (128, "bf16", 32)])
+def test_plan_fits_shared_memory(lib, T, dtype, threads):
+    """The tile (T+W-1 rows of 8*threads channels plus 16 bytes) shrinks the block until it fits."""
+    w = W3.replace(T=T, dtype=dtype, n_seq=2, n_pad=0, extra_slots=0)
+    rc, pl = _plan(lib, _args(w))
+    esize = 2 if dtype == "bf16" else 4
+    assert rc == 0 and pl.threads == threads
+    assert pl.smem_bytes == (T + 3) * (8 * threads * esize + 16)
+    assert pl.smem_bytes <= 96 * 1024 or threads == 32
+    assert pl.smem_bytes <= 227 * 1024
+
+
+def test_commit_validation(lib):
+    w = W3.replace(n_seq=2, n_pad=0, extra_slots=0)
+    inp = wl.make_inputs(w)
+    a = cv.make_commit_args(inp["conv_state"], inp["window"], inp["accept_len"], layout="dedup", T=w.T,
+                            width=w.width, check_device=False)
+    a.accept_len = None
+    assert lib.cv_conv_commit(ctypes.byref(a), None) == -2
+    a = cv.make_commit_args(inp["conv_state"], inp["window"], inp["accept_len"], layout="dedup", T=w.T,
+                            width=w.width, check_device=False)
+    a.width = 6
+    assert lib.cv_conv_commit(ctypes.byref(a), None) == -5
+    a.width = 4
+    a.win_step_stride = 99
+    assert lib.cv_conv_commit(ctypes.byref(a), None) == -8
+
+
+def test_binding_rejects_cpu_tensors(lib):
+    w = wl.WORKLOADS[wl.WORKLOAD_ORDER[0]]
+    inp = wl.make_inputs(w)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        cv.conv_verify(inp["x"], inp["conv_state"], inp["weight"], None, inp["out"], inp["window"], layout="dense",
+                       qk_channels=256, head_dim=64)
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    with pytest.raises(RuntimeError, match="not built"):
+        cv.load_library(str(tmp_path / "nope.so"))

@@ -1,0 +1,249 @@
+"""Parity of the CUDA library (through the C ABI) with the CPU oracle, element by element.
+
+State, snapshots, commit and status codes must match bitwise; outputs within 1e-5 relative (+1e-7
+absolute floor) in fp32 and 2 bf16 ulp in bf16.  Every buffer starts filled with a sentinel so
+untouched regions (padded sequences, unused slots, state columns past W-1) are compared too.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+from gpu_helpers import run_gpu_commit, run_gpu_verify, to_device
+from helpers import assert_bits_equal, assert_out_close, clone_inputs, run_oracle_commit, run_oracle_verify
+from spec_decode_verify_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+
+def check_verify_and_commit(cv, w: wl.VerifyWorkload, inp: dict, commit=True):
+    ref = run_oracle_verify(w, inp)
+    got = run_gpu_verify(cv, w, inp)
+    assert_bits_equal(got["err"].cpu(), ref["status"], "err")
+    assert_bits_equal(got["window"].cpu(), ref["window"], "window")
+    assert_bits_equal(got["conv_state"].cpu(), ref["conv_state"], "state")
+    assert_out_close(got["out"].cpu(), ref["out"], "out")
+    if commit:
+        st_ref = run_oracle_commit(w, ref)
+        st_got = run_gpu_commit(cv, w, got)
+        assert_bits_equal(st_got.cpu(), st_ref, "commit err")
+        assert_bits_equal(got["conv_state"].cpu(), ref["conv_state"], "committed state")
+    return ref, got
+
+
+@pytest.mark.parametrize("name", wl.WORKLOAD_ORDER)
+def test_named_workloads(cuda_lib, name):
+    """All five named workloads at full size, in the launch configuration the bench times."""
+    w = wl.WORKLOADS[name]
+    check_verify_and_commit(cuda_lib, w, wl.make_inputs(w))
+
+
+def test_named_workloads_second_seed(cuda_lib):
+    for name in wl.WORKLOAD_ORDER[:2] + wl.WORKLOAD_ORDER[3:]:
+        w = wl.WORKLOADS[name]
+        check_verify_and_commit(cuda_lib, w, wl.make_inputs(w, seed=w.seed + 1000))
+
+
+@pytest.mark.parametrize("case", range(60))
+def test_random_sweep(cuda_lib, case):
+    """Random small shapes: W in 2..4, T in {1,2,3,4,8,9,16,17}, ragged dims (not multiples of 8 or
+    of the block), head_dim 8..128, fp32/bf16, dense/dedup, bias on/off, padded rows, offsets."""
+    rng = np.random.default_rng(1000 + case)
+    over = {}
+    if case % 3 == 0:
+        over["n_pad"] = 1
+        over["extra_slots"] = 2
+        over["n_seq"] = 4
+    if case % 4 == 1:
+        over["state_offset"] = True
+    w = wl.random_case(rng, **over)
+    if w.n_pad >= w.n_seq:
+        w = w.replace(n_pad=w.n_seq - 1)
+    check_verify_and_commit(cuda_lib, w, wl.make_inputs(w))
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("dim", [1, 7, 8, 9, 1023, 1024, 1025, 2048 + 8 + 3])
+def test_ragged_dims(cuda_lib, dtype, dim):
+    w = wl.VerifyWorkload("ragged", n_seq=3, T=5, dim=dim, width=4, qk_channels=0, head_dim=8, dtype=dtype,
+                          layout="dedup", bias=True, n_pad=1, extra_slots=1, seed=dim)
+    check_verify_and_commit(cuda_lib, w, wl.make_inputs(w))
+
+
+@pytest.mark.parametrize("hd", [8, 16, 32, 64, 128, 256])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_head_dims(cuda_lib, hd, dtype):
+    w = wl.VerifyWorkload("hd", n_seq=2, T=3, dim=4 * hd + 40, width=4, qk_channels=4 * hd, head_dim=hd,
+                          dtype=dtype, layout="dense", bias=True, seed=hd)
+    check_verify_and_commit(cuda_lib, w, wl.make_inputs(w))
+
+
+@pytest.mark.parametrize("T", [1, 31, 64, 128])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_long_T(cuda_lib, T, dtype):
+    w = wl.VerifyWorkload("longT", n_seq=2, T=T, dim=1000, width=4, qk_channels=512, head_dim=128, dtype=dtype,
+                          layout="dedup" if T % 2 else "dense", seed=T)
+    check_verify_and_commit(cuda_lib, w, wl.make_inputs(w))
+
+
+def test_unaligned_strided_x(cuda_lib):
+    """x as an odd-offset, odd-stride slice (no 16-byte vectors possible): scalar load path."""
+    w = wl.VerifyWorkload("xodd", n_seq=3, T=4, dim=300, width=4, qk_channels=256, head_dim=64, dtype="bf16",
+                          layout="dense", x_row_stride=301, seed=5)
+    inp = wl.make_inputs(w)
+    base = inp["x_base"]
+    inp["x"] = base.view(-1)[1:].as_strided((3, 4, 300), (4 * 301, 301, 1))
+    check_verify_and_commit(cuda_lib, w, inp)
+
+
+def test_transposed_dedup_row(cuda_lib):
+    """The dedup row stored column-major ([n_seq, T+W-2, dim] seen as [n_seq, dim, T+W-2])."""
+    for dtype in ["f32", "bf16"]:
+        w = wl.VerifyWorkload("tr", n_seq=3, T=8, dim=1200, width=4, qk_channels=512, head_dim=128, dtype=dtype,
+                              layout="dedup", bias=True, seed=7)
+        inp = wl.make_inputs(w)
+        inp["window"] = wl.sentinel_tensor((w.n_seq, w.T + 2, w.dim), w.torch_dtype).transpose(1, 2)
+        check_verify_and_commit(cuda_lib, w, inp)
+
+
+def test_dense_window_permuted(cuda_lib):
+    """Dense snapshots with the token axis innermost-but-one: arbitrary strides take the element path."""
+    w = wl.VerifyWorkload("perm", n_seq=2, T=5, dim=520, width=3, qk_channels=0, head_dim=8, dtype="bf16",
+                          layout="dense", seed=9)
+    inp = wl.make_inputs(w)
+    inp["window"] = wl.sentinel_tensor((w.n_seq, w.dim, w.width - 1, w.T), w.torch_dtype).permute(0, 3, 1, 2)
+    check_verify_and_commit(cuda_lib, w, inp)
+
+
+def test_sequential_equals_batched_in_T_on_gpu(cuda_lib):
+    """P-4 on the GPU: T single-token launches give bit-identical outputs and final state."""
+    w = wl.VerifyWorkload("seq", n_seq=3, T=6, dim=1100, width=4, qk_channels=512, head_dim=128, dtype="bf16",
+                          layout="dense", bias=True, seed=21)
+    inp = wl.make_inputs(w)
+    full = run_gpu_verify(cuda_lib, w, inp)
+    w1 = w.replace(T=1)
+    cur = clone_inputs(inp)
+    for t in range(w.T):
+        step = dict(cur)
+        step["x"] = inp["x"][:, t:t + 1]
+        step["out"] = wl.sentinel_tensor((w.n_seq, 1, w.dim), w.torch_dtype)
+        step["window"] = wl.sentinel_tensor(wl.window_shape(w1), w.torch_dtype)
+        r1 = run_gpu_verify(cuda_lib, w1, step)
+        assert_bits_equal(r1["out"][:, 0].cpu(), full["out"][:, t].cpu(), f"out {t}")
+        assert_bits_equal(r1["window"][:, 0].cpu(), full["window"][:, t].cpu(), f"snapshot {t}")
+        cur["conv_state"] = r1["conv_state"].cpu()
+    assert_bits_equal(cur["conv_state"], full["conv_state"].cpu(), "final state")
+
+
+def test_batched_equals_separate_on_gpu(cuda_lib):
+    """P-5 on the GPU: batched launch == one launch per sequence, bitwise."""
+    w = wl.VerifyWorkload("bat", n_seq=4, T=8, dim=2100, width=4, qk_channels=1024, head_dim=128, dtype="bf16",
+                          layout="dedup", n_pad=1, extra_slots=2, seed=22)
+    inp = wl.make_inputs(w)
+    full = run_gpu_verify(cuda_lib, w, inp)
+    for s in range(w.n_seq):
+        ws = w.replace(n_seq=1, n_pad=0)
+        one = clone_inputs(inp)
+        one["x"] = inp["x"][s:s + 1]
+        one["cache_idx"] = inp["cache_idx"][s:s + 1].clone()
+        one["out"] = wl.sentinel_tensor((1, w.T, w.dim), w.torch_dtype)
+        one["window"] = wl.sentinel_tensor(wl.window_shape(ws), w.torch_dtype)
+        r1 = run_gpu_verify(cuda_lib, ws, one)
+        assert_bits_equal(r1["out"][0].cpu(), full["out"][s].cpu(), "out")
+        assert_bits_equal(r1["window"][0].cpu(), full["window"][s].cpu(), "window")
+
+
+def test_dedup_equals_dense_on_gpu(cuda_lib):
+    """P-6 on the GPU: the dedup row read through its view equals the dense snapshots bitwise."""
+    w = wl.VerifyWorkload("dd", n_seq=3, T=9, dim=3000, width=4, qk_channels=1024, head_dim=128, dtype="bf16",
+                          layout="dense", seed=23)
+    inp = wl.make_inputs(w)
+    dense = run_gpu_verify(cuda_lib, w, inp)
+    wd = w.replace(layout="dedup")
+    inp_d = clone_inputs(inp)
+    inp_d["window"] = wl.sentinel_tensor(wl.window_shape(wd), w.torch_dtype)
+    dd = run_gpu_verify(cuda_lib, wd, inp_d)
+    row = dd["window"]
+    view = row.as_strided((w.n_seq, w.T, w.dim, 3), (row.stride(0), row.stride(2), row.stride(1), row.stride(2)))
+    assert_bits_equal(view.cpu(), dense["window"].cpu(), "view")
+    assert_bits_equal(dd["out"].cpu(), dense["out"].cpu(), "out")
+
+
+def test_commit_equals_shorter_verify_on_gpu(cuda_lib):
+    """P-9 on the GPU: verify(T) + commit(a) state == verify(first a tokens) state, bitwise."""
+    w = wl.VerifyWorkload("cm", n_seq=6, T=8, dim=2048, width=4, qk_channels=1024, head_dim=128, dtype="bf16",
+                          layout="dedup", n_pad=1, extra_slots=2, seed=24)
+    inp = wl.make_inputs(w)
+    d = run_gpu_verify(cuda_lib, w, inp)
+    assert (run_gpu_commit(cuda_lib, w, d).cpu() == 0).all()
+    for s in range(w.n_seq):
+        slot = int(inp["cache_idx"][s])
+        if slot < 0:
+            continue
+        a = int(inp["accept_len"][s])
+        wa = w.replace(T=a, n_seq=1, n_pad=0)
+        one = clone_inputs(inp)
+        one["x"] = inp["x"][s:s + 1, :a]
+        one["cache_idx"] = inp["cache_idx"][s:s + 1].clone()
+        one["out"] = wl.sentinel_tensor((1, a, w.dim), w.torch_dtype)
+        one["window"] = wl.sentinel_tensor(wl.window_shape(wa), w.torch_dtype)
+        ra = run_gpu_verify(cuda_lib, wa, one)
+        assert_bits_equal(d["conv_state"][slot].cpu(), ra["conv_state"][slot].cpu(), f"seq {s}")
+
+
+def test_status_codes_on_gpu(cuda_lib):
+    """Bad slot / offset / accept: flagged per sequence, the sequence untouched, others unaffected."""
+    w = wl.VerifyWorkload("bad", n_seq=5, T=4, dim=900, width=4, qk_channels=256, head_dim=64, dtype="bf16",
+                          layout="dense", state_offset=True, seed=25)
+    inp = wl.make_inputs(w)
+    inp["cache_idx"][0] = w.n_slots + 3
+    inp["state_off"][1] = w.state_cols - w.width + 2
+    inp["state_off"][2] = -4
+    inp["cache_idx"][3] = -1
+    ref, got = check_verify_and_commit(cuda_lib, w, inp, commit=False)
+    assert got["err"].tolist() == [1, 2, 2, 0, 0]
+    acc = inp["accept_len"].clone()
+    acc[4] = 0
+    st_ref = run_oracle_commit(w, ref, accept_len=acc)
+    st_got = run_gpu_commit(cuda_lib, w, got, accept_len=acc)
+    assert_bits_equal(st_got.cpu(), st_ref, "commit err")
+    assert st_got.tolist() == [1, 0, 0, 0, 4]
+    assert_bits_equal(got["conv_state"].cpu(), ref["conv_state"], "state")
+
+
+def test_nan_payload_and_signed_zero_on_gpu(cuda_lib):
+    w = wl.VerifyWorkload("nan", n_seq=2, T=3, dim=64, width=4, qk_channels=0, head_dim=8, dtype="bf16",
+                          layout="dedup", seed=26)
+    inp = wl.make_inputs(w)
+    slot = int(inp["cache_idx"][0])
+    inp["conv_state"].view(torch.int16)[slot, 3, 1] = 0x7FA1
+    inp["conv_state"].view(torch.int16)[slot, 4, 2] = -32768
+    inp["x"].view(torch.int16)[0, 1, 5] = 0x7F81
+    check_verify_and_commit(cuda_lib, w, inp)
+
+
+def test_empty_batch_is_noop(cuda_lib):
+    w = wl.VerifyWorkload("empty", n_seq=1, T=2, dim=64, width=4, qk_channels=0, head_dim=8, dtype="bf16",
+                          layout="dense", seed=27)
+    d = to_device(wl.make_inputs(w))
+    before = d["conv_state"].clone()
+    cuda_lib.conv_verify(d["x"][:0], d["conv_state"], d["weight"], None, d["out"][:0], d["window"][:0],
+                         layout="dense", qk_channels=0, head_dim=8)
+    torch.cuda.synchronize()
+    assert torch.equal(before.view(torch.int16), d["conv_state"].view(torch.int16))
+
+
+def test_all_padded_touches_nothing(cuda_lib):
+    w = wl.VerifyWorkload("allpad", n_seq=3, T=4, dim=512, width=4, qk_channels=256, head_dim=128, dtype="bf16",
+                          layout="dedup", n_pad=3, seed=28)
+    check_verify_and_commit(cuda_lib, w, wl.make_inputs(w))
+
+
+def test_cpu_tensors_rejected(cuda_lib):
+    """No CPU path: CPU tensors raise instead of computing."""
+    w = wl.WORKLOADS[wl.WORKLOAD_ORDER[0]]
+    inp = wl.make_inputs(w)
+    with pytest.raises(ValueError):
+        cuda_lib.conv_verify(inp["x"], inp["conv_state"], inp["weight"], None, inp["out"], inp["window"],
+                             layout="dense", qk_channels=256, head_dim=64)
