@@ -58,7 +58,7 @@ class CommitArgs(ctypes.Structure):
 class LaunchPlan(ctypes.Structure):
     """Mirror of cv_launch_plan."""
     _fields_ = [("grid_x", c_i32), ("grid_y", c_i32), ("threads", c_i32), ("smem_bytes", c_i32),
-                ("channels_per_block", c_i32), ("reserved0", c_i32)]
+                ("channels_per_block", c_i32), ("path", c_i32)]
 
 
 class CvError(RuntimeError):

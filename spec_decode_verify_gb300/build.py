@@ -16,7 +16,7 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libconvverify.so")
 INCLUDE = os.path.join(ROOT, "include")
-SOURCES = ["cv_abi.cu"]
+SOURCES = ["cv_abi.cu"] + [f"cv_inst_{d}_w{w}.cu" for d in ("bf16", "f32") for w in (2, 3, 4)]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
               "-I", INCLUDE, "-I", CSRC]

@@ -1,26 +1,43 @@
 // C ABI of the verify/commit library: argument validation, launch planning and dispatch to the
-// kernels in cv_kernels.cuh.  Every check runs on the host before anything is launched; the
-// function reports a negative status and launches nothing when a check fails.
+// kernels.  Every check runs on the host before anything is launched; a failed check returns a
+// negative status and launches nothing.
+//
+// Path selection for cv_conv_verify:
+//   fast, static T  (path 1): packed, 16-byte aligned buffers, dim % 8 == 0, T <= the largest
+//                             compiled static T (16 for bf16, 8 for fp32); either window layout.
+//   fast, chunked   (path 2): the same buffers with a dense window and a larger T.
+//   general         (path 0): everything else (any strides, any dim, dedup rows with a larger T).
 #include <atomic>
 #include <cstdint>
 #include <cstring>
 
 #include "convverify.h"
-#include "cv_kernels.cuh"
+#include "cv_launch.h"
 
 namespace {
 
-constexpr int kMaxThreads = 256;
+constexpr int kFastThreads = 128;
 constexpr int kMinThreads = 32;
-constexpr int kSmemBudget = 96 * 1024;   // per-block tile budget; keeps >= 2 blocks per SM
-constexpr int kCommitThreads = 256;
+constexpr int kGenericSmemBudget = 96 * 1024;
+constexpr int kCommitThreads = 128;
+constexpr int kSmemMax = 227 * 1024;
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool stride16(long long stride_elems, int esize) { return ((stride_elems * esize) & 15) == 0; }
 bool pow2(int v) { return v > 0 && (v & (v - 1)) == 0; }
 
-// Validates verify arguments; on success fills the launch plan.
-int plan_verify(const cv_verify_args *a, cv_launch_plan *pl) {
+const cvk::KernelSet &kernel_set(int dtype, int width) {
+    if (dtype == CV_BF16) {
+        if (width == 2) return cvk::kernels_bf16_w2();
+        if (width == 3) return cvk::kernels_bf16_w3();
+        return cvk::kernels_bf16_w4();
+    }
+    if (width == 2) return cvk::kernels_f32_w2();
+    if (width == 3) return cvk::kernels_f32_w3();
+    return cvk::kernels_f32_w4();
+}
+
+int check_verify(const cv_verify_args *a) {
     if (!a) return CV_ERR_NULL_ARGS;
     if (a->dtype != CV_F32 && a->dtype != CV_BF16) return CV_ERR_DTYPE;
     if (a->width < 2 || a->width > 4) return CV_ERR_WIDTH;
@@ -47,50 +64,89 @@ int plan_verify(const cv_verify_args *a, cv_launch_plan *pl) {
                 if (o == i) return CV_ERR_ALIAS;
         if (a->out == a->window) return CV_ERR_ALIAS;
     }
-
-    const int esize = a->dtype == CV_BF16 ? 2 : 4;
-    const int rows = a->T + a->width - 1;
-    const int pad = 16 / esize;  // one 16-byte vector of padding per tile row
-    const int min_threads = (a->qk_channels > 0 && a->head_dim / 8 > kMinThreads) ? a->head_dim / 8 : kMinThreads;
-    int threads = 128;
-    // small channel counts: do not launch threads that own no channel
-    while (threads > min_threads && 8 * (threads / 2) >= a->dim) threads /= 2;
-    // the block's channel count must hold whole L2 groups
-    while (a->qk_channels > 0 && 8 * threads < a->head_dim) threads *= 2;
-    long long smem = (long long)rows * (8 * threads + pad) * esize;
-    while (smem > kSmemBudget && threads > min_threads && 8 * (threads / 2) >= (a->qk_channels > 0 ? a->head_dim : 8)) {
-        threads /= 2;
-        smem = (long long)rows * (8 * threads + pad) * esize;
-    }
-    if (smem > 227 * 1024 || threads > kMaxThreads) return CV_ERR_SMEM;
-    const int bc = 8 * threads;
-    pl->grid_x = (a->dim + bc - 1) / bc;
-    pl->grid_y = a->n_seq;
-    pl->threads = threads;
-    pl->smem_bytes = (int)smem;
-    pl->channels_per_block = bc;
-    pl->reserved0 = 0;
     return CV_OK;
 }
 
-// Opt a kernel into more than 48 KB of dynamic shared memory, once per device.
-template <typename K>
-cudaError_t ensure_smem(K kernel, int bytes, std::atomic<unsigned long long> &done) {
+bool fast_eligible(const cv_verify_args *a, int esize, int max_static_t) {
+    const int R = a->width - 1;
+    const long long Q = a->T + R - 1;
+    if (a->dim % 8 != 0) return false;
+    if (!aligned16(a->x) || !stride16(a->x_seq_stride, esize) || !stride16(a->x_tok_stride, esize)) return false;
+    if (!aligned16(a->out) || !stride16(a->out_seq_stride, esize) || !stride16(a->out_tok_stride, esize)) return false;
+    if (!aligned16(a->weight) || (a->bias && !aligned16(a->bias))) return false;
+    if (!aligned16(a->window) || !stride16(a->win_seq_stride, esize) || a->win_col_stride != 1) return false;
+    if (a->window_layout == CV_WINDOW_DEDUP) return a->win_ch_stride == Q && a->T <= max_static_t;
+    return a->win_ch_stride == R && stride16(a->win_step_stride, esize);
+}
+
+bool state_packed(const void *state, long long slot_stride, long long ch_stride, int width, int esize) {
+    return aligned16(state) && stride16(slot_stride, esize) && ch_stride == width - 1;
+}
+
+// Validates verify arguments; on success fills the launch plan.
+int plan_verify(const cv_verify_args *a, cv_launch_plan *pl) {
+    const int rc = check_verify(a);
+    if (rc != CV_OK) return rc;
+    const int esize = a->dtype == CV_BF16 ? 2 : 4;
+    const int R = a->width - 1;
+    const int min_threads =
+        (a->qk_channels > 0 && a->head_dim / 8 > kMinThreads) ? a->head_dim / 8 : kMinThreads;
+    const cvk::KernelSet &ks = kernel_set(a->dtype, a->width);
+    std::memset(pl, 0, sizeof *pl);
+
+    if (fast_eligible(a, esize, ks.max_static_t)) {
+        int threads = kFastThreads;
+        while (threads > min_threads && 8 * (threads / 2) >= a->dim) threads /= 2;
+        const long long bc = 8LL * threads;
+        long long smem = bc * R * esize;  // committed-window image
+        if (a->window_layout == CV_WINDOW_DEDUP) smem += bc * (a->T + R - 1) * esize;
+        pl->threads = threads;
+        pl->channels_per_block = (int)bc;
+        pl->smem_bytes = (int)smem;
+        pl->path = a->T <= ks.max_static_t ? 1 : 2;
+    } else {
+        const int rows = a->T + a->width - 1;
+        const int pad = 16 / esize;  // one 16-byte vector of padding per tile row
+        int threads = 128;
+        while (threads > min_threads && 8 * (threads / 2) >= a->dim) threads /= 2;
+        long long smem = (long long)rows * (8 * threads + pad) * esize;
+        while (smem > kGenericSmemBudget && threads > min_threads) {
+            threads /= 2;
+            smem = (long long)rows * (8 * threads + pad) * esize;
+        }
+        if (smem > kSmemMax) return CV_ERR_SMEM;
+        pl->threads = threads;
+        pl->channels_per_block = 8 * threads;
+        pl->smem_bytes = (int)smem;
+        pl->path = 0;
+    }
+    pl->grid_x = (a->dim + pl->channels_per_block - 1) / pl->channels_per_block;
+    pl->grid_y = a->n_seq;
+    return CV_OK;
+}
+
+// Opt a kernel into more than 48 KB of dynamic shared memory (once per kernel and device).
+cudaError_t ensure_smem(const void *kernel, int bytes) {
     if (bytes <= 48 * 1024) return cudaSuccess;
+    static std::atomic<unsigned long long> done_cache[64][4];  // tiny open-addressing cache
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    const unsigned long long bit = 1ull << (dev & 63);
-    if (done.load(std::memory_order_relaxed) & bit) return cudaSuccess;
-    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
-    if (e == cudaSuccess) done.fetch_or(bit);
-    return e;
+    const unsigned long long key = reinterpret_cast<uintptr_t>(kernel) ^ ((unsigned long long)dev << 56);
+    const unsigned h = (unsigned)((key >> 4) * 0x9E3779B1u) & 63u;
+    for (auto &slot : done_cache[h])
+        if (slot.load(std::memory_order_relaxed) == key) return cudaSuccess;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax);
+    if (e != cudaSuccess) return e;
+    for (auto &slot : done_cache[h]) {
+        unsigned long long z = 0;
+        if (slot.compare_exchange_strong(z, key)) break;
+    }
+    return cudaSuccess;
 }
 
-template <typename B, int W>
 int launch_verify(const cv_verify_args *a, const cv_launch_plan &pl, cudaStream_t stream) {
-    static std::atomic<unsigned long long> smem_done{0};
-    const int esize = (int)sizeof(B);
+    const int esize = a->dtype == CV_BF16 ? 2 : 4;
     cvk::VerifyParams p;
     std::memset(&p, 0, sizeof p);
     p.x = a->x;
@@ -124,23 +180,15 @@ int launch_verify(const cv_verify_args *a, const cv_launch_plan &pl, cudaStream_
     p.eps = a->l2_eps;
     p.x_vec = aligned16(a->x) && stride16(a->x_seq_stride, esize) && stride16(a->x_tok_stride, esize);
     p.out_vec = aligned16(a->out) && stride16(a->out_seq_stride, esize) && stride16(a->out_tok_stride, esize);
-    p.st_vec = aligned16(a->conv_state) && stride16(a->state_slot_stride, esize) && a->state_ch_stride == W - 1;
+    p.st_vec = state_packed(a->conv_state, a->state_slot_stride, a->state_ch_stride, a->width, esize);
     p.w_vec = aligned16(a->weight);
     p.b_vec = a->bias ? aligned16(a->bias) : 0;
 
-    auto kernel = cvk::verify_kernel<B, W>;
-    if (ensure_smem(kernel, pl.smem_bytes, smem_done) != cudaSuccess) return CV_ERR_LAUNCH;
-    kernel<<<dim3(pl.grid_x, pl.grid_y), pl.threads, pl.smem_bytes, stream>>>(p);
+    const cvk::KernelSet &ks = kernel_set(a->dtype, a->width);
+    cvk::VerifyKernel k = pl.path == 0 ? ks.generic : (pl.path == 1 ? ks.fast[a->T] : ks.fast[0]);
+    if (ensure_smem(reinterpret_cast<const void *>(k), pl.smem_bytes) != cudaSuccess) return CV_ERR_LAUNCH;
+    k<<<dim3(pl.grid_x, pl.grid_y), pl.threads, pl.smem_bytes, stream>>>(p);
     return cudaGetLastError() == cudaSuccess ? CV_OK : CV_ERR_LAUNCH;
-}
-
-template <typename B>
-int dispatch_verify(const cv_verify_args *a, const cv_launch_plan &pl, cudaStream_t st) {
-    switch (a->width) {
-        case 2: return launch_verify<B, 2>(a, pl, st);
-        case 3: return launch_verify<B, 3>(a, pl, st);
-        default: return launch_verify<B, 4>(a, pl, st);
-    }
 }
 
 int check_commit(const cv_commit_args *a) {
@@ -161,9 +209,10 @@ int check_commit(const cv_commit_args *a) {
     return CV_OK;
 }
 
-template <typename B, int W>
 int launch_commit(const cv_commit_args *a, cudaStream_t stream) {
-    const int esize = (int)sizeof(B);
+    const int esize = a->dtype == CV_BF16 ? 2 : 4;
+    const int R = a->width - 1;
+    const long long Q = a->T + R - 1;
     cvk::CommitParams p;
     std::memset(&p, 0, sizeof p);
     p.state = a->conv_state;
@@ -181,22 +230,28 @@ int launch_commit(const cv_commit_args *a, cudaStream_t stream) {
     p.T = a->T;
     p.dim = a->dim;
     p.n_slots = a->n_slots;
-    p.st_vec = aligned16(a->conv_state) && stride16(a->state_slot_stride, esize) && a->state_ch_stride == W - 1;
-    const long long elems = (long long)a->dim * (W - 1);
-    const long long per_block = (long long)kCommitThreads * (p.st_vec ? 16 / esize : 1);
-    long long gx = (elems + per_block - 1) / per_block;
-    if (gx > 1024) gx = 1024;
-    cvk::commit_kernel<B, W><<<dim3((unsigned)gx, a->n_seq), kCommitThreads, 0, stream>>>(p);
-    return cudaGetLastError() == cudaSuccess ? CV_OK : CV_ERR_LAUNCH;
-}
 
-template <typename B>
-int dispatch_commit(const cv_commit_args *a, cudaStream_t st) {
-    switch (a->width) {
-        case 2: return launch_commit<B, 2>(a, st);
-        case 3: return launch_commit<B, 3>(a, st);
-        default: return launch_commit<B, 4>(a, st);
+    const bool packed_state = state_packed(a->conv_state, a->state_slot_stride, a->state_ch_stride, a->width, esize);
+    const bool win_ok = a->dim % 8 == 0 && aligned16(a->window) && stride16(a->win_seq_stride, esize) &&
+                        a->win_col_stride == 1;
+    int threads = kCommitThreads;
+    while (threads > kMinThreads && 8 * (threads / 2) >= a->dim) threads /= 2;
+    int smem = 0;
+    if (packed_state && win_ok && a->window_layout == CV_WINDOW_DENSE && a->win_ch_stride == R &&
+        stride16(a->win_step_stride, esize)) {
+        p.mode = 1;
+    } else if (packed_state && win_ok && a->window_layout == CV_WINDOW_DEDUP && a->win_ch_stride == Q) {
+        while (threads > kMinThreads && 8LL * threads * Q * esize > 48 * 1024) threads /= 2;
+        p.mode = 2;
+        smem = (int)(8LL * threads * Q * esize);
+    } else {
+        p.mode = 0;
     }
+    const int bc = 8 * threads;
+    auto k = kernel_set(a->dtype, a->width).commit;
+    if (ensure_smem(reinterpret_cast<const void *>(k), smem) != cudaSuccess) return CV_ERR_LAUNCH;
+    k<<<dim3((a->dim + bc - 1) / bc, a->n_seq), threads, smem, stream>>>(p);
+    return cudaGetLastError() == cudaSuccess ? CV_OK : CV_ERR_LAUNCH;
 }
 
 }  // namespace
@@ -213,16 +268,14 @@ int cv_conv_verify(const cv_verify_args *args, void *stream) {
     const int rc = plan_verify(args, &pl);
     if (rc != CV_OK) return rc;
     if (args->n_seq == 0) return CV_OK;
-    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    return args->dtype == CV_BF16 ? dispatch_verify<uint16_t>(args, pl, st) : dispatch_verify<uint32_t>(args, pl, st);
+    return launch_verify(args, pl, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int cv_conv_commit(const cv_commit_args *args, void *stream) {
     const int rc = check_commit(args);
     if (rc != CV_OK) return rc;
     if (args->n_seq == 0) return CV_OK;
-    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    return args->dtype == CV_BF16 ? dispatch_commit<uint16_t>(args, st) : dispatch_commit<uint32_t>(args, st);
+    return launch_commit(args, reinterpret_cast<cudaStream_t>(stream));
 }
 
 const char *cv_status_string(int status) {

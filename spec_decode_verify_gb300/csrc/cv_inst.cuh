@@ -1,0 +1,28 @@
+// Builds the kernel table of one (element type, conv width); included once per instantiation unit
+// with CV_INST_B, CV_INST_W, CV_INST_MAXT and CV_INST_NAME defined.
+#include <utility>
+
+#include "cv_commit.cuh"
+#include "cv_launch.h"
+#include "cv_verify_fast.cuh"
+#include "cv_verify_generic.cuh"
+
+namespace cvk {
+namespace {
+template <typename B, int W, int... Ts>
+KernelSet make_set(std::integer_sequence<int, Ts...>) {
+    KernelSet k{};
+    k.fast[0] = verify_fast<B, W, 0>;
+    ((k.fast[Ts + 1] = verify_fast<B, W, Ts + 1>), ...);
+    k.max_static_t = (int)sizeof...(Ts);
+    k.generic = verify_generic<B, W>;
+    k.commit = commit_kernel<B, W>;
+    return k;
+}
+}  // namespace
+
+const KernelSet &CV_INST_NAME() {
+    static const KernelSet k = make_set<CV_INST_B, CV_INST_W>(std::make_integer_sequence<int, CV_INST_MAXT>{});
+    return k;
+}
+}  // namespace cvk

@@ -1,0 +1,6 @@
+// Kernel instantiations for f32 elements, conv width 2.
+#define CV_INST_B uint32_t
+#define CV_INST_W 2
+#define CV_INST_MAXT 8
+#define CV_INST_NAME kernels_f32_w2
+#include "cv_inst.cuh"

@@ -1,0 +1,30 @@
+// Internal: the kernel tables each instantiation unit provides to the C ABI layer.
+#pragma once
+
+#include "cv_device.cuh"
+
+namespace cvk {
+
+using VerifyKernel = void (*)(VerifyParams);
+using CommitKernel = void (*)(CommitParams);
+
+// Largest T compiled with T as a template parameter (fully unrolled token loop, dedup row built
+// in registers).  Above it the dense layout runs the chunked kernel and the dedup layout the
+// general kernel.
+constexpr int kMaxStaticT = 16;
+
+struct KernelSet {
+    VerifyKernel fast[kMaxStaticT + 1];  // [T] for 1 <= T <= max_static_t; [0] = chunked, any T, dense only
+    int max_static_t;
+    VerifyKernel generic;
+    CommitKernel commit;
+};
+
+const KernelSet &kernels_bf16_w2();
+const KernelSet &kernels_bf16_w3();
+const KernelSet &kernels_bf16_w4();
+const KernelSet &kernels_f32_w2();
+const KernelSet &kernels_f32_w3();
+const KernelSet &kernels_f32_w4();
+
+}  // namespace cvk

@@ -1,77 +1,19 @@
-// Device code of the batched speculative-verify conv1d update (sm_103a).
+// Verify kernel for any strides and layouts (the general path).
 //
-// Verify: one CTA per (channel block, sequence), the launch shape of the Atlas batched verify
-// (fn gdn_verify_fused_conv_kn_batched: grid (ceil(dim/block), n_seq)).  Each thread owns 8
-// consecutive channels, so every global access of x, out, state and weights is a 16-byte vector
-// and a warp touches 512 contiguous bytes per instruction.  The block's inputs are staged once in
-// shared memory as a token-major tile
+// Used when the fast path's preconditions do not hold: unaligned or odd-strided x / out, a
+// channel count that is not a multiple of 8, transposed or permuted snapshot layouts, or a
+// deduplicated row longer than the fast path keeps in registers.  One block per (channel block,
+// sequence); the block's inputs are staged once in a token-major shared-memory tile
 //     tile[j][c] = full_c[j],  j in [0, W-1+T)   (rows 0..W-2: committed window, then x_0..x_{T-1})
-// and every snapshot layout is written from that tile in destination order: the deduplicated row
-// of the sglang tile store (PR #46184, "Modifications") becomes one contiguous, coalesced run of
-// channels*(T+W-2) elements per block instead of W-1 scattered stores per token, the dense
-// intermediates become one run per token, and the committed window one run for the state.  All
-// snapshot and state traffic moves raw bits, so NaN payloads and signed zeros survive.
-//
-// Arithmetic per channel and token, in fp32: acc = bias + sum_j w[j]*full[t+j] with each product
-// rounded before its add (explicit _rn intrinsics keep the compiler from fusing them), SiLU, then
-// for q|k channels an L2 normalisation over the head_dim group as a warp-shuffle reduction over
-// head_dim/8 lanes (glm5next_kda mod.rs: "conv1d + SiLU -> L2(q,k only)", eps inside the root).
-//
-// Commit: one thread per 16 bytes of the destination state rows; the accept count is read on the
-// device (memra Engine::ssm_conv_ring_rebuild_dc keeps the accept count on the device too).
+// and every snapshot layout and the committed window are written from that tile in destination
+// order (channel-major runs, channel-stride-1 runs, or element by element).  The arithmetic is the
+// same as the fast path's: fp32, bias first, taps in order with each product rounded, SiLU, L2
+// over the head_dim group as an xor-shuffle over head_dim/8 lanes.
 #pragma once
 
-#include <cuda_bf16.h>
-#include <cuda_runtime.h>
-#include <stdint.h>
+#include "cv_device.cuh"
 
 namespace cvk {
-
-struct VerifyParams {
-    const void *x;
-    long long x_seq, x_tok;
-    void *out;
-    long long out_seq, out_tok;
-    void *state;
-    long long st_slot, st_ch;
-    const int *cache_idx;
-    const int *state_off;
-    const void *weight;
-    const void *bias;
-    void *win;
-    long long w_seq, w_step, w_ch, w_col;  // w_step already equals w_col for the dedup layout
-    int *err;
-    int n_seq, T, dim, n_slots, state_cols;
-    int qk_channels, head_dim, pitch;      // pitch: elements per shared-memory tile row
-    float eps;
-    int dedup;
-    int x_vec, out_vec, st_vec, w_vec, b_vec;  // 16-byte vector paths allowed (host-checked)
-};
-
-struct CommitParams {
-    void *state;
-    long long st_slot, st_ch;
-    const int *cache_idx;
-    const void *win;
-    long long w_seq, w_step, w_ch, w_col;
-    const int *accept_len;
-    int *err;
-    int n_seq, T, dim, n_slots;
-    int st_vec;
-};
-
-// ---------------------------------------------------------------- element helpers
-// B is the raw bit type of one element: uint16_t for bf16, uint32_t for fp32.
-
-template <typename B> __device__ __forceinline__ float widen(B b);
-template <> __device__ __forceinline__ float widen<uint16_t>(uint16_t b) { return __uint_as_float((uint32_t)b << 16); }
-template <> __device__ __forceinline__ float widen<uint32_t>(uint32_t b) { return __uint_as_float(b); }
-
-template <typename B> __device__ __forceinline__ B narrow(float f);
-template <> __device__ __forceinline__ uint16_t narrow<uint16_t>(float f) {
-    return __bfloat16_as_ushort(__float2bfloat16_rn(f));
-}
-template <> __device__ __forceinline__ uint32_t narrow<uint32_t>(float f) { return __float_as_uint(f); }
 
 // Eight consecutive elements as 16-byte words: one uint4 for bf16, two for fp32.
 template <typename B> struct Oct {
@@ -105,17 +47,6 @@ template <typename B> __device__ __forceinline__ void store_oct(B *p, const Oct<
 #pragma unroll
     for (int i = 0; i < Oct<B>::NV; ++i) *reinterpret_cast<uint4 *>(p + i * (16 / sizeof(B))) = o.v[i];
 }
-
-__device__ __forceinline__ void cp_async16(void *smem, const void *gmem) {
-    const unsigned s = (unsigned)__cvta_generic_to_shared(smem);
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(s), "l"(gmem) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit_wait_all() {
-    asm volatile("cp.async.commit_group;\n" ::: "memory");
-    asm volatile("cp.async.wait_group 0;\n" ::: "memory");
-}
-
-__device__ __forceinline__ float silu(float a) { return a / (1.0f + expf(-a)); }
 
 // Write one view of the tile: element (c, q) for c < nch, q < ncol is tile[(jofs+q)*pitch + c] and
 // goes to dst[c*ch_stride + q*col_stride].  Three shapes: channel-major contiguous (the dedup row
@@ -172,7 +103,7 @@ __device__ __forceinline__ void write_view(const B *__restrict__ tile, int pitch
 
 // ---------------------------------------------------------------- verify
 template <typename B, int W>
-__global__ void __launch_bounds__(256) verify_kernel(const __grid_constant__ VerifyParams p) {
+__global__ void __launch_bounds__(256) verify_generic(const __grid_constant__ VerifyParams p) {
     constexpr int R = W - 1;  // committed window columns
     extern __shared__ __align__(16) unsigned char smem_raw[];
     B *tile = reinterpret_cast<B *>(smem_raw);
@@ -185,11 +116,7 @@ __global__ void __launch_bounds__(256) verify_kernel(const __grid_constant__ Ver
 
     const int slot = p.cache_idx ? p.cache_idx[s] : s;
     const int off = p.state_off ? p.state_off[s] : 0;
-    int status = 0;
-    if (slot >= 0) {
-        if (slot >= p.n_slots) status |= 1;
-        if (off < 0 || off > p.state_cols - R) status |= 2;
-    }
+    const int status = seq_status(slot, off, p.n_slots, p.state_cols, R);
     if (p.err && blockIdx.x == 0 && tid == 0) p.err[s] = status;
     if (slot < 0 || status) return;  // padded or rejected: touch nothing (uniform per block)
 
@@ -290,7 +217,7 @@ __global__ void __launch_bounds__(256) verify_kernel(const __grid_constant__ Ver
         }
     }
 
-    if (p.x_vec) cp_async_commit_wait_all();
+    if (p.x_vec) cp_async_wait_all();
     __syncthreads();
 
     // (4) snapshots and committed window, written from the tile in destination order
@@ -357,55 +284,6 @@ __global__ void __launch_bounds__(256) verify_kernel(const __grid_constant__ Ver
             store_oct(op, o);
         } else {
             for (int e = 0; e < my; ++e) op[e] = narrow<B>(y[e]);
-        }
-    }
-}
-
-// ---------------------------------------------------------------- commit
-template <typename B, int W>
-__global__ void __launch_bounds__(256) commit_kernel(const __grid_constant__ CommitParams p) {
-    constexpr int R = W - 1;
-    constexpr int CH = 16 / (int)sizeof(B);
-    const int s = blockIdx.y;
-    const int slot = p.cache_idx ? p.cache_idx[s] : s;
-    const int a = p.accept_len[s];
-    int status = 0;
-    if (slot >= 0) {
-        if (slot >= p.n_slots) status |= 1;
-        if (a < 1 || a > p.T) status |= 4;
-    }
-    if (p.err && blockIdx.x == 0 && threadIdx.x == 0) p.err[s] = status;
-    if (slot < 0 || status) return;
-
-    const B *src = reinterpret_cast<const B *>(p.win) + (long long)s * p.w_seq + (long long)(a - 1) * p.w_step;
-    B *dst = reinterpret_cast<B *>(p.state) + (long long)slot * p.st_slot;
-    const long long n = (long long)p.dim * R;
-    const long long gtid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-    const long long gstride = (long long)gridDim.x * blockDim.x;
-    if (p.st_vec) {
-        // destination rows are packed ([dim][R] contiguous): one 16-byte store per thread step
-        for (long long m = gtid; m * CH < n; m += gstride) {
-            const long long pos = m * CH;
-            uint32_t wv[4];
-            B *vb = reinterpret_cast<B *>(wv);
-#pragma unroll
-            for (int e = 0; e < CH; ++e) {
-                const long long q = pos + e;
-                const long long c = q / R;
-                const int k = (int)(q - c * R);
-                vb[e] = (q < n) ? src[c * p.w_ch + k * p.w_col] : (B)0;
-            }
-            if (pos + CH <= n) {
-                *reinterpret_cast<uint4 *>(dst + pos) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
-            } else {
-                for (int e = 0; pos + e < n; ++e) dst[pos + e] = vb[e];
-            }
-        }
-    } else {
-        for (long long i = gtid; i < n; i += gstride) {
-            const long long c = i / R;
-            const int k = (int)(i - c * R);
-            dst[c * p.st_ch + k] = src[c * p.w_ch + k * p.w_col];
         }
     }
 }

@@ -66,11 +66,36 @@ W3 = wl.WORKLOADS["n128_t8_dim10240_w4_bf16_dedup_pad13"]
 
 
 def test_plan_for_benchmark_workload(lib):
+    """128 x 8 x 10240 bf16 dedup: the static-T fast path, 1024 channels per block, shared memory for
+    the dedup row image (T+W-2 = 10 columns) and the committed-window image (3 columns)."""
     rc, pl = _plan(lib, _args(W3))
     assert rc == 0
-    assert (pl.grid_x, pl.grid_y, pl.threads, pl.channels_per_block) == (10, 128, 128, 1024)
-    assert pl.smem_bytes == (8 + 3) * (1024 + 8) * 2
+    assert (pl.grid_x, pl.grid_y, pl.threads, pl.channels_per_block, pl.path) == (10, 128, 128, 1024, 1)
+    assert pl.smem_bytes == 1024 * (10 + 3) * 2
     assert pl.channels_per_block % W3.head_dim == 0
+
+
+@pytest.mark.parametrize("name,path", [
+    ("n1_t2_dim512_w4_f32_dense", 1), ("n4_t4_dim4096_w4_bf16_dedup_bias", 1),
+    ("n8_t17_dim8192_w4_bf16_dense_qkvsplit_xstride12288", 2), ("n64_t8_dim6144_w3_bf16_dense_nol2_stateoff", 1)])
+def test_plan_paths_of_named_workloads(lib, name, path):
+    w = wl.WORKLOADS[name]
+    rc, pl = _plan(lib, _args(w))
+    assert rc == 0 and pl.path == path
+
+
+def test_plan_general_path_cases(lib):
+    """Odd dims, long dedup rows and transposed rows take the general kernel."""
+    assert _plan(lib, _args(W3.replace(dim=10236, qk_channels=4096)))[1].path == 0
+    assert _plan(lib, _args(W3.replace(T=17)))[1].path == 0
+    assert _plan(lib, _args(W3.replace(T=9, dtype="f32")))[1].path == 0
+    assert _plan(lib, _args(W3.replace(T=8, dtype="f32")))[1].path == 1
+    a = _args(W3)
+    a.win_ch_stride, a.win_col_stride, a.win_step_stride = 1, W3.dim, W3.dim
+    assert _plan(lib, a)[1].path == 0
+    a = _args(W3)
+    a.x_tok_stride = W3.dim + 1
+    assert _plan(lib, a)[1].path == 0
 
 
 @pytest.mark.parametrize("field,value,status", [
@@ -112,14 +137,15 @@ def test_zero_sequences_is_ok_without_gpu(lib):
     assert lib.cv_conv_verify(ctypes.byref(a), None) == 0
 
 
-@pytest.mark.parametrize("T,dtype,threads", [(8, "bf16", 128), (17, "bf16", 128), (32, "bf16", 128),
-                                             (64, "f32", 32), (128, "f32", 32), (128, "bf16", 32)])
-def test_plan_fits_shared_memory(lib, T, dtype, threads):
-    """The tile (T+W-1 rows of 8*threads channels plus 16 bytes) shrinks the block until it fits."""
+@pytest.mark.parametrize("T,dtype,threads", [(17, "bf16", 128), (32, "bf16", 128), (64, "f32", 32),
+                                             (128, "f32", 32), (128, "bf16", 32)])
+def test_general_plan_fits_shared_memory(lib, T, dtype, threads):
+    """General kernel: the tile (T+W-1 rows of 8*threads channels plus 16 bytes) shrinks the block
+    until it fits."""
     w = W3.replace(T=T, dtype=dtype, n_seq=2, n_pad=0, extra_slots=0)
     rc, pl = _plan(lib, _args(w))
     esize = 2 if dtype == "bf16" else 4
-    assert rc == 0 and pl.threads == threads
+    assert rc == 0 and pl.path == 0 and pl.threads == threads
     assert pl.smem_bytes == (T + 3) * (8 * threads * esize + 16)
     assert pl.smem_bytes <= 96 * 1024 or threads == 32
     assert pl.smem_bytes <= 227 * 1024
