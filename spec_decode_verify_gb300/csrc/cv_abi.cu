@@ -7,6 +7,9 @@
 //                             compiled static T (16 for bf16, 8 for fp32); either window layout.
 //   fast, chunked   (path 2): the same buffers with a dense window and a larger T.
 //   general         (path 0): everything else (any strides, any dim, dedup rows with a larger T).
+//   pipelined       (path 3): path 1's buffers with packed state rows: persistent blocks walk
+//                             (sequence, channel block) units and load each by bulk copy into
+//                             double-buffered shared memory, two units ahead.
 #include <atomic>
 #include <cstdint>
 #include <cstring>
@@ -17,6 +20,12 @@
 namespace {
 
 constexpr int kFastThreads = 128;
+constexpr int kPipeThreads = 128;
+// blocks per SM the pipelined kernel's launch bounds provide registers for
+constexpr int pipe_blocks_per_sm(int cpt, int T) { return (cpt == 4 && T <= 8) ? 4 : 2; }
+constexpr int kNumSMs = 152;             // GB300; sizes the persistent grid
+constexpr int kSmemPerSM = 232448;       // usable shared memory per SM
+constexpr int kSmemPerBlockReserved = 1024;
 constexpr int kMinThreads = 32;
 constexpr int kGenericSmemBudget = 96 * 1024;
 constexpr int kCommitThreads = 128;
@@ -94,10 +103,41 @@ int plan_verify(const cv_verify_args *a, cv_launch_plan *pl) {
     const cvk::KernelSet &ks = kernel_set(a->dtype, a->width);
     std::memset(pl, 0, sizeof *pl);
 
-    if (fast_eligible(a, esize, ks.max_static_t)) {
+    const bool fast = fast_eligible(a, esize, ks.max_static_t);
+    const int cpt = (a->qk_channels > 0 && a->head_dim / 4 > 32) ? 8 : 4;
+    if (fast && a->T <= ks.max_static_t &&
+        state_packed(a->conv_state, a->state_slot_stride, a->state_ch_stride, a->width, esize)) {
+        auto part = [](long long b) { return (b + 127) / 128 * 128; };
+        int threads = kPipeThreads;
+        while (threads > 32 && cpt * (threads / 2) >= a->dim) threads /= 2;
+        while (a->qk_channels > 0 && cpt * threads < a->head_dim) threads *= 2;
+        const long long bc = (long long)cpt * threads;
+        const long long Q = a->T + R - 1;
+        const long long stage = part(a->T * bc * esize) + part(R * bc * esize) + part(a->width * bc * esize) +
+                                part(bc * esize);
+        long long smem = 2 * stage + part(R * bc * esize) + 24;
+        if (a->window_layout == CV_WINDOW_DEDUP) smem += part(Q * bc * esize);
+        int per_sm = (int)(kSmemPerSM / (smem + kSmemPerBlockReserved));
+        if (per_sm > pipe_blocks_per_sm(cpt, a->T)) per_sm = pipe_blocks_per_sm(cpt, a->T);
+        if (smem <= kSmemMax && per_sm >= 1) {
+            const long long units = (long long)a->n_seq * ((a->dim + bc - 1) / bc);
+            long long g = (long long)kNumSMs * per_sm;
+            if (g > units) g = units;
+            pl->threads = threads;
+            pl->channels_per_block = (int)bc;
+            pl->smem_bytes = (int)smem;
+            pl->path = 3;
+            pl->grid_x = (int)(g > 0 ? g : 1);
+            pl->grid_y = 1;
+            return CV_OK;
+        }
+    }
+    if (fast) {
+        // 4 channels per thread (twice the threads of 8) unless an L2 group would span more than a warp
         int threads = kFastThreads;
-        while (threads > min_threads && 8 * (threads / 2) >= a->dim) threads /= 2;
-        const long long bc = 8LL * threads;
+        while (threads > 32 && cpt * (threads / 2) >= a->dim) threads /= 2;
+        while (a->qk_channels > 0 && cpt * threads < a->head_dim) threads *= 2;
+        const long long bc = (long long)cpt * threads;
         long long smem = bc * R * esize;  // committed-window image
         if (a->window_layout == CV_WINDOW_DEDUP) smem += bc * (a->T + R - 1) * esize;
         pl->threads = threads;
@@ -185,7 +225,11 @@ int launch_verify(const cv_verify_args *a, const cv_launch_plan &pl, cudaStream_
     p.b_vec = a->bias ? aligned16(a->bias) : 0;
 
     const cvk::KernelSet &ks = kernel_set(a->dtype, a->width);
-    cvk::VerifyKernel k = pl.path == 0 ? ks.generic : (pl.path == 1 ? ks.fast[a->T] : ks.fast[0]);
+    const int ci = pl.channels_per_block / pl.threads == 8 ? 1 : 0;
+    cvk::VerifyKernel k = pl.path == 0   ? ks.generic
+                          : pl.path == 1 ? ks.fast[ci][a->T]
+                          : pl.path == 2 ? ks.fast[ci][0]
+                                         : ks.pipe[ci][a->T];
     if (ensure_smem(reinterpret_cast<const void *>(k), pl.smem_bytes) != cudaSuccess) return CV_ERR_LAUNCH;
     k<<<dim3(pl.grid_x, pl.grid_y), pl.threads, pl.smem_bytes, stream>>>(p);
     return cudaGetLastError() == cudaSuccess ? CV_OK : CV_ERR_LAUNCH;

@@ -80,17 +80,94 @@ template <typename B> __device__ __forceinline__ uint32_t elem_raw(const uint32_
     return w[i];
 }
 
+// One word holding half h0 of word a (low half) and half h1 of word b (high half): one byte
+// permute with a selector that is a compile-time constant once the callers are unrolled.
+__device__ __forceinline__ uint32_t halves(uint32_t a, int h0, uint32_t b, int h1) {
+    return __byte_perm(a, b, (2 * h0) | ((2 * h0 + 1) << 4) | ((4 + 2 * h1) << 8) | ((5 + 2 * h1) << 12));
+}
+
 // Two raw 16-bit values -> one word (lo in the low half).  For fp32 only lo is used.
 __device__ __forceinline__ uint32_t pack_halves(uint32_t lo, uint32_t hi) { return __byte_perm(lo, hi, 0x5410); }
 
-// SiLU(a) = a * sigmoid(a), sigmoid through the exp intrinsic and the approximate reciprocal
-// instruction (rcp.approx keeps subnormal results, so a very negative a still yields its tiny
-// value and a -> -inf gives -0 like a / (1 + exp(-a))).  Relative error a few fp32 ulp.
-__device__ __forceinline__ float silu(float a) {
-    const float d = 1.0f + __expf(-a);
-    float r;
-    asm("rcp.approx.f32 %0, %1;" : "=f"(r) : "f"(d));
+// SiLU(a) = a / (1 + exp(-a)).  silu_fast evaluates exp(-a) = 2^(-a * log2 e) with the
+// ex2.approx instruction and the quotient as a * rcp.approx(1 + exp(-a)); relative error a few
+// fp32 ulp.  Both instructions flush subnormals, which matters only below a = -87
+// (1 + exp(-a) > 2^126): silu_exact is the plain expression, taken when some input is below -80
+// (see silu_run).
+__device__ __forceinline__ float silu_fast(float a) {
+    float e, r;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(a * -1.4426950408889634f));
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(1.0f + e));
     return a * r;
+}
+__device__ __forceinline__ float silu_exact(float a) { return a / (1.0f + expf(-a)); }
+
+// SiLU of n values with one range check for the run (a branch realistic inputs never take).
+template <int N>
+__device__ __forceinline__ void silu_run(const float *a, float *y) {
+    float lo = a[0];
+#pragma unroll
+    for (int i = 0; i < N; ++i) {
+        y[i] = silu_fast(a[i]);
+        lo = fminf(lo, a[i]);
+    }
+    if (lo < -80.0f) {
+#pragma unroll
+        for (int i = 0; i < N; ++i) y[i] = silu_exact(a[i]);
+    }
+}
+__device__ __forceinline__ float silu(float a) { return a < -80.0f ? silu_exact(a) : silu_fast(a); }
+
+// Sum of squares of a thread's CPT (4 or 8) values in one fixed order: a chain over each run of 4
+// channels, then the runs added pairwise.  The xor-shuffle tree over lanes continues the same
+// pairwise order, so the group sum is bit-identical whether a thread owns 4 or 8 channels.
+template <int CPT>
+__device__ __forceinline__ float sum_squares(const float *y) {
+    static_assert(CPT == 4 || CPT == 8, "4 or 8 channels per thread");
+    float a = y[0] * y[0];
+    a = fmaf(y[1], y[1], a);
+    a = fmaf(y[2], y[2], a);
+    a = fmaf(y[3], y[3], a);
+    if constexpr (CPT == 8) {
+        float b = y[4] * y[4];
+        b = fmaf(y[5], y[5], b);
+        b = fmaf(y[6], y[6], b);
+        b = fmaf(y[7], y[7], b);
+        a = a + b;
+    }
+    return a;
+}
+
+// Vector access of `NWORDS` 32-bit words at an address aligned to VA bytes (8 or 16).
+template <int VA, int NWORDS>
+__device__ __forceinline__ void ldv(uint32_t *w, const void *p) {
+    static_assert(VA == 8 || VA == 16, "vector width");
+    if constexpr (VA == 16) {
+        static_assert(NWORDS % 4 == 0, "16-byte vectors");
+#pragma unroll
+        for (int i = 0; i < NWORDS / 4; ++i) {
+            const uint4 q = reinterpret_cast<const uint4 *>(p)[i];
+            w[4 * i] = q.x, w[4 * i + 1] = q.y, w[4 * i + 2] = q.z, w[4 * i + 3] = q.w;
+        }
+    } else {
+        static_assert(NWORDS % 2 == 0, "8-byte vectors");
+#pragma unroll
+        for (int i = 0; i < NWORDS / 2; ++i) {
+            const uint2 q = reinterpret_cast<const uint2 *>(p)[i];
+            w[2 * i] = q.x, w[2 * i + 1] = q.y;
+        }
+    }
+}
+template <int VA, int NWORDS>
+__device__ __forceinline__ void stv(void *p, const uint32_t *w) {
+    if constexpr (VA == 16) {
+#pragma unroll
+        for (int i = 0; i < NWORDS / 4; ++i)
+            reinterpret_cast<uint4 *>(p)[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+    } else {
+#pragma unroll
+        for (int i = 0; i < NWORDS / 2; ++i) reinterpret_cast<uint2 *>(p)[i] = make_uint2(w[2 * i], w[2 * i + 1]);
+    }
 }
 
 __device__ __forceinline__ uint4 ld16(const void *p) { return *reinterpret_cast<const uint4 *>(p); }
@@ -110,6 +187,43 @@ __device__ __forceinline__ void bulk_commit_and_wait_read() {
 }
 // Make this thread's generic-proxy shared-memory writes visible to the bulk-copy (async) proxy.
 __device__ __forceinline__ void fence_smem_to_async() { asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory"); }
+
+// ---- mbarrier + bulk (TMA) loads for the pipelined kernel
+__device__ __forceinline__ void mbar_init(uint64_t *bar, unsigned count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_init_fence() { asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory"); }
+// Arrive once and announce `bytes` of asynchronous transactions that complete the phase.
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, unsigned bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, unsigned parity) {
+    unsigned done;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(done)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+// Wait for the phase with the given parity to complete, giving up after `limit` polls (each poll
+// may suspend the thread for a hardware-defined time).  Returns false on timeout.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, unsigned parity, unsigned limit) {
+    for (unsigned i = 0; i < limit; ++i)
+        if (mbar_try_wait(bar, parity)) return true;
+    return false;
+}
+// Global -> shared bulk copy completing `bytes` transactions on `bar`: 16-byte aligned addresses,
+// bytes % 16 == 0.
+__device__ __forceinline__ void bulk_load(void *sdst, const void *gsrc, unsigned bytes, uint64_t *bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(
+                     smem_u32(sdst)),
+                 "l"(gsrc), "r"(bytes), "r"(smem_u32(bar))
+                 : "memory");
+}
 
 __device__ __forceinline__ void cp_async16(void *smem, const void *gmem) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(smem_u32(smem)), "l"(gmem) : "memory");

@@ -6,14 +6,19 @@
 #include "cv_launch.h"
 #include "cv_verify_fast.cuh"
 #include "cv_verify_generic.cuh"
+#include "cv_verify_pipe.cuh"
 
 namespace cvk {
 namespace {
 template <typename B, int W, int... Ts>
 KernelSet make_set(std::integer_sequence<int, Ts...>) {
     KernelSet k{};
-    k.fast[0] = verify_fast<B, W, 0>;
-    ((k.fast[Ts + 1] = verify_fast<B, W, Ts + 1>), ...);
+    k.fast[0][0] = verify_fast<B, W, 0, 4>;
+    k.fast[1][0] = verify_fast<B, W, 0, 8>;
+    ((k.fast[0][Ts + 1] = verify_fast<B, W, Ts + 1, 4>), ...);
+    ((k.fast[1][Ts + 1] = verify_fast<B, W, Ts + 1, 8>), ...);
+    ((k.pipe[0][Ts + 1] = verify_pipe<B, W, Ts + 1, 4>), ...);
+    ((k.pipe[1][Ts + 1] = verify_pipe<B, W, Ts + 1, 8>), ...);
     k.max_static_t = (int)sizeof...(Ts);
     k.generic = verify_generic<B, W>;
     k.commit = commit_kernel<B, W>;

@@ -14,7 +14,11 @@ using CommitKernel = void (*)(CommitParams);
 constexpr int kMaxStaticT = 16;
 
 struct KernelSet {
-    VerifyKernel fast[kMaxStaticT + 1];  // [T] for 1 <= T <= max_static_t; [0] = chunked, any T, dense only
+    // fast[c][T]: c = 0 for 4 channels per thread, 1 for 8; T in 1..max_static_t compiled with T
+    // as a constant, [c][0] = chunked, any T, dense layout only
+    VerifyKernel fast[2][kMaxStaticT + 1];
+    // pipe[c][T]: persistent, bulk-copy pipelined, T in 1..max_static_t (index 0 unused)
+    VerifyKernel pipe[2][kMaxStaticT + 1];
     int max_static_t;
     VerifyKernel generic;
     CommitKernel commit;

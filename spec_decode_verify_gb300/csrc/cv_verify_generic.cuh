@@ -266,9 +266,7 @@ __global__ void __launch_bounds__(256) verify_generic(const __grid_constant__ Ve
             win[R - 1][e] = xv[e];
         }
         if (l2_block) {
-            float ss = 0.0f;
-#pragma unroll
-            for (int e = 0; e < 8; ++e) ss += y[e] * y[e];
+            float ss = sum_squares<8>(y);
             for (int o = lanes >> 1; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
             if (l2_mine) {
                 const float r = rsqrtf(ss + p.eps);

@@ -1,0 +1,297 @@
+// Persistent, bulk-copy-pipelined verify kernel: the main path for packed buffers with T <= 16.
+//
+// A unit of work is one block of CPT*threads channels of one sequence (the block of the Atlas
+// batched verify, fn gdn_verify_fused_conv_kn_batched).  A persistent block walks the units
+// u = blockIdx.x, blockIdx.x + gridDim.x, ...; one thread issues each unit's loads as bulk copies
+// (TMA, cp.async.bulk) into one of two shared-memory stages -- the T x rows, the committed
+// windows, the taps and the bias -- completing on that stage's mbarrier, two units ahead.  So the
+// reads of later units overlap the arithmetic and the stores of the current one on every SM,
+// instead of all blocks loading, then computing, then storing in lock-step.
+// Per unit each thread moves its CPT channels from the stage to registers, writes what depends on
+// the inputs only (the deduplicated row of sglang PR #46184 -- step t's window is columns
+// t..t+W-2 of [state[1..W-2], x_0..x_{T-1}] -- as one staged image written by one bulk copy;
+// dense snapshots as vector stores; the committed window, staged and bulk-copied into the packed
+// state rows) and computes the outputs: fp32 conv with bias first and each product rounded before
+// its add, SiLU, the L2 normalisation of the q|k groups over head_dim/CPT lanes with the T
+// shuffle trees interleaved (glm5next_kda mod.rs), one rounding, vector stores.
+// Every mbarrier wait is bounded: a block that waits too long sets CV_SEQ_TIMEOUT in err (when
+// given) for the unit's sequence, drains its copies in flight (again bounded) and returns.
+// Preconditions (checked on the host): those of the fast path, packed 16-byte-aligned state rows
+// ([dim][W-1]), T <= 16 (bf16) / 8 (fp32), head_dim / CPT <= 32.
+#pragma once
+
+#include <type_traits>
+
+#include "cv_device.cuh"
+
+namespace cvk {
+
+constexpr unsigned kWaitPolls = 1u << 20;  // mbarrier polls before a block gives up
+constexpr int kSeqTimeout = 8;             // err bit: a bulk copy did not complete in time
+
+__host__ __device__ constexpr int pipe_align(int bytes) { return bytes % 16 == 0 ? 16 : 8; }
+
+// Bytes of one stage for a block of bc channels (x rows, windows, taps, bias), each part 128-aligned.
+__host__ __device__ constexpr long long pipe_part(long long b) { return (b + 127) / 128 * 128; }
+
+template <typename B, int W, int TS, int CPT>
+__global__ void __launch_bounds__(128, (CPT == 4 && TS <= 8) ? 4 : 2) verify_pipe(const __grid_constant__ VerifyParams p) {
+    static_assert(TS > 0, "the pipelined kernel needs a compile-time T");
+    constexpr int R = W - 1;
+    constexpr int Q = TS + R - 1;  // dedup row columns
+    constexpr int ES = (int)sizeof(B);
+    constexpr int EW = 4 / ES;
+    constexpr int NW = CPT / EW;
+    constexpr int VX = pipe_align(CPT * ES);
+    constexpr int VS = pipe_align(CPT * R * ES);
+    constexpr int VW = pipe_align(CPT * W * ES);
+    constexpr int VI = pipe_align(CPT * Q * ES);
+    extern __shared__ __align__(128) unsigned char smem[];
+
+    const int tid = threadIdx.x;
+    const int BC = CPT * blockDim.x;
+    const int nblk = (p.dim + BC - 1) / BC;
+    const int n_units = p.n_seq * nblk;
+    const bool dense = !p.dedup;
+    const bool has_bias = p.bias != nullptr;
+
+    // shared memory: stage 0, stage 1, row image, window image, 2 mbarriers, 2 unit slots
+    const long long xb = pipe_part((long long)TS * BC * ES), sb = pipe_part((long long)R * BC * ES),
+                    wb = pipe_part((long long)W * BC * ES), bb = pipe_part((long long)BC * ES);
+    const long long stage_bytes = xb + sb + wb + bb;
+    unsigned char *const img = smem + 2 * stage_bytes;
+    unsigned char *const stimg = img + (dense ? 0 : pipe_part((long long)Q * BC * ES));
+    uint64_t *const bar = reinterpret_cast<uint64_t *>(stimg + sb);
+    volatile int *const info = reinterpret_cast<volatile int *>(bar + 2);
+
+    const int iters = (int)blockIdx.x < n_units ? (n_units - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+    if (tid == 0) {
+        mbar_init(&bar[0], 1);
+        mbar_init(&bar[1], 1);
+        mbar_init_fence();
+    }
+    __syncthreads();
+
+    // thread 0: start the copies of iteration k into stage k & 1 (or only arrive, for padding)
+    auto issue = [&](int k) {
+        const int st = k & 1;
+        unsigned char *stg = smem + st * stage_bytes;
+        const int u = (int)blockIdx.x + k * (int)gridDim.x;
+        const int s = u / nblk, c0 = (u - s * nblk) * BC;
+        const int nch = min(BC, p.dim - c0);
+        const int slot = p.cache_idx ? __ldg(p.cache_idx + s) : s;
+        const int off = p.state_off ? __ldg(p.state_off + s) : 0;
+        const int status = seq_status(slot, off, p.n_slots, p.state_cols, R);
+        if (p.err && c0 == 0) p.err[s] = status;
+        const bool go = slot >= 0 && status == 0;
+        info[st] = go ? slot : -1;
+        if (go) {
+            const unsigned bytes = (unsigned)((TS + R + W + (has_bias ? 1 : 0)) * nch * ES);
+            mbar_arrive_expect_tx(&bar[st], bytes);
+            const B *xs = reinterpret_cast<const B *>(p.x) + (long long)s * p.x_seq + c0;
+            for (int t = 0; t < TS; ++t)
+                bulk_load(stg + (long long)t * BC * ES, xs + (long long)t * p.x_tok, (unsigned)(nch * ES), &bar[st]);
+            bulk_load(stg + xb, reinterpret_cast<const B *>(p.state) + (long long)slot * p.st_slot + (long long)c0 * R,
+                      (unsigned)(nch * R * ES), &bar[st]);
+            bulk_load(stg + xb + sb, reinterpret_cast<const B *>(p.weight) + (long long)c0 * W, (unsigned)(nch * W * ES),
+                      &bar[st]);
+            if (has_bias)
+                bulk_load(stg + xb + sb + wb, reinterpret_cast<const B *>(p.bias) + c0, (unsigned)(nch * ES), &bar[st]);
+        } else {
+            mbar_arrive(&bar[st]);
+        }
+    };
+    if (tid == 0) {
+        if (iters > 0) issue(0);
+        if (iters > 1) issue(1);
+    }
+
+    const int cl = tid * CPT;
+    // unit u = blockIdx.x + k * gridDim.x as (sequence, channel block), stepped without divisions
+    const int g_s = (int)gridDim.x / nblk, g_b = (int)gridDim.x - g_s * nblk;
+    int s = (int)blockIdx.x / nblk, cb = (int)blockIdx.x - s * nblk;
+    constexpr int LOG_CPT = CPT == 4 ? 2 : 3;
+    const int lanes = p.head_dim >> LOG_CPT;  // threads per L2 group
+    for (int k = 0; k < iters; ++k) {
+        const int st = k & 1;
+        const unsigned char *stg = smem + st * stage_bytes;
+        const int c0 = cb * BC;
+        const int nch = min(BC, p.dim - c0);
+        const bool act = cl < nch;
+        const int c = c0 + cl;
+
+        const bool ok = mbar_wait_bounded(&bar[st], (unsigned)((k >> 1) & 1), kWaitPolls);
+        if (__syncthreads_or(!ok)) {
+            if (tid == 0) {
+                if (p.err) atomicOr(p.err + s, kSeqTimeout);
+                // drain the copies still in flight into this block's shared memory (bounded)
+                mbar_wait_bounded(&bar[st], (unsigned)((k >> 1) & 1), kWaitPolls);
+                if (k + 1 < iters) mbar_wait_bounded(&bar[st ^ 1], (unsigned)(((k + 1) >> 1) & 1), kWaitPolls);
+                asm volatile("cp.async.bulk.wait_group.read 0;\n" ::: "memory");
+            }
+            return;
+        }
+        const int slot = info[st];
+        const bool go = slot >= 0;
+
+        float fw[CPT][R + TS];  // inputs widened to fp32: [0, R) committed window, then x
+        float wt[CPT][W];
+        float bs[CPT];
+        uint32_t xr[TS][NW];    // raw x rows
+        uint32_t sw[R * NW];    // raw committed window, channel-major [CPT][R]
+        if (go && act) {
+#pragma unroll
+            for (int t = 0; t < TS; ++t) ldv<VX, NW>(xr[t], stg + ((long long)t * BC + cl) * ES);
+            ldv<VS, R * NW>(sw, stg + xb + (long long)cl * R * ES);
+#pragma unroll
+            for (int e = 0; e < CPT; ++e)
+#pragma unroll
+                for (int kk = 0; kk < R; ++kk) fw[e][kk] = elem_f<B>(sw, e * R + kk);
+            uint32_t ww[W * NW];
+            ldv<VW, W * NW>(ww, stg + xb + sb + (long long)cl * W * ES);
+#pragma unroll
+            for (int e = 0; e < CPT; ++e)
+#pragma unroll
+                for (int j = 0; j < W; ++j) wt[e][j] = elem_f<B>(ww, e * W + j);
+            uint32_t bw[NW];
+#pragma unroll
+            for (int i = 0; i < NW; ++i) bw[i] = 0u;
+            if (has_bias) ldv<VX, NW>(bw, stg + xb + sb + wb + (long long)cl * ES);
+#pragma unroll
+            for (int e = 0; e < CPT; ++e) bs[e] = elem_f<B>(bw, e);
+
+            // word and half holding input j of channel e (j < R: committed window, else x_{j-R})
+            auto word_of = [&](int e, int j) -> uint32_t { return j < R ? sw[(e * R + j) / EW] : xr[j - R][e / EW]; };
+            auto half_of = [&](int e, int j) -> int { return j < R ? (e * R + j) % EW : e % EW; };
+            // word i of a channel-major run of n columns starting at input j0
+            auto run_word = [&](int i, int n, int j0) -> uint32_t {
+                if (ES == 2) {
+                    const int a = 2 * i, b = 2 * i + 1;
+                    return halves(word_of(a / n, j0 + a % n), half_of(a / n, j0 + a % n), word_of(b / n, j0 + b % n),
+                                  half_of(b / n, j0 + b % n));
+                }
+                return word_of(i / n, j0 + i % n);
+            };
+            if (!dense) {
+                uint32_t im[Q * NW];  // CPT channels x Q columns; column q holds input q+1
+#pragma unroll
+                for (int i = 0; i < Q * NW; ++i) im[i] = run_word(i, Q, 1);
+                stv<VI, Q * NW>(img + (long long)tid * CPT * Q * ES, im);
+            } else {
+                B *wsq = reinterpret_cast<B *>(p.win) + (long long)s * p.w_seq + (long long)c * R;
+#pragma unroll
+                for (int t = 0; t < TS; ++t) {
+                    uint32_t w[R * NW];
+#pragma unroll
+                    for (int i = 0; i < R * NW; ++i) w[i] = run_word(i, R, t + 1);
+                    stv<VS, R * NW>(wsq + (long long)t * p.w_step, w);
+                }
+            }
+            uint32_t fin[R * NW];
+#pragma unroll
+            for (int i = 0; i < R * NW; ++i) fin[i] = run_word(i, R, TS);
+            stv<VS, R * NW>(stimg + (long long)tid * CPT * R * ES, fin);
+        }
+        fence_smem_to_async();
+        __syncthreads();  // images complete; stage st fully moved to registers
+        if (tid == 0) {
+            if (go) {
+                if (!dense)
+                    bulk_store(reinterpret_cast<B *>(p.win) + (long long)s * p.w_seq + (long long)c0 * Q, img,
+                               (unsigned)(nch * Q * ES));
+                bulk_store(reinterpret_cast<B *>(p.state) + (long long)slot * p.st_slot + (long long)c0 * R, stimg,
+                           (unsigned)(nch * R * ES));
+                asm volatile("cp.async.bulk.commit_group;\n" ::: "memory");
+            }
+            if (k + 2 < iters) issue(k + 2);
+        }
+        if (go) {
+            const bool l2_block = c0 < p.qk_channels;
+            const bool l2_mine = c < p.qk_channels;
+            float y[TS][CPT];
+            if (act) {
+                // conv + SiLU; one range check for the whole unit (see silu_fast)
+                float lo = 0.0f;
+#pragma unroll
+                for (int t = 0; t < TS; ++t) {
+#pragma unroll
+                    for (int e = 0; e < CPT; ++e) fw[e][R + t] = elem_f<B>(xr[t], e);
+#pragma unroll
+                    for (int e = 0; e < CPT; ++e) {
+                        float acc = bs[e];
+#pragma unroll
+                        for (int j = 0; j < W; ++j) acc = __fadd_rn(acc, __fmul_rn(wt[e][j], fw[e][t + j]));
+                        y[t][e] = silu_fast(acc);
+                        lo = fminf(lo, acc);
+                    }
+                }
+                if (lo < -80.0f) {
+#pragma unroll
+                    for (int t = 0; t < TS; ++t)
+#pragma unroll
+                        for (int e = 0; e < CPT; ++e) {
+                            float acc = bs[e];
+#pragma unroll
+                            for (int j = 0; j < W; ++j) acc = __fadd_rn(acc, __fmul_rn(wt[e][j], fw[e][t + j]));
+                            y[t][e] = silu_exact(acc);
+                        }
+                }
+            } else {
+#pragma unroll
+                for (int t = 0; t < TS; ++t)
+#pragma unroll
+                    for (int e = 0; e < CPT; ++e) y[t][e] = 0.0f;
+            }
+            if (l2_block) {
+                float ss[TS];
+#pragma unroll
+                for (int t = 0; t < TS; ++t) ss[t] = sum_squares<CPT>(y[t]);
+                if (CPT == 4 && lanes > 1) {
+#pragma unroll
+                    for (int t = 0; t < TS; ++t) ss[t] += __shfl_xor_sync(0xffffffffu, ss[t], 1);
+                }
+                for (int o = lanes >> 1; o >= (CPT == 4 ? 2 : 1); o >>= 1) {
+#pragma unroll
+                    for (int t = 0; t < TS; ++t) ss[t] += __shfl_xor_sync(0xffffffffu, ss[t], o);
+                }
+                if (l2_mine) {
+#pragma unroll
+                    for (int t = 0; t < TS; ++t) {
+                        const float r = rsqrtf(ss[t] + p.eps);
+#pragma unroll
+                        for (int e = 0; e < CPT; ++e) y[t][e] *= r;
+                    }
+                }
+            }
+            if (act) {
+                B *os = reinterpret_cast<B *>(p.out) + (long long)s * p.out_seq + c;
+#pragma unroll
+                for (int t = 0; t < TS; ++t) {
+                    uint32_t ow[NW];
+                    if (ES == 2) {
+#pragma unroll
+                        for (int i = 0; i < NW; ++i) {
+                            __nv_bfloat162 h = __floats2bfloat162_rn(y[t][2 * i], y[t][2 * i + 1]);
+                            ow[i] = *reinterpret_cast<uint32_t *>(&h);
+                        }
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < NW; ++i) ow[i] = __float_as_uint(y[t][i]);
+                    }
+                    stv<VX, NW>(os + (long long)t * p.out_tok, ow);
+                }
+            }
+        }
+        // the images are rewritten next iteration: their bulk reads must be done
+        if (tid == 0) asm volatile("cp.async.bulk.wait_group.read 0;\n" ::: "memory");
+        __syncthreads();
+        s += g_s;
+        cb += g_b;
+        if (cb >= nblk) {
+            cb -= nblk;
+            ++s;
+        }
+    }
+}
+
+}  // namespace cvk

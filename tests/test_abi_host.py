@@ -66,22 +66,31 @@ W3 = wl.WORKLOADS["n128_t8_dim10240_w4_bf16_dedup_pad13"]
 
 
 def test_plan_for_benchmark_workload(lib):
-    """128 x 8 x 10240 bf16 dedup: the static-T fast path, 1024 channels per block, shared memory for
-    the dedup row image (T+W-2 = 10 columns) and the committed-window image (3 columns)."""
+    """128 x 8 x 10240 bf16 dedup, packed state: the pipelined path.  4 channels per thread (an L2
+    group of 128 spans 32 lanes), 128 threads per unit of 512 channels.  Shared memory: two stages
+    of (8 x rows + 3 window columns + 4 taps + bias), each part rounded to 128 bytes, the dedup row
+    image (10 columns), the committed-window image (3 columns) and 24 bytes of barriers and slots;
+    4 blocks fit an SM, so the persistent grid is 152 * 4 = 608 blocks for 128 * 20 units."""
     rc, pl = _plan(lib, _args(W3))
     assert rc == 0
-    assert (pl.grid_x, pl.grid_y, pl.threads, pl.channels_per_block, pl.path) == (10, 128, 128, 1024, 1)
-    assert pl.smem_bytes == 1024 * (10 + 3) * 2
-    assert pl.channels_per_block % W3.head_dim == 0
+    stage = 8 * 512 * 2 + 3 * 512 * 2 + 4 * 512 * 2 + 512 * 2
+    smem = 2 * stage + 10 * 512 * 2 + 3 * 512 * 2 + 24
+    assert (pl.threads, pl.channels_per_block, pl.path, pl.smem_bytes) == (128, 512, 3, smem)
+    assert (pl.grid_x, pl.grid_y) == (152 * 4, 1)
 
 
 @pytest.mark.parametrize("name,path", [
-    ("n1_t2_dim512_w4_f32_dense", 1), ("n4_t4_dim4096_w4_bf16_dedup_bias", 1),
+    ("n1_t2_dim512_w4_f32_dense", 3), ("n4_t4_dim4096_w4_bf16_dedup_bias", 3),
     ("n8_t17_dim8192_w4_bf16_dense_qkvsplit_xstride12288", 2), ("n64_t8_dim6144_w3_bf16_dense_nol2_stateoff", 1)])
 def test_plan_paths_of_named_workloads(lib, name, path):
     w = wl.WORKLOADS[name]
     rc, pl = _plan(lib, _args(w))
     assert rc == 0 and pl.path == path
+    units = w.n_seq * -(-w.dim // pl.channels_per_block)
+    if path == 3:
+        assert pl.grid_y == 1 and 1 <= pl.grid_x <= units
+    else:
+        assert pl.grid_y == w.n_seq and pl.grid_x * pl.channels_per_block >= w.dim
 
 
 def test_plan_general_path_cases(lib):
@@ -89,7 +98,14 @@ def test_plan_general_path_cases(lib):
     assert _plan(lib, _args(W3.replace(dim=10236, qk_channels=4096)))[1].path == 0
     assert _plan(lib, _args(W3.replace(T=17)))[1].path == 0
     assert _plan(lib, _args(W3.replace(T=9, dtype="f32")))[1].path == 0
-    assert _plan(lib, _args(W3.replace(T=8, dtype="f32")))[1].path == 1
+    assert _plan(lib, _args(W3.replace(T=8, dtype="f32")))[1].path == 3
+    pl = _plan(lib, _args(W3.replace(head_dim=256, qk_channels=4096)))[1]
+    assert pl.path == 3 and pl.channels_per_block == 8 * pl.threads  # a 256-channel group needs 8 per thread
+    a = _args(W3)
+    a.state_ch_stride = 4  # state rows wider than the window: no bulk copy of the state
+    a.state_cols = 4
+    assert _plan(lib, a)[1].path == 1
+    assert _plan(lib, _args(W3.replace(T=12)))[1].path == 3
     a = _args(W3)
     a.win_ch_stride, a.win_col_stride, a.win_step_stride = 1, W3.dim, W3.dim
     assert _plan(lib, a)[1].path == 0

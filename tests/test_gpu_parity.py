@@ -247,3 +247,51 @@ def test_cpu_tensors_rejected(cuda_lib):
     with pytest.raises(ValueError):
         cuda_lib.conv_verify(inp["x"], inp["conv_state"], inp["weight"], None, inp["out"], inp["window"],
                              layout="dense", qk_channels=256, head_dim=64)
+
+
+def _run_with_state_view(cuda_lib, w, inp, state_dev, x_dev):
+    d = to_device(inp)
+    d["conv_state"] = state_dev
+    d["x"] = x_dev
+    d["err"] = torch.zeros(w.n_seq, dtype=torch.int32, device="cuda")
+    plan = cuda_lib.verify_plan(d["x"], d["conv_state"], d["weight"], d["bias"], d["out"], d["window"],
+                                layout=w.layout, qk_channels=w.qk_channels, head_dim=w.head_dim,
+                                cache_idx=d["cache_idx"])
+    cuda_lib.conv_verify(d["x"], d["conv_state"], d["weight"], d["bias"], d["out"], d["window"], layout=w.layout,
+                         qk_channels=w.qk_channels, head_dim=w.head_dim, cache_idx=d["cache_idx"], err=d["err"])
+    torch.cuda.synchronize()
+    return plan.path, d
+
+
+@pytest.mark.parametrize("layout", ["dense", "dedup"])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_all_paths_bit_identical(cuda_lib, layout, dtype):
+    """The same inputs through the pipelined kernel (packed state rows), the static-T kernel (state
+    rows one column wider, element stores) and the general kernel (x shifted off 16-byte alignment)
+    give bit-identical outputs, snapshots and committed windows -- and match the oracle."""
+    w = wl.VerifyWorkload("paths", n_seq=5, T=6, dim=1536, width=4, qk_channels=512, head_dim=128, dtype=dtype,
+                          layout=layout, bias=True, n_pad=1, extra_slots=2, seed=31)
+    inp = wl.make_inputs(w)
+    ref = run_oracle_verify(w, inp)
+    R = w.width - 1
+    results = {}
+    # packed state
+    p3, d3 = _run_with_state_view(cuda_lib, w, inp, inp["conv_state"].cuda(), to_device(inp)["x"])
+    # wider state rows: [n_slots, dim, R+1] with the window in columns 0..R-1, last column sentinel
+    wide = wl.sentinel_tensor((w.n_slots, w.dim, R + 1), w.torch_dtype)
+    wide[:, :, :R] = inp["conv_state"]
+    p1, d1 = _run_with_state_view(cuda_lib, w, inp, wide.cuda(), to_device(inp)["x"])
+    # x one element off alignment (copy into a buffer shifted by one element)
+    xb = torch.zeros(w.n_seq * w.T * w.dim + 1, dtype=w.torch_dtype)
+    xb[1:] = inp["x"].reshape(-1)
+    x_odd = xb.cuda()[1:].view(w.n_seq, w.T, w.dim)
+    p0, d0 = _run_with_state_view(cuda_lib, w, inp, inp["conv_state"].cuda(), x_odd)
+    assert (p3, p1, p0) == (3, 1, 0)
+    for name, d in (("pipelined", d3), ("static", d1), ("general", d0)):
+        assert_bits_equal(d["out"].cpu(), d3["out"].cpu(), f"out {name}")
+        assert_bits_equal(d["window"].cpu(), ref["window"], f"window {name}")
+        assert_out_close(d["out"].cpu(), ref["out"], f"out {name}")
+    assert_bits_equal(d3["conv_state"].cpu(), ref["conv_state"], "state pipelined")
+    assert_bits_equal(d0["conv_state"].cpu(), ref["conv_state"], "state general")
+    assert_bits_equal(d1["conv_state"][:, :, :R].cpu(), ref["conv_state"], "state static")
+    assert_bits_equal(d1["conv_state"][:, :, R:].cpu(), wide[:, :, R:], "state static, column past the window")
