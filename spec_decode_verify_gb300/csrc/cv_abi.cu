@@ -113,15 +113,19 @@ int plan_verify(const cv_verify_args *a, cv_launch_plan *pl) {
         while (a->qk_channels > 0 && cpt * threads < a->head_dim) threads *= 2;
         const long long bc = (long long)cpt * threads;
         const long long Q = a->T + R - 1;
-        const long long stage = part(a->T * bc * esize) + part(R * bc * esize) + part(a->width * bc * esize) +
-                                part(bc * esize);
-        long long smem = 2 * stage + part(R * bc * esize) + 24;
-        if (a->window_layout == CV_WINDOW_DEDUP) smem += part(Q * bc * esize);
+        // two stages (x rows + committed windows) and two image buffers (dedup row + windows)
+        const long long stage = part(a->T * bc * esize) + part(R * bc * esize);
+        long long image = part(R * bc * esize);
+        if (a->window_layout == CV_WINDOW_DEDUP) image += part(Q * bc * esize);
+        const long long smem = 2 * stage + 2 * image + 24;
         int per_sm = (int)(kSmemPerSM / (smem + kSmemPerBlockReserved));
         if (per_sm > pipe_blocks_per_sm(cpt, a->T)) per_sm = pipe_blocks_per_sm(cpt, a->T);
         if (smem <= kSmemMax && per_sm >= 1) {
-            const long long units = (long long)a->n_seq * ((a->dim + bc - 1) / bc);
+            const long long nblk = (a->dim + bc - 1) / bc;
+            const long long units = (long long)a->n_seq * nblk;
+            // a multiple of the channel-block count keeps each block on one channel block
             long long g = (long long)kNumSMs * per_sm;
+            if (g >= nblk) g = g / nblk * nblk;
             if (g > units) g = units;
             pl->threads = threads;
             pl->channels_per_block = (int)bc;
@@ -285,9 +289,24 @@ int launch_commit(const cv_commit_args *a, cudaStream_t stream) {
         stride16(a->win_step_stride, esize)) {
         p.mode = 1;
     } else if (packed_state && win_ok && a->window_layout == CV_WINDOW_DEDUP && a->win_ch_stride == Q) {
-        while (threads > kMinThreads && 8LL * threads * Q * esize > 48 * 1024) threads /= 2;
-        p.mode = 2;
-        smem = (int)(8LL * threads * Q * esize);
+        // persistent, pipelined: two stages of one unit's rows (8*threads channels x Q columns)
+        threads = kCommitThreads;
+        while (threads > kMinThreads && 8 * (threads / 2) >= a->dim) threads /= 2;
+        const long long stage = (8LL * threads * Q * esize + 127) / 128 * 128;
+        const long long sm = 2 * stage + 32;
+        if (sm <= kSmemMax) {
+            p.mode = 2;
+            const long long units = (long long)a->n_seq * ((a->dim + 8LL * threads - 1) / (8LL * threads));
+            long long per_sm = kSmemPerSM / (sm + kSmemPerBlockReserved);
+            if (per_sm > 8) per_sm = 8;
+            long long g = kNumSMs * per_sm;
+            if (g > units) g = units;
+            auto kp = kernel_set(a->dtype, a->width).commit_pipe;
+            if (ensure_smem(reinterpret_cast<const void *>(kp), (int)sm) != cudaSuccess) return CV_ERR_LAUNCH;
+            kp<<<(unsigned)(g > 0 ? g : 1), threads, (int)sm, stream>>>(p);
+            return cudaGetLastError() == cudaSuccess ? CV_OK : CV_ERR_LAUNCH;
+        }
+        p.mode = 0;
     } else {
         p.mode = 0;
     }

@@ -39,7 +39,7 @@ struct CommitParams {
     const int *accept_len;
     int *err;
     int n_seq, T, dim, n_slots;
-    int mode;  // 0: element by element, 1: packed dense snapshot -> packed state, 2: packed dedup row -> packed state
+    int mode;  // 0: element by element, 1: packed dense snapshot -> packed state, 2: packed dedup row -> packed state (pipelined)
 };
 
 // Per-sequence status shared by both kernels: 1 = slot out of range, 2 = state offset out of range.
@@ -174,6 +174,14 @@ __device__ __forceinline__ uint4 ld16(const void *p) { return *reinterpret_cast<
 __device__ __forceinline__ void st16(void *p, uint4 v) { *reinterpret_cast<uint4 *>(p) = v; }
 
 __device__ __forceinline__ unsigned smem_u32(const void *p) { return (unsigned)__cvta_generic_to_shared(p); }
+
+// Dynamic shared memory the launch provided, in bytes.  Kernels that carve a layout out of it
+// compare the two on entry and return without touching anything when the layout does not fit.
+__device__ __forceinline__ unsigned dynamic_smem_bytes() {
+    unsigned v;
+    asm("mov.u32 %0, %%dynamic_smem_size;" : "=r"(v));
+    return v;
+}
 
 // Shared -> global bulk copy (TMA, no tensor map): both addresses 16-byte aligned, bytes % 16 == 0.
 __device__ __forceinline__ void bulk_store(void *gdst, const void *ssrc, unsigned bytes) {

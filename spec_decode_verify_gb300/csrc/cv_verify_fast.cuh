@@ -217,6 +217,7 @@ __global__ void __launch_bounds__(256) verify_fast(const __grid_constant__ Verif
     bool bulk = false;
     if constexpr (TS > 0) {
         constexpr int Q = TS + R - 1;  // dedup row columns
+        if ((long long)BC * ((dense ? 0 : Q) + R) * ES > (long long)dynamic_smem_bytes()) return;  // launch mismatch
         constexpr int VI = chunk_align(CPT * Q * ES);
         // ---- 2. input-only outputs
         unsigned char *st_img = dense ? smem : smem + (size_t)BC * Q * ES;
@@ -262,6 +263,7 @@ __global__ void __launch_bounds__(256) verify_fast(const __grid_constant__ Verif
 #pragma unroll
         for (int u = 0; u < TS; ++u) store_token(u, y[u]);
     } else {
+        if ((long long)BC * R * ES > (long long)dynamic_smem_bytes()) return;  // launch mismatch
         // chunked: any T, dense window
         uint32_t fin[R * NW];
 #pragma unroll

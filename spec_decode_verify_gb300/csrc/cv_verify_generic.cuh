@@ -119,6 +119,7 @@ __global__ void __launch_bounds__(256) verify_generic(const __grid_constant__ Ve
     const int status = seq_status(slot, off, p.n_slots, p.state_cols, R);
     if (p.err && blockIdx.x == 0 && tid == 0) p.err[s] = status;
     if (slot < 0 || status) return;  // padded or rejected: touch nothing (uniform per block)
+    if ((long long)(T + R) * pitch * (long long)sizeof(B) > (long long)dynamic_smem_bytes()) return;  // launch mismatch
 
     const int nch = min(BC, p.dim - c0);
     const int cl = tid * 8;  // first block-local channel of this thread

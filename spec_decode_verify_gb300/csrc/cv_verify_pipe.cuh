@@ -2,11 +2,13 @@
 //
 // A unit of work is one block of CPT*threads channels of one sequence (the block of the Atlas
 // batched verify, fn gdn_verify_fused_conv_kn_batched).  A persistent block walks the units
-// u = blockIdx.x, blockIdx.x + gridDim.x, ...; one thread issues each unit's loads as bulk copies
-// (TMA, cp.async.bulk) into one of two shared-memory stages -- the T x rows, the committed
-// windows, the taps and the bias -- completing on that stage's mbarrier, two units ahead.  So the
-// reads of later units overlap the arithmetic and the stores of the current one on every SM,
-// instead of all blocks loading, then computing, then storing in lock-step.
+// u = blockIdx.x, blockIdx.x + gridDim.x, ...; when the grid is a multiple of the channel-block
+// count every unit of a block has the same channels, so the taps and bias are loaded once.  One
+// thread issues each unit's loads as bulk copies (TMA, cp.async.bulk) into one of two
+// shared-memory stages -- the T x rows and the committed windows -- completing on that stage's
+// mbarrier, two units ahead.  So the reads of later units overlap the arithmetic and the stores of
+// the current one on every SM, instead of all blocks loading, then computing, then storing in
+// lock-step.  The staged images are double-buffered too, so one block barrier per unit suffices.
 // Per unit each thread moves its CPT channels from the stage to registers, writes what depends on
 // the inputs only (the deduplicated row of sglang PR #46184 -- step t's window is columns
 // t..t+W-2 of [state[1..W-2], x_0..x_{T-1}] -- as one staged image written by one bulk copy;
@@ -37,6 +39,7 @@ __host__ __device__ constexpr long long pipe_part(long long b) { return (b + 127
 template <typename B, int W, int TS, int CPT>
 __global__ void __launch_bounds__(128, (CPT == 4 && TS <= 8) ? 4 : 2) verify_pipe(const __grid_constant__ VerifyParams p) {
     static_assert(TS > 0, "the pipelined kernel needs a compile-time T");
+    // (taps and bias are read from global memory, so W*CPT*ES need only be 8-byte aligned)
     constexpr int R = W - 1;
     constexpr int Q = TS + R - 1;  // dedup row columns
     constexpr int ES = (int)sizeof(B);
@@ -55,14 +58,16 @@ __global__ void __launch_bounds__(128, (CPT == 4 && TS <= 8) ? 4 : 2) verify_pip
     const bool dense = !p.dedup;
     const bool has_bias = p.bias != nullptr;
 
-    // shared memory: stage 0, stage 1, row image, window image, 2 mbarriers, 2 unit slots
-    const long long xb = pipe_part((long long)TS * BC * ES), sb = pipe_part((long long)R * BC * ES),
-                    wb = pipe_part((long long)W * BC * ES), bb = pipe_part((long long)BC * ES);
-    const long long stage_bytes = xb + sb + wb + bb;
-    unsigned char *const img = smem + 2 * stage_bytes;
-    unsigned char *const stimg = img + (dense ? 0 : pipe_part((long long)Q * BC * ES));
-    uint64_t *const bar = reinterpret_cast<uint64_t *>(stimg + sb);
+    // shared memory: stage 0, stage 1 (x rows + committed windows), image buffers 0 and 1 (dedup
+    // row image + committed-window image), 2 mbarriers, 2 unit slots
+    const long long xb = pipe_part((long long)TS * BC * ES), sb = pipe_part((long long)R * BC * ES);
+    const long long stage_bytes = xb + sb;
+    const long long rb = dense ? 0 : pipe_part((long long)Q * BC * ES);
+    const long long img_bytes = rb + sb;
+    unsigned char *const img0 = smem + 2 * stage_bytes;
+    uint64_t *const bar = reinterpret_cast<uint64_t *>(img0 + 2 * img_bytes);
     volatile int *const info = reinterpret_cast<volatile int *>(bar + 2);
+    if (2 * stage_bytes + 2 * img_bytes + 24 > (long long)dynamic_smem_bytes()) return;  // launch mismatch
 
     const int iters = (int)blockIdx.x < n_units ? (n_units - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
     if (tid == 0) {
@@ -86,17 +91,12 @@ __global__ void __launch_bounds__(128, (CPT == 4 && TS <= 8) ? 4 : 2) verify_pip
         const bool go = slot >= 0 && status == 0;
         info[st] = go ? slot : -1;
         if (go) {
-            const unsigned bytes = (unsigned)((TS + R + W + (has_bias ? 1 : 0)) * nch * ES);
-            mbar_arrive_expect_tx(&bar[st], bytes);
+            mbar_arrive_expect_tx(&bar[st], (unsigned)((TS + R) * nch * ES));
             const B *xs = reinterpret_cast<const B *>(p.x) + (long long)s * p.x_seq + c0;
             for (int t = 0; t < TS; ++t)
                 bulk_load(stg + (long long)t * BC * ES, xs + (long long)t * p.x_tok, (unsigned)(nch * ES), &bar[st]);
             bulk_load(stg + xb, reinterpret_cast<const B *>(p.state) + (long long)slot * p.st_slot + (long long)c0 * R,
                       (unsigned)(nch * R * ES), &bar[st]);
-            bulk_load(stg + xb + sb, reinterpret_cast<const B *>(p.weight) + (long long)c0 * W, (unsigned)(nch * W * ES),
-                      &bar[st]);
-            if (has_bias)
-                bulk_load(stg + xb + sb + wb, reinterpret_cast<const B *>(p.bias) + c0, (unsigned)(nch * ES), &bar[st]);
         } else {
             mbar_arrive(&bar[st]);
         }
@@ -112,31 +112,47 @@ __global__ void __launch_bounds__(128, (CPT == 4 && TS <= 8) ? 4 : 2) verify_pip
     int s = (int)blockIdx.x / nblk, cb = (int)blockIdx.x - s * nblk;
     constexpr int LOG_CPT = CPT == 4 ? 2 : 3;
     const int lanes = p.head_dim >> LOG_CPT;  // threads per L2 group
+    float wt[CPT][W];                         // taps and bias of the current channel block
+    float bs[CPT];
+    int wcb = -1;
     for (int k = 0; k < iters; ++k) {
         const int st = k & 1;
         const unsigned char *stg = smem + st * stage_bytes;
+        unsigned char *const img = img0 + (k & 1) * img_bytes;
+        unsigned char *const stimg = img + rb;
         const int c0 = cb * BC;
         const int nch = min(BC, p.dim - c0);
         const bool act = cl < nch;
         const int c = c0 + cl;
+        if (cb != wcb) {  // once per block when the grid is a multiple of the channel-block count
+            wcb = cb;
+#pragma unroll
+            for (int e = 0; e < CPT; ++e) {
+                bs[e] = 0.0f;
+#pragma unroll
+                for (int j = 0; j < W; ++j) wt[e][j] = 0.0f;
+            }
+            if (act) {
+                uint32_t ww[W * NW];
+                ldv<VW, W * NW>(ww, reinterpret_cast<const B *>(p.weight) + (long long)c * W);
+#pragma unroll
+                for (int e = 0; e < CPT; ++e)
+#pragma unroll
+                    for (int j = 0; j < W; ++j) wt[e][j] = elem_f<B>(ww, e * W + j);
+                if (has_bias) {
+                    uint32_t bw[NW];
+                    ldv<VX, NW>(bw, reinterpret_cast<const B *>(p.bias) + c);
+#pragma unroll
+                    for (int e = 0; e < CPT; ++e) bs[e] = elem_f<B>(bw, e);
+                }
+            }
+        }
 
         const bool ok = mbar_wait_bounded(&bar[st], (unsigned)((k >> 1) & 1), kWaitPolls);
-        if (__syncthreads_or(!ok)) {
-            if (tid == 0) {
-                if (p.err) atomicOr(p.err + s, kSeqTimeout);
-                // drain the copies still in flight into this block's shared memory (bounded)
-                mbar_wait_bounded(&bar[st], (unsigned)((k >> 1) & 1), kWaitPolls);
-                if (k + 1 < iters) mbar_wait_bounded(&bar[st ^ 1], (unsigned)(((k + 1) >> 1) & 1), kWaitPolls);
-                asm volatile("cp.async.bulk.wait_group.read 0;\n" ::: "memory");
-            }
-            return;
-        }
-        const int slot = info[st];
+        const int slot = ok ? info[st] : -1;
         const bool go = slot >= 0;
 
         float fw[CPT][R + TS];  // inputs widened to fp32: [0, R) committed window, then x
-        float wt[CPT][W];
-        float bs[CPT];
         uint32_t xr[TS][NW];    // raw x rows
         uint32_t sw[R * NW];    // raw committed window, channel-major [CPT][R]
         if (go && act) {
@@ -147,18 +163,6 @@ __global__ void __launch_bounds__(128, (CPT == 4 && TS <= 8) ? 4 : 2) verify_pip
             for (int e = 0; e < CPT; ++e)
 #pragma unroll
                 for (int kk = 0; kk < R; ++kk) fw[e][kk] = elem_f<B>(sw, e * R + kk);
-            uint32_t ww[W * NW];
-            ldv<VW, W * NW>(ww, stg + xb + sb + (long long)cl * W * ES);
-#pragma unroll
-            for (int e = 0; e < CPT; ++e)
-#pragma unroll
-                for (int j = 0; j < W; ++j) wt[e][j] = elem_f<B>(ww, e * W + j);
-            uint32_t bw[NW];
-#pragma unroll
-            for (int i = 0; i < NW; ++i) bw[i] = 0u;
-            if (has_bias) ldv<VX, NW>(bw, stg + xb + sb + wb + (long long)cl * ES);
-#pragma unroll
-            for (int e = 0; e < CPT; ++e) bs[e] = elem_f<B>(bw, e);
 
             // word and half holding input j of channel e (j < R: committed window, else x_{j-R})
             auto word_of = [&](int e, int j) -> uint32_t { return j < R ? sw[(e * R + j) / EW] : xr[j - R][e / EW]; };
@@ -193,7 +197,20 @@ __global__ void __launch_bounds__(128, (CPT == 4 && TS <= 8) ? 4 : 2) verify_pip
             stv<VS, R * NW>(stimg + (long long)tid * CPT * R * ES, fin);
         }
         fence_smem_to_async();
-        __syncthreads();  // images complete; stage st fully moved to registers
+        // the image buffer written next unit was last read by this unit's predecessor's bulk copy,
+        // the only group thread 0 can still have in flight
+        if (tid == 0) asm volatile("cp.async.bulk.wait_group.read 0;\n" ::: "memory");
+        // one barrier per unit: images complete, stage st moved to registers, and the vote on
+        // whether any thread's wait timed out
+        if (__syncthreads_or(!ok)) {
+            if (tid == 0) {
+                if (p.err) atomicOr(p.err + s, kSeqTimeout);
+                // drain the copies still in flight into this block's shared memory (bounded)
+                mbar_wait_bounded(&bar[st], (unsigned)((k >> 1) & 1), kWaitPolls);
+                if (k + 1 < iters) mbar_wait_bounded(&bar[st ^ 1], (unsigned)(((k + 1) >> 1) & 1), kWaitPolls);
+            }
+            return;
+        }
         if (tid == 0) {
             if (go) {
                 if (!dense)
@@ -282,9 +299,6 @@ __global__ void __launch_bounds__(128, (CPT == 4 && TS <= 8) ? 4 : 2) verify_pip
                 }
             }
         }
-        // the images are rewritten next iteration: their bulk reads must be done
-        if (tid == 0) asm volatile("cp.async.bulk.wait_group.read 0;\n" ::: "memory");
-        __syncthreads();
         s += g_s;
         cb += g_b;
         if (cb >= nblk) {
@@ -292,6 +306,8 @@ __global__ void __launch_bounds__(128, (CPT == 4 && TS <= 8) ? 4 : 2) verify_pip
             ++s;
         }
     }
+    // keep the block's shared memory alive until the last bulk copies have read it
+    if (tid == 0) asm volatile("cp.async.bulk.wait_group.read 0;\n" ::: "memory");
 }
 
 }  // namespace cvk

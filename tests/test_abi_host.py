@@ -68,15 +68,14 @@ W3 = wl.WORKLOADS["n128_t8_dim10240_w4_bf16_dedup_pad13"]
 def test_plan_for_benchmark_workload(lib):
     """128 x 8 x 10240 bf16 dedup, packed state: the pipelined path.  4 channels per thread (an L2
     group of 128 spans 32 lanes), 128 threads per unit of 512 channels.  Shared memory: two stages
-    of (8 x rows + 3 window columns + 4 taps + bias), each part rounded to 128 bytes, the dedup row
-    image (10 columns), the committed-window image (3 columns) and 24 bytes of barriers and slots;
-    4 blocks fit an SM, so the persistent grid is 152 * 4 = 608 blocks for 128 * 20 units."""
+    of (8 x rows + 3 window columns) and two image buffers of (10 dedup columns + 3 window columns),
+    plus 24 bytes of barriers and slots; 4 blocks fit an SM, and the persistent grid is the largest
+    multiple of the 20 channel blocks within 152 * 4 blocks, so each block keeps its taps."""
     rc, pl = _plan(lib, _args(W3))
     assert rc == 0
-    stage = 8 * 512 * 2 + 3 * 512 * 2 + 4 * 512 * 2 + 512 * 2
-    smem = 2 * stage + 10 * 512 * 2 + 3 * 512 * 2 + 24
+    smem = 2 * (8 + 3) * 512 * 2 + 2 * (10 + 3) * 512 * 2 + 24
     assert (pl.threads, pl.channels_per_block, pl.path, pl.smem_bytes) == (128, 512, 3, smem)
-    assert (pl.grid_x, pl.grid_y) == (152 * 4, 1)
+    assert (pl.grid_x, pl.grid_y) == (600, 1)
 
 
 @pytest.mark.parametrize("name,path", [
