@@ -29,6 +29,7 @@ constexpr int kSmemPerBlockReserved = 1024;
 constexpr int kMinThreads = 32;
 constexpr int kGenericSmemBudget = 96 * 1024;
 constexpr int kCommitThreads = 128;
+constexpr int kCommitRowThreads = 64;  // dedup commit: 512 channels per block
 constexpr int kSmemMax = 227 * 1024;
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -289,21 +290,16 @@ int launch_commit(const cv_commit_args *a, cudaStream_t stream) {
         stride16(a->win_step_stride, esize)) {
         p.mode = 1;
     } else if (packed_state && win_ok && a->window_layout == CV_WINDOW_DEDUP && a->win_ch_stride == Q) {
-        // persistent, pipelined: two stages of one unit's rows (8*threads channels x Q columns)
-        threads = kCommitThreads;
-        while (threads > kMinThreads && 8 * (threads / 2) >= a->dim) threads /= 2;
-        const long long stage = (8LL * threads * Q * esize + 127) / 128 * 128;
-        const long long sm = 2 * stage + 32;
+        // one block of 8*64 channels per sequence, its rows staged by one bulk copy
+        int rt = kCommitRowThreads;
+        while (rt > kMinThreads && 8 * (rt / 2) >= a->dim) rt /= 2;
+        const long long sm = (8LL * rt * Q * esize + 127) / 128 * 128 + 8;
         if (sm <= kSmemMax) {
             p.mode = 2;
-            const long long units = (long long)a->n_seq * ((a->dim + 8LL * threads - 1) / (8LL * threads));
-            long long per_sm = kSmemPerSM / (sm + kSmemPerBlockReserved);
-            if (per_sm > 8) per_sm = 8;
-            long long g = kNumSMs * per_sm;
-            if (g > units) g = units;
-            auto kp = kernel_set(a->dtype, a->width).commit_pipe;
-            if (ensure_smem(reinterpret_cast<const void *>(kp), (int)sm) != cudaSuccess) return CV_ERR_LAUNCH;
-            kp<<<(unsigned)(g > 0 ? g : 1), threads, (int)sm, stream>>>(p);
+            const int bc = 8 * rt;
+            auto kr = kernel_set(a->dtype, a->width).commit_rows;
+            if (ensure_smem(reinterpret_cast<const void *>(kr), (int)sm) != cudaSuccess) return CV_ERR_LAUNCH;
+            kr<<<dim3((a->dim + bc - 1) / bc, a->n_seq), rt, (int)sm, stream>>>(p);
             return cudaGetLastError() == cudaSuccess ? CV_OK : CV_ERR_LAUNCH;
         }
         p.mode = 0;

@@ -10,7 +10,7 @@
 //   mode 1, dense snapshots packed [.., dim, W-1] and state rows packed [dim][W-1]: the snapshot's
 //     channel block is one contiguous run, copied with 16-byte vectors;
 //   mode 0, anything else: element by element.
-// commit_pipe (below) handles packed deduplicated rows with packed state rows.
+// commit_rows (below) handles packed deduplicated rows with packed state rows.
 #pragma once
 
 #include "cv_device.cuh"
@@ -58,103 +58,72 @@ __global__ void __launch_bounds__(128) commit_kernel(const __grid_constant__ Com
     }
 }
 
-// Persistent, bulk-copy-pipelined commit for packed deduplicated rows and packed state rows
-// (mode 2): a unit is one block of 8*threads channels of one sequence; thread 0
-// loads each unit's rows (one contiguous run of channels*(T+W-2) elements) by bulk copy into one
-// of two shared-memory stages, two units ahead, so the row reads of later units overlap the
-// gather and the stores of the current one; the state run [c][k] = row[c][a-1+k] is gathered from
-// the stage and written with 16-byte coalesced stores.
-// Bounded waits as in the pipelined verify: a timeout sets bit 8 in err and the block returns.
+// Commit of packed deduplicated rows into packed state rows (mode 2): one block per (block of
+// 8*threads channels, sequence), a single wave of small blocks.  The row address does not depend
+// on the cache slot, so thread 0 starts the bulk copy (TMA, cp.async.bulk) of the block's rows --
+// one contiguous run of channels*(T+W-2) elements -- before anything else, and the slot and the
+// accept count are read while it is in flight; no dependent load precedes the data.  The state
+// run [c][k] = row[c][a-1+k] is then gathered from shared memory and written with 16-byte
+// coalesced stores.  A padded or rejected sequence still waits for its copy (the shared memory must
+// outlive it) and writes nothing.  The wait is bounded: a timeout sets bit 8 in err.
 template <typename B, int W>
-__global__ void __launch_bounds__(128) commit_pipe(const __grid_constant__ CommitParams p) {
+__global__ void __launch_bounds__(64) commit_rows(const __grid_constant__ CommitParams p) {
     constexpr int R = W - 1;
     constexpr int ES = (int)sizeof(B);
     constexpr int VE = 16 / ES;
     extern __shared__ __align__(128) unsigned char smem[];
     const int tid = threadIdx.x;
+    const int s = blockIdx.y;
     const int BC = 8 * blockDim.x;
+    const int c0 = blockIdx.x * BC;
+    const int nch = min(BC, p.dim - c0);
     const int Q = p.T + R - 1;
-    const int nblk = (p.dim + BC - 1) / BC;
-    const int n_units = p.n_seq * nblk;
-    const long long stage_bytes = ((long long)BC * Q * ES + 127) / 128 * 128;
-    uint64_t *const bar = reinterpret_cast<uint64_t *>(smem + 2 * stage_bytes);
-    volatile int *const info = reinterpret_cast<volatile int *>(bar + 2);  // [slot, accept] per stage
-    if (2 * stage_bytes + 32 > (long long)dynamic_smem_bytes()) return;  // launch mismatch
-    const int iters = (int)blockIdx.x < n_units ? (n_units - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+    const long long row_bytes = ((long long)BC * Q * ES + 127) / 128 * 128;
+    uint64_t *const bar = reinterpret_cast<uint64_t *>(smem + row_bytes);
+    if (row_bytes + 8 > (long long)dynamic_smem_bytes()) return;  // launch mismatch
     if (tid == 0) {
-        mbar_init(&bar[0], 1);
-        mbar_init(&bar[1], 1);
+        mbar_init(bar, 1);
         mbar_init_fence();
+        mbar_arrive_expect_tx(bar, (unsigned)(nch * Q * ES));
+        bulk_load(smem, reinterpret_cast<const B *>(p.win) + (long long)s * p.w_seq + (long long)c0 * Q,
+                  (unsigned)(nch * Q * ES), bar);
     }
-    __syncthreads();
-
-    auto issue = [&](int k) {
-        const int st = k & 1;
-        const int u = (int)blockIdx.x + k * (int)gridDim.x;
-        const int s = u / nblk, c0 = (u - s * nblk) * BC;
-        const int nch = min(BC, p.dim - c0);
-        const int slot = p.cache_idx ? __ldg(p.cache_idx + s) : s;
-        const int a = __ldg(p.accept_len + s);
-        int status = 0;
-        if (slot >= 0) {
-            if (slot >= p.n_slots) status |= 1;
-            if (a < 1 || a > p.T) status |= 4;
-        }
-        if (p.err && c0 == 0) p.err[s] = status;
-        const bool go = slot >= 0 && status == 0;
-        info[2 * st] = go ? slot : -1;
-        info[2 * st + 1] = a;
-        if (go) {
-            mbar_arrive_expect_tx(&bar[st], (unsigned)(nch * Q * ES));
-            bulk_load(smem + st * stage_bytes,
-                      reinterpret_cast<const B *>(p.win) + (long long)s * p.w_seq + (long long)c0 * Q,
-                      (unsigned)(nch * Q * ES), &bar[st]);
-        } else {
-            mbar_arrive(&bar[st]);
-        }
-    };
-    if (tid == 0) {
-        if (iters > 0) issue(0);
-        if (iters > 1) issue(1);
+    const int slot = p.cache_idx ? __ldg(p.cache_idx + s) : s;
+    const int a = __ldg(p.accept_len + s);
+    int status = 0;
+    if (slot >= 0) {
+        if (slot >= p.n_slots) status |= 1;
+        if (a < 1 || a > p.T) status |= 4;
     }
-    for (int k = 0; k < iters; ++k) {
-        const int st = k & 1;
-        const int u = (int)blockIdx.x + k * (int)gridDim.x;
-        const int s = u / nblk, c0 = (u - s * nblk) * BC;
-        const int nch = min(BC, p.dim - c0);
-        const bool ok = mbar_wait_bounded(&bar[st], (unsigned)((k >> 1) & 1), kCommitWaitPolls);
-        if (__syncthreads_or(!ok)) {
-            if (tid == 0) {
-                if (p.err) atomicOr(p.err + s, 8);
-                mbar_wait_bounded(&bar[st], (unsigned)((k >> 1) & 1), kCommitWaitPolls);
-                if (k + 1 < iters) mbar_wait_bounded(&bar[st ^ 1], (unsigned)(((k + 1) >> 1) & 1), kCommitWaitPolls);
-            }
-            return;
+    if (p.err && blockIdx.x == 0 && tid == 0) p.err[s] = status;
+    __syncthreads();  // the barrier's initialisation is visible to every waiting thread
+    const bool ok = mbar_wait_bounded(bar, 0u, kCommitWaitPolls);
+    if (__syncthreads_or(!ok)) {  // every thread agrees before anyone leaves
+        if (tid == 0) {
+            if (p.err) atomicOr(p.err + s, 8);
+            mbar_wait_bounded(bar, 0u, kCommitWaitPolls);  // drain the copy (bounded)
         }
-        const int slot = info[2 * st];
-        const int col0 = info[2 * st + 1] - 1;
-        if (slot >= 0) {
-            const B *sm = reinterpret_cast<const B *>(smem + st * stage_bytes);
-            B *d = reinterpret_cast<B *>(p.state) + (long long)slot * p.st_slot + (long long)c0 * R;
-            const int nd = nch * R / VE;
-            for (int m = tid; m < nd; m += blockDim.x) {
-                uint32_t wv[4];
+        return;
+    }
+    if (slot < 0 || status) return;
+    const B *sm = reinterpret_cast<const B *>(smem);
+    B *d = reinterpret_cast<B *>(p.state) + (long long)slot * p.st_slot + (long long)c0 * R;
+    const int col0 = a - 1;
+    const int nd = nch * R / VE;
+    for (int m = tid; m < nd; m += blockDim.x) {
+        uint32_t wv[4];
 #pragma unroll
-                for (int h = 0; h < 4; ++h) {
-                    uint32_t bits[2] = {0u, 0u};
+        for (int h = 0; h < 4; ++h) {
+            uint32_t bits[2] = {0u, 0u};
 #pragma unroll
-                    for (int z = 0; z < 4 / ES; ++z) {
-                        const int pos = m * VE + h * (4 / ES) + z;
-                        const int cc = pos / R, kk = pos - cc * R;
-                        bits[z] = (uint32_t)sm[cc * Q + col0 + kk];
-                    }
-                    wv[h] = (ES == 2) ? pack_halves(bits[0], bits[1]) : bits[0];
-                }
-                st16(d + m * VE, make_uint4(wv[0], wv[1], wv[2], wv[3]));
+            for (int z = 0; z < 4 / ES; ++z) {
+                const int pos = m * VE + h * (4 / ES) + z;
+                const int cc = pos / R, kk = pos - cc * R;
+                bits[z] = (uint32_t)sm[cc * Q + col0 + kk];
             }
+            wv[h] = (ES == 2) ? pack_halves(bits[0], bits[1]) : bits[0];
         }
-        __syncthreads();  // stage st consumed
-        if (tid == 0 && k + 2 < iters) issue(k + 2);
+        st16(d + m * VE, make_uint4(wv[0], wv[1], wv[2], wv[3]));
     }
 }
 

@@ -22,7 +22,7 @@ KernelSet make_set(std::integer_sequence<int, Ts...>) {
     k.max_static_t = (int)sizeof...(Ts);
     k.generic = verify_generic<B, W>;
     k.commit = commit_kernel<B, W>;
-    k.commit_pipe = commit_pipe<B, W>;
+    k.commit_rows = commit_rows<B, W>;
     return k;
 }
 }  // namespace

@@ -22,7 +22,7 @@ struct KernelSet {
     int max_static_t;
     VerifyKernel generic;
     CommitKernel commit;
-    CommitKernel commit_pipe;
+    CommitKernel commit_rows;
 };
 
 const KernelSet &kernels_bf16_w2();

@@ -77,15 +77,24 @@ __global__ void __launch_bounds__(128, (CPT == 4 && TS <= 8) ? 4 : 2) verify_pip
     }
     __syncthreads();
 
-    // thread 0: start the copies of iteration k into stage k & 1 (or only arrive, for padding)
+    // thread 0: start the copies of iteration k into stage k & 1 (or only arrive, for padding).  The
+    // index data of the next unit (cache slot, state offset) is loaded one issue ahead, so no issue
+    // waits for a global-memory round trip.
+    int pf_slot = 0, pf_off = 0;
+    auto load_index = [&](int k) {
+        if (k >= iters) return;
+        const int s = ((int)blockIdx.x + k * (int)gridDim.x) / nblk;
+        pf_slot = p.cache_idx ? __ldg(p.cache_idx + s) : s;
+        pf_off = p.state_off ? __ldg(p.state_off + s) : 0;
+    };
     auto issue = [&](int k) {
         const int st = k & 1;
         unsigned char *stg = smem + st * stage_bytes;
         const int u = (int)blockIdx.x + k * (int)gridDim.x;
         const int s = u / nblk, c0 = (u - s * nblk) * BC;
         const int nch = min(BC, p.dim - c0);
-        const int slot = p.cache_idx ? __ldg(p.cache_idx + s) : s;
-        const int off = p.state_off ? __ldg(p.state_off + s) : 0;
+        const int slot = pf_slot, off = pf_off;
+        load_index(k + 1);
         const int status = seq_status(slot, off, p.n_slots, p.state_cols, R);
         if (p.err && c0 == 0) p.err[s] = status;
         const bool go = slot >= 0 && status == 0;
@@ -102,6 +111,7 @@ __global__ void __launch_bounds__(128, (CPT == 4 && TS <= 8) ? 4 : 2) verify_pip
         }
     };
     if (tid == 0) {
+        load_index(0);
         if (iters > 0) issue(0);
         if (iters > 1) issue(1);
     }
