@@ -189,7 +189,7 @@ CV_API int cv_conv_commit(const cv_commit_args *args, void *stream);
  * cv_verify_plan -- validate `args` exactly as cv_conv_verify does and report the launch it would
  * make, without touching the GPU.  grid = (grid_x, grid_y), block = threads, dynamic shared
  * memory = smem_bytes; each block owns channels_per_block channels of one sequence.  path says
- * which kernel runs: 1 = packed buffers with T a compile-time constant (T <= 16 for bf16, <= 8
+ * which kernel runs: 1 = packed buffers with T a compile-time constant (T <= 17 for bf16, <= 8
  * for fp32), 2 = packed buffers, dense window, larger T in chunks of 8 tokens, 0 = the general
  * kernel (any strides).  Host pointer `plan` must not be NULL.  Returns the same status
  * cv_conv_verify would return before launching.

@@ -4,7 +4,7 @@
 //
 // Path selection for cv_conv_verify:
 //   fast, static T  (path 1): packed, 16-byte aligned buffers, dim % 8 == 0, T <= the largest
-//                             compiled static T (16 for bf16, 8 for fp32); either window layout.
+//                             compiled static T (17 for bf16, 8 for fp32); either window layout.
 //   fast, chunked   (path 2): the same buffers with a dense window and a larger T.
 //   general         (path 0): everything else (any strides, any dim, dedup rows with a larger T).
 //   pipelined       (path 3): path 1's buffers with packed state rows: persistent blocks walk
@@ -89,6 +89,15 @@ bool fast_eligible(const cv_verify_args *a, int esize, int max_static_t) {
     return a->win_ch_stride == R && stride16(a->win_step_stride, esize);
 }
 
+// Halve a block (down to 32 threads) while the launch would have fewer than two blocks per SM and
+// the smaller block still holds whole L2 groups: small batches then still fill the GPU.
+int shrink_for_parallelism(int threads, int cpt, const cv_verify_args *a) {
+    const int min_bc = a->qk_channels > 0 ? a->head_dim : 8;
+    auto units = [&](int t) { return (long long)a->n_seq * ((a->dim + (long long)cpt * t - 1) / ((long long)cpt * t)); };
+    while (threads > 32 && units(threads) < 2LL * kNumSMs && cpt * (threads / 2) >= min_bc) threads /= 2;
+    return threads;
+}
+
 bool state_packed(const void *state, long long slot_stride, long long ch_stride, int width, int esize) {
     return aligned16(state) && stride16(slot_stride, esize) && ch_stride == width - 1;
 }
@@ -112,6 +121,7 @@ int plan_verify(const cv_verify_args *a, cv_launch_plan *pl) {
         int threads = kPipeThreads;
         while (threads > 32 && cpt * (threads / 2) >= a->dim) threads /= 2;
         while (a->qk_channels > 0 && cpt * threads < a->head_dim) threads *= 2;
+        threads = shrink_for_parallelism(threads, cpt, a);
         const long long bc = (long long)cpt * threads;
         const long long Q = a->T + R - 1;
         // two stages (x rows + committed windows) and two image buffers (dedup row + windows)
@@ -142,6 +152,7 @@ int plan_verify(const cv_verify_args *a, cv_launch_plan *pl) {
         int threads = kFastThreads;
         while (threads > 32 && cpt * (threads / 2) >= a->dim) threads /= 2;
         while (a->qk_channels > 0 && cpt * threads < a->head_dim) threads *= 2;
+        threads = shrink_for_parallelism(threads, cpt, a);
         const long long bc = (long long)cpt * threads;
         long long smem = bc * R * esize;  // committed-window image
         if (a->window_layout == CV_WINDOW_DEDUP) smem += bc * (a->T + R - 1) * esize;

@@ -50,10 +50,25 @@ __global__ void __launch_bounds__(128) commit_kernel(const __grid_constant__ Com
         const int nv = nch * R / VE;
         for (int i = tid; i < nv; i += NT) st16(d + i * VE, ld16(src + i * VE));
     } else {
+        // element by element, in rounds of 8 per thread: all loads of a round before its stores, so
+        // the loads' latencies overlap
+        constexpr int U = 8;
         const B *src = reinterpret_cast<const B *>(p.win) + (long long)s * p.w_seq + (long long)(a - 1) * p.w_step;
-        for (int i = tid; i < nch * R; i += NT) {
-            const int cc = c0 + i / R, k = i % R;
-            dst[(long long)cc * p.st_ch + k] = src[(long long)cc * p.w_ch + (long long)k * p.w_col];
+        const int n = nch * R;
+        for (int i0 = tid; i0 < n; i0 += U * NT) {
+            B v[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int i = i0 + u * NT;
+                const int cc = c0 + i / R, k = i % R;
+                if (i < n) v[u] = src[(long long)cc * p.w_ch + (long long)k * p.w_col];
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int i = i0 + u * NT;
+                const int cc = c0 + i / R, k = i % R;
+                if (i < n) dst[(long long)cc * p.st_ch + k] = v[u];
+            }
         }
     }
 }

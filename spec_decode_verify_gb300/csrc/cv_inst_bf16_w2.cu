@@ -1,6 +1,6 @@
 // Kernel instantiations for bf16 elements, conv width 2.
 #define CV_INST_B uint16_t
 #define CV_INST_W 2
-#define CV_INST_MAXT 16
+#define CV_INST_MAXT 17
 #define CV_INST_NAME kernels_bf16_w2
 #include "cv_inst.cuh"

@@ -1,6 +1,6 @@
 // Kernel instantiations for bf16 elements, conv width 3.
 #define CV_INST_B uint16_t
 #define CV_INST_W 3
-#define CV_INST_MAXT 16
+#define CV_INST_MAXT 17
 #define CV_INST_NAME kernels_bf16_w3
 #include "cv_inst.cuh"

@@ -11,7 +11,7 @@ using CommitKernel = void (*)(CommitParams);
 // Largest T compiled with T as a template parameter (fully unrolled token loop, dedup row built
 // in registers).  Above it the dense layout runs the chunked kernel and the dedup layout the
 // general kernel.
-constexpr int kMaxStaticT = 16;
+constexpr int kMaxStaticT = 17;
 
 struct KernelSet {
     // fast[c][T]: c = 0 for 4 channels per thread, 1 for 8; T in 1..max_static_t compiled with T

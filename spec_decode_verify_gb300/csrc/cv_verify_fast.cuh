@@ -20,7 +20,7 @@
 //      q|k channels the L2 normalisation over the head_dim group as an xor-shuffle over
 //      head_dim/CPT lanes (glm5next_kda mod.rs: conv1d + SiLU -> L2(q,k only), eps inside the
 //      root); one rounding to the output type; vector stores.
-// T is a template parameter for T <= 16 (bf16) / 8 (fp32), which unrolls the token loop and makes
+// T is a template parameter for T <= 17 (bf16) / 8 (fp32), which unrolls the token loop and makes
 // the row permutation static; TS = 0 runs any T with a dense window in unrolled chunks of 4.
 // Preconditions (checked on the host): dim % 8 == 0; x, out, weight, bias, window 16-byte aligned
 // with 16-byte-multiple strides; window packed (dense [.., T, dim, W-1] or dedup [.., dim, T+W-2]

@@ -1,4 +1,4 @@
-// Persistent, bulk-copy-pipelined verify kernel: the main path for packed buffers with T <= 16.
+// Persistent, bulk-copy-pipelined verify kernel: the main path for packed buffers with T <= 17.
 //
 // A unit of work is one block of CPT*threads channels of one sequence (the block of the Atlas
 // batched verify, fn gdn_verify_fused_conv_kn_batched).  A persistent block walks the units
@@ -19,7 +19,7 @@
 // Every mbarrier wait is bounded: a block that waits too long sets CV_SEQ_TIMEOUT in err (when
 // given) for the unit's sequence, drains its copies in flight (again bounded) and returns.
 // Preconditions (checked on the host): those of the fast path, packed 16-byte-aligned state rows
-// ([dim][W-1]), T <= 16 (bf16) / 8 (fp32), head_dim / CPT <= 32.
+// ([dim][W-1]), T <= 17 (bf16) / 8 (fp32), head_dim / CPT <= 32.
 #pragma once
 
 #include <type_traits>
@@ -79,41 +79,58 @@ __global__ void __launch_bounds__(128, (CPT == 4 && TS <= 8) ? 4 : 2) verify_pip
 
     // thread 0: start the copies of iteration k into stage k & 1 (or only arrive, for padding).  The
     // index data of the next unit (cache slot, state offset) is loaded one issue ahead, so no issue
-    // waits for a global-memory round trip.
-    int pf_slot = 0, pf_off = 0;
-    auto load_index = [&](int k) {
+    // waits for a global-memory round trip; the first two units load theirs together at the start
+    // and send their x copies out before the indices arrive (the x rows do not depend on the slot).
+    auto unit_of = [&](int k, int &s, int &c0, int &nch) {
+        const int u = (int)blockIdx.x + k * (int)gridDim.x;
+        s = u / nblk;
+        c0 = (u - s * nblk) * BC;
+        nch = min(BC, p.dim - c0);
+    };
+    auto load_index = [&](int k, int &slot, int &off) {
         if (k >= iters) return;
         const int s = ((int)blockIdx.x + k * (int)gridDim.x) / nblk;
-        pf_slot = p.cache_idx ? __ldg(p.cache_idx + s) : s;
-        pf_off = p.state_off ? __ldg(p.state_off + s) : 0;
+        slot = p.cache_idx ? __ldg(p.cache_idx + s) : s;
+        off = p.state_off ? __ldg(p.state_off + s) : 0;
     };
-    auto issue = [&](int k) {
+    auto issue_x = [&](int k) {
         const int st = k & 1;
-        unsigned char *stg = smem + st * stage_bytes;
-        const int u = (int)blockIdx.x + k * (int)gridDim.x;
-        const int s = u / nblk, c0 = (u - s * nblk) * BC;
-        const int nch = min(BC, p.dim - c0);
-        const int slot = pf_slot, off = pf_off;
-        load_index(k + 1);
+        int s, c0, nch;
+        unit_of(k, s, c0, nch);
+        mbar_expect_tx(&bar[st], (unsigned)(TS * nch * ES));
+        const B *xs = reinterpret_cast<const B *>(p.x) + (long long)s * p.x_seq + c0;
+        for (int t = 0; t < TS; ++t)
+            bulk_load(smem + st * stage_bytes + (long long)t * BC * ES, xs + (long long)t * p.x_tok,
+                      (unsigned)(nch * ES), &bar[st]);
+    };
+    // the phase cannot complete before the single arrival at its end, so a late expect_tx is safe
+    auto issue = [&](int k, int slot, int off, bool x_sent) {
+        const int st = k & 1;
+        int s, c0, nch;
+        unit_of(k, s, c0, nch);
         const int status = seq_status(slot, off, p.n_slots, p.state_cols, R);
         if (p.err && c0 == 0) p.err[s] = status;
         const bool go = slot >= 0 && status == 0;
         info[st] = go ? slot : -1;
         if (go) {
-            mbar_arrive_expect_tx(&bar[st], (unsigned)((TS + R) * nch * ES));
-            const B *xs = reinterpret_cast<const B *>(p.x) + (long long)s * p.x_seq + c0;
-            for (int t = 0; t < TS; ++t)
-                bulk_load(stg + (long long)t * BC * ES, xs + (long long)t * p.x_tok, (unsigned)(nch * ES), &bar[st]);
-            bulk_load(stg + xb, reinterpret_cast<const B *>(p.state) + (long long)slot * p.st_slot + (long long)c0 * R,
+            if (!x_sent) issue_x(k);
+            mbar_expect_tx(&bar[st], (unsigned)(R * nch * ES));
+            bulk_load(smem + st * stage_bytes + xb,
+                      reinterpret_cast<const B *>(p.state) + (long long)slot * p.st_slot + (long long)c0 * R,
                       (unsigned)(nch * R * ES), &bar[st]);
-        } else {
-            mbar_arrive(&bar[st]);
         }
+        mbar_arrive(&bar[st]);
     };
+    int pf_slot = 0, pf_off = 0;
     if (tid == 0) {
-        load_index(0);
-        if (iters > 0) issue(0);
-        if (iters > 1) issue(1);
+        int slot0 = 0, off0 = 0, slot1 = 0, off1 = 0;
+        load_index(0, slot0, off0);
+        load_index(1, slot1, off1);
+        if (iters > 0) issue_x(0);
+        if (iters > 1) issue_x(1);
+        if (iters > 0) issue(0, slot0, off0, true);
+        if (iters > 1) issue(1, slot1, off1, true);
+        load_index(2, pf_slot, pf_off);
     }
 
     const int cl = tid * CPT;
@@ -230,7 +247,10 @@ __global__ void __launch_bounds__(128, (CPT == 4 && TS <= 8) ? 4 : 2) verify_pip
                            (unsigned)(nch * R * ES));
                 asm volatile("cp.async.bulk.commit_group;\n" ::: "memory");
             }
-            if (k + 2 < iters) issue(k + 2);
+            if (k + 2 < iters) {
+                issue(k + 2, pf_slot, pf_off, false);
+                load_index(k + 3, pf_slot, pf_off);
+            }
         }
         if (go) {
             const bool l2_block = c0 < p.qk_channels;
