@@ -34,7 +34,7 @@ class _VerifyArgs(ctypes.Structure):
         ("state", c_vp), ("n_slots", c_i32), ("state_cols", c_i32), ("st_slot", c_i64), ("st_ch", c_i64),
         ("cache_idx", c_vp), ("state_off", c_vp), ("weight", c_vp), ("bias", c_vp),
         ("window", c_vp), ("dedup", c_i32), ("w_seq", c_i64), ("w_step", c_i64), ("w_ch", c_i64),
-        ("w_col", c_i64), ("status", c_vp),
+        ("w_col", c_i64), ("status", c_vp), ("history", c_i32),
     ]
 
 
@@ -110,7 +110,9 @@ def window_strides(window: torch.Tensor, layout: str):
     """(seq, step, ch, col) element strides of a window buffer.
 
     dense: window is [n_seq, T, dim, W-1].  dedup: window is the [n_seq, dim, T+W-2] row buffer and
-    the step stride equals the column stride."""
+    the step stride equals the column stride.  history: there is no window buffer."""
+    if layout == "history":
+        return 0, 0, 0, 0
     if layout == "dense":
         s = window.stride()
         return s[0], s[1], s[2], s[3]
@@ -124,8 +126,13 @@ def conv_verify(x, conv_state, weight, bias, out, window, *, layout, qk_channels
 
     x [n_seq, T, dim] (channel stride 1), conv_state [n_slots, dim, S] (column stride 1),
     weight [dim, W] contiguous, bias [dim] or None, out [n_seq, T, dim] (channel stride 1),
-    window dense [n_seq, T, dim, W-1] / dedup [n_seq, dim, T+W-2]; cache_idx, state_off, status
+    window dense [n_seq, T, dim, W-1] / dedup [n_seq, dim, T+W-2] / None for the history layout
+    (the state row, S >= T+W-2 columns, receives the snapshot row); cache_idx, state_off, status
     int32 [n_seq] or None."""
+    if layout not in ("dense", "dedup", "history"):
+        raise ValueError(f"unknown layout {layout!r}")
+    if (layout == "history") != (window is None):
+        raise ValueError("the history layout takes no window buffer; the other layouts need one")
     n_seq, T, dim = x.shape
     W = weight.shape[1]
     assert x.stride(2) == 1 and out.stride(2) == 1 and conv_state.stride(2) == 1
@@ -138,7 +145,7 @@ def conv_verify(x, conv_state, weight, bias, out, window, *, layout, qk_channels
         state_cols=conv_state.shape[2], st_slot=conv_state.stride(0), st_ch=conv_state.stride(1),
         cache_idx=_ptr(cache_idx), state_off=_ptr(state_off), weight=_ptr(weight), bias=_ptr(bias),
         window=_ptr(window), dedup=1 if layout == "dedup" else 0, w_seq=ws[0], w_step=ws[1], w_ch=ws[2],
-        w_col=ws[3], status=_ptr(status))
+        w_col=ws[3], status=_ptr(status), history=1 if layout == "history" else 0)
     rc = _load().oracle_conv_verify(ctypes.byref(a))
     if rc != 0:
         raise RuntimeError(f"oracle_conv_verify returned {rc}")

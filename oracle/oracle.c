@@ -42,6 +42,14 @@
  *     any store").
  *   - An optional per-sequence offset o into the state row says where the committed window is
  *     read (PR #46184 test coverage: "a num_accept_tokens state offset").
+ *   - History-row state (a reading, not a printed kernel): PR #46184's slots hold one [dim, T+K-2]
+ *     window row, and its tests cover "a num_accept_tokens state offset" into the state.  In the
+ *     history layout the state row itself is that row: the call reads its committed window at
+ *     columns [o, o+W-1) and then writes columns [0, T+W-2) of the same row with the row
+ *     [full[1 .. W-2], x_0 .. x_{T-1}], through the same per-token view (element (t, k) at column
+ *     t+k) the dedup layout uses.  Snapshot a-1 then sits at columns [a-1, a+W-2), so the next
+ *     call passes o = a-1 and no commit is needed.  No separate window buffer is written; columns
+ *     at and above T+W-2 are not touched.
  *   - Commit: restore the state to the snapshot of the accepted prefix (PR #46184: the window
  *     "lets the conv state of the accepted prefix be restored after verify"; mod.rs decode_k:
  *     snapshot t is what a partial accept rewinds to).  With a accepted tokens (1 <= a <= T) the
@@ -74,6 +82,7 @@ typedef struct {
     int32_t dedup;
     int64_t w_seq, w_step, w_ch, w_col;
     int32_t *status; /* [n_seq] or NULL */
+    int32_t history; /* 1: the state row is the snapshot row (no window buffer) */
 } oracle_verify_args;
 
 typedef struct {
@@ -132,6 +141,7 @@ int oracle_conv_verify(const oracle_verify_args *a) {
     const int W = a->width, T = a->T, dim = a->dim, bf = a->is_bf16;
     uint32_t full[1024]; /* W-1 + T raw elements of one channel */
     if (W < 1 || T < 1 || dim < 1 || W - 1 + T > 1024) return -1;
+    if (a->history && T + W - 2 > a->state_cols) return -3;
     /* y[t*dim + c]: post-SiLU fp32 values of one sequence, normalised in place below */
     float *y = (float *)malloc(sizeof(float) * (size_t)T * (size_t)dim);
     if (!y) return -2;
@@ -159,6 +169,13 @@ int oracle_conv_verify(const oracle_verify_args *a) {
                     acc = acc + prod;
                 }
                 y[(int64_t)t * dim + c] = acc / (1.0f + expf(-acc));
+            }
+
+            if (a->history) {
+                /* snapshot t into the state row itself, at columns t .. t+W-2 (after every read) */
+                for (int t = 0; t < T; ++t)
+                    for (int k = 0; k < W - 1; ++k) put_bits(a->state, bf, srow + t + k, full[t + 1 + k]);
+                continue;
             }
 
             /* snapshot t = window after token t = full[t+1 .. t+W-1] */

@@ -24,7 +24,7 @@ MUTANTS = [
      lambda: pins.test_p1_matches_float64_conv1d("f32", "dense", 3)),
     ("eps_as_norm_floor", "1.0f / sqrtf(ss + a->l2_eps)", "1.0f / fmaxf(sqrtf(ss), a->l2_eps)",
      lambda: pins.test_p3_one_hot_taps_and_constant_group()),
-    ("snapshot_off_by_one", "full[t + 1 + k])", "full[t + k])",
+    ("snapshot_off_by_one", "win_index(a, s, t, c, k), full[t + 1 + k])", "win_index(a, s, t, c, k), full[t + k])",
      lambda: pins.test_p4_sequential_equals_batched_in_T("dense", "f32")),
     ("state_write_lags", "put_bits(a->state, bf, srow + k, full[T + k])", "put_bits(a->state, bf, srow + k, full[T - 1 + k])",
      lambda: pins.test_p11_single_token_update()),
@@ -38,6 +38,11 @@ MUTANTS = [
      lambda: pins.test_bf16_rounding_matches_torch()),
     ("dedup_step_uses_ch", "int64_t step = a->dedup ? a->w_col : a->w_step;", "int64_t step = a->dedup ? 0 : a->w_step;",
      lambda: pins.test_p6_dedup_view_equals_dense(4)),
+    ("history_row_shifted", "srow + t + k, full[t + 1 + k])", "srow + t + k, full[t + k])",
+     lambda: pins.test_h1_history_row_equals_dedup_row(3)),
+    ("history_row_last_window_only", "for (int t = 0; t < T; ++t)\n                    for (int k = 0; k < W - 1; ++k) put_bits(a->state",
+     "for (int t = T - 1; t < T; ++t)\n                    for (int k = 0; k < W - 1; ++k) put_bits(a->state",
+     lambda: pins.test_h2_history_chain_equals_verify_commit_chain()),
     ("padded_row_written", "if (slot < 0 || st) continue;\n\n", "if (st) continue;\n        if (slot < 0) { if (a->out) put_bits(a->out, bf, (int64_t)s * a->out_seq, 0); continue; }\n\n",
      lambda: pins.test_p7_padded_rows_untouched()),
 ]

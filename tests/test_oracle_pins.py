@@ -287,6 +287,112 @@ def test_p10_state_offset_equals_preshifted_state():
         assert_bits_equal(r["conv_state"][slot, :, w.width - 1:], inp["conv_state"][slot, :, w.width - 1:], "tail")
 
 
+def _history_and_dedup(width, seed=11):
+    wh = small(n_seq=5, T=6, width=width, dtype="bf16", layout="history", state_offset=True, n_pad=1,
+               extra_slots=2, seed=seed)
+    inp = wl.make_inputs(wh)
+    assert inp["window"] is None and inp["conv_state"].shape[2] == wh.T + width - 2
+    return wh, inp
+
+
+@pytest.mark.parametrize("width", [2, 3, 4])
+def test_h1_history_row_equals_dedup_row(width):
+    """History layout (the state row is the deduplicated row of sglang PR #46184, "Motivation"):
+    for the same inputs and offsets, each active slot's state row receives bitwise the row the
+    dedup layout writes to its window buffer, the outputs are bitwise equal, and columns at and
+    above T+W-2, unused slots and padded sequences' slots are untouched."""
+    wh, inp = _history_and_dedup(width)
+    Q = wh.T + width - 2
+    wide = torch.cat([inp["conv_state"], wl.sentinel_tensor((wh.n_slots, wh.dim, 2), wh.torch_dtype)], dim=2)
+    ih = clone_inputs(inp)
+    ih["conv_state"] = wide.clone()
+    rh = run_oracle_verify(wh, ih)
+    wd = wh.replace(layout="dedup")
+    assert wd.state_cols == Q
+    idd = clone_inputs(inp)
+    idd["window"] = wl.sentinel_tensor(wl.window_shape(wd), wd.torch_dtype)
+    rd = run_oracle_verify(wd, idd)
+    assert (rh["status"] == 0).all()
+    assert_bits_equal(rh["out"], rd["out"], "out")
+    active = set()
+    for s in range(wh.n_seq):
+        slot = int(inp["cache_idx"][s])
+        if slot < 0:
+            continue
+        active.add(slot)
+        assert_bits_equal(rh["conv_state"][slot, :, :Q], rd["window"][s], f"seq {s} history row")
+    assert_bits_equal(rh["conv_state"][:, :, Q:], wide[:, :, Q:], "columns beyond the row")
+    for slot in range(wh.n_slots):
+        if slot not in active:
+            assert_bits_equal(rh["conv_state"][slot], wide[slot], f"untouched slot {slot}")
+
+
+def test_h2_history_chain_equals_verify_commit_chain():
+    """Two steps with the history layout (verify at offsets o, then verify at accept_len - 1, no
+    commit) against the plain layout (verify on the committed windows, commit, verify, commit):
+    the outputs of both steps agree bitwise, and after step 2 the history row read at a2 - 1 is the
+    state the plain chain commits (PR #46184: the window restores the accepted prefix's state)."""
+    wh, inp1 = _history_and_dedup(4, seed=21)
+    R = wh.width - 1
+    x2 = wl.make_inputs(wh, seed=22)
+    cidx = inp1["cache_idx"]
+    o1, a1, a2 = inp1["state_off"], inp1["accept_len"], x2["accept_len"]
+    # history chain
+    h1 = run_oracle_verify(wh, inp1)
+    i2 = clone_inputs(inp1)
+    i2.update(x=x2["x"], x_base=x2["x_base"], conv_state=h1["conv_state"].clone(), state_off=(a1 - 1).to(torch.int32),
+              out=wl.sentinel_tensor((wh.n_seq, wh.T, wh.dim), wh.torch_dtype))
+    h2 = run_oracle_verify(wh, i2)
+    # plain chain on the committed windows (state pre-shifted to offset 0, pinned by P-10)
+    wp = wh.replace(layout="dedup", state_offset=False)
+    st0 = wl.sentinel_tensor((wp.n_slots, wp.dim, R), wp.torch_dtype)
+    for s in range(wh.n_seq):
+        slot = int(cidx[s])
+        if slot >= 0:
+            st0[slot] = inp1["conv_state"][slot, :, int(o1[s]):int(o1[s]) + R]
+    p1in = clone_inputs(inp1)
+    p1in.update(conv_state=st0, state_off=None, window=wl.sentinel_tensor(wl.window_shape(wp), wp.torch_dtype))
+    p1 = run_oracle_verify(wp, p1in)
+    assert (run_oracle_commit(wp, p1, accept_len=a1) == 0).all()
+    p2in = clone_inputs(p1)
+    p2in.update(x=x2["x"], x_base=x2["x_base"], out=wl.sentinel_tensor((wh.n_seq, wh.T, wh.dim), wh.torch_dtype),
+                window=wl.sentinel_tensor(wl.window_shape(wp), wp.torch_dtype))
+    p2 = run_oracle_verify(wp, p2in)
+    assert (run_oracle_commit(wp, p2, accept_len=a2) == 0).all()
+    assert_bits_equal(h1["out"], p1["out"], "step 1 out")
+    assert_bits_equal(h2["out"], p2["out"], "step 2 out")
+    for s in range(wh.n_seq):
+        slot = int(cidx[s])
+        if slot < 0:
+            continue
+        a = int(a2[s])
+        assert_bits_equal(h2["conv_state"][slot, :, a - 1:a - 1 + R], p2["conv_state"][slot], f"seq {s} committed")
+
+
+def test_h3_history_sequential_single_tokens():
+    """P-4 in the history layout: T calls of one token each, every call reading the committed
+    window at column 0 of the row the previous call wrote (the whole token accepted), give the
+    outputs of one call over the T tokens bitwise, and the last call's row starts with the window
+    the T-token call leaves at column T-1."""
+    T = 7
+    wh = small(n_seq=3, T=T, width=4, dtype="f32", layout="history", state_offset=False)
+    inp = wl.make_inputs(wh)
+    R = wh.width - 1
+    whole = run_oracle_verify(wh, inp)
+    w1 = wh.replace(T=1)
+    st = wl.sentinel_tensor((wh.n_slots, wh.dim, R), wh.torch_dtype)
+    st[:] = inp["conv_state"][:, :, :R]
+    for t in range(T):
+        one = clone_inputs(inp)
+        one.update(x=inp["x"][:, t:t + 1], conv_state=st, out=wl.sentinel_tensor((wh.n_seq, 1, wh.dim), wh.torch_dtype))
+        r = run_oracle_verify(w1, one)
+        st = r["conv_state"]
+        assert_bits_equal(r["out"][:, 0], whole["out"][:, t], f"token {t}")
+    for s in range(wh.n_seq):
+        slot = int(inp["cache_idx"][s])
+        assert_bits_equal(st[slot], whole["conv_state"][slot, :, T - 1:T - 1 + R], f"seq {s} final window")
+
+
 def test_p11_single_token_update():
     """P-11: T = 1 is the standard single-token causal conv update: the state shifts left by one
     and takes x; out = SiLU(sum_j w_j [state, x]_j + bias)."""
