@@ -3,7 +3,8 @@
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
 
 A step is one pass of the whole path over one batch: cv_conv_verify (conv + SiLU + L2, snapshots,
-committed window) followed by cv_conv_commit (restore the accepted prefix).  Default workload: 128
+committed window) followed by cv_conv_commit (restore the accepted prefix); with the history-row
+state layout the step is the verify alone (the next verify reads at accept_len - 1).  Default workload: 128
 sequences x 8 draft tokens, dim 10240 (q|k 4096, head_dim 128), conv width 4, bf16, deduplicated
 window rows, 13 padded sequences.  Inputs are synthetic and already resident in HBM when the
 timed region starts; every step uses the next of several rotating buffer sets whose total size is
@@ -37,7 +38,7 @@ from spec_decode_verify_gb300 import workloads as wl  # noqa: E402
 METRIC = "verify-conv µs/step and achieved HBM GB/s (% of GB300 peak), 1 GPU"
 UNIT = "us/step"
 HBM_NOMINAL_GBS = 8000.0  # the metric's roofline: bytes moved / 8 TB/s
-PROFILE = os.path.join(ROOT, "profiles", "verify_pipe_n128_t8_dim10240_bf16_dedup.md")
+PROFILES = os.path.join(ROOT, "profiles")
 # the sources of the verify kernel the benchmark workload runs (the pipelined path)
 KERNEL_SRCS = [os.path.join(ROOT, "spec_decode_verify_gb300", "csrc", f)
                for f in ("cv_verify_pipe.cuh", "cv_device.cuh")]
@@ -61,18 +62,23 @@ def measured_peak():
         return 6800.0, "fallback"
 
 
-def profile_traffic():
-    """DRAM bytes per verify launch from the committed ncu summary, if it matches this kernel."""
-    try:
-        text = open(PROFILE).read()
-    except OSError:
-        return None, None
-    m = re.search(r"bench-traffic: dram_bytes_per_launch=(\d+) kernel_sha=([0-9a-f]+)", text)
-    if not m:
-        return None, None
-    if m.group(2) != kernel_sha():
-        return None, "stale"
-    return int(m.group(1)), "ncu"
+def profile_traffic(workload: str):
+    """DRAM bytes per verify launch from a committed ncu summary of this workload, if it was taken
+    of the current kernel sources (a `bench-traffic:` line in profiles/*.md)."""
+    stale = False
+    for name in sorted(os.listdir(PROFILES)) if os.path.isdir(PROFILES) else []:
+        if not name.endswith(".md"):
+            continue
+        text = open(os.path.join(PROFILES, name)).read()
+        for m in re.finditer(r"bench-traffic: workload=(\S+) dram_bytes_per_launch=(\d+) kernel_sha=([0-9a-f]+)",
+                             text):
+            if m.group(1) != workload:
+                continue
+            if m.group(3) != kernel_sha():
+                stale = True
+                continue
+            return int(m.group(2)), f"ncu ({name})"
+    return None, ("stale" if stale else None)
 
 
 class ClockSampler:
@@ -169,13 +175,14 @@ def oracle_step_times(w, reps_max: int, budget_s: float):
     for _ in range(reps_max):
         state = inp["conv_state"].clone()
         out = inp["out"].clone()
-        win = inp["window"].clone()
+        win = inp["window"].clone() if inp["window"] is not None else None
         t0 = time.perf_counter()
         oracle.conv_verify(inp["x"], state, inp["weight"], inp["bias"], out, win, layout=w.layout,
                            qk_channels=w.qk_channels, head_dim=w.head_dim, l2_eps=w.l2_eps,
                            cache_idx=inp["cache_idx"], state_off=inp["state_off"])
-        oracle.conv_commit(state, win, inp["accept_len"], layout=w.layout, T=w.T, width=w.width,
-                           cache_idx=inp["cache_idx"])
+        if w.layout != "history":
+            oracle.conv_commit(state, win, inp["accept_len"], layout=w.layout, T=w.T, width=w.width,
+                               cache_idx=inp["cache_idx"])
         times.append(time.perf_counter() - t0)
         if time.perf_counter() - t_begin > budget_s and len(times) >= 3:
             break
@@ -208,7 +215,7 @@ def run_reference(args, w, world, rank):
 def workload_config(w, l2_note):
     c = {"workload": w.name, "n_seq": w.n_seq, "padded_seqs": w.n_pad, "T": w.T, "dim": w.dim, "width": w.width,
          "qk_channels": w.qk_channels, "head_dim": w.head_dim, "layout": w.layout, "bias": w.bias,
-         "step": "cv_conv_verify + cv_conv_commit"}
+         "step": "cv_conv_verify" if w.layout == "history" else "cv_conv_verify + cv_conv_commit"}
     if l2_note:
         c["l2"] = l2_note
     return c
@@ -231,7 +238,8 @@ def run_ours(args, w, world, rank, local, dist):
     props = torch.cuda.get_device_properties(dev)
     l2 = getattr(props, "L2_cache_size", 0) or 129 * 2 ** 20
     per_set = sum(inp[k].numel() * inp[k].element_size()
-                  for k in ("x_base", "conv_state", "out", "window"))
+                  for k in ("x_base", "conv_state", "out", "window") if inp[k] is not None)
+    has_commit = w.layout != "history"
     n_sets = max(2, math.ceil(4 * l2 / per_set))
     l2_note = f"rotating {n_sets} buffer sets, {n_sets * per_set / 2**20:.0f} MiB >= 4x L2 ({l2 / 2**20:.0f} MiB)"
 
@@ -244,16 +252,20 @@ def run_ours(args, w, world, rank, local, dist):
         xb = inp["x_base"].to(dev)
         x = xb.as_strided(inp["x"].shape, inp["x"].stride(), inp["x"].storage_offset())
         s = dict(x_base=xb, x=x, conv_state=inp["conv_state"].to(dev), out=inp["out"].to(dev),
-                 window=inp["window"].to(dev), accept=inp["accept_len"].to(dev))
+                 window=inp["window"].to(dev) if has_commit else None, accept=inp["accept_len"].to(dev))
         s["va"] = cv.make_verify_args(x, s["conv_state"], weight, bias, s["out"], s["window"], layout=w.layout,
                                       qk_channels=w.qk_channels, head_dim=w.head_dim, l2_eps=w.l2_eps,
                                       cache_idx=cache_idx, state_off=state_off)
-        s["ca"] = cv.make_commit_args(s["conv_state"], s["window"], s["accept"], layout=w.layout, T=w.T,
-                                      width=w.width, cache_idx=cache_idx)
+        if has_commit:
+            s["ca"] = cv.make_commit_args(s["conv_state"], s["window"], s["accept"], layout=w.layout, T=w.T,
+                                          width=w.width, cache_idx=cache_idx)
         sets.append(s)
-    verify_fn, commit_fn = lib.cv_conv_verify, lib.cv_conv_commit
+    verify_fn, lib_commit = lib.cv_conv_verify, lib.cv_conv_commit
     vrefs = [ctypes.byref(s["va"]) for s in sets]
-    crefs = [ctypes.byref(s["ca"]) for s in sets]
+    crefs = [ctypes.byref(s["ca"]) if has_commit else None for s in sets]
+
+    def commit_fn(ref, stream_ptr):
+        return lib_commit(ref, stream_ptr) if has_commit else 0
 
     def step(i):
         rc = verify_fn(vrefs[i % n_sets], sp)
@@ -278,27 +290,37 @@ def run_ours(args, w, world, rank, local, dist):
     torch.cuda.synchronize(dev)
 
     K = args.steps
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    # (1) the step time: K steps back to back between two events, nothing else on the stream
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(dist, dev)
     torch.cuda.synchronize(dev)
     # keep the GPU busy while the host queues the K steps, so no launch waits on the host
-    torch.cuda._sleep(int(min(2e9, 60000 * K + 2e6)))
+    torch.cuda._sleep(int(min(2e9, 40000 * K + 2e6)))
     start.record(stream)
     for i in range(K):
-        ev[i][0].record(stream)
-        verify_fn(vrefs[i % n_sets], sp)
-        ev[i][1].record(stream)
-        commit_fn(crefs[i % n_sets], sp)
-        ev[i][2].record(stream)
+        step(i)
     end.record(stream)
     torch.cuda.synchronize(dev)
+    barrier(dist, dev)
+    # (2) the split into verify and commit: K launches of each kernel alone, back to back, between
+    # two events on the launching stream (an event between every two launches would add its own gap)
+    def time_alone(fn, refs):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(dev)
+        torch.cuda._sleep(int(min(2e9, 30000 * K + 2e6)))
+        e0.record(stream)
+        for i in range(K):
+            fn(refs[i % n_sets], sp)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        return e0.elapsed_time(e1) * 1e3 / K
+
+    verify_us = time_alone(verify_fn, vrefs)
+    commit_us = time_alone(commit_fn, crefs) if has_commit else 0.0
     barrier(dist, dev)
     clocks = sampler.stop()
 
     step_us = start.elapsed_time(end) * 1e3 / K
-    verify_us = statistics.mean(ev[i][0].elapsed_time(ev[i][1]) for i in range(K)) * 1e3
-    commit_us = statistics.mean(ev[i][1].elapsed_time(ev[i][2]) for i in range(K)) * 1e3
     step_us_max = reduce_max(dist, step_us, dev)
     verify_us_max = reduce_max(dist, verify_us, dev)
 
@@ -337,7 +359,7 @@ def run_ours(args, w, world, rank, local, dist):
     nbytes = wl.algorithmic_bytes(w)
     peak, peak_kind = measured_peak()
     achieved = nbytes["verify"] / (verify_us_max * 1e-6) / 1e9
-    traffic, traffic_src = profile_traffic()
+    traffic, traffic_src = profile_traffic(w.name)
     line = {
         "metric": METRIC, "value": round(step_us_max, 3), "unit": UNIT, "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": round(step_us_max / 1e3, 6), "higher_is_better": False,
@@ -350,7 +372,7 @@ def run_ours(args, w, world, rank, local, dist):
                      "frac": round(achieved / peak, 4), "traffic": traffic,
                      "kernel": "verify_pipe", "peak_source": f"{peak_kind} hbm_gbs (copy)",
                      "traffic_source": traffic_src},
-        "gpu_launches": 2 * K,
+        "gpu_launches": (2 if has_commit else 1) * K,
         "clocks": clocks,
         "e2e": e2e,
     }

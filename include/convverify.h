@@ -63,7 +63,16 @@ typedef enum cv_window_layout {
        + (t+k)*win_col_stride + c*win_ch_stride, i.e. one [dim, T+W-2] row per sequence whose
        column q holds input q+1 of [committed window, x_0 .. x_{T-1}].  win_step_stride must
        equal win_col_stride. */
-    CV_WINDOW_DEDUP = 2
+    CV_WINDOW_DEDUP = 2,
+    /* history-row state: no window buffer (window may be NULL; the win_* strides are ignored).
+       The state row is the deduplicated row itself: the call reads the committed window at
+       columns [o, o+W-1) of conv_state[slot][c] and then writes columns [0, T+W-2) of that row
+       with [full[1 .. W-2], x_0 .. x_{T-1}], so snapshot t sits at columns [t, t+W-1).  The next
+       call passes state_off[s] = accept_len[s] - 1 and no commit runs (a reading of the
+       [sglang-46184] slot row together with its accepted-token state offset).  Needs
+       state_cols >= T+W-2; columns at and above T+W-2 are not touched.  cv_conv_commit rejects
+       this layout. */
+    CV_WINDOW_HISTORY = 3
 } cv_window_layout;
 
 /* Status codes returned by the entry points. */
@@ -71,13 +80,15 @@ enum {
     CV_OK = 0,
     CV_ERR_NULL_ARGS = -1,    /* args pointer is NULL */
     CV_ERR_NULL_POINTER = -2, /* a required buffer pointer is NULL */
-    CV_ERR_SHAPE = -3,        /* n_seq outside 0..65535, dim < 1, n_slots < 1, state_cols < W-1 */
+    CV_ERR_SHAPE = -3,        /* n_seq outside 0..65535, dim < 1, n_slots < 1, state_cols < W-1,
+                                 or state_cols < T+W-2 in the history layout */
     CV_ERR_TOKENS = -4,       /* T outside 1..CV_MAX_T */
     CV_ERR_WIDTH = -5,        /* conv width outside 2..4 */
     CV_ERR_DTYPE = -6,        /* dtype not a cv_dtype */
     CV_ERR_HEAD_DIM = -7,     /* qk_channels > 0 and head_dim not a power of two in 8..256, or
                                  qk_channels not a multiple of head_dim, or qk_channels > dim */
-    CV_ERR_LAYOUT = -8,       /* unknown layout, or DEDUP with win_step_stride != win_col_stride */
+    CV_ERR_LAYOUT = -8,       /* unknown layout, DEDUP with win_step_stride != win_col_stride, or
+                                 HISTORY passed to cv_conv_commit */
     CV_ERR_STRIDE = -9,       /* a negative stride, or state rows that overlap (state_ch_stride <
                                  state_cols with dim > 1) */
     CV_ERR_ALIAS = -10,       /* out or window has the same base address as x, conv_state or weight,
@@ -98,14 +109,20 @@ enum {
  * c, let o = state_off ? state_off[s] : 0 and
  *     full = [conv_state[slot][c][o .. o+W-2], x[s][0][c], ..., x[s][T-1][c]]     (W-1+T values)
  * Then for every token t:
- *     acc   = bias[c] (or 0) + sum_{j=0}^{W-1} weight[c][j] * full[t+j]   fp32, taps in order, each
- *                                                                         product rounded, no FMA
+ *     acc   = bias[c] (or 0) + sum_{j=0}^{W-1} weight[c][j] * full[t+j]   fp32, bias first, then the
+ *                                                                         taps in order as fused
+ *                                                                         multiply-adds
  *     y     = acc / (1 + exp(-acc))                                      SiLU [kda-mod]
  *     for c < qk_channels: y *= 1/sqrt(sum over c's head_dim group of y^2 + l2_eps)   [kda-mod]
  *     out[s][t][c] = y rounded once to dtype
+ *                    (the outputs match the plain definition -- each product rounded, exact
+ *                    exp, sqrt and division -- to within 1e-5 relative (+1e-7) in fp32 and 2 ulp
+ *                    in bf16; they are identical for every launch path and batch split)
  *     snapshot (s, t, c, k) = full[t+1+k], k < W-1      raw bit copy, dense or dedup layout
  * and finally conv_state[slot][c][0 .. W-2] = full[T .. T+W-2] (the committed window, equal to
- * snapshot T-1); state columns >= W-1 are not touched.  A sequence with slot < 0 is padding: its
+ * snapshot T-1); state columns >= W-1 are not touched.  In the CV_WINDOW_HISTORY layout the
+ * snapshots go into the state row instead (columns [0, T+W-2), see the layout) and no window
+ * buffer is written.  A sequence with slot < 0 is padding: its
  * out rows, window rows and every state slot are left untouched ([sglang-46184]).
  *
  * Arguments (all in cv_verify_args):
@@ -125,7 +142,8 @@ enum {
  *                      read, the num_accept_tokens offset of [sglang-46184]
  *   weight             [dim][W] contiguous, read-only; weight[c][W-1] multiplies the newest input
  *   bias               [dim] read-only, or NULL
- *   window             snapshot buffer, write-only, laid out as window_layout says
+ *   window             snapshot buffer, write-only, laid out as window_layout says (NULL allowed
+ *                      and ignored for CV_WINDOW_HISTORY)
  *   err                int32 [n_seq] device array or NULL: receives the CV_SEQ_* bits of each
  *                      sequence (0 for fine and for padded sequences)
  * Preconditions the library cannot check: distinct sequences use distinct slots; out and window do
@@ -189,9 +207,11 @@ CV_API int cv_conv_commit(const cv_commit_args *args, void *stream);
  * cv_verify_plan -- validate `args` exactly as cv_conv_verify does and report the launch it would
  * make, without touching the GPU.  grid = (grid_x, grid_y), block = threads, dynamic shared
  * memory = smem_bytes; each block owns channels_per_block channels of one sequence.  path says
- * which kernel runs: 1 = packed buffers with T a compile-time constant (T <= 17 for bf16, <= 8
- * for fp32), 2 = packed buffers, dense window, larger T in chunks of 8 tokens, 0 = the general
- * kernel (any strides).  Host pointer `plan` must not be NULL.  Returns the same status
+ * which kernel runs: 3 = persistent pipelined kernel (packed buffers and packed state rows, T a
+ * compile-time constant; grid_y = 1 and each block walks (sequence, channel block) units),
+ * 1 = packed buffers with T a compile-time constant (T <= 17 for bf16, <= 8 for fp32),
+ * 2 = packed buffers, dense window, larger T in chunks of 8 tokens, 0 = the general kernel (any
+ * strides).  Host pointer `plan` must not be NULL.  Returns the same status
  * cv_conv_verify would return before launching.
  */
 typedef struct cv_launch_plan {

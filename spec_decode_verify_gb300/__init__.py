@@ -15,12 +15,12 @@ import os
 from typing import Optional
 
 __all__ = ["conv_verify", "conv_commit", "verify_plan", "status_string", "load_library", "library_path",
-           "CvError", "DENSE", "DEDUP", "SEQ_BAD_SLOT", "SEQ_BAD_OFFSET", "SEQ_BAD_ACCEPT"]
+           "CvError", "DENSE", "DEDUP", "HISTORY", "SEQ_BAD_SLOT", "SEQ_BAD_OFFSET", "SEQ_BAD_ACCEPT"]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 library_path = os.path.join(_PKG, "_build", "libconvverify.so")
 
-DENSE, DEDUP = 1, 2
+DENSE, DEDUP, HISTORY = 1, 2, 3
 F32, BF16 = 0, 1
 SEQ_BAD_SLOT, SEQ_BAD_OFFSET, SEQ_BAD_ACCEPT = 1, 2, 4
 MAX_T = 128
@@ -122,10 +122,14 @@ def _layout_code(layout) -> int:
         return DENSE
     if layout in (DEDUP, "dedup"):
         return DEDUP
+    if layout in (HISTORY, "history"):
+        return HISTORY
     raise ValueError(f"unknown window layout {layout!r}")
 
 
 def _window_strides(window, layout: int):
+    if layout == HISTORY or window is None:  # no window buffer
+        return 0, 0, 0, 0
     s = window.stride()
     if layout == DENSE:  # [n_seq, T, dim, W-1]
         return s[0], s[1], s[2], s[3]
@@ -145,8 +149,10 @@ def make_verify_args(x, conv_state, weight, bias, out, window, *, layout, qk_cha
 
     x [n_seq, T, dim] (channel stride 1, any seq/token strides), conv_state [n_slots, dim, S]
     (column stride 1), weight [dim, W] contiguous, bias [dim] or None, out [n_seq, T, dim] (channel
-    stride 1), window dense [n_seq, T, dim, W-1] or dedup [n_seq, dim, T+W-2] (any strides),
-    cache_idx / state_off / err int32 [n_seq] or None."""
+    stride 1), window dense [n_seq, T, dim, W-1] or dedup [n_seq, dim, T+W-2] (any strides), or
+    None with layout "history" (conv_state [n_slots, dim, S >= T+W-2] then receives the snapshot
+    row and the next call reads at state_off = accept_len - 1), cache_idx / state_off / err int32
+    [n_seq] or None."""
     lay = _layout_code(layout)
     ptr = _dev_ptr if check_device else (lambda t, n, required=True: None if t is None else t.data_ptr())
     n_seq, T, dim = x.shape
@@ -163,7 +169,8 @@ def make_verify_args(x, conv_state, weight, bias, out, window, *, layout, qk_cha
         conv_state=ptr(conv_state, "conv_state"), n_slots=conv_state.shape[0], state_cols=conv_state.shape[2],
         state_slot_stride=conv_state.stride(0), state_ch_stride=conv_state.stride(1),
         cache_idx=ptr(cache_idx, "cache_idx", False), state_off=ptr(state_off, "state_off", False),
-        weight=ptr(weight, "weight"), bias=ptr(bias, "bias", False), window=ptr(window, "window"),
+        weight=ptr(weight, "weight"), bias=ptr(bias, "bias", False),
+        window=ptr(window, "window", lay != HISTORY),
         window_layout=lay, reserved0=0, win_seq_stride=ws[0], win_step_stride=ws[1], win_ch_stride=ws[2],
         win_col_stride=ws[3], err=ptr(err, "err", False))
 
@@ -172,9 +179,10 @@ def conv_verify(x, conv_state, weight, bias, out, window, *, layout, qk_channels
                 cache_idx=None, state_off=None, err=None, stream=None) -> None:
     """Queue one batched verify on ``stream`` (default: torch's current stream).
 
-    Writes out, window, conv_state (and err); raises CvError on an invalid argument."""
+    Writes out, window, conv_state (and err); raises CvError on an invalid argument.  With layout
+    "history" pass window=None: the snapshots go into the state rows."""
     for t in (x, conv_state, weight, out, window):
-        if t.dtype != x.dtype:
+        if t is not None and t.dtype != x.dtype:
             raise TypeError("x, conv_state, weight, out and window must share one dtype")
     if bias is not None and bias.dtype != x.dtype:
         raise TypeError("bias must have the dtype of x")

@@ -9,7 +9,9 @@
 //   general         (path 0): everything else (any strides, any dim, dedup rows with a larger T).
 //   pipelined       (path 3): path 1's buffers with packed state rows: persistent blocks walk
 //                             (sequence, channel block) units and load each by bulk copy into
-//                             double-buffered shared memory, two units ahead.
+//                             double-buffered shared memory, two units ahead.  The history layout
+//                             takes it when its state rows are the packed [dim][T+W-2] rows, and
+//                             the general kernel otherwise.
 #include <atomic>
 #include <cstdint>
 #include <cstring>
@@ -31,6 +33,10 @@ constexpr int kGenericSmemBudget = 96 * 1024;
 constexpr int kCommitThreads = 128;
 constexpr int kCommitRowThreads = 64;  // dedup commit: 512 channels per block
 constexpr int kSmemMax = 227 * 1024;
+// the pipelined kernel lists the active sequences in shared memory up to this batch size
+constexpr int kCompactMaxSeq = 1024;
+
+bool pipe_compacts(const cv_verify_args *a) { return a->cache_idx != nullptr && a->n_seq <= kCompactMaxSeq; }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool stride16(long long stride_elems, int esize) { return ((stride_elems * esize) & 15) == 0; }
@@ -54,36 +60,45 @@ int check_verify(const cv_verify_args *a) {
     if (a->T < 1 || a->T > CV_MAX_T) return CV_ERR_TOKENS;
     if (a->n_seq < 0 || a->n_seq > 65535 || a->dim < 1 || a->n_slots < 1 || a->state_cols < a->width - 1)
         return CV_ERR_SHAPE;
-    if (a->window_layout != CV_WINDOW_DENSE && a->window_layout != CV_WINDOW_DEDUP) return CV_ERR_LAYOUT;
+    const bool hist = a->window_layout == CV_WINDOW_HISTORY;
+    if (a->window_layout != CV_WINDOW_DENSE && a->window_layout != CV_WINDOW_DEDUP && !hist) return CV_ERR_LAYOUT;
     if (a->window_layout == CV_WINDOW_DEDUP && a->win_step_stride != a->win_col_stride) return CV_ERR_LAYOUT;
+    if (hist && a->state_cols < a->T + a->width - 2) return CV_ERR_SHAPE;
     if (a->qk_channels < 0 || a->qk_channels > a->dim) return CV_ERR_HEAD_DIM;
     if (a->qk_channels > 0 && (!pow2(a->head_dim) || a->head_dim < 8 || a->head_dim > 256 ||
                                a->qk_channels % a->head_dim != 0))
         return CV_ERR_HEAD_DIM;
     if (a->x_seq_stride < 0 || a->x_tok_stride < 0 || a->out_seq_stride < 0 || a->out_tok_stride < 0 ||
-        a->state_slot_stride < 0 || a->state_ch_stride < 0 || a->win_seq_stride < 0 || a->win_step_stride < 0 ||
-        a->win_ch_stride < 0 || a->win_col_stride < 0)
+        a->state_slot_stride < 0 || a->state_ch_stride < 0)
+        return CV_ERR_STRIDE;
+    if (!hist && (a->win_seq_stride < 0 || a->win_step_stride < 0 || a->win_ch_stride < 0 || a->win_col_stride < 0))
         return CV_ERR_STRIDE;
     if (a->dim > 1 && a->state_ch_stride < a->state_cols) return CV_ERR_STRIDE;
-    if (a->n_seq > 0 && (!a->x || !a->out || !a->conv_state || !a->weight || !a->window)) return CV_ERR_NULL_POINTER;
+    if (a->n_seq > 0 && (!a->x || !a->out || !a->conv_state || !a->weight || (!hist && !a->window)))
+        return CV_ERR_NULL_POINTER;
     if (a->n_seq > 0) {
-        const void *outs[2] = {a->out, a->window};
+        const void *outs[2] = {a->out, hist ? nullptr : a->window};
         const void *ins[3] = {a->x, a->conv_state, a->weight};
         for (const void *o : outs)
             for (const void *i : ins)
-                if (o == i) return CV_ERR_ALIAS;
-        if (a->out == a->window) return CV_ERR_ALIAS;
+                if (o && o == i) return CV_ERR_ALIAS;
+        if (!hist && a->out == a->window) return CV_ERR_ALIAS;
     }
     return CV_OK;
+}
+
+// x, out, taps and bias allow 16-byte vectors and bulk copies of whole channel blocks.
+bool io_packed(const cv_verify_args *a, int esize) {
+    if (a->dim % 8 != 0) return false;
+    if (!aligned16(a->x) || !stride16(a->x_seq_stride, esize) || !stride16(a->x_tok_stride, esize)) return false;
+    if (!aligned16(a->out) || !stride16(a->out_seq_stride, esize) || !stride16(a->out_tok_stride, esize)) return false;
+    return aligned16(a->weight) && (!a->bias || aligned16(a->bias));
 }
 
 bool fast_eligible(const cv_verify_args *a, int esize, int max_static_t) {
     const int R = a->width - 1;
     const long long Q = a->T + R - 1;
-    if (a->dim % 8 != 0) return false;
-    if (!aligned16(a->x) || !stride16(a->x_seq_stride, esize) || !stride16(a->x_tok_stride, esize)) return false;
-    if (!aligned16(a->out) || !stride16(a->out_seq_stride, esize) || !stride16(a->out_tok_stride, esize)) return false;
-    if (!aligned16(a->weight) || (a->bias && !aligned16(a->bias))) return false;
+    if (a->window_layout == CV_WINDOW_HISTORY || !io_packed(a, esize)) return false;
     if (!aligned16(a->window) || !stride16(a->win_seq_stride, esize) || a->win_col_stride != 1) return false;
     if (a->window_layout == CV_WINDOW_DEDUP) return a->win_ch_stride == Q && a->T <= max_static_t;
     return a->win_ch_stride == R && stride16(a->win_step_stride, esize);
@@ -113,10 +128,14 @@ int plan_verify(const cv_verify_args *a, cv_launch_plan *pl) {
     const cvk::KernelSet &ks = kernel_set(a->dtype, a->width);
     std::memset(pl, 0, sizeof *pl);
 
+    const bool hist = a->window_layout == CV_WINDOW_HISTORY;
     const bool fast = fast_eligible(a, esize, ks.max_static_t);
     const int cpt = (a->qk_channels > 0 && a->head_dim / 4 > 32) ? 8 : 4;
-    if (fast && a->T <= ks.max_static_t &&
-        state_packed(a->conv_state, a->state_slot_stride, a->state_ch_stride, a->width, esize)) {
+    // the history layout pipelines when its state rows are exactly the packed [dim][T+W-2] rows
+    const bool hist_pipe = hist && io_packed(a, esize) && a->T <= ks.max_static_t && aligned16(a->conv_state) &&
+                           stride16(a->state_slot_stride, esize) && a->state_ch_stride == a->T + R - 1;
+    if (hist_pipe || (fast && a->T <= ks.max_static_t &&
+                      state_packed(a->conv_state, a->state_slot_stride, a->state_ch_stride, a->width, esize))) {
         auto part = [](long long b) { return (b + 127) / 128 * 128; };
         int threads = kPipeThreads;
         while (threads > 32 && cpt * (threads / 2) >= a->dim) threads /= 2;
@@ -124,11 +143,12 @@ int plan_verify(const cv_verify_args *a, cv_launch_plan *pl) {
         threads = shrink_for_parallelism(threads, cpt, a);
         const long long bc = (long long)cpt * threads;
         const long long Q = a->T + R - 1;
-        // two stages (x rows + committed windows) and two image buffers (dedup row + windows)
-        const long long stage = part(a->T * bc * esize) + part(R * bc * esize);
-        long long image = part(R * bc * esize);
-        if (a->window_layout == CV_WINDOW_DEDUP) image += part(Q * bc * esize);
-        const long long smem = 2 * stage + 2 * image + 24;
+        // two stages (x rows + committed windows, or whole history rows) and two image buffers
+        // (dedup row + committed windows, or the history row alone); 2 mbarriers, 2 slots, 2 offsets
+        const long long stage = part(a->T * bc * esize) + part((hist ? Q : R) * bc * esize);
+        long long image = hist ? 0 : part(R * bc * esize);
+        if (a->window_layout != CV_WINDOW_DENSE) image += part(Q * bc * esize);
+        const long long smem = 2 * stage + 2 * image + 32 + (pipe_compacts(a) ? 16 + 4LL * a->n_seq : 0);
         int per_sm = (int)(kSmemPerSM / (smem + kSmemPerBlockReserved));
         if (per_sm > pipe_blocks_per_sm(cpt, a->T)) per_sm = pipe_blocks_per_sm(cpt, a->T);
         if (smem <= kSmemMax && per_sm >= 1) {
@@ -181,6 +201,26 @@ int plan_verify(const cv_verify_args *a, cv_launch_plan *pl) {
     return CV_OK;
 }
 
+// Launch with programmatic stream serialization: the kernel may be scheduled while the previous
+// grid in the stream finishes; every kernel waits (griddepcontrol.wait) for that grid's completion
+// before its first global-memory access, so the order of the stream's work is kept.
+template <typename P>
+cudaError_t launch_pdl(void (*kernel)(P), dim3 grid, int threads, int smem, cudaStream_t stream, const P &p) {
+    cudaLaunchConfig_t cfg;
+    std::memset(&cfg, 0, sizeof cfg);
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(threads);
+    cfg.dynamicSmemBytes = (size_t)smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    std::memset(attr, 0, sizeof attr);
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, p);
+}
+
 // Opt a kernel into more than 48 KB of dynamic shared memory (once per kernel and device).
 cudaError_t ensure_smem(const void *kernel, int bytes) {
     if (bytes <= 48 * 1024) return cudaSuccess;
@@ -220,6 +260,9 @@ int launch_verify(const cv_verify_args *a, const cv_launch_plan &pl, cudaStream_
     p.bias = a->bias;
     p.win = a->window;
     p.dedup = a->window_layout == CV_WINDOW_DEDUP;
+    p.hist = a->window_layout == CV_WINDOW_HISTORY;
+    p.compact = pl.path == 3 && pipe_compacts(a);
+    if (p.hist) p.win = nullptr;
     p.w_seq = a->win_seq_stride;
     p.w_step = p.dedup ? a->win_col_stride : a->win_step_stride;
     p.w_ch = a->win_ch_stride;
@@ -247,7 +290,8 @@ int launch_verify(const cv_verify_args *a, const cv_launch_plan &pl, cudaStream_
                           : pl.path == 2 ? ks.fast[ci][0]
                                          : ks.pipe[ci][a->T];
     if (ensure_smem(reinterpret_cast<const void *>(k), pl.smem_bytes) != cudaSuccess) return CV_ERR_LAUNCH;
-    k<<<dim3(pl.grid_x, pl.grid_y), pl.threads, pl.smem_bytes, stream>>>(p);
+    if (launch_pdl(k, dim3(pl.grid_x, pl.grid_y), pl.threads, pl.smem_bytes, stream, p) != cudaSuccess)
+        return CV_ERR_LAUNCH;
     return cudaGetLastError() == cudaSuccess ? CV_OK : CV_ERR_LAUNCH;
 }
 
@@ -258,6 +302,7 @@ int check_commit(const cv_commit_args *a) {
     if (a->T < 1 || a->T > CV_MAX_T) return CV_ERR_TOKENS;
     if (a->n_seq < 0 || a->n_seq > 65535 || a->dim < 1 || a->n_slots < 1 || a->state_cols < a->width - 1)
         return CV_ERR_SHAPE;
+    // (the history layout has nothing to commit: the next verify reads at accept_len - 1)
     if (a->window_layout != CV_WINDOW_DENSE && a->window_layout != CV_WINDOW_DEDUP) return CV_ERR_LAYOUT;
     if (a->window_layout == CV_WINDOW_DEDUP && a->win_step_stride != a->win_col_stride) return CV_ERR_LAYOUT;
     if (a->state_slot_stride < 0 || a->state_ch_stride < 0 || a->win_seq_stride < 0 || a->win_step_stride < 0 ||
@@ -310,7 +355,8 @@ int launch_commit(const cv_commit_args *a, cudaStream_t stream) {
             const int bc = 8 * rt;
             auto kr = kernel_set(a->dtype, a->width).commit_rows;
             if (ensure_smem(reinterpret_cast<const void *>(kr), (int)sm) != cudaSuccess) return CV_ERR_LAUNCH;
-            kr<<<dim3((a->dim + bc - 1) / bc, a->n_seq), rt, (int)sm, stream>>>(p);
+            if (launch_pdl(kr, dim3((a->dim + bc - 1) / bc, a->n_seq), rt, (int)sm, stream, p) != cudaSuccess)
+                return CV_ERR_LAUNCH;
             return cudaGetLastError() == cudaSuccess ? CV_OK : CV_ERR_LAUNCH;
         }
         p.mode = 0;
@@ -320,7 +366,8 @@ int launch_commit(const cv_commit_args *a, cudaStream_t stream) {
     const int bc = 8 * threads;
     auto k = kernel_set(a->dtype, a->width).commit;
     if (ensure_smem(reinterpret_cast<const void *>(k), smem) != cudaSuccess) return CV_ERR_LAUNCH;
-    k<<<dim3((a->dim + bc - 1) / bc, a->n_seq), threads, smem, stream>>>(p);
+    if (launch_pdl(k, dim3((a->dim + bc - 1) / bc, a->n_seq), threads, smem, stream, p) != cudaSuccess)
+        return CV_ERR_LAUNCH;
     return cudaGetLastError() == cudaSuccess ? CV_OK : CV_ERR_LAUNCH;
 }
 
@@ -358,7 +405,8 @@ const char *cv_status_string(int status) {
         case CV_ERR_WIDTH: return "conv width outside 2..4";
         case CV_ERR_DTYPE: return "unknown dtype";
         case CV_ERR_HEAD_DIM: return "invalid head_dim / qk_channels";
-        case CV_ERR_LAYOUT: return "unknown window layout, or dedup step stride != column stride";
+        case CV_ERR_LAYOUT:
+            return "unknown window layout, dedup step stride != column stride, or history layout passed to commit";
         case CV_ERR_STRIDE: return "negative stride or overlapping state rows";
         case CV_ERR_ALIAS: return "an output buffer has the base address of an input or of the other output";
         case CV_ERR_LAUNCH: return "CUDA launch failed";

@@ -21,6 +21,8 @@ constexpr unsigned kCommitWaitPolls = 1u << 20;  // mbarrier polls before a bloc
 
 template <typename B, int W>
 __global__ void __launch_bounds__(128) commit_kernel(const __grid_constant__ CommitParams p) {
+    grid_dep_wait();
+    grid_dep_launch();
     constexpr int R = W - 1;
     constexpr int ES = (int)sizeof(B);
     constexpr int VE = 16 / ES;
@@ -83,6 +85,8 @@ __global__ void __launch_bounds__(128) commit_kernel(const __grid_constant__ Com
 // outlive it) and writes nothing.  The wait is bounded: a timeout sets bit 8 in err.
 template <typename B, int W>
 __global__ void __launch_bounds__(64) commit_rows(const __grid_constant__ CommitParams p) {
+    grid_dep_wait();
+    grid_dep_launch();
     constexpr int R = W - 1;
     constexpr int ES = (int)sizeof(B);
     constexpr int VE = 16 / ES;

@@ -27,6 +27,8 @@ struct VerifyParams {
     int qk_channels, head_dim, pitch;      // pitch: elements per shared-memory row (generic kernel)
     float eps;
     int dedup;
+    int hist;     // history-row state: the snapshot row goes into the state row (no window buffer)
+    int compact;  // pipelined kernel: walk only the sequences with a cache slot >= 0 (list in shared memory)
     int x_vec, out_vec, st_vec, w_vec, b_vec;  // 16-byte vector access allowed (checked on the host)
 };
 
@@ -117,6 +119,26 @@ __device__ __forceinline__ void silu_run(const float *a, float *y) {
     }
 }
 __device__ __forceinline__ float silu(float a) { return a < -80.0f ? silu_exact(a) : silu_fast(a); }
+
+// Programmatic dependent launch (the library launches every kernel with programmatic stream
+// serialization).  grid_dep_wait returns once the grids this one depends on in the stream have
+// completed and their memory is visible -- immediately when there is no such dependency -- so
+// every kernel calls it before its first global-memory access.  grid_dep_launch then lets the
+// next grid in the stream be scheduled onto SMs this one frees, so its launch and prologue overlap
+// this grid's tail (it still waits for this grid's completion before touching memory).
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory"); }
+
+// One token's conv: the bias (or 0) first, then the W taps in order, each a fused multiply-add
+// (one rounding per tap).  Every kernel computes it this way, so all launch paths agree bit for
+// bit; against a definition that rounds each product before its add it differs by a few fp32 ulp,
+// far inside the output tolerance (the snapshots and the state are raw copies and unaffected).
+template <int W>
+__device__ __forceinline__ float conv_fma(float acc, const float *w, const float *in) {
+#pragma unroll
+    for (int j = 0; j < W; ++j) acc = fmaf(w[j], in[j], acc);
+    return acc;
+}
 
 // Sum of squares of a thread's CPT (4 or 8) values in one fixed order: a chain over each run of 4
 // channels, then the runs added pairwise.  The xor-shuffle tree over lanes continues the same

@@ -16,7 +16,7 @@
 //        - dense snapshots: the thread's CPT x (W-1) run per token as vector stores;
 //        - committed window (= snapshot T-1) -> state columns [0, W-1), staged and bulk-copied
 //          when the state rows are packed;
-//   3. conv (fp32, bias first, taps in order, each product rounded before its add), SiLU, and for
+//   3. conv (fp32, bias first, taps in order as fused multiply-adds), SiLU, and for
 //      q|k channels the L2 normalisation over the head_dim group as an xor-shuffle over
 //      head_dim/CPT lanes (glm5next_kda mod.rs: conv1d + SiLU -> L2(q,k only), eps inside the
 //      root); one rounding to the output type; vector stores.
@@ -38,6 +38,8 @@ __host__ __device__ constexpr int chunk_align(int bytes) { return bytes % 16 == 
 
 template <typename B, int W, int TS, int CPT>
 __global__ void __launch_bounds__(256) verify_fast(const __grid_constant__ VerifyParams p) {
+    grid_dep_wait();
+    grid_dep_launch();
     constexpr int R = W - 1;                  // committed window columns
     constexpr int TC = TS > 0 ? TS : 4;       // tokens held in registers at a time
     constexpr int ES = (int)sizeof(B);        // element bytes
@@ -156,9 +158,7 @@ __global__ void __launch_bounds__(256) verify_fast(const __grid_constant__ Verif
         float acc[CPT];
 #pragma unroll
         for (int e = 0; e < CPT; ++e) {
-            acc[e] = bs[e];
-#pragma unroll
-            for (int j = 0; j < W; ++j) acc[e] = __fadd_rn(acc[e], __fmul_rn(wt[e][j], fw[e][u + j]));
+            acc[e] = conv_fma<W>(bs[e], wt[e], &fw[e][u]);
         }
         silu_run<CPT>(acc, yu);
     };

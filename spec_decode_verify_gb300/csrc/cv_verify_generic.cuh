@@ -1,13 +1,14 @@
 // Verify kernel for any strides and layouts (the general path).
 //
 // Used when the fast path's preconditions do not hold: unaligned or odd-strided x / out, a
-// channel count that is not a multiple of 8, transposed or permuted snapshot layouts, or a
-// deduplicated row longer than the fast path keeps in registers.  One block per (channel block,
+// channel count that is not a multiple of 8, transposed or permuted snapshot layouts, a
+// deduplicated row longer than the fast path keeps in registers, or history-row state rows wider
+// than the row (or T above the static range).  One block per (channel block,
 // sequence); the block's inputs are staged once in a token-major shared-memory tile
 //     tile[j][c] = full_c[j],  j in [0, W-1+T)   (rows 0..W-2: committed window, then x_0..x_{T-1})
 // and every snapshot layout and the committed window are written from that tile in destination
 // order (channel-major runs, channel-stride-1 runs, or element by element).  The arithmetic is the
-// same as the fast path's: fp32, bias first, taps in order with each product rounded, SiLU, L2
+// same as the fast path's: fp32, bias first, taps in order as fused multiply-adds, SiLU, L2
 // over the head_dim group as an xor-shuffle over head_dim/8 lanes.
 #pragma once
 
@@ -104,6 +105,8 @@ __device__ __forceinline__ void write_view(const B *__restrict__ tile, int pitch
 // ---------------------------------------------------------------- verify
 template <typename B, int W>
 __global__ void __launch_bounds__(256) verify_generic(const __grid_constant__ VerifyParams p) {
+    grid_dep_wait();
+    grid_dep_launch();
     constexpr int R = W - 1;  // committed window columns
     extern __shared__ __align__(16) unsigned char smem_raw[];
     B *tile = reinterpret_cast<B *>(smem_raw);
@@ -222,7 +225,12 @@ __global__ void __launch_bounds__(256) verify_generic(const __grid_constant__ Ve
     __syncthreads();
 
     // (4) snapshots and committed window, written from the tile in destination order
-    {
+    if (p.hist) {
+        // history-row state: the snapshot row [full[1 .. W-2], x_0 .. x_{T-1}] replaces columns
+        // [0, T+W-2) of the state row (every thread read its committed window before the barrier)
+        B *sb = reinterpret_cast<B *>(p.state) + (long long)slot * p.st_slot + (long long)c0 * p.st_ch;
+        write_view<B>(tile, pitch, 1, T + R - 1, sb, p.st_ch, 1, nch);
+    } else {
         B *wb = reinterpret_cast<B *>(p.win) + (long long)s * p.w_seq;
         if (p.dedup) {
             write_view<B>(tile, pitch, 1, T + R - 1, wb + (long long)c0 * p.w_ch, p.w_ch, p.w_col, nch);
@@ -254,10 +262,11 @@ __global__ void __launch_bounds__(256) verify_generic(const __grid_constant__ Ve
         float y[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
+            // the same fused multiply-add chain as conv_fma (bias, then the taps in order)
             float acc = has_bias ? bs[e] : 0.0f;
 #pragma unroll
-            for (int j = 0; j < R; ++j) acc = __fadd_rn(acc, __fmul_rn(wt[e][j], win[j][e]));
-            acc = __fadd_rn(acc, __fmul_rn(wt[e][R], xv[e]));
+            for (int j = 0; j < R; ++j) acc = fmaf(wt[e][j], win[j][e], acc);
+            acc = fmaf(wt[e][R], xv[e], acc);
             y[e] = silu(acc);
         }
 #pragma unroll

@@ -13,13 +13,18 @@
 // the inputs only (the deduplicated row of sglang PR #46184 -- step t's window is columns
 // t..t+W-2 of [state[1..W-2], x_0..x_{T-1}] -- as one staged image written by one bulk copy;
 // dense snapshots as vector stores; the committed window, staged and bulk-copied into the packed
-// state rows) and computes the outputs: fp32 conv with bias first and each product rounded before
-// its add, SiLU, the L2 normalisation of the q|k groups over head_dim/CPT lanes with the T
+// state rows) and computes the outputs: fp32 conv with bias first and the taps as fused
+// multiply-adds, SiLU, the L2 normalisation of the q|k groups over head_dim/CPT lanes with the T
 // shuffle trees interleaved (glm5next_kda mod.rs), one rounding, vector stores.
 // Every mbarrier wait is bounded: a block that waits too long sets CV_SEQ_TIMEOUT in err (when
 // given) for the unit's sequence, drains its copies in flight (again bounded) and returns.
+// History-row state (no window buffer): the stage holds each channel's whole [T+W-2] state row,
+// the committed window is taken from columns [off, off+W-1) of it, and the row image is stored
+// back over the state row instead of into a window buffer; there is no separate committed-window
+// image.
 // Preconditions (checked on the host): those of the fast path, packed 16-byte-aligned state rows
-// ([dim][W-1]), T <= 17 (bf16) / 8 (fp32), head_dim / CPT <= 32.
+// ([dim][W-1], or [dim][T+W-2] for the history layout), T <= 17 (bf16) / 8 (fp32),
+// head_dim / CPT <= 32.
 #pragma once
 
 #include <type_traits>
@@ -38,6 +43,8 @@ __host__ __device__ constexpr long long pipe_part(long long b) { return (b + 127
 
 template <typename B, int W, int TS, int CPT>
 __global__ void __launch_bounds__(128, (CPT == 4 && TS <= 8) ? 4 : 2) verify_pipe(const __grid_constant__ VerifyParams p) {
+    grid_dep_wait();
+    grid_dep_launch();
     static_assert(TS > 0, "the pipelined kernel needs a compile-time T");
     // (taps and bias are read from global memory, so W*CPT*ES need only be 8-byte aligned)
     constexpr int R = W - 1;
@@ -54,22 +61,28 @@ __global__ void __launch_bounds__(128, (CPT == 4 && TS <= 8) ? 4 : 2) verify_pip
     const int tid = threadIdx.x;
     const int BC = CPT * blockDim.x;
     const int nblk = (p.dim + BC - 1) / BC;
-    const int n_units = p.n_seq * nblk;
-    const bool dense = !p.dedup;
+    const bool hist = p.hist != 0;        // history-row state: no window buffer
+    const bool dense = !p.dedup && !hist;  // dense window: no row image
     const bool has_bias = p.bias != nullptr;
+    const int SC = hist ? Q : R;           // state columns staged per channel
 
-    // shared memory: stage 0, stage 1 (x rows + committed windows), image buffers 0 and 1 (dedup
-    // row image + committed-window image), 2 mbarriers, 2 unit slots
-    const long long xb = pipe_part((long long)TS * BC * ES), sb = pipe_part((long long)R * BC * ES);
-    const long long stage_bytes = xb + sb;
+    // shared memory: stage 0, stage 1 (x rows + committed windows, or whole history rows), image
+    // buffers 0 and 1 (dedup row image + committed-window image, or the history row image alone),
+    // 2 mbarriers, 2 unit slots, 2 unit state offsets, then (when compacting) 4 warp counts and the
+    // list of active sequences
+    const long long xb = pipe_part((long long)TS * BC * ES);
+    const long long stage_bytes = xb + pipe_part((long long)SC * BC * ES);
     const long long rb = dense ? 0 : pipe_part((long long)Q * BC * ES);
-    const long long img_bytes = rb + sb;
+    const long long img_bytes = rb + (hist ? 0 : pipe_part((long long)R * BC * ES));
     unsigned char *const img0 = smem + 2 * stage_bytes;
     uint64_t *const bar = reinterpret_cast<uint64_t *>(img0 + 2 * img_bytes);
-    volatile int *const info = reinterpret_cast<volatile int *>(bar + 2);
-    if (2 * stage_bytes + 2 * img_bytes + 24 > (long long)dynamic_smem_bytes()) return;  // launch mismatch
+    volatile int *const info = reinterpret_cast<volatile int *>(bar + 2);  // [0, 2): slots, [2, 4): offsets
+    int *const wcount = reinterpret_cast<int *>(bar + 4);
+    int *const act = wcount + 4;
+    const bool compact = p.compact != 0;
+    if (2 * stage_bytes + 2 * img_bytes + 32 + (compact ? 16 + 4LL * p.n_seq : 0) > (long long)dynamic_smem_bytes())
+        return;  // launch mismatch
 
-    const int iters = (int)blockIdx.x < n_units ? (n_units - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
     if (tid == 0) {
         mbar_init(&bar[0], 1);
         mbar_init(&bar[1], 1);
@@ -77,19 +90,49 @@ __global__ void __launch_bounds__(128, (CPT == 4 && TS <= 8) ? 4 : 2) verify_pip
     }
     __syncthreads();
 
+    // Units walk the active sequences only: the block lists the sequences whose cache slot is not
+    // negative (ascending), so padded sequences cost no unit and every block gets its fair share of
+    // real work.  Padded sequences' err entries are written here (0) by block 0.
+    int n_act = p.n_seq;
+    if (compact) {
+        const int lane = tid & 31, warp = tid >> 5, nwarps = ((int)blockDim.x + 31) >> 5;
+        n_act = 0;
+        for (int i0 = 0; i0 < p.n_seq; i0 += (int)blockDim.x) {
+            const int i = i0 + tid;
+            const bool a = i < p.n_seq && __ldg(p.cache_idx + i) >= 0;
+            if (i < p.n_seq && !a && p.err && blockIdx.x == 0) p.err[i] = 0;
+            const unsigned m = __ballot_sync(0xffffffffu, a);
+            if (lane == 0) wcount[warp] = __popc(m);
+            __syncthreads();
+            int before = 0, total = 0;
+            for (int w = 0; w < nwarps; ++w) {
+                const int c = wcount[w];
+                before += w < warp ? c : 0;
+                total += c;
+            }
+            if (a) act[n_act + before + __popc(m & ((1u << lane) - 1u))] = i;
+            n_act += total;
+            __syncthreads();
+        }
+    }
+    auto seq_at = [&](int q) { return compact ? act[q] : q; };
+    const int n_units = n_act * nblk;
+    const int iters = (int)blockIdx.x < n_units ? (n_units - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+
     // thread 0: start the copies of iteration k into stage k & 1 (or only arrive, for padding).  The
     // index data of the next unit (cache slot, state offset) is loaded one issue ahead, so no issue
     // waits for a global-memory round trip; the first two units load theirs together at the start
     // and send their x copies out before the indices arrive (the x rows do not depend on the slot).
     auto unit_of = [&](int k, int &s, int &c0, int &nch) {
         const int u = (int)blockIdx.x + k * (int)gridDim.x;
-        s = u / nblk;
-        c0 = (u - s * nblk) * BC;
+        const int q = u / nblk;
+        s = seq_at(q);
+        c0 = (u - q * nblk) * BC;
         nch = min(BC, p.dim - c0);
     };
     auto load_index = [&](int k, int &slot, int &off) {
         if (k >= iters) return;
-        const int s = ((int)blockIdx.x + k * (int)gridDim.x) / nblk;
+        const int s = seq_at(((int)blockIdx.x + k * (int)gridDim.x) / nblk);
         slot = p.cache_idx ? __ldg(p.cache_idx + s) : s;
         off = p.state_off ? __ldg(p.state_off + s) : 0;
     };
@@ -112,12 +155,14 @@ __global__ void __launch_bounds__(128, (CPT == 4 && TS <= 8) ? 4 : 2) verify_pip
         if (p.err && c0 == 0) p.err[s] = status;
         const bool go = slot >= 0 && status == 0;
         info[st] = go ? slot : -1;
+        info[2 + st] = off;
         if (go) {
             if (!x_sent) issue_x(k);
-            mbar_expect_tx(&bar[st], (unsigned)(R * nch * ES));
+            // packed state rows of SC columns: the committed windows, or whole history rows
+            mbar_expect_tx(&bar[st], (unsigned)(SC * nch * ES));
             bulk_load(smem + st * stage_bytes + xb,
-                      reinterpret_cast<const B *>(p.state) + (long long)slot * p.st_slot + (long long)c0 * R,
-                      (unsigned)(nch * R * ES), &bar[st]);
+                      reinterpret_cast<const B *>(p.state) + (long long)slot * p.st_slot + (long long)c0 * SC,
+                      (unsigned)(nch * SC * ES), &bar[st]);
         }
         mbar_arrive(&bar[st]);
     };
@@ -136,7 +181,7 @@ __global__ void __launch_bounds__(128, (CPT == 4 && TS <= 8) ? 4 : 2) verify_pip
     const int cl = tid * CPT;
     // unit u = blockIdx.x + k * gridDim.x as (sequence, channel block), stepped without divisions
     const int g_s = (int)gridDim.x / nblk, g_b = (int)gridDim.x - g_s * nblk;
-    int s = (int)blockIdx.x / nblk, cb = (int)blockIdx.x - s * nblk;
+    int q = (int)blockIdx.x / nblk, cb = (int)blockIdx.x - q * nblk;  // q: index into the sequence list
     constexpr int LOG_CPT = CPT == 4 ? 2 : 3;
     const int lanes = p.head_dim >> LOG_CPT;  // threads per L2 group
     float wt[CPT][W];                         // taps and bias of the current channel block
@@ -144,6 +189,7 @@ __global__ void __launch_bounds__(128, (CPT == 4 && TS <= 8) ? 4 : 2) verify_pip
     int wcb = -1;
     for (int k = 0; k < iters; ++k) {
         const int st = k & 1;
+        const int s = seq_at(q);
         const unsigned char *stg = smem + st * stage_bytes;
         unsigned char *const img = img0 + (k & 1) * img_bytes;
         unsigned char *const stimg = img + rb;
@@ -177,6 +223,7 @@ __global__ void __launch_bounds__(128, (CPT == 4 && TS <= 8) ? 4 : 2) verify_pip
 
         const bool ok = mbar_wait_bounded(&bar[st], (unsigned)((k >> 1) & 1), kWaitPolls);
         const int slot = ok ? info[st] : -1;
+        const int off = info[2 + st];
         const bool go = slot >= 0;
 
         float fw[CPT][R + TS];  // inputs widened to fp32: [0, R) committed window, then x
@@ -185,7 +232,21 @@ __global__ void __launch_bounds__(128, (CPT == 4 && TS <= 8) ? 4 : 2) verify_pip
         if (go && act) {
 #pragma unroll
             for (int t = 0; t < TS; ++t) ldv<VX, NW>(xr[t], stg + ((long long)t * BC + cl) * ES);
-            ldv<VS, R * NW>(sw, stg + xb + (long long)cl * R * ES);
+            if (hist) {
+                // the committed window sits at columns [off, off+W-1) of each staged history row
+                using U = std::conditional_t<ES == 2, unsigned short, unsigned>;
+                const U *row = reinterpret_cast<const U *>(stg + xb) + (long long)cl * Q + off;
+                U v[CPT * R];
+#pragma unroll
+                for (int e = 0; e < CPT; ++e)
+#pragma unroll
+                    for (int kk = 0; kk < R; ++kk) v[e * R + kk] = row[e * Q + kk];
+#pragma unroll
+                for (int i = 0; i < R * NW; ++i)
+                    sw[i] = ES == 2 ? ((uint32_t)v[2 * i] | ((uint32_t)v[(2 * i + 1) % (CPT * R)] << 16)) : (uint32_t)v[i];
+            } else {
+                ldv<VS, R * NW>(sw, stg + xb + (long long)cl * R * ES);
+            }
 #pragma unroll
             for (int e = 0; e < CPT; ++e)
 #pragma unroll
@@ -218,10 +279,12 @@ __global__ void __launch_bounds__(128, (CPT == 4 && TS <= 8) ? 4 : 2) verify_pip
                     stv<VS, R * NW>(wsq + (long long)t * p.w_step, w);
                 }
             }
-            uint32_t fin[R * NW];
+            if (!hist) {
+                uint32_t fin[R * NW];
 #pragma unroll
-            for (int i = 0; i < R * NW; ++i) fin[i] = run_word(i, R, TS);
-            stv<VS, R * NW>(stimg + (long long)tid * CPT * R * ES, fin);
+                for (int i = 0; i < R * NW; ++i) fin[i] = run_word(i, R, TS);
+                stv<VS, R * NW>(stimg + (long long)tid * CPT * R * ES, fin);
+            }
         }
         fence_smem_to_async();
         // the image buffer written next unit was last read by this unit's predecessor's bulk copy,
@@ -240,11 +303,17 @@ __global__ void __launch_bounds__(128, (CPT == 4 && TS <= 8) ? 4 : 2) verify_pip
         }
         if (tid == 0) {
             if (go) {
-                if (!dense)
-                    bulk_store(reinterpret_cast<B *>(p.win) + (long long)s * p.w_seq + (long long)c0 * Q, img,
+                if (hist) {
+                    // the row image replaces columns [0, T+W-2) of the (packed) history rows
+                    bulk_store(reinterpret_cast<B *>(p.state) + (long long)slot * p.st_slot + (long long)c0 * Q, img,
                                (unsigned)(nch * Q * ES));
-                bulk_store(reinterpret_cast<B *>(p.state) + (long long)slot * p.st_slot + (long long)c0 * R, stimg,
-                           (unsigned)(nch * R * ES));
+                } else {
+                    if (!dense)
+                        bulk_store(reinterpret_cast<B *>(p.win) + (long long)s * p.w_seq + (long long)c0 * Q, img,
+                                   (unsigned)(nch * Q * ES));
+                    bulk_store(reinterpret_cast<B *>(p.state) + (long long)slot * p.st_slot + (long long)c0 * R,
+                               stimg, (unsigned)(nch * R * ES));
+                }
                 asm volatile("cp.async.bulk.commit_group;\n" ::: "memory");
             }
             if (k + 2 < iters) {
@@ -265,9 +334,7 @@ __global__ void __launch_bounds__(128, (CPT == 4 && TS <= 8) ? 4 : 2) verify_pip
                     for (int e = 0; e < CPT; ++e) fw[e][R + t] = elem_f<B>(xr[t], e);
 #pragma unroll
                     for (int e = 0; e < CPT; ++e) {
-                        float acc = bs[e];
-#pragma unroll
-                        for (int j = 0; j < W; ++j) acc = __fadd_rn(acc, __fmul_rn(wt[e][j], fw[e][t + j]));
+                        const float acc = conv_fma<W>(bs[e], wt[e], &fw[e][t]);
                         y[t][e] = silu_fast(acc);
                         lo = fminf(lo, acc);
                     }
@@ -277,10 +344,7 @@ __global__ void __launch_bounds__(128, (CPT == 4 && TS <= 8) ? 4 : 2) verify_pip
                     for (int t = 0; t < TS; ++t)
 #pragma unroll
                         for (int e = 0; e < CPT; ++e) {
-                            float acc = bs[e];
-#pragma unroll
-                            for (int j = 0; j < W; ++j) acc = __fadd_rn(acc, __fmul_rn(wt[e][j], fw[e][t + j]));
-                            y[t][e] = silu_exact(acc);
+                            y[t][e] = silu_exact(conv_fma<W>(bs[e], wt[e], &fw[e][t]));
                         }
                 }
             } else {
@@ -329,11 +393,11 @@ __global__ void __launch_bounds__(128, (CPT == 4 && TS <= 8) ? 4 : 2) verify_pip
                 }
             }
         }
-        s += g_s;
+        q += g_s;
         cb += g_b;
         if (cb >= nblk) {
             cb -= nblk;
-            ++s;
+            ++q;
         }
     }
     // keep the block's shared memory alive until the last bulk copies have read it

@@ -16,7 +16,7 @@ def to_device(inp: dict, device="cuda") -> dict:
         x = inp["x"]
         out["x_base"] = base
         out["x"] = base.as_strided(x.shape, x.stride(), x.storage_offset())
-    if "window" in inp:
+    if inp.get("window") is not None:
         w = inp["window"]
         # keep the window's strides (a transposed row stays transposed)
         if not w.is_contiguous():

@@ -69,18 +69,59 @@ def test_plan_for_benchmark_workload(lib):
     """128 x 8 x 10240 bf16 dedup, packed state: the pipelined path.  4 channels per thread (an L2
     group of 128 spans 32 lanes), 128 threads per unit of 512 channels.  Shared memory: two stages
     of (8 x rows + 3 window columns) and two image buffers of (10 dedup columns + 3 window columns),
-    plus 24 bytes of barriers and slots; 4 blocks fit an SM, and the persistent grid is the largest
-    multiple of the 20 channel blocks within 152 * 4 blocks, so each block keeps its taps."""
+    plus 32 bytes of barriers, slots and offsets and 16 + 4 * 128 bytes for the list of active
+    sequences; 4 blocks fit an SM, and the persistent grid is the largest multiple of the 20 channel
+    blocks within 152 * 4 blocks, so each block keeps its taps."""
     rc, pl = _plan(lib, _args(W3))
     assert rc == 0
-    smem = 2 * (8 + 3) * 512 * 2 + 2 * (10 + 3) * 512 * 2 + 24
+    smem = 2 * (8 + 3) * 512 * 2 + 2 * (10 + 3) * 512 * 2 + 32 + 16 + 4 * 128
     assert (pl.threads, pl.channels_per_block, pl.path, pl.smem_bytes) == (128, 512, 3, smem)
     assert (pl.grid_x, pl.grid_y) == (600, 1)
 
 
+HIST = wl.WORKLOADS["n128_t8_dim10240_w4_bf16_history_pad13"]
+
+
+def test_plan_for_history_workload(lib):
+    """History rows: the stages hold whole [10]-column rows and the only image is the row image,
+    so one block needs 2 * (8 + 10) * 1024 + 2 * 10 * 1024 + 32 bytes (plus the sequence list) and
+    3 blocks fit an SM; the
+    grid is the largest multiple of 20 within 152 * 3."""
+    a = _args(HIST)
+    assert a.window is None and a.state_cols == 10 and a.state_ch_stride == 10
+    rc, pl = _plan(lib, a)
+    assert rc == 0
+    smem = 2 * (8 + 10) * 512 * 2 + 2 * 10 * 512 * 2 + 32 + 16 + 4 * 128
+    assert (pl.threads, pl.channels_per_block, pl.path, pl.smem_bytes) == (128, 512, 3, smem)
+    assert (pl.grid_x, pl.grid_y) == (440, 1)
+
+
+def test_history_validation_and_paths(lib):
+    # rows narrower than T+W-2 are rejected
+    a = _args(HIST)
+    a.state_cols = 9
+    assert _plan(lib, a)[0] == -3
+    # wider rows (not the packed row) take the general kernel
+    a = _args(HIST)
+    a.state_cols, a.state_ch_stride = 11, 11
+    assert _plan(lib, a)[1].path == 0
+    # the history layout ignores the window strides; commit rejects the layout
+    a = _args(HIST)
+    a.win_seq_stride = -5
+    assert _plan(lib, a)[0] == 0
+    inp = wl.make_inputs(HIST.replace(n_seq=2, n_pad=0, extra_slots=0))
+    c = cv.make_commit_args(inp["conv_state"], None, inp["accept_len"], layout="history", T=8, width=4,
+                            check_device=False)
+    assert lib.cv_conv_commit(ctypes.byref(c), None) == -8
+    # long T: the general kernel
+    assert _plan(lib, _args(HIST.replace(T=18)))[1].path == 0
+    assert _plan(lib, _args(HIST.replace(T=8, dtype="f32")))[1].path == 3
+
+
 @pytest.mark.parametrize("name,path", [
     ("n1_t2_dim512_w4_f32_dense", 3), ("n4_t4_dim4096_w4_bf16_dedup_bias", 3),
-    ("n8_t17_dim8192_w4_bf16_dense_qkvsplit_xstride12288", 3), ("n64_t8_dim6144_w3_bf16_dense_nol2_stateoff", 1)])
+    ("n8_t17_dim8192_w4_bf16_dense_qkvsplit_xstride12288", 3), ("n64_t8_dim6144_w3_bf16_dense_nol2_stateoff", 1),
+    ("n128_t8_dim10240_w4_bf16_history_pad13", 3)])
 def test_plan_paths_of_named_workloads(lib, name, path):
     w = wl.WORKLOADS[name]
     rc, pl = _plan(lib, _args(w))
@@ -92,6 +133,18 @@ def test_plan_paths_of_named_workloads(lib, name, path):
         assert pl.grid_y == w.n_seq and pl.grid_x * pl.channels_per_block >= w.dim
     # small batches are split into at least two units per SM where the L2 groups allow it
     assert units >= 2 * 152 or pl.threads == 32 or pl.channels_per_block // 2 < max(w.head_dim, 8)
+
+
+def test_plan_sequence_list_only_with_cache_indices(lib):
+    """The pipelined kernel lists the active sequences in shared memory when there are cache
+    indices (and at most 1024 sequences); without indices every sequence is active."""
+    a = _args(W3)
+    base = _plan(lib, a)[1].smem_bytes
+    a.cache_idx = None
+    assert _plan(lib, a)[1].smem_bytes == base - 16 - 4 * 128
+    a = _args(W3.replace(n_seq=1025, n_pad=0))
+    pl = _plan(lib, a)[1]
+    assert pl.path == 3 and pl.smem_bytes == base - 16 - 4 * 128
 
 
 def test_plan_general_path_cases(lib):
@@ -117,7 +170,7 @@ def test_plan_general_path_cases(lib):
 
 @pytest.mark.parametrize("field,value,status", [
     ("dtype", 7, -6), ("width", 1, -5), ("width", 5, -5), ("T", 0, -4), ("T", 129, -4), ("n_seq", -1, -3),
-    ("n_seq", 65536, -3), ("dim", 0, -3), ("n_slots", 0, -3), ("state_cols", 2, -3), ("window_layout", 3, -8),
+    ("n_seq", 65536, -3), ("dim", 0, -3), ("n_slots", 0, -3), ("state_cols", 2, -3), ("window_layout", 4, -8), ("window_layout", 3, -3),
     ("win_step_stride", 5, -8), ("qk_channels", 10240 + 128, -7), ("head_dim", 96, -7), ("head_dim", 4, -7),
     ("head_dim", 512, -7), ("qk_channels", 4000, -7), ("x_tok_stride", -1, -9), ("state_ch_stride", 2, -9),
     ("x", None, -2), ("weight", None, -2), ("window", None, -2),

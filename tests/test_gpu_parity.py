@@ -21,10 +21,11 @@ def check_verify_and_commit(cv, w: wl.VerifyWorkload, inp: dict, commit=True):
     ref = run_oracle_verify(w, inp)
     got = run_gpu_verify(cv, w, inp)
     assert_bits_equal(got["err"].cpu(), ref["status"], "err")
-    assert_bits_equal(got["window"].cpu(), ref["window"], "window")
+    if w.layout != "history":
+        assert_bits_equal(got["window"].cpu(), ref["window"], "window")
     assert_bits_equal(got["conv_state"].cpu(), ref["conv_state"], "state")
     assert_out_close(got["out"].cpu(), ref["out"], "out")
-    if commit:
+    if commit and w.layout != "history":  # the history layout has nothing to commit
         st_ref = run_oracle_commit(w, ref)
         st_got = run_gpu_commit(cv, w, got)
         assert_bits_equal(st_got.cpu(), st_ref, "commit err")
@@ -34,7 +35,7 @@ def check_verify_and_commit(cv, w: wl.VerifyWorkload, inp: dict, commit=True):
 
 @pytest.mark.parametrize("name", wl.WORKLOAD_ORDER)
 def test_named_workloads(cuda_lib, name):
-    """All five named workloads at full size, in the launch configuration the bench times."""
+    """All named workloads at full size, in the launch configuration the bench times."""
     w = wl.WORKLOADS[name]
     check_verify_and_commit(cuda_lib, w, wl.make_inputs(w))
 
@@ -295,3 +296,49 @@ def test_all_paths_bit_identical(cuda_lib, layout, dtype):
     assert_bits_equal(d0["conv_state"].cpu(), ref["conv_state"], "state general")
     assert_bits_equal(d1["conv_state"][:, :, :R].cpu(), ref["conv_state"], "state static")
     assert_bits_equal(d1["conv_state"][:, :, R:].cpu(), wide[:, :, R:], "state static, column past the window")
+
+
+@pytest.mark.parametrize("name", ["n128_t8_dim10240_w4_bf16_dedup_pad13", "n64_t8_dim6144_w3_bf16_dense_nol2_stateoff",
+                                  "n128_t8_dim10240_w4_bf16_history_pad13"])
+def test_chained_steps_without_host_sync(cuda_lib, name):
+    """Three decode steps queued back to back on one stream with no host synchronisation between
+    the launches (each launch may be scheduled while the previous grid finishes): every step's
+    outputs and the final state equal the oracle's three steps, so each kernel still sees all the
+    previous kernel's writes (state rows, snapshots) and none of its reads are overtaken."""
+    import spec_decode_verify_gb300 as cv
+    w = wl.WORKLOADS[name]
+    steps = [wl.make_inputs(w, seed=w.seed + 31 * i) for i in range(3)]
+    base = steps[0]
+    hist = w.layout == "history"
+    # oracle chain
+    ref = clone_inputs(base)
+    outs_ref = []
+    for i, si in enumerate(steps):
+        ref.update(x=si["x"], x_base=si["x_base"], out=wl.sentinel_tensor(si["out"].shape, w.torch_dtype))
+        if i > 0 and hist:
+            ref["state_off"] = (steps[i - 1]["accept_len"] - 1).to(torch.int32)
+        ref = run_oracle_verify(w, ref)
+        if not hist:
+            run_oracle_commit(w, ref, accept_len=si["accept_len"])
+        outs_ref.append(ref["out"].clone())
+    # GPU chain: every input staged on the device first, then all launches without a sync
+    dev = torch.device("cuda")
+    state = base["conv_state"].to(dev)
+    weight, bias = base["weight"].to(dev), (base["bias"].to(dev) if base["bias"] is not None else None)
+    cidx = base["cache_idx"].to(dev)
+    xs = [si["x_base"].to(dev).as_strided(si["x"].shape, si["x"].stride(), si["x"].storage_offset()) for si in steps]
+    accs = [si["accept_len"].to(dev) for si in steps]
+    offs = [base["state_off"].to(dev) if base["state_off"] is not None else None]
+    offs += [(steps[i - 1]["accept_len"] - 1).to(torch.int32).to(dev) if hist else offs[0] for i in (1, 2)]
+    outs = [base["out"].to(dev) for _ in steps]
+    win = base["window"].to(dev) if not hist else None
+    torch.cuda.synchronize()
+    for i in range(3):
+        cv.conv_verify(xs[i], state, weight, bias, outs[i], win, layout=w.layout, qk_channels=w.qk_channels,
+                       head_dim=w.head_dim, l2_eps=w.l2_eps, cache_idx=cidx, state_off=offs[i])
+        if not hist:
+            cv.conv_commit(state, win, accs[i], layout=w.layout, T=w.T, width=w.width, cache_idx=cidx)
+    torch.cuda.synchronize()
+    for i in range(3):
+        assert_out_close(outs[i].cpu(), outs_ref[i], f"step {i} out")
+    assert_bits_equal(state.cpu(), ref["conv_state"], "state after three steps")
