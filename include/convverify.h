@@ -6,18 +6,19 @@
  * snapshot of the conv window; one commit call later restores the state of the accepted prefix.
  *
  * Sources (the pages this library follows):
- *   [atlas-batched]  Atlas spark_model API doc, fn gdn_verify_fused_conv_kn_batched: all K draft
- *                    positions in one launch, every per-token snapshot written inline to a strided
- *                    intermediates array, conv_state left holding the committed window, batched
- *                    over n_seq with per-sequence strides, bit-identical to n separate calls.
+ *   [atlas-batched]  Atlas spark_model API doc, fn gdn_verify_fused_conv_kn_batched: one launch
+ *                    covers the K draft positions, the kernel itself stores each position's
+ *                    rollback snapshot into a strided buffer, the state ends on the committed
+ *                    window, and the batch over n_seq (per-sequence strides) matches n separate
+ *                    calls bit for bit.
  *   [sglang-46184]   sglang pull request #46184 (dedup conv window tile store), sections
  *                    "Motivation" and "Modifications": the deduplicated [dim, T+K-2] window row
  *                    seen as an overlapping [T, dim, K-1] view whose step stride equals its
- *                    column stride; step t's window is columns t..t+2 of
- *                    [state[1], state[2], x_0 .. x_{T-1}]; padded rows exit before any store; a
- *                    num_accept_tokens state offset.
- *   [kda-mod]        Atlas spark_model/layers/glm5next_kda/mod.rs: conv1d + SiLU, then L2 of the
- *                    q|k channels only (V never), eps inside the square root; decode_k snapshot
+ *                    column stride; the window of step t starts at column t of the row that
+ *                    follows the first committed column with x_0 .. x_{T-1}; padded rows store
+ *                    nothing; the tests cover an accepted-token offset into the state.
+ *   [kda-mod]        Atlas spark_model/layers/glm5next_kda/mod.rs: conv1d with SiLU, then an L2
+ *                    normalisation of the q|k channels alone (V untouched), eps under the root; decode_k snapshot
  *                    t = state after row t, which a partial accept rewinds to.
  *
  * Conventions for every entry point:
@@ -109,15 +110,15 @@ enum {
  * c, let o = state_off ? state_off[s] : 0 and
  *     full = [conv_state[slot][c][o .. o+W-2], x[s][0][c], ..., x[s][T-1][c]]     (W-1+T values)
  * Then for every token t:
- *     acc   = bias[c] (or 0) + sum_{j=0}^{W-1} weight[c][j] * full[t+j]   fp32, bias first, then the
- *                                                                         taps in order as fused
- *                                                                         multiply-adds
+ *     acc   = bias[c] (or 0) + sum_{j=0}^{W-1} weight[c][j] * full[t+j]   fp32, bias first, taps in
+ *                                                                         order, each product
+ *                                                                         rounded (exact for bf16)
  *     y     = acc / (1 + exp(-acc))                                      SiLU [kda-mod]
  *     for c < qk_channels: y *= 1/sqrt(sum over c's head_dim group of y^2 + l2_eps)   [kda-mod]
  *     out[s][t][c] = y rounded once to dtype
- *                    (the outputs match the plain definition -- each product rounded, exact
- *                    exp, sqrt and division -- to within 1e-5 relative (+1e-7) in fp32 and 2 ulp
- *                    in bf16; they are identical for every launch path and batch split)
+ *                    (SiLU and the normalisation use fast hardware approximations: the outputs
+ *                    match the exact expressions to within 1e-5 relative (+1e-7) in fp32 and
+ *                    2 ulp in bf16, and are identical for every launch path and batch split)
  *     snapshot (s, t, c, k) = full[t+1+k], k < W-1      raw bit copy, dense or dedup layout
  * and finally conv_state[slot][c][0 .. W-2] = full[T .. T+W-2] (the committed window, equal to
  * snapshot T-1); state columns >= W-1 are not touched.  In the CV_WINDOW_HISTORY layout the
@@ -176,7 +177,7 @@ CV_API int cv_conv_verify(const cv_verify_args *args, void *stream);
 
 /*
  * cv_conv_commit -- restore the state of the accepted prefix ([sglang-46184] "Motivation": the
- * window lets the conv state of the accepted prefix be restored after verify; [kda-mod] decode_k:
+ * window exists so the state can be rolled back to the accepted prefix; [kda-mod] decode_k:
  * snapshot t is the state after row t, which a partial accept rewinds to).
  *
  * For every sequence s with slot = cache_idx ? cache_idx[s] : s, slot >= 0, and a = accept_len[s]

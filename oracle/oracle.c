@@ -7,27 +7,29 @@
  *
  * What it computes, with the passages it follows:
  *
- *   - Causal depthwise conv1d update over T draft tokens (sglang PR #46184, "Motivation": verify
- *     calls causal_conv1d_update with an intermediate conv window; Atlas fn
- *     gdn_verify_fused_conv_kn_batched: all K draft positions in one launch).  For one channel c the
+ *   - Causal depthwise conv1d update over T draft tokens (sglang PR #46184, "Motivation": chain
+ *     verify runs the conv update with an intermediate window; Atlas fn
+ *     gdn_verify_fused_conv_kn_batched: the K draft positions of a batch are handled by a single
+ *     launch).  For one channel c the
  *     sequence is full = [state[o .. o+W-2], x_0 .. x_{T-1}] (W-1 committed inputs, then the T new
  *     ones) and token t sees the W inputs full[t .. t+W-1]:
  *         acc_t = bias[c] + sum_{j=0}^{W-1} w[c][j] * full[t+j]
  *     so w[c][W-1] multiplies the newest input x_t (the textbook causal convolution).  fp32
  *     accumulate, bias first, taps in ascending j, every product rounded before its add (no fused
  *     multiply-add: this file is built with -ffp-contract=off).
- *   - SiLU fused into the conv (glm5next_kda mod.rs, module doc "conv1d + SiLU -> L2(q,k only)"):
+ *   - SiLU fused into the conv (glm5next_kda mod.rs, module doc: the decode conv is followed by
+ *     SiLU and then by an L2 normalisation of q and k alone):
  *         y_t = acc_t / (1 + exp(-acc_t))            in fp32.
  *   - L2 normalisation of the q|k channels only, per head_dim group, exactly once, V never
- *     (mod.rs "Decode conv fuses L2 ... q/k are normalised exactly once; V never"), with the
- *     eps inside the square root (mod.rs Glm5NextKdaConfig::l2_eps: "1/sqrt(sum + eps), not
- *     max(norm, eps)"):
+ *     (mod.rs module doc: the decode conv applies the normalisation to q and k a single time and
+ *     leaves V alone), with the eps inside the square root (mod.rs Glm5NextKdaConfig::l2_eps: eps
+ *     is added to the sum of squares under the root, it is not a floor on the norm):
  *         y_t[c] *= 1 / sqrt(sum_{c' in group(c)} y_t[c']^2 + eps)     for c < qk_channels.
  *     The sum runs over the group's channels in ascending order.  The result is rounded once to
  *     the output type (round to nearest even for bf16).
- *   - Per-token rollback snapshots (Atlas fn gdn_verify_fused_conv_kn_batched: "every per-token
- *     conv-state rollback snapshot written inline"; mod.rs decode_k: snapshot t is the state AFTER
- *     row t).  Snapshot t of channel c is the committed window after token t, full[t+1 .. t+W-1],
+ *   - Per-token rollback snapshots (Atlas fn gdn_verify_fused_conv_kn_batched: the kernel also
+ *     stores, for each draft token, the conv state a rollback would return to; mod.rs decode_k:
+ *     snapshot t is the state AFTER row t).  Snapshot t of channel c is the committed window after token t, full[t+1 .. t+W-1],
  *     copied as raw bits.  Dense layout: element (s, t, c, k) at
  *         s*seq + t*step + c*ch + k*col.
  *     Deduplicated layout (sglang PR #46184, "Motivation" and "Modifications"): one
@@ -36,22 +38,24 @@
  *     oracle writes every (t, k) of the view one by one: this is the per-token store path, which
  *     the PR shows to hit the same addresses with the same values as the row written once.
  *   - The state is left holding the committed window after the last token, full[T .. T+W-2]
- *     (Atlas fn doc: "conv_state is left holding the committed (post final-position) window"),
+ *     (Atlas fn doc: after the call the state holds the window past the final draft position),
  *     written to state columns [0, W-1).  Columns at and above W-1 are not touched.
- *   - Padded sequences (cache index < 0) touch nothing (PR #46184: "Padded rows still exit before
- *     any store").
+ *   - Padded sequences (cache index < 0) touch nothing (PR #46184, "Modifications": padded rows
+ *     leave the kernel before storing anything).
  *   - An optional per-sequence offset o into the state row says where the committed window is
- *     read (PR #46184 test coverage: "a num_accept_tokens state offset").
+ *     read (PR #46184, "Modifications", test coverage: an offset into the state given by the
+ *     number of accepted tokens).
  *   - History-row state (a reading, not a printed kernel): PR #46184's slots hold one [dim, T+K-2]
- *     window row, and its tests cover "a num_accept_tokens state offset" into the state.  In the
+ *     window row, and its tests cover an accepted-token offset into the state.  In the
  *     history layout the state row itself is that row: the call reads its committed window at
  *     columns [o, o+W-1) and then writes columns [0, T+W-2) of the same row with the row
  *     [full[1 .. W-2], x_0 .. x_{T-1}], through the same per-token view (element (t, k) at column
  *     t+k) the dedup layout uses.  Snapshot a-1 then sits at columns [a-1, a+W-2), so the next
  *     call passes o = a-1 and no commit is needed.  No separate window buffer is written; columns
  *     at and above T+W-2 are not touched.
- *   - Commit: restore the state to the snapshot of the accepted prefix (PR #46184: the window
- *     "lets the conv state of the accepted prefix be restored after verify"; mod.rs decode_k:
+ *   - Commit: restore the state to the snapshot of the accepted prefix (PR #46184, "Motivation":
+ *     the window exists so the state can be rolled back to the accepted prefix after verify;
+ *     mod.rs decode_k:
  *     snapshot t is what a partial accept rewinds to).  With a accepted tokens (1 <= a <= T) the
  *     state becomes snapshot a-1.
  *

@@ -1,7 +1,7 @@
 // Commit kernel: restore the conv state of the accepted prefix from the verify's snapshots.
 //
-// sglang PR #46184 ("Motivation"): the intermediate window lets the conv state of the accepted
-// prefix be restored after verify; glm5next_kda mod.rs decode_k: snapshot t is the state after row
+// sglang PR #46184 ("Motivation"): the intermediate window is kept so the state can be rolled
+// back to the accepted prefix once verify is done; glm5next_kda mod.rs decode_k: snapshot t is the state after row
 // t, which a partial accept rewinds to.  The accept count a = accept_len[s] is read on the device,
 // so no host round trip sits between the accept decision and the restore; the state becomes
 // snapshot a-1.

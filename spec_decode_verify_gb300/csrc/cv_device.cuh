@@ -129,14 +129,16 @@ __device__ __forceinline__ float silu(float a) { return a < -80.0f ? silu_exact(
 __device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
 __device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory"); }
 
-// One token's conv: the bias (or 0) first, then the W taps in order, each a fused multiply-add
-// (one rounding per tap).  Every kernel computes it this way, so all launch paths agree bit for
-// bit; against a definition that rounds each product before its add it differs by a few fp32 ulp,
-// far inside the output tolerance (the snapshots and the state are raw copies and unaffected).
-template <int W>
-__device__ __forceinline__ float conv_fma(float acc, const float *w, const float *in) {
+// One token's conv: the bias (or 0) first, then the W taps in order.  For bf16 elements every
+// product of a tap and an input (8 significant bits each) is exact in fp32, so a fused
+// multiply-add rounds exactly where the separate multiply and add would: the chain costs one
+// instruction per tap and still equals the rounded-product definition bit for bit (a product
+// below 2^-126 could round differently, far outside any real input).  For fp32 elements the
+// product itself is rounded first, as the definition says.
+template <typename B, int W>
+__device__ __forceinline__ float conv_chain(float acc, const float *w, const float *in) {
 #pragma unroll
-    for (int j = 0; j < W; ++j) acc = fmaf(w[j], in[j], acc);
+    for (int j = 0; j < W; ++j) acc = sizeof(B) == 2 ? fmaf(w[j], in[j], acc) : __fadd_rn(acc, __fmul_rn(w[j], in[j]));
     return acc;
 }
 

@@ -8,18 +8,18 @@
 //      thread), taps and bias -- straight into registers;
 //   2. everything that depends on the inputs only is written first, so its registers die early and
 //      its stores overlap the arithmetic:
-//        - deduplicated row (sglang PR #46184: step t's window is columns t..t+W-2 of
-//          [state[1..W-2], x_0..x_{T-1}]): each thread assembles its CPT channels x (T+W-2)
+//        - deduplicated row (sglang PR #46184: the W-1 columns from column t of
+//          [state[1..W-2], x_0..x_{T-1}] form the window of step t): each thread assembles its CPT channels x (T+W-2)
 //          columns in registers by a static permutation and stages them in shared memory; ONE bulk
 //          copy (TMA, cp.async.bulk) then writes the block's channels*(T+W-2) contiguous elements,
 //          instead of W-1 scattered stores per token;
 //        - dense snapshots: the thread's CPT x (W-1) run per token as vector stores;
 //        - committed window (= snapshot T-1) -> state columns [0, W-1), staged and bulk-copied
 //          when the state rows are packed;
-//   3. conv (fp32, bias first, taps in order as fused multiply-adds), SiLU, and for
+//   3. conv (fp32, bias first, taps in order, see conv_chain), SiLU, and for
 //      q|k channels the L2 normalisation over the head_dim group as an xor-shuffle over
-//      head_dim/CPT lanes (glm5next_kda mod.rs: conv1d + SiLU -> L2(q,k only), eps inside the
-//      root); one rounding to the output type; vector stores.
+//      head_dim/CPT lanes (glm5next_kda mod.rs: SiLU after the conv, then L2 on q and k alone,
+//      eps inside the root); one rounding to the output type; vector stores.
 // T is a template parameter for T <= 17 (bf16) / 8 (fp32), which unrolls the token loop and makes
 // the row permutation static; TS = 0 runs any T with a dense window in unrolled chunks of 4.
 // Preconditions (checked on the host): dim % 8 == 0; x, out, weight, bias, window 16-byte aligned
@@ -158,7 +158,7 @@ __global__ void __launch_bounds__(256) verify_fast(const __grid_constant__ Verif
         float acc[CPT];
 #pragma unroll
         for (int e = 0; e < CPT; ++e) {
-            acc[e] = conv_fma<W>(bs[e], wt[e], &fw[e][u]);
+            acc[e] = conv_chain<B, W>(bs[e], wt[e], &fw[e][u]);
         }
         silu_run<CPT>(acc, yu);
     };

@@ -8,7 +8,7 @@
 //     tile[j][c] = full_c[j],  j in [0, W-1+T)   (rows 0..W-2: committed window, then x_0..x_{T-1})
 // and every snapshot layout and the committed window are written from that tile in destination
 // order (channel-major runs, channel-stride-1 runs, or element by element).  The arithmetic is the
-// same as the fast path's: fp32, bias first, taps in order as fused multiply-adds, SiLU, L2
+// same as the fast path's: fp32, bias first, taps in order (conv_chain), SiLU, L2
 // over the head_dim group as an xor-shuffle over head_dim/8 lanes.
 #pragma once
 
@@ -262,11 +262,12 @@ __global__ void __launch_bounds__(256) verify_generic(const __grid_constant__ Ve
         float y[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
-            // the same fused multiply-add chain as conv_fma (bias, then the taps in order)
-            float acc = has_bias ? bs[e] : 0.0f;
+            // the same chain as conv_chain: bias, then the taps in order
+            float in[W];
 #pragma unroll
-            for (int j = 0; j < R; ++j) acc = fmaf(wt[e][j], win[j][e], acc);
-            acc = fmaf(wt[e][R], xv[e], acc);
+            for (int j = 0; j < R; ++j) in[j] = win[j][e];
+            in[R] = xv[e];
+            const float acc = conv_chain<B, W>(has_bias ? bs[e] : 0.0f, wt[e], in);
             y[e] = silu(acc);
         }
 #pragma unroll

@@ -10,11 +10,12 @@
 // the current one on every SM, instead of all blocks loading, then computing, then storing in
 // lock-step.  The staged images are double-buffered too, so one block barrier per unit suffices.
 // Per unit each thread moves its CPT channels from the stage to registers, writes what depends on
-// the inputs only (the deduplicated row of sglang PR #46184 -- step t's window is columns
-// t..t+W-2 of [state[1..W-2], x_0..x_{T-1}] -- as one staged image written by one bulk copy;
+// the inputs only (the deduplicated row of sglang PR #46184 -- the window of step t is the W-1
+// columns from column t of [state[1..W-2], x_0..x_{T-1}] -- as one staged image written by one
+// bulk copy;
 // dense snapshots as vector stores; the committed window, staged and bulk-copied into the packed
-// state rows) and computes the outputs: fp32 conv with bias first and the taps as fused
-// multiply-adds, SiLU, the L2 normalisation of the q|k groups over head_dim/CPT lanes with the T
+// state rows) and computes the outputs: fp32 conv with bias first and the taps in order
+// (conv_chain), SiLU, the L2 normalisation of the q|k groups over head_dim/CPT lanes with the T
 // shuffle trees interleaved (glm5next_kda mod.rs), one rounding, vector stores.
 // Every mbarrier wait is bounded: a block that waits too long sets CV_SEQ_TIMEOUT in err (when
 // given) for the unit's sequence, drains its copies in flight (again bounded) and returns.
@@ -334,7 +335,7 @@ __global__ void __launch_bounds__(128, (CPT == 4 && TS <= 8) ? 4 : 2) verify_pip
                     for (int e = 0; e < CPT; ++e) fw[e][R + t] = elem_f<B>(xr[t], e);
 #pragma unroll
                     for (int e = 0; e < CPT; ++e) {
-                        const float acc = conv_fma<W>(bs[e], wt[e], &fw[e][t]);
+                        const float acc = conv_chain<B, W>(bs[e], wt[e], &fw[e][t]);
                         y[t][e] = silu_fast(acc);
                         lo = fminf(lo, acc);
                     }
@@ -344,7 +345,7 @@ __global__ void __launch_bounds__(128, (CPT == 4 && TS <= 8) ? 4 : 2) verify_pip
                     for (int t = 0; t < TS; ++t)
 #pragma unroll
                         for (int e = 0; e < CPT; ++e) {
-                            y[t][e] = silu_exact(conv_fma<W>(bs[e], wt[e], &fw[e][t]));
+                            y[t][e] = silu_exact(conv_chain<B, W>(bs[e], wt[e], &fw[e][t]));
                         }
                 }
             } else {

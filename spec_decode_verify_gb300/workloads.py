@@ -9,7 +9,8 @@ The five named workloads follow the shapes the pages describe:
     bf16, T 8, batch 128) with the deduplicated window layout of MambaPool ("Motivation");
   * the Atlas batched verify (fn gdn_verify_fused_conv_kn_batched: K draft positions, strided
     input/output rows, dense intermediates) with the q|k|v conv weights bound as
-    concat([q, k, v]) (glm5next_kda mod.rs, "The checkpoint SPLITS the conv");
+    concat([q, k, v]) (glm5next_kda mod.rs: the checkpoint stores the q, k and v conv weights
+    as separate tensors);
   * a width-3 conv without L2 groups and with a per-sequence accepted-token state offset (PR
     #46184's tests cover an offset of the accepted-token count into the state; its "Scope" names
     width-3 deduplicated windows);

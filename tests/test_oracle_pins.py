@@ -434,8 +434,9 @@ def _read_golden(name):
 
 
 def test_golden_dedup_row_columns():
-    """The page's printed row layout (tests/golden/dedup_row_columns.txt): step t's window is columns
-    t..t+2 of [state[1], state[2], x_0, ..., x_{T-1}], T+2 columns, for the T values it tests."""
+    """The page's printed row layout (tests/golden/dedup_row_columns.txt): the row is the committed
+    window without its oldest column followed by x_0 .. x_{T-1} (T+2 columns for width 4), and the
+    window of step t is its 3 columns from column t, for the T values the page tests."""
     for line in _read_golden("dedup_row_columns.txt"):
         T_s, cols = line.split(":")
         T = int(T_s)
