@@ -34,7 +34,7 @@ class _VerifyArgs(ctypes.Structure):
         ("state", c_vp), ("n_slots", c_i32), ("state_cols", c_i32), ("st_slot", c_i64), ("st_ch", c_i64),
         ("cache_idx", c_vp), ("state_off", c_vp), ("weight", c_vp), ("bias", c_vp),
         ("window", c_vp), ("dedup", c_i32), ("w_seq", c_i64), ("w_step", c_i64), ("w_ch", c_i64),
-        ("w_col", c_i64), ("status", c_vp), ("history", c_i32),
+        ("w_col", c_i64), ("status", c_vp), ("history", c_i32), ("recompute", c_i32),
     ]
 
 
@@ -43,7 +43,8 @@ class _CommitArgs(ctypes.Structure):
         ("n_seq", c_i32), ("T", c_i32), ("dim", c_i32), ("width", c_i32), ("is_bf16", c_i32),
         ("state", c_vp), ("n_slots", c_i32), ("st_slot", c_i64), ("st_ch", c_i64), ("cache_idx", c_vp),
         ("window", c_vp), ("dedup", c_i32), ("w_seq", c_i64), ("w_step", c_i64), ("w_ch", c_i64),
-        ("w_col", c_i64), ("accept_len", c_vp), ("status", c_vp),
+        ("w_col", c_i64), ("accept_len", c_vp), ("status", c_vp), ("recompute", c_i32), ("x", c_vp),
+        ("x_seq", c_i64), ("x_tok", c_i64),
     ]
 
 
@@ -110,8 +111,8 @@ def window_strides(window: torch.Tensor, layout: str):
     """(seq, step, ch, col) element strides of a window buffer.
 
     dense: window is [n_seq, T, dim, W-1].  dedup: window is the [n_seq, dim, T+W-2] row buffer and
-    the step stride equals the column stride.  history: there is no window buffer."""
-    if layout == "history":
+    the step stride equals the column stride.  history, recompute: there is no window buffer."""
+    if layout in ("history", "recompute"):
         return 0, 0, 0, 0
     if layout == "dense":
         s = window.stride()
@@ -127,12 +128,12 @@ def conv_verify(x, conv_state, weight, bias, out, window, *, layout, qk_channels
     x [n_seq, T, dim] (channel stride 1), conv_state [n_slots, dim, S] (column stride 1),
     weight [dim, W] contiguous, bias [dim] or None, out [n_seq, T, dim] (channel stride 1),
     window dense [n_seq, T, dim, W-1] / dedup [n_seq, dim, T+W-2] / None for the history layout
-    (the state row, S >= T+W-2 columns, receives the snapshot row); cache_idx, state_off, status
-    int32 [n_seq] or None."""
-    if layout not in ("dense", "dedup", "history"):
+    (the state row, S >= T+W-2 columns, receives the snapshot row) and the recompute layout
+    (outputs only, state untouched); cache_idx, state_off, status int32 [n_seq] or None."""
+    if layout not in ("dense", "dedup", "history", "recompute"):
         raise ValueError(f"unknown layout {layout!r}")
-    if (layout == "history") != (window is None):
-        raise ValueError("the history layout takes no window buffer; the other layouts need one")
+    if (layout in ("history", "recompute")) != (window is None):
+        raise ValueError("the history and recompute layouts take no window buffer; the others need one")
     n_seq, T, dim = x.shape
     W = weight.shape[1]
     assert x.stride(2) == 1 and out.stride(2) == 1 and conv_state.stride(2) == 1
@@ -145,14 +146,22 @@ def conv_verify(x, conv_state, weight, bias, out, window, *, layout, qk_channels
         state_cols=conv_state.shape[2], st_slot=conv_state.stride(0), st_ch=conv_state.stride(1),
         cache_idx=_ptr(cache_idx), state_off=_ptr(state_off), weight=_ptr(weight), bias=_ptr(bias),
         window=_ptr(window), dedup=1 if layout == "dedup" else 0, w_seq=ws[0], w_step=ws[1], w_ch=ws[2],
-        w_col=ws[3], status=_ptr(status), history=1 if layout == "history" else 0)
+        w_col=ws[3], status=_ptr(status), history=1 if layout == "history" else 0,
+        recompute=1 if layout == "recompute" else 0)
     rc = _load().oracle_conv_verify(ctypes.byref(a))
     if rc != 0:
         raise RuntimeError(f"oracle_conv_verify returned {rc}")
 
 
-def conv_commit(conv_state, window, accept_len, *, layout, T, width, cache_idx=None, status=None):
-    """Run the oracle commit in place: state slot of seq s <- snapshot accept_len[s]-1."""
+def conv_commit(conv_state, window, accept_len, *, layout, T, width, cache_idx=None, status=None, x=None):
+    """Run the oracle commit in place: state slot of seq s <- snapshot accept_len[s]-1.
+
+    layout "recompute": window is None and x [n_seq, T, dim] (channel stride 1) is the verify's
+    input; the snapshot is rebuilt from the state's window and x."""
+    if (layout == "recompute") != (x is not None and window is None):
+        raise ValueError("the recompute commit takes x and no window; the others take a window")
+    if x is not None:
+        assert x.stride(2) == 1
     ws = window_strides(window, layout)
     n_seq = accept_len.shape[0]
     a = _CommitArgs(
@@ -160,7 +169,8 @@ def conv_commit(conv_state, window, accept_len, *, layout, T, width, cache_idx=N
         state=_ptr(conv_state), n_slots=conv_state.shape[0], st_slot=conv_state.stride(0),
         st_ch=conv_state.stride(1), cache_idx=_ptr(cache_idx), window=_ptr(window),
         dedup=1 if layout == "dedup" else 0, w_seq=ws[0], w_step=ws[1], w_ch=ws[2], w_col=ws[3],
-        accept_len=_ptr(accept_len), status=_ptr(status))
+        accept_len=_ptr(accept_len), status=_ptr(status), recompute=1 if layout == "recompute" else 0,
+        x=_ptr(x), x_seq=x.stride(0) if x is not None else 0, x_tok=x.stride(1) if x is not None else 0)
     rc = _load().oracle_conv_commit(ctypes.byref(a))
     if rc != 0:
         raise RuntimeError(f"oracle_conv_commit returned {rc}")

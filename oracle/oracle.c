@@ -53,6 +53,12 @@
  *     t+k) the dedup layout uses.  Snapshot a-1 then sits at columns [a-1, a+W-2), so the next
  *     call passes o = a-1 and no commit is needed.  No separate window buffer is written; columns
  *     at and above T+W-2 are not touched.
+ *   - Recompute rollback (memra-engine Engine doc, ssm_conv_ring_rebuild_dc: the conv state is rebuilt
+ *     from the ring kept from before the verify, the verify's inputs and the device-side accept
+ *     count).  In the recompute layout the verify writes the outputs only: no snapshots, and the
+ *     state keeps the pre-verify window.  The commit then sets state[k] = full[a+k] for k < W-1,
+ *     with full = [state[0 .. W-2], x_0 .. x_{T-1}] read at commit time -- the same value snapshot
+ *     a-1 holds.
  *   - Commit: restore the state to the snapshot of the accepted prefix (PR #46184, "Motivation":
  *     the window exists so the state can be rolled back to the accepted prefix after verify;
  *     mod.rs decode_k:
@@ -86,7 +92,8 @@ typedef struct {
     int32_t dedup;
     int64_t w_seq, w_step, w_ch, w_col;
     int32_t *status; /* [n_seq] or NULL */
-    int32_t history; /* 1: the state row is the snapshot row (no window buffer) */
+    int32_t history;   /* 1: the state row is the snapshot row (no window buffer) */
+    int32_t recompute; /* 1: outputs only; no snapshots and the state is not written */
 } oracle_verify_args;
 
 typedef struct {
@@ -100,6 +107,9 @@ typedef struct {
     int64_t w_seq, w_step, w_ch, w_col;
     const int32_t *accept_len;
     int32_t *status;
+    int32_t recompute; /* 1: rebuild from the state's window and x (no window buffer) */
+    const void *x;
+    int64_t x_seq, x_tok;
 } oracle_commit_args;
 
 /* ---- element access: raw bits, so copies keep NaN payloads and signed zeros ---- */
@@ -175,6 +185,8 @@ int oracle_conv_verify(const oracle_verify_args *a) {
                 y[(int64_t)t * dim + c] = acc / (1.0f + expf(-acc));
             }
 
+            if (a->recompute) continue; /* outputs only: the state keeps the pre-verify window */
+
             if (a->history) {
                 /* snapshot t into the state row itself, at columns t .. t+W-2 (after every read) */
                 for (int t = 0; t < T; ++t)
@@ -214,6 +226,7 @@ int oracle_conv_verify(const oracle_verify_args *a) {
 
 int oracle_conv_commit(const oracle_commit_args *a) {
     const int W = a->width, bf = a->is_bf16;
+    if (a->recompute && W - 1 + a->T > 1024) return -1;
     for (int s = 0; s < a->n_seq; ++s) {
         const int slot = a->cache_idx ? a->cache_idx[s] : s;
         int st = 0;
@@ -223,6 +236,18 @@ int oracle_conv_commit(const oracle_commit_args *a) {
         if (a->status) a->status[s] = st;
         if (slot < 0 || st) continue;
         const int t = acc - 1;
+        if (a->recompute) {
+            for (int c = 0; c < a->dim; ++c) {
+                const int64_t srow = (int64_t)slot * a->st_slot + (int64_t)c * a->st_ch;
+                uint32_t full[1024]; /* W-1 + T raw elements of one channel */
+                for (int k = 0; k < W - 1; ++k) full[k] = get_bits(a->state, bf, srow + k);
+                for (int u = 0; u < a->T; ++u)
+                    full[W - 1 + u] = get_bits(a->x, bf, (int64_t)s * a->x_seq + (int64_t)u * a->x_tok + c);
+                /* snapshot acc-1 = full[acc .. acc+W-2], written after the row's reads */
+                for (int k = 0; k < W - 1; ++k) put_bits(a->state, bf, srow + k, full[acc + k]);
+            }
+            continue;
+        }
         const int64_t step = a->dedup ? a->w_col : a->w_step;
         for (int c = 0; c < a->dim; ++c)
             for (int k = 0; k < W - 1; ++k) {

@@ -14,8 +14,10 @@ The five named workloads follow the shapes the pages describe:
   * a width-3 conv without L2 groups and with a per-sequence accepted-token state offset (PR
     #46184's tests cover an offset of the accepted-token count into the state; its "Scope" names
     width-3 deduplicated windows);
-  * the benchmark shape again with the history-row state: the state row of each slot is the
-    deduplicated [dim, T+W-2] row itself and the committed window is read at accept_len - 1.
+  * the benchmark shape again with the recompute rollback (memra-engine ssm_conv_ring_rebuild_dc:
+    no snapshots; the commit rebuilds the state from the kept window and the accepted inputs) and
+    with the history-row state: the state row of each slot is the deduplicated [dim, T+W-2] row
+    itself and the committed window is read at accept_len - 1.
 Values: x, state ~ N(0, 1), weights ~ U(-0.5, 0.5), bias ~ N(0, 0.1); bf16 values are drawn in
 fp32 and converted by torch (round to nearest even).
 """
@@ -43,7 +45,9 @@ class VerifyWorkload:
     qk_channels: int
     head_dim: int
     dtype: str  # "f32" or "bf16"
-    layout: str  # "dense", "dedup" or "history" (the state row is the dedup row; no window buffer)
+    # "dense", "dedup", "history" (the state row is the dedup row; no window buffer) or "recompute"
+    # (no snapshots; the commit rebuilds the state from the pre-verify window and x)
+    layout: str
     bias: bool = False
     l2_eps: float = 1e-6
     n_pad: int = 0  # sequences whose cache index is -1
@@ -93,6 +97,9 @@ WORKLOADS = {
         VerifyWorkload("n64_t8_dim6144_w3_bf16_dense_nol2_stateoff", n_seq=64, T=8, dim=6144, width=3,
                        qk_channels=0, head_dim=128, dtype="bf16", layout="dense", state_offset=True,
                        seed=4),
+        VerifyWorkload("n128_t8_dim10240_w4_bf16_recompute_pad13", n_seq=128, T=8, dim=10240, width=4,
+                       qk_channels=4096, head_dim=128, dtype="bf16", layout="recompute", n_pad=13,
+                       extra_slots=16, seed=6),
         VerifyWorkload("n128_t8_dim10240_w4_bf16_history_pad13", n_seq=128, T=8, dim=10240, width=4,
                        qk_channels=4096, head_dim=128, dtype="bf16", layout="history", n_pad=13,
                        extra_slots=16, state_offset=True, seed=5),
@@ -114,7 +121,7 @@ def sentinel_tensor(shape, dtype) -> torch.Tensor:
 
 
 def window_shape(w: VerifyWorkload):
-    if w.layout == "history":
+    if w.layout in ("history", "recompute"):
         return None
     if w.layout == "dense":
         return (w.n_seq, w.T, w.dim, w.width - 1)
@@ -128,7 +135,7 @@ def make_inputs(w: VerifyWorkload, seed: Optional[int] = None) -> dict:
     [n_slots, dim, state_cols], weight [dim, W], bias [dim] or None, cache_idx int32 [n_seq]
     (-1 = padded), state_off int32 [n_seq] or None, accept_len int32 [n_seq] in 1..T, and
     sentinel-filled out [n_seq, T, dim] and window buffers (dense [n_seq, T, dim, W-1], dedup
-    [n_seq, dim, T+W-2], None for the history layout).
+    [n_seq, dim, T+W-2], None for the history and recompute layouts).
     """
     rng = np.random.default_rng(w.seed if seed is None else seed)
     dt = w.torch_dtype
@@ -152,7 +159,7 @@ def make_inputs(w: VerifyWorkload, seed: Optional[int] = None) -> dict:
     accept = torch.from_numpy(rng.integers(1, w.T + 1, size=w.n_seq).astype(np.int32))
     state_off = (accept - 1).to(torch.int32) if w.state_offset else None
     out = sentinel_tensor((w.n_seq, w.T, w.dim), dt)
-    window = None if w.layout == "history" else sentinel_tensor(window_shape(w), dt)
+    window = None if w.layout in ("history", "recompute") else sentinel_tensor(window_shape(w), dt)
     return dict(x=x, x_base=x_wide, conv_state=state, weight=weight, bias=bias, cache_idx=cache_idx,
                 state_off=state_off, accept_len=accept, out=out, window=window)
 
@@ -183,6 +190,12 @@ def algorithmic_bytes(w: VerifyWorkload, n_active: Optional[int] = None) -> dict
         # committed window read; the snapshot row written into the state row; nothing to commit
         per_seq = (w.T * w.dim + (w.width - 1) * w.dim + w.T * w.dim + (w.T + w.width - 2) * w.dim) * e
         return dict(verify=n * per_seq + shared, commit=0, per_seq=per_seq)
+    if w.layout == "recompute":
+        # verify: x and committed window read, outputs written; commit: the window and the accepted
+        # x rows (at most W-1 of them, counted as W-1) read, the window written
+        per_seq = (w.T * w.dim + (w.width - 1) * w.dim + w.T * w.dim) * e
+        commit = n * 3 * (w.width - 1) * w.dim * e + 8 * w.n_seq
+        return dict(verify=n * per_seq + shared, commit=commit, per_seq=per_seq)
     win_cols = (w.T + w.width - 2) if w.layout == "dedup" else w.T * (w.width - 1)
     per_seq = (w.T * w.dim + (w.width - 1) * w.dim + w.T * w.dim + win_cols * w.dim + (w.width - 1) * w.dim) * e
     commit = n * 2 * (w.width - 1) * w.dim * e + 8 * w.n_seq

@@ -94,5 +94,6 @@ def run_oracle_commit(w: wl.VerifyWorkload, r: dict, accept_len=None) -> torch.T
     """Oracle commit in place on ``r`` (the result of run_oracle_verify); returns the status."""
     st = torch.full((w.n_seq,), -7, dtype=torch.int32)
     oracle.conv_commit(r["conv_state"], r["window"], r["accept_len"] if accept_len is None else accept_len,
-                       layout=w.layout, T=w.T, width=w.width, cache_idx=r["cache_idx"], status=st)
+                       layout=w.layout, T=w.T, width=w.width, cache_idx=r["cache_idx"], status=st,
+                       x=r["x"] if w.layout == "recompute" else None)
     return st

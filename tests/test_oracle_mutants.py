@@ -43,6 +43,12 @@ MUTANTS = [
     ("history_row_last_window_only", "for (int t = 0; t < T; ++t)\n                    for (int k = 0; k < W - 1; ++k) put_bits(a->state",
      "for (int t = T - 1; t < T; ++t)\n                    for (int k = 0; k < W - 1; ++k) put_bits(a->state",
      lambda: pins.test_h2_history_chain_equals_verify_commit_chain()),
+    ("recompute_wrong_snapshot", "put_bits(a->state, bf, srow + k, full[acc + k]);",
+     "put_bits(a->state, bf, srow + k, full[acc - 1 + k]);",
+     lambda: pins.test_r3_recompute_commit_closed_form()),
+    ("recompute_verify_writes_state", "if (a->recompute) continue; /* outputs only",
+     "if (a->recompute) { put_bits(a->state, bf, srow, full[T]); continue; } /* outputs only",
+     lambda: pins.test_r1_recompute_verify_writes_outputs_only(3, "f32")),
     ("padded_row_written", "if (slot < 0 || st) continue;\n\n", "if (st) continue;\n        if (slot < 0) { if (a->out) put_bits(a->out, bf, (int64_t)s * a->out_seq, 0); continue; }\n\n",
      lambda: pins.test_p7_padded_rows_untouched()),
 ]

@@ -393,6 +393,59 @@ def test_h3_history_sequential_single_tokens():
         assert_bits_equal(st[slot], whole["conv_state"][slot, :, T - 1:T - 1 + R], f"seq {s} final window")
 
 
+@pytest.mark.parametrize("width", [2, 3, 4])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_r1_recompute_verify_writes_outputs_only(width, dtype):
+    """Recompute layout (memra-engine ssm_conv_ring_rebuild_dc keeps the pre-verify ring): the
+    outputs equal the dense layout's bitwise, and no state element changes."""
+    wr = small(n_seq=4, T=6, width=width, dtype=dtype, layout="recompute", n_pad=1, extra_slots=2, seed=41)
+    inp = wl.make_inputs(wr)
+    assert inp["window"] is None
+    rr = run_oracle_verify(wr, inp)
+    wd = wr.replace(layout="dense")
+    idn = clone_inputs(inp)
+    idn["window"] = wl.sentinel_tensor(wl.window_shape(wd), wd.torch_dtype)
+    rd = run_oracle_verify(wd, idn)
+    assert_bits_equal(rr["out"], rd["out"], "out")
+    assert_bits_equal(rr["conv_state"], inp["conv_state"], "state untouched")
+    assert_bits_equal(rr["status"], rd["status"], "status")
+
+
+@pytest.mark.parametrize("layout", ["dense", "dedup"])
+def test_r2_recompute_commit_equals_snapshot_commit(layout):
+    """For every accept count a in 1..T, the rebuilt state equals the state the snapshot path
+    commits (P-9 pins that one to a shorter verify), bitwise; padded and unused slots untouched."""
+    T = 7
+    wr = small(n_seq=T + 1, T=T, width=4, dtype="bf16", layout="recompute", n_pad=1, extra_slots=2, seed=43)
+    inp = wl.make_inputs(wr)
+    inp["accept_len"] = torch.tensor([1 + s % T for s in range(wr.n_seq)], dtype=torch.int32)
+    rr = run_oracle_verify(wr, inp)
+    assert (run_oracle_commit(wr, rr) == 0).all()
+    wd = wr.replace(layout=layout)
+    idn = clone_inputs(inp)
+    idn["window"] = wl.sentinel_tensor(wl.window_shape(wd), wd.torch_dtype)
+    rd = run_oracle_verify(wd, idn)
+    assert (run_oracle_commit(wd, rd) == 0).all()
+    assert_bits_equal(rr["conv_state"], rd["conv_state"], "rebuilt state")
+
+
+def test_r3_recompute_commit_closed_form():
+    """Closed form: with a >= W-1 the rebuilt window is x_{a-W+1} .. x_{a-1} (inputs only); with
+    a < W-1 it is the old window shifted left by a, then x_0 .. x_{a-1}."""
+    W, T = 4, 5
+    wr = small(n_seq=T, T=T, width=W, dtype="f32", layout="recompute", seed=47)
+    inp = wl.make_inputs(wr)
+    inp["accept_len"] = torch.arange(1, T + 1, dtype=torch.int32)
+    rr = run_oracle_verify(wr, inp)
+    run_oracle_commit(wr, rr)
+    for s in range(wr.n_seq):
+        slot, a = int(inp["cache_idx"][s]), int(inp["accept_len"][s])
+        old = inp["conv_state"][slot]           # [dim, W-1]
+        xs = inp["x"][s].t()                    # [dim, T]
+        want = xs[:, a - (W - 1):a] if a >= W - 1 else torch.cat([old[:, a:], xs[:, :a]], dim=1)
+        assert_bits_equal(rr["conv_state"][slot], want.contiguous(), f"seq {s} a {a}")
+
+
 def test_p11_single_token_update():
     """P-11: T = 1 is the standard single-token causal conv update: the state shifts left by one
     and takes x; out = SiLU(sum_j w_j [state, x]_j + bias)."""
