@@ -4,7 +4,8 @@
 
 A step is one pass of the whole path over one batch: cv_conv_verify (conv + SiLU + L2, snapshots,
 committed window) followed by cv_conv_commit (restore the accepted prefix); with the history-row
-state layout the step is the verify alone (the next verify reads at accept_len - 1).  Default workload: 128
+state layout the step is the verify alone (the next verify reads at accept_len - 1), and with the
+recompute rollback the verify writes outputs only and the commit rebuilds the state from x.  Default workload: 128
 sequences x 8 draft tokens, dim 10240 (q|k 4096, head_dim 128), conv width 4, bf16, deduplicated
 window rows, 13 padded sequences.  Inputs are synthetic and already resident in HBM when the
 timed region starts; every step uses the next of several rotating buffer sets whose total size is
@@ -182,7 +183,7 @@ def oracle_step_times(w, reps_max: int, budget_s: float):
                            cache_idx=inp["cache_idx"], state_off=inp["state_off"])
         if w.layout != "history":
             oracle.conv_commit(state, win, inp["accept_len"], layout=w.layout, T=w.T, width=w.width,
-                               cache_idx=inp["cache_idx"])
+                               cache_idx=inp["cache_idx"], x=inp["x"] if w.layout == "recompute" else None)
         times.append(time.perf_counter() - t0)
         if time.perf_counter() - t_begin > budget_s and len(times) >= 3:
             break
@@ -252,13 +253,15 @@ def run_ours(args, w, world, rank, local, dist):
         xb = inp["x_base"].to(dev)
         x = xb.as_strided(inp["x"].shape, inp["x"].stride(), inp["x"].storage_offset())
         s = dict(x_base=xb, x=x, conv_state=inp["conv_state"].to(dev), out=inp["out"].to(dev),
-                 window=inp["window"].to(dev) if has_commit else None, accept=inp["accept_len"].to(dev))
+                 window=inp["window"].to(dev) if inp["window"] is not None else None,
+                 accept=inp["accept_len"].to(dev))
         s["va"] = cv.make_verify_args(x, s["conv_state"], weight, bias, s["out"], s["window"], layout=w.layout,
                                       qk_channels=w.qk_channels, head_dim=w.head_dim, l2_eps=w.l2_eps,
                                       cache_idx=cache_idx, state_off=state_off)
         if has_commit:
             s["ca"] = cv.make_commit_args(s["conv_state"], s["window"], s["accept"], layout=w.layout, T=w.T,
-                                          width=w.width, cache_idx=cache_idx)
+                                          width=w.width, cache_idx=cache_idx,
+                                          x=x if w.layout == "recompute" else None)
         sets.append(s)
     verify_fn, lib_commit = lib.cv_conv_verify, lib.cv_conv_commit
     vrefs = [ctypes.byref(s["va"]) for s in sets]

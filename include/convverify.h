@@ -48,7 +48,7 @@ extern "C" {
 #define CV_API
 #endif
 
-#define CV_ABI_VERSION 1
+#define CV_ABI_VERSION 2
 #define CV_MAX_T 128 /* draft tokens per verify call */
 
 typedef enum cv_dtype {
@@ -73,7 +73,13 @@ typedef enum cv_window_layout {
        [sglang-46184] slot row together with its accepted-token state offset).  Needs
        state_cols >= T+W-2; columns at and above T+W-2 are not touched.  cv_conv_commit rejects
        this layout. */
-    CV_WINDOW_HISTORY = 3
+    CV_WINDOW_HISTORY = 3,
+    /* recompute rollback ([memra-engine] ssm_conv_ring_rebuild_dc): no window buffer (window may
+       be NULL; the win_* strides are ignored).  The verify writes the outputs only -- no
+       snapshots, and conv_state is not written, so it keeps the pre-verify window.  The matching
+       cv_conv_commit (same layout) then rebuilds the state from that window and the verify's x:
+       conv_state[slot][c][k] = full[a+k], the value snapshot a-1 would hold. */
+    CV_WINDOW_RECOMPUTE = 4
 } cv_window_layout;
 
 /* Status codes returned by the entry points. */
@@ -123,7 +129,8 @@ enum {
  * and finally conv_state[slot][c][0 .. W-2] = full[T .. T+W-2] (the committed window, equal to
  * snapshot T-1); state columns >= W-1 are not touched.  In the CV_WINDOW_HISTORY layout the
  * snapshots go into the state row instead (columns [0, T+W-2), see the layout) and no window
- * buffer is written.  A sequence with slot < 0 is padding: its
+ * buffer is written; in the CV_WINDOW_RECOMPUTE layout neither snapshots nor the state are
+ * written.  A sequence with slot < 0 is padding: its
  * out rows, window rows and every state slot are left untouched ([sglang-46184]).
  *
  * Arguments (all in cv_verify_args):
@@ -144,7 +151,7 @@ enum {
  *   weight             [dim][W] contiguous, read-only; weight[c][W-1] multiplies the newest input
  *   bias               [dim] read-only, or NULL
  *   window             snapshot buffer, write-only, laid out as window_layout says (NULL allowed
- *                      and ignored for CV_WINDOW_HISTORY)
+ *                      and ignored for CV_WINDOW_HISTORY and CV_WINDOW_RECOMPUTE)
  *   err                int32 [n_seq] device array or NULL: receives the CV_SEQ_* bits of each
  *                      sequence (0 for fine and for padded sequences)
  * Preconditions the library cannot check: distinct sequences use distinct slots; out and window do
@@ -186,6 +193,13 @@ CV_API int cv_conv_verify(const cv_verify_args *args, void *stream);
  * a = T rewrites the state with the value it already holds.  A sequence whose a is out of range
  * gets CV_SEQ_BAD_ACCEPT in err[s] and is untouched.  The window must be the one the matching
  * cv_conv_verify wrote (same layout and strides).
+ *
+ * CV_WINDOW_RECOMPUTE: there is no window; x (with x_seq_stride, x_tok_stride, channel stride 1)
+ * must be the input of the matching verify, unchanged since, and the state still holds the
+ * pre-verify window in columns [0, W-1) (the verify leaves it alone in this layout).  With
+ * full = [conv_state[slot][c][0 .. W-2], x[s][0][c] .. x[s][T-1][c]], the commit sets
+ * conv_state[slot][c][k] = full[a+k] for k < W-1; each state row is read before it is written.
+ * CV_WINDOW_HISTORY has nothing to commit and returns CV_ERR_LAYOUT.
  */
 typedef struct cv_commit_args {
     int32_t n_seq, T, dim, width;
@@ -200,6 +214,9 @@ typedef struct cv_commit_args {
     int64_t win_seq_stride, win_step_stride, win_ch_stride, win_col_stride;
     const int32_t *accept_len; /* int32 [n_seq] device array, required */
     int32_t *err;              /* int32 [n_seq] device array or NULL */
+    /* CV_WINDOW_RECOMPUTE only (ignored otherwise): the verify's input [n_seq][T][dim] */
+    const void *x;
+    int64_t x_seq_stride, x_tok_stride;
 } cv_commit_args;
 
 CV_API int cv_conv_commit(const cv_commit_args *args, void *stream);
@@ -217,6 +234,7 @@ CV_API int cv_conv_commit(const cv_commit_args *args, void *stream);
  */
 typedef struct cv_launch_plan {
     int32_t grid_x, grid_y, threads, smem_bytes, channels_per_block, path;
+    int32_t stages; /* path 3: units whose loads are in flight per block (2); 0 otherwise */
 } cv_launch_plan;
 
 CV_API int cv_verify_plan(const cv_verify_args *args, cv_launch_plan *plan);

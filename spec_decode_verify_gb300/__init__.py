@@ -6,7 +6,7 @@ element strides; every step of the computation runs in the library's CUDA kernel
 CPU path: CPU tensors are rejected and a missing library raises.
 
     conv_verify(x, conv_state, weight, bias, out, window, layout=..., qk_channels=..., head_dim=...)
-    conv_commit(conv_state, window, accept_len, layout=..., T=..., width=...)
+    conv_commit(conv_state, window, accept_len, layout=..., T=..., width=..., x=...)
 """
 from __future__ import annotations
 
@@ -15,12 +15,12 @@ import os
 from typing import Optional
 
 __all__ = ["conv_verify", "conv_commit", "verify_plan", "status_string", "load_library", "library_path",
-           "CvError", "DENSE", "DEDUP", "HISTORY", "SEQ_BAD_SLOT", "SEQ_BAD_OFFSET", "SEQ_BAD_ACCEPT"]
+           "CvError", "DENSE", "DEDUP", "HISTORY", "RECOMPUTE", "SEQ_BAD_SLOT", "SEQ_BAD_OFFSET", "SEQ_BAD_ACCEPT"]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 library_path = os.path.join(_PKG, "_build", "libconvverify.so")
 
-DENSE, DEDUP, HISTORY = 1, 2, 3
+DENSE, DEDUP, HISTORY, RECOMPUTE = 1, 2, 3, 4
 F32, BF16 = 0, 1
 SEQ_BAD_SLOT, SEQ_BAD_OFFSET, SEQ_BAD_ACCEPT = 1, 2, 4
 MAX_T = 128
@@ -51,14 +51,14 @@ class CommitArgs(ctypes.Structure):
         ("conv_state", c_vp), ("state_slot_stride", c_i64), ("state_ch_stride", c_i64),
         ("state_cols", c_i32), ("window_layout", c_i32), ("cache_idx", c_vp), ("window", c_vp),
         ("win_seq_stride", c_i64), ("win_step_stride", c_i64), ("win_ch_stride", c_i64), ("win_col_stride", c_i64),
-        ("accept_len", c_vp), ("err", c_vp),
+        ("accept_len", c_vp), ("err", c_vp), ("x", c_vp), ("x_seq_stride", c_i64), ("x_tok_stride", c_i64),
     ]
 
 
 class LaunchPlan(ctypes.Structure):
     """Mirror of cv_launch_plan."""
     _fields_ = [("grid_x", c_i32), ("grid_y", c_i32), ("threads", c_i32), ("smem_bytes", c_i32),
-                ("channels_per_block", c_i32), ("path", c_i32)]
+                ("channels_per_block", c_i32), ("path", c_i32), ("stages", c_i32)]
 
 
 class CvError(RuntimeError):
@@ -124,11 +124,13 @@ def _layout_code(layout) -> int:
         return DEDUP
     if layout in (HISTORY, "history"):
         return HISTORY
+    if layout in (RECOMPUTE, "recompute"):
+        return RECOMPUTE
     raise ValueError(f"unknown window layout {layout!r}")
 
 
 def _window_strides(window, layout: int):
-    if layout == HISTORY or window is None:  # no window buffer
+    if layout in (HISTORY, RECOMPUTE) or window is None:  # no window buffer
         return 0, 0, 0, 0
     s = window.stride()
     if layout == DENSE:  # [n_seq, T, dim, W-1]
@@ -151,8 +153,8 @@ def make_verify_args(x, conv_state, weight, bias, out, window, *, layout, qk_cha
     (column stride 1), weight [dim, W] contiguous, bias [dim] or None, out [n_seq, T, dim] (channel
     stride 1), window dense [n_seq, T, dim, W-1] or dedup [n_seq, dim, T+W-2] (any strides), or
     None with layout "history" (conv_state [n_slots, dim, S >= T+W-2] then receives the snapshot
-    row and the next call reads at state_off = accept_len - 1), cache_idx / state_off / err int32
-    [n_seq] or None."""
+    row and the next call reads at state_off = accept_len - 1) or "recompute" (outputs only; the
+    commit rebuilds the state from x), cache_idx / state_off / err int32 [n_seq] or None."""
     lay = _layout_code(layout)
     ptr = _dev_ptr if check_device else (lambda t, n, required=True: None if t is None else t.data_ptr())
     n_seq, T, dim = x.shape
@@ -170,7 +172,7 @@ def make_verify_args(x, conv_state, weight, bias, out, window, *, layout, qk_cha
         state_slot_stride=conv_state.stride(0), state_ch_stride=conv_state.stride(1),
         cache_idx=ptr(cache_idx, "cache_idx", False), state_off=ptr(state_off, "state_off", False),
         weight=ptr(weight, "weight"), bias=ptr(bias, "bias", False),
-        window=ptr(window, "window", lay != HISTORY),
+        window=ptr(window, "window", lay not in (HISTORY, RECOMPUTE)),
         window_layout=lay, reserved0=0, win_seq_stride=ws[0], win_step_stride=ws[1], win_ch_stride=ws[2],
         win_col_stride=ws[3], err=ptr(err, "err", False))
 
@@ -207,8 +209,12 @@ def verify_plan(x, conv_state, weight, bias, out, window, *, layout, qk_channels
 
 
 def make_commit_args(conv_state, window, accept_len, *, layout, T, width, cache_idx=None, err=None,
-                     check_device=True) -> CommitArgs:
+                     x=None, check_device=True) -> CommitArgs:
+    """Build cv_commit_args.  Layout "recompute": window is None and x is the verify's input
+    [n_seq, T, dim] (channel stride 1)."""
     lay = _layout_code(layout)
+    if x is not None and x.stride(2) != 1:
+        raise ValueError("x needs a unit channel stride")
     ptr = _dev_ptr if check_device else (lambda t, n, required=True: None if t is None else t.data_ptr())
     ws = _window_strides(window, lay)
     if conv_state.stride(2) != 1:
@@ -218,16 +224,21 @@ def make_commit_args(conv_state, window, accept_len, *, layout, T, width, cache_
         n_slots=conv_state.shape[0], conv_state=ptr(conv_state, "conv_state"),
         state_slot_stride=conv_state.stride(0), state_ch_stride=conv_state.stride(1),
         state_cols=conv_state.shape[2], window_layout=lay, cache_idx=ptr(cache_idx, "cache_idx", False),
-        window=ptr(window, "window"), win_seq_stride=ws[0], win_step_stride=ws[1], win_ch_stride=ws[2],
-        win_col_stride=ws[3], accept_len=ptr(accept_len, "accept_len"), err=ptr(err, "err", False))
+        window=ptr(window, "window", lay != RECOMPUTE), win_seq_stride=ws[0], win_step_stride=ws[1],
+        win_ch_stride=ws[2], win_col_stride=ws[3], accept_len=ptr(accept_len, "accept_len"),
+        err=ptr(err, "err", False), x=ptr(x, "x", lay == RECOMPUTE),
+        x_seq_stride=x.stride(0) if x is not None else 0, x_tok_stride=x.stride(1) if x is not None else 0)
 
 
-def conv_commit(conv_state, window, accept_len, *, layout, T, width, cache_idx=None, err=None, stream=None) -> None:
-    """Queue the commit: conv_state[slot] <- snapshot accept_len[s]-1 of sequence s."""
-    if window.dtype != conv_state.dtype:
-        raise TypeError("window and conv_state must share one dtype")
+def conv_commit(conv_state, window, accept_len, *, layout, T, width, cache_idx=None, err=None, x=None,
+                stream=None) -> None:
+    """Queue the commit: conv_state[slot] <- snapshot accept_len[s]-1 of sequence s (rebuilt from the
+    kept window and x with layout "recompute")."""
+    for t in (window, x):
+        if t is not None and t.dtype != conv_state.dtype:
+            raise TypeError("window / x and conv_state must share one dtype")
     a = make_commit_args(conv_state, window, accept_len, layout=layout, T=T, width=width, cache_idx=cache_idx,
-                         err=err)
+                         err=err, x=x)
     rc = load_library().cv_conv_commit(ctypes.byref(a), _stream_ptr(stream))
     if rc != 0:
         raise CvError(rc, "cv_conv_commit")

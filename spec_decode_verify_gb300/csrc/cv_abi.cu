@@ -61,7 +61,9 @@ int check_verify(const cv_verify_args *a) {
     if (a->n_seq < 0 || a->n_seq > 65535 || a->dim < 1 || a->n_slots < 1 || a->state_cols < a->width - 1)
         return CV_ERR_SHAPE;
     const bool hist = a->window_layout == CV_WINDOW_HISTORY;
-    if (a->window_layout != CV_WINDOW_DENSE && a->window_layout != CV_WINDOW_DEDUP && !hist) return CV_ERR_LAYOUT;
+    const bool recomp = a->window_layout == CV_WINDOW_RECOMPUTE;
+    const bool nowin = hist || recomp;  // no window buffer
+    if (a->window_layout != CV_WINDOW_DENSE && a->window_layout != CV_WINDOW_DEDUP && !nowin) return CV_ERR_LAYOUT;
     if (a->window_layout == CV_WINDOW_DEDUP && a->win_step_stride != a->win_col_stride) return CV_ERR_LAYOUT;
     if (hist && a->state_cols < a->T + a->width - 2) return CV_ERR_SHAPE;
     if (a->qk_channels < 0 || a->qk_channels > a->dim) return CV_ERR_HEAD_DIM;
@@ -71,18 +73,18 @@ int check_verify(const cv_verify_args *a) {
     if (a->x_seq_stride < 0 || a->x_tok_stride < 0 || a->out_seq_stride < 0 || a->out_tok_stride < 0 ||
         a->state_slot_stride < 0 || a->state_ch_stride < 0)
         return CV_ERR_STRIDE;
-    if (!hist && (a->win_seq_stride < 0 || a->win_step_stride < 0 || a->win_ch_stride < 0 || a->win_col_stride < 0))
+    if (!nowin && (a->win_seq_stride < 0 || a->win_step_stride < 0 || a->win_ch_stride < 0 || a->win_col_stride < 0))
         return CV_ERR_STRIDE;
     if (a->dim > 1 && a->state_ch_stride < a->state_cols) return CV_ERR_STRIDE;
-    if (a->n_seq > 0 && (!a->x || !a->out || !a->conv_state || !a->weight || (!hist && !a->window)))
+    if (a->n_seq > 0 && (!a->x || !a->out || !a->conv_state || !a->weight || (!nowin && !a->window)))
         return CV_ERR_NULL_POINTER;
     if (a->n_seq > 0) {
-        const void *outs[2] = {a->out, hist ? nullptr : a->window};
+        const void *outs[2] = {a->out, nowin ? nullptr : a->window};
         const void *ins[3] = {a->x, a->conv_state, a->weight};
         for (const void *o : outs)
             for (const void *i : ins)
                 if (o && o == i) return CV_ERR_ALIAS;
-        if (!hist && a->out == a->window) return CV_ERR_ALIAS;
+        if (!nowin && a->out == a->window) return CV_ERR_ALIAS;
     }
     return CV_OK;
 }
@@ -98,7 +100,8 @@ bool io_packed(const cv_verify_args *a, int esize) {
 bool fast_eligible(const cv_verify_args *a, int esize, int max_static_t) {
     const int R = a->width - 1;
     const long long Q = a->T + R - 1;
-    if (a->window_layout == CV_WINDOW_HISTORY || !io_packed(a, esize)) return false;
+    if (a->window_layout == CV_WINDOW_HISTORY || a->window_layout == CV_WINDOW_RECOMPUTE || !io_packed(a, esize))
+        return false;
     if (!aligned16(a->window) || !stride16(a->win_seq_stride, esize) || a->win_col_stride != 1) return false;
     if (a->window_layout == CV_WINDOW_DEDUP) return a->win_ch_stride == Q && a->T <= max_static_t;
     return a->win_ch_stride == R && stride16(a->win_step_stride, esize);
@@ -129,13 +132,18 @@ int plan_verify(const cv_verify_args *a, cv_launch_plan *pl) {
     std::memset(pl, 0, sizeof *pl);
 
     const bool hist = a->window_layout == CV_WINDOW_HISTORY;
+    const bool recomp = a->window_layout == CV_WINDOW_RECOMPUTE;
     const bool fast = fast_eligible(a, esize, ks.max_static_t);
     const int cpt = (a->qk_channels > 0 && a->head_dim / 4 > 32) ? 8 : 4;
     // the history layout pipelines when its state rows are exactly the packed [dim][T+W-2] rows
     const bool hist_pipe = hist && io_packed(a, esize) && a->T <= ks.max_static_t && aligned16(a->conv_state) &&
                            stride16(a->state_slot_stride, esize) && a->state_ch_stride == a->T + R - 1;
-    if (hist_pipe || (fast && a->T <= ks.max_static_t &&
-                      state_packed(a->conv_state, a->state_slot_stride, a->state_ch_stride, a->width, esize))) {
+    // the recompute layout pipelines with packed state rows (it only reads them)
+    const bool recomp_pipe = recomp && io_packed(a, esize) && a->T <= ks.max_static_t &&
+                             state_packed(a->conv_state, a->state_slot_stride, a->state_ch_stride, a->width, esize);
+    if (hist_pipe || recomp_pipe ||
+        (fast && a->T <= ks.max_static_t &&
+         state_packed(a->conv_state, a->state_slot_stride, a->state_ch_stride, a->width, esize))) {
         auto part = [](long long b) { return (b + 127) / 128 * 128; };
         int threads = kPipeThreads;
         while (threads > 32 && cpt * (threads / 2) >= a->dim) threads /= 2;
@@ -144,14 +152,16 @@ int plan_verify(const cv_verify_args *a, cv_launch_plan *pl) {
         const long long bc = (long long)cpt * threads;
         const long long Q = a->T + R - 1;
         // two stages (x rows + committed windows, or whole history rows) and two image buffers
-        // (dedup row + committed windows, or the history row alone); 2 mbarriers, 2 slots, 2 offsets
+        // (dedup row + committed windows, or the history row alone; none for the recompute
+        // rollback); 2 mbarriers, 2 slots, 2 offsets
         const long long stage = part(a->T * bc * esize) + part((hist ? Q : R) * bc * esize);
-        long long image = hist ? 0 : part(R * bc * esize);
-        if (a->window_layout != CV_WINDOW_DENSE) image += part(Q * bc * esize);
+        long long image = (hist || recomp) ? 0 : part(R * bc * esize);
+        if (a->window_layout == CV_WINDOW_DEDUP || hist) image += part(Q * bc * esize);
         const long long smem = 2 * stage + 2 * image + 32 + (pipe_compacts(a) ? 16 + 4LL * a->n_seq : 0);
         int per_sm = (int)(kSmemPerSM / (smem + kSmemPerBlockReserved));
         if (per_sm > pipe_blocks_per_sm(cpt, a->T)) per_sm = pipe_blocks_per_sm(cpt, a->T);
-        if (smem <= kSmemMax && per_sm >= 1) {
+        const int nst = (smem <= kSmemMax && per_sm >= 1) ? 2 : 0;
+        if (nst > 0) {
             const long long nblk = (a->dim + bc - 1) / bc;
             const long long units = (long long)a->n_seq * nblk;
             // a multiple of the channel-block count keeps each block on one channel block
@@ -162,6 +172,7 @@ int plan_verify(const cv_verify_args *a, cv_launch_plan *pl) {
             pl->channels_per_block = (int)bc;
             pl->smem_bytes = (int)smem;
             pl->path = 3;
+            pl->stages = nst;
             pl->grid_x = (int)(g > 0 ? g : 1);
             pl->grid_y = 1;
             return CV_OK;
@@ -261,8 +272,9 @@ int launch_verify(const cv_verify_args *a, const cv_launch_plan &pl, cudaStream_
     p.win = a->window;
     p.dedup = a->window_layout == CV_WINDOW_DEDUP;
     p.hist = a->window_layout == CV_WINDOW_HISTORY;
+    p.recomp = a->window_layout == CV_WINDOW_RECOMPUTE;
     p.compact = pl.path == 3 && pipe_compacts(a);
-    if (p.hist) p.win = nullptr;
+    if (p.hist || p.recomp) p.win = nullptr;
     p.w_seq = a->win_seq_stride;
     p.w_step = p.dedup ? a->win_col_stride : a->win_step_stride;
     p.w_ch = a->win_ch_stride;
@@ -303,14 +315,17 @@ int check_commit(const cv_commit_args *a) {
     if (a->n_seq < 0 || a->n_seq > 65535 || a->dim < 1 || a->n_slots < 1 || a->state_cols < a->width - 1)
         return CV_ERR_SHAPE;
     // (the history layout has nothing to commit: the next verify reads at accept_len - 1)
-    if (a->window_layout != CV_WINDOW_DENSE && a->window_layout != CV_WINDOW_DEDUP) return CV_ERR_LAYOUT;
+    const bool recomp = a->window_layout == CV_WINDOW_RECOMPUTE;
+    if (a->window_layout != CV_WINDOW_DENSE && a->window_layout != CV_WINDOW_DEDUP && !recomp) return CV_ERR_LAYOUT;
     if (a->window_layout == CV_WINDOW_DEDUP && a->win_step_stride != a->win_col_stride) return CV_ERR_LAYOUT;
-    if (a->state_slot_stride < 0 || a->state_ch_stride < 0 || a->win_seq_stride < 0 || a->win_step_stride < 0 ||
-        a->win_ch_stride < 0 || a->win_col_stride < 0)
+    if (a->state_slot_stride < 0 || a->state_ch_stride < 0) return CV_ERR_STRIDE;
+    if (!recomp && (a->win_seq_stride < 0 || a->win_step_stride < 0 || a->win_ch_stride < 0 || a->win_col_stride < 0))
         return CV_ERR_STRIDE;
+    if (recomp && (a->x_seq_stride < 0 || a->x_tok_stride < 0)) return CV_ERR_STRIDE;
     if (a->dim > 1 && a->state_ch_stride < a->state_cols) return CV_ERR_STRIDE;
-    if (a->n_seq > 0 && (!a->conv_state || !a->window || !a->accept_len)) return CV_ERR_NULL_POINTER;
-    if (a->n_seq > 0 && a->conv_state == a->window) return CV_ERR_ALIAS;
+    if (a->n_seq > 0 && (!a->conv_state || !a->accept_len)) return CV_ERR_NULL_POINTER;
+    if (a->n_seq > 0 && (recomp ? !a->x : !a->window)) return CV_ERR_NULL_POINTER;
+    if (a->n_seq > 0 && (recomp ? a->conv_state == a->x : a->conv_state == a->window)) return CV_ERR_ALIAS;
     return CV_OK;
 }
 
@@ -335,6 +350,24 @@ int launch_commit(const cv_commit_args *a, cudaStream_t stream) {
     p.T = a->T;
     p.dim = a->dim;
     p.n_slots = a->n_slots;
+
+    if (a->window_layout == CV_WINDOW_RECOMPUTE) {
+        p.mode = 3;
+        p.win = nullptr;
+        p.x = a->x;
+        p.x_seq = a->x_seq_stride;
+        p.x_tok = a->x_tok_stride;
+        // 8 channels per thread with 16-byte vectors when the rows and x allow it
+        const bool vec = a->dim % 8 == 0 &&
+                         state_packed(a->conv_state, a->state_slot_stride, a->state_ch_stride, a->width, esize) &&
+                         aligned16(a->x) && stride16(a->x_seq_stride, esize) && stride16(a->x_tok_stride, esize);
+        const int threads = kCommitThreads;
+        const int per_block = vec ? 8 * threads : threads;
+        auto kr = vec ? kernel_set(a->dtype, a->width).commit_recompute_vec : kernel_set(a->dtype, a->width).commit_recompute;
+        if (launch_pdl(kr, dim3((a->dim + per_block - 1) / per_block, a->n_seq), threads, 0, stream, p) != cudaSuccess)
+            return CV_ERR_LAUNCH;
+        return cudaGetLastError() == cudaSuccess ? CV_OK : CV_ERR_LAUNCH;
+    }
 
     const bool packed_state = state_packed(a->conv_state, a->state_slot_stride, a->state_ch_stride, a->width, esize);
     const bool win_ok = a->dim % 8 == 0 && aligned16(a->window) && stride16(a->win_seq_stride, esize) &&

@@ -10,8 +10,12 @@
 //   mode 1, dense snapshots packed [.., dim, W-1] and state rows packed [dim][W-1]: the snapshot's
 //     channel block is one contiguous run, copied with 16-byte vectors;
 //   mode 0, anything else: element by element.
-// commit_rows (below) handles packed deduplicated rows with packed state rows.
+// commit_rows (below) handles packed deduplicated rows with packed state rows, and
+// commit_recompute the recompute rollback (no snapshots: the state is rebuilt from its kept window
+// and the verify's inputs).
 #pragma once
+
+#include <type_traits>
 
 #include "cv_device.cuh"
 
@@ -144,6 +148,108 @@ __global__ void __launch_bounds__(64) commit_rows(const __grid_constant__ Commit
         }
         st16(d + m * VE, make_uint4(wv[0], wv[1], wv[2], wv[3]));
     }
+}
+
+// Recompute rollback (memra-engine Engine doc, ssm_conv_ring_rebuild_dc: the conv state is rebuilt
+// from the window kept from before the verify and the verify's inputs, with the accept count read
+// on the device).  One thread per channel: with full = [state[0 .. W-2], x_0 .. x_{T-1}], the new
+// window is full[a .. a+W-2] -- state columns while a+k < W-1, x rows a+k-(W-1) after -- loaded
+// first and stored after, so the in-place rewrite of the row is safe.  Across a warp the state
+// elements are one contiguous run (packed rows) and each x row is contiguous, so every access is
+// coalesced; the accesses are 2- or 4-byte, enough since at most 3 x 2 elements move per channel.
+template <typename B, int W>
+__global__ void __launch_bounds__(128) commit_recompute(const __grid_constant__ CommitParams p) {
+    grid_dep_wait();
+    grid_dep_launch();
+    constexpr int R = W - 1;
+    const int s = blockIdx.y;
+    const int slot = p.cache_idx ? __ldg(p.cache_idx + s) : s;
+    const int a = __ldg(p.accept_len + s);
+    int status = 0;
+    if (slot >= 0) {
+        if (slot >= p.n_slots) status |= 1;
+        if (a < 1 || a > p.T) status |= 4;
+    }
+    if (p.err && blockIdx.x == 0 && threadIdx.x == 0) p.err[s] = status;
+    if (slot < 0 || status) return;
+    const int c = blockIdx.x * blockDim.x + threadIdx.x;
+    if (c >= p.dim) return;
+    B *row = reinterpret_cast<B *>(p.state) + (long long)slot * p.st_slot + (long long)c * p.st_ch;
+    const B *xs = reinterpret_cast<const B *>(p.x) + (long long)s * p.x_seq + c;
+    B v[R];
+#pragma unroll
+    for (int k = 0; k < R; ++k) {
+        const int j = a + k;  // position in full
+        v[k] = j < R ? row[j] : xs[(long long)(j - R) * p.x_tok];
+    }
+#pragma unroll
+    for (int k = 0; k < R; ++k) row[k] = v[k];
+}
+
+// The same rebuild for packed state rows and 16-byte aligned x rows: 8 channels per thread, so a
+// thread moves its window run and each needed x row as 16-byte vectors and one block covers
+// 8*threads channels -- the whole batch fits in one wave, each thread making one round trip for
+// the indices and one for the data.  The accept count is a runtime value, so each new column k
+// takes, per channel, either old column a+k (picked by selects among the W-1 old columns) or
+// element e of the x row a+k-(W-1) (loaded whole when some column needs it).
+template <typename B, int W>
+__global__ void __launch_bounds__(128) commit_recompute_vec(const __grid_constant__ CommitParams p) {
+    grid_dep_wait();
+    grid_dep_launch();
+    constexpr int R = W - 1;
+    constexpr int ES = (int)sizeof(B);
+    constexpr int NXV = 8 * ES / 16;      // 16-byte vectors per x row of 8 channels
+    constexpr int NSV = 8 * R * ES / 16;  // 16-byte vectors per window run of 8 channels
+    using U = std::conditional_t<ES == 2, unsigned short, unsigned>;
+    const int s = blockIdx.y;
+    const int slot = p.cache_idx ? __ldg(p.cache_idx + s) : s;
+    const int a = __ldg(p.accept_len + s);
+    int status = 0;
+    if (slot >= 0) {
+        if (slot >= p.n_slots) status |= 1;
+        if (a < 1 || a > p.T) status |= 4;
+    }
+    if (p.err && blockIdx.x == 0 && threadIdx.x == 0) p.err[s] = status;
+    if (slot < 0 || status) return;
+    const int c = 8 * (blockIdx.x * blockDim.x + threadIdx.x);
+    if (c >= p.dim) return;  // dim % 8 == 0 on this path
+    uint4 *run = reinterpret_cast<uint4 *>(reinterpret_cast<B *>(p.state) + (long long)slot * p.st_slot +
+                                           (long long)c * R);
+    const B *xs = reinterpret_cast<const B *>(p.x) + (long long)s * p.x_seq + c;
+    union {
+        uint4 v[NSV];
+        U e[8 * R];
+    } old, neu;
+    union {
+        uint4 v[NXV];
+        U e[8];
+    } xr[R];
+#pragma unroll
+    for (int i = 0; i < NSV; ++i) old.v[i] = run[i];
+#pragma unroll
+    for (int k = 0; k < R; ++k) {
+        const int j = a + k;
+        if (j >= R) {
+#pragma unroll
+            for (int i = 0; i < NXV; ++i)
+                xr[k].v[i] = __ldg(reinterpret_cast<const uint4 *>(xs + (long long)(j - R) * p.x_tok) + i);
+        } else {
+#pragma unroll
+            for (int i = 0; i < NXV; ++i) xr[k].v[i] = make_uint4(0u, 0u, 0u, 0u);
+        }
+    }
+#pragma unroll
+    for (int e = 0; e < 8; ++e)
+#pragma unroll
+        for (int k = 0; k < R; ++k) {
+            const int j = a + k;
+            U o = old.e[e * R];
+#pragma unroll
+            for (int q = 1; q < R; ++q) o = j == q ? old.e[e * R + q] : o;
+            neu.e[e * R + k] = j < R ? o : xr[k].e[e];
+        }
+#pragma unroll
+    for (int i = 0; i < NSV; ++i) run[i] = neu.v[i];
 }
 
 }  // namespace cvk

@@ -29,6 +29,7 @@ struct VerifyParams {
     int dedup;
     int hist;     // history-row state: the snapshot row goes into the state row (no window buffer)
     int compact;  // pipelined kernel: walk only the sequences with a cache slot >= 0 (list in shared memory)
+    int recomp;   // recompute rollback: outputs only (no snapshots, state not written)
     int x_vec, out_vec, st_vec, w_vec, b_vec;  // 16-byte vector access allowed (checked on the host)
 };
 
@@ -41,7 +42,9 @@ struct CommitParams {
     const int *accept_len;
     int *err;
     int n_seq, T, dim, n_slots;
-    int mode;  // 0: element by element, 1: packed dense snapshot -> packed state, 2: packed dedup row -> packed state (pipelined)
+    int mode;  // 0: element by element, 1: packed dense snapshot -> packed state, 2: packed dedup row -> packed state, 3: recompute from x
+    const void *x;  // mode 3: the verify's input
+    long long x_seq, x_tok;
 };
 
 // Per-sequence status shared by both kernels: 1 = slot out of range, 2 = state offset out of range.

@@ -23,6 +23,8 @@ KernelSet make_set(std::integer_sequence<int, Ts...>) {
     k.generic = verify_generic<B, W>;
     k.commit = commit_kernel<B, W>;
     k.commit_rows = commit_rows<B, W>;
+    k.commit_recompute = commit_recompute<B, W>;
+    k.commit_recompute_vec = commit_recompute_vec<B, W>;
     return k;
 }
 }  // namespace

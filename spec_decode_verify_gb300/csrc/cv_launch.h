@@ -23,6 +23,8 @@ struct KernelSet {
     VerifyKernel generic;
     CommitKernel commit;
     CommitKernel commit_rows;
+    CommitKernel commit_recompute;
+    CommitKernel commit_recompute_vec;
 };
 
 const KernelSet &kernels_bf16_w2();

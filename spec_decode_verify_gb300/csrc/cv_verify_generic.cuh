@@ -225,7 +225,9 @@ __global__ void __launch_bounds__(256) verify_generic(const __grid_constant__ Ve
     __syncthreads();
 
     // (4) snapshots and committed window, written from the tile in destination order
-    if (p.hist) {
+    if (p.recomp) {
+        // recompute rollback: outputs only; the state keeps the pre-verify window
+    } else if (p.hist) {
         // history-row state: the snapshot row [full[1 .. W-2], x_0 .. x_{T-1}] replaces columns
         // [0, T+W-2) of the state row (every thread read its committed window before the barrier)
         B *sb = reinterpret_cast<B *>(p.state) + (long long)slot * p.st_slot + (long long)c0 * p.st_ch;

@@ -22,7 +22,7 @@
 // History-row state (no window buffer): the stage holds each channel's whole [T+W-2] state row,
 // the committed window is taken from columns [off, off+W-1) of it, and the row image is stored
 // back over the state row instead of into a window buffer; there is no separate committed-window
-// image.
+// image.  Recompute rollback: outputs only; nothing is staged for storing and no bulk store runs.
 // Preconditions (checked on the host): those of the fast path, packed 16-byte-aligned state rows
 // ([dim][W-1], or [dim][T+W-2] for the history layout), T <= 17 (bf16) / 8 (fp32),
 // head_dim / CPT <= 32.
@@ -63,7 +63,8 @@ __global__ void __launch_bounds__(128, (CPT == 4 && TS <= 8) ? 4 : 2) verify_pip
     const int BC = CPT * blockDim.x;
     const int nblk = (p.dim + BC - 1) / BC;
     const bool hist = p.hist != 0;        // history-row state: no window buffer
-    const bool dense = !p.dedup && !hist;  // dense window: no row image
+    const bool recomp = p.recomp != 0;    // recompute rollback: outputs only
+    const bool dense = !p.dedup && !hist;  // dense window (or none): no row image
     const bool has_bias = p.bias != nullptr;
     const int SC = hist ? Q : R;           // state columns staged per channel
 
@@ -74,7 +75,7 @@ __global__ void __launch_bounds__(128, (CPT == 4 && TS <= 8) ? 4 : 2) verify_pip
     const long long xb = pipe_part((long long)TS * BC * ES);
     const long long stage_bytes = xb + pipe_part((long long)SC * BC * ES);
     const long long rb = dense ? 0 : pipe_part((long long)Q * BC * ES);
-    const long long img_bytes = rb + (hist ? 0 : pipe_part((long long)R * BC * ES));
+    const long long img_bytes = recomp ? 0 : rb + (hist ? 0 : pipe_part((long long)R * BC * ES));
     unsigned char *const img0 = smem + 2 * stage_bytes;
     uint64_t *const bar = reinterpret_cast<uint64_t *>(img0 + 2 * img_bytes);
     volatile int *const info = reinterpret_cast<volatile int *>(bar + 2);  // [0, 2): slots, [2, 4): offsets
@@ -265,7 +266,9 @@ __global__ void __launch_bounds__(128, (CPT == 4 && TS <= 8) ? 4 : 2) verify_pip
                 }
                 return word_of(i / n, j0 + i % n);
             };
-            if (!dense) {
+            if (recomp) {
+                // outputs only: no snapshots, and the state keeps the pre-verify window
+            } else if (!dense) {
                 uint32_t im[Q * NW];  // CPT channels x Q columns; column q holds input q+1
 #pragma unroll
                 for (int i = 0; i < Q * NW; ++i) im[i] = run_word(i, Q, 1);
@@ -280,7 +283,7 @@ __global__ void __launch_bounds__(128, (CPT == 4 && TS <= 8) ? 4 : 2) verify_pip
                     stv<VS, R * NW>(wsq + (long long)t * p.w_step, w);
                 }
             }
-            if (!hist) {
+            if (!hist && !recomp) {
                 uint32_t fin[R * NW];
 #pragma unroll
                 for (int i = 0; i < R * NW; ++i) fin[i] = run_word(i, R, TS);
@@ -303,7 +306,7 @@ __global__ void __launch_bounds__(128, (CPT == 4 && TS <= 8) ? 4 : 2) verify_pip
             return;
         }
         if (tid == 0) {
-            if (go) {
+            if (go && !recomp) {
                 if (hist) {
                     // the row image replaces columns [0, T+W-2) of the (packed) history rows
                     bulk_store(reinterpret_cast<B *>(p.state) + (long long)slot * p.st_slot + (long long)c0 * Q, img,

@@ -40,6 +40,6 @@ def run_gpu_commit(cv, w: wl.VerifyWorkload, d: dict, accept_len=None) -> torch.
     e = torch.full((w.n_seq,), -7, dtype=torch.int32, device="cuda")
     acc = d["accept_len"] if accept_len is None else accept_len.to("cuda")
     cv.conv_commit(d["conv_state"], d["window"], acc, layout=w.layout, T=w.T, width=w.width,
-                   cache_idx=d["cache_idx"], err=e)
+                   cache_idx=d["cache_idx"], err=e, x=d["x"] if w.layout == "recompute" else None)
     torch.cuda.synchronize()
     return e

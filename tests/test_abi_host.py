@@ -33,7 +33,7 @@ def test_exports_every_declared_function(lib):
     assert {"cv_conv_verify", "cv_conv_commit", "cv_verify_plan", "cv_status_string", "cv_abi_version"} <= set(names)
     for n in names:
         assert hasattr(lib, n), f"{n} declared in the header but not exported"
-    assert lib.cv_abi_version() == 1
+    assert lib.cv_abi_version() == 2
 
 
 def test_exports_nothing_undeclared(lib):
@@ -65,17 +65,23 @@ def _plan(lib, a):
 W3 = wl.WORKLOADS["n128_t8_dim10240_w4_bf16_dedup_pad13"]
 
 
+def _pipe_smem(stage, image, n_seq):
+    """The pipelined kernel's shared memory: two stages, two image buffers, 32 bytes of barriers,
+    slots and offsets, and 16 + 4 * n_seq bytes for the list of active sequences."""
+    return 2 * stage + 2 * image + 32 + 16 + 4 * n_seq
+
+
 def test_plan_for_benchmark_workload(lib):
     """128 x 8 x 10240 bf16 dedup, packed state: the pipelined path.  4 channels per thread (an L2
     group of 128 spans 32 lanes), 128 threads per unit of 512 channels.  Shared memory: two stages
     of (8 x rows + 3 window columns) and two image buffers of (10 dedup columns + 3 window columns),
-    plus 32 bytes of barriers, slots and offsets and 16 + 4 * 128 bytes for the list of active
-    sequences; 4 blocks fit an SM, and the persistent grid is the largest multiple of the 20 channel
-    blocks within 152 * 4 blocks, so each block keeps its taps."""
+    plus barriers, slots, offsets and the list of active sequences; 4 blocks fit an SM, and the
+    persistent grid is the largest multiple of the 20 channel blocks within 152 * 4 blocks, so each
+    block keeps its taps."""
     rc, pl = _plan(lib, _args(W3))
     assert rc == 0
-    smem = 2 * (8 + 3) * 512 * 2 + 2 * (10 + 3) * 512 * 2 + 32 + 16 + 4 * 128
-    assert (pl.threads, pl.channels_per_block, pl.path, pl.smem_bytes) == (128, 512, 3, smem)
+    smem = _pipe_smem((8 + 3) * 512 * 2, (10 + 3) * 512 * 2, 128)
+    assert (pl.threads, pl.channels_per_block, pl.path, pl.smem_bytes, pl.stages) == (128, 512, 3, smem, 2)
     assert (pl.grid_x, pl.grid_y) == (600, 1)
 
 
@@ -84,15 +90,14 @@ HIST = wl.WORKLOADS["n128_t8_dim10240_w4_bf16_history_pad13"]
 
 def test_plan_for_history_workload(lib):
     """History rows: the stages hold whole [10]-column rows and the only image is the row image,
-    so one block needs 2 * (8 + 10) * 1024 + 2 * 10 * 1024 + 32 bytes (plus the sequence list) and
-    3 blocks fit an SM; the
-    grid is the largest multiple of 20 within 152 * 3."""
+    so one block needs 2 * (8 + 10) * 1024 + 2 * 10 * 1024 bytes plus the index words and 3 blocks
+    fit an SM; the grid is the largest multiple of 20 within 152 * 3."""
     a = _args(HIST)
     assert a.window is None and a.state_cols == 10 and a.state_ch_stride == 10
     rc, pl = _plan(lib, a)
     assert rc == 0
-    smem = 2 * (8 + 10) * 512 * 2 + 2 * 10 * 512 * 2 + 32 + 16 + 4 * 128
-    assert (pl.threads, pl.channels_per_block, pl.path, pl.smem_bytes) == (128, 512, 3, smem)
+    smem = _pipe_smem((8 + 10) * 512 * 2, 10 * 512 * 2, 128)
+    assert (pl.threads, pl.channels_per_block, pl.path, pl.smem_bytes, pl.stages) == (128, 512, 3, smem, 2)
     assert (pl.grid_x, pl.grid_y) == (440, 1)
 
 
@@ -121,7 +126,7 @@ def test_history_validation_and_paths(lib):
 @pytest.mark.parametrize("name,path", [
     ("n1_t2_dim512_w4_f32_dense", 3), ("n4_t4_dim4096_w4_bf16_dedup_bias", 3),
     ("n8_t17_dim8192_w4_bf16_dense_qkvsplit_xstride12288", 3), ("n64_t8_dim6144_w3_bf16_dense_nol2_stateoff", 1),
-    ("n128_t8_dim10240_w4_bf16_history_pad13", 3)])
+    ("n128_t8_dim10240_w4_bf16_history_pad13", 3), ("n128_t8_dim10240_w4_bf16_recompute_pad13", 3)])
 def test_plan_paths_of_named_workloads(lib, name, path):
     w = wl.WORKLOADS[name]
     rc, pl = _plan(lib, _args(w))
@@ -135,16 +140,39 @@ def test_plan_paths_of_named_workloads(lib, name, path):
     assert units >= 2 * 152 or pl.threads == 32 or pl.channels_per_block // 2 < max(w.head_dim, 8)
 
 
+def test_recompute_plan_and_commit_validation(lib):
+    """Recompute layout: the stages hold x rows and committed windows and there are no images;
+    its commit needs x and no window."""
+    w = wl.WORKLOADS["n128_t8_dim10240_w4_bf16_recompute_pad13"]
+    a = _args(w)
+    assert a.window is None
+    rc, pl = _plan(lib, a)
+    assert rc == 0 and pl.path == 3 and pl.smem_bytes == _pipe_smem((8 + 3) * 512 * 2, 0, 128)
+    a.state_ch_stride, a.state_cols = 4, 4  # unpacked rows: the general kernel
+    assert _plan(lib, a)[1].path == 0
+    inp = wl.make_inputs(w.replace(n_seq=2, n_pad=0, extra_slots=0))
+    c = cv.make_commit_args(inp["conv_state"], None, inp["accept_len"], layout="recompute", T=8, width=4,
+                            x=inp["x"], check_device=False)
+    assert c.x is not None and c.x_tok_stride == w.dim and c.x_seq_stride == 8 * w.dim
+    c.x = None
+    assert lib.cv_conv_commit(ctypes.byref(c), None) == -2
+    c = cv.make_commit_args(inp["conv_state"], None, inp["accept_len"], layout="recompute", T=8, width=4,
+                            x=inp["x"], check_device=False)
+    c.x_tok_stride = -1
+    assert lib.cv_conv_commit(ctypes.byref(c), None) == -9
+
+
 def test_plan_sequence_list_only_with_cache_indices(lib):
     """The pipelined kernel lists the active sequences in shared memory when there are cache
     indices (and at most 1024 sequences); without indices every sequence is active."""
     a = _args(W3)
-    base = _plan(lib, a)[1].smem_bytes
+    base = _plan(lib, a)[1]
     a.cache_idx = None
-    assert _plan(lib, a)[1].smem_bytes == base - 16 - 4 * 128
+    pl = _plan(lib, a)[1]
+    assert pl.stages == base.stages and pl.smem_bytes == base.smem_bytes - 16 - 4 * 128
     a = _args(W3.replace(n_seq=1025, n_pad=0))
     pl = _plan(lib, a)[1]
-    assert pl.path == 3 and pl.smem_bytes == base - 16 - 4 * 128
+    assert pl.path == 3 and pl.stages == base.stages and pl.smem_bytes == base.smem_bytes - 16 - 4 * 128
 
 
 def test_plan_general_path_cases(lib):
@@ -170,7 +198,7 @@ def test_plan_general_path_cases(lib):
 
 @pytest.mark.parametrize("field,value,status", [
     ("dtype", 7, -6), ("width", 1, -5), ("width", 5, -5), ("T", 0, -4), ("T", 129, -4), ("n_seq", -1, -3),
-    ("n_seq", 65536, -3), ("dim", 0, -3), ("n_slots", 0, -3), ("state_cols", 2, -3), ("window_layout", 4, -8), ("window_layout", 3, -3),
+    ("n_seq", 65536, -3), ("dim", 0, -3), ("n_slots", 0, -3), ("state_cols", 2, -3), ("window_layout", 5, -8), ("window_layout", 0, -8), ("window_layout", 3, -3),
     ("win_step_stride", 5, -8), ("qk_channels", 10240 + 128, -7), ("head_dim", 96, -7), ("head_dim", 4, -7),
     ("head_dim", 512, -7), ("qk_channels", 4000, -7), ("x_tok_stride", -1, -9), ("state_ch_stride", 2, -9),
     ("x", None, -2), ("weight", None, -2), ("window", None, -2),

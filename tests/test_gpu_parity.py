@@ -21,7 +21,7 @@ def check_verify_and_commit(cv, w: wl.VerifyWorkload, inp: dict, commit=True):
     ref = run_oracle_verify(w, inp)
     got = run_gpu_verify(cv, w, inp)
     assert_bits_equal(got["err"].cpu(), ref["status"], "err")
-    if w.layout != "history":
+    if w.layout not in ("history", "recompute"):
         assert_bits_equal(got["window"].cpu(), ref["window"], "window")
     assert_bits_equal(got["conv_state"].cpu(), ref["conv_state"], "state")
     assert_out_close(got["out"].cpu(), ref["out"], "out")
@@ -299,7 +299,8 @@ def test_all_paths_bit_identical(cuda_lib, layout, dtype):
 
 
 @pytest.mark.parametrize("name", ["n128_t8_dim10240_w4_bf16_dedup_pad13", "n64_t8_dim6144_w3_bf16_dense_nol2_stateoff",
-                                  "n128_t8_dim10240_w4_bf16_history_pad13"])
+                                  "n128_t8_dim10240_w4_bf16_history_pad13",
+                                  "n128_t8_dim10240_w4_bf16_recompute_pad13"])
 def test_chained_steps_without_host_sync(cuda_lib, name):
     """Three decode steps queued back to back on one stream with no host synchronisation between
     the launches (each launch may be scheduled while the previous grid finishes): every step's
@@ -331,13 +332,14 @@ def test_chained_steps_without_host_sync(cuda_lib, name):
     offs = [base["state_off"].to(dev) if base["state_off"] is not None else None]
     offs += [(steps[i - 1]["accept_len"] - 1).to(torch.int32).to(dev) if hist else offs[0] for i in (1, 2)]
     outs = [base["out"].to(dev) for _ in steps]
-    win = base["window"].to(dev) if not hist else None
+    win = base["window"].to(dev) if base["window"] is not None else None
     torch.cuda.synchronize()
     for i in range(3):
         cv.conv_verify(xs[i], state, weight, bias, outs[i], win, layout=w.layout, qk_channels=w.qk_channels,
                        head_dim=w.head_dim, l2_eps=w.l2_eps, cache_idx=cidx, state_off=offs[i])
         if not hist:
-            cv.conv_commit(state, win, accs[i], layout=w.layout, T=w.T, width=w.width, cache_idx=cidx)
+            cv.conv_commit(state, win, accs[i], layout=w.layout, T=w.T, width=w.width, cache_idx=cidx,
+                           x=xs[i] if w.layout == "recompute" else None)
     torch.cuda.synchronize()
     for i in range(3):
         assert_out_close(outs[i].cpu(), outs_ref[i], f"step {i} out")
