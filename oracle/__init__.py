@@ -48,6 +48,16 @@ class _CommitArgs(ctypes.Structure):
     ]
 
 
+class _PrefillArgs(ctypes.Structure):
+    _fields_ = [
+        ("n_seq", c_i32), ("dim", c_i32), ("width", c_i32), ("qk_channels", c_i32), ("head_dim", c_i32),
+        ("is_bf16", c_i32), ("l2_eps", ctypes.c_float), ("total_tokens", c_i32),
+        ("x", c_vp), ("x_tok", c_i64), ("out", c_vp), ("out_tok", c_i64), ("cu_seqlens", c_vp),
+        ("state", c_vp), ("n_slots", c_i32), ("state_cols", c_i32), ("st_slot", c_i64), ("st_ch", c_i64),
+        ("cache_idx", c_vp), ("has_initial_state", c_vp), ("weight", c_vp), ("bias", c_vp), ("status", c_vp),
+    ]
+
+
 def build(force: bool = False) -> str:
     """Compile oracle.c into _build/liboracle.so (plain C, no vector intrinsics, no contraction)."""
     os.makedirs(_BUILD, exist_ok=True)
@@ -68,6 +78,8 @@ def _open(path: str):
     lib.oracle_conv_verify.restype = c_i32
     lib.oracle_conv_commit.argtypes = [ctypes.POINTER(_CommitArgs)]
     lib.oracle_conv_commit.restype = c_i32
+    lib.oracle_conv_prefill.argtypes = [ctypes.POINTER(_PrefillArgs)]
+    lib.oracle_conv_prefill.restype = c_i32
     lib.oracle_round_f32_to_bf16.argtypes = [ctypes.c_float]
     lib.oracle_round_f32_to_bf16.restype = ctypes.c_uint32
     return lib
@@ -174,6 +186,28 @@ def conv_commit(conv_state, window, accept_len, *, layout, T, width, cache_idx=N
     rc = _load().oracle_conv_commit(ctypes.byref(a))
     if rc != 0:
         raise RuntimeError(f"oracle_conv_commit returned {rc}")
+
+
+def conv_prefill(x, conv_state, weight, bias, out, cu_seqlens, *, qk_channels, head_dim, l2_eps, cache_idx=None,
+                 has_initial_state=None, status=None):
+    """Run the oracle prefill in place on CPU tensors (conv_state, out, status are written).
+
+    x, out [total_tokens, dim] (channel stride 1, any token stride), conv_state [n_slots, dim, S]
+    (column stride 1), weight [dim, W] contiguous, bias [dim] or None, cu_seqlens int32
+    [n_seq + 1], cache_idx / has_initial_state / status int32 [n_seq] or None."""
+    total, dim = x.shape
+    n_seq = cu_seqlens.shape[0] - 1
+    assert x.stride(1) == 1 and out.stride(1) == 1 and conv_state.stride(2) == 1 and weight.is_contiguous()
+    a = _PrefillArgs(
+        n_seq=n_seq, dim=dim, width=weight.shape[1], qk_channels=qk_channels, head_dim=head_dim,
+        is_bf16=_is_bf16(x), l2_eps=l2_eps, total_tokens=total, x=_ptr(x), x_tok=x.stride(0), out=_ptr(out),
+        out_tok=out.stride(0), cu_seqlens=_ptr(cu_seqlens), state=_ptr(conv_state), n_slots=conv_state.shape[0],
+        state_cols=conv_state.shape[2], st_slot=conv_state.stride(0), st_ch=conv_state.stride(1),
+        cache_idx=_ptr(cache_idx), has_initial_state=_ptr(has_initial_state), weight=_ptr(weight),
+        bias=_ptr(bias), status=_ptr(status))
+    rc = _load().oracle_conv_prefill(ctypes.byref(a))
+    if rc != 0:
+        raise RuntimeError(f"oracle_conv_prefill returned {rc}")
 
 
 def round_f32_to_bf16_bits(v: float) -> int:

@@ -65,8 +65,17 @@
  *     snapshot t is what a partial accept rewinds to).  With a accepted tokens (1 <= a <= T) the
  *     state becomes snapshot a-1.
  *
+ *   - Prefill (glm5next_kda mod.rs, the prefill path of the layer: the conv over all T prompt
+ *     tokens with SiLU, then the L2 normalisation of q|k, which that code runs as a second launch;
+ *     here the normalisation is applied to the fp32 SiLU values and rounded once, as in decode).
+ *     Packed variable-length sequences: sequence s owns tokens [cu[s], cu[s+1]) of x and out.
+ *     full = [initial window, x_0 .. x_{L-1}], the initial window being state[0 .. W-2] when the
+ *     sequence has an initial state and zeros otherwise; out_t is the verify's output for token t;
+ *     the state is left holding the last W-1 entries of full.
+ *
  * Status codes written per sequence (same meaning as the library's): 1 = cache slot out of range,
- * 2 = state offset out of range, 4 = accept count out of range.  A flagged sequence is untouched.
+ * 2 = state offset out of range, 4 = accept count out of range, 16 = token span invalid (prefill).
+ * A flagged sequence is untouched.
  */
 #include <math.h>
 #include <stdint.h>
@@ -255,6 +264,82 @@ int oracle_conv_commit(const oracle_commit_args *a) {
                 const int64_t dst = (int64_t)slot * a->st_slot + (int64_t)c * a->st_ch + k;
                 put_bits(a->state, bf, dst, get_bits(a->window, bf, src));
             }
+    }
+    return 0;
+}
+
+typedef struct {
+    int32_t n_seq, dim, width, qk_channels, head_dim, is_bf16;
+    float l2_eps;
+    int32_t total_tokens;
+    const void *x;
+    int64_t x_tok;
+    void *out;
+    int64_t out_tok;
+    const int32_t *cu_seqlens;        /* [n_seq + 1] */
+    void *state;
+    int32_t n_slots, state_cols;
+    int64_t st_slot, st_ch;
+    const int32_t *cache_idx;         /* NULL: sequence s uses slot s */
+    const int32_t *has_initial_state; /* NULL: every sequence has one */
+    const void *weight, *bias;
+    int32_t *status;
+} oracle_prefill_args;
+
+int oracle_conv_prefill(const oracle_prefill_args *a) {
+    const int W = a->width, dim = a->dim, bf = a->is_bf16;
+    for (int s = 0; s < a->n_seq; ++s) {
+        const int slot = a->cache_idx ? a->cache_idx[s] : s;
+        const int b = a->cu_seqlens[s], e = a->cu_seqlens[s + 1];
+        int st = 0;
+        if (slot >= 0 && slot >= a->n_slots) st |= 1;
+        if (slot >= 0 && (b < 0 || e < b || e > a->total_tokens)) st |= 16;
+        if (a->status) a->status[s] = st;
+        if (slot < 0 || st) continue;
+        const int L = e - b;
+        const int init = a->has_initial_state ? a->has_initial_state[s] != 0 : 1;
+        uint32_t *full = (uint32_t *)malloc(sizeof(uint32_t) * (size_t)(W - 1 + L));
+        float *y = (float *)malloc(sizeof(float) * ((size_t)L * (size_t)dim + 1));
+        if (!full || !y) {
+            free(full);
+            free(y);
+            return -2;
+        }
+        for (int c = 0; c < dim; ++c) {
+            const int64_t srow = (int64_t)slot * a->st_slot + (int64_t)c * a->st_ch;
+            for (int k = 0; k < W - 1; ++k) full[k] = init ? get_bits(a->state, bf, srow + k) : 0u;
+            for (int t = 0; t < L; ++t) full[W - 1 + t] = get_bits(a->x, bf, (int64_t)(b + t) * a->x_tok + c);
+            for (int t = 0; t < L; ++t) {
+                float acc = a->bias ? bits_to_float(get_bits(a->bias, bf, c), bf) : 0.0f;
+                for (int j = 0; j < W; ++j) {
+                    const float wj = bits_to_float(get_bits(a->weight, bf, (int64_t)c * W + j), bf);
+                    const float prod = wj * bits_to_float(full[t + j], bf);
+                    acc = acc + prod;
+                }
+                y[(int64_t)t * dim + c] = acc / (1.0f + expf(-acc));
+            }
+            /* the last W-1 entries of full, after every read of this row */
+            for (int k = 0; k < W - 1; ++k) put_bits(a->state, bf, srow + k, full[L + k]);
+        }
+        for (int t = 0; t < L; ++t) {
+            float *yt = y + (int64_t)t * dim;
+            if (a->qk_channels > 0) {
+                const int hd = a->head_dim;
+                for (int g = 0; g + hd <= a->qk_channels; g += hd) {
+                    float ss = 0.0f;
+                    for (int c = g; c < g + hd; ++c) {
+                        const float sq = yt[c] * yt[c];
+                        ss = ss + sq;
+                    }
+                    const float r = 1.0f / sqrtf(ss + a->l2_eps);
+                    for (int c = g; c < g + hd; ++c) yt[c] = yt[c] * r;
+                }
+            }
+            for (int c = 0; c < dim; ++c)
+                put_bits(a->out, bf, (int64_t)(b + t) * a->out_tok + c, float_to_bits(yt[c], bf));
+        }
+        free(full);
+        free(y);
     }
     return 0;
 }

@@ -200,3 +200,114 @@ def algorithmic_bytes(w: VerifyWorkload, n_active: Optional[int] = None) -> dict
     per_seq = (w.T * w.dim + (w.width - 1) * w.dim + w.T * w.dim + win_cols * w.dim + (w.width - 1) * w.dim) * e
     commit = n * 2 * (w.width - 1) * w.dim * e + 8 * w.n_seq
     return dict(verify=n * per_seq + shared, commit=commit, per_seq=per_seq)
+
+
+# ----------------------------------------------------------------------------- prefill
+
+@dataclasses.dataclass(frozen=True)
+class PrefillWorkload:
+    """Packed variable-length prefill: sequence s owns tokens [cu[s], cu[s+1]) of x and out."""
+    name: str
+    lengths: tuple  # tokens per sequence (0 allowed)
+    dim: int
+    width: int
+    qk_channels: int
+    head_dim: int
+    dtype: str
+    bias: bool = False
+    l2_eps: float = 1e-6
+    pad: tuple = ()  # indices of padded sequences (cache index -1)
+    no_init: tuple = ()  # indices of sequences without an initial state (zero window)
+    extra_slots: int = 0
+    x_row_stride: Optional[int] = None
+    seed: int = 0
+
+    @property
+    def n_seq(self) -> int:
+        return len(self.lengths)
+
+    @property
+    def total_tokens(self) -> int:
+        return int(sum(self.lengths))
+
+    @property
+    def max_seqlen(self) -> int:
+        return int(max(self.lengths)) if self.lengths else 0
+
+    @property
+    def n_slots(self) -> int:
+        return self.n_seq + self.extra_slots
+
+    @property
+    def torch_dtype(self):
+        return torch.float32 if self.dtype == "f32" else torch.bfloat16
+
+    @property
+    def esize(self) -> int:
+        return 4 if self.dtype == "f32" else 2
+
+    def replace(self, **kw) -> "PrefillWorkload":
+        return dataclasses.replace(self, **kw)
+
+
+def _mixed_lengths(seed: int, n: int, lo: int, hi: int) -> tuple:
+    rng = np.random.default_rng(seed)
+    return tuple(int(v) for v in rng.integers(lo, hi + 1, size=n))
+
+
+PREFILL_WORKLOADS = {
+    w.name: w
+    for w in [
+        # small: ragged lengths (an empty one, a single token, lengths around the chunk size),
+        # a padded sequence and one without an initial state
+        PrefillWorkload("prefill_n6_mixed_dim4096_w4_bf16", lengths=(37, 1, 0, 256, 300, 129), dim=4096, width=4,
+                        qk_channels=2048, head_dim=128, dtype="bf16", bias=True, pad=(4,), no_init=(1, 3),
+                        extra_slots=2, seed=20),
+        # the benchmark shape of the verify (dim 10240, q|k 4096, head_dim 128, width 4, bf16) over
+        # 8 prompts of 1024..7168 tokens (about 32k tokens), every other one without a cached state
+        PrefillWorkload("prefill_n8_len1k_7k_dim10240_w4_bf16", lengths=_mixed_lengths(21, 8, 1024, 7168),
+                        dim=10240, width=4, qk_channels=4096, head_dim=128, dtype="bf16", no_init=(1, 3, 5, 7),
+                        extra_slots=8, seed=21),
+    ]
+}
+PREFILL_ORDER = list(PREFILL_WORKLOADS)
+PREFILL_BENCH = "prefill_n8_len1k_7k_dim10240_w4_bf16"
+
+
+def make_prefill_inputs(w: PrefillWorkload, seed: Optional[int] = None) -> dict:
+    """CPU tensors for one prefill: x [total, dim] (a view with token stride x_row_stride when
+    set), conv_state [n_slots, dim, W-1], weight [dim, W], bias [dim] or None, cu_seqlens int32
+    [n_seq+1], cache_idx int32 [n_seq] (-1 = padded), has_initial_state int32 [n_seq], and a
+    sentinel-filled out [total, dim]."""
+    rng = np.random.default_rng(w.seed if seed is None else seed)
+    dt = w.torch_dtype
+    total = w.total_tokens
+    row = w.x_row_stride or w.dim
+    x_wide = _to_dtype(rng.standard_normal((max(total, 1), row), dtype=np.float32), dt)
+    x = x_wide[:total, : w.dim]
+    state = _to_dtype(rng.standard_normal((w.n_slots, w.dim, w.width - 1), dtype=np.float32), dt)
+    weight = _to_dtype(rng.uniform(-0.5, 0.5, size=(w.dim, w.width)).astype(np.float32), dt)
+    bias = _to_dtype(rng.normal(0.0, 0.1, size=(w.dim,)).astype(np.float32), dt) if w.bias else None
+    perm = rng.permutation(w.n_slots)[: w.n_seq].astype(np.int32)
+    for i in w.pad:
+        perm[i] = -1
+    cu = np.zeros(w.n_seq + 1, dtype=np.int32)
+    cu[1:] = np.cumsum(np.asarray(w.lengths, dtype=np.int64))
+    init = np.ones(w.n_seq, dtype=np.int32)
+    for i in w.no_init:
+        init[i] = 0
+    out = sentinel_tensor((total, w.dim), dt)
+    return dict(x=x, x_base=x_wide, conv_state=state, weight=weight, bias=bias, cu_seqlens=torch.from_numpy(cu),
+                cache_idx=torch.from_numpy(perm.copy()), has_initial_state=torch.from_numpy(init), out=out)
+
+
+def prefill_algorithmic_bytes(w: PrefillWorkload) -> int:
+    """Bytes a prefill must move: x read and out written for every token of an active sequence,
+    the initial window read (sequences with one) and the final window written per active sequence,
+    weights and bias once, the index arrays once."""
+    e = w.esize
+    act = [i for i in range(w.n_seq) if i not in w.pad]
+    tokens = sum(w.lengths[i] for i in act)
+    windows = sum((2 if i not in w.no_init else 1) for i in act) * (w.width - 1) * w.dim
+    shared = (w.dim * w.width + (w.dim if w.bias else 0)) * e + 4 * (3 * w.n_seq + 1)
+    return (2 * tokens * w.dim + windows) * e + shared

@@ -10,6 +10,7 @@ import pytest
 
 import oracle
 import test_oracle_pins as pins
+import test_oracle_prefill_pins as ppins
 
 SRC = os.path.join(os.path.dirname(oracle.__file__), "oracle.c")
 
@@ -49,6 +50,14 @@ MUTANTS = [
     ("recompute_verify_writes_state", "if (a->recompute) continue; /* outputs only",
      "if (a->recompute) { put_bits(a->state, bf, srow, full[T]); continue; } /* outputs only",
      lambda: pins.test_r1_recompute_verify_writes_outputs_only(3, "f32")),
+    ("prefill_init_ignored", "full[k] = init ? get_bits(a->state, bf, srow + k) : 0u;",
+     "full[k] = get_bits(a->state, bf, srow + k);", lambda: ppins.test_pf4_no_initial_state_is_a_zero_window()),
+    ("prefill_state_lags", "put_bits(a->state, bf, srow + k, full[L + k]);",
+     "put_bits(a->state, bf, srow + k, full[L > 0 ? L - 1 + k : k]);",
+     lambda: ppins.test_pf3_split_prompt_equals_whole()),
+    ("prefill_token_offset", "full[W - 1 + t] = get_bits(a->x, bf, (int64_t)(b + t) * a->x_tok + c);",
+     "full[W - 1 + t] = get_bits(a->x, bf, (int64_t)(t) * a->x_tok + c);",
+     lambda: ppins.test_pf5_packed_equals_separate_and_untouched()),
     ("padded_row_written", "if (slot < 0 || st) continue;\n\n", "if (st) continue;\n        if (slot < 0) { if (a->out) put_bits(a->out, bf, (int64_t)s * a->out_seq, 0); continue; }\n\n",
      lambda: pins.test_p7_padded_rows_untouched()),
 ]
