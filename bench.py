@@ -389,13 +389,177 @@ def run_ours(args, w, world, rank, local, dist):
     return 0
 
 
+# ----------------------------------------------------------------------------- prefill workloads
+
+def prefill_config(w, l2_note):
+    c = {"workload": w.name, "n_seq": w.n_seq, "total_tokens": w.total_tokens, "max_seqlen": w.max_seqlen,
+         "dim": w.dim, "width": w.width, "qk_channels": w.qk_channels, "head_dim": w.head_dim,
+         "padded_seqs": len(w.pad), "without_initial_state": len(w.no_init), "step": "cv_conv_prefill"}
+    if l2_note:
+        c["l2"] = l2_note
+    return c
+
+
+def oracle_prefill_times(w, reps_max: int, budget_s: float):
+    """Time the oracle prefill on the whole workload (one core); returns per-step seconds."""
+    import oracle
+    inp = wl.make_prefill_inputs(w)
+    times = []
+    t_begin = time.perf_counter()
+    for _ in range(reps_max):
+        state, out = inp["conv_state"].clone(), inp["out"].clone()
+        t0 = time.perf_counter()
+        oracle.conv_prefill(inp["x"], state, inp["weight"], inp["bias"], out, inp["cu_seqlens"],
+                            qk_channels=w.qk_channels, head_dim=w.head_dim, l2_eps=w.l2_eps,
+                            cache_idx=inp["cache_idx"], has_initial_state=inp["has_initial_state"])
+        times.append(time.perf_counter() - t0)
+        if time.perf_counter() - t_begin > budget_s and len(times) >= 1:
+            break
+    return times
+
+
+def run_reference_prefill(args, w, world, rank):
+    if rank != 0:
+        return 0
+    import oracle
+    oracle.build()
+    warm = oracle_prefill_times(w, 1, 1e9)
+    times = oracle_prefill_times(w, args.steps, args.cpu_budget_s * 6)
+    us = statistics.mean(times) * 1e6
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(us, 3), "unit": UNIT, "n_gpus": world,
+        "steps": len(times), "warmup": len(warm), "ms_per_step": round(us / 1e3, 6), "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+        "config": prefill_config(w, None),
+        "cpu_baseline": {"value": round(us, 3), "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": f"whole workload ({w.total_tokens} tokens) per step, {len(times)} steps; "
+                                   f"plain C loop, one thread"},
+        "e2e": {"value": round(us, 3), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours_prefill(args, w, world, rank, local, dist):
+    import spec_decode_verify_gb300 as cv
+    from spec_decode_verify_gb300 import build as cvbuild
+
+    cvbuild.build()
+    lib = cv.load_library()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    sp = stream.cuda_stream
+    inp = wl.make_prefill_inputs(w, seed=w.seed + 1009 * rank)
+    props = torch.cuda.get_device_properties(dev)
+    l2 = getattr(props, "L2_cache_size", 0) or 129 * 2 ** 20
+    per_set = sum(inp[k].numel() * inp[k].element_size() for k in ("x_base", "conv_state", "out"))
+    n_sets = max(2, math.ceil(4 * l2 / per_set))
+    l2_note = f"rotating {n_sets} buffer sets, {n_sets * per_set / 2**20:.0f} MiB >= 4x L2 ({l2 / 2**20:.0f} MiB)"
+    weight = inp["weight"].to(dev)
+    bias = inp["bias"].to(dev) if inp["bias"] is not None else None
+    cu, cidx, init = (inp[k].to(dev) for k in ("cu_seqlens", "cache_idx", "has_initial_state"))
+    sets = []
+    for _ in range(n_sets):
+        xb = inp["x_base"].to(dev)
+        x = xb.as_strided(inp["x"].shape, inp["x"].stride(), inp["x"].storage_offset())
+        s = dict(x_base=xb, x=x, conv_state=inp["conv_state"].to(dev), out=inp["out"].to(dev))
+        s["pa"] = cv.make_prefill_args(x, s["conv_state"], weight, bias, s["out"], cu, max_seqlen=w.max_seqlen,
+                                       qk_channels=w.qk_channels, head_dim=w.head_dim, l2_eps=w.l2_eps,
+                                       cache_idx=cidx, has_initial_state=init)
+        sets.append(s)
+    refs = [ctypes.byref(s["pa"]) for s in sets]
+    fn = lib.cv_conv_prefill
+
+    for i in range(args.warmup):
+        if fn(refs[i % n_sets], sp) != 0:
+            raise RuntimeError("launch failed during warm-up")
+    torch.cuda.synchronize(dev)
+    sampler = ClockSampler(dev.index)
+    sampler.start()
+    t_end = time.perf_counter() + args.clock_probe_s
+    i = 0
+    while time.perf_counter() < t_end:
+        fn(refs[i % n_sets], sp)
+        i += 1
+        if i % 16 == 0:
+            torch.cuda.synchronize(dev)
+    torch.cuda.synchronize(dev)
+    K = args.steps
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(dist, dev)
+    torch.cuda.synchronize(dev)
+    torch.cuda._sleep(int(min(2e9, 400000 * K + 2e6)))
+    start.record(stream)
+    for i in range(K):
+        fn(refs[i % n_sets], sp)
+    end.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(dist, dev)
+    clocks = sampler.stop()
+    step_us = reduce_max(dist, start.elapsed_time(end) * 1e3 / K, dev)
+
+    e2e = None
+    if not args.no_e2e:
+        s0 = sets[0]
+        x_host = inp["x_base"].clone().pin_memory()
+        out_host = torch.empty_like(s0["out"], device="cpu").pin_memory()
+        h2d = x_host.numel() * x_host.element_size()
+        d2h = out_host.numel() * out_host.element_size()
+        for _ in range(3):
+            s0["x_base"].copy_(x_host, non_blocking=True)
+            fn(refs[0], sp)
+            out_host.copy_(s0["out"], non_blocking=True)
+        torch.cuda.synchronize(dev)
+        barrier(dist, dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(K):
+            s0["x_base"].copy_(x_host, non_blocking=True)
+            fn(refs[0], sp)
+            out_host.copy_(s0["out"], non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier(dist, dev)
+        e2e_us = reduce_max(dist, e0.elapsed_time(e1) * 1e3 / K, dev)
+        e2e = {"value": round(e2e_us, 3), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+    if rank != 0:
+        return 0
+    nbytes = wl.prefill_algorithmic_bytes(w)
+    peak, peak_kind = measured_peak()
+    achieved = nbytes / (step_us * 1e-6) / 1e9
+    traffic, traffic_src = profile_traffic(w.name)
+    line = {
+        "metric": METRIC, "value": round(step_us, 3), "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": round(step_us / 1e3, 6), "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+        "config": prefill_config(w, l2_note),
+        "prefill_us": round(step_us, 3), "prefill_gbs": round(achieved, 1), "prefill_algorithmic_bytes": nbytes,
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": traffic, "kernel": "prefill_conv",
+                     "peak_source": f"{peak_kind} hbm_gbs (copy)", "traffic_source": traffic_src},
+        "gpu_launches": K,
+        "clocks": clocks,
+        "e2e": e2e,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        times = oracle_prefill_times(w, 20, args.cpu_budget_s)
+        line["cpu_baseline"] = {"value": round(statistics.median(times) * 1e6, 1), "unit": UNIT, "cores": 1,
+                                "kind": "oracle",
+                                "sample": f"whole workload ({w.total_tokens} tokens) per step, median of {len(times)} "
+                                          f"steps; plain C loop, one thread"}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default=wl.BENCH_WORKLOAD, choices=wl.WORKLOAD_ORDER)
+    ap.add_argument("--workload", default=wl.BENCH_WORKLOAD, choices=wl.WORKLOAD_ORDER + wl.PREFILL_ORDER)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--clock-probe-s", type=float, default=1.5)
@@ -403,9 +567,14 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
-    w = wl.WORKLOADS[args.workload]
     world, rank, local, dist = dist_setup()
     try:
+        if args.workload in wl.PREFILL_WORKLOADS:
+            w = wl.PREFILL_WORKLOADS[args.workload]
+            if args.impl == "reference":
+                return run_reference_prefill(args, w, world, rank)
+            return run_ours_prefill(args, w, world, rank, local, dist)
+        w = wl.WORKLOADS[args.workload]
         if args.impl == "reference":
             return run_reference(args, w, world, rank)
         return run_ours(args, w, world, rank, local, dist)

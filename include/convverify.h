@@ -108,6 +108,8 @@ enum {
 #define CV_SEQ_BAD_SLOT 1   /* cache slot >= n_slots */
 #define CV_SEQ_BAD_OFFSET 2 /* state offset < 0 or offset + W-1 > state_cols */
 #define CV_SEQ_BAD_ACCEPT 4 /* accept count outside 1..T (commit only) */
+#define CV_SEQ_TIMEOUT 8    /* a bounded wait for a bulk copy gave up (the sequence may be partly written) */
+#define CV_SEQ_BAD_SPAN 16  /* prefill: token span invalid or longer than max_seqlen */
 
 /*
  * cv_conv_verify -- [atlas-batched] fused multi-token verify, batched over sequences.
@@ -220,6 +222,55 @@ typedef struct cv_commit_args {
 } cv_commit_args;
 
 CV_API int cv_conv_commit(const cv_commit_args *args, void *stream);
+
+/*
+ * cv_conv_prefill -- the conv over whole prompts, packed back to back ([kda-mod], the layer's
+ * prefill path: conv + SiLU over every prompt token, then the L2 normalisation of q|k).
+ *
+ * Sequence s owns tokens [cu_seqlens[s], cu_seqlens[s+1]) of x and out (L = its length, 0
+ * allowed).  With slot = cache_idx ? cache_idx[s] : s and slot >= 0, for every channel c:
+ *     full = [w0, x[cu_seqlens[s]][c], ..., x[cu_seqlens[s]+L-1][c]]      (W-1+L values)
+ * where w0 = conv_state[slot][c][0 .. W-2] if has_initial_state[s] (or has_initial_state is
+ * NULL), else W-1 zeros.  Token t's output is computed exactly as cv_conv_verify's output for
+ * token t (conv, SiLU, the L2 normalisation of the q|k groups applied to the fp32 values, one
+ * rounding), and afterwards conv_state[slot][c][0 .. W-2] = full[L .. L+W-2] (the last W-1
+ * inputs, raw bits).  State columns >= W-1 are not touched; a sequence with slot < 0 touches
+ * nothing.  Device-side problems go to err[s]: CV_SEQ_BAD_SLOT, or CV_SEQ_BAD_SPAN when the span
+ * is reversed, leaves [0, total_tokens) or is longer than max_seqlen; that sequence is untouched.
+ *
+ * Arguments (all in cv_prefill_args):
+ *   n_seq, dim, width, qk_channels, head_dim, dtype, l2_eps   as for cv_conv_verify
+ *   total_tokens       rows of x and out (>= 0)
+ *   max_seqlen         host-side bound on every L (sizes the grid), >= 0
+ *   x                  [total_tokens][dim] read-only; token stride x_tok_stride, channel stride 1
+ *   out                [total_tokens][dim] write-only; token stride out_tok_stride, channel stride 1
+ *   cu_seqlens         int32 [n_seq + 1] device array (required)
+ *   conv_state         [n_slots][dim][state_cols], column stride 1, read-modify-write
+ *   cache_idx, has_initial_state, err   int32 [n_seq] device arrays or NULL
+ *   weight, bias       [dim][W] and [dim] (bias may be NULL)
+ * Returns CV_OK after the launch is queued, or a negative CV_ERR_* code with nothing launched.
+ */
+typedef struct cv_prefill_args {
+    int32_t n_seq, dim, width, qk_channels, head_dim;
+    int32_t dtype; /* cv_dtype */
+    float l2_eps;
+    int32_t total_tokens, max_seqlen;
+    const void *x;
+    int64_t x_tok_stride;
+    void *out;
+    int64_t out_tok_stride;
+    const int32_t *cu_seqlens;
+    void *conv_state;
+    int32_t n_slots, state_cols;
+    int64_t state_slot_stride, state_ch_stride;
+    const int32_t *cache_idx;
+    const int32_t *has_initial_state;
+    const void *weight;
+    const void *bias;
+    int32_t *err;
+} cv_prefill_args;
+
+CV_API int cv_conv_prefill(const cv_prefill_args *args, void *stream);
 
 /*
  * cv_verify_plan -- validate `args` exactly as cv_conv_verify does and report the launch it would

@@ -7,6 +7,7 @@ CPU path: CPU tensors are rejected and a missing library raises.
 
     conv_verify(x, conv_state, weight, bias, out, window, layout=..., qk_channels=..., head_dim=...)
     conv_commit(conv_state, window, accept_len, layout=..., T=..., width=..., x=...)
+    conv_prefill(x, conv_state, weight, bias, out, cu_seqlens, max_seqlen=..., qk_channels=..., head_dim=...)
 """
 from __future__ import annotations
 
@@ -14,7 +15,7 @@ import ctypes
 import os
 from typing import Optional
 
-__all__ = ["conv_verify", "conv_commit", "verify_plan", "status_string", "load_library", "library_path",
+__all__ = ["conv_verify", "conv_commit", "conv_prefill", "verify_plan", "status_string", "load_library", "library_path",
            "CvError", "DENSE", "DEDUP", "HISTORY", "RECOMPUTE", "SEQ_BAD_SLOT", "SEQ_BAD_OFFSET", "SEQ_BAD_ACCEPT"]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -22,7 +23,7 @@ library_path = os.path.join(_PKG, "_build", "libconvverify.so")
 
 DENSE, DEDUP, HISTORY, RECOMPUTE = 1, 2, 3, 4
 F32, BF16 = 0, 1
-SEQ_BAD_SLOT, SEQ_BAD_OFFSET, SEQ_BAD_ACCEPT = 1, 2, 4
+SEQ_BAD_SLOT, SEQ_BAD_OFFSET, SEQ_BAD_ACCEPT, SEQ_TIMEOUT, SEQ_BAD_SPAN = 1, 2, 4, 8, 16
 MAX_T = 128
 
 c_i32, c_i64, c_vp = ctypes.c_int32, ctypes.c_int64, ctypes.c_void_p
@@ -55,6 +56,18 @@ class CommitArgs(ctypes.Structure):
     ]
 
 
+class PrefillArgs(ctypes.Structure):
+    """Mirror of cv_prefill_args."""
+    _fields_ = [
+        ("n_seq", c_i32), ("dim", c_i32), ("width", c_i32), ("qk_channels", c_i32), ("head_dim", c_i32),
+        ("dtype", c_i32), ("l2_eps", ctypes.c_float), ("total_tokens", c_i32), ("max_seqlen", c_i32),
+        ("x", c_vp), ("x_tok_stride", c_i64), ("out", c_vp), ("out_tok_stride", c_i64), ("cu_seqlens", c_vp),
+        ("conv_state", c_vp), ("n_slots", c_i32), ("state_cols", c_i32), ("state_slot_stride", c_i64),
+        ("state_ch_stride", c_i64), ("cache_idx", c_vp), ("has_initial_state", c_vp), ("weight", c_vp),
+        ("bias", c_vp), ("err", c_vp),
+    ]
+
+
 class LaunchPlan(ctypes.Structure):
     """Mirror of cv_launch_plan."""
     _fields_ = [("grid_x", c_i32), ("grid_y", c_i32), ("threads", c_i32), ("smem_bytes", c_i32),
@@ -83,6 +96,8 @@ def load_library(path: Optional[str] = None):
     lib.cv_conv_verify.restype = c_i32
     lib.cv_conv_commit.argtypes = [ctypes.POINTER(CommitArgs), c_vp]
     lib.cv_conv_commit.restype = c_i32
+    lib.cv_conv_prefill.argtypes = [ctypes.POINTER(PrefillArgs), c_vp]
+    lib.cv_conv_prefill.restype = c_i32
     lib.cv_verify_plan.argtypes = [ctypes.POINTER(VerifyArgs), ctypes.POINTER(LaunchPlan)]
     lib.cv_verify_plan.restype = c_i32
     lib.cv_status_string.argtypes = [c_i32]
@@ -242,3 +257,46 @@ def conv_commit(conv_state, window, accept_len, *, layout, T, width, cache_idx=N
     rc = load_library().cv_conv_commit(ctypes.byref(a), _stream_ptr(stream))
     if rc != 0:
         raise CvError(rc, "cv_conv_commit")
+
+
+def make_prefill_args(x, conv_state, weight, bias, out, cu_seqlens, *, max_seqlen, qk_channels, head_dim,
+                      l2_eps=1e-6, cache_idx=None, has_initial_state=None, err=None, check_device=True) -> PrefillArgs:
+    """Build cv_prefill_args from tensors.
+
+    x, out [total_tokens, dim] (channel stride 1, any token stride), conv_state [n_slots, dim, S]
+    (column stride 1), weight [dim, W] contiguous, bias [dim] or None, cu_seqlens int32
+    [n_seq + 1], cache_idx / has_initial_state / err int32 [n_seq] or None; max_seqlen bounds
+    every sequence's length (host int)."""
+    ptr = _dev_ptr if check_device else (lambda t, n, required=True: None if t is None else t.data_ptr())
+    total, dim = x.shape
+    if x.stride(1) != 1 or out.stride(1) != 1 or conv_state.stride(2) != 1:
+        raise ValueError("x, out and conv_state need a unit innermost stride")
+    if not weight.is_contiguous() or (bias is not None and not bias.is_contiguous()):
+        raise ValueError("weight and bias must be contiguous")
+    return PrefillArgs(
+        n_seq=cu_seqlens.shape[0] - 1, dim=dim, width=weight.shape[1], qk_channels=qk_channels, head_dim=head_dim,
+        dtype=_dtype_code(x), l2_eps=l2_eps, total_tokens=total, max_seqlen=int(max_seqlen),
+        x=ptr(x, "x", total > 0), x_tok_stride=x.stride(0), out=ptr(out, "out", total > 0),
+        out_tok_stride=out.stride(0), cu_seqlens=ptr(cu_seqlens, "cu_seqlens"),
+        conv_state=ptr(conv_state, "conv_state"), n_slots=conv_state.shape[0], state_cols=conv_state.shape[2],
+        state_slot_stride=conv_state.stride(0), state_ch_stride=conv_state.stride(1),
+        cache_idx=ptr(cache_idx, "cache_idx", False), has_initial_state=ptr(has_initial_state, "has_initial_state", False),
+        weight=ptr(weight, "weight"), bias=ptr(bias, "bias", False), err=ptr(err, "err", False))
+
+
+def conv_prefill(x, conv_state, weight, bias, out, cu_seqlens, *, max_seqlen, qk_channels, head_dim, l2_eps=1e-6,
+                 cache_idx=None, has_initial_state=None, err=None, stream=None) -> None:
+    """Queue one packed variable-length prefill on ``stream`` (default: torch's current stream).
+
+    Writes out, conv_state (and err); raises CvError on an invalid argument."""
+    for t in (x, conv_state, weight, out):
+        if t.dtype != x.dtype:
+            raise TypeError("x, conv_state, weight and out must share one dtype")
+    if bias is not None and bias.dtype != x.dtype:
+        raise TypeError("bias must have the dtype of x")
+    a = make_prefill_args(x, conv_state, weight, bias, out, cu_seqlens, max_seqlen=max_seqlen, qk_channels=qk_channels,
+                          head_dim=head_dim, l2_eps=l2_eps, cache_idx=cache_idx, has_initial_state=has_initial_state,
+                          err=err)
+    rc = load_library().cv_conv_prefill(ctypes.byref(a), _stream_ptr(stream))
+    if rc != 0:
+        raise CvError(rc, "cv_conv_prefill")

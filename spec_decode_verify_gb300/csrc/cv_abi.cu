@@ -35,6 +35,8 @@ constexpr int kCommitRowThreads = 64;  // dedup commit: 512 channels per block
 constexpr int kSmemMax = 227 * 1024;
 // the pipelined kernel lists the active sequences in shared memory up to this batch size
 constexpr int kCompactMaxSeq = 1024;
+constexpr int kPrefillMaxChunk = 256;  // tokens per prefill block, at most / at least (multiples of
+constexpr int kPrefillMinChunk = 32;   // the kernel's 8-token batch, and >= W-1)
 
 bool pipe_compacts(const cv_verify_args *a) { return a->cache_idx != nullptr && a->n_seq <= kCompactMaxSeq; }
 
@@ -404,9 +406,84 @@ int launch_commit(const cv_commit_args *a, cudaStream_t stream) {
     return cudaGetLastError() == cudaSuccess ? CV_OK : CV_ERR_LAUNCH;
 }
 
+int check_prefill(const cv_prefill_args *a) {
+    if (!a) return CV_ERR_NULL_ARGS;
+    if (a->dtype != CV_F32 && a->dtype != CV_BF16) return CV_ERR_DTYPE;
+    if (a->width < 2 || a->width > 4) return CV_ERR_WIDTH;
+    if (a->n_seq < 0 || a->n_seq > 65535 || a->dim < 1 || a->n_slots < 1 || a->state_cols < a->width - 1 ||
+        a->total_tokens < 0 || a->max_seqlen < 0)
+        return CV_ERR_SHAPE;
+    if (a->qk_channels < 0 || a->qk_channels > a->dim) return CV_ERR_HEAD_DIM;
+    if (a->qk_channels > 0 && (!pow2(a->head_dim) || a->head_dim < 8 || a->head_dim > 256 ||
+                               a->qk_channels % a->head_dim != 0))
+        return CV_ERR_HEAD_DIM;
+    if (a->x_tok_stride < 0 || a->out_tok_stride < 0 || a->state_slot_stride < 0 || a->state_ch_stride < 0)
+        return CV_ERR_STRIDE;
+    if (a->dim > 1 && a->state_ch_stride < a->state_cols) return CV_ERR_STRIDE;
+    if (a->n_seq > 0 && (!a->cu_seqlens || !a->conv_state || !a->weight)) return CV_ERR_NULL_POINTER;
+    if (a->n_seq > 0 && a->total_tokens > 0 && (!a->x || !a->out)) return CV_ERR_NULL_POINTER;
+    if (a->n_seq > 0 && a->out && (a->out == a->x || a->out == a->conv_state || a->out == a->weight))
+        return CV_ERR_ALIAS;
+    return CV_OK;
+}
+
+int launch_prefill(const cv_prefill_args *a, cudaStream_t stream) {
+    const int esize = a->dtype == CV_BF16 ? 2 : 4;
+    cvk::PrefillParams p;
+    std::memset(&p, 0, sizeof p);
+    p.x = a->x;
+    p.x_tok = a->x_tok_stride;
+    p.out = a->out;
+    p.out_tok = a->out_tok_stride;
+    p.cu_seqlens = a->cu_seqlens;
+    p.state = a->conv_state;
+    p.st_slot = a->state_slot_stride;
+    p.st_ch = a->state_ch_stride;
+    p.cache_idx = a->cache_idx;
+    p.has_init = a->has_initial_state;
+    p.weight = a->weight;
+    p.bias = a->bias;
+    p.err = a->err;
+    p.n_slots = a->n_slots;
+    p.total_tokens = a->total_tokens;
+    p.max_seqlen = a->max_seqlen;
+    p.dim = a->dim;
+    p.qk_channels = a->qk_channels;
+    p.head_dim = a->qk_channels > 0 ? a->head_dim : 8;
+    p.eps = a->l2_eps;
+    const int cpt = (a->qk_channels > 0 && a->head_dim / 4 > 32) ? 8 : 4;
+    // vector rows need the whole run of a thread 16-byte aligned (8 for 4 bf16 channels)
+    p.x_vec = a->dim % 8 == 0 && aligned16(a->x) && stride16(a->x_tok_stride, esize);
+    p.out_vec = a->dim % 8 == 0 && aligned16(a->out) && stride16(a->out_tok_stride, esize);
+    int threads = 128;
+    while (threads > 32 && cpt * (threads / 2) >= a->dim) threads /= 2;
+    while (a->qk_channels > 0 && cpt * threads < a->head_dim) threads *= 2;
+    const long long bc = (long long)cpt * threads;
+    const long long nblk = (a->dim + bc - 1) / bc;
+    // the longest chunk (fewest halo re-reads) that still gives every SM several blocks
+    int chunk = kPrefillMaxChunk;
+    while (chunk > kPrefillMinChunk &&
+           nblk * a->n_seq * ((a->max_seqlen + chunk - 1) / chunk) < 8LL * kNumSMs)
+        chunk /= 2;
+    p.chunk = chunk;
+    const long long chunks = a->max_seqlen > 0 ? (a->max_seqlen + chunk - 1) / chunk : 1;
+    if (chunks > 65535) return CV_ERR_SHAPE;
+    const dim3 grid((unsigned)((a->dim + bc - 1) / bc), (unsigned)chunks, (unsigned)a->n_seq);
+    auto k = kernel_set(a->dtype, a->width).prefill[cpt == 8 ? 1 : 0];
+    if (launch_pdl(k, grid, threads, 0, stream, p) != cudaSuccess) return CV_ERR_LAUNCH;
+    return cudaGetLastError() == cudaSuccess ? CV_OK : CV_ERR_LAUNCH;
+}
+
 }  // namespace
 
 extern "C" {
+
+int cv_conv_prefill(const cv_prefill_args *args, void *stream) {
+    const int rc = check_prefill(args);
+    if (rc != CV_OK) return rc;
+    if (args->n_seq == 0) return CV_OK;
+    return launch_prefill(args, reinterpret_cast<cudaStream_t>(stream));
+}
 
 int cv_verify_plan(const cv_verify_args *args, cv_launch_plan *plan) {
     if (!plan) return CV_ERR_NULL_POINTER;

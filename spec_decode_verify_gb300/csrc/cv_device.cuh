@@ -47,6 +47,25 @@ struct CommitParams {
     long long x_seq, x_tok;
 };
 
+struct PrefillParams {
+    const void *x;
+    long long x_tok;
+    void *out;
+    long long out_tok;
+    const int *cu_seqlens;  // [n_seq + 1]
+    void *state;
+    long long st_slot, st_ch;
+    const int *cache_idx;
+    const int *has_init;  // [n_seq] or null (every sequence has an initial window)
+    const void *weight;
+    const void *bias;
+    int *err;
+    int n_slots, total_tokens, max_seqlen, dim, qk_channels, head_dim;
+    float eps;
+    int x_vec, out_vec;  // vector access of x / out allowed (checked on the host)
+    int chunk;           // tokens per block
+};
+
 // Per-sequence status shared by both kernels: 1 = slot out of range, 2 = state offset out of range.
 __device__ __forceinline__ int seq_status(int slot, int off, int n_slots, int state_cols, int R) {
     int st = 0;

@@ -4,6 +4,7 @@
 
 #include "cv_commit.cuh"
 #include "cv_launch.h"
+#include "cv_prefill.cuh"
 #include "cv_verify_fast.cuh"
 #include "cv_verify_generic.cuh"
 #include "cv_verify_pipe.cuh"
@@ -25,6 +26,8 @@ KernelSet make_set(std::integer_sequence<int, Ts...>) {
     k.commit_rows = commit_rows<B, W>;
     k.commit_recompute = commit_recompute<B, W>;
     k.commit_recompute_vec = commit_recompute_vec<B, W>;
+    k.prefill[0] = prefill_conv<B, W, 4>;
+    k.prefill[1] = prefill_conv<B, W, 8>;
     return k;
 }
 }  // namespace

@@ -7,6 +7,7 @@ namespace cvk {
 
 using VerifyKernel = void (*)(VerifyParams);
 using CommitKernel = void (*)(CommitParams);
+using PrefillKernel = void (*)(PrefillParams);
 
 // Largest T compiled with T as a template parameter (fully unrolled token loop, dedup row built
 // in registers).  Above it the dense layout runs the chunked kernel and the dedup layout the
@@ -25,6 +26,8 @@ struct KernelSet {
     CommitKernel commit_rows;
     CommitKernel commit_recompute;
     CommitKernel commit_recompute_vec;
+    // prefill[c]: c = 0 for 4 channels per thread, 1 for 8
+    PrefillKernel prefill[2];
 };
 
 const KernelSet &kernels_bf16_w2();

@@ -276,3 +276,33 @@ def test_binding_rejects_cpu_tensors(lib):
 def test_missing_library_fails_loudly(tmp_path):
     with pytest.raises(RuntimeError, match="not built"):
         cv.load_library(str(tmp_path / "nope.so"))
+
+
+def _prefill_args(**over):
+    w = wl.PREFILL_WORKLOADS[wl.PREFILL_ORDER[0]]
+    inp = wl.make_prefill_inputs(w)
+    a = cv.make_prefill_args(inp["x"], inp["conv_state"], inp["weight"], inp["bias"], inp["out"], inp["cu_seqlens"],
+                             max_seqlen=w.max_seqlen, qk_channels=w.qk_channels, head_dim=w.head_dim,
+                             cache_idx=inp["cache_idx"], has_initial_state=inp["has_initial_state"], check_device=False)
+    for k, v in over.items():
+        setattr(a, k, v)
+    return a
+
+
+@pytest.mark.parametrize("field,value,status", [
+    ("dtype", 3, -6), ("width", 5, -5), ("n_seq", -1, -3), ("dim", 0, -3), ("total_tokens", -1, -3),
+    ("max_seqlen", -2, -3), ("max_seqlen", 256 * 65536 + 1, -3), ("head_dim", 48, -7), ("qk_channels", 4096 + 8, -7),
+    ("x_tok_stride", -1, -9), ("state_ch_stride", 1, -9), ("cu_seqlens", None, -2), ("weight", None, -2),
+    ("x", None, -2),
+])
+def test_prefill_invalid_arguments_rejected(lib, field, value, status):
+    a = _prefill_args(**{field: value})
+    assert lib.cv_conv_prefill(ctypes.byref(a), None) == status
+
+
+def test_prefill_aliasing_and_empty(lib):
+    a = _prefill_args()
+    a.out = a.x
+    assert lib.cv_conv_prefill(ctypes.byref(a), None) == -10
+    a = _prefill_args(n_seq=0)
+    assert lib.cv_conv_prefill(ctypes.byref(a), None) == 0
