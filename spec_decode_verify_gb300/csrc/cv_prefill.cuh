@@ -12,7 +12,9 @@
 // for the first chunk and the W-1 x rows before the chunk otherwise (a chunk is at least W-1
 // tokens long).  Each thread keeps its channels' window in registers and walks the chunk 8 tokens
 // at a time: the next batch's 8 x rows are loaded (vector loads when aligned) while this batch's
-// conv + SiLU, batched L2 shuffle trees, rounding and stores run.  The first chunk's block also writes the
+// conv + SiLU, batched L2 shuffle trees, rounding and stores run.  The launch bounds hold a
+// thread to 128 registers (4 blocks, 16 warps per SM), which beat more registers with fewer
+// warps, smaller batches with more warps, and a bulk-copy ring of staged rows when timed.  The first chunk's block also writes the
 // final window -- the last W-1 entries of [initial window, x] -- into the state: it is the only
 // block that reads the initial window, so no other block races with that write.
 #pragma once
@@ -25,7 +27,7 @@ constexpr int kPrefillBatch = 8;  // tokens per batch; the next batch's rows loa
 constexpr int kSeqBadSpan = 16;     // err bit: the sequence's token span is invalid
 
 template <typename B, int W, int CPT>
-__global__ void __launch_bounds__(128) prefill_conv(const __grid_constant__ PrefillParams p) {
+__global__ void __launch_bounds__(128, CPT == 4 ? 4 : 2) prefill_conv(const __grid_constant__ PrefillParams p) {
     grid_dep_wait();
     grid_dep_launch();
     constexpr int R = W - 1;
