@@ -118,6 +118,22 @@ int shrink_for_parallelism(int threads, int cpt, const cv_verify_args *a) {
     return threads;
 }
 
+// Units (sequence x channel block) per block of the pipelined kernel's persistent grid, for the
+// block size it would use (an upper bound on its shared-memory residency of 4 blocks per SM).
+double units_per_pipe_block(const cv_verify_args *a, int cpt) {
+    int threads = kPipeThreads;
+    while (threads > 32 && cpt * (threads / 2) >= a->dim) threads /= 2;
+    while (a->qk_channels > 0 && cpt * threads < a->head_dim) threads *= 2;
+    threads = shrink_for_parallelism(threads, cpt, a);
+    const long long bc = (long long)cpt * threads;
+    const long long nblk = (a->dim + bc - 1) / bc;
+    const long long units = (long long)a->n_seq * nblk;
+    long long g = (long long)kNumSMs * pipe_blocks_per_sm(cpt, a->T);
+    if (g >= nblk) g = g / nblk * nblk;
+    if (g > units) g = units;
+    return g > 0 ? (double)units / (double)g : 0.0;
+}
+
 bool state_packed(const void *state, long long slot_stride, long long ch_stride, int width, int esize) {
     return aligned16(state) && stride16(slot_stride, esize) && ch_stride == width - 1;
 }
@@ -137,15 +153,18 @@ int plan_verify(const cv_verify_args *a, cv_launch_plan *pl) {
     const bool recomp = a->window_layout == CV_WINDOW_RECOMPUTE;
     const bool fast = fast_eligible(a, esize, ks.max_static_t);
     const int cpt = (a->qk_channels > 0 && a->head_dim / 4 > 32) ? 8 : 4;
-    // the history layout pipelines when its state rows are exactly the packed [dim][T+W-2] rows
-    const bool hist_pipe = hist && io_packed(a, esize) && a->T <= ks.max_static_t && aligned16(a->conv_state) &&
-                           stride16(a->state_slot_stride, esize) && a->state_ch_stride == a->T + R - 1;
-    // the recompute layout pipelines with packed state rows (it only reads them)
-    const bool recomp_pipe = recomp && io_packed(a, esize) && a->T <= ks.max_static_t &&
-                             state_packed(a->conv_state, a->state_slot_stride, a->state_ch_stride, a->width, esize);
-    if (hist_pipe || recomp_pipe ||
-        (fast && a->T <= ks.max_static_t &&
-         state_packed(a->conv_state, a->state_slot_stride, a->state_ch_stride, a->width, esize))) {
+    // the pipelined kernel stages packed state rows whole (state_ch_stride == state_cols): the
+    // committed windows of [dim][W-1] rows, or wider rows read at an offset; the history layout
+    // needs rows of exactly T+W-2 columns
+    const bool rows_packed = aligned16(a->conv_state) && stride16(a->state_slot_stride, esize) &&
+                             a->state_ch_stride == a->state_cols;
+    bool pipe_ok = io_packed(a, esize) && a->T <= ks.max_static_t && rows_packed &&
+                         (hist ? a->state_cols == a->T + R - 1 : (recomp || fast));
+    const bool wide = !hist && a->state_cols != R;
+    // (wide rows cost whole-row reads and element stores of the window; the pipeline pays that
+    // back only when every block walks at least two units, otherwise the one-pass kernel wins)
+    if (pipe_ok && wide && fast && units_per_pipe_block(a, cpt) < 2.0) pipe_ok = false;
+    if (pipe_ok) {
         auto part = [](long long b) { return (b + 127) / 128 * 128; };
         int threads = kPipeThreads;
         while (threads > 32 && cpt * (threads / 2) >= a->dim) threads /= 2;
@@ -156,8 +175,8 @@ int plan_verify(const cv_verify_args *a, cv_launch_plan *pl) {
         // two stages (x rows + committed windows, or whole history rows) and two image buffers
         // (dedup row + committed windows, or the history row alone; none for the recompute
         // rollback); 2 mbarriers, 2 slots, 2 offsets
-        const long long stage = part(a->T * bc * esize) + part((hist ? Q : R) * bc * esize);
-        long long image = (hist || recomp) ? 0 : part(R * bc * esize);
+        const long long stage = part(a->T * bc * esize) + part((long long)a->state_cols * bc * esize);
+        long long image = (hist || recomp || wide) ? 0 : part(R * bc * esize);
         if (a->window_layout == CV_WINDOW_DEDUP || hist) image += part(Q * bc * esize);
         const long long smem = 2 * stage + 2 * image + 32 + (pipe_compacts(a) ? 16 + 4LL * a->n_seq : 0);
         int per_sm = (int)(kSmemPerSM / (smem + kSmemPerBlockReserved));

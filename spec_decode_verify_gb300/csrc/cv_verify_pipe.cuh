@@ -23,9 +23,11 @@
 // the committed window is taken from columns [off, off+W-1) of it, and the row image is stored
 // back over the state row instead of into a window buffer; there is no separate committed-window
 // image.  Recompute rollback: outputs only; nothing is staged for storing and no bulk store runs.
+// State rows wider than the window (read at a state offset) are staged whole too; the committed
+// window then goes to their first W-1 columns by direct stores.
 // Preconditions (checked on the host): those of the fast path, packed 16-byte-aligned state rows
-// ([dim][W-1], or [dim][T+W-2] for the history layout), T <= 17 (bf16) / 8 (fp32),
-// head_dim / CPT <= 32.
+// (state_ch_stride == state_cols; exactly T+W-2 columns for the history layout), T <= 17 (bf16) /
+// 8 (fp32), head_dim / CPT <= 32.
 #pragma once
 
 #include <type_traits>
@@ -66,7 +68,11 @@ __global__ void __launch_bounds__(128, (CPT == 4 && TS <= 8) ? 4 : 2) verify_pip
     const bool recomp = p.recomp != 0;    // recompute rollback: outputs only
     const bool dense = !p.dedup && !hist;  // dense window (or none): no row image
     const bool has_bias = p.bias != nullptr;
-    const int SC = hist ? Q : R;           // state columns staged per channel
+    // state columns staged per channel: the committed windows of packed [dim][W-1] rows, or whole
+    // rows when they are wider (history rows, or rows read at a state offset)
+    const int SC = p.state_cols;
+    const bool whole_rows = SC != R;
+    const bool wide = whole_rows && !hist;  // wider rows, not history: the window is stored directly
 
     // shared memory: stage 0, stage 1 (x rows + committed windows, or whole history rows), image
     // buffers 0 and 1 (dedup row image + committed-window image, or the history row image alone),
@@ -75,7 +81,7 @@ __global__ void __launch_bounds__(128, (CPT == 4 && TS <= 8) ? 4 : 2) verify_pip
     const long long xb = pipe_part((long long)TS * BC * ES);
     const long long stage_bytes = xb + pipe_part((long long)SC * BC * ES);
     const long long rb = dense ? 0 : pipe_part((long long)Q * BC * ES);
-    const long long img_bytes = recomp ? 0 : rb + (hist ? 0 : pipe_part((long long)R * BC * ES));
+    const long long img_bytes = recomp ? 0 : rb + ((hist || wide) ? 0 : pipe_part((long long)R * BC * ES));
     unsigned char *const img0 = smem + 2 * stage_bytes;
     uint64_t *const bar = reinterpret_cast<uint64_t *>(img0 + 2 * img_bytes);
     volatile int *const info = reinterpret_cast<volatile int *>(bar + 2);  // [0, 2): slots, [2, 4): offsets
@@ -160,7 +166,7 @@ __global__ void __launch_bounds__(128, (CPT == 4 && TS <= 8) ? 4 : 2) verify_pip
         info[2 + st] = off;
         if (go) {
             if (!x_sent) issue_x(k);
-            // packed state rows of SC columns: the committed windows, or whole history rows
+            // packed state rows of SC columns: the committed windows, or whole rows
             mbar_expect_tx(&bar[st], (unsigned)(SC * nch * ES));
             bulk_load(smem + st * stage_bytes + xb,
                       reinterpret_cast<const B *>(p.state) + (long long)slot * p.st_slot + (long long)c0 * SC,
@@ -234,15 +240,15 @@ __global__ void __launch_bounds__(128, (CPT == 4 && TS <= 8) ? 4 : 2) verify_pip
         if (go && act) {
 #pragma unroll
             for (int t = 0; t < TS; ++t) ldv<VX, NW>(xr[t], stg + ((long long)t * BC + cl) * ES);
-            if (hist) {
-                // the committed window sits at columns [off, off+W-1) of each staged history row
+            if (whole_rows) {
+                // the committed window sits at columns [off, off+W-1) of each staged row
                 using U = std::conditional_t<ES == 2, unsigned short, unsigned>;
-                const U *row = reinterpret_cast<const U *>(stg + xb) + (long long)cl * Q + off;
+                const U *row = reinterpret_cast<const U *>(stg + xb) + (long long)cl * SC + off;
                 U v[CPT * R];
 #pragma unroll
                 for (int e = 0; e < CPT; ++e)
 #pragma unroll
-                    for (int kk = 0; kk < R; ++kk) v[e * R + kk] = row[e * Q + kk];
+                    for (int kk = 0; kk < R; ++kk) v[e * R + kk] = row[e * SC + kk];
 #pragma unroll
                 for (int i = 0; i < R * NW; ++i)
                     sw[i] = ES == 2 ? ((uint32_t)v[2 * i] | ((uint32_t)v[(2 * i + 1) % (CPT * R)] << 16)) : (uint32_t)v[i];
@@ -283,7 +289,19 @@ __global__ void __launch_bounds__(128, (CPT == 4 && TS <= 8) ? 4 : 2) verify_pip
                     stv<VS, R * NW>(wsq + (long long)t * p.w_step, w);
                 }
             }
-            if (!hist && !recomp) {
+            if (wide && !recomp) {
+                // committed window -> columns [0, W-1) of the wide rows, stored directly (the rows'
+                // other columns are not this call's to rewrite); this thread alone owns them
+                B *srow = reinterpret_cast<B *>(p.state) + (long long)slot * p.st_slot + (long long)c * SC;
+#pragma unroll
+                for (int e = 0; e < CPT; ++e)
+#pragma unroll
+                    for (int kk = 0; kk < R; ++kk) {
+                        const int j = TS + kk;  // input j of channel e
+                        srow[(long long)e * SC + kk] =
+                            (B)(ES == 2 ? (word_of(e, j) >> (16 * half_of(e, j))) & 0xffffu : word_of(e, j));
+                    }
+            } else if (!hist && !recomp) {
                 uint32_t fin[R * NW];
 #pragma unroll
                 for (int i = 0; i < R * NW; ++i) fin[i] = run_word(i, R, TS);
@@ -315,8 +333,9 @@ __global__ void __launch_bounds__(128, (CPT == 4 && TS <= 8) ? 4 : 2) verify_pip
                     if (!dense)
                         bulk_store(reinterpret_cast<B *>(p.win) + (long long)s * p.w_seq + (long long)c0 * Q, img,
                                    (unsigned)(nch * Q * ES));
-                    bulk_store(reinterpret_cast<B *>(p.state) + (long long)slot * p.st_slot + (long long)c0 * R,
-                               stimg, (unsigned)(nch * R * ES));
+                    if (!wide)
+                        bulk_store(reinterpret_cast<B *>(p.state) + (long long)slot * p.st_slot + (long long)c0 * R,
+                                   stimg, (unsigned)(nch * R * ES));
                 }
                 asm volatile("cp.async.bulk.commit_group;\n" ::: "memory");
             }

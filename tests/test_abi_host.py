@@ -148,7 +148,9 @@ def test_recompute_plan_and_commit_validation(lib):
     assert a.window is None
     rc, pl = _plan(lib, a)
     assert rc == 0 and pl.path == 3 and pl.smem_bytes == _pipe_smem((8 + 3) * 512 * 2, 0, 128)
-    a.state_ch_stride, a.state_cols = 4, 4  # unpacked rows: the general kernel
+    a.state_ch_stride, a.state_cols = 4, 4  # wider packed rows: still pipelined (staged whole)
+    assert _plan(lib, a)[1].path == 3
+    a.state_ch_stride = 6  # rows with gaps: the general kernel
     assert _plan(lib, a)[1].path == 0
     inp = wl.make_inputs(w.replace(n_seq=2, n_pad=0, extra_slots=0))
     c = cv.make_commit_args(inp["conv_state"], None, inp["accept_len"], layout="recompute", T=8, width=4,
@@ -184,8 +186,13 @@ def test_plan_general_path_cases(lib):
     pl = _plan(lib, _args(W3.replace(head_dim=256, qk_channels=4096)))[1]
     assert pl.path == 3 and pl.channels_per_block == 8 * pl.threads  # a 256-channel group needs 8 per thread
     a = _args(W3)
-    a.state_ch_stride = 4  # state rows wider than the window: no bulk copy of the state
+    a.state_ch_stride = 4  # packed rows wider than the window: staged whole (4+ units per block)
     a.state_cols = 4
+    assert _plan(lib, a)[1].path == 3
+    a.n_seq = 32  # too few units per block for wide rows: the one-pass kernel
+    assert _plan(lib, a)[1].path == 1
+    a.n_seq = 128
+    a.state_ch_stride = 8  # rows with a gap between them: no bulk copy of the state
     assert _plan(lib, a)[1].path == 1
     assert _plan(lib, _args(W3.replace(T=12)))[1].path == 3
     a = _args(W3)

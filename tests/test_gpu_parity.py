@@ -267,35 +267,44 @@ def _run_with_state_view(cuda_lib, w, inp, state_dev, x_dev):
 @pytest.mark.parametrize("layout", ["dense", "dedup"])
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 def test_all_paths_bit_identical(cuda_lib, layout, dtype):
-    """The same inputs through the pipelined kernel (packed state rows), the static-T kernel (state
-    rows one column wider, element stores) and the general kernel (x shifted off 16-byte alignment)
-    give bit-identical outputs, snapshots and committed windows -- and match the oracle."""
-    w = wl.VerifyWorkload("paths", n_seq=5, T=6, dim=1536, width=4, qk_channels=512, head_dim=128, dtype=dtype,
-                          layout=layout, bias=True, n_pad=1, extra_slots=2, seed=31)
+    """The same inputs through the pipelined kernel (packed state rows, and packed rows one column
+    wider, staged whole), the static-T kernel (rows with a gap between them, element stores) and
+    the general kernel (x shifted off 16-byte alignment) give bit-identical outputs, snapshots and
+    committed windows -- and match the oracle."""
+    # 420 sequences x 3 channel blocks: enough units per block for wide rows to be pipelined
+    w = wl.VerifyWorkload("paths", n_seq=420, T=6, dim=1536, width=4, qk_channels=512, head_dim=128, dtype=dtype,
+                          layout=layout, bias=True, n_pad=7, extra_slots=2, seed=31)
     inp = wl.make_inputs(w)
     ref = run_oracle_verify(w, inp)
     R = w.width - 1
     results = {}
     # packed state
     p3, d3 = _run_with_state_view(cuda_lib, w, inp, inp["conv_state"].cuda(), to_device(inp)["x"])
-    # wider state rows: [n_slots, dim, R+1] with the window in columns 0..R-1, last column sentinel
+    # packed rows one column wider: [n_slots, dim, R+1], the window in columns 0..R-1
     wide = wl.sentinel_tensor((w.n_slots, w.dim, R + 1), w.torch_dtype)
     wide[:, :, :R] = inp["conv_state"]
-    p1, d1 = _run_with_state_view(cuda_lib, w, inp, wide.cuda(), to_device(inp)["x"])
+    p3w, d3w = _run_with_state_view(cuda_lib, w, inp, wide.cuda(), to_device(inp)["x"])
+    # rows with a gap: a [.., R+1] view of [.., R+2] storage (channel stride R+2)
+    gap = wl.sentinel_tensor((w.n_slots, w.dim, R + 2), w.torch_dtype)
+    gap[:, :, :R] = inp["conv_state"]
+    gap_dev = gap.cuda()
+    p1, d1 = _run_with_state_view(cuda_lib, w, inp, gap_dev[:, :, :R + 1], to_device(inp)["x"])
     # x one element off alignment (copy into a buffer shifted by one element)
     xb = torch.zeros(w.n_seq * w.T * w.dim + 1, dtype=w.torch_dtype)
     xb[1:] = inp["x"].reshape(-1)
     x_odd = xb.cuda()[1:].view(w.n_seq, w.T, w.dim)
     p0, d0 = _run_with_state_view(cuda_lib, w, inp, inp["conv_state"].cuda(), x_odd)
-    assert (p3, p1, p0) == (3, 1, 0)
-    for name, d in (("pipelined", d3), ("static", d1), ("general", d0)):
+    assert (p3, p3w, p1, p0) == (3, 3, 1, 0)
+    for name, d in (("pipelined", d3), ("pipelined wide", d3w), ("static", d1), ("general", d0)):
         assert_bits_equal(d["out"].cpu(), d3["out"].cpu(), f"out {name}")
         assert_bits_equal(d["window"].cpu(), ref["window"], f"window {name}")
         assert_out_close(d["out"].cpu(), ref["out"], f"out {name}")
     assert_bits_equal(d3["conv_state"].cpu(), ref["conv_state"], "state pipelined")
     assert_bits_equal(d0["conv_state"].cpu(), ref["conv_state"], "state general")
+    assert_bits_equal(d3w["conv_state"][:, :, :R].cpu(), ref["conv_state"], "state pipelined wide")
+    assert_bits_equal(d3w["conv_state"][:, :, R:].cpu(), wide[:, :, R:], "state pipelined wide, column past the window")
     assert_bits_equal(d1["conv_state"][:, :, :R].cpu(), ref["conv_state"], "state static")
-    assert_bits_equal(d1["conv_state"][:, :, R:].cpu(), wide[:, :, R:], "state static, column past the window")
+    assert_bits_equal(gap_dev[:, :, R:].cpu(), gap[:, :, R:], "state static, columns past the window")
 
 
 @pytest.mark.parametrize("name", ["n128_t8_dim10240_w4_bf16_dedup_pad13", "n64_t8_dim6144_w3_bf16_dense_nol2_stateoff",
@@ -344,3 +353,23 @@ def test_chained_steps_without_host_sync(cuda_lib, name):
     for i in range(3):
         assert_out_close(outs[i].cpu(), outs_ref[i], f"step {i} out")
     assert_bits_equal(state.cpu(), ref["conv_state"], "state after three steps")
+
+
+@pytest.mark.parametrize("layout", ["dense", "dedup", "recompute"])
+@pytest.mark.parametrize("T,width", [(1, 2), (3, 3), (8, 4), (12, 3), (17, 4)])
+def test_wide_state_rows_pipelined(cuda_lib, layout, T, width):
+    """Packed state rows wider than the window (read at a per-sequence offset) take the pipelined
+    kernel when every block walks several units: it stages the rows whole and stores the committed
+    window into their first W-1 columns directly; every offset 0..T-1 appears and the result equals
+    the oracle's."""
+    w = wl.VerifyWorkload("wide", n_seq=140 + T, T=T, dim=4096 + 512, width=width, qk_channels=1024, head_dim=128,
+                          dtype="bf16", layout=layout, bias=True, n_pad=1, extra_slots=3, state_offset=True,
+                          seed=50 * T + width)
+    inp = wl.make_inputs(w)
+    inp["state_off"] = (torch.arange(w.n_seq, dtype=torch.int32) % T).contiguous()
+    d = {k: (v.to("cuda") if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    pl = cuda_lib.verify_plan(d["x"], d["conv_state"], d["weight"], d["bias"], d["out"], d["window"], layout=layout,
+                              qk_channels=w.qk_channels, head_dim=w.head_dim, cache_idx=d["cache_idx"],
+                              state_off=d["state_off"])
+    assert pl.path == 3
+    check_verify_and_commit(cuda_lib, w, inp)
