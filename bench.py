@@ -40,14 +40,16 @@ METRIC = "verify-conv µs/step and achieved HBM GB/s (% of GB300 peak), 1 GPU"
 UNIT = "us/step"
 HBM_NOMINAL_GBS = 8000.0  # the metric's roofline: bytes moved / 8 TB/s
 PROFILES = os.path.join(ROOT, "profiles")
-# the sources of the verify kernel the benchmark workload runs (the pipelined path)
-KERNEL_SRCS = [os.path.join(ROOT, "spec_decode_verify_gb300", "csrc", f)
-               for f in ("cv_verify_pipe.cuh", "cv_device.cuh")]
+# the sources of the kernel each kind of workload runs (verify: the pipelined path)
+KERNEL_SRCS = {
+    "verify": [os.path.join(ROOT, "spec_decode_verify_gb300", "csrc", f) for f in ("cv_verify_pipe.cuh", "cv_device.cuh")],
+    "prefill": [os.path.join(ROOT, "spec_decode_verify_gb300", "csrc", f) for f in ("cv_prefill.cuh", "cv_device.cuh")],
+}
 
 
-def kernel_sha() -> str:
+def kernel_sha(kind: str = "verify") -> str:
     h = hashlib.sha256()
-    for path in KERNEL_SRCS:
+    for path in KERNEL_SRCS[kind]:
         with open(path, "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -63,9 +65,10 @@ def measured_peak():
         return 6800.0, "fallback"
 
 
-def profile_traffic(workload: str):
-    """DRAM bytes per verify launch from a committed ncu summary of this workload, if it was taken
-    of the current kernel sources (a `bench-traffic:` line in profiles/*.md)."""
+def profile_traffic(workload: str, kind: str = "verify"):
+    """DRAM bytes per launch of the workload's main kernel from a committed ncu summary of this
+    workload, if it was taken of the current kernel sources (a `bench-traffic:` line in
+    profiles/*.md)."""
     stale = False
     for name in sorted(os.listdir(PROFILES)) if os.path.isdir(PROFILES) else []:
         if not name.endswith(".md"):
@@ -75,7 +78,7 @@ def profile_traffic(workload: str):
                              text):
             if m.group(1) != workload:
                 continue
-            if m.group(3) != kernel_sha():
+            if m.group(3) != kernel_sha(kind):
                 stale = True
                 continue
             return int(m.group(2)), f"ncu ({name})"
@@ -529,7 +532,7 @@ def run_ours_prefill(args, w, world, rank, local, dist):
     nbytes = wl.prefill_algorithmic_bytes(w)
     peak, peak_kind = measured_peak()
     achieved = nbytes / (step_us * 1e-6) / 1e9
-    traffic, traffic_src = profile_traffic(w.name)
+    traffic, traffic_src = profile_traffic(w.name, "prefill")
     line = {
         "metric": METRIC, "value": round(step_us, 3), "unit": UNIT, "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": round(step_us / 1e3, 6), "higher_is_better": False,
