@@ -34,7 +34,7 @@ class _VerifyArgs(ctypes.Structure):
         ("state", c_vp), ("n_slots", c_i32), ("state_cols", c_i32), ("st_slot", c_i64), ("st_ch", c_i64),
         ("cache_idx", c_vp), ("state_off", c_vp), ("weight", c_vp), ("bias", c_vp),
         ("window", c_vp), ("dedup", c_i32), ("w_seq", c_i64), ("w_step", c_i64), ("w_ch", c_i64),
-        ("w_col", c_i64), ("status", c_vp), ("history", c_i32), ("recompute", c_i32),
+        ("w_col", c_i64), ("status", c_vp), ("history", c_i32), ("recompute", c_i32), ("state_is_bf16", c_i32),
     ]
 
 
@@ -159,7 +159,9 @@ def conv_verify(x, conv_state, weight, bias, out, window, *, layout, qk_channels
         cache_idx=_ptr(cache_idx), state_off=_ptr(state_off), weight=_ptr(weight), bias=_ptr(bias),
         window=_ptr(window), dedup=1 if layout == "dedup" else 0, w_seq=ws[0], w_step=ws[1], w_ch=ws[2],
         w_col=ws[3], status=_ptr(status), history=1 if layout == "history" else 0,
-        recompute=1 if layout == "recompute" else 0)
+        recompute=1 if layout == "recompute" else 0, state_is_bf16=_is_bf16(conv_state))
+    if window is not None and window.dtype != conv_state.dtype:
+        raise TypeError("the window has the state's dtype")
     rc = _load().oracle_conv_verify(ctypes.byref(a))
     if rc != 0:
         raise RuntimeError(f"oracle_conv_verify returned {rc}")

@@ -65,6 +65,12 @@
  *     snapshot t is what a partial accept rewinds to).  With a accepted tokens (1 <= a <= T) the
  *     state becomes snapshot a-1.
  *
+ *   - Mixed dtypes (sglang PR #46184, "Accuracy Tests": its extra check covers mixed input and state
+ *     dtypes).  The state and the snapshots may be stored in the other dtype than x, out, weight and
+ *     bias.  The arithmetic widens every input exactly to fp32; the snapshots and the state hold
+ *     the inputs converted to the state dtype: raw bits when the dtypes agree, an exact widening
+ *     for bf16 inputs into fp32 state, and round-to-nearest-even (any NaN to the quiet NaN) for
+ *     fp32 inputs into bf16 state.
  *   - Prefill (glm5next_kda mod.rs, the prefill path of the layer: the conv over all T prompt
  *     tokens with SiLU, then the L2 normalisation of q|k, which that code runs as a second launch;
  *     here the normalisation is applied to the fp32 SiLU values and rounded once, as in decode).
@@ -103,6 +109,7 @@ typedef struct {
     int32_t *status; /* [n_seq] or NULL */
     int32_t history;   /* 1: the state row is the snapshot row (no window buffer) */
     int32_t recompute; /* 1: outputs only; no snapshots and the state is not written */
+    int32_t state_is_bf16; /* dtype of state and window: 0 fp32, 1 bf16 (may differ from is_bf16) */
 } oracle_verify_args;
 
 typedef struct {
@@ -154,6 +161,14 @@ static uint32_t float_to_bits(float f, int is_bf16) {
     return u >> 16;
 }
 
+/* An element of x (dtype xbf) in the state's dtype (sbf): raw bits when they agree, else widened
+ * exactly (bf16 -> fp32) or rounded to nearest even (fp32 -> bf16). */
+static uint32_t to_state_bits(uint32_t v, int xbf, int sbf) {
+    if (xbf == sbf) return v;
+    if (xbf) return v << 16;
+    return float_to_bits(bits_to_float(v, 0), 1);
+}
+
 static int64_t win_index(const oracle_verify_args *a, int s, int t, int c, int k) {
     int64_t step = a->dedup ? a->w_col : a->w_step;
     return (int64_t)s * a->w_seq + (int64_t)t * step + (int64_t)c * a->w_ch + (int64_t)k * a->w_col;
@@ -161,8 +176,9 @@ static int64_t win_index(const oracle_verify_args *a, int s, int t, int c, int k
 
 /* Returns 0; per-sequence problems go to status[]. */
 int oracle_conv_verify(const oracle_verify_args *a) {
-    const int W = a->width, T = a->T, dim = a->dim, bf = a->is_bf16;
-    uint32_t full[1024]; /* W-1 + T raw elements of one channel */
+    const int W = a->width, T = a->T, dim = a->dim, bf = a->is_bf16, sbf = a->state_is_bf16;
+    uint32_t full[1024];  /* W-1 + T elements of one channel, as bits of the state's dtype */
+    float fullf[1024];    /* the same inputs widened to fp32 (exact) */
     if (W < 1 || T < 1 || dim < 1 || W - 1 + T > 1024) return -1;
     if (a->history && T + W - 2 > a->state_cols) return -3;
     /* y[t*dim + c]: post-SiLU fp32 values of one sequence, normalised in place below */
@@ -180,15 +196,21 @@ int oracle_conv_verify(const oracle_verify_args *a) {
 
         for (int c = 0; c < dim; ++c) {
             const int64_t srow = (int64_t)slot * a->st_slot + (int64_t)c * a->st_ch;
-            for (int k = 0; k < W - 1; ++k) full[k] = get_bits(a->state, bf, srow + o + k);
-            for (int t = 0; t < T; ++t)
-                full[W - 1 + t] = get_bits(a->x, bf, (int64_t)s * a->x_seq + (int64_t)t * a->x_tok + c);
+            for (int k = 0; k < W - 1; ++k) {
+                full[k] = get_bits(a->state, sbf, srow + o + k);
+                fullf[k] = bits_to_float(full[k], sbf);
+            }
+            for (int t = 0; t < T; ++t) {
+                const uint32_t xv = get_bits(a->x, bf, (int64_t)s * a->x_seq + (int64_t)t * a->x_tok + c);
+                full[W - 1 + t] = to_state_bits(xv, bf, sbf);
+                fullf[W - 1 + t] = bits_to_float(xv, bf);
+            }
 
             for (int t = 0; t < T; ++t) {
                 float acc = a->bias ? bits_to_float(get_bits(a->bias, bf, c), bf) : 0.0f;
                 for (int j = 0; j < W; ++j) {
                     const float wj = bits_to_float(get_bits(a->weight, bf, (int64_t)c * W + j), bf);
-                    const float prod = wj * bits_to_float(full[t + j], bf);
+                    const float prod = wj * fullf[t + j];
                     acc = acc + prod;
                 }
                 y[(int64_t)t * dim + c] = acc / (1.0f + expf(-acc));
@@ -199,16 +221,16 @@ int oracle_conv_verify(const oracle_verify_args *a) {
             if (a->history) {
                 /* snapshot t into the state row itself, at columns t .. t+W-2 (after every read) */
                 for (int t = 0; t < T; ++t)
-                    for (int k = 0; k < W - 1; ++k) put_bits(a->state, bf, srow + t + k, full[t + 1 + k]);
+                    for (int k = 0; k < W - 1; ++k) put_bits(a->state, sbf, srow + t + k, full[t + 1 + k]);
                 continue;
             }
 
             /* snapshot t = window after token t = full[t+1 .. t+W-1] */
             for (int t = 0; t < T; ++t)
-                for (int k = 0; k < W - 1; ++k) put_bits(a->window, bf, win_index(a, s, t, c, k), full[t + 1 + k]);
+                for (int k = 0; k < W - 1; ++k) put_bits(a->window, sbf, win_index(a, s, t, c, k), full[t + 1 + k]);
 
             /* committed window after the last token, written after every read of this row */
-            for (int k = 0; k < W - 1; ++k) put_bits(a->state, bf, srow + k, full[T + k]);
+            for (int k = 0; k < W - 1; ++k) put_bits(a->state, sbf, srow + k, full[T + k]);
         }
 
         for (int t = 0; t < T; ++t) {

@@ -55,6 +55,7 @@ class VerifyWorkload:
     x_row_stride: Optional[int] = None  # token stride of x when it is a slice of a wider buffer
     qkv_split: Optional[tuple] = None  # (q, k, v) channel counts of separately drawn conv weights
     state_offset: bool = False  # per-sequence offset = accept_len - 1 into a wider state row
+    state_dtype: Optional[str] = None  # dtype of state and window when it differs from x ("f32"/"bf16")
     seed: int = 0
 
     @property
@@ -72,8 +73,17 @@ class VerifyWorkload:
         return torch.float32 if self.dtype == "f32" else torch.bfloat16
 
     @property
+    def state_torch_dtype(self):
+        sd = self.state_dtype or self.dtype
+        return torch.float32 if sd == "f32" else torch.bfloat16
+
+    @property
     def esize(self) -> int:
         return 4 if self.dtype == "f32" else 2
+
+    @property
+    def state_esize(self) -> int:
+        return 4 if (self.state_dtype or self.dtype) == "f32" else 2
 
     def replace(self, **kw) -> "VerifyWorkload":
         return dataclasses.replace(self, **kw)
@@ -143,7 +153,7 @@ def make_inputs(w: VerifyWorkload, seed: Optional[int] = None) -> dict:
     xw = rng.standard_normal((w.n_seq * w.T, row), dtype=np.float32)
     x_wide = _to_dtype(xw, dt)
     x = x_wide.view(w.n_seq, w.T, row)[:, :, : w.dim]
-    state = _to_dtype(rng.standard_normal((w.n_slots, w.dim, w.state_cols), dtype=np.float32), dt)
+    state = _to_dtype(rng.standard_normal((w.n_slots, w.dim, w.state_cols), dtype=np.float32), w.state_torch_dtype)
     if w.qkv_split:
         parts = [rng.uniform(-0.5, 0.5, size=(n, 1, w.width)).astype(np.float32) for n in w.qkv_split]
         weight = _to_dtype(np.concatenate(parts, axis=0), dt).squeeze(1)
@@ -159,7 +169,7 @@ def make_inputs(w: VerifyWorkload, seed: Optional[int] = None) -> dict:
     accept = torch.from_numpy(rng.integers(1, w.T + 1, size=w.n_seq).astype(np.int32))
     state_off = (accept - 1).to(torch.int32) if w.state_offset else None
     out = sentinel_tensor((w.n_seq, w.T, w.dim), dt)
-    window = None if w.layout in ("history", "recompute") else sentinel_tensor(window_shape(w), dt)
+    window = None if w.layout in ("history", "recompute") else sentinel_tensor(window_shape(w), w.state_torch_dtype)
     return dict(x=x, x_base=x_wide, conv_state=state, weight=weight, bias=bias, cache_idx=cache_idx,
                 state_off=state_off, accept_len=accept, out=out, window=window)
 
@@ -183,22 +193,23 @@ def algorithmic_bytes(w: VerifyWorkload, n_active: Optional[int] = None) -> dict
     """Bytes the verify and the commit must move (each element once), per the data movement of
     the method: x read, committed window read, outputs written, snapshots written, state written;
     weights and bias read once; the int32 index arrays once."""
-    e = w.esize
+    e, se = w.esize, w.state_esize  # x/out/taps element size; state/window element size
     n = (w.n_seq - w.n_pad) if n_active is None else n_active
     shared = (w.dim * w.width + (w.dim if w.bias else 0)) * e + 4 * w.n_seq * (1 + (1 if w.state_offset else 0))
+    R = w.width - 1
     if w.layout == "history":
         # committed window read; the snapshot row written into the state row; nothing to commit
-        per_seq = (w.T * w.dim + (w.width - 1) * w.dim + w.T * w.dim + (w.T + w.width - 2) * w.dim) * e
+        per_seq = 2 * w.T * w.dim * e + (R + w.T + w.width - 2) * w.dim * se
         return dict(verify=n * per_seq + shared, commit=0, per_seq=per_seq)
     if w.layout == "recompute":
         # verify: x and committed window read, outputs written; commit: the window and the accepted
         # x rows (at most W-1 of them, counted as W-1) read, the window written
-        per_seq = (w.T * w.dim + (w.width - 1) * w.dim + w.T * w.dim) * e
-        commit = n * 3 * (w.width - 1) * w.dim * e + 8 * w.n_seq
+        per_seq = 2 * w.T * w.dim * e + R * w.dim * se
+        commit = n * (2 * R * w.dim * se + R * w.dim * e) + 8 * w.n_seq
         return dict(verify=n * per_seq + shared, commit=commit, per_seq=per_seq)
-    win_cols = (w.T + w.width - 2) if w.layout == "dedup" else w.T * (w.width - 1)
-    per_seq = (w.T * w.dim + (w.width - 1) * w.dim + w.T * w.dim + win_cols * w.dim + (w.width - 1) * w.dim) * e
-    commit = n * 2 * (w.width - 1) * w.dim * e + 8 * w.n_seq
+    win_cols = (w.T + w.width - 2) if w.layout == "dedup" else w.T * R
+    per_seq = 2 * w.T * w.dim * e + (R + win_cols + R) * w.dim * se
+    commit = n * 2 * R * w.dim * se + 8 * w.n_seq
     return dict(verify=n * per_seq + shared, commit=commit, per_seq=per_seq)
 
 

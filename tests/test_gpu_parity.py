@@ -373,3 +373,11 @@ def test_wide_state_rows_pipelined(cuda_lib, layout, T, width):
                               state_off=d["state_off"])
     assert pl.path == 3
     check_verify_and_commit(cuda_lib, w, inp)
+
+
+def test_maximum_batch_on_gpu(cuda_lib):
+    """The largest batch the ABI accepts (65535 sequences; the pipelined kernel then walks every
+    sequence without a shared-memory list), with padded sequences and a pool of unused slots."""
+    w = wl.VerifyWorkload("maxbatch", n_seq=65535, T=3, dim=64, width=4, qk_channels=32, head_dim=16, dtype="bf16",
+                          layout="dedup", bias=True, n_pad=1000, extra_slots=100, seed=65535)
+    check_verify_and_commit(cuda_lib, w, wl.make_inputs(w))

@@ -17,7 +17,7 @@ SRC = os.path.join(os.path.dirname(oracle.__file__), "oracle.c")
 # (id, text in oracle.c, planted replacement, pin that must fail).  Every planted mistake keeps all
 # accesses inside the test's buffers.
 MUTANTS = [
-    ("taps_reversed", "bits_to_float(full[t + j], bf)", "bits_to_float(full[t + W - 1 - j], bf)",
+    ("taps_reversed", "const float prod = wj * fullf[t + j];", "const float prod = wj * fullf[t + W - 1 - j];",
      lambda: pins.test_p2_impulse_response()),
     ("bias_dropped", "float acc = a->bias ? bits_to_float(get_bits(a->bias, bf, c), bf) : 0.0f;", "float acc = 0.0f;",
      lambda: pins.test_p1_matches_float64_conv1d("f32", "dense", 4)),
@@ -27,9 +27,9 @@ MUTANTS = [
      lambda: pins.test_p3_one_hot_taps_and_constant_group()),
     ("snapshot_off_by_one", "win_index(a, s, t, c, k), full[t + 1 + k])", "win_index(a, s, t, c, k), full[t + k])",
      lambda: pins.test_p4_sequential_equals_batched_in_T("dense", "f32")),
-    ("state_write_lags", "put_bits(a->state, bf, srow + k, full[T + k])", "put_bits(a->state, bf, srow + k, full[T - 1 + k])",
+    ("state_write_lags", "put_bits(a->state, sbf, srow + k, full[T + k])", "put_bits(a->state, sbf, srow + k, full[T - 1 + k])",
      lambda: pins.test_p11_single_token_update()),
-    ("offset_ignored", "get_bits(a->state, bf, srow + o + k)", "get_bits(a->state, bf, srow + k)",
+    ("offset_ignored", "get_bits(a->state, sbf, srow + o + k)", "get_bits(a->state, sbf, srow + k)",
      lambda: pins.test_p10_state_offset_equals_preshifted_state()),
     ("commit_wrong_snapshot", "const int t = acc - 1;", "const int t = acc < a->T ? acc : acc - 1;",
      lambda: pins.test_p9_commit_equals_shorter_verify("dedup")),
@@ -58,6 +58,11 @@ MUTANTS = [
     ("prefill_token_offset", "full[W - 1 + t] = get_bits(a->x, bf, (int64_t)(b + t) * a->x_tok + c);",
      "full[W - 1 + t] = get_bits(a->x, bf, (int64_t)(t) * a->x_tok + c);",
      lambda: ppins.test_pf5_packed_equals_separate_and_untouched()),
+    ("mixed_snapshot_truncates", "return float_to_bits(bits_to_float(v, 0), 1);", "return v >> 16;",
+     lambda: pins.test_m3_fp32_inputs_round_into_bf16_snapshots()),
+    ("mixed_state_read_as_x_dtype", "full[k] = get_bits(a->state, sbf, srow + o + k);\n                fullf[k] = bits_to_float(full[k], sbf);",
+     "full[k] = get_bits(a->state, sbf, srow + o + k);\n                fullf[k] = bits_to_float(full[k], bf);",
+     lambda: pins.test_m4_mixed_matches_float64_conv1d("bf16", "f32")),
     ("padded_row_written", "if (slot < 0 || st) continue;\n\n", "if (st) continue;\n        if (slot < 0) { if (a->out) put_bits(a->out, bf, (int64_t)s * a->out_seq, 0); continue; }\n\n",
      lambda: pins.test_p7_padded_rows_untouched()),
 ]

@@ -546,3 +546,86 @@ def test_nan_and_signed_zero_copies():
     assert wb[0, 0, 0, 0] == 0x7FA1
     assert wb[0, 0, 1, 2] == 0x8000 and wb[0, 1, 1, 1] == 0x8000 and wb[0, 2, 1, 0] == 0x8000
     assert np.isnan(r["out"][0, :2, 0].float().numpy()).all()
+
+
+def _mixed(layout, x_dtype, state_dtype, seed=61, **kw):
+    w = small(n_seq=4, T=5, width=4, dtype=x_dtype, state_dtype=state_dtype, layout=layout, n_pad=1, extra_slots=1,
+              seed=seed, **kw)
+    return w, wl.make_inputs(w)
+
+
+@pytest.mark.parametrize("layout", ["dense", "dedup", "history"])
+def test_m1_bf16_inputs_fp32_state_equal_the_bf16_run(layout):
+    """Mixed dtypes (sglang PR #46184, "Accuracy Tests": mixed input and state dtypes).  bf16 x with
+    an fp32 state holding bf16 values computes what the all-bf16 run computes: outputs bitwise, and
+    snapshots and state equal the bf16 ones widened to fp32 (an exact conversion)."""
+    w = small(n_seq=4, T=5, width=4, dtype="bf16", layout=layout, n_pad=1, extra_slots=1, seed=61,
+              state_offset=(layout == "history"))
+    inp = wl.make_inputs(w)
+    rb = run_oracle_verify(w, inp)
+    wm = w.replace(state_dtype="f32")
+    im = clone_inputs(inp)
+    im["conv_state"] = inp["conv_state"].float()
+    if inp["window"] is not None:
+        im["window"] = inp["window"].float()
+    rm = run_oracle_verify(wm, im)
+    assert_bits_equal(rm["out"], rb["out"], "out")
+    assert_bits_equal(rm["conv_state"], rb["conv_state"].float(), "state")
+    if layout != "history":
+        assert_bits_equal(rm["window"], rb["window"].float(), "window")
+
+
+@pytest.mark.parametrize("layout", ["dense", "dedup"])
+def test_m2_fp32_inputs_bf16_state_equal_the_fp32_run(layout):
+    """fp32 x holding bf16 values with a bf16 state computes what the all-fp32 run computes on the
+    widened state: outputs bitwise; snapshots and state are the fp32 ones narrowed (exactly)."""
+    w = small(n_seq=4, T=5, width=4, dtype="f32", layout=layout, n_pad=1, extra_slots=1, seed=63)
+    inp = wl.make_inputs(w)
+    inp["x_base"] = inp["x_base"].bfloat16().float()
+    inp["x"] = inp["x_base"].as_strided(inp["x"].shape, inp["x"].stride(), inp["x"].storage_offset())
+    inp["conv_state"] = inp["conv_state"].bfloat16().float()
+    rf = run_oracle_verify(w, inp)
+    wm = w.replace(state_dtype="bf16")
+    im = clone_inputs(inp)
+    im["conv_state"] = inp["conv_state"].bfloat16()
+    im["window"] = inp["window"].bfloat16()
+    rm = run_oracle_verify(wm, im)
+    assert_bits_equal(rm["out"], rf["out"], "out")
+    assert_bits_equal(rm["conv_state"], rf["conv_state"].bfloat16(), "state")
+    assert_bits_equal(rm["window"], rf["window"].bfloat16(), "window")
+
+
+def test_m3_fp32_inputs_round_into_bf16_snapshots():
+    """fp32 x (not bf16-representable) into a bf16 state: the snapshot elements that come from x
+    equal torch's round-to-nearest-even conversion of x, those from the old state its raw bits."""
+    w, inp = _mixed("dense", "f32", "bf16", seed=65)
+    r = run_oracle_verify(w, inp)
+    R = w.width - 1
+    for s in range(w.n_seq):
+        slot = int(inp["cache_idx"][s])
+        if slot < 0:
+            continue
+        full = torch.cat([inp["conv_state"][slot], inp["x"][s].t().to(torch.bfloat16)], dim=1)  # [dim, R+T]
+        for t in range(w.T):
+            assert_bits_equal(r["window"][s, t], full[:, t + 1:t + 1 + R].contiguous(), f"seq {s} snapshot {t}")
+        assert_bits_equal(r["conv_state"][slot], full[:, w.T:w.T + R].contiguous(), f"seq {s} state")
+
+
+@pytest.mark.parametrize("xd,sd", [("bf16", "f32"), ("f32", "bf16")])
+def test_m4_mixed_matches_float64_conv1d(xd, sd):
+    """Library special case with mixed dtypes: outputs equal torch float64 conv1d over [state
+    window, x] (each widened from its own dtype) with SiLU and L2, within 1e-5 relative."""
+    w, inp = _mixed("dense", xd, sd, seed=67)
+    r = run_oracle_verify(w, inp)
+    for s in range(w.n_seq):
+        slot = int(inp["cache_idx"][s])
+        if slot < 0:
+            continue
+        full = torch.cat([inp["conv_state"][slot].double(), inp["x"][s].double().t()], dim=1)
+        acc = F.conv1d(full[None], inp["weight"].double()[:, None, :], inp["bias"].double(), groups=w.dim)[0]
+        y = (acc / (1 + torch.exp(-acc))).t()
+        g = y[:, : w.qk_channels].reshape(w.T, -1, w.head_dim)
+        y[:, : w.qk_channels] = (g / torch.sqrt((g * g).sum(-1, keepdim=True) + w.l2_eps)).reshape(w.T, -1)
+        got = r["out"][s].double()
+        tol = 1e-5 if xd == "f32" else 2 ** -7
+        assert torch.allclose(got, y, rtol=tol, atol=1e-6), float((got - y).abs().max())
