@@ -48,13 +48,18 @@ extern "C" {
 #define CV_API
 #endif
 
-#define CV_ABI_VERSION 2
+#define CV_ABI_VERSION 3
 #define CV_MAX_T 128 /* draft tokens per verify call */
 
 typedef enum cv_dtype {
     CV_F32 = 0,  /* IEEE binary32 */
     CV_BF16 = 1  /* bfloat16; arithmetic in fp32, outputs rounded to nearest even */
 } cv_dtype;
+
+/* cv_verify_args.state_dtype: the dtype of conv_state and the snapshots. */
+#define CV_STATE_SAME 0 /* the dtype of x (a zero-initialised struct asks for no mixing) */
+#define CV_STATE_F32 1  /* fp32 state with bf16 x */
+#define CV_STATE_BF16 2 /* bf16 state with fp32 x */
 
 typedef enum cv_window_layout {
     /* window element (s, t, c, k) at s*win_seq_stride + t*win_step_stride + c*win_ch_stride
@@ -140,7 +145,8 @@ enum {
  *   width              conv width W in 2..4 (the window is held in registers)
  *   qk_channels        leading channels that are L2-normalised (0 = none); multiple of head_dim
  *   head_dim           L2 group size when qk_channels > 0: power of two, 8..256
- *   dtype              cv_dtype of x, out, conv_state, window, weight and bias
+ *   dtype              cv_dtype of x, out, weight and bias (and of conv_state and window unless
+ *                      state_dtype says otherwise)
  *   l2_eps             added to the group's sum of squares inside the square root
  *   x                  [n_seq][T][dim] read-only; element (s,t,c) at s*x_seq_stride + t*x_tok_stride + c
  *                      (x may be a strided slice of a wider projection output)
@@ -156,6 +162,11 @@ enum {
  *                      and ignored for CV_WINDOW_HISTORY and CV_WINDOW_RECOMPUTE)
  *   err                int32 [n_seq] device array or NULL: receives the CV_SEQ_* bits of each
  *                      sequence (0 for fine and for padded sequences)
+ *   state_dtype        CV_STATE_SAME, or the other dtype for conv_state and window (mixed dtypes,
+ *                      [sglang-46184] "Accuracy Tests"): inputs are widened exactly for the
+ *                      arithmetic; snapshots and state receive x converted to the state dtype
+ *                      (exact widening bf16 -> fp32, or round to nearest even fp32 -> bf16 with any
+ *                      NaN becoming the quiet NaN 0x7fc0).  Mixed calls run the general kernel.
  * Preconditions the library cannot check: distinct sequences use distinct slots; out and window do
  * not overlap themselves, each other, x, conv_state or weight.
  * Returns CV_OK after the launch is queued, or a negative CV_ERR_* code with nothing launched.
@@ -180,6 +191,7 @@ typedef struct cv_verify_args {
     int32_t reserved0;
     int64_t win_seq_stride, win_step_stride, win_ch_stride, win_col_stride;
     int32_t *err;
+    int32_t state_dtype; /* CV_STATE_* */
 } cv_verify_args;
 
 CV_API int cv_conv_verify(const cv_verify_args *args, void *stream);
@@ -201,7 +213,8 @@ CV_API int cv_conv_verify(const cv_verify_args *args, void *stream);
  * pre-verify window in columns [0, W-1) (the verify leaves it alone in this layout).  With
  * full = [conv_state[slot][c][0 .. W-2], x[s][0][c] .. x[s][T-1][c]], the commit sets
  * conv_state[slot][c][k] = full[a+k] for k < W-1; each state row is read before it is written.
- * CV_WINDOW_HISTORY has nothing to commit and returns CV_ERR_LAYOUT.
+ * CV_WINDOW_HISTORY has nothing to commit and returns CV_ERR_LAYOUT.  dtype here is the dtype of
+ * conv_state and window (with mixed dtypes, the state's); the recompute layout needs x in it too.
  */
 typedef struct cv_commit_args {
     int32_t n_seq, T, dim, width;

@@ -41,7 +41,7 @@ class VerifyArgs(ctypes.Structure):
         ("cache_idx", c_vp), ("state_off", c_vp), ("weight", c_vp), ("bias", c_vp),
         ("window", c_vp), ("window_layout", c_i32), ("reserved0", c_i32),
         ("win_seq_stride", c_i64), ("win_step_stride", c_i64), ("win_ch_stride", c_i64), ("win_col_stride", c_i64),
-        ("err", c_vp),
+        ("err", c_vp), ("state_dtype", c_i32),
     ]
 
 
@@ -166,7 +166,8 @@ def make_verify_args(x, conv_state, weight, bias, out, window, *, layout, qk_cha
 
     x [n_seq, T, dim] (channel stride 1, any seq/token strides), conv_state [n_slots, dim, S]
     (column stride 1), weight [dim, W] contiguous, bias [dim] or None, out [n_seq, T, dim] (channel
-    stride 1), window dense [n_seq, T, dim, W-1] or dedup [n_seq, dim, T+W-2] (any strides), or
+    stride 1; it may have the other dtype than x: mixed dtypes), window dense [n_seq, T, dim, W-1] or
+    dedup [n_seq, dim, T+W-2] (any strides, the dtype of conv_state), or
     None with layout "history" (conv_state [n_slots, dim, S >= T+W-2] then receives the snapshot
     row and the next call reads at state_off = accept_len - 1) or "recompute" (outputs only; the
     commit rebuilds the state from x), cache_idx / state_off / err int32 [n_seq] or None."""
@@ -189,7 +190,8 @@ def make_verify_args(x, conv_state, weight, bias, out, window, *, layout, qk_cha
         weight=ptr(weight, "weight"), bias=ptr(bias, "bias", False),
         window=ptr(window, "window", lay not in (HISTORY, RECOMPUTE)),
         window_layout=lay, reserved0=0, win_seq_stride=ws[0], win_step_stride=ws[1], win_ch_stride=ws[2],
-        win_col_stride=ws[3], err=ptr(err, "err", False))
+        win_col_stride=ws[3], err=ptr(err, "err", False),
+        state_dtype=0 if conv_state.dtype == x.dtype else _dtype_code(conv_state) + 1)
 
 
 def conv_verify(x, conv_state, weight, bias, out, window, *, layout, qk_channels, head_dim, l2_eps=1e-6,
@@ -198,9 +200,12 @@ def conv_verify(x, conv_state, weight, bias, out, window, *, layout, qk_channels
 
     Writes out, window, conv_state (and err); raises CvError on an invalid argument.  With layout
     "history" pass window=None: the snapshots go into the state rows."""
-    for t in (x, conv_state, weight, out, window):
-        if t is not None and t.dtype != x.dtype:
-            raise TypeError("x, conv_state, weight, out and window must share one dtype")
+    for t in (weight, out):
+        if t.dtype != x.dtype:
+            raise TypeError("x, weight and out must share one dtype")
+    if window is not None and window.dtype != conv_state.dtype:
+        raise TypeError("window must have the dtype of conv_state")
+    _dtype_code(conv_state)
     if bias is not None and bias.dtype != x.dtype:
         raise TypeError("bias must have the dtype of x")
     a = make_verify_args(x, conv_state, weight, bias, out, window, layout=layout, qk_channels=qk_channels,

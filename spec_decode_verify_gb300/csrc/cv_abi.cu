@@ -58,6 +58,8 @@ const cvk::KernelSet &kernel_set(int dtype, int width) {
 int check_verify(const cv_verify_args *a) {
     if (!a) return CV_ERR_NULL_ARGS;
     if (a->dtype != CV_F32 && a->dtype != CV_BF16) return CV_ERR_DTYPE;
+    if (a->state_dtype != CV_STATE_SAME && a->state_dtype != CV_STATE_F32 && a->state_dtype != CV_STATE_BF16)
+        return CV_ERR_DTYPE;
     if (a->width < 2 || a->width > 4) return CV_ERR_WIDTH;
     if (a->T < 1 || a->T > CV_MAX_T) return CV_ERR_TOKENS;
     if (a->n_seq < 0 || a->n_seq > 65535 || a->dim < 1 || a->n_slots < 1 || a->state_cols < a->width - 1)
@@ -139,10 +141,15 @@ bool state_packed(const void *state, long long slot_stride, long long ch_stride,
 }
 
 // Validates verify arguments; on success fills the launch plan.
+// dtype of conv_state and the snapshots
+int state_dtype_of(const cv_verify_args *a) { return a->state_dtype == CV_STATE_SAME ? a->dtype : a->state_dtype - 1; }
+bool mixed_dtypes(const cv_verify_args *a) { return state_dtype_of(a) != a->dtype; }
+
 int plan_verify(const cv_verify_args *a, cv_launch_plan *pl) {
     const int rc = check_verify(a);
     if (rc != CV_OK) return rc;
     const int esize = a->dtype == CV_BF16 ? 2 : 4;
+    const bool mixed = mixed_dtypes(a);
     const int R = a->width - 1;
     const int min_threads =
         (a->qk_channels > 0 && a->head_dim / 8 > kMinThreads) ? a->head_dim / 8 : kMinThreads;
@@ -158,7 +165,7 @@ int plan_verify(const cv_verify_args *a, cv_launch_plan *pl) {
     // needs rows of exactly T+W-2 columns
     const bool rows_packed = aligned16(a->conv_state) && stride16(a->state_slot_stride, esize) &&
                              a->state_ch_stride == a->state_cols;
-    bool pipe_ok = io_packed(a, esize) && a->T <= ks.max_static_t && rows_packed &&
+    bool pipe_ok = !mixed && io_packed(a, esize) && a->T <= ks.max_static_t && rows_packed &&
                          (hist ? a->state_cols == a->T + R - 1 : (recomp || fast));
     const bool wide = !hist && a->state_cols != R;
     // (wide rows cost whole-row reads and element stores of the window; the pipeline pays that
@@ -199,7 +206,7 @@ int plan_verify(const cv_verify_args *a, cv_launch_plan *pl) {
             return CV_OK;
         }
     }
-    if (fast) {
+    if (fast && !mixed) {
         // 4 channels per thread (twice the threads of 8) unless an L2 group would span more than a warp
         int threads = kFastThreads;
         while (threads > 32 && cpt * (threads / 2) >= a->dim) threads /= 2;
@@ -213,14 +220,16 @@ int plan_verify(const cv_verify_args *a, cv_launch_plan *pl) {
         pl->smem_bytes = (int)smem;
         pl->path = a->T <= ks.max_static_t ? 1 : 2;
     } else {
+        // (with mixed dtypes the tile holds fp32 bits)
+        const int tsize = mixed ? 4 : esize;
         const int rows = a->T + a->width - 1;
-        const int pad = 16 / esize;  // one 16-byte vector of padding per tile row
+        const int pad = 16 / tsize;  // one 16-byte vector of padding per tile row
         int threads = 128;
         while (threads > min_threads && 8 * (threads / 2) >= a->dim) threads /= 2;
-        long long smem = (long long)rows * (8 * threads + pad) * esize;
+        long long smem = (long long)rows * (8 * threads + pad) * tsize;
         while (smem > kGenericSmemBudget && threads > min_threads) {
             threads /= 2;
-            smem = (long long)rows * (8 * threads + pad) * esize;
+            smem = (long long)rows * (8 * threads + pad) * tsize;
         }
         if (smem > kSmemMax) return CV_ERR_SMEM;
         pl->threads = threads;
@@ -308,17 +317,19 @@ int launch_verify(const cv_verify_args *a, const cv_launch_plan &pl, cudaStream_
     p.state_cols = a->state_cols;
     p.qk_channels = a->qk_channels;
     p.head_dim = a->qk_channels > 0 ? a->head_dim : 8;
-    p.pitch = pl.channels_per_block + 16 / esize;
+    const bool mixed = mixed_dtypes(a);
+    const int ssize = state_dtype_of(a) == CV_BF16 ? 2 : 4;
+    p.pitch = pl.channels_per_block + 16 / (mixed ? 4 : esize);
     p.eps = a->l2_eps;
     p.x_vec = aligned16(a->x) && stride16(a->x_seq_stride, esize) && stride16(a->x_tok_stride, esize);
     p.out_vec = aligned16(a->out) && stride16(a->out_seq_stride, esize) && stride16(a->out_tok_stride, esize);
-    p.st_vec = state_packed(a->conv_state, a->state_slot_stride, a->state_ch_stride, a->width, esize);
+    p.st_vec = state_packed(a->conv_state, a->state_slot_stride, a->state_ch_stride, a->width, ssize);
     p.w_vec = aligned16(a->weight);
     p.b_vec = a->bias ? aligned16(a->bias) : 0;
 
     const cvk::KernelSet &ks = kernel_set(a->dtype, a->width);
     const int ci = pl.channels_per_block / pl.threads == 8 ? 1 : 0;
-    cvk::VerifyKernel k = pl.path == 0   ? ks.generic
+    cvk::VerifyKernel k = pl.path == 0   ? (mixed ? ks.generic_mixed : ks.generic)
                           : pl.path == 1 ? ks.fast[ci][a->T]
                           : pl.path == 2 ? ks.fast[ci][0]
                                          : ks.pipe[ci][a->T];

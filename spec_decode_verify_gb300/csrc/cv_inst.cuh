@@ -22,6 +22,8 @@ KernelSet make_set(std::integer_sequence<int, Ts...>) {
     ((k.pipe[1][Ts + 1] = verify_pipe<B, W, Ts + 1, 8>), ...);
     k.max_static_t = (int)sizeof...(Ts);
     k.generic = verify_generic<B, W>;
+    // mixed dtypes: the state and the snapshots in the other dtype
+    k.generic_mixed = verify_generic<B, W, std::conditional_t<sizeof(B) == 2, uint32_t, uint16_t>>;
     k.commit = commit_kernel<B, W>;
     k.commit_rows = commit_rows<B, W>;
     k.commit_recompute = commit_recompute<B, W>;

@@ -12,6 +12,8 @@
 // over the head_dim group as an xor-shuffle over head_dim/8 lanes.
 #pragma once
 
+#include <type_traits>
+
 #include "cv_device.cuh"
 
 namespace cvk {
@@ -53,10 +55,47 @@ template <typename B> __device__ __forceinline__ void store_oct(B *p, const Oct<
 // goes to dst[c*ch_stride + q*col_stride].  Three shapes: channel-major contiguous (the dedup row
 // and the dense per-token chunks: one coalesced run of nch*ncol elements), channel-stride-1 (a
 // transposed row: one contiguous run of channels per column), and anything else element by element.
-template <typename B>
-__device__ __forceinline__ void write_view(const B *__restrict__ tile, int pitch, int jofs, int ncol, B *dst,
+// Tile element -> destination element: the same bits when the types agree; otherwise (a tile of
+// fp32 bits written to bf16) round to nearest even, any NaN to the quiet NaN 0x7fc0.
+template <typename BD, typename TT>
+__device__ __forceinline__ BD from_tile(TT v) {
+    if constexpr (sizeof(BD) == sizeof(TT)) {
+        return (BD)v;
+    } else {
+        const uint32_t u = (uint32_t)v;
+        if ((u & 0x7fffffffu) > 0x7f800000u) return (BD)0x7fc0u;
+        return (BD)__bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(u)));
+    }
+}
+// Source element -> tile element: the same bits, or bf16 widened exactly to fp32 bits.
+template <typename TT, typename BS>
+__device__ __forceinline__ TT to_tile(BS v) {
+    if constexpr (sizeof(TT) == sizeof(BS))
+        return (TT)v;
+    else
+        return (TT)((uint32_t)v << 16);
+}
+
+template <typename B, typename BD = B>
+__device__ __forceinline__ void write_view(const B *__restrict__ tile, int pitch, int jofs, int ncol, BD *dst,
                                            long long ch_stride, long long col_stride, int nch) {
     constexpr int CH = 16 / (int)sizeof(B);
+    if constexpr (!std::is_same_v<B, BD>) {
+        // converting writes: element by element in destination order
+        const int n = nch * ncol;
+        if (col_stride == 1) {
+            for (int i = threadIdx.x; i < n; i += blockDim.x) {
+                const int c = i / ncol, q = i - c * ncol;
+                dst[c * ch_stride + q] = from_tile<BD>(tile[(jofs + q) * pitch + c]);
+            }
+        } else {
+            for (int i = threadIdx.x; i < n; i += blockDim.x) {
+                const int q = i / nch, c = i - q * nch;
+                dst[c * ch_stride + q * col_stride] = from_tile<BD>(tile[(jofs + q) * pitch + c]);
+            }
+        }
+        return;
+    } else {
     const int tid = threadIdx.x, NT = blockDim.x;
     const int n = nch * ncol;
     const bool aligned = ((reinterpret_cast<uintptr_t>(dst) & 15u) == 0);
@@ -100,16 +139,22 @@ __device__ __forceinline__ void write_view(const B *__restrict__ tile, int pitch
             dst[c * ch_stride + q * col_stride] = tile[(jofs + q) * pitch + c];
         }
     }
+    }
 }
 
 // ---------------------------------------------------------------- verify
-template <typename B, int W>
+// BX: x, out, taps and bias; BS: state and snapshots.  When they differ (mixed dtypes) the tile
+// holds fp32 bits: inputs are widened into it and snapshots are converted out of it.
+template <typename BX, int W, typename BS = BX>
 __global__ void __launch_bounds__(256) verify_generic(const __grid_constant__ VerifyParams p) {
+    using B = BX;
+    constexpr bool MIXED = !std::is_same_v<BX, BS>;
+    using TT = std::conditional_t<MIXED, uint32_t, BX>;  // tile element
     grid_dep_wait();
     grid_dep_launch();
     constexpr int R = W - 1;  // committed window columns
     extern __shared__ __align__(16) unsigned char smem_raw[];
-    B *tile = reinterpret_cast<B *>(smem_raw);
+    TT *tile = reinterpret_cast<TT *>(smem_raw);
 
     const int s = blockIdx.y;
     const int tid = threadIdx.x;
@@ -122,7 +167,7 @@ __global__ void __launch_bounds__(256) verify_generic(const __grid_constant__ Ve
     const int status = seq_status(slot, off, p.n_slots, p.state_cols, R);
     if (p.err && blockIdx.x == 0 && tid == 0) p.err[s] = status;
     if (slot < 0 || status) return;  // padded or rejected: touch nothing (uniform per block)
-    if ((long long)(T + R) * pitch * (long long)sizeof(B) > (long long)dynamic_smem_bytes()) return;  // launch mismatch
+    if ((long long)(T + R) * pitch * (long long)sizeof(TT) > (long long)dynamic_smem_bytes()) return;  // launch mismatch
 
     const int nch = min(BC, p.dim - c0);
     const int cl = tid * 8;  // first block-local channel of this thread
@@ -131,7 +176,12 @@ __global__ void __launch_bounds__(256) verify_generic(const __grid_constant__ Ve
 
     // (1) x_0..x_{T-1} -> tile rows R..R+T-1 (asynchronous 16-byte copies, no registers)
     const B *xs = reinterpret_cast<const B *>(p.x) + (long long)s * p.x_seq + c0;
-    if (p.x_vec) {
+    if (MIXED) {
+        for (int i = tid; i < T * nch; i += blockDim.x) {
+            const int t = i / nch, c = i - t * nch;
+            tile[(R + t) * pitch + c] = to_tile<TT>(xs[t * p.x_tok + c]);
+        }
+    } else if (p.x_vec) {
         if (full8) {
             for (int t = 0; t < T; ++t) {
 #pragma unroll
@@ -140,23 +190,23 @@ __global__ void __launch_bounds__(256) verify_generic(const __grid_constant__ Ve
             }
         } else {
             for (int t = 0; t < T; ++t)
-                for (int e = 0; e < my; ++e) tile[(R + t) * pitch + cl + e] = xs[t * p.x_tok + cl + e];
+                for (int e = 0; e < my; ++e) tile[(R + t) * pitch + cl + e] = to_tile<TT>(xs[t * p.x_tok + cl + e]);
         }
     } else {
         for (int i = tid; i < T * nch; i += blockDim.x) {
             const int t = i / nch, c = i - t * nch;
-            tile[(R + t) * pitch + c] = xs[t * p.x_tok + c];
+            tile[(R + t) * pitch + c] = to_tile<TT>(xs[t * p.x_tok + c]);
         }
     }
 
     // (2) committed window of this thread's channels -> registers and tile rows 0..R-1
     float win[R][8];
     {
-        B raw[R][8];
-        B *sp = reinterpret_cast<B *>(p.state) + (long long)slot * p.st_slot + (long long)(c0 + cl) * p.st_ch + off;
+        BS raw[R][8];
+        BS *sp = reinterpret_cast<BS *>(p.state) + (long long)slot * p.st_slot + (long long)(c0 + cl) * p.st_ch + off;
         if (full8 && p.st_vec && off == 0) {
             // 8 channels x R columns are contiguous: R 16-byte vectors (2R for fp32)
-            Oct<B> o[R];
+            Oct<BS> o[R];
 #pragma unroll
             for (int k = 0; k < R; ++k) load_oct(o[k], sp + k * 8);
 #pragma unroll
@@ -170,20 +220,20 @@ __global__ void __launch_bounds__(256) verify_generic(const __grid_constant__ Ve
 #pragma unroll
             for (int e = 0; e < 8; ++e)
 #pragma unroll
-                for (int k = 0; k < R; ++k) raw[k][e] = (e < my) ? sp[e * p.st_ch + k] : (B)0;
+                for (int k = 0; k < R; ++k) raw[k][e] = (e < my) ? sp[e * p.st_ch + k] : (BS)0;
         }
 #pragma unroll
         for (int k = 0; k < R; ++k) {
-            if (full8) {
-                Oct<B> o;
+            if (full8 && !MIXED) {
+                Oct<TT> o;
 #pragma unroll
-                for (int e = 0; e < 8; ++e) o.set(e, raw[k][e]);
+                for (int e = 0; e < 8; ++e) o.set(e, (TT)raw[k][e]);
                 store_oct(tile + k * pitch + cl, o);
             } else {
-                for (int e = 0; e < my; ++e) tile[k * pitch + cl + e] = raw[k][e];
+                for (int e = 0; e < my; ++e) tile[k * pitch + cl + e] = to_tile<TT>(raw[k][e]);
             }
 #pragma unroll
-            for (int e = 0; e < 8; ++e) win[k][e] = widen<B>(raw[k][e]);
+            for (int e = 0; e < 8; ++e) win[k][e] = widen<BS>(raw[k][e]);
         }
     }
 
@@ -230,18 +280,19 @@ __global__ void __launch_bounds__(256) verify_generic(const __grid_constant__ Ve
     } else if (p.hist) {
         // history-row state: the snapshot row [full[1 .. W-2], x_0 .. x_{T-1}] replaces columns
         // [0, T+W-2) of the state row (every thread read its committed window before the barrier)
-        B *sb = reinterpret_cast<B *>(p.state) + (long long)slot * p.st_slot + (long long)c0 * p.st_ch;
-        write_view<B>(tile, pitch, 1, T + R - 1, sb, p.st_ch, 1, nch);
+        BS *sb = reinterpret_cast<BS *>(p.state) + (long long)slot * p.st_slot + (long long)c0 * p.st_ch;
+        write_view<TT, BS>(tile, pitch, 1, T + R - 1, sb, p.st_ch, 1, nch);
     } else {
-        B *wb = reinterpret_cast<B *>(p.win) + (long long)s * p.w_seq;
+        BS *wb = reinterpret_cast<BS *>(p.win) + (long long)s * p.w_seq;
         if (p.dedup) {
-            write_view<B>(tile, pitch, 1, T + R - 1, wb + (long long)c0 * p.w_ch, p.w_ch, p.w_col, nch);
+            write_view<TT, BS>(tile, pitch, 1, T + R - 1, wb + (long long)c0 * p.w_ch, p.w_ch, p.w_col, nch);
         } else {
             for (int t = 0; t < T; ++t)
-                write_view<B>(tile, pitch, t + 1, R, wb + t * p.w_step + (long long)c0 * p.w_ch, p.w_ch, p.w_col, nch);
+                write_view<TT, BS>(tile, pitch, t + 1, R, wb + t * p.w_step + (long long)c0 * p.w_ch, p.w_ch, p.w_col,
+                                   nch);
         }
-        B *sb = reinterpret_cast<B *>(p.state) + (long long)slot * p.st_slot + (long long)c0 * p.st_ch;
-        write_view<B>(tile, pitch, T, R, sb, p.st_ch, 1, nch);
+        BS *sb = reinterpret_cast<BS *>(p.state) + (long long)slot * p.st_slot + (long long)c0 * p.st_ch;
+        write_view<TT, BS>(tile, pitch, T, R, sb, p.st_ch, 1, nch);
     }
 
     // (5) conv + SiLU (+ L2 over the head_dim group) for every token, outputs stored as vectors
@@ -253,13 +304,13 @@ __global__ void __launch_bounds__(256) verify_generic(const __grid_constant__ Ve
     for (int t = 0; t < T; ++t) {
         float xv[8];
         if (full8) {
-            Oct<B> o;
+            Oct<TT> o;
             load_oct(o, tile + (R + t) * pitch + cl);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) xv[e] = widen<B>(o.get(e));
+            for (int e = 0; e < 8; ++e) xv[e] = widen<TT>(o.get(e));
         } else {
 #pragma unroll
-            for (int e = 0; e < 8; ++e) xv[e] = (e < my) ? widen<B>(tile[(R + t) * pitch + cl + e]) : 0.0f;
+            for (int e = 0; e < 8; ++e) xv[e] = (e < my) ? widen<TT>(tile[(R + t) * pitch + cl + e]) : 0.0f;
         }
         float y[8];
 #pragma unroll
@@ -269,7 +320,8 @@ __global__ void __launch_bounds__(256) verify_generic(const __grid_constant__ Ve
 #pragma unroll
             for (int j = 0; j < R; ++j) in[j] = win[j][e];
             in[R] = xv[e];
-            const float acc = conv_chain<B, W>(has_bias ? bs[e] : 0.0f, wt[e], in);
+            // (mixed dtypes: fp32 state values make the products inexact, so each one is rounded)
+            const float acc = conv_chain<std::conditional_t<MIXED, uint32_t, B>, W>(has_bias ? bs[e] : 0.0f, wt[e], in);
             y[e] = silu(acc);
         }
 #pragma unroll

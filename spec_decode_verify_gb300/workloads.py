@@ -14,6 +14,8 @@ The five named workloads follow the shapes the pages describe:
   * a width-3 conv without L2 groups and with a per-sequence accepted-token state offset (PR
     #46184's tests cover an offset of the accepted-token count into the state; its "Scope" names
     width-3 deduplicated windows);
+  * the benchmark shape with an fp32 state and fp32 snapshots under bf16 inputs (PR #46184's
+    extra check covers mixed input and state dtypes);
   * the benchmark shape again with the recompute rollback (memra-engine ssm_conv_ring_rebuild_dc:
     no snapshots; the commit rebuilds the state from the kept window and the accepted inputs) and
     with the history-row state: the state row of each slot is the deduplicated [dim, T+W-2] row
@@ -110,6 +112,9 @@ WORKLOADS = {
         VerifyWorkload("n128_t8_dim10240_w4_bf16_recompute_pad13", n_seq=128, T=8, dim=10240, width=4,
                        qk_channels=4096, head_dim=128, dtype="bf16", layout="recompute", n_pad=13,
                        extra_slots=16, seed=6),
+        VerifyWorkload("n128_t8_dim10240_w4_bf16x_f32state_dedup_pad13", n_seq=128, T=8, dim=10240, width=4,
+                       qk_channels=4096, head_dim=128, dtype="bf16", state_dtype="f32", layout="dedup", n_pad=13,
+                       extra_slots=16, seed=7),
         VerifyWorkload("n128_t8_dim10240_w4_bf16_history_pad13", n_seq=128, T=8, dim=10240, width=4,
                        qk_channels=4096, head_dim=128, dtype="bf16", layout="history", n_pad=13,
                        extra_slots=16, state_offset=True, seed=5),

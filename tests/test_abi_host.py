@@ -33,7 +33,7 @@ def test_exports_every_declared_function(lib):
     assert {"cv_conv_verify", "cv_conv_commit", "cv_verify_plan", "cv_status_string", "cv_abi_version"} <= set(names)
     for n in names:
         assert hasattr(lib, n), f"{n} declared in the header but not exported"
-    assert lib.cv_abi_version() == 2
+    assert lib.cv_abi_version() == 3
 
 
 def test_exports_nothing_undeclared(lib):
@@ -313,3 +313,19 @@ def test_prefill_aliasing_and_empty(lib):
     assert lib.cv_conv_prefill(ctypes.byref(a), None) == -10
     a = _prefill_args(n_seq=0)
     assert lib.cv_conv_prefill(ctypes.byref(a), None) == 0
+
+
+def test_mixed_dtypes_plan_and_validation(lib):
+    """bf16 x with an fp32 state (and the reverse) plan the general kernel with an fp32 tile;
+    unknown state dtypes are rejected."""
+    w = W3.replace(state_dtype="f32", n_seq=4, n_pad=0, extra_slots=0)
+    a = _args(w)
+    assert a.state_dtype == 1  # CV_STATE_F32
+    rc, pl = _plan(lib, a)
+    assert rc == 0 and pl.path == 0
+    assert pl.smem_bytes == (8 + 3) * (8 * pl.threads + 4) * 4
+    a.state_dtype = 3
+    assert _plan(lib, a)[0] == -6
+    w2 = W3.replace(dtype="f32", state_dtype="bf16", n_seq=4, n_pad=0, extra_slots=0)
+    a2 = _args(w2)
+    assert a2.state_dtype == 2 and _plan(lib, a2)[1].path == 0
