@@ -35,6 +35,7 @@ class _VerifyArgs(ctypes.Structure):
         ("cache_idx", c_vp), ("state_off", c_vp), ("weight", c_vp), ("bias", c_vp),
         ("window", c_vp), ("dedup", c_i32), ("w_seq", c_i64), ("w_step", c_i64), ("w_ch", c_i64),
         ("w_col", c_i64), ("status", c_vp), ("history", c_i32), ("recompute", c_i32), ("state_is_bf16", c_i32),
+        ("parent", c_vp),
     ]
 
 
@@ -134,14 +135,17 @@ def window_strides(window: torch.Tensor, layout: str):
 
 
 def conv_verify(x, conv_state, weight, bias, out, window, *, layout, qk_channels, head_dim, l2_eps,
-                cache_idx=None, state_off=None, status=None):
+                cache_idx=None, state_off=None, status=None, parent=None):
     """Run the oracle verify in place on CPU tensors (conv_state, out, window, status are written).
 
     x [n_seq, T, dim] (channel stride 1), conv_state [n_slots, dim, S] (column stride 1),
     weight [dim, W] contiguous, bias [dim] or None, out [n_seq, T, dim] (channel stride 1),
     window dense [n_seq, T, dim, W-1] / dedup [n_seq, dim, T+W-2] / None for the history layout
     (the state row, S >= T+W-2 columns, receives the snapshot row) and the recompute layout
-    (outputs only, state untouched); cache_idx, state_off, status int32 [n_seq] or None."""
+    (outputs only, state untouched); cache_idx, state_off, status int32 [n_seq] or None; parent
+    int32 [n_seq, T] contiguous (tree verify, dense layout only) or None (a chain)."""
+    if parent is not None:
+        assert layout == "dense" and parent.is_contiguous() and parent.dtype == torch.int32
     if layout not in ("dense", "dedup", "history", "recompute"):
         raise ValueError(f"unknown layout {layout!r}")
     if (layout in ("history", "recompute")) != (window is None):
@@ -159,7 +163,7 @@ def conv_verify(x, conv_state, weight, bias, out, window, *, layout, qk_channels
         cache_idx=_ptr(cache_idx), state_off=_ptr(state_off), weight=_ptr(weight), bias=_ptr(bias),
         window=_ptr(window), dedup=1 if layout == "dedup" else 0, w_seq=ws[0], w_step=ws[1], w_ch=ws[2],
         w_col=ws[3], status=_ptr(status), history=1 if layout == "history" else 0,
-        recompute=1 if layout == "recompute" else 0, state_is_bf16=_is_bf16(conv_state))
+        recompute=1 if layout == "recompute" else 0, state_is_bf16=_is_bf16(conv_state), parent=_ptr(parent))
     if window is not None and window.dtype != conv_state.dtype:
         raise TypeError("the window has the state's dtype")
     rc = _load().oracle_conv_verify(ctypes.byref(a))

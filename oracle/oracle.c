@@ -71,6 +71,13 @@
  *     the inputs converted to the state dtype: raw bits when the dtypes agree, an exact widening
  *     for bf16 inputs into fp32 state, and round-to-nearest-even (any NaN to the quiet NaN) for
  *     fp32 inputs into bf16 state.
+ *   - Tree verify (sglang PR #46184, "Scope": tree verify keeps dense windows and per-token stores).
+ *     Draft token t has a parent p(t) in [-1, t) (-1: the committed window).  Its conv sees the
+ *     parent's window followed by x_t, and its snapshot is that window shifted by one with x_t
+ *     appended: window(t) = [window(p)[1 .. W-2], x_t], window(-1) = the committed window.  A
+ *     chain (p(t) = t-1) is the plain verify.  The state is left on window(T-1), as for a chain;
+ *     the commit restores the window of the accepted path's last token (accept_len = its index + 1).
+ *     Only the dense layout holds tree snapshots.  A parent outside [-1, t) flags the sequence (32).
  *   - Prefill (glm5next_kda mod.rs, the prefill path of the layer: the conv over all T prompt
  *     tokens with SiLU, then the L2 normalisation of q|k, which that code runs as a second launch;
  *     here the normalisation is applied to the fp32 SiLU values and rounded once, as in decode).
@@ -80,7 +87,8 @@
  *     the state is left holding the last W-1 entries of full.
  *
  * Status codes written per sequence (same meaning as the library's): 1 = cache slot out of range,
- * 2 = state offset out of range, 4 = accept count out of range, 16 = token span invalid (prefill).
+ * 2 = state offset out of range, 4 = accept count out of range, 16 = token span invalid (prefill),
+ * 32 = a draft token's parent outside [-1, t) (tree verify).
  * A flagged sequence is untouched.
  */
 #include <math.h>
@@ -110,6 +118,7 @@ typedef struct {
     int32_t history;   /* 1: the state row is the snapshot row (no window buffer) */
     int32_t recompute; /* 1: outputs only; no snapshots and the state is not written */
     int32_t state_is_bf16; /* dtype of state and window: 0 fp32, 1 bf16 (may differ from is_bf16) */
+    const int32_t *parent; /* [n_seq][T] parent of each draft token (-1: the committed window) or NULL */
 } oracle_verify_args;
 
 typedef struct {
@@ -191,9 +200,57 @@ int oracle_conv_verify(const oracle_verify_args *a) {
         int st = 0;
         if (slot >= 0 && slot >= a->n_slots) st |= 1;
         if (slot >= 0 && (o < 0 || o + W - 1 > a->state_cols)) st |= 2;
+        if (slot >= 0 && a->parent)
+            for (int t = 0; t < T; ++t) {
+                const int par = a->parent[(int64_t)s * T + t];
+                if (par < -1 || par >= t) st |= 32;
+            }
         if (a->status) a->status[s] = st;
         if (slot < 0 || st) continue;
 
+        if (a->parent) {
+            /* wbits[(t+1)*(W-1) + k]: window after token t (entry 0: the committed window), as bits of
+               the state's dtype; wf: the same values widened */
+            const int R = W - 1;
+            uint32_t *wbits = (uint32_t *)malloc(sizeof(uint32_t) * (size_t)(T + 1) * (size_t)R + 4);
+            float *wf = (float *)malloc(sizeof(float) * (size_t)(T + 1) * (size_t)R + 4);
+            if (!wbits || !wf) {
+                free(wbits);
+                free(wf);
+                free(y);
+                return -2;
+            }
+            for (int c = 0; c < dim; ++c) {
+                const int64_t srow = (int64_t)slot * a->st_slot + (int64_t)c * a->st_ch;
+                for (int k = 0; k < R; ++k) {
+                    wbits[k] = get_bits(a->state, sbf, srow + o + k);
+                    wf[k] = bits_to_float(wbits[k], sbf);
+                }
+                for (int t = 0; t < T; ++t) {
+                    const int base = (a->parent[(int64_t)s * T + t] + 1) * R;
+                    const uint32_t xv = get_bits(a->x, bf, (int64_t)s * a->x_seq + (int64_t)t * a->x_tok + c);
+                    const float xf = bits_to_float(xv, bf);
+                    float acc = a->bias ? bits_to_float(get_bits(a->bias, bf, c), bf) : 0.0f;
+                    for (int j = 0; j < W; ++j) {
+                        const float wj = bits_to_float(get_bits(a->weight, bf, (int64_t)c * W + j), bf);
+                        const float prod = wj * (j < R ? wf[base + j] : xf);
+                        acc = acc + prod;
+                    }
+                    y[(int64_t)t * dim + c] = acc / (1.0f + expf(-acc));
+                    const int nb = (t + 1) * R;
+                    for (int k = 0; k + 1 < R; ++k) {
+                        wbits[nb + k] = wbits[base + k + 1];
+                        wf[nb + k] = wf[base + k + 1];
+                    }
+                    wbits[nb + R - 1] = to_state_bits(xv, bf, sbf);
+                    wf[nb + R - 1] = xf;
+                    for (int k = 0; k < R; ++k) put_bits(a->window, sbf, win_index(a, s, t, c, k), wbits[nb + k]);
+                }
+                for (int k = 0; k < R; ++k) put_bits(a->state, sbf, srow + k, wbits[T * R + k]);
+            }
+            free(wbits);
+            free(wf);
+        } else
         for (int c = 0; c < dim; ++c) {
             const int64_t srow = (int64_t)slot * a->st_slot + (int64_t)c * a->st_ch;
             for (int k = 0; k < W - 1; ++k) {

@@ -86,7 +86,7 @@ def run_oracle_verify(w: wl.VerifyWorkload, inp: dict, status: bool = True) -> d
     r["status"] = torch.full((w.n_seq,), -7, dtype=torch.int32) if status else None
     oracle.conv_verify(r["x"], r["conv_state"], r["weight"], r["bias"], r["out"], r["window"], layout=w.layout,
                        qk_channels=w.qk_channels, head_dim=w.head_dim, l2_eps=w.l2_eps, cache_idx=r["cache_idx"],
-                       state_off=r["state_off"], status=r["status"])
+                       state_off=r["state_off"], status=r["status"], parent=r.get("parent"))
     return r
 
 

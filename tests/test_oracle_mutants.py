@@ -19,9 +19,18 @@ SRC = os.path.join(os.path.dirname(oracle.__file__), "oracle.c")
 MUTANTS = [
     ("taps_reversed", "const float prod = wj * fullf[t + j];", "const float prod = wj * fullf[t + W - 1 - j];",
      lambda: pins.test_p2_impulse_response()),
-    ("bias_dropped", "float acc = a->bias ? bits_to_float(get_bits(a->bias, bf, c), bf) : 0.0f;", "float acc = 0.0f;",
+    ("bias_dropped",
+     "                float acc = a->bias ? bits_to_float(get_bits(a->bias, bf, c), bf) : 0.0f;\n"
+     "                for (int j = 0; j < W; ++j) {\n"
+     "                    const float wj = bits_to_float(get_bits(a->weight, bf, (int64_t)c * W + j), bf);\n"
+     "                    const float prod = wj * fullf[t + j];",
+     "                float acc = 0.0f;\n"
+     "                for (int j = 0; j < W; ++j) {\n"
+     "                    const float wj = bits_to_float(get_bits(a->weight, bf, (int64_t)c * W + j), bf);\n"
+     "                    const float prod = wj * fullf[t + j];",
      lambda: pins.test_p1_matches_float64_conv1d("f32", "dense", 4)),
-    ("silu_sign", "acc / (1.0f + expf(-acc))", "acc / (1.0f + expf(acc))",
+    ("silu_sign", "acc / (1.0f + expf(-acc));\n            }\n\n            if (a->recompute)",
+     "acc / (1.0f + expf(acc));\n            }\n\n            if (a->recompute)",
      lambda: pins.test_p1_matches_float64_conv1d("f32", "dense", 3)),
     ("eps_as_norm_floor", "1.0f / sqrtf(ss + a->l2_eps)", "1.0f / fmaxf(sqrtf(ss), a->l2_eps)",
      lambda: pins.test_p3_one_hot_taps_and_constant_group()),
@@ -29,7 +38,7 @@ MUTANTS = [
      lambda: pins.test_p4_sequential_equals_batched_in_T("dense", "f32")),
     ("state_write_lags", "put_bits(a->state, sbf, srow + k, full[T + k])", "put_bits(a->state, sbf, srow + k, full[T - 1 + k])",
      lambda: pins.test_p11_single_token_update()),
-    ("offset_ignored", "get_bits(a->state, sbf, srow + o + k)", "get_bits(a->state, sbf, srow + k)",
+    ("offset_ignored", "full[k] = get_bits(a->state, sbf, srow + o + k);", "full[k] = get_bits(a->state, sbf, srow + k);",
      lambda: pins.test_p10_state_offset_equals_preshifted_state()),
     ("commit_wrong_snapshot", "const int t = acc - 1;", "const int t = acc < a->T ? acc : acc - 1;",
      lambda: pins.test_p9_commit_equals_shorter_verify("dedup")),
@@ -63,6 +72,8 @@ MUTANTS = [
     ("mixed_state_read_as_x_dtype", "full[k] = get_bits(a->state, sbf, srow + o + k);\n                fullf[k] = bits_to_float(full[k], sbf);",
      "full[k] = get_bits(a->state, sbf, srow + o + k);\n                fullf[k] = bits_to_float(full[k], bf);",
      lambda: pins.test_m4_mixed_matches_float64_conv1d("bf16", "f32")),
+    ("tree_parent_ignored", "const int base = (a->parent[(int64_t)s * T + t] + 1) * R;", "const int base = t * R;",
+     lambda: pins.test_tr2_tree_paths_equal_chain_verifies()),
     ("padded_row_written", "if (slot < 0 || st) continue;\n\n", "if (st) continue;\n        if (slot < 0) { if (a->out) put_bits(a->out, bf, (int64_t)s * a->out_seq, 0); continue; }\n\n",
      lambda: pins.test_p7_padded_rows_untouched()),
 ]

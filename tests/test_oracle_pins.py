@@ -629,3 +629,91 @@ def test_m4_mixed_matches_float64_conv1d(xd, sd):
         got = r["out"][s].double()
         tol = 1e-5 if xd == "f32" else 2 ** -7
         assert torch.allclose(got, y, rtol=tol, atol=1e-6), float((got - y).abs().max())
+
+
+def _tree_inputs(w, parents, seed_shift=0):
+    inp = wl.make_inputs(w, seed=w.seed + seed_shift)
+    inp["parent"] = torch.tensor(parents, dtype=torch.int32).reshape(w.n_seq, w.T).contiguous()
+    return inp
+
+
+@pytest.mark.parametrize("width", [2, 3, 4])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_tr1_chain_parents_equal_the_plain_verify(width, dtype):
+    """Tree verify (sglang PR #46184, "Scope": tree verify keeps dense windows): parents t-1 make a
+    chain, which must reproduce the plain verify bitwise (outputs, snapshots, state)."""
+    w = small(n_seq=4, T=6, width=width, dtype=dtype, layout="dense", n_pad=1, extra_slots=1, seed=71,
+              state_offset=True)
+    chain = [[t - 1 for t in range(w.T)] for _ in range(w.n_seq)]
+    inp = _tree_inputs(w, chain)
+    rt = run_oracle_verify(w, inp)
+    plain = dict(inp)
+    plain.pop("parent")
+    rp = run_oracle_verify(w, plain)
+    for k in ("out", "window", "conv_state", "status"):
+        assert_bits_equal(rt[k], rp[k], k)
+
+
+def _paths(parents):
+    """Root-to-node token lists of a parent array."""
+    out = []
+    for t in range(len(parents)):
+        p, path = t, []
+        while p >= 0:
+            path.append(p)
+            p = parents[p]
+        out.append(path[::-1])
+    return out
+
+
+def test_tr2_tree_paths_equal_chain_verifies():
+    """Every node of a branching tree gets the output and snapshot that a chain verify over its
+    root-to-node path gives for its last token (bitwise)."""
+    T = 7
+    parents = [-1, 0, 0, 1, 1, 2, -1]  # two roots, branches at 0 and 1
+    w = small(n_seq=1, T=T, width=4, dtype="bf16", layout="dense", n_pad=0, extra_slots=0, seed=73)
+    inp = _tree_inputs(w, [parents])
+    rt = run_oracle_verify(w, inp)
+    for t, path in enumerate(_paths(parents)):
+        L = len(path)
+        wc = w.replace(T=L)
+        one = clone_inputs(inp)
+        one.pop("parent")
+        xc = inp["x"][:, path].contiguous()
+        one.update(x=xc, x_base=xc, out=wl.sentinel_tensor((1, L, w.dim), w.torch_dtype),
+                   window=wl.sentinel_tensor(wl.window_shape(wc), w.torch_dtype))
+        rc = run_oracle_verify(wc, one)
+        assert_bits_equal(rt["out"][0, t], rc["out"][0, L - 1], f"node {t} out")
+        assert_bits_equal(rt["window"][0, t], rc["window"][0, L - 1], f"node {t} snapshot")
+
+
+def test_tr3_commit_of_an_accepted_node_equals_its_path_state():
+    """Committing the window of an accepted path's last token (accept_len = its index + 1) leaves
+    the state a chain verify over that path leaves, bitwise."""
+    T = 6
+    parents = [-1, 0, 0, 2, 1, 4]
+    w = small(n_seq=1, T=T, width=3, dtype="f32", layout="dense", n_pad=0, extra_slots=0, seed=75)
+    inp = _tree_inputs(w, [parents])
+    for node, path in enumerate(_paths(parents)):
+        rt = run_oracle_verify(w, inp)
+        assert (run_oracle_commit(w, rt, accept_len=torch.tensor([node + 1], dtype=torch.int32)) == 0).all()
+        wc = w.replace(T=len(path))
+        one = clone_inputs(inp)
+        one.pop("parent")
+        xc = inp["x"][:, path].contiguous()
+        one.update(x=xc, x_base=xc, out=wl.sentinel_tensor((1, len(path), w.dim), w.torch_dtype),
+                   window=wl.sentinel_tensor(wl.window_shape(wc), w.torch_dtype))
+        rc = run_oracle_verify(wc, one)
+        assert_bits_equal(rt["conv_state"], rc["conv_state"], f"node {node}")
+
+
+def test_tree_invalid_parents_flagged():
+    """A parent outside [-1, t) flags the sequence (32) and touches nothing of it."""
+    w = small(n_seq=3, T=4, width=4, dtype="bf16", layout="dense", n_pad=0, extra_slots=0, seed=77)
+    inp = _tree_inputs(w, [[-1, 0, 1, 2], [-1, 1, 0, 0], [-2, 0, 0, 0]])
+    r = run_oracle_verify(w, inp)
+    assert r["status"].tolist() == [0, 32, 32]
+    for s in (1, 2):
+        slot = int(inp["cache_idx"][s])
+        assert_bits_equal(r["conv_state"][slot], inp["conv_state"][slot], "state")
+        assert_bits_equal(r["window"][s], inp["window"][s], "window")
