@@ -183,7 +183,7 @@ def oracle_step_times(w, reps_max: int, budget_s: float):
         t0 = time.perf_counter()
         oracle.conv_verify(inp["x"], state, inp["weight"], inp["bias"], out, win, layout=w.layout,
                            qk_channels=w.qk_channels, head_dim=w.head_dim, l2_eps=w.l2_eps,
-                           cache_idx=inp["cache_idx"], state_off=inp["state_off"])
+                           cache_idx=inp["cache_idx"], state_off=inp["state_off"], parent=inp.get("parent"))
         if w.layout != "history":
             oracle.conv_commit(state, win, inp["accept_len"], layout=w.layout, T=w.T, width=w.width,
                                cache_idx=inp["cache_idx"], x=inp["x"] if w.layout == "recompute" else None)
@@ -251,6 +251,7 @@ def run_ours(args, w, world, rank, local, dist):
     bias = inp["bias"].to(dev) if inp["bias"] is not None else None
     cache_idx = inp["cache_idx"].to(dev)
     state_off = inp["state_off"].to(dev) if inp["state_off"] is not None else None
+    parent = inp["parent"].to(dev) if inp.get("parent") is not None else None
     sets = []
     for i in range(n_sets):
         xb = inp["x_base"].to(dev)
@@ -260,7 +261,7 @@ def run_ours(args, w, world, rank, local, dist):
                  accept=inp["accept_len"].to(dev))
         s["va"] = cv.make_verify_args(x, s["conv_state"], weight, bias, s["out"], s["window"], layout=w.layout,
                                       qk_channels=w.qk_channels, head_dim=w.head_dim, l2_eps=w.l2_eps,
-                                      cache_idx=cache_idx, state_off=state_off)
+                                      cache_idx=cache_idx, state_off=state_off, parent=parent)
         if has_commit:
             s["ca"] = cv.make_commit_args(s["conv_state"], s["window"], s["accept"], layout=w.layout, T=w.T,
                                           width=w.width, cache_idx=cache_idx,

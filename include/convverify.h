@@ -48,7 +48,7 @@ extern "C" {
 #define CV_API
 #endif
 
-#define CV_ABI_VERSION 3
+#define CV_ABI_VERSION 4
 #define CV_MAX_T 128 /* draft tokens per verify call */
 
 typedef enum cv_dtype {
@@ -115,6 +115,7 @@ enum {
 #define CV_SEQ_BAD_ACCEPT 4 /* accept count outside 1..T (commit only) */
 #define CV_SEQ_TIMEOUT 8    /* a bounded wait for a bulk copy gave up (the sequence may be partly written) */
 #define CV_SEQ_BAD_SPAN 16  /* prefill: token span invalid or longer than max_seqlen */
+#define CV_SEQ_BAD_TREE 32  /* tree verify: a draft token's parent outside [-1, t) */
 
 /*
  * cv_conv_verify -- [atlas-batched] fused multi-token verify, batched over sequences.
@@ -167,6 +168,14 @@ enum {
  *                      arithmetic; snapshots and state receive x converted to the state dtype
  *                      (exact widening bf16 -> fp32, or round to nearest even fp32 -> bf16 with any
  *                      NaN becoming the quiet NaN 0x7fc0).  Mixed calls run the general kernel.
+ *   parent             int32 [n_seq][T] device array (row-major, contiguous) or NULL (a chain):
+ *                      tree verify ([sglang-46184] "Scope": tree verify keeps dense windows).  Token
+ *                      t's parent p in [-1, t) (-1: the committed window); its conv sees the
+ *                      parent's window followed by x_t, and snapshot t is window(t) =
+ *                      [window(p)[1 .. W-2], x_t].  The state is left on window(T-1).  The commit
+ *                      restores the accepted path's last node: accept_len = its index + 1.  Needs
+ *                      the dense layout and one dtype; a parent outside [-1, t) flags
+ *                      CV_SEQ_BAD_TREE.
  * Preconditions the library cannot check: distinct sequences use distinct slots; out and window do
  * not overlap themselves, each other, x, conv_state or weight.
  * Returns CV_OK after the launch is queued, or a negative CV_ERR_* code with nothing launched.
@@ -192,6 +201,7 @@ typedef struct cv_verify_args {
     int64_t win_seq_stride, win_step_stride, win_ch_stride, win_col_stride;
     int32_t *err;
     int32_t state_dtype; /* CV_STATE_* */
+    const int32_t *parent;
 } cv_verify_args;
 
 CV_API int cv_conv_verify(const cv_verify_args *args, void *stream);

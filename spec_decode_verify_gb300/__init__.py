@@ -16,14 +16,15 @@ import os
 from typing import Optional
 
 __all__ = ["conv_verify", "conv_commit", "conv_prefill", "verify_plan", "status_string", "load_library", "library_path",
-           "CvError", "DENSE", "DEDUP", "HISTORY", "RECOMPUTE", "SEQ_BAD_SLOT", "SEQ_BAD_OFFSET", "SEQ_BAD_ACCEPT"]
+           "CvError", "DENSE", "DEDUP", "HISTORY", "RECOMPUTE", "SEQ_BAD_SLOT", "SEQ_BAD_OFFSET", "SEQ_BAD_ACCEPT",
+           "SEQ_TIMEOUT", "SEQ_BAD_SPAN", "SEQ_BAD_TREE"]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 library_path = os.path.join(_PKG, "_build", "libconvverify.so")
 
 DENSE, DEDUP, HISTORY, RECOMPUTE = 1, 2, 3, 4
 F32, BF16 = 0, 1
-SEQ_BAD_SLOT, SEQ_BAD_OFFSET, SEQ_BAD_ACCEPT, SEQ_TIMEOUT, SEQ_BAD_SPAN = 1, 2, 4, 8, 16
+SEQ_BAD_SLOT, SEQ_BAD_OFFSET, SEQ_BAD_ACCEPT, SEQ_TIMEOUT, SEQ_BAD_SPAN, SEQ_BAD_TREE = 1, 2, 4, 8, 16, 32
 MAX_T = 128
 
 c_i32, c_i64, c_vp = ctypes.c_int32, ctypes.c_int64, ctypes.c_void_p
@@ -41,7 +42,7 @@ class VerifyArgs(ctypes.Structure):
         ("cache_idx", c_vp), ("state_off", c_vp), ("weight", c_vp), ("bias", c_vp),
         ("window", c_vp), ("window_layout", c_i32), ("reserved0", c_i32),
         ("win_seq_stride", c_i64), ("win_step_stride", c_i64), ("win_ch_stride", c_i64), ("win_col_stride", c_i64),
-        ("err", c_vp), ("state_dtype", c_i32),
+        ("err", c_vp), ("state_dtype", c_i32), ("parent", c_vp),
     ]
 
 
@@ -161,16 +162,20 @@ def _stream_ptr(stream) -> Optional[int]:
 
 
 def make_verify_args(x, conv_state, weight, bias, out, window, *, layout, qk_channels, head_dim,
-                     l2_eps=1e-6, cache_idx=None, state_off=None, err=None, check_device=True) -> VerifyArgs:
+                     l2_eps=1e-6, cache_idx=None, state_off=None, err=None, parent=None,
+                     check_device=True) -> VerifyArgs:
     """Build cv_verify_args from tensors.
 
     x [n_seq, T, dim] (channel stride 1, any seq/token strides), conv_state [n_slots, dim, S]
-    (column stride 1), weight [dim, W] contiguous, bias [dim] or None, out [n_seq, T, dim] (channel
-    stride 1; it may have the other dtype than x: mixed dtypes), window dense [n_seq, T, dim, W-1] or
+    (column stride 1; it may have the other dtype than x: mixed dtypes), weight [dim, W] contiguous,
+    bias [dim] or None, out [n_seq, T, dim] (channel stride 1), window dense [n_seq, T, dim, W-1] or
     dedup [n_seq, dim, T+W-2] (any strides, the dtype of conv_state), or
     None with layout "history" (conv_state [n_slots, dim, S >= T+W-2] then receives the snapshot
     row and the next call reads at state_off = accept_len - 1) or "recompute" (outputs only; the
-    commit rebuilds the state from x), cache_idx / state_off / err int32 [n_seq] or None."""
+    commit rebuilds the state from x), cache_idx / state_off / err int32 [n_seq] or None, parent int32
+    [n_seq, T] contiguous (tree verify, dense layout) or None."""
+    if parent is not None and (not parent.is_contiguous() or parent.dtype.itemsize != 4):
+        raise ValueError("parent must be a contiguous int32 [n_seq, T] tensor")
     lay = _layout_code(layout)
     ptr = _dev_ptr if check_device else (lambda t, n, required=True: None if t is None else t.data_ptr())
     n_seq, T, dim = x.shape
@@ -191,11 +196,12 @@ def make_verify_args(x, conv_state, weight, bias, out, window, *, layout, qk_cha
         window=ptr(window, "window", lay not in (HISTORY, RECOMPUTE)),
         window_layout=lay, reserved0=0, win_seq_stride=ws[0], win_step_stride=ws[1], win_ch_stride=ws[2],
         win_col_stride=ws[3], err=ptr(err, "err", False),
-        state_dtype=0 if conv_state.dtype == x.dtype else _dtype_code(conv_state) + 1)
+        state_dtype=0 if conv_state.dtype == x.dtype else _dtype_code(conv_state) + 1,
+        parent=ptr(parent, "parent", False))
 
 
 def conv_verify(x, conv_state, weight, bias, out, window, *, layout, qk_channels, head_dim, l2_eps=1e-6,
-                cache_idx=None, state_off=None, err=None, stream=None) -> None:
+                cache_idx=None, state_off=None, err=None, parent=None, stream=None) -> None:
     """Queue one batched verify on ``stream`` (default: torch's current stream).
 
     Writes out, window, conv_state (and err); raises CvError on an invalid argument.  With layout
@@ -209,18 +215,19 @@ def conv_verify(x, conv_state, weight, bias, out, window, *, layout, qk_channels
     if bias is not None and bias.dtype != x.dtype:
         raise TypeError("bias must have the dtype of x")
     a = make_verify_args(x, conv_state, weight, bias, out, window, layout=layout, qk_channels=qk_channels,
-                         head_dim=head_dim, l2_eps=l2_eps, cache_idx=cache_idx, state_off=state_off, err=err)
+                         head_dim=head_dim, l2_eps=l2_eps, cache_idx=cache_idx, state_off=state_off, err=err,
+                         parent=parent)
     rc = load_library().cv_conv_verify(ctypes.byref(a), _stream_ptr(stream))
     if rc != 0:
         raise CvError(rc, "cv_conv_verify")
 
 
 def verify_plan(x, conv_state, weight, bias, out, window, *, layout, qk_channels, head_dim, l2_eps=1e-6,
-                cache_idx=None, state_off=None, err=None) -> LaunchPlan:
+                cache_idx=None, state_off=None, err=None, parent=None) -> LaunchPlan:
     """The launch cv_conv_verify would make (validates without touching the GPU)."""
     a = make_verify_args(x, conv_state, weight, bias, out, window, layout=layout, qk_channels=qk_channels,
                          head_dim=head_dim, l2_eps=l2_eps, cache_idx=cache_idx, state_off=state_off, err=err,
-                         check_device=False)
+                         parent=parent, check_device=False)
     pl = LaunchPlan()
     rc = load_library().cv_verify_plan(ctypes.byref(a), ctypes.byref(pl))
     if rc != 0:

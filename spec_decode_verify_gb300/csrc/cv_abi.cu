@@ -30,6 +30,7 @@ constexpr int kSmemPerSM = 232448;       // usable shared memory per SM
 constexpr int kSmemPerBlockReserved = 1024;
 constexpr int kMinThreads = 32;
 constexpr int kGenericSmemBudget = 96 * 1024;
+constexpr long long kTreeSmemBudget = 64 * 1024;  // tree verify: token windows kept per block
 constexpr int kCommitThreads = 128;
 constexpr int kCommitRowThreads = 64;  // dedup commit: 512 channels per block
 constexpr int kSmemMax = 227 * 1024;
@@ -70,6 +71,9 @@ int check_verify(const cv_verify_args *a) {
     if (a->window_layout != CV_WINDOW_DENSE && a->window_layout != CV_WINDOW_DEDUP && !nowin) return CV_ERR_LAYOUT;
     if (a->window_layout == CV_WINDOW_DEDUP && a->win_step_stride != a->win_col_stride) return CV_ERR_LAYOUT;
     if (hist && a->state_cols < a->T + a->width - 2) return CV_ERR_SHAPE;
+    // tree verify: dense snapshots only, one dtype
+    if (a->parent && a->window_layout != CV_WINDOW_DENSE) return CV_ERR_LAYOUT;
+    if (a->parent && a->state_dtype != CV_STATE_SAME && a->state_dtype - 1 != a->dtype) return CV_ERR_DTYPE;
     if (a->qk_channels < 0 || a->qk_channels > a->dim) return CV_ERR_HEAD_DIM;
     if (a->qk_channels > 0 && (!pow2(a->head_dim) || a->head_dim < 8 || a->head_dim > 256 ||
                                a->qk_channels % a->head_dim != 0))
@@ -151,6 +155,21 @@ int plan_verify(const cv_verify_args *a, cv_launch_plan *pl) {
     const int esize = a->dtype == CV_BF16 ? 2 : 4;
     const bool mixed = mixed_dtypes(a);
     const int R = a->width - 1;
+    std::memset(pl, 0, sizeof *pl);
+    if (a->parent) {
+        // tree verify: its own kernel, 8 channels per thread, one block per (channel block, sequence)
+        int threads = 128;
+        while (threads > kMinThreads && 8 * (threads / 2) >= a->dim) threads /= 2;
+        // the block's token windows in shared memory when they fit in kTreeSmemBudget
+        const long long kept = (long long)a->T * R * 8 * threads * esize;
+        pl->threads = threads;
+        pl->channels_per_block = 8 * threads;
+        pl->smem_bytes = kept <= kTreeSmemBudget ? (int)kept : 0;
+        pl->path = 5;
+        pl->grid_x = (a->dim + pl->channels_per_block - 1) / pl->channels_per_block;
+        pl->grid_y = a->n_seq;
+        return CV_OK;
+    }
     const int min_threads =
         (a->qk_channels > 0 && a->head_dim / 8 > kMinThreads) ? a->head_dim / 8 : kMinThreads;
     const cvk::KernelSet &ks = kernel_set(a->dtype, a->width);
@@ -303,6 +322,7 @@ int launch_verify(const cv_verify_args *a, const cv_launch_plan &pl, cudaStream_
     p.dedup = a->window_layout == CV_WINDOW_DEDUP;
     p.hist = a->window_layout == CV_WINDOW_HISTORY;
     p.recomp = a->window_layout == CV_WINDOW_RECOMPUTE;
+    p.parent = a->parent;
     p.compact = pl.path == 3 && pipe_compacts(a);
     if (p.hist || p.recomp) p.win = nullptr;
     p.w_seq = a->win_seq_stride;
@@ -326,13 +346,21 @@ int launch_verify(const cv_verify_args *a, const cv_launch_plan &pl, cudaStream_
     p.st_vec = state_packed(a->conv_state, a->state_slot_stride, a->state_ch_stride, a->width, ssize);
     p.w_vec = aligned16(a->weight);
     p.b_vec = a->bias ? aligned16(a->bias) : 0;
+    if (pl.path == 5) {
+        // tree verify: pitch != 0 -> token windows in shared memory; st_vec -> packed 16-byte dense
+        // snapshot runs of 8 channels x (W-1) columns
+        p.pitch = pl.smem_bytes > 0 ? 1 : 0;
+        p.st_vec = a->dim % 8 == 0 && aligned16(a->window) && a->win_ch_stride == a->width - 1 &&
+                   a->win_col_stride == 1 && stride16(a->win_seq_stride, esize) && stride16(a->win_step_stride, esize);
+    }
 
     const cvk::KernelSet &ks = kernel_set(a->dtype, a->width);
     const int ci = pl.channels_per_block / pl.threads == 8 ? 1 : 0;
     cvk::VerifyKernel k = pl.path == 0   ? (mixed ? ks.generic_mixed : ks.generic)
                           : pl.path == 1 ? ks.fast[ci][a->T]
                           : pl.path == 2 ? ks.fast[ci][0]
-                                         : ks.pipe[ci][a->T];
+                          : pl.path == 3 ? ks.pipe[ci][a->T]
+                                         : ks.tree;
     if (ensure_smem(reinterpret_cast<const void *>(k), pl.smem_bytes) != cudaSuccess) return CV_ERR_LAUNCH;
     if (launch_pdl(k, dim3(pl.grid_x, pl.grid_y), pl.threads, pl.smem_bytes, stream, p) != cudaSuccess)
         return CV_ERR_LAUNCH;

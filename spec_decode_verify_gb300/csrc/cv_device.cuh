@@ -30,6 +30,7 @@ struct VerifyParams {
     int hist;     // history-row state: the snapshot row goes into the state row (no window buffer)
     int compact;  // pipelined kernel: walk only the sequences with a cache slot >= 0 (list in shared memory)
     int recomp;   // recompute rollback: outputs only (no snapshots, state not written)
+    const int *parent;  // tree verify: [n_seq][T] parent of each draft token, or null (a chain)
     int x_vec, out_vec, st_vec, w_vec, b_vec;  // 16-byte vector access allowed (checked on the host)
 };
 

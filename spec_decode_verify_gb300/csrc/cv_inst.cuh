@@ -8,6 +8,7 @@
 #include "cv_verify_fast.cuh"
 #include "cv_verify_generic.cuh"
 #include "cv_verify_pipe.cuh"
+#include "cv_verify_tree.cuh"
 
 namespace cvk {
 namespace {
@@ -22,6 +23,7 @@ KernelSet make_set(std::integer_sequence<int, Ts...>) {
     ((k.pipe[1][Ts + 1] = verify_pipe<B, W, Ts + 1, 8>), ...);
     k.max_static_t = (int)sizeof...(Ts);
     k.generic = verify_generic<B, W>;
+    k.tree = verify_tree<B, W>;
     // mixed dtypes: the state and the snapshots in the other dtype
     k.generic_mixed = verify_generic<B, W, std::conditional_t<sizeof(B) == 2, uint32_t, uint16_t>>;
     k.commit = commit_kernel<B, W>;

@@ -22,6 +22,7 @@ struct KernelSet {
     VerifyKernel pipe[2][kMaxStaticT + 1];
     int max_static_t;
     VerifyKernel generic;
+    VerifyKernel tree;  // draft tokens with parents (dense snapshots)
     VerifyKernel generic_mixed;  // state and snapshots in the other dtype (bf16 <-> fp32)
     CommitKernel commit;
     CommitKernel commit_rows;

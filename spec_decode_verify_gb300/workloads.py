@@ -16,6 +16,8 @@ The five named workloads follow the shapes the pages describe:
     width-3 deduplicated windows);
   * the benchmark shape with an fp32 state and fp32 snapshots under bf16 inputs (PR #46184's
     extra check covers mixed input and state dtypes);
+  * the benchmark shape with the draft tokens forming a random tree (PR #46184 "Scope": tree
+    verify keeps dense windows);
   * the benchmark shape again with the recompute rollback (memra-engine ssm_conv_ring_rebuild_dc:
     no snapshots; the commit rebuilds the state from the kept window and the accepted inputs) and
     with the history-row state: the state row of each slot is the deduplicated [dim, T+W-2] row
@@ -58,6 +60,7 @@ class VerifyWorkload:
     qkv_split: Optional[tuple] = None  # (q, k, v) channel counts of separately drawn conv weights
     state_offset: bool = False  # per-sequence offset = accept_len - 1 into a wider state row
     state_dtype: Optional[str] = None  # dtype of state and window when it differs from x ("f32"/"bf16")
+    tree: bool = False  # draft tokens form a tree: a random earlier parent (or -1) per token
     seed: int = 0
 
     @property
@@ -115,6 +118,9 @@ WORKLOADS = {
         VerifyWorkload("n128_t8_dim10240_w4_bf16x_f32state_dedup_pad13", n_seq=128, T=8, dim=10240, width=4,
                        qk_channels=4096, head_dim=128, dtype="bf16", state_dtype="f32", layout="dedup", n_pad=13,
                        extra_slots=16, seed=7),
+        VerifyWorkload("n128_t8_dim10240_w4_bf16_tree_dense_pad13", n_seq=128, T=8, dim=10240, width=4,
+                       qk_channels=4096, head_dim=128, dtype="bf16", layout="dense", n_pad=13, extra_slots=16,
+                       tree=True, seed=8),
         VerifyWorkload("n128_t8_dim10240_w4_bf16_history_pad13", n_seq=128, T=8, dim=10240, width=4,
                        qk_channels=4096, head_dim=128, dtype="bf16", layout="history", n_pad=13,
                        extra_slots=16, state_offset=True, seed=5),
@@ -175,8 +181,14 @@ def make_inputs(w: VerifyWorkload, seed: Optional[int] = None) -> dict:
     state_off = (accept - 1).to(torch.int32) if w.state_offset else None
     out = sentinel_tensor((w.n_seq, w.T, w.dim), dt)
     window = None if w.layout in ("history", "recompute") else sentinel_tensor(window_shape(w), w.state_torch_dtype)
-    return dict(x=x, x_base=x_wide, conv_state=state, weight=weight, bias=bias, cache_idx=cache_idx,
-                state_off=state_off, accept_len=accept, out=out, window=window)
+    r = dict(x=x, x_base=x_wide, conv_state=state, weight=weight, bias=bias, cache_idx=cache_idx,
+             state_off=state_off, accept_len=accept, out=out, window=window)
+    if w.tree:
+        par = np.full((w.n_seq, w.T), -1, dtype=np.int32)
+        for t in range(1, w.T):
+            par[:, t] = rng.integers(-1, t, size=w.n_seq)
+        r["parent"] = torch.from_numpy(par)
+    return r
 
 
 def random_case(rng: np.random.Generator, **over) -> VerifyWorkload:

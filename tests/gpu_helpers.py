@@ -31,7 +31,7 @@ def run_gpu_verify(cv, w: wl.VerifyWorkload, inp: dict, err=True) -> dict:
     d["err"] = torch.full((w.n_seq,), -7, dtype=torch.int32, device="cuda") if err else None
     cv.conv_verify(d["x"], d["conv_state"], d["weight"], d["bias"], d["out"], d["window"], layout=w.layout,
                    qk_channels=w.qk_channels, head_dim=w.head_dim, l2_eps=w.l2_eps, cache_idx=d["cache_idx"],
-                   state_off=d["state_off"], err=d["err"])
+                   state_off=d["state_off"], err=d["err"], parent=d.get("parent"))
     torch.cuda.synchronize()
     return d
 

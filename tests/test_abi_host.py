@@ -33,7 +33,7 @@ def test_exports_every_declared_function(lib):
     assert {"cv_conv_verify", "cv_conv_commit", "cv_verify_plan", "cv_status_string", "cv_abi_version"} <= set(names)
     for n in names:
         assert hasattr(lib, n), f"{n} declared in the header but not exported"
-    assert lib.cv_abi_version() == 3
+    assert lib.cv_abi_version() == 4
 
 
 def test_exports_nothing_undeclared(lib):
@@ -51,7 +51,8 @@ def _args(w: wl.VerifyWorkload, **over):
     inp = wl.make_inputs(w)
     a = cv.make_verify_args(inp["x"], inp["conv_state"], inp["weight"], inp["bias"], inp["out"], inp["window"],
                             layout=w.layout, qk_channels=w.qk_channels, head_dim=w.head_dim,
-                            cache_idx=inp["cache_idx"], check_device=False)
+                            cache_idx=inp["cache_idx"], parent=inp.get("parent"), check_device=False)
+    _args.keep = inp  # the struct holds raw pointers into these tensors
     for k, v in over.items():
         setattr(a, k, v)
     return a
@@ -126,7 +127,8 @@ def test_history_validation_and_paths(lib):
 @pytest.mark.parametrize("name,path", [
     ("n1_t2_dim512_w4_f32_dense", 3), ("n4_t4_dim4096_w4_bf16_dedup_bias", 3),
     ("n8_t17_dim8192_w4_bf16_dense_qkvsplit_xstride12288", 3), ("n64_t8_dim6144_w3_bf16_dense_nol2_stateoff", 1),
-    ("n128_t8_dim10240_w4_bf16_history_pad13", 3), ("n128_t8_dim10240_w4_bf16_recompute_pad13", 3)])
+    ("n128_t8_dim10240_w4_bf16_history_pad13", 3), ("n128_t8_dim10240_w4_bf16_recompute_pad13", 3),
+    ("n128_t8_dim10240_w4_bf16_tree_dense_pad13", 5), ("n128_t8_dim10240_w4_bf16x_f32state_dedup_pad13", 0)])
 def test_plan_paths_of_named_workloads(lib, name, path):
     w = wl.WORKLOADS[name]
     rc, pl = _plan(lib, _args(w))
@@ -329,3 +331,22 @@ def test_mixed_dtypes_plan_and_validation(lib):
     w2 = W3.replace(dtype="f32", state_dtype="bf16", n_seq=4, n_pad=0, extra_slots=0)
     a2 = _args(w2)
     assert a2.state_dtype == 2 and _plan(lib, a2)[1].path == 0
+
+
+def test_tree_plan_and_validation(lib):
+    """Tree verify: its own kernel (path 5) for the dense layout; other layouts and mixed dtypes
+    are rejected."""
+    w = wl.WORKLOADS["n8_t17_dim8192_w4_bf16_dense_qkvsplit_xstride12288"]
+    inp = wl.make_inputs(w)
+    parent = torch.arange(-1, w.T - 1, dtype=torch.int32).repeat(w.n_seq, 1).contiguous()
+    a = cv.make_verify_args(inp["x"], inp["conv_state"], inp["weight"], inp["bias"], inp["out"], inp["window"],
+                            layout="dense", qk_channels=w.qk_channels, head_dim=w.head_dim,
+                            cache_idx=inp["cache_idx"], parent=parent, check_device=False)
+    rc, pl = _plan(lib, a)
+    assert rc == 0 and pl.path == 5 and (pl.threads, pl.grid_x, pl.grid_y) == (128, 8, 8)
+    a.window_layout = 2
+    a.win_step_stride = a.win_col_stride
+    assert _plan(lib, a)[0] == -8
+    a = _args(W3.replace(state_dtype="f32", layout="dense", n_seq=2, n_pad=0, extra_slots=0))
+    a.parent = parent.data_ptr()
+    assert _plan(lib, a)[0] == -6
