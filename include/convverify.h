@@ -167,7 +167,8 @@ enum {
  *                      [sglang-46184] "Accuracy Tests"): inputs are widened exactly for the
  *                      arithmetic; snapshots and state receive x converted to the state dtype
  *                      (exact widening bf16 -> fp32, or round to nearest even fp32 -> bf16 with any
- *                      NaN becoming the quiet NaN 0x7fc0).  Mixed calls run the general kernel.
+ *                      NaN becoming the quiet NaN 0x7fc0).  Mixed calls take the pipelined kernel
+ *                      (path 3) for T <= 8 with packed buffers, the general kernel otherwise.
  *   parent             int32 [n_seq][T] device array (row-major, contiguous) or NULL (a chain):
  *                      tree verify ([sglang-46184] "Scope": tree verify keeps dense windows).  Token
  *                      t's parent p in [-1, t) (-1: the committed window); its conv sees the

@@ -11,7 +11,8 @@
 //                             (sequence, channel block) units and load each by bulk copy into
 //                             double-buffered shared memory, two units ahead.  The history layout
 //                             takes it when its state rows are the packed [dim][T+W-2] rows, and
-//                             the general kernel otherwise.
+//                             the general kernel otherwise.  Mixed dtypes (state and snapshots in
+//                             the other dtype) take it for T <= 8, the general kernel otherwise.
 #include <atomic>
 #include <cstdint>
 #include <cstring>
@@ -105,14 +106,15 @@ bool io_packed(const cv_verify_args *a, int esize) {
     return aligned16(a->weight) && (!a->bias || aligned16(a->bias));
 }
 
-bool fast_eligible(const cv_verify_args *a, int esize, int max_static_t) {
+// (esize: bytes of an x element; ssize: of a state and snapshot element)
+bool fast_eligible(const cv_verify_args *a, int esize, int ssize, int max_static_t) {
     const int R = a->width - 1;
     const long long Q = a->T + R - 1;
     if (a->window_layout == CV_WINDOW_HISTORY || a->window_layout == CV_WINDOW_RECOMPUTE || !io_packed(a, esize))
         return false;
-    if (!aligned16(a->window) || !stride16(a->win_seq_stride, esize) || a->win_col_stride != 1) return false;
+    if (!aligned16(a->window) || !stride16(a->win_seq_stride, ssize) || a->win_col_stride != 1) return false;
     if (a->window_layout == CV_WINDOW_DEDUP) return a->win_ch_stride == Q && a->T <= max_static_t;
-    return a->win_ch_stride == R && stride16(a->win_step_stride, esize);
+    return a->win_ch_stride == R && stride16(a->win_step_stride, ssize);
 }
 
 // Halve a block (down to 32 threads) while the launch would have fewer than two blocks per SM and
@@ -177,19 +179,22 @@ int plan_verify(const cv_verify_args *a, cv_launch_plan *pl) {
 
     const bool hist = a->window_layout == CV_WINDOW_HISTORY;
     const bool recomp = a->window_layout == CV_WINDOW_RECOMPUTE;
-    const bool fast = fast_eligible(a, esize, ks.max_static_t);
+    const int ssize = state_dtype_of(a) == CV_BF16 ? 2 : 4;
+    const bool fast = fast_eligible(a, esize, ssize, ks.max_static_t);
     const int cpt = (a->qk_channels > 0 && a->head_dim / 4 > 32) ? 8 : 4;
     // the pipelined kernel stages packed state rows whole (state_ch_stride == state_cols): the
     // committed windows of [dim][W-1] rows, or wider rows read at an offset; the history layout
     // needs rows of exactly T+W-2 columns
-    const bool rows_packed = aligned16(a->conv_state) && stride16(a->state_slot_stride, esize) &&
+    const bool rows_packed = aligned16(a->conv_state) && stride16(a->state_slot_stride, ssize) &&
                              a->state_ch_stride == a->state_cols;
-    bool pipe_ok = !mixed && io_packed(a, esize) && a->T <= ks.max_static_t && rows_packed &&
-                         (hist ? a->state_cols == a->T + R - 1 : (recomp || fast));
+    // (mixed dtypes: compiled for T <= kMaxMixedT)
+    bool pipe_ok = (!mixed || a->T <= cvk::kMaxMixedT) && io_packed(a, esize) && a->T <= ks.max_static_t &&
+                   rows_packed && (hist ? a->state_cols == a->T + R - 1 : (recomp || fast));
     const bool wide = !hist && a->state_cols != R;
     // (wide rows cost whole-row reads and element stores of the window; the pipeline pays that
     // back only when every block walks at least two units, otherwise the one-pass kernel wins)
-    if (pipe_ok && wide && fast && units_per_pipe_block(a, cpt) < 2.0) pipe_ok = false;
+    // (mixed dtypes have no one-pass kernel)
+    if (pipe_ok && wide && fast && !mixed && units_per_pipe_block(a, cpt) < 2.0) pipe_ok = false;
     if (pipe_ok) {
         auto part = [](long long b) { return (b + 127) / 128 * 128; };
         int threads = kPipeThreads;
@@ -200,10 +205,10 @@ int plan_verify(const cv_verify_args *a, cv_launch_plan *pl) {
         const long long Q = a->T + R - 1;
         // two stages (x rows + committed windows, or whole history rows) and two image buffers
         // (dedup row + committed windows, or the history row alone; none for the recompute
-        // rollback); 2 mbarriers, 2 slots, 2 offsets
-        const long long stage = part(a->T * bc * esize) + part((long long)a->state_cols * bc * esize);
-        long long image = (hist || recomp || wide) ? 0 : part(R * bc * esize);
-        if (a->window_layout == CV_WINDOW_DEDUP || hist) image += part(Q * bc * esize);
+        // rollback), the state parts in the state's dtype; 2 mbarriers, 2 slots, 2 offsets
+        const long long stage = part(a->T * bc * esize) + part((long long)a->state_cols * bc * ssize);
+        long long image = (hist || recomp || wide) ? 0 : part(R * bc * ssize);
+        if (a->window_layout == CV_WINDOW_DEDUP || hist) image += part(Q * bc * ssize);
         const long long smem = 2 * stage + 2 * image + 32 + (pipe_compacts(a) ? 16 + 4LL * a->n_seq : 0);
         int per_sm = (int)(kSmemPerSM / (smem + kSmemPerBlockReserved));
         if (per_sm > pipe_blocks_per_sm(cpt, a->T)) per_sm = pipe_blocks_per_sm(cpt, a->T);
@@ -359,7 +364,7 @@ int launch_verify(const cv_verify_args *a, const cv_launch_plan &pl, cudaStream_
     cvk::VerifyKernel k = pl.path == 0   ? (mixed ? ks.generic_mixed : ks.generic)
                           : pl.path == 1 ? ks.fast[ci][a->T]
                           : pl.path == 2 ? ks.fast[ci][0]
-                          : pl.path == 3 ? ks.pipe[ci][a->T]
+                          : pl.path == 3 ? (mixed ? ks.pipe_mixed[ci][a->T] : ks.pipe[ci][a->T])
                                          : ks.tree;
     if (ensure_smem(reinterpret_cast<const void *>(k), pl.smem_bytes) != cudaSuccess) return CV_ERR_LAUNCH;
     if (launch_pdl(k, dim3(pl.grid_x, pl.grid_y), pl.threads, pl.smem_bytes, stream, p) != cudaSuccess)

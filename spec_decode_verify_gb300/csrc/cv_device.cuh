@@ -93,6 +93,21 @@ template <typename B> __device__ __forceinline__ uint32_t raw_of(float f) {
     return sizeof(B) == 2 ? (__float_as_uint(f) >> 16) : __float_as_uint(f);
 }
 
+// Raw bits of an element of type BX as an element of type BS: the same bits when the types agree,
+// bf16 widened exactly to fp32, or fp32 rounded to the nearest bf16 (ties to even; any NaN becomes
+// the quiet NaN 0x7fc0).
+template <typename BX, typename BS>
+__device__ __forceinline__ uint32_t convert_bits(uint32_t v) {
+    if constexpr (sizeof(BX) == sizeof(BS)) {
+        return v;
+    } else if constexpr (sizeof(BX) == 2) {
+        return v << 16;
+    } else {
+        if ((v & 0x7fffffffu) > 0x7f800000u) return 0x7fc0u;
+        return __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(v)));
+    }
+}
+
 // Element i (0..7) of 8 packed elements held as 32-bit words, widened to fp32.
 template <typename B> __device__ __forceinline__ float elem_f(const uint32_t *w, int i) {
     if (sizeof(B) == 2) return (i & 1) ? __uint_as_float(w[i >> 1] & 0xffff0000u) : __uint_as_float(w[i >> 1] << 16);

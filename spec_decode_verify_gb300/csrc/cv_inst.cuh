@@ -12,9 +12,20 @@
 
 namespace cvk {
 namespace {
+// the other dtype of the state and the snapshots (mixed dtypes)
+template <typename B>
+using OtherT = std::conditional_t<sizeof(B) == 2, uint32_t, uint16_t>;
+
+template <typename B, int W, int... Ms>
+void set_mixed(KernelSet &k, std::integer_sequence<int, Ms...>) {
+    ((k.pipe_mixed[0][Ms + 1] = verify_pipe<B, W, Ms + 1, 4, OtherT<B>>), ...);
+    ((k.pipe_mixed[1][Ms + 1] = verify_pipe<B, W, Ms + 1, 8, OtherT<B>>), ...);
+}
+
 template <typename B, int W, int... Ts>
 KernelSet make_set(std::integer_sequence<int, Ts...>) {
     KernelSet k{};
+    set_mixed<B, W>(k, std::make_integer_sequence<int, (sizeof...(Ts) < kMaxMixedT ? sizeof...(Ts) : kMaxMixedT)>{});
     k.fast[0][0] = verify_fast<B, W, 0, 4>;
     k.fast[1][0] = verify_fast<B, W, 0, 8>;
     ((k.fast[0][Ts + 1] = verify_fast<B, W, Ts + 1, 4>), ...);
@@ -25,7 +36,7 @@ KernelSet make_set(std::integer_sequence<int, Ts...>) {
     k.generic = verify_generic<B, W>;
     k.tree = verify_tree<B, W>;
     // mixed dtypes: the state and the snapshots in the other dtype
-    k.generic_mixed = verify_generic<B, W, std::conditional_t<sizeof(B) == 2, uint32_t, uint16_t>>;
+    k.generic_mixed = verify_generic<B, W, OtherT<B>>;
     k.commit = commit_kernel<B, W>;
     k.commit_rows = commit_rows<B, W>;
     k.commit_recompute = commit_recompute<B, W>;

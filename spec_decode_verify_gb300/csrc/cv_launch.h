@@ -13,6 +13,8 @@ using PrefillKernel = void (*)(PrefillParams);
 // in registers).  Above it the dense layout runs the chunked kernel and the dedup layout the
 // general kernel.
 constexpr int kMaxStaticT = 17;
+// Largest T of the pipelined kernel compiled for mixed dtypes; above it they take the general kernel.
+constexpr int kMaxMixedT = 8;
 
 struct KernelSet {
     // fast[c][T]: c = 0 for 4 channels per thread, 1 for 8; T in 1..max_static_t compiled with T
@@ -20,6 +22,9 @@ struct KernelSet {
     VerifyKernel fast[2][kMaxStaticT + 1];
     // pipe[c][T]: persistent, bulk-copy pipelined, T in 1..max_static_t (index 0 unused)
     VerifyKernel pipe[2][kMaxStaticT + 1];
+    // pipe_mixed[c][T]: the same with the state and the snapshots in the other dtype (bf16 <-> fp32),
+    // T in 1..kMaxMixedT
+    VerifyKernel pipe_mixed[2][kMaxMixedT + 1];
     int max_static_t;
     VerifyKernel generic;
     VerifyKernel tree;  // draft tokens with parents (dense snapshots)

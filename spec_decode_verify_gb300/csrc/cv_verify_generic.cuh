@@ -56,13 +56,16 @@ template <typename B> __device__ __forceinline__ void store_oct(B *p, const Oct<
 // and the dense per-token chunks: one coalesced run of nch*ncol elements), channel-stride-1 (a
 // transposed row: one contiguous run of channels per column), and anything else element by element.
 // Tile element -> destination element: the same bits when the types agree; otherwise (a tile of
-// fp32 bits written to bf16) round to nearest even, any NaN to the quiet NaN 0x7fc0.
+// fp32 bits written to bf16) the upper half when the element was widened from the state (its raw
+// bits come back, NaN payloads included), else round to nearest even, any NaN to the quiet NaN
+// 0x7fc0.
 template <typename BD, typename TT>
-__device__ __forceinline__ BD from_tile(TT v) {
+__device__ __forceinline__ BD from_tile(TT v, bool widened) {
     if constexpr (sizeof(BD) == sizeof(TT)) {
         return (BD)v;
     } else {
         const uint32_t u = (uint32_t)v;
+        if (widened) return (BD)(u >> 16);
         if ((u & 0x7fffffffu) > 0x7f800000u) return (BD)0x7fc0u;
         return (BD)__bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(u)));
     }
@@ -76,9 +79,11 @@ __device__ __forceinline__ TT to_tile(BS v) {
         return (TT)((uint32_t)v << 16);
 }
 
+// (converting writes: tile rows below state_rows hold the committed window, widened from the
+// state's own type)
 template <typename B, typename BD = B>
 __device__ __forceinline__ void write_view(const B *__restrict__ tile, int pitch, int jofs, int ncol, BD *dst,
-                                           long long ch_stride, long long col_stride, int nch) {
+                                           long long ch_stride, long long col_stride, int nch, int state_rows = 0) {
     constexpr int CH = 16 / (int)sizeof(B);
     if constexpr (!std::is_same_v<B, BD>) {
         // converting writes: element by element in destination order
@@ -86,12 +91,12 @@ __device__ __forceinline__ void write_view(const B *__restrict__ tile, int pitch
         if (col_stride == 1) {
             for (int i = threadIdx.x; i < n; i += blockDim.x) {
                 const int c = i / ncol, q = i - c * ncol;
-                dst[c * ch_stride + q] = from_tile<BD>(tile[(jofs + q) * pitch + c]);
+                dst[c * ch_stride + q] = from_tile<BD>(tile[(jofs + q) * pitch + c], jofs + q < state_rows);
             }
         } else {
             for (int i = threadIdx.x; i < n; i += blockDim.x) {
                 const int q = i / nch, c = i - q * nch;
-                dst[c * ch_stride + q * col_stride] = from_tile<BD>(tile[(jofs + q) * pitch + c]);
+                dst[c * ch_stride + q * col_stride] = from_tile<BD>(tile[(jofs + q) * pitch + c], jofs + q < state_rows);
             }
         }
         return;
@@ -281,18 +286,18 @@ __global__ void __launch_bounds__(256) verify_generic(const __grid_constant__ Ve
         // history-row state: the snapshot row [full[1 .. W-2], x_0 .. x_{T-1}] replaces columns
         // [0, T+W-2) of the state row (every thread read its committed window before the barrier)
         BS *sb = reinterpret_cast<BS *>(p.state) + (long long)slot * p.st_slot + (long long)c0 * p.st_ch;
-        write_view<TT, BS>(tile, pitch, 1, T + R - 1, sb, p.st_ch, 1, nch);
+        write_view<TT, BS>(tile, pitch, 1, T + R - 1, sb, p.st_ch, 1, nch, R);
     } else {
         BS *wb = reinterpret_cast<BS *>(p.win) + (long long)s * p.w_seq;
         if (p.dedup) {
-            write_view<TT, BS>(tile, pitch, 1, T + R - 1, wb + (long long)c0 * p.w_ch, p.w_ch, p.w_col, nch);
+            write_view<TT, BS>(tile, pitch, 1, T + R - 1, wb + (long long)c0 * p.w_ch, p.w_ch, p.w_col, nch, R);
         } else {
             for (int t = 0; t < T; ++t)
                 write_view<TT, BS>(tile, pitch, t + 1, R, wb + t * p.w_step + (long long)c0 * p.w_ch, p.w_ch, p.w_col,
-                                   nch);
+                                   nch, R);
         }
         BS *sb = reinterpret_cast<BS *>(p.state) + (long long)slot * p.st_slot + (long long)c0 * p.st_ch;
-        write_view<TT, BS>(tile, pitch, T, R, sb, p.st_ch, 1, nch);
+        write_view<TT, BS>(tile, pitch, T, R, sb, p.st_ch, 1, nch, R);
     }
 
     // (5) conv + SiLU (+ L2 over the head_dim group) for every token, outputs stored as vectors

@@ -25,6 +25,11 @@
 // image.  Recompute rollback: outputs only; nothing is staged for storing and no bulk store runs.
 // State rows wider than the window (read at a state offset) are staged whole too; the committed
 // window then goes to their first W-1 columns by direct stores.
+// Mixed dtypes (S, the type of the state and the snapshots, differs from B, the type of x, out, taps
+// and bias): the stages and the images hold each part in its own type; state columns keep their
+// bits, x elements enter them widened exactly (bf16 -> fp32) or rounded to the nearest bf16, and
+// the conv takes every input at its own precision with each product rounded (fp32 state values
+// make the products inexact).
 // Preconditions (checked on the host): those of the fast path, packed 16-byte-aligned state rows
 // (state_ch_stride == state_cols; exactly T+W-2 columns for the history layout), T <= 17 (bf16) /
 // 8 (fp32), head_dim / CPT <= 32.
@@ -44,7 +49,7 @@ __host__ __device__ constexpr int pipe_align(int bytes) { return bytes % 16 == 0
 // Bytes of one stage for a block of bc channels (x rows, windows, taps, bias), each part 128-aligned.
 __host__ __device__ constexpr long long pipe_part(long long b) { return (b + 127) / 128 * 128; }
 
-template <typename B, int W, int TS, int CPT>
+template <typename B, int W, int TS, int CPT, typename S = B>
 __global__ void __launch_bounds__(128, (CPT == 4 && TS <= 8) ? 4 : 2) verify_pipe(const __grid_constant__ VerifyParams p) {
     grid_dep_wait();
     grid_dep_launch();
@@ -52,13 +57,16 @@ __global__ void __launch_bounds__(128, (CPT == 4 && TS <= 8) ? 4 : 2) verify_pip
     // (taps and bias are read from global memory, so W*CPT*ES need only be 8-byte aligned)
     constexpr int R = W - 1;
     constexpr int Q = TS + R - 1;  // dedup row columns
-    constexpr int ES = (int)sizeof(B);
+    constexpr bool MIXED = !std::is_same_v<B, S>;
+    constexpr int ES = (int)sizeof(B);   // x, out, taps, bias
+    constexpr int ESS = (int)sizeof(S);  // state, snapshots
     constexpr int EW = 4 / ES;
-    constexpr int NW = CPT / EW;
+    constexpr int NW = CPT / EW;          // words of CPT x elements
+    constexpr int NWS = CPT * ESS / 4;    // words of CPT state elements
     constexpr int VX = pipe_align(CPT * ES);
-    constexpr int VS = pipe_align(CPT * R * ES);
+    constexpr int VS = pipe_align(CPT * R * ESS);
     constexpr int VW = pipe_align(CPT * W * ES);
-    constexpr int VI = pipe_align(CPT * Q * ES);
+    constexpr int VI = pipe_align(CPT * Q * ESS);
     extern __shared__ __align__(128) unsigned char smem[];
 
     const int tid = threadIdx.x;
@@ -79,9 +87,9 @@ __global__ void __launch_bounds__(128, (CPT == 4 && TS <= 8) ? 4 : 2) verify_pip
     // 2 mbarriers, 2 unit slots, 2 unit state offsets, then (when compacting) 4 warp counts and the
     // list of active sequences
     const long long xb = pipe_part((long long)TS * BC * ES);
-    const long long stage_bytes = xb + pipe_part((long long)SC * BC * ES);
-    const long long rb = dense ? 0 : pipe_part((long long)Q * BC * ES);
-    const long long img_bytes = recomp ? 0 : rb + ((hist || wide) ? 0 : pipe_part((long long)R * BC * ES));
+    const long long stage_bytes = xb + pipe_part((long long)SC * BC * ESS);
+    const long long rb = dense ? 0 : pipe_part((long long)Q * BC * ESS);
+    const long long img_bytes = recomp ? 0 : rb + ((hist || wide) ? 0 : pipe_part((long long)R * BC * ESS));
     unsigned char *const img0 = smem + 2 * stage_bytes;
     uint64_t *const bar = reinterpret_cast<uint64_t *>(img0 + 2 * img_bytes);
     volatile int *const info = reinterpret_cast<volatile int *>(bar + 2);  // [0, 2): slots, [2, 4): offsets
@@ -167,10 +175,10 @@ __global__ void __launch_bounds__(128, (CPT == 4 && TS <= 8) ? 4 : 2) verify_pip
         if (go) {
             if (!x_sent) issue_x(k);
             // packed state rows of SC columns: the committed windows, or whole rows
-            mbar_expect_tx(&bar[st], (unsigned)(SC * nch * ES));
+            mbar_expect_tx(&bar[st], (unsigned)(SC * nch * ESS));
             bulk_load(smem + st * stage_bytes + xb,
-                      reinterpret_cast<const B *>(p.state) + (long long)slot * p.st_slot + (long long)c0 * SC,
-                      (unsigned)(nch * SC * ES), &bar[st]);
+                      reinterpret_cast<const S *>(p.state) + (long long)slot * p.st_slot + (long long)c0 * SC,
+                      (unsigned)(nch * SC * ESS), &bar[st]);
         }
         mbar_arrive(&bar[st]);
     };
@@ -187,6 +195,8 @@ __global__ void __launch_bounds__(128, (CPT == 4 && TS <= 8) ? 4 : 2) verify_pip
     }
 
     const int cl = tid * CPT;
+    // products rounded one by one unless they are exact (bf16 times bf16)
+    using CB = std::conditional_t<MIXED, uint32_t, B>;
     // unit u = blockIdx.x + k * gridDim.x as (sequence, channel block), stepped without divisions
     const int g_s = (int)gridDim.x / nblk, g_b = (int)gridDim.x - g_s * nblk;
     int q = (int)blockIdx.x / nblk, cb = (int)blockIdx.x - q * nblk;  // q: index into the sequence list
@@ -236,13 +246,13 @@ __global__ void __launch_bounds__(128, (CPT == 4 && TS <= 8) ? 4 : 2) verify_pip
 
         float fw[CPT][R + TS];  // inputs widened to fp32: [0, R) committed window, then x
         uint32_t xr[TS][NW];    // raw x rows
-        uint32_t sw[R * NW];    // raw committed window, channel-major [CPT][R]
+        uint32_t sw[R * NWS];   // raw committed window, channel-major [CPT][R]
         if (go && act) {
 #pragma unroll
             for (int t = 0; t < TS; ++t) ldv<VX, NW>(xr[t], stg + ((long long)t * BC + cl) * ES);
             if (whole_rows) {
                 // the committed window sits at columns [off, off+W-1) of each staged row
-                using U = std::conditional_t<ES == 2, unsigned short, unsigned>;
+                using U = std::conditional_t<ESS == 2, unsigned short, unsigned>;
                 const U *row = reinterpret_cast<const U *>(stg + xb) + (long long)cl * SC + off;
                 U v[CPT * R];
 #pragma unroll
@@ -250,21 +260,35 @@ __global__ void __launch_bounds__(128, (CPT == 4 && TS <= 8) ? 4 : 2) verify_pip
 #pragma unroll
                     for (int kk = 0; kk < R; ++kk) v[e * R + kk] = row[e * SC + kk];
 #pragma unroll
-                for (int i = 0; i < R * NW; ++i)
-                    sw[i] = ES == 2 ? ((uint32_t)v[2 * i] | ((uint32_t)v[(2 * i + 1) % (CPT * R)] << 16)) : (uint32_t)v[i];
+                for (int i = 0; i < R * NWS; ++i)
+                    sw[i] = ESS == 2 ? ((uint32_t)v[2 * i] | ((uint32_t)v[(2 * i + 1) % (CPT * R)] << 16)) : (uint32_t)v[i];
             } else {
-                ldv<VS, R * NW>(sw, stg + xb + (long long)cl * R * ES);
+                ldv<VS, R * NWS>(sw, stg + xb + (long long)cl * R * ESS);
             }
 #pragma unroll
             for (int e = 0; e < CPT; ++e)
 #pragma unroll
-                for (int kk = 0; kk < R; ++kk) fw[e][kk] = elem_f<B>(sw, e * R + kk);
+                for (int kk = 0; kk < R; ++kk) fw[e][kk] = elem_f<S>(sw, e * R + kk);
 
             // word and half holding input j of channel e (j < R: committed window, else x_{j-R})
             auto word_of = [&](int e, int j) -> uint32_t { return j < R ? sw[(e * R + j) / EW] : xr[j - R][e / EW]; };
             auto half_of = [&](int e, int j) -> int { return j < R ? (e * R + j) % EW : e % EW; };
-            // word i of a channel-major run of n columns starting at input j0
+            // raw bits of input j of channel e in the state's type (x elements converted)
+            auto elem_bits = [&](int e, int j) -> uint32_t {
+                if constexpr (MIXED)
+                    return j < R ? elem_raw<S>(sw, e * R + j) : convert_bits<B, S>(elem_raw<B>(xr[j - R], e));
+                else
+                    return ES == 2 ? (word_of(e, j) >> (16 * half_of(e, j))) & 0xffffu : word_of(e, j);
+            };
+            // word i (state type) of a channel-major run of n columns starting at input j0
             auto run_word = [&](int i, int n, int j0) -> uint32_t {
+                if constexpr (MIXED) {
+                    if constexpr (ESS == 2) {
+                        const int a = 2 * i, b = 2 * i + 1;
+                        return pack_halves(elem_bits(a / n, j0 + a % n), elem_bits(b / n, j0 + b % n));
+                    }
+                    return elem_bits(i / n, j0 + i % n);
+                }
                 if (ES == 2) {
                     const int a = 2 * i, b = 2 * i + 1;
                     return halves(word_of(a / n, j0 + a % n), half_of(a / n, j0 + a % n), word_of(b / n, j0 + b % n),
@@ -275,37 +299,33 @@ __global__ void __launch_bounds__(128, (CPT == 4 && TS <= 8) ? 4 : 2) verify_pip
             if (recomp) {
                 // outputs only: no snapshots, and the state keeps the pre-verify window
             } else if (!dense) {
-                uint32_t im[Q * NW];  // CPT channels x Q columns; column q holds input q+1
+                uint32_t im[Q * NWS];  // CPT channels x Q columns; column q holds input q+1
 #pragma unroll
-                for (int i = 0; i < Q * NW; ++i) im[i] = run_word(i, Q, 1);
-                stv<VI, Q * NW>(img + (long long)tid * CPT * Q * ES, im);
+                for (int i = 0; i < Q * NWS; ++i) im[i] = run_word(i, Q, 1);
+                stv<VI, Q * NWS>(img + (long long)tid * CPT * Q * ESS, im);
             } else {
-                B *wsq = reinterpret_cast<B *>(p.win) + (long long)s * p.w_seq + (long long)c * R;
+                S *wsq = reinterpret_cast<S *>(p.win) + (long long)s * p.w_seq + (long long)c * R;
 #pragma unroll
                 for (int t = 0; t < TS; ++t) {
-                    uint32_t w[R * NW];
+                    uint32_t w[R * NWS];
 #pragma unroll
-                    for (int i = 0; i < R * NW; ++i) w[i] = run_word(i, R, t + 1);
-                    stv<VS, R * NW>(wsq + (long long)t * p.w_step, w);
+                    for (int i = 0; i < R * NWS; ++i) w[i] = run_word(i, R, t + 1);
+                    stv<VS, R * NWS>(wsq + (long long)t * p.w_step, w);
                 }
             }
             if (wide && !recomp) {
                 // committed window -> columns [0, W-1) of the wide rows, stored directly (the rows'
                 // other columns are not this call's to rewrite); this thread alone owns them
-                B *srow = reinterpret_cast<B *>(p.state) + (long long)slot * p.st_slot + (long long)c * SC;
+                S *srow = reinterpret_cast<S *>(p.state) + (long long)slot * p.st_slot + (long long)c * SC;
 #pragma unroll
                 for (int e = 0; e < CPT; ++e)
 #pragma unroll
-                    for (int kk = 0; kk < R; ++kk) {
-                        const int j = TS + kk;  // input j of channel e
-                        srow[(long long)e * SC + kk] =
-                            (B)(ES == 2 ? (word_of(e, j) >> (16 * half_of(e, j))) & 0xffffu : word_of(e, j));
-                    }
+                    for (int kk = 0; kk < R; ++kk) srow[(long long)e * SC + kk] = (S)elem_bits(e, TS + kk);
             } else if (!hist && !recomp) {
-                uint32_t fin[R * NW];
+                uint32_t fin[R * NWS];
 #pragma unroll
-                for (int i = 0; i < R * NW; ++i) fin[i] = run_word(i, R, TS);
-                stv<VS, R * NW>(stimg + (long long)tid * CPT * R * ES, fin);
+                for (int i = 0; i < R * NWS; ++i) fin[i] = run_word(i, R, TS);
+                stv<VS, R * NWS>(stimg + (long long)tid * CPT * R * ESS, fin);
             }
         }
         fence_smem_to_async();
@@ -327,15 +347,15 @@ __global__ void __launch_bounds__(128, (CPT == 4 && TS <= 8) ? 4 : 2) verify_pip
             if (go && !recomp) {
                 if (hist) {
                     // the row image replaces columns [0, T+W-2) of the (packed) history rows
-                    bulk_store(reinterpret_cast<B *>(p.state) + (long long)slot * p.st_slot + (long long)c0 * Q, img,
-                               (unsigned)(nch * Q * ES));
+                    bulk_store(reinterpret_cast<S *>(p.state) + (long long)slot * p.st_slot + (long long)c0 * Q, img,
+                               (unsigned)(nch * Q * ESS));
                 } else {
                     if (!dense)
-                        bulk_store(reinterpret_cast<B *>(p.win) + (long long)s * p.w_seq + (long long)c0 * Q, img,
-                                   (unsigned)(nch * Q * ES));
+                        bulk_store(reinterpret_cast<S *>(p.win) + (long long)s * p.w_seq + (long long)c0 * Q, img,
+                                   (unsigned)(nch * Q * ESS));
                     if (!wide)
-                        bulk_store(reinterpret_cast<B *>(p.state) + (long long)slot * p.st_slot + (long long)c0 * R,
-                                   stimg, (unsigned)(nch * R * ES));
+                        bulk_store(reinterpret_cast<S *>(p.state) + (long long)slot * p.st_slot + (long long)c0 * R,
+                                   stimg, (unsigned)(nch * R * ESS));
                 }
                 asm volatile("cp.async.bulk.commit_group;\n" ::: "memory");
             }
@@ -357,7 +377,7 @@ __global__ void __launch_bounds__(128, (CPT == 4 && TS <= 8) ? 4 : 2) verify_pip
                     for (int e = 0; e < CPT; ++e) fw[e][R + t] = elem_f<B>(xr[t], e);
 #pragma unroll
                     for (int e = 0; e < CPT; ++e) {
-                        const float acc = conv_chain<B, W>(bs[e], wt[e], &fw[e][t]);
+                        const float acc = conv_chain<CB, W>(bs[e], wt[e], &fw[e][t]);
                         y[t][e] = silu_fast(acc);
                         lo = fminf(lo, acc);
                     }
@@ -367,7 +387,7 @@ __global__ void __launch_bounds__(128, (CPT == 4 && TS <= 8) ? 4 : 2) verify_pip
                     for (int t = 0; t < TS; ++t)
 #pragma unroll
                         for (int e = 0; e < CPT; ++e) {
-                            y[t][e] = silu_exact(conv_chain<B, W>(bs[e], wt[e], &fw[e][t]));
+                            y[t][e] = silu_exact(conv_chain<CB, W>(bs[e], wt[e], &fw[e][t]));
                         }
                 }
             } else {

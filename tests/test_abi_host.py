@@ -128,7 +128,7 @@ def test_history_validation_and_paths(lib):
     ("n1_t2_dim512_w4_f32_dense", 3), ("n4_t4_dim4096_w4_bf16_dedup_bias", 3),
     ("n8_t17_dim8192_w4_bf16_dense_qkvsplit_xstride12288", 3), ("n64_t8_dim6144_w3_bf16_dense_nol2_stateoff", 1),
     ("n128_t8_dim10240_w4_bf16_history_pad13", 3), ("n128_t8_dim10240_w4_bf16_recompute_pad13", 3),
-    ("n128_t8_dim10240_w4_bf16_tree_dense_pad13", 5), ("n128_t8_dim10240_w4_bf16x_f32state_dedup_pad13", 0)])
+    ("n128_t8_dim10240_w4_bf16_tree_dense_pad13", 5), ("n128_t8_dim10240_w4_bf16x_f32state_dedup_pad13", 3)])
 def test_plan_paths_of_named_workloads(lib, name, path):
     w = wl.WORKLOADS[name]
     rc, pl = _plan(lib, _args(w))
@@ -318,19 +318,32 @@ def test_prefill_aliasing_and_empty(lib):
 
 
 def test_mixed_dtypes_plan_and_validation(lib):
-    """bf16 x with an fp32 state (and the reverse) plan the general kernel with an fp32 tile;
-    unknown state dtypes are rejected."""
+    """bf16 x with an fp32 state (and the reverse) plan the pipelined kernel for T <= 8, its stage
+    and image parts sized in each part's own dtype, and the general kernel with an fp32 tile above
+    that; unknown state dtypes are rejected."""
+    part = lambda b: (b + 127) // 128 * 128
     w = W3.replace(state_dtype="f32", n_seq=4, n_pad=0, extra_slots=0)
     a = _args(w)
     assert a.state_dtype == 1  # CV_STATE_F32
     rc, pl = _plan(lib, a)
-    assert rc == 0 and pl.path == 0
-    assert pl.smem_bytes == (8 + 3) * (8 * pl.threads + 4) * 4
+    assert rc == 0 and pl.path == 3 and pl.stages == 2
+    bc = pl.channels_per_block
+    stage = part(8 * bc * 2) + part(3 * bc * 4)  # bf16 x rows, fp32 committed windows
+    image = part(10 * bc * 4) + part(3 * bc * 4)  # fp32 dedup row, fp32 committed window
+    assert pl.smem_bytes == _pipe_smem(stage, image, 4)
     a.state_dtype = 3
     assert _plan(lib, a)[0] == -6
     w2 = W3.replace(dtype="f32", state_dtype="bf16", n_seq=4, n_pad=0, extra_slots=0)
     a2 = _args(w2)
-    assert a2.state_dtype == 2 and _plan(lib, a2)[1].path == 0
+    rc, pl2 = _plan(lib, a2)
+    assert a2.state_dtype == 2 and rc == 0 and pl2.path == 3
+    bc = pl2.channels_per_block
+    assert pl2.smem_bytes == _pipe_smem(part(8 * bc * 4) + part(3 * bc * 2), part(10 * bc * 2) + part(3 * bc * 2), 4)
+    # T = 9: no mixed pipelined kernel; the general kernel's tile holds fp32 bits
+    w3 = W3.replace(state_dtype="f32", T=9, n_seq=4, n_pad=0, extra_slots=0)
+    rc, pl3 = _plan(lib, _args(w3))
+    assert rc == 0 and pl3.path == 0
+    assert pl3.smem_bytes == (9 + 3) * (8 * pl3.threads + 4) * 4
 
 
 def test_tree_plan_and_validation(lib):

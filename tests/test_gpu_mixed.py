@@ -64,3 +64,51 @@ def test_mixed_nan_and_rounding(cuda_lib):
     x[0, 3, 7] = torch.tensor(0x3f808000, dtype=torch.int32).view(torch.float32)  # a tie: rounds to even
     x[1, 3, 9] = -0.0
     check(cuda_lib, w, inp, commit=False)
+
+
+def _plan_path(cv, w, inp):
+    d = {k: (v.to("cuda") if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    return cv.verify_plan(d["x"], d["conv_state"], d["weight"], d["bias"], d["out"], d["window"], layout=w.layout,
+                          qk_channels=w.qk_channels, head_dim=w.head_dim, cache_idx=d["cache_idx"],
+                          state_off=d["state_off"]).path
+
+
+@pytest.mark.parametrize("case", range(16))
+def test_mixed_pipelined_sweep(cuda_lib, case):
+    """Packed buffers with T <= 8 take the pipelined kernel in both directions and every layout:
+    W 2..4, dims that leave a ragged last channel block, L2 groups of 8..128, bias, padded
+    sequences, unused pool slots, wide state rows read at offsets (dense and dedup) and history
+    rows."""
+    rng = np.random.default_rng(12000 + case)
+    xd = "bf16" if case % 2 == 0 else "f32"
+    sd = "f32" if xd == "bf16" else "bf16"
+    layout = ["dense", "dedup", "history", "recompute"][(case // 2) % 4]
+    T = int(rng.integers(1, 9))
+    width = int(rng.integers(2, 5))
+    hd = int(rng.choice([8, 32, 64, 128]))
+    qk = int(rng.integers(0, 4)) * hd
+    dim = qk + 8 * int(rng.integers(1, 200))
+    w = wl.VerifyWorkload("mixpipe", n_seq=int(rng.integers(2, 40)), T=T, dim=dim, width=width, qk_channels=qk,
+                          head_dim=hd, dtype=xd, state_dtype=sd, layout=layout, bias=bool(case % 3),
+                          n_pad=1, extra_slots=2, state_offset=layout == "history" or (case % 8 >= 4 and T > 1),
+                          seed=700 + case)
+    inp = wl.make_inputs(w)
+    assert _plan_path(cuda_lib, w, inp) == 3
+    check(cuda_lib, w, inp)
+
+
+@pytest.mark.parametrize("T", [4, 9])
+def test_mixed_state_nan_payloads_kept(cuda_lib, T):
+    """A bf16 state holding NaNs with payloads, read with fp32 x: state columns move as raw bits
+    (snapshots and the committed window keep each payload) while x enters as rounded bf16; on the
+    pipelined kernel (T = 4) and the general one (T = 9)."""
+    w = wl.VerifyWorkload("mixstnan", n_seq=3, T=T, dim=256, width=4, qk_channels=128, head_dim=64, dtype="f32",
+                          state_dtype="bf16", layout="dedup", bias=True, seed=9 + T)
+    inp = wl.make_inputs(w)
+    st = inp["conv_state"].view(torch.int16)
+    slots = inp["cache_idx"].tolist()
+    st[slots[0], 5, 2] = 0x7fa1
+    st[slots[1], 17, 1] = -1  # 0xffff: a negative quiet NaN with a full payload
+    st[slots[2], 200, 0] = 0x7f81
+    assert _plan_path(cuda_lib, w, inp) == (3 if T <= 8 else 0)
+    check(cuda_lib, w, inp)
