@@ -304,7 +304,8 @@ CV_API int cv_conv_prefill(const cv_prefill_args *args, void *stream);
  * compile-time constant; grid_y = 1 and each block walks (sequence, channel block) units),
  * 1 = packed buffers with T a compile-time constant (T <= 17 for bf16, <= 8 for fp32),
  * 2 = packed buffers, dense window, larger T in chunks of 8 tokens, 0 = the general kernel (any
- * strides).  Host pointer `plan` must not be NULL.  Returns the same status
+ * strides), 5 = tree verify (parent given; a one-warp block of 256 channels stages its committed
+ * windows, x rows and parents in smem_bytes of shared memory and walks the tokens).  Host pointer `plan` must not be NULL.  Returns the same status
  * cv_conv_verify would return before launching.
  */
 typedef struct cv_launch_plan {

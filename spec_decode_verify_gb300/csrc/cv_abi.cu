@@ -31,7 +31,6 @@ constexpr int kSmemPerSM = 232448;       // usable shared memory per SM
 constexpr int kSmemPerBlockReserved = 1024;
 constexpr int kMinThreads = 32;
 constexpr int kGenericSmemBudget = 96 * 1024;
-constexpr long long kTreeSmemBudget = 64 * 1024;  // tree verify: token windows kept per block
 constexpr int kCommitThreads = 128;
 constexpr int kCommitRowThreads = 64;  // dedup commit: 512 channels per block
 constexpr int kSmemMax = 227 * 1024;
@@ -159,14 +158,16 @@ int plan_verify(const cv_verify_args *a, cv_launch_plan *pl) {
     const int R = a->width - 1;
     std::memset(pl, 0, sizeof *pl);
     if (a->parent) {
-        // tree verify: its own kernel, 8 channels per thread, one block per (channel block, sequence)
-        int threads = 128;
-        while (threads > kMinThreads && 8 * (threads / 2) >= a->dim) threads /= 2;
-        // the block's token windows in shared memory when they fit in kTreeSmemBudget
-        const long long kept = (long long)a->T * R * 8 * threads * esize;
-        pl->threads = threads;
-        pl->channels_per_block = 8 * threads;
-        pl->smem_bytes = kept <= kTreeSmemBudget ? (int)kept : 0;
+        // tree verify: its own kernel, one warp per (kTreeChannels channels, sequence) walking the
+        // tokens (more resident blocks beat more warps per block: each block's latency chain is
+        // fixed); the block stages its committed windows and x rows ((W-1+T) rows of
+        // kTreeChannels elements) and the T parents in shared memory
+        const int warps = 1;
+        const long long staged = (long long)(R + a->T) * cvk::kTreeChannels * esize + 4LL * a->T;
+        if (staged > kSmemMax) return CV_ERR_SMEM;
+        pl->threads = 32 * warps;
+        pl->channels_per_block = cvk::kTreeChannels;
+        pl->smem_bytes = (int)staged;
         pl->path = 5;
         pl->grid_x = (a->dim + pl->channels_per_block - 1) / pl->channels_per_block;
         pl->grid_y = a->n_seq;
@@ -352,11 +353,13 @@ int launch_verify(const cv_verify_args *a, const cv_launch_plan &pl, cudaStream_
     p.w_vec = aligned16(a->weight);
     p.b_vec = a->bias ? aligned16(a->bias) : 0;
     if (pl.path == 5) {
-        // tree verify: pitch != 0 -> token windows in shared memory; st_vec -> packed 16-byte dense
-        // snapshot runs of 8 channels x (W-1) columns
-        p.pitch = pl.smem_bytes > 0 ? 1 : 0;
+        // tree verify: st_vec -> packed 16-byte dense snapshot runs of 8 channels x (W-1) columns;
+        // st_packed -> the committed windows read as 16-byte runs
+        p.pitch = 0;
         p.st_vec = a->dim % 8 == 0 && aligned16(a->window) && a->win_ch_stride == a->width - 1 &&
                    a->win_col_stride == 1 && stride16(a->win_seq_stride, esize) && stride16(a->win_step_stride, esize);
+        p.st_packed = aligned16(a->conv_state) && stride16(a->state_slot_stride, esize) &&
+                      a->state_ch_stride == a->width - 1 && a->state_cols == a->width - 1;
     }
 
     const cvk::KernelSet &ks = kernel_set(a->dtype, a->width);

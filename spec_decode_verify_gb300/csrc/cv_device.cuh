@@ -32,7 +32,11 @@ struct VerifyParams {
     int recomp;   // recompute rollback: outputs only (no snapshots, state not written)
     const int *parent;  // tree verify: [n_seq][T] parent of each draft token, or null (a chain)
     int x_vec, out_vec, st_vec, w_vec, b_vec;  // 16-byte vector access allowed (checked on the host)
+    int st_packed;  // tree verify: the committed windows are packed, 16-byte-aligned [dim][W-1] rows
 };
+
+// Tree verify: channels per block, 8 per lane of a warp.
+constexpr int kTreeChannels = 256;
 
 struct CommitParams {
     void *state;

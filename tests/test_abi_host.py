@@ -356,10 +356,22 @@ def test_tree_plan_and_validation(lib):
                             layout="dense", qk_channels=w.qk_channels, head_dim=w.head_dim,
                             cache_idx=inp["cache_idx"], parent=parent, check_device=False)
     rc, pl = _plan(lib, a)
-    assert rc == 0 and pl.path == 5 and (pl.threads, pl.grid_x, pl.grid_y) == (128, 8, 8)
+    # blocks of 256 channels, one warp walking the tokens
+    assert rc == 0 and pl.path == 5 and (pl.threads, pl.grid_x, pl.grid_y) == (32, 32, 8)
+    assert pl.channels_per_block == 256
+    # staged: (W-1+T) rows of 256 bf16, then T int32 parents
+    assert pl.smem_bytes == (3 + 17) * 256 * 2 + 4 * 17
     a.window_layout = 2
     a.win_step_stride = a.win_col_stride
     assert _plan(lib, a)[0] == -8
     a = _args(W3.replace(state_dtype="f32", layout="dense", n_seq=2, n_pad=0, extra_slots=0))
     a.parent = parent.data_ptr()
     assert _plan(lib, a)[0] == -6
+    # 128 fp32 tokens: 131 staged rows of 1 KB
+    w = W3.replace(dtype="f32", layout="dense", T=128, n_seq=2, n_pad=0, extra_slots=0)
+    a = _args(w)
+    big = torch.arange(-1, 127, dtype=torch.int32).repeat(2, 1).contiguous()
+    a.parent = big.data_ptr()
+    rc, pl = _plan(lib, a)
+    assert rc == 0 and pl.path == 5 and pl.threads == 32 and pl.smem_bytes == (3 + 128) * 256 * 4 + 4 * 128
+    assert pl.grid_x == 10240 // 256

@@ -86,3 +86,29 @@ def test_tree_invalid_parents_flagged_on_gpu(cuda_lib):
     assert got["err"].cpu().tolist() == [0, 32, 32]
     assert_bits_equal(got["conv_state"].cpu(), ref["conv_state"], "state")
     assert_bits_equal(got["window"].cpu(), ref["window"], "window")
+
+
+@pytest.mark.parametrize("dtype,T,width", [("f32", 128, 4), ("bf16", 100, 3), ("f32", 33, 2)])
+def test_tree_long_drafts(cuda_lib, dtype, T, width):
+    """Long drafts: the staged rows outgrow the shared-memory budget and the block shrinks (to 32
+    threads for 128 fp32 tokens); deep random trees, padded rows, a ragged last channel block."""
+    rng = np.random.default_rng(T + width)
+    w = wl.VerifyWorkload("treelong", n_seq=3, T=T, dim=1096, width=width, qk_channels=512, head_dim=64,
+                          dtype=dtype, layout="dense", bias=True, n_pad=1, extra_slots=2, seed=T)
+    inp = wl.make_inputs(w)
+    inp["parent"] = random_parents(rng, w.n_seq, w.T)
+    check(cuda_lib, w, inp)
+
+
+def test_tree_root_heavy_and_deep(cuda_lib):
+    """Every token a child of the committed window (each window reaches into it), and a single
+    deep path, in one batch on the packed-state fast loads."""
+    T = 8
+    w = wl.VerifyWorkload("treeshape", n_seq=2, T=T, dim=2048, width=4, qk_channels=1024, head_dim=128,
+                          dtype="bf16", layout="dense", seed=29)
+    inp = wl.make_inputs(w)
+    p = torch.full((2, T), -1, dtype=torch.int32)
+    p[1] = torch.arange(-1, T - 1, dtype=torch.int32)
+    p[1, 4] = 1  # a branch off the path
+    inp["parent"] = p
+    check(cuda_lib, w, inp)
