@@ -304,13 +304,14 @@ CV_API int cv_conv_prefill(const cv_prefill_args *args, void *stream);
  * compile-time constant; grid_y = 1 and each block walks (sequence, channel block) units),
  * 1 = packed buffers with T a compile-time constant (T <= 17 for bf16, <= 8 for fp32),
  * 2 = packed buffers, dense window, larger T in chunks of 8 tokens, 0 = the general kernel (any
- * strides), 5 = tree verify (parent given; a one-warp block of 256 channels stages its committed
- * windows, x rows and parents in smem_bytes of shared memory and walks the tokens).  Host pointer `plan` must not be NULL.  Returns the same status
+ * strides), 5 = tree verify (parent given; persistent one-warp blocks walk (sequence, 256
+ * channels) units, staging each unit's committed windows, x rows and parents in one of `stages`
+ * shared-memory buffers; grid_y = 1).  Host pointer `plan` must not be NULL.  Returns the same status
  * cv_conv_verify would return before launching.
  */
 typedef struct cv_launch_plan {
     int32_t grid_x, grid_y, threads, smem_bytes, channels_per_block, path;
-    int32_t stages; /* path 3: units whose loads are in flight per block (2); 0 otherwise */
+    int32_t stages; /* paths 3 and 5: unit buffers per block (loads in flight); 0 otherwise */
 } cv_launch_plan;
 
 CV_API int cv_verify_plan(const cv_verify_args *args, cv_launch_plan *plan);

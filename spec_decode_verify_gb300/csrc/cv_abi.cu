@@ -19,6 +19,7 @@
 
 #include "convverify.h"
 #include "cv_launch.h"
+#include "cv_verify_tree.cuh"  // tree_buffer_bytes
 
 namespace {
 
@@ -31,6 +32,8 @@ constexpr int kSmemPerSM = 232448;       // usable shared memory per SM
 constexpr int kSmemPerBlockReserved = 1024;
 constexpr int kMinThreads = 32;
 constexpr int kGenericSmemBudget = 96 * 1024;
+constexpr int kTreeWarps = 2;         // tree verify: warps per block (tokens split among them)
+constexpr int kTreeBlocksPerSM = 10;  // tree verify: resident blocks per SM at most
 constexpr int kCommitThreads = 128;
 constexpr int kCommitRowThreads = 64;  // dedup commit: 512 channels per block
 constexpr int kSmemMax = 227 * 1024;
@@ -158,19 +161,28 @@ int plan_verify(const cv_verify_args *a, cv_launch_plan *pl) {
     const int R = a->width - 1;
     std::memset(pl, 0, sizeof *pl);
     if (a->parent) {
-        // tree verify: its own kernel, one warp per (kTreeChannels channels, sequence) walking the
-        // tokens (more resident blocks beat more warps per block: each block's latency chain is
-        // fixed); the block stages its committed windows and x rows ((W-1+T) rows of
-        // kTreeChannels elements) and the T parents in shared memory
-        const int warps = 1;
-        const long long staged = (long long)(R + a->T) * cvk::kTreeChannels * esize + 4LL * a->T;
-        if (staged > kSmemMax) return CV_ERR_SMEM;
-        pl->threads = 32 * warps;
+        // tree verify: its own persistent kernel of kTreeWarps-warp blocks walking (sequence,
+        // kTreeChannels channels) units; two unit buffers (the next unit loads while this one
+        // computes) when they fit, else one; a grid of kTreeBlocksPerSM blocks per SM at most (as
+        // shared memory allows), a multiple of the channel-block count so that a block keeps its taps
+        const long long buf = cvk::tree_buffer_bytes(a->T, a->width, esize);
+        const int nbuf = 2 * buf <= kSmemMax ? 2 : 1;
+        if (buf > kSmemMax) return CV_ERR_SMEM;
+        int per_sm = (int)(kSmemPerSM / (nbuf * buf + kSmemPerBlockReserved));
+        if (per_sm > kTreeBlocksPerSM) per_sm = kTreeBlocksPerSM;
+        if (per_sm < 1) per_sm = 1;
+        const long long nblk = (a->dim + cvk::kTreeChannels - 1) / cvk::kTreeChannels;
+        const long long units = (long long)a->n_seq * nblk;
+        long long g = (long long)kNumSMs * per_sm;
+        if (g >= nblk) g = g / nblk * nblk;
+        if (g > units) g = units;
+        pl->threads = 32 * (a->T < kTreeWarps ? a->T : kTreeWarps);
         pl->channels_per_block = cvk::kTreeChannels;
-        pl->smem_bytes = (int)staged;
+        pl->smem_bytes = (int)(nbuf * buf);
+        pl->stages = nbuf;
         pl->path = 5;
-        pl->grid_x = (a->dim + pl->channels_per_block - 1) / pl->channels_per_block;
-        pl->grid_y = a->n_seq;
+        pl->grid_x = (int)(g > 0 ? g : 1);
+        pl->grid_y = 1;
         return CV_OK;
     }
     const int min_threads =
@@ -353,9 +365,9 @@ int launch_verify(const cv_verify_args *a, const cv_launch_plan &pl, cudaStream_
     p.w_vec = aligned16(a->weight);
     p.b_vec = a->bias ? aligned16(a->bias) : 0;
     if (pl.path == 5) {
-        // tree verify: st_vec -> packed 16-byte dense snapshot runs of 8 channels x (W-1) columns;
-        // st_packed -> the committed windows read as 16-byte runs
-        p.pitch = 0;
+        // tree verify: pitch = unit buffers (1 or 2); st_vec -> packed 16-byte dense snapshot runs of
+        // 8 channels x (W-1) columns; st_packed -> the committed windows read as 16-byte runs
+        p.pitch = pl.stages;
         p.st_vec = a->dim % 8 == 0 && aligned16(a->window) && a->win_ch_stride == a->width - 1 &&
                    a->win_col_stride == 1 && stride16(a->win_seq_stride, esize) && stride16(a->win_step_stride, esize);
         p.st_packed = aligned16(a->conv_state) && stride16(a->state_slot_stride, esize) &&

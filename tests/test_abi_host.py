@@ -134,7 +134,7 @@ def test_plan_paths_of_named_workloads(lib, name, path):
     rc, pl = _plan(lib, _args(w))
     assert rc == 0 and pl.path == path
     units = w.n_seq * -(-w.dim // pl.channels_per_block)
-    if path == 3:
+    if path in (3, 5):  # persistent grids
         assert pl.grid_y == 1 and 1 <= pl.grid_x <= units
     else:
         assert pl.grid_y == w.n_seq and pl.grid_x * pl.channels_per_block >= w.dim
@@ -356,22 +356,36 @@ def test_tree_plan_and_validation(lib):
                             layout="dense", qk_channels=w.qk_channels, head_dim=w.head_dim,
                             cache_idx=inp["cache_idx"], parent=parent, check_device=False)
     rc, pl = _plan(lib, a)
-    # blocks of 256 channels, one warp walking the tokens
-    assert rc == 0 and pl.path == 5 and (pl.threads, pl.grid_x, pl.grid_y) == (32, 32, 8)
-    assert pl.channels_per_block == 256
-    # staged: (W-1+T) rows of 256 bf16, then T int32 parents
-    assert pl.smem_bytes == (3 + 17) * 256 * 2 + 4 * 17
+    # persistent two-warp blocks over (sequence, 256 channels) units, two unit buffers of
+    # (W-1+T) rows of 256 bf16 + the packed [256][W-1] window run + T int32 parents (16-byte rounded)
+    buf = (3 + 17) * 256 * 2 + 256 * 3 * 2 + 80
+    assert rc == 0 and pl.path == 5 and pl.threads == 64 and pl.channels_per_block == 256
+    assert pl.smem_bytes == 2 * buf and pl.stages == 2
+    # 9 blocks per SM fit (232448 // (2 * buf + 1024)); 8 x 32 = 256 units bound the grid
+    assert (pl.grid_x, pl.grid_y) == (256, 1)
     a.window_layout = 2
     a.win_step_stride = a.win_col_stride
     assert _plan(lib, a)[0] == -8
     a = _args(W3.replace(state_dtype="f32", layout="dense", n_seq=2, n_pad=0, extra_slots=0))
     a.parent = parent.data_ptr()
     assert _plan(lib, a)[0] == -6
-    # 128 fp32 tokens: 131 staged rows of 1 KB
+    # 128 fp32 tokens: two buffers of 131 staged rows of 1 KB do not fit, one does
     w = W3.replace(dtype="f32", layout="dense", T=128, n_seq=2, n_pad=0, extra_slots=0)
     a = _args(w)
     big = torch.arange(-1, 127, dtype=torch.int32).repeat(2, 1).contiguous()
     a.parent = big.data_ptr()
     rc, pl = _plan(lib, a)
-    assert rc == 0 and pl.path == 5 and pl.threads == 32 and pl.smem_bytes == (3 + 128) * 256 * 4 + 4 * 128
-    assert pl.grid_x == 10240 // 256
+    assert rc == 0 and pl.path == 5 and pl.threads == 64 and pl.stages == 1
+    assert pl.smem_bytes == (3 + 128) * 256 * 4 + 256 * 3 * 4 + 512
+    assert pl.grid_x == 2 * 10240 // 256  # one block per SM would be 152 > the 80 units
+    # the benchmark shape: 10 blocks per SM, a multiple of the 40 channel blocks
+    a = _args(W3.replace(layout="dense"))
+    par8 = torch.arange(-1, 7, dtype=torch.int32).repeat(W3.n_seq, 1).contiguous()
+    a.parent = par8.data_ptr()
+    rc, pl = _plan(lib, a)
+    buf = (3 + 8) * 256 * 2 + 256 * 3 * 2 + 32
+    per_sm = min(10, 232448 // (2 * buf + 1024))
+    assert rc == 0 and pl.smem_bytes == 2 * buf and pl.grid_x == 152 * per_sm // 40 * 40 == 1520
+    # one draft token: one warp
+    a.T = 1
+    assert _plan(lib, a)[1].threads == 32
