@@ -40,11 +40,16 @@ METRIC = "verify-conv µs/step and achieved HBM GB/s (% of GB300 peak), 1 GPU"
 UNIT = "us/step"
 HBM_NOMINAL_GBS = 8000.0  # the metric's roofline: bytes moved / 8 TB/s
 PROFILES = os.path.join(ROOT, "profiles")
-# the sources of the kernel each kind of workload runs (verify: the pipelined path)
+# the sources of each main kernel (verify: the pipelined path), keyed as in profiles' traffic lines
+_CSRC = os.path.join(ROOT, "spec_decode_verify_gb300", "csrc")
 KERNEL_SRCS = {
-    "verify": [os.path.join(ROOT, "spec_decode_verify_gb300", "csrc", f) for f in ("cv_verify_pipe.cuh", "cv_device.cuh")],
-    "prefill": [os.path.join(ROOT, "spec_decode_verify_gb300", "csrc", f) for f in ("cv_prefill.cuh", "cv_device.cuh")],
+    kind: [os.path.join(_CSRC, f) for f in (src, "cv_device.cuh")]
+    for kind, src in (("verify", "cv_verify_pipe.cuh"), ("prefill", "cv_prefill.cuh"), ("fast", "cv_verify_fast.cuh"),
+                      ("generic", "cv_verify_generic.cuh"), ("tree", "cv_verify_tree.cuh"))
 }
+# launch path of cv_verify_plan -> (kernel, source kind)
+PATH_KERNELS = {0: ("verify_generic", "generic"), 1: ("verify_fast", "fast"), 2: ("verify_fast", "fast"),
+                3: ("verify_pipe", "verify"), 5: ("verify_tree", "tree")}
 
 
 def kernel_sha(kind: str = "verify") -> str:
@@ -325,6 +330,10 @@ def run_ours(args, w, world, rank, local, dist):
         sets.append(s)
     verify_fn, lib_commit = lib.cv_conv_verify, lib.cv_conv_commit
     vrefs = [ctypes.byref(s["va"]) for s in sets]
+    plan = cv.LaunchPlan()
+    if lib.cv_verify_plan(vrefs[0], ctypes.byref(plan)) != 0:
+        raise RuntimeError("cv_verify_plan rejected the workload")
+    kernel_name, kernel_kind = PATH_KERNELS[plan.path]
     crefs = [ctypes.byref(s["ca"]) if has_commit else None for s in sets]
 
     def commit_fn(ref, stream_ptr):
@@ -403,7 +412,7 @@ def run_ours(args, w, world, rank, local, dist):
     nbytes = wl.algorithmic_bytes(w)
     peak, peak_kind = measured_peak()
     achieved = nbytes["verify"] / (verify_us_max * 1e-6) / 1e9
-    traffic, traffic_src = profile_traffic(w.name)
+    traffic, traffic_src = profile_traffic(w.name, kernel_kind)
     line = {
         "metric": METRIC, "value": round(step_us_max, 3), "unit": UNIT, "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": round(step_us_max / 1e3, 6), "higher_is_better": False,
@@ -414,7 +423,7 @@ def run_ours(args, w, world, rank, local, dist):
         "verify_algorithmic_bytes": nbytes["verify"], "commit_algorithmic_bytes": nbytes["commit"],
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic,
-                     "kernel": "verify_pipe", "peak_source": f"{peak_kind} hbm_gbs (copy)",
+                     "kernel": kernel_name, "peak_source": f"{peak_kind} hbm_gbs (copy)",
                      "traffic_source": traffic_src},
         "gpu_launches": (2 if has_commit else 1) * K,
         "clocks": clocks,
