@@ -112,3 +112,21 @@ def test_mixed_state_nan_payloads_kept(cuda_lib, T):
     st[slots[2], 200, 0] = 0x7f81
     assert _plan_path(cuda_lib, w, inp) == (3 if T <= 8 else 0)
     check(cuda_lib, w, inp)
+
+
+@pytest.mark.parametrize("xd,layout,T", [("bf16", "dedup", 8), ("f32", "dense", 5), ("bf16", "history", 3),
+                                         ("f32", "recompute", 7), ("bf16", "dense", 1)])
+def test_mixed_pipelined_head_dim_256(cuda_lib, xd, layout, T):
+    """L2 groups of 256 channels: the pipelined kernel with 8 channels per thread, in both
+    directions, with a ragged last channel block, padded sequences and a bias."""
+    sd = "f32" if xd == "bf16" else "bf16"
+    w = wl.VerifyWorkload("mix256", n_seq=9, T=T, dim=512 + 1024 + 40, width=4, qk_channels=1024, head_dim=256,
+                          dtype=xd, state_dtype=sd, layout=layout, bias=True, n_pad=2, extra_slots=3,
+                          state_offset=layout == "history", seed=T)
+    inp = wl.make_inputs(w)
+    d = {k: (v.to("cuda") if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    pl = cuda_lib.verify_plan(d["x"], d["conv_state"], d["weight"], d["bias"], d["out"], d["window"], layout=layout,
+                              qk_channels=w.qk_channels, head_dim=w.head_dim, cache_idx=d["cache_idx"],
+                              state_off=d["state_off"])
+    assert pl.path == 3 and pl.channels_per_block == 8 * pl.threads
+    check(cuda_lib, w, inp)
