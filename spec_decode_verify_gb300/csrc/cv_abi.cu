@@ -34,8 +34,14 @@ constexpr int kMinThreads = 32;
 constexpr int kGenericSmemBudget = 96 * 1024;
 constexpr int kTreeWarps = 2;         // tree verify: warps per block (tokens split among them)
 constexpr int kTreeBlocksPerSM = 10;  // tree verify: resident blocks per SM at most
-constexpr int kCommitThreads = 128;
-constexpr int kCommitRowThreads = 64;  // dedup commit: 512 channels per block
+// commit block sizes per mode (measured on the steps they end): small blocks start beside the
+// verify's resident blocks while it drains
+constexpr int kCommitDenseThreads = 64;      // packed dense snapshot -> packed state (16-byte copies)
+constexpr int kCommitElementThreads = 32;    // element by element
+constexpr int kCommitRecomputeThreads = 64;  // recompute rollback
+// dedup commit: 256 channels per block (small blocks fit beside the verify's resident blocks, so
+// more of them start, under programmatic dependent launch, while the verify drains)
+constexpr int kCommitRowThreads = 32;
 constexpr int kSmemMax = 227 * 1024;
 // the pipelined kernel lists the active sequences in shared memory up to this batch size
 constexpr int kCompactMaxSeq = 1024;
@@ -441,7 +447,7 @@ int launch_commit(const cv_commit_args *a, cudaStream_t stream) {
         const bool vec = a->dim % 8 == 0 &&
                          state_packed(a->conv_state, a->state_slot_stride, a->state_ch_stride, a->width, esize) &&
                          aligned16(a->x) && stride16(a->x_seq_stride, esize) && stride16(a->x_tok_stride, esize);
-        const int threads = kCommitThreads;
+        const int threads = kCommitRecomputeThreads;
         const int per_block = vec ? 8 * threads : threads;
         auto kr = vec ? kernel_set(a->dtype, a->width).commit_recompute_vec : kernel_set(a->dtype, a->width).commit_recompute;
         if (launch_pdl(kr, dim3((a->dim + per_block - 1) / per_block, a->n_seq), threads, 0, stream, p) != cudaSuccess)
@@ -452,14 +458,12 @@ int launch_commit(const cv_commit_args *a, cudaStream_t stream) {
     const bool packed_state = state_packed(a->conv_state, a->state_slot_stride, a->state_ch_stride, a->width, esize);
     const bool win_ok = a->dim % 8 == 0 && aligned16(a->window) && stride16(a->win_seq_stride, esize) &&
                         a->win_col_stride == 1;
-    int threads = kCommitThreads;
-    while (threads > kMinThreads && 8 * (threads / 2) >= a->dim) threads /= 2;
     int smem = 0;
     if (packed_state && win_ok && a->window_layout == CV_WINDOW_DENSE && a->win_ch_stride == R &&
         stride16(a->win_step_stride, esize)) {
         p.mode = 1;
     } else if (packed_state && win_ok && a->window_layout == CV_WINDOW_DEDUP && a->win_ch_stride == Q) {
-        // one block of 8*64 channels per sequence, its rows staged by one bulk copy
+        // one block of 8*kCommitRowThreads channels per sequence, its rows staged by one bulk copy
         int rt = kCommitRowThreads;
         while (rt > kMinThreads && 8 * (rt / 2) >= a->dim) rt /= 2;
         const long long sm = (8LL * rt * Q * esize + 127) / 128 * 128 + 8;
@@ -476,6 +480,8 @@ int launch_commit(const cv_commit_args *a, cudaStream_t stream) {
     } else {
         p.mode = 0;
     }
+    int threads = p.mode == 1 ? kCommitDenseThreads : kCommitElementThreads;
+    while (threads > kMinThreads && 8 * (threads / 2) >= a->dim) threads /= 2;
     const int bc = 8 * threads;
     auto k = kernel_set(a->dtype, a->width).commit;
     if (ensure_smem(reinterpret_cast<const void *>(k), smem) != cudaSuccess) return CV_ERR_LAUNCH;
