@@ -133,6 +133,26 @@ def _dev_ptr(t, name, required=True):
     return t.data_ptr()
 
 
+def _need_shape(t, name, shape):
+    """Shapes are checked here because the library sees only pointers: a buffer smaller than the
+    sizes describe would be read or written past its end."""
+    if t is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+
+
+def _need_int32(t, name, n=None, shape=None):
+    """An int32 device array: contiguous, of the given shape, or holding at least n elements."""
+    if t is None:
+        return
+    import torch
+    if t.dtype != torch.int32 or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous int32 tensor")
+    if shape is not None:
+        _need_shape(t, name, shape)
+    if n is not None and t.numel() < n:
+        raise ValueError(f"{name} needs at least {n} elements, got {t.numel()}")
+
+
 def _layout_code(layout) -> int:
     if layout in (DENSE, "dense"):
         return DENSE
@@ -174,12 +194,24 @@ def make_verify_args(x, conv_state, weight, bias, out, window, *, layout, qk_cha
     row and the next call reads at state_off = accept_len - 1) or "recompute" (outputs only; the
     commit rebuilds the state from x), cache_idx / state_off / err int32 [n_seq] or None, parent int32
     [n_seq, T] contiguous (tree verify, dense layout) or None."""
-    if parent is not None and (not parent.is_contiguous() or parent.dtype.itemsize != 4):
-        raise ValueError("parent must be a contiguous int32 [n_seq, T] tensor")
     lay = _layout_code(layout)
     ptr = _dev_ptr if check_device else (lambda t, n, required=True: None if t is None else t.data_ptr())
+    if x.dim() != 3 or conv_state.dim() != 3 or weight.dim() != 2:
+        raise ValueError("x must be [n_seq, T, dim], conv_state [n_slots, dim, S] and weight [dim, W]")
     n_seq, T, dim = x.shape
     W = weight.shape[1]
+    _need_shape(out, "out", x.shape)
+    _need_shape(weight, "weight", (dim, W))
+    _need_shape(bias, "bias", (dim,))
+    if conv_state.shape[1] != dim:
+        raise ValueError(f"conv_state must have dim = {dim} channels, got {conv_state.shape[1]}")
+    if lay == DENSE:
+        _need_shape(window, "window", (n_seq, T, dim, W - 1))
+    elif lay == DEDUP:
+        _need_shape(window, "window", (n_seq, dim, T + W - 2))
+    for t, name in ((cache_idx, "cache_idx"), (state_off, "state_off"), (err, "err")):
+        _need_int32(t, name, n=n_seq)
+    _need_int32(parent, "parent", shape=(n_seq, T))
     if x.stride(2) != 1 or out.stride(2) != 1 or conv_state.stride(2) != 1:
         raise ValueError("x, out and conv_state need a unit innermost stride")
     if not weight.is_contiguous() or (bias is not None and not bias.is_contiguous()):
@@ -244,8 +276,20 @@ def make_commit_args(conv_state, window, accept_len, *, layout, T, width, cache_
         raise ValueError("x needs a unit channel stride")
     ptr = _dev_ptr if check_device else (lambda t, n, required=True: None if t is None else t.data_ptr())
     ws = _window_strides(window, lay)
-    if conv_state.stride(2) != 1:
-        raise ValueError("conv_state needs a unit column stride")
+    if conv_state.dim() != 3 or conv_state.stride(2) != 1:
+        raise ValueError("conv_state must be [n_slots, dim, S] with a unit column stride")
+    _need_int32(accept_len, "accept_len")
+    if accept_len.dim() != 1:
+        raise ValueError("accept_len must be [n_seq]")
+    n_seq, dim = accept_len.shape[0], conv_state.shape[1]
+    for t, name in ((cache_idx, "cache_idx"), (err, "err")):
+        _need_int32(t, name, n=n_seq)
+    if lay == DENSE:
+        _need_shape(window, "window", (n_seq, T, dim, width - 1))
+    elif lay == DEDUP:
+        _need_shape(window, "window", (n_seq, dim, T + width - 2))
+    else:
+        _need_shape(x, "x", (n_seq, T, dim))
     return CommitArgs(
         n_seq=accept_len.shape[0], T=T, dim=conv_state.shape[1], width=width, dtype=_dtype_code(conv_state),
         n_slots=conv_state.shape[0], conv_state=ptr(conv_state, "conv_state"),
@@ -280,7 +324,19 @@ def make_prefill_args(x, conv_state, weight, bias, out, cu_seqlens, *, max_seqle
     [n_seq + 1], cache_idx / has_initial_state / err int32 [n_seq] or None; max_seqlen bounds
     every sequence's length (host int)."""
     ptr = _dev_ptr if check_device else (lambda t, n, required=True: None if t is None else t.data_ptr())
+    if x.dim() != 2 or conv_state.dim() != 3 or weight.dim() != 2:
+        raise ValueError("x must be [total_tokens, dim], conv_state [n_slots, dim, S] and weight [dim, W]")
     total, dim = x.shape
+    _need_shape(out, "out", x.shape)
+    _need_shape(weight, "weight", (dim, weight.shape[1]))
+    _need_shape(bias, "bias", (dim,))
+    if conv_state.shape[1] != dim:
+        raise ValueError(f"conv_state must have dim = {dim} channels, got {conv_state.shape[1]}")
+    _need_int32(cu_seqlens, "cu_seqlens")
+    if cu_seqlens.dim() != 1 or cu_seqlens.shape[0] < 1:
+        raise ValueError("cu_seqlens must be [n_seq + 1]")
+    for t, name in ((cache_idx, "cache_idx"), (has_initial_state, "has_initial_state"), (err, "err")):
+        _need_int32(t, name, n=cu_seqlens.shape[0] - 1)
     if x.stride(1) != 1 or out.stride(1) != 1 or conv_state.stride(2) != 1:
         raise ValueError("x, out and conv_state need a unit innermost stride")
     if not weight.is_contiguous() or (bias is not None and not bias.is_contiguous()):

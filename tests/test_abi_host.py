@@ -389,3 +389,71 @@ def test_tree_plan_and_validation(lib):
     # one draft token: one warp
     a.T = 1
     assert _plan(lib, a)[1].threads == 32
+
+
+def _verify_inputs(layout="dedup", **over):
+    w = wl.VerifyWorkload("bind", n_seq=3, T=4, dim=64, width=4, qk_channels=32, head_dim=16, dtype="bf16",
+                          layout=layout, bias=True, seed=1, **over)
+    return w, wl.make_inputs(w)
+
+
+def _make(w, inp, **over):
+    kw = dict(layout=w.layout, qk_channels=w.qk_channels, head_dim=w.head_dim, cache_idx=inp["cache_idx"],
+              state_off=inp.get("state_off"), parent=inp.get("parent"), check_device=False)
+    kw.update({k: v for k, v in over.items() if k in kw})
+    args = [over.get(k, inp[k]) for k in ("x", "conv_state", "weight", "bias", "out", "window")]
+    return cv.make_verify_args(*args, **kw)
+
+
+@pytest.mark.parametrize("what", ["out", "bias", "weight", "window", "state_dim", "cache_idx_short",
+                                  "cache_idx_int64", "parent_shape", "parent_float", "err_short"])
+def test_binding_rejects_buffers_smaller_than_described(what):
+    """The library sees only pointers, so the binding checks every buffer against the sizes the
+    arguments describe: a wrong shape or index dtype raises before anything reaches the library."""
+    w, inp = _verify_inputs(layout="dense")
+    n, T, dim = w.n_seq, w.T, w.dim
+    bad = {
+        "out": dict(out=torch.empty(n, T, dim - 8, dtype=torch.bfloat16)),
+        "bias": dict(bias=torch.empty(dim + 1, dtype=torch.bfloat16)),
+        "weight": dict(weight=torch.empty(dim - 8, 4, dtype=torch.bfloat16)),
+        "window": dict(window=torch.empty(n, T - 1, dim, 3, dtype=torch.bfloat16)),
+        "state_dim": dict(conv_state=torch.empty(w.n_slots, dim - 8, 3, dtype=torch.bfloat16)),
+        "cache_idx_short": dict(cache_idx=torch.zeros(n - 1, dtype=torch.int32)),
+        "cache_idx_int64": dict(cache_idx=torch.zeros(n, dtype=torch.int64)),
+        "parent_shape": dict(parent=torch.full((n, T - 1), -1, dtype=torch.int32)),
+        "parent_float": dict(parent=torch.full((n, T), -1.0, dtype=torch.float32)),
+        "err_short": dict(err=torch.zeros(n - 1, dtype=torch.int32)),
+    }[what]
+    if "err" in bad:
+        with pytest.raises(ValueError):
+            cv.make_verify_args(inp["x"], inp["conv_state"], inp["weight"], inp["bias"], inp["out"], inp["window"],
+                                layout="dense", qk_channels=w.qk_channels, head_dim=w.head_dim, err=bad["err"],
+                                check_device=False)
+        return
+    with pytest.raises(ValueError):
+        _make(w, inp, **bad)
+    _make(w, inp)  # the unmodified inputs pass
+
+
+def test_binding_commit_and_prefill_shapes():
+    """The commit checks its window against (n_seq, T, dim) and its index arrays; the prefill its
+    out, taps and per-sequence arrays against cu_seqlens."""
+    w, inp = _verify_inputs(layout="dedup")
+    ok = dict(layout="dedup", T=w.T, width=w.width, cache_idx=inp["cache_idx"], check_device=False)
+    cv.make_commit_args(inp["conv_state"], inp["window"], inp["accept_len"], **ok)
+    with pytest.raises(ValueError):
+        cv.make_commit_args(inp["conv_state"], inp["window"][:, :, :-1], inp["accept_len"], **ok)
+    with pytest.raises(ValueError):
+        cv.make_commit_args(inp["conv_state"], inp["window"], inp["accept_len"].to(torch.int64), **ok)
+    with pytest.raises(ValueError):
+        cv.make_commit_args(inp["conv_state"], inp["window"], inp["accept_len"],
+                            **dict(ok, cache_idx=inp["cache_idx"][:-1]))
+    pw = wl.PREFILL_WORKLOADS[wl.PREFILL_ORDER[0]]
+    p = wl.make_prefill_inputs(pw)
+    kw = dict(max_seqlen=pw.max_seqlen, qk_channels=pw.qk_channels, head_dim=pw.head_dim, check_device=False)
+    cv.make_prefill_args(p["x"], p["conv_state"], p["weight"], p["bias"], p["out"], p["cu_seqlens"], **kw)
+    with pytest.raises(ValueError):
+        cv.make_prefill_args(p["x"], p["conv_state"], p["weight"], p["bias"], p["out"][:-1], p["cu_seqlens"], **kw)
+    with pytest.raises(ValueError):
+        cv.make_prefill_args(p["x"], p["conv_state"], p["weight"], p["bias"], p["out"], p["cu_seqlens"],
+                             cache_idx=torch.zeros(p["cu_seqlens"].numel() - 2, dtype=torch.int32), **kw)
