@@ -26,6 +26,7 @@ import os
 import re
 import statistics
 import subprocess
+import tempfile
 import sys
 import time
 
@@ -96,11 +97,11 @@ class ClockSampler:
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, index: int):
+    def __init__(self, index: int, path=None):
         self.index = index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{index}.csv") if os.path.isdir(
-            os.path.join(ROOT, "gpurun_out")) else f"/tmp/cv_clocks_{os.getpid()}.csv"
+        # the raw samples go to `path` (kept), else to a temporary file
+        self.path = path or os.path.join(tempfile.gettempdir(), f"cv_clocks_{os.getpid()}_{index}.csv")
 
     def start(self):
         try:
@@ -350,7 +351,7 @@ def run_ours(args, w, world, rank, local, dist):
     torch.cuda.synchronize(dev)
 
     # clocks: sample during a loaded stretch right before and through the timed region
-    sampler = ClockSampler(dev.index)
+    sampler = ClockSampler(dev.index, args.clocks_csv)
     sampler.start()
     t_end = time.perf_counter() + args.clock_probe_s
     i = 0
@@ -526,7 +527,7 @@ def run_ours_prefill(args, w, world, rank, local, dist):
         if fn(refs[i % n_sets], sp) != 0:
             raise RuntimeError("launch failed during warm-up")
     torch.cuda.synchronize(dev)
-    sampler = ClockSampler(dev.index)
+    sampler = ClockSampler(dev.index, args.clocks_csv)
     sampler.start()
     t_end = time.perf_counter() + args.clock_probe_s
     i = 0
@@ -595,6 +596,7 @@ def main():
     ap.add_argument("--workload", default=wl.BENCH_WORKLOAD, choices=wl.WORKLOAD_ORDER + wl.PREFILL_ORDER)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--clocks-csv", default=None, help="keep the raw nvidia-smi clock samples in this file")
     ap.add_argument("--clock-probe-s", type=float, default=1.5)
     ap.add_argument("--cpu-budget-s", type=float, default=10.0)
     args = ap.parse_args()
