@@ -299,13 +299,14 @@ CV_API int cv_conv_prefill(const cv_prefill_args *args, void *stream);
 /*
  * cv_verify_plan -- validate `args` exactly as cv_conv_verify does and report the launch it would
  * make, without touching the GPU.  grid = (grid_x, grid_y), block = threads, dynamic shared
- * memory = smem_bytes; each block owns channels_per_block channels of one sequence.  path says
+ * memory = smem_bytes; a unit of work is channels_per_block channels of one sequence (one unit per
+ * block, or, on the persistent paths 3 and 5, a stream of units per block).  path says
  * which kernel runs: 3 = persistent pipelined kernel (packed buffers and packed state rows, T a
  * compile-time constant; grid_y = 1 and each block walks (sequence, channel block) units),
  * 1 = packed buffers with T a compile-time constant (T <= 17 for bf16, <= 8 for fp32),
  * 2 = packed buffers, dense window, larger T in chunks of 8 tokens, 0 = the general kernel (any
- * strides), 5 = tree verify (parent given; persistent one-warp blocks walk (sequence, 256
- * channels) units, staging each unit's committed windows, x rows and parents in one of `stages`
+ * strides), 5 = tree verify (parent given; persistent blocks of one or two warps walk (sequence,
+ * 256 channels) units, staging each unit's committed windows, x rows and parents in one of `stages`
  * shared-memory buffers; grid_y = 1).  Host pointer `plan` must not be NULL.  Returns the same status
  * cv_conv_verify would return before launching.
  */
