@@ -74,6 +74,11 @@ MUTANTS = [
      lambda: pins.test_m4_mixed_matches_float64_conv1d("bf16", "f32")),
     ("tree_parent_ignored", "const int base = (a->parent[(int64_t)s * T + t] + 1) * R;", "const int base = t * R;",
      lambda: pins.test_tr2_tree_paths_equal_chain_verifies()),
+    ("tree_window_not_shifted", "wbits[nb + k] = wbits[base + k + 1];", "wbits[nb + k] = wbits[base + k];",
+     lambda: pins.test_tr1_chain_parents_equal_the_plain_verify(4, "bf16")),
+    ("tree_state_one_token_short", "put_bits(a->state, sbf, srow + k, wbits[T * R + k]);",
+     "put_bits(a->state, sbf, srow + k, wbits[(T - 1) * R + k]);",
+     lambda: pins.test_tr1_chain_parents_equal_the_plain_verify(4, "f32")),
     ("padded_row_written", "if (slot < 0 || st) continue;\n\n", "if (st) continue;\n        if (slot < 0) { if (a->out) put_bits(a->out, bf, (int64_t)s * a->out_seq, 0); continue; }\n\n",
      lambda: pins.test_p7_padded_rows_untouched()),
 ]
