@@ -717,3 +717,26 @@ def test_tree_invalid_parents_flagged():
         slot = int(inp["cache_idx"][s])
         assert_bits_equal(r["conv_state"][slot], inp["conv_state"][slot], "state")
         assert_bits_equal(r["window"][s], inp["window"][s], "window")
+
+
+@pytest.mark.parametrize("layout", ["dense", "dedup"])
+def test_p_extreme_conv_values_match_float64(layout):
+    """Conv results far from zero on both sides (x and state scaled by 200: about a fifth of them
+    below -80, where exp(-acc) passes 1e34 and, past -88.7, overflows fp32): the oracle's fp32
+    SiLU and L2 still match the float64 definition within the fp32 output tolerance."""
+    w = small(dtype="f32", layout=layout, width=4, n_pad=0, extra_slots=1, seed=303)
+    inp = wl.make_inputs(w)
+    inp["x_base"].mul_(200.0)
+    inp["conv_state"].mul_(200.0)
+    r = run_oracle_verify(w, inp)
+    outs, _, _ = float64_reference(w, inp)
+    below = 0
+    for s, ref in outs.items():
+        got = r["out"][s].double()
+        err = (got - ref).abs()
+        assert (err <= 1e-5 * ref.abs() + 1e-6).all(), float(err.max())
+        slot = int(inp["cache_idx"][s])
+        full = torch.cat([inp["conv_state"][slot, :, :3].double(), inp["x"][s].double().t()], dim=1)
+        acc = F.conv1d(full[None], inp["weight"].double()[:, None, :], inp["bias"].double(), groups=w.dim)[0]
+        below += int((acc < -80).sum())
+    assert below > 0.1 * w.n_seq * w.T * w.dim  # the range the exact SiLU form covers is exercised
