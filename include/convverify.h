@@ -31,7 +31,10 @@
  *   - Invalid arguments are reported by a negative status before anything is launched; nothing is
  *     written then.  Problems that only the device can see (a cache slot or state offset out of
  *     range, an accept count out of range) are reported per sequence through the optional `err`
- *     array, and that sequence is left untouched.  No kernel traps or waits on anything.
+ *     array, and that sequence is left untouched.  No kernel traps.  The kernels that stage data
+ *     through bulk copies wait for them with bounded waits (wait_polls below): a wait that gives
+ *     up flags CV_SEQ_TIMEOUT for every sequence the block did not finish, and the kernel returns
+ *     with its context intact.
  */
 #ifndef CONVVERIFY_H
 #define CONVVERIFY_H
@@ -48,7 +51,7 @@ extern "C" {
 #define CV_API
 #endif
 
-#define CV_ABI_VERSION 4
+#define CV_ABI_VERSION 5
 #define CV_MAX_T 128 /* draft tokens per verify call */
 
 typedef enum cv_dtype {
@@ -113,7 +116,8 @@ enum {
 #define CV_SEQ_BAD_SLOT 1   /* cache slot >= n_slots */
 #define CV_SEQ_BAD_OFFSET 2 /* state offset < 0 or offset + W-1 > state_cols */
 #define CV_SEQ_BAD_ACCEPT 4 /* accept count outside 1..T (commit only) */
-#define CV_SEQ_TIMEOUT 8    /* a bounded wait for a bulk copy gave up (the sequence may be partly written) */
+#define CV_SEQ_TIMEOUT 8    /* a bounded wait for a bulk copy gave up: the sequence may be partly
+                               written (every sequence whose data the block had not finished) */
 #define CV_SEQ_BAD_SPAN 16  /* prefill: token span invalid or longer than max_seqlen */
 #define CV_SEQ_BAD_TREE 32  /* tree verify: a draft token's parent outside [-1, t) */
 
@@ -162,7 +166,17 @@ enum {
  *   window             snapshot buffer, write-only, laid out as window_layout says (NULL allowed
  *                      and ignored for CV_WINDOW_HISTORY and CV_WINDOW_RECOMPUTE)
  *   err                int32 [n_seq] device array or NULL: receives the CV_SEQ_* bits of each
- *                      sequence (0 for fine and for padded sequences)
+ *                      sequence (0 for fine and for padded sequences).  On the pipelined path the
+ *                      library clears it (an asynchronous memset on `stream`) before the kernel ORs
+ *                      the bits in, since several blocks report for one sequence.
+ *   wait_polls         limit of each unit's first wait for its bulk copies on the pipelined path
+ *                      (path 3): 0 = the default (2^20 polls of mbarrier.try_wait, far beyond any
+ *                      copy's latency), n > 0 = n polls, negative = no poll at all, so the wait
+ *                      gives up at once.  Nonzero values exist to exercise the timeout path: the
+ *                      block flags CV_SEQ_TIMEOUT for the unit's sequence and for those of every
+ *                      later unit it owns, waits (with the default limit) for the copies it has in
+ *                      flight, and returns; the other sequences are computed as usual.  Other paths
+ *                      ignore it.
  *   state_dtype        CV_STATE_SAME, or the other dtype for conv_state and window (mixed dtypes,
  *                      [sglang-46184] "Accuracy Tests"): inputs are widened exactly for the
  *                      arithmetic; snapshots and state receive x converted to the state dtype
@@ -198,7 +212,7 @@ typedef struct cv_verify_args {
     const void *bias;
     void *window;
     int32_t window_layout; /* cv_window_layout */
-    int32_t reserved0;
+    int32_t wait_polls;    /* limit of the bounded waits (see above); 0 = the default */
     int64_t win_seq_stride, win_step_stride, win_ch_stride, win_col_stride;
     int32_t *err;
     int32_t state_dtype; /* CV_STATE_* */
@@ -216,7 +230,10 @@ CV_API int cv_conv_verify(const cv_verify_args *args, void *stream);
  * read on the device (no host round trip), 1 <= a <= T:
  *     conv_state[slot][c][k] = snapshot (s, a-1, c, k)      for every c < dim, k < W-1
  * a = T rewrites the state with the value it already holds.  A sequence whose a is out of range
- * gets CV_SEQ_BAD_ACCEPT in err[s] and is untouched.  The window must be the one the matching
+ * gets CV_SEQ_BAD_ACCEPT in err[s] and is untouched.  Packed deduplicated rows are staged by a
+ * bulk copy with a bounded wait (wait_polls as in cv_verify_args; a timeout flags CV_SEQ_TIMEOUT
+ * and leaves the block's channels unwritten); that kernel ORs its bits into err, which the library
+ * clears first with an asynchronous memset on `stream`.  The window must be the one the matching
  * cv_conv_verify wrote (same layout and strides).
  *
  * CV_WINDOW_RECOMPUTE: there is no window; x (with x_seq_stride, x_tok_stride, channel stride 1)
@@ -243,6 +260,7 @@ typedef struct cv_commit_args {
     /* CV_WINDOW_RECOMPUTE only (ignored otherwise): the verify's input [n_seq][T][dim] */
     const void *x;
     int64_t x_seq_stride, x_tok_stride;
+    int32_t wait_polls; /* limit of the bounded wait, as in cv_verify_args; 0 = the default */
 } cv_commit_args;
 
 CV_API int cv_conv_commit(const cv_commit_args *args, void *stream);

@@ -40,7 +40,7 @@ class VerifyArgs(ctypes.Structure):
         ("conv_state", c_vp), ("n_slots", c_i32), ("state_cols", c_i32),
         ("state_slot_stride", c_i64), ("state_ch_stride", c_i64),
         ("cache_idx", c_vp), ("state_off", c_vp), ("weight", c_vp), ("bias", c_vp),
-        ("window", c_vp), ("window_layout", c_i32), ("reserved0", c_i32),
+        ("window", c_vp), ("window_layout", c_i32), ("wait_polls", c_i32),
         ("win_seq_stride", c_i64), ("win_step_stride", c_i64), ("win_ch_stride", c_i64), ("win_col_stride", c_i64),
         ("err", c_vp), ("state_dtype", c_i32), ("parent", c_vp),
     ]
@@ -54,6 +54,7 @@ class CommitArgs(ctypes.Structure):
         ("state_cols", c_i32), ("window_layout", c_i32), ("cache_idx", c_vp), ("window", c_vp),
         ("win_seq_stride", c_i64), ("win_step_stride", c_i64), ("win_ch_stride", c_i64), ("win_col_stride", c_i64),
         ("accept_len", c_vp), ("err", c_vp), ("x", c_vp), ("x_seq_stride", c_i64), ("x_tok_stride", c_i64),
+        ("wait_polls", c_i32),
     ]
 
 
@@ -182,7 +183,7 @@ def _stream_ptr(stream) -> Optional[int]:
 
 
 def make_verify_args(x, conv_state, weight, bias, out, window, *, layout, qk_channels, head_dim,
-                     l2_eps=1e-6, cache_idx=None, state_off=None, err=None, parent=None,
+                     l2_eps=1e-6, cache_idx=None, state_off=None, err=None, parent=None, wait_polls=0,
                      check_device=True) -> VerifyArgs:
     """Build cv_verify_args from tensors.
 
@@ -193,7 +194,8 @@ def make_verify_args(x, conv_state, weight, bias, out, window, *, layout, qk_cha
     None with layout "history" (conv_state [n_slots, dim, S >= T+W-2] then receives the snapshot
     row and the next call reads at state_off = accept_len - 1) or "recompute" (outputs only; the
     commit rebuilds the state from x), cache_idx / state_off / err int32 [n_seq] or None, parent int32
-    [n_seq, T] contiguous (tree verify, dense layout) or None."""
+    [n_seq, T] contiguous (tree verify, dense layout) or None.  wait_polls: the limit of the
+    pipelined kernel's bounded waits (0 = the default; see cv_verify_args)."""
     lay = _layout_code(layout)
     ptr = _dev_ptr if check_device else (lambda t, n, required=True: None if t is None else t.data_ptr())
     if x.dim() != 3 or conv_state.dim() != 3 or weight.dim() != 2:
@@ -226,14 +228,14 @@ def make_verify_args(x, conv_state, weight, bias, out, window, *, layout, qk_cha
         cache_idx=ptr(cache_idx, "cache_idx", False), state_off=ptr(state_off, "state_off", False),
         weight=ptr(weight, "weight"), bias=ptr(bias, "bias", False),
         window=ptr(window, "window", lay not in (HISTORY, RECOMPUTE)),
-        window_layout=lay, reserved0=0, win_seq_stride=ws[0], win_step_stride=ws[1], win_ch_stride=ws[2],
+        window_layout=lay, wait_polls=int(wait_polls), win_seq_stride=ws[0], win_step_stride=ws[1], win_ch_stride=ws[2],
         win_col_stride=ws[3], err=ptr(err, "err", False),
         state_dtype=0 if conv_state.dtype == x.dtype else _dtype_code(conv_state) + 1,
         parent=ptr(parent, "parent", False))
 
 
 def conv_verify(x, conv_state, weight, bias, out, window, *, layout, qk_channels, head_dim, l2_eps=1e-6,
-                cache_idx=None, state_off=None, err=None, parent=None, stream=None) -> None:
+                cache_idx=None, state_off=None, err=None, parent=None, wait_polls=0, stream=None) -> None:
     """Queue one batched verify on ``stream`` (default: torch's current stream).
 
     Writes out, window, conv_state (and err); raises CvError on an invalid argument.  With layout
@@ -248,7 +250,7 @@ def conv_verify(x, conv_state, weight, bias, out, window, *, layout, qk_channels
         raise TypeError("bias must have the dtype of x")
     a = make_verify_args(x, conv_state, weight, bias, out, window, layout=layout, qk_channels=qk_channels,
                          head_dim=head_dim, l2_eps=l2_eps, cache_idx=cache_idx, state_off=state_off, err=err,
-                         parent=parent)
+                         parent=parent, wait_polls=wait_polls)
     rc = load_library().cv_conv_verify(ctypes.byref(a), _stream_ptr(stream))
     if rc != 0:
         raise CvError(rc, "cv_conv_verify")
@@ -268,7 +270,7 @@ def verify_plan(x, conv_state, weight, bias, out, window, *, layout, qk_channels
 
 
 def make_commit_args(conv_state, window, accept_len, *, layout, T, width, cache_idx=None, err=None,
-                     x=None, check_device=True) -> CommitArgs:
+                     x=None, wait_polls=0, check_device=True) -> CommitArgs:
     """Build cv_commit_args.  Layout "recompute": window is None and x is the verify's input
     [n_seq, T, dim] (channel stride 1)."""
     lay = _layout_code(layout)
@@ -298,18 +300,19 @@ def make_commit_args(conv_state, window, accept_len, *, layout, T, width, cache_
         window=ptr(window, "window", lay != RECOMPUTE), win_seq_stride=ws[0], win_step_stride=ws[1],
         win_ch_stride=ws[2], win_col_stride=ws[3], accept_len=ptr(accept_len, "accept_len"),
         err=ptr(err, "err", False), x=ptr(x, "x", lay == RECOMPUTE),
-        x_seq_stride=x.stride(0) if x is not None else 0, x_tok_stride=x.stride(1) if x is not None else 0)
+        x_seq_stride=x.stride(0) if x is not None else 0, x_tok_stride=x.stride(1) if x is not None else 0,
+        wait_polls=int(wait_polls))
 
 
 def conv_commit(conv_state, window, accept_len, *, layout, T, width, cache_idx=None, err=None, x=None,
-                stream=None) -> None:
+                wait_polls=0, stream=None) -> None:
     """Queue the commit: conv_state[slot] <- snapshot accept_len[s]-1 of sequence s (rebuilt from the
     kept window and x with layout "recompute")."""
     for t in (window, x):
         if t is not None and t.dtype != conv_state.dtype:
             raise TypeError("window / x and conv_state must share one dtype")
     a = make_commit_args(conv_state, window, accept_len, layout=layout, T=T, width=width, cache_idx=cache_idx,
-                         err=err, x=x)
+                         err=err, x=x, wait_polls=wait_polls)
     rc = load_library().cv_conv_commit(ctypes.byref(a), _stream_ptr(stream))
     if rc != 0:
         raise CvError(rc, "cv_conv_commit")

@@ -27,8 +27,6 @@ constexpr int kFastThreads = 128;
 constexpr int kPipeThreads = 128;
 // blocks per SM the pipelined kernel's launch bounds provide registers for
 constexpr int pipe_blocks_per_sm(int cpt, int T) { return (cpt == 4 && T <= 8) ? 4 : 2; }
-constexpr int kNumSMs = 152;             // GB300; sizes the persistent grid
-constexpr int kSmemPerSM = 232448;       // usable shared memory per SM
 constexpr int kSmemPerBlockReserved = 1024;
 constexpr int kMinThreads = 32;
 constexpr int kGenericSmemBudget = 96 * 1024;
@@ -42,11 +40,45 @@ constexpr int kCommitRecomputeThreads = 64;  // recompute rollback
 // dedup commit: 256 channels per block (small blocks fit beside the verify's resident blocks, so
 // more of them start, under programmatic dependent launch, while the verify drains)
 constexpr int kCommitRowThreads = 32;
-constexpr int kSmemMax = 227 * 1024;
 // the pipelined kernel lists the active sequences in shared memory up to this batch size
 constexpr int kCompactMaxSeq = 1024;
 constexpr int kPrefillMaxChunk = 256;  // tokens per prefill block, at most / at least (multiples of
 constexpr int kPrefillMinChunk = 32;   // the kernel's 8-token batch, and >= W-1)
+
+// The device the launch plans size for: SM count (the persistent grids), shared memory per SM
+// (residency) and per block (opt-in maximum), queried once per device and cached.  Without a
+// usable device (cv_verify_plan on a host without a GPU) the plans are made for a GB300: 152 SMs,
+// 228 KB per SM, 227 KB per block.
+struct DeviceLimits {
+    int sms, smem_per_sm, smem_per_block;
+};
+DeviceLimits device_limits() {
+    constexpr DeviceLimits kGB300{152, 232448, 227 * 1024};
+    constexpr int kMaxDevices = 64;
+    static std::atomic<int> cached[kMaxDevices][3];  // zero until queried
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) {
+        cudaGetLastError();  // clear the error the failed query recorded
+        return kGB300;
+    }
+    if (dev < kMaxDevices && cached[dev][0].load(std::memory_order_acquire) > 0)
+        return {cached[dev][0].load(std::memory_order_relaxed), cached[dev][1].load(std::memory_order_relaxed),
+                cached[dev][2].load(std::memory_order_relaxed)};
+    DeviceLimits d{0, 0, 0};
+    if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.smem_per_block, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess ||
+        d.sms < 1) {
+        cudaGetLastError();
+        return kGB300;
+    }
+    if (dev < kMaxDevices) {
+        cached[dev][1].store(d.smem_per_sm, std::memory_order_relaxed);
+        cached[dev][2].store(d.smem_per_block, std::memory_order_relaxed);
+        cached[dev][0].store(d.sms, std::memory_order_release);
+    }
+    return d;
+}
 
 bool pipe_compacts(const cv_verify_args *a) { return a->cache_idx != nullptr && a->n_seq <= kCompactMaxSeq; }
 
@@ -127,24 +159,24 @@ bool fast_eligible(const cv_verify_args *a, int esize, int ssize, int max_static
 
 // Halve a block (down to 32 threads) while the launch would have fewer than two blocks per SM and
 // the smaller block still holds whole L2 groups: small batches then still fill the GPU.
-int shrink_for_parallelism(int threads, int cpt, const cv_verify_args *a) {
+int shrink_for_parallelism(int threads, int cpt, const cv_verify_args *a, int sms) {
     const int min_bc = a->qk_channels > 0 ? a->head_dim : 8;
     auto units = [&](int t) { return (long long)a->n_seq * ((a->dim + (long long)cpt * t - 1) / ((long long)cpt * t)); };
-    while (threads > 32 && units(threads) < 2LL * kNumSMs && cpt * (threads / 2) >= min_bc) threads /= 2;
+    while (threads > 32 && units(threads) < 2LL * sms && cpt * (threads / 2) >= min_bc) threads /= 2;
     return threads;
 }
 
 // Units (sequence x channel block) per block of the pipelined kernel's persistent grid, for the
 // block size it would use (an upper bound on its shared-memory residency of 4 blocks per SM).
-double units_per_pipe_block(const cv_verify_args *a, int cpt) {
+double units_per_pipe_block(const cv_verify_args *a, int cpt, int sms) {
     int threads = kPipeThreads;
     while (threads > 32 && cpt * (threads / 2) >= a->dim) threads /= 2;
     while (a->qk_channels > 0 && cpt * threads < a->head_dim) threads *= 2;
-    threads = shrink_for_parallelism(threads, cpt, a);
+    threads = shrink_for_parallelism(threads, cpt, a, sms);
     const long long bc = (long long)cpt * threads;
     const long long nblk = (a->dim + bc - 1) / bc;
     const long long units = (long long)a->n_seq * nblk;
-    long long g = (long long)kNumSMs * pipe_blocks_per_sm(cpt, a->T);
+    long long g = (long long)sms * pipe_blocks_per_sm(cpt, a->T);
     if (g >= nblk) g = g / nblk * nblk;
     if (g > units) g = units;
     return g > 0 ? (double)units / (double)g : 0.0;
@@ -165,6 +197,7 @@ int plan_verify(const cv_verify_args *a, cv_launch_plan *pl) {
     const int esize = a->dtype == CV_BF16 ? 2 : 4;
     const bool mixed = mixed_dtypes(a);
     const int R = a->width - 1;
+    const DeviceLimits lim = device_limits();
     std::memset(pl, 0, sizeof *pl);
     if (a->parent) {
         // tree verify: its own persistent kernel of kTreeWarps-warp blocks walking (sequence,
@@ -172,14 +205,14 @@ int plan_verify(const cv_verify_args *a, cv_launch_plan *pl) {
         // computes) when they fit, else one; a grid of kTreeBlocksPerSM blocks per SM at most (as
         // shared memory allows), a multiple of the channel-block count so that a block keeps its taps
         const long long buf = cvk::tree_buffer_bytes(a->T, a->width, esize);
-        const int nbuf = 2 * buf <= kSmemMax ? 2 : 1;
-        if (buf > kSmemMax) return CV_ERR_SMEM;
-        int per_sm = (int)(kSmemPerSM / (nbuf * buf + kSmemPerBlockReserved));
+        const int nbuf = 2 * buf <= lim.smem_per_block ? 2 : 1;
+        if (buf > lim.smem_per_block) return CV_ERR_SMEM;
+        int per_sm = (int)(lim.smem_per_sm / (nbuf * buf + kSmemPerBlockReserved));
         if (per_sm > kTreeBlocksPerSM) per_sm = kTreeBlocksPerSM;
         if (per_sm < 1) per_sm = 1;
         const long long nblk = (a->dim + cvk::kTreeChannels - 1) / cvk::kTreeChannels;
         const long long units = (long long)a->n_seq * nblk;
-        long long g = (long long)kNumSMs * per_sm;
+        long long g = (long long)lim.sms * per_sm;
         if (g >= nblk) g = g / nblk * nblk;
         if (g > units) g = units;
         pl->threads = 32 * (a->T < kTreeWarps ? a->T : kTreeWarps);
@@ -213,13 +246,13 @@ int plan_verify(const cv_verify_args *a, cv_launch_plan *pl) {
     // (wide rows cost whole-row reads and element stores of the window; the pipeline pays that
     // back only when every block walks at least two units, otherwise the one-pass kernel wins)
     // (mixed dtypes have no one-pass kernel)
-    if (pipe_ok && wide && fast && !mixed && units_per_pipe_block(a, cpt) < 2.0) pipe_ok = false;
+    if (pipe_ok && wide && fast && !mixed && units_per_pipe_block(a, cpt, lim.sms) < 2.0) pipe_ok = false;
     if (pipe_ok) {
         auto part = [](long long b) { return (b + 127) / 128 * 128; };
         int threads = kPipeThreads;
         while (threads > 32 && cpt * (threads / 2) >= a->dim) threads /= 2;
         while (a->qk_channels > 0 && cpt * threads < a->head_dim) threads *= 2;
-        threads = shrink_for_parallelism(threads, cpt, a);
+        threads = shrink_for_parallelism(threads, cpt, a, lim.sms);
         const long long bc = (long long)cpt * threads;
         const long long Q = a->T + R - 1;
         // two stages (x rows + committed windows, or whole history rows) and two image buffers
@@ -229,14 +262,14 @@ int plan_verify(const cv_verify_args *a, cv_launch_plan *pl) {
         long long image = (hist || recomp || wide) ? 0 : part(R * bc * ssize);
         if (a->window_layout == CV_WINDOW_DEDUP || hist) image += part(Q * bc * ssize);
         const long long smem = 2 * stage + 2 * image + 32 + (pipe_compacts(a) ? 16 + 4LL * a->n_seq : 0);
-        int per_sm = (int)(kSmemPerSM / (smem + kSmemPerBlockReserved));
+        int per_sm = (int)(lim.smem_per_sm / (smem + kSmemPerBlockReserved));
         if (per_sm > pipe_blocks_per_sm(cpt, a->T)) per_sm = pipe_blocks_per_sm(cpt, a->T);
-        const int nst = (smem <= kSmemMax && per_sm >= 1) ? 2 : 0;
+        const int nst = (smem <= lim.smem_per_block && per_sm >= 1) ? 2 : 0;
         if (nst > 0) {
             const long long nblk = (a->dim + bc - 1) / bc;
             const long long units = (long long)a->n_seq * nblk;
             // a multiple of the channel-block count keeps each block on one channel block
-            long long g = (long long)kNumSMs * per_sm;
+            long long g = (long long)lim.sms * per_sm;
             if (g >= nblk) g = g / nblk * nblk;
             if (g > units) g = units;
             pl->threads = threads;
@@ -254,7 +287,7 @@ int plan_verify(const cv_verify_args *a, cv_launch_plan *pl) {
         int threads = kFastThreads;
         while (threads > 32 && cpt * (threads / 2) >= a->dim) threads /= 2;
         while (a->qk_channels > 0 && cpt * threads < a->head_dim) threads *= 2;
-        threads = shrink_for_parallelism(threads, cpt, a);
+        threads = shrink_for_parallelism(threads, cpt, a, lim.sms);
         const long long bc = (long long)cpt * threads;
         long long smem = bc * R * esize;  // committed-window image
         if (a->window_layout == CV_WINDOW_DEDUP) smem += bc * (a->T + R - 1) * esize;
@@ -274,7 +307,7 @@ int plan_verify(const cv_verify_args *a, cv_launch_plan *pl) {
             threads /= 2;
             smem = (long long)rows * (8 * threads + pad) * tsize;
         }
-        if (smem > kSmemMax) return CV_ERR_SMEM;
+        if (smem > lim.smem_per_block) return CV_ERR_SMEM;
         pl->threads = threads;
         pl->channels_per_block = 8 * threads;
         pl->smem_bytes = (int)smem;
@@ -316,7 +349,7 @@ cudaError_t ensure_smem(const void *kernel, int bytes) {
     const unsigned h = (unsigned)((key >> 4) * 0x9E3779B1u) & 63u;
     for (auto &slot : done_cache[h])
         if (slot.load(std::memory_order_relaxed) == key) return cudaSuccess;
-    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax);
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, device_limits().smem_per_block);
     if (e != cudaSuccess) return e;
     for (auto &slot : done_cache[h]) {
         unsigned long long z = 0;
@@ -354,6 +387,7 @@ int launch_verify(const cv_verify_args *a, const cv_launch_plan &pl, cudaStream_
     p.w_ch = a->win_ch_stride;
     p.w_col = a->win_col_stride;
     p.err = a->err;
+    p.wait_polls = a->wait_polls;
     p.n_seq = a->n_seq;
     p.T = a->T;
     p.dim = a->dim;
@@ -388,6 +422,9 @@ int launch_verify(const cv_verify_args *a, const cv_launch_plan &pl, cudaStream_
                           : pl.path == 3 ? (mixed ? ks.pipe_mixed[ci][a->T] : ks.pipe[ci][a->T])
                                          : ks.tree;
     if (ensure_smem(reinterpret_cast<const void *>(k), pl.smem_bytes) != cudaSuccess) return CV_ERR_LAUNCH;
+    // the pipelined kernel ORs the per-sequence bits into err (several blocks share a sequence)
+    if (pl.path == 3 && a->err && cudaMemsetAsync(a->err, 0, sizeof(int32_t) * (size_t)a->n_seq, stream) != cudaSuccess)
+        return CV_ERR_LAUNCH;
     if (launch_pdl(k, dim3(pl.grid_x, pl.grid_y), pl.threads, pl.smem_bytes, stream, p) != cudaSuccess)
         return CV_ERR_LAUNCH;
     return cudaGetLastError() == cudaSuccess ? CV_OK : CV_ERR_LAUNCH;
@@ -432,6 +469,7 @@ int launch_commit(const cv_commit_args *a, cudaStream_t stream) {
     p.w_col = a->win_col_stride;
     p.accept_len = a->accept_len;
     p.err = a->err;
+    p.wait_polls = a->wait_polls;
     p.n_seq = a->n_seq;
     p.T = a->T;
     p.dim = a->dim;
@@ -467,11 +505,14 @@ int launch_commit(const cv_commit_args *a, cudaStream_t stream) {
         int rt = kCommitRowThreads;
         while (rt > kMinThreads && 8 * (rt / 2) >= a->dim) rt /= 2;
         const long long sm = (8LL * rt * Q * esize + 127) / 128 * 128 + 8;
-        if (sm <= kSmemMax) {
+        if (sm <= device_limits().smem_per_block) {
             p.mode = 2;
             const int bc = 8 * rt;
             auto kr = kernel_set(a->dtype, a->width).commit_rows;
             if (ensure_smem(reinterpret_cast<const void *>(kr), (int)sm) != cudaSuccess) return CV_ERR_LAUNCH;
+            // commit_rows ORs its bits into err
+            if (a->err && cudaMemsetAsync(a->err, 0, sizeof(int32_t) * (size_t)a->n_seq, stream) != cudaSuccess)
+                return CV_ERR_LAUNCH;
             if (launch_pdl(kr, dim3((a->dim + bc - 1) / bc, a->n_seq), rt, (int)sm, stream, p) != cudaSuccess)
                 return CV_ERR_LAUNCH;
             return cudaGetLastError() == cudaSuccess ? CV_OK : CV_ERR_LAUNCH;
@@ -547,7 +588,7 @@ int launch_prefill(const cv_prefill_args *a, cudaStream_t stream) {
     // the longest chunk (fewest halo re-reads) that still gives every SM several blocks
     int chunk = kPrefillMaxChunk;
     while (chunk > kPrefillMinChunk &&
-           nblk * a->n_seq * ((a->max_seqlen + chunk - 1) / chunk) < 8LL * kNumSMs)
+           nblk * a->n_seq * ((a->max_seqlen + chunk - 1) / chunk) < 8LL * device_limits().sms)
         chunk /= 2;
     p.chunk = chunk;
     const long long chunks = a->max_seqlen > 0 ? (a->max_seqlen + chunk - 1) / chunk : 1;

@@ -86,7 +86,10 @@ __global__ void __launch_bounds__(128) commit_kernel(const __grid_constant__ Com
 // accept count are read while it is in flight; no dependent load precedes the data.  The state
 // run [c][k] = row[c][a-1+k] is then gathered from shared memory and written with 16-byte
 // coalesced stores.  A padded or rejected sequence still waits for its copy (the shared memory must
-// outlive it) and writes nothing.  The wait is bounded: a timeout sets bit 8 in err.
+// outlive it) and writes nothing.  The wait is bounded (p.wait_polls polls, 0 = the default,
+// negative = none): a timeout sets bit 8 in err, and the copy is then drained with the default
+// limit before the block leaves.  Every err bit is ORed in; the library zeroes err before the
+// launch.
 template <typename B, int W>
 __global__ void __launch_bounds__(64) commit_rows(const __grid_constant__ CommitParams p) {
     grid_dep_wait();
@@ -118,12 +121,13 @@ __global__ void __launch_bounds__(64) commit_rows(const __grid_constant__ Commit
         if (slot >= p.n_slots) status |= 1;
         if (a < 1 || a > p.T) status |= 4;
     }
-    if (p.err && blockIdx.x == 0 && tid == 0) p.err[s] = status;
+    if (p.err && blockIdx.x == 0 && tid == 0 && status) atomicOr(p.err + s, status);
     __syncthreads();  // the barrier's initialisation is visible to every waiting thread
-    const bool ok = mbar_wait_bounded(bar, 0u, kCommitWaitPolls);
+    const unsigned polls = p.wait_polls == 0 ? kCommitWaitPolls : p.wait_polls < 0 ? 0u : (unsigned)p.wait_polls;
+    const bool ok = mbar_wait_bounded(bar, 0u, polls);
     if (__syncthreads_or(!ok)) {  // every thread agrees before anyone leaves
         if (tid == 0) {
-            if (p.err) atomicOr(p.err + s, 8);
+            if (p.err && slot >= 0) atomicOr(p.err + s, 8);
             mbar_wait_bounded(bar, 0u, kCommitWaitPolls);  // drain the copy (bounded)
         }
         return;

@@ -33,6 +33,7 @@ struct VerifyParams {
     const int *parent;  // tree verify: [n_seq][T] parent of each draft token, or null (a chain)
     int x_vec, out_vec, st_vec, w_vec, b_vec;  // 16-byte vector access allowed (checked on the host)
     int st_packed;  // tree verify: the committed windows are packed, 16-byte-aligned [dim][W-1] rows
+    int wait_polls;  // polls of the first bounded wait per unit: 0 = the default, < 0 = none (gives up at once)
 };
 
 // Tree verify: channels per block, 8 per lane of a warp.
@@ -50,6 +51,7 @@ struct CommitParams {
     int mode;  // 0: element by element, 1: packed dense snapshot -> packed state, 2: packed dedup row -> packed state, 3: recompute from x
     const void *x;  // mode 3: the verify's input
     long long x_seq, x_tok;
+    int wait_polls;  // polls of the bounded wait for the staged rows: 0 = the default, < 0 = none
 };
 
 struct PrefillParams {
@@ -136,8 +138,9 @@ __device__ __forceinline__ uint32_t pack_halves(uint32_t lo, uint32_t hi) { retu
 // SiLU(a) = a / (1 + exp(-a)).  silu_fast evaluates exp(-a) = 2^(-a * log2 e) with the
 // ex2.approx instruction and the quotient as a * rcp.approx(1 + exp(-a)); relative error a few
 // fp32 ulp.  Both instructions flush subnormals, which matters only below a = -87
-// (1 + exp(-a) > 2^126): silu_exact is the plain expression, taken when some input is below -80
-// (see silu_run).
+// (1 + exp(-a) > 2^126): silu_exact is the plain expression, taken for every value below -80 and
+// for no other (see silu), so each output's bits depend on its own conv result alone, whichever
+// kernel computes it and whatever other values it is computed beside.
 __device__ __forceinline__ float silu_fast(float a) {
     float e, r;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(a * -1.4426950408889634f));
@@ -146,7 +149,9 @@ __device__ __forceinline__ float silu_fast(float a) {
 }
 __device__ __forceinline__ float silu_exact(float a) { return a / (1.0f + expf(-a)); }
 
-// SiLU of n values with one range check for the run (a branch realistic inputs never take).
+// SiLU of n values with one range check for the run (a branch realistic inputs never take); in
+// that branch only the values below -80 switch to the exact form, so the result equals silu()
+// value by value.
 template <int N>
 __device__ __forceinline__ void silu_run(const float *a, float *y) {
     float lo = a[0];
@@ -157,7 +162,7 @@ __device__ __forceinline__ void silu_run(const float *a, float *y) {
     }
     if (lo < -80.0f) {
 #pragma unroll
-        for (int i = 0; i < N; ++i) y[i] = silu_exact(a[i]);
+        for (int i = 0; i < N; ++i) y[i] = a[i] < -80.0f ? silu_exact(a[i]) : y[i];
     }
 }
 __device__ __forceinline__ float silu(float a) { return a < -80.0f ? silu_exact(a) : silu_fast(a); }

@@ -17,8 +17,12 @@
 // state rows) and computes the outputs: fp32 conv with bias first and the taps in order
 // (conv_chain), SiLU, the L2 normalisation of the q|k groups over head_dim/CPT lanes with the T
 // shuffle trees interleaved (glm5next_kda mod.rs), one rounding, vector stores.
-// Every mbarrier wait is bounded: a block that waits too long sets CV_SEQ_TIMEOUT in err (when
-// given) for the unit's sequence, drains its copies in flight (again bounded) and returns.
+// Every mbarrier wait is bounded: a block that waits too long for a unit's copies sets
+// CV_SEQ_TIMEOUT in err (when given) for that unit's sequence and for the sequence of every later
+// unit it owns (none of which it will run), drains its copies in flight (with the full default
+// limit, so nothing lands in shared memory after the block has left) and returns.  The limit of
+// that first wait per unit is p.wait_polls (0: the default; negative: no poll at all, a wait
+// that gives up at once).  Every err bit is ORed in; the library zeroes err before the launch.
 // History-row state (no window buffer): the stage holds each channel's whole [T+W-2] state row,
 // the committed window is taken from columns [off, off+W-1) of it, and the row image is stored
 // back over the state row instead of into a window buffer; there is no separate committed-window
@@ -116,7 +120,6 @@ __global__ void __launch_bounds__(128, (CPT == 4 && TS <= 8) ? 4 : 2) verify_pip
         for (int i0 = 0; i0 < p.n_seq; i0 += (int)blockDim.x) {
             const int i = i0 + tid;
             const bool a = i < p.n_seq && __ldg(p.cache_idx + i) >= 0;
-            if (i < p.n_seq && !a && p.err && blockIdx.x == 0) p.err[i] = 0;
             const unsigned m = __ballot_sync(0xffffffffu, a);
             if (lane == 0) wcount[warp] = __popc(m);
             __syncthreads();
@@ -168,7 +171,7 @@ __global__ void __launch_bounds__(128, (CPT == 4 && TS <= 8) ? 4 : 2) verify_pip
         int s, c0, nch;
         unit_of(k, s, c0, nch);
         const int status = seq_status(slot, off, p.n_slots, p.state_cols, R);
-        if (p.err && c0 == 0) p.err[s] = status;
+        if (p.err && c0 == 0 && status) atomicOr(p.err + s, status);
         const bool go = slot >= 0 && status == 0;
         info[st] = go ? slot : -1;
         info[2 + st] = off;
@@ -182,6 +185,8 @@ __global__ void __launch_bounds__(128, (CPT == 4 && TS <= 8) ? 4 : 2) verify_pip
         }
         mbar_arrive(&bar[st]);
     };
+    // polls of each unit's first wait for its copies (the drain after a timeout uses kWaitPolls)
+    const unsigned first_polls = p.wait_polls == 0 ? kWaitPolls : p.wait_polls < 0 ? 0u : (unsigned)p.wait_polls;
     int pf_slot = 0, pf_off = 0;
     if (tid == 0) {
         int slot0 = 0, off0 = 0, slot1 = 0, off1 = 0;
@@ -239,7 +244,7 @@ __global__ void __launch_bounds__(128, (CPT == 4 && TS <= 8) ? 4 : 2) verify_pip
             }
         }
 
-        const bool ok = mbar_wait_bounded(&bar[st], (unsigned)((k >> 1) & 1), kWaitPolls);
+        const bool ok = mbar_wait_bounded(&bar[st], (unsigned)((k >> 1) & 1), first_polls);
         const int slot = ok ? info[st] : -1;
         const int off = info[2 + st];
         const bool go = slot >= 0;
@@ -336,7 +341,14 @@ __global__ void __launch_bounds__(128, (CPT == 4 && TS <= 8) ? 4 : 2) verify_pip
         // whether any thread's wait timed out
         if (__syncthreads_or(!ok)) {
             if (tid == 0) {
-                if (p.err) atomicOr(p.err + s, kSeqTimeout);
+                // this unit and every later unit of the block stay (partly) unwritten: flag their
+                // sequences (padded ones excepted)
+                if (p.err)
+                    for (int k2 = k; k2 < iters; ++k2) {
+                        int s2, c2, n2;
+                        unit_of(k2, s2, c2, n2);
+                        if (!p.cache_idx || __ldg(p.cache_idx + s2) >= 0) atomicOr(p.err + s2, kSeqTimeout);
+                    }
                 // drain the copies still in flight into this block's shared memory (bounded)
                 mbar_wait_bounded(&bar[st], (unsigned)((k >> 1) & 1), kWaitPolls);
                 if (k + 1 < iters) mbar_wait_bounded(&bar[st ^ 1], (unsigned)(((k + 1) >> 1) & 1), kWaitPolls);
@@ -383,11 +395,13 @@ __global__ void __launch_bounds__(128, (CPT == 4 && TS <= 8) ? 4 : 2) verify_pip
                     }
                 }
                 if (lo < -80.0f) {
+                    // only the values below -80 take the exact form (the same bits as silu())
 #pragma unroll
                     for (int t = 0; t < TS; ++t)
 #pragma unroll
                         for (int e = 0; e < CPT; ++e) {
-                            y[t][e] = silu_exact(conv_chain<CB, W>(bs[e], wt[e], &fw[e][t]));
+                            const float acc = conv_chain<CB, W>(bs[e], wt[e], &fw[e][t]);
+                            if (acc < -80.0f) y[t][e] = silu_exact(acc);
                         }
                 }
             } else {

@@ -22,7 +22,7 @@
 // rows 0..W-2 the committed window, rows W-1..W+T-2 the x rows.  For each token the warp walks the
 // parents (warp-uniform) to its W input rows and reads them as 16-byte runs; each lane owns 8
 // consecutive channels, and warp w of the block takes tokens w, w + warps, ....  Conv
-// (conv_chain), SiLU (the fast form, the exact one for a token whose channels reach below -80),
+// (conv_chain), SiLU (the fast form; the exact one for each value below -80, see silu_run),
 // the L2 groups (sum_squares and the xor-shuffle tree over head_dim/8 lanes) and the rounding are
 // those of the chain kernels, so a chain gives their results bit for bit; snapshots and the state
 // are the staged raw bits.  Units whose buffers do not allow 16-byte
@@ -252,7 +252,7 @@ __global__ void __launch_bounds__(128, 4) verify_tree(const __grid_constant__ Ve
                     }
                     acc[e] = conv_chain<B, W>(bs[e], wt, v);
                 }
-                silu_run<8>(acc, y);  // (one range check for the token's 8 channels)
+                silu_run<8>(acc, y);  // (one range check for the token's 8 channels, exact form per value)
                 // snapshot t = window(t): the last R inputs (raw bits)
                 if (win_vec) {
                     union { uint4 v[R * NV]; B b[8 * R]; } u;

@@ -33,7 +33,8 @@ def test_exports_every_declared_function(lib):
     assert {"cv_conv_verify", "cv_conv_commit", "cv_verify_plan", "cv_status_string", "cv_abi_version"} <= set(names)
     for n in names:
         assert hasattr(lib, n), f"{n} declared in the header but not exported"
-    assert lib.cv_abi_version() == 4
+    version = int(re.search(r"#define CV_ABI_VERSION (\d+)", open(HEADER).read()).group(1))
+    assert lib.cv_abi_version() == version
 
 
 def test_exports_nothing_undeclared(lib):
@@ -457,3 +458,31 @@ def test_binding_commit_and_prefill_shapes():
     with pytest.raises(ValueError):
         cv.make_prefill_args(p["x"], p["conv_state"], p["weight"], p["bias"], p["out"], p["cu_seqlens"],
                              cache_idx=torch.zeros(p["cu_seqlens"].numel() - 2, dtype=torch.int32), **kw)
+
+
+def test_struct_layouts_match_header(tmp_path):
+    """The binding's ctypes mirrors have the C structs' field offsets and sizes (a field added to
+    the header but not to the binding, or the reverse, would shift every later field)."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    mirrors = {"cv_verify_args": cv.VerifyArgs, "cv_commit_args": cv.CommitArgs,
+               "cv_prefill_args": cv.PrefillArgs, "cv_launch_plan": cv.LaunchPlan}
+    lines = ["#include <stddef.h>", "#include <stdio.h>", f'#include "{HEADER}"', "int main(void) {"]
+    for cname, py in mirrors.items():
+        lines.append(f'printf("{cname} size %zu\\n", sizeof({cname}));')
+        for fname, _ in py._fields_:
+            lines.append(f'printf("{cname} {fname} %zu\\n", offsetof({cname}, {fname}));')
+    lines += ["return 0;", "}"]
+    src = tmp_path / "layout.c"
+    src.write_text("\n".join(lines))
+    exe = tmp_path / "layout"
+    subprocess.run([cc, "-std=c99", "-o", str(exe), str(src)], check=True)
+    got = subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split("\n")
+    c_side = {tuple(ln.split()[:2]): int(ln.split()[2]) for ln in got if ln.strip()}
+    for cname, py in mirrors.items():
+        assert c_side[(cname, "size")] == ctypes.sizeof(py), f"{cname}: sizeof differs"
+        for fname, _ in py._fields_:
+            assert c_side[(cname, fname)] == getattr(py, fname).offset, f"{cname}.{fname}: offset differs"
