@@ -200,6 +200,19 @@ def e2e_pipelined(dev, dist, K, sets, inp, launch, ins, outs):
     return reduce_max(dist, e0.elapsed_time(e1) * 1e3 / K, dev), h2d, d2h
 
 
+def launch_ranks(n: int) -> int:
+    """Run this same command as n ranks under torch.distributed.run (one node, one rank per GPU,
+    rendezvous on 127.0.0.1) and return its exit status.  Used when --gpus N > 1 is given without a
+    launcher, so that an N-GPU line always comes from N ranks."""
+    import socket
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        port = sk.getsockname()[1]
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes", "1", "--nproc-per-node", str(n),
+           "--master-addr", "127.0.0.1", "--master-port", str(port), os.path.abspath(__file__), *sys.argv[1:]]
+    return subprocess.run(cmd).returncode
+
+
 def dist_setup():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -267,7 +280,7 @@ def run_reference(args, w, world, rank):
         "impl": "reference", "metric": METRIC, "value": round(us, 3), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(us / 1e3, 6), "higher_is_better": False,
         "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
-        "config": workload_config(w, None),
+        "config": workload_config(w),
         "cpu_baseline": {"value": round(us, 3), "unit": UNIT, "cores": 1, "kind": "oracle",
                          "sample": f"whole workload ({w.n_seq} sequences) per step, {len(times)} steps after "
                                    f"{len(warm)} warm-up; plain C loop, one thread"},
@@ -278,13 +291,16 @@ def run_reference(args, w, world, rank):
     return 0
 
 
-def workload_config(w, l2_note):
-    c = {"workload": w.name, "n_seq": w.n_seq, "padded_seqs": w.n_pad, "T": w.T, "dim": w.dim, "width": w.width,
-         "qk_channels": w.qk_channels, "head_dim": w.head_dim, "layout": w.layout, "bias": w.bias,
-         "step": "cv_conv_verify" if w.layout == "history" else "cv_conv_verify + cv_conv_commit"}
-    if l2_note:
-        c["l2"] = l2_note
-    return c
+# How the GPU arm keeps each step out of L2 (both arms' config carries it, so the two configs are
+# identical; the GPU arm's line adds the set count and sizes under "l2_sets").
+L2_RULE = "inputs larger than L2: every step uses the next of rotating buffer sets totalling >= 4x L2"
+
+
+def workload_config(w):
+    return {"workload": w.name, "n_seq": w.n_seq, "padded_seqs": w.n_pad, "T": w.T, "dim": w.dim, "width": w.width,
+            "qk_channels": w.qk_channels, "head_dim": w.head_dim, "layout": w.layout, "bias": w.bias,
+            "step": "cv_conv_verify" if w.layout == "history" else "cv_conv_verify + cv_conv_commit",
+            "l2": L2_RULE}
 
 
 # ----------------------------------------------------------------------------- GPU arm
@@ -418,7 +434,7 @@ def run_ours(args, w, world, rank, local, dist):
         "metric": METRIC, "value": round(step_us_max, 3), "unit": UNIT, "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": round(step_us_max / 1e3, 6), "higher_is_better": False,
         "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
-        "config": workload_config(w, l2_note),
+        "config": workload_config(w), "l2_sets": l2_note,
         "verify_us": round(verify_us_max, 3), "commit_us": round(commit_us, 3),
         "verify_gbs": round(achieved, 1), "verify_frac_of_8tbs": round(achieved / HBM_NOMINAL_GBS, 4),
         "verify_algorithmic_bytes": nbytes["verify"], "commit_algorithmic_bytes": nbytes["commit"],
@@ -442,13 +458,11 @@ def run_ours(args, w, world, rank, local, dist):
 
 # ----------------------------------------------------------------------------- prefill workloads
 
-def prefill_config(w, l2_note):
-    c = {"workload": w.name, "n_seq": w.n_seq, "total_tokens": w.total_tokens, "max_seqlen": w.max_seqlen,
-         "dim": w.dim, "width": w.width, "qk_channels": w.qk_channels, "head_dim": w.head_dim,
-         "padded_seqs": len(w.pad), "without_initial_state": len(w.no_init), "step": "cv_conv_prefill"}
-    if l2_note:
-        c["l2"] = l2_note
-    return c
+def prefill_config(w):
+    return {"workload": w.name, "n_seq": w.n_seq, "total_tokens": w.total_tokens, "max_seqlen": w.max_seqlen,
+            "dim": w.dim, "width": w.width, "qk_channels": w.qk_channels, "head_dim": w.head_dim,
+            "padded_seqs": len(w.pad), "without_initial_state": len(w.no_init), "step": "cv_conv_prefill",
+            "l2": L2_RULE}
 
 
 def oracle_prefill_times(w, reps_max: int, budget_s: float):
@@ -481,7 +495,7 @@ def run_reference_prefill(args, w, world, rank):
         "impl": "reference", "metric": METRIC, "value": round(us, 3), "unit": UNIT, "n_gpus": world,
         "steps": len(times), "warmup": len(warm), "ms_per_step": round(us / 1e3, 6), "higher_is_better": False,
         "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
-        "config": prefill_config(w, None),
+        "config": prefill_config(w),
         "cpu_baseline": {"value": round(us, 3), "unit": UNIT, "cores": 1, "kind": "oracle",
                          "sample": f"whole workload ({w.total_tokens} tokens) per step, {len(times)} steps; "
                                    f"plain C loop, one thread"},
@@ -568,7 +582,7 @@ def run_ours_prefill(args, w, world, rank, local, dist):
         "metric": METRIC, "value": round(step_us, 3), "unit": UNIT, "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": round(step_us / 1e3, 6), "higher_is_better": False,
         "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
-        "config": prefill_config(w, l2_note),
+        "config": prefill_config(w), "l2_sets": l2_note,
         "prefill_us": round(step_us, 3), "prefill_gbs": round(achieved, 1), "prefill_algorithmic_bytes": nbytes,
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic, "kernel": "prefill_conv",
@@ -587,6 +601,79 @@ def run_ours_prefill(args, w, world, rank, local, dist):
     return 0
 
 
+# ----------------------------------------------------------------------------- bandwidth probe
+
+PROBE_MIXES = [(1, 0), (0, 1), (1, 1), (2, 1), (1, 2), (10, 19), (1, 3)]
+
+
+def run_probe_mix(args):
+    """HBM bandwidth of read:write mixes (libcvprobe.so, 16-byte vector streams): the roofline the
+    verify's own mix (about 1:1.9) can reach, against the 1:1 copy of the measured peak.  Each mix is
+    timed like the verify: K launches back to back between two CUDA events, every launch on the
+    next of several buffer sets totalling >= 4x L2, each launch moving `--probe-mb` MB.  Prints one
+    JSON line per mix."""
+    from spec_decode_verify_gb300 import build as cvbuild
+    cvbuild.build()
+    lib = ctypes.CDLL(cvbuild.PROBE_LIB)
+    lib.cv_probe_mix.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_longlong, ctypes.c_int, ctypes.c_int,
+                                 ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p]
+    lib.cv_probe_mix.restype = ctypes.c_int
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    props = torch.cuda.get_device_properties(dev)
+    sms = props.multi_processor_count
+    l2 = getattr(props, "L2_cache_size", 0) or 129 * 2 ** 20
+    threads = 256
+    blocks = sms * (2048 // threads)
+    sp = torch.cuda.current_stream(dev).cuda_stream
+    sink = torch.empty(blocks * threads * 16, dtype=torch.uint8, device=dev)
+    peak, peak_kind = measured_peak()
+    sampler = ClockSampler(dev.index, args.clocks_csv)
+    sampler.start()
+    lines = []
+    mixes = PROBE_MIXES if not args.probe_mixes else [tuple(int(v) for v in m.split(":")) for m in args.probe_mixes.split(",")]
+    for r, w in mixes:
+        unit = 16 * (r + w)
+        n_units = int(args.probe_mb * 1e6) // unit
+        per_set = n_units * unit
+        n_sets = max(2, math.ceil(4 * l2 / per_set))
+        sets = [(torch.empty(max(r, 1) * n_units * 16, dtype=torch.uint8, device=dev),
+                 torch.empty(max(w, 1) * n_units * 16, dtype=torch.uint8, device=dev)) for _ in range(n_sets)]
+        for src, dst in sets:
+            src.random_(0, 256)
+
+        def launch(i):
+            src, dst = sets[i % n_sets]
+            rc = lib.cv_probe_mix(src.data_ptr(), dst.data_ptr(), n_units, r, w, blocks, threads, sink.data_ptr(), sp)
+            if rc != 0:
+                raise RuntimeError(f"cv_probe_mix({r},{w}) failed: CUDA error {rc}")
+
+        for i in range(max(args.warmup, 3) * n_sets):
+            launch(i)
+        torch.cuda.synchronize(dev)
+        K = args.steps
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda._sleep(int(min(2e9, 40000 * K + 2e6)))
+        e0.record()
+        for i in range(K):
+            launch(i)
+        e1.record()
+        torch.cuda.synchronize(dev)
+        us = e0.elapsed_time(e1) * 1e3 / K
+        gbs = per_set / (us * 1e-6) / 1e9
+        lines.append({"probe": "mix", "read": r, "write": w, "bytes_per_launch": per_set, "us_per_launch": round(us, 3),
+                      "gbs": round(gbs, 1), "frac_of_copy_peak": round(gbs / peak, 4), "peak": peak,
+                      "peak_source": f"{peak_kind} hbm_gbs (copy)", "grid": [blocks, threads], "sets": n_sets,
+                      "steps": K})
+        del sets
+        torch.cuda.empty_cache()
+    clocks = sampler.stop()
+    for ln in lines:
+        ln["clocks"] = clocks
+        print(json.dumps(ln), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -599,9 +686,21 @@ def main():
     ap.add_argument("--clocks-csv", default=None, help="keep the raw nvidia-smi clock samples in this file")
     ap.add_argument("--clock-probe-s", type=float, default=1.5)
     ap.add_argument("--cpu-budget-s", type=float, default=10.0)
+    ap.add_argument("--probe-mix", action="store_true",
+                    help="time read:write bandwidth mixes (the verify's roofline) instead of the path")
+    ap.add_argument("--probe-mb", type=float, default=75.4, help="MB moved per probe launch")
+    ap.add_argument("--probe-mixes", default="", help="read:write mixes to time, e.g. 10:19,1:1 (default: all)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
+    if args.probe_mix:
+        return run_probe_mix(args)
+    if args.gpus < 1:
+        ap.error("--gpus must be at least 1")
+    if "WORLD_SIZE" not in os.environ and args.gpus > 1:
+        return launch_ranks(args.gpus)
+    if int(os.environ.get("WORLD_SIZE", "1")) != args.gpus:
+        ap.error(f"--gpus {args.gpus} does not match WORLD_SIZE {os.environ.get('WORLD_SIZE')}")
     world, rank, local, dist = dist_setup()
     try:
         if args.workload in wl.PREFILL_WORKLOADS:

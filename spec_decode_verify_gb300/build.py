@@ -1,4 +1,5 @@
-"""Build the CUDA library in-tree: spec_decode_verify_gb300/_build/libconvverify.so (sm_103a only).
+"""Build the CUDA library in-tree: spec_decode_verify_gb300/_build/libconvverify.so (sm_103a only),
+and beside it libcvprobe.so, the bandwidth probe bench.py --probe-mix times.
 
 Run as ``python -m spec_decode_verify_gb300.build``; ``__graft_entry__.build()`` calls it too.
 """
@@ -16,7 +17,9 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libconvverify.so")
 INCLUDE = os.path.join(ROOT, "include")
-SOURCES = ["cv_abi.cu"] + [f"cv_inst_{d}_w{w}.cu" for d in ("bf16", "f32") for w in (2, 3, 4)]
+# the verify library, then (last) the bandwidth probe of bench.py --probe-mix, linked on its own
+SOURCES = ["cv_abi.cu"] + [f"cv_inst_{d}_w{w}.cu" for d in ("bf16", "f32") for w in (2, 3, 4)] + ["cv_probe.cu"]
+PROBE_LIB = os.path.join(BUILD, "libcvprobe.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
               "-I", INCLUDE, "-I", CSRC]
@@ -30,9 +33,9 @@ def nvcc() -> str:
 
 
 def _stale() -> bool:
-    if not os.path.exists(LIB):
+    if not os.path.exists(LIB) or not os.path.exists(PROBE_LIB):
         return True
-    t = os.path.getmtime(LIB)
+    t = min(os.path.getmtime(LIB), os.path.getmtime(PROBE_LIB))
     deps = [os.path.join(CSRC, f) for f in os.listdir(CSRC)] + [os.path.join(INCLUDE, f) for f in os.listdir(INCLUDE)]
     return any(os.path.getmtime(d) > t for d in deps)
 
@@ -56,12 +59,14 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
 
     with cf.ThreadPoolExecutor(max_workers=min(8, len(SOURCES))) as ex:
         objs = list(ex.map(compile_one, SOURCES))
-    tmp = LIB + f".{os.getpid()}.tmp"
-    cmd = [cc, *ARCH, "-shared", "-o", tmp, *objs, "-lcudart"]
-    r = subprocess.run(cmd, capture_output=True, text=True)
-    if r.returncode != 0:
-        raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
+    probe_obj = objs.pop()  # the bandwidth probe goes into its own library
+    for lib, parts in ((LIB, objs), (PROBE_LIB, [probe_obj])):
+        tmp = lib + f".{os.getpid()}.tmp"
+        cmd = [cc, *ARCH, "-shared", "-o", tmp, *parts, "-lcudart"]
+        r = subprocess.run(cmd, capture_output=True, text=True)
+        if r.returncode != 0:
+            raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
+        os.replace(tmp, lib)
     return LIB
 
 

@@ -1,0 +1,201 @@
+"""GPU parity where conv results reach far below zero: x and the state scaled by 200, so about a
+fifth of the conv results fall below -80 and most of those past -88.7, where exp(-acc) overflows
+fp32.  There every kernel takes SiLU's exact form for each such value (the fast approximations
+flush subnormals), so this file runs that branch on every launch path -- pipelined, static-T,
+chunked, general, tree, mixed-dtype and prefill -- and checks it against the oracle: snapshots and
+state bitwise, outputs within the output tolerance (bf16 with the absolute floor at the exp
+overflow point, where two correct expf implementations may disagree on overflowing), and the same
+output bits from every path.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+import torch.nn.functional as F
+
+import oracle
+from gpu_helpers import run_gpu_commit, run_gpu_verify, to_device
+from helpers import (BF16_EXP_OVERFLOW_FLOOR, assert_bits_equal, assert_out_close, clone_inputs, run_oracle_commit,
+                     run_oracle_verify)
+from spec_decode_verify_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+SCALE = 200.0
+
+
+def scale_(inp, keys=("x_base", "conv_state")):
+    """Multiply the inputs by SCALE in place (x is a view of x_base, so it follows)."""
+    for k in keys:
+        t = inp[k]
+        t.copy_((t.double() * SCALE).to(t.dtype))
+    return inp
+
+
+def close(got, ref, what):
+    assert_out_close(got, ref, what, bf16_floor=BF16_EXP_OVERFLOW_FLOOR)
+
+
+def share_below(w, inp, seqs=4):
+    """Share of conv results below -80 over the first active sequences (float64 conv1d)."""
+    below = total = 0
+    R = w.width - 1
+    for s in range(w.n_seq):
+        slot = int(inp["cache_idx"][s])
+        if slot < 0:
+            continue
+        off = int(inp["state_off"][s]) if inp.get("state_off") is not None else 0
+        full = torch.cat([inp["conv_state"][slot, :, off:off + R].double(), inp["x"][s].double().t()], dim=1)
+        bias = inp["bias"].double() if inp["bias"] is not None else None
+        acc = F.conv1d(full[None], inp["weight"].double()[:, None, :], bias, groups=w.dim)[0]
+        below += int((acc < -80).sum())
+        total += acc.numel()
+        seqs -= 1
+        if seqs == 0:
+            break
+    return below / max(total, 1)
+
+
+def check(cv, w, inp, commit=True):
+    ref = run_oracle_verify(w, inp)
+    got = run_gpu_verify(cv, w, inp)
+    assert_bits_equal(got["err"].cpu(), ref["status"], "err")
+    if inp.get("window") is not None:
+        assert_bits_equal(got["window"].cpu(), ref["window"], "window")
+    assert_bits_equal(got["conv_state"].cpu(), ref["conv_state"], "state")
+    close(got["out"].cpu(), ref["out"], "out")
+    if commit and w.layout != "history":
+        st_ref = run_oracle_commit(w, ref)
+        st_got = run_gpu_commit(cv, w, got)
+        assert_bits_equal(st_got.cpu(), st_ref, "commit err")
+        assert_bits_equal(got["conv_state"].cpu(), ref["conv_state"], "committed state")
+    return ref, got
+
+
+def _run_view(cv, w, inp, state_dev, x_dev):
+    d = to_device(inp)
+    d["conv_state"] = state_dev
+    d["x"] = x_dev
+    d["err"] = torch.zeros(w.n_seq, dtype=torch.int32, device="cuda")
+    plan = cv.verify_plan(d["x"], d["conv_state"], d["weight"], d["bias"], d["out"], d["window"], layout=w.layout,
+                          qk_channels=w.qk_channels, head_dim=w.head_dim, cache_idx=d["cache_idx"])
+    cv.conv_verify(d["x"], d["conv_state"], d["weight"], d["bias"], d["out"], d["window"], layout=w.layout,
+                   qk_channels=w.qk_channels, head_dim=w.head_dim, cache_idx=d["cache_idx"], err=d["err"])
+    torch.cuda.synchronize()
+    return plan.path, d
+
+
+@pytest.mark.parametrize("layout", ["dense", "dedup"])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_extreme_values_all_paths(cuda_lib, layout, dtype):
+    """The same scaled inputs through the pipelined kernel (packed state rows, and rows one column
+    wider staged whole), the static-T kernel (rows with a gap) and the general kernel (x off
+    16-byte alignment): the oracle's snapshots and state bitwise, its outputs within tolerance, and
+    the same output bits from all four."""
+    w = wl.VerifyWorkload("extreme", n_seq=420, T=6, dim=1536, width=4, qk_channels=512, head_dim=128, dtype=dtype,
+                          layout=layout, bias=True, n_pad=7, extra_slots=2, seed=41)
+    inp = scale_(wl.make_inputs(w))
+    assert share_below(w, inp) > 0.1
+    ref = run_oracle_verify(w, inp)
+    R = w.width - 1
+    p3, d3 = _run_view(cuda_lib, w, inp, inp["conv_state"].cuda(), to_device(inp)["x"])
+    wide = wl.sentinel_tensor((w.n_slots, w.dim, R + 1), w.torch_dtype)
+    wide[:, :, :R] = inp["conv_state"]
+    p3w, d3w = _run_view(cuda_lib, w, inp, wide.cuda(), to_device(inp)["x"])
+    gap = wl.sentinel_tensor((w.n_slots, w.dim, R + 2), w.torch_dtype)
+    gap[:, :, :R] = inp["conv_state"]
+    p1, d1 = _run_view(cuda_lib, w, inp, gap.cuda()[:, :, :R + 1], to_device(inp)["x"])
+    xb = torch.zeros(w.n_seq * w.T * w.dim + 1, dtype=w.torch_dtype)
+    xb[1:] = inp["x"].reshape(-1)
+    p0, d0 = _run_view(cuda_lib, w, inp, inp["conv_state"].cuda(), xb.cuda()[1:].view(w.n_seq, w.T, w.dim))
+    assert (p3, p3w, p1, p0) == (3, 3, 1, 0)
+    for name, d in (("pipelined", d3), ("pipelined wide", d3w), ("static", d1), ("general", d0)):
+        close(d["out"].cpu(), ref["out"], f"out {name}")
+        assert_bits_equal(d["out"].cpu(), d3["out"].cpu(), f"out {name} vs pipelined")
+        assert_bits_equal(d["window"].cpu(), ref["window"], f"window {name}")
+    assert_bits_equal(d3["conv_state"].cpu(), ref["conv_state"], "state pipelined")
+    assert_bits_equal(d0["conv_state"].cpu(), ref["conv_state"], "state general")
+    assert_bits_equal(d3w["conv_state"][:, :, :R].cpu(), ref["conv_state"], "state pipelined wide")
+    assert_bits_equal(d1["conv_state"][:, :, :R].cpu(), ref["conv_state"], "state static")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_extreme_values_chunked_long_T(cuda_lib, dtype):
+    """A dense window with T beyond the static range (the chunked kernel, 4 tokens at a time)."""
+    w = wl.VerifyWorkload("extreme_long", n_seq=3, T=24, dim=1024, width=4, qk_channels=256, head_dim=64,
+                          dtype=dtype, layout="dense", bias=True, seed=42)
+    inp = scale_(wl.make_inputs(w))
+    assert share_below(w, inp) > 0.1
+    check(cuda_lib, w, inp)
+
+
+@pytest.mark.parametrize("name", ["n128_t8_dim10240_w4_bf16_dedup_pad13", "n128_t8_dim10240_w4_bf16_history_pad13",
+                                  "n128_t8_dim10240_w4_bf16_recompute_pad13",
+                                  "n64_t8_dim6144_w3_bf16_dense_nol2_stateoff"])
+def test_extreme_values_named_shapes(cuda_lib, name):
+    """The benchmark shape in the dedup, history and recompute layouts, and the width-3 shape
+    with state offsets, all with scaled inputs."""
+    w = wl.WORKLOADS[name]
+    inp = scale_(wl.make_inputs(w))
+    assert share_below(w, inp) > 0.1
+    check(cuda_lib, w, inp)
+
+
+@pytest.mark.parametrize("xd,sd", [("bf16", "f32"), ("f32", "bf16")])
+@pytest.mark.parametrize("T", [8, 12])
+def test_extreme_values_mixed_dtypes(cuda_lib, xd, sd, T):
+    """Mixed dtypes on the pipelined kernel (T 8) and on the general kernel (T 12)."""
+    w = wl.VerifyWorkload("extreme_mixed", n_seq=40, T=T, dim=2048, width=4, qk_channels=1024, head_dim=128,
+                          dtype=xd, state_dtype=sd, layout="dedup", n_pad=3, extra_slots=3, seed=43)
+    inp = scale_(wl.make_inputs(w))
+    check(cuda_lib, w, inp)
+
+
+def test_extreme_values_tree(cuda_lib):
+    """Tree verify with random parents against the oracle, and with chain parents bit for bit equal
+    to the plain verify (both with scaled inputs)."""
+    w = wl.VerifyWorkload("extreme_tree", n_seq=24, T=8, dim=2048, width=4, qk_channels=1024, head_dim=128,
+                          dtype="bf16", layout="dense", n_pad=2, extra_slots=2, tree=True, seed=44)
+    inp = scale_(wl.make_inputs(w))
+    check(cuda_lib, w, inp)
+    chain = torch.arange(-1, w.T - 1, dtype=torch.int32).repeat(w.n_seq, 1).contiguous()
+    inp_chain = dict(inp, parent=chain)
+    got_tree = run_gpu_verify(cuda_lib, w, inp_chain)
+    plain = dict(inp)
+    plain.pop("parent")
+    got_plain = run_gpu_verify(cuda_lib, w.replace(tree=False), plain)
+    assert_bits_equal(got_tree["out"].cpu(), got_plain["out"].cpu(), "tree with chain parents vs plain verify")
+    assert_bits_equal(got_tree["window"].cpu(), got_plain["window"].cpu(), "snapshots")
+
+
+def test_extreme_values_prefill(cuda_lib):
+    """The prefill kernel on scaled prompts: the oracle's state bitwise and outputs within tolerance,
+    and the GPU verify over the same tokens gives the same bits."""
+    T = 17
+    w = wl.PrefillWorkload("extreme_prefill", lengths=(T, T, T), dim=4096, width=4, qk_channels=2048, head_dim=128,
+                           dtype="bf16", bias=True, seed=45)
+    inp = scale_(wl.make_prefill_inputs(w))
+    ref = {k: (v.clone() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    ref["x"] = inp["x"]
+    ref["status"] = torch.full((w.n_seq,), -7, dtype=torch.int32)
+    oracle.conv_prefill(ref["x"], ref["conv_state"], ref["weight"], ref["bias"], ref["out"], ref["cu_seqlens"],
+                        qk_channels=w.qk_channels, head_dim=w.head_dim, l2_eps=w.l2_eps, cache_idx=ref["cache_idx"],
+                        has_initial_state=ref["has_initial_state"], status=ref["status"])
+    dev = torch.device("cuda")
+    d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    d["x"] = d["x_base"][: w.total_tokens]
+    cuda_lib.conv_prefill(d["x"], d["conv_state"], d["weight"], d["bias"], d["out"], d["cu_seqlens"],
+                          max_seqlen=w.max_seqlen, qk_channels=w.qk_channels, head_dim=w.head_dim,
+                          cache_idx=d["cache_idx"], has_initial_state=d["has_initial_state"])
+    torch.cuda.synchronize()
+    assert_bits_equal(d["conv_state"].cpu(), ref["conv_state"], "prefill state")
+    close(d["out"].cpu(), ref["out"], "prefill out")
+    xv = inp["x"].reshape(3, T, w.dim).to(dev)
+    st = inp["conv_state"].to(dev)
+    out = torch.empty(3, T, w.dim, dtype=w.torch_dtype, device=dev)
+    win = torch.empty(3, T, w.dim, w.width - 1, dtype=w.torch_dtype, device=dev)
+    cuda_lib.conv_verify(xv, st, inp["weight"].to(dev), inp["bias"].to(dev), out, win, layout="dense",
+                         qk_channels=w.qk_channels, head_dim=w.head_dim, cache_idx=inp["cache_idx"].to(dev))
+    torch.cuda.synchronize()
+    assert_bits_equal(d["out"].cpu(), out.reshape(3 * T, w.dim).cpu(), "prefill vs verify out")

@@ -72,3 +72,40 @@ def test_reference_arm_other_ranks_exit_without_work(monkeypatch):
 
     # rank 1 of 2 returns 0 immediately and prints nothing
     assert bench.run_reference(Args, wl.WORKLOADS[bench.wl.BENCH_WORKLOAD], 2, 1) == 0
+
+
+def _bench_env():
+    env = {k: v for k, v in os.environ.items()
+           if k not in ("WORLD_SIZE", "RANK", "LOCAL_RANK", "MASTER_ADDR", "MASTER_PORT")}
+    env["CUDA_VISIBLE_DEVICES"] = ""  # the CPU path of the launcher (gloo), even on a GPU host
+    return env
+
+
+def test_bench_gpus_n_launches_n_ranks():
+    """`bench.py --gpus 2` without a launcher starts two ranks itself (torch.distributed.run, gloo
+    on CPU): the one JSON line comes from rank 0 and reports n_gpus 2 (the reference arm, which
+    runs on the CPU)."""
+    import json
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--impl", "reference", "--gpus", "2",
+                        "--steps", "1", "--warmup", "3", "--workload", "n1_t2_dim512_w4_f32_dense"],
+                       capture_output=True, text=True, env=_bench_env(), timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [json.loads(ln) for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1, r.stdout
+    assert lines[0]["n_gpus"] == 2 and lines[0]["impl"] == "reference"
+
+
+def test_bench_gpus_must_match_world_size():
+    """Under a launcher, --gpus must equal WORLD_SIZE (an N-GPU line never comes from fewer ranks)."""
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = _bench_env()
+    env.update(WORLD_SIZE="1", RANK="0", LOCAL_RANK="0")
+    r = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--impl", "reference", "--gpus", "2",
+                        "--steps", "1", "--warmup", "3", "--workload", "n1_t2_dim512_w4_f32_dense"],
+                       capture_output=True, text=True, env=env, timeout=300)
+    assert r.returncode != 0 and "does not match WORLD_SIZE" in r.stderr
