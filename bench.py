@@ -624,17 +624,19 @@ def run_probe_mix(args):
     sms = props.multi_processor_count
     l2 = getattr(props, "L2_cache_size", 0) or 129 * 2 ** 20
     threads = 256
-    blocks = sms * (2048 // threads)
     sp = torch.cuda.current_stream(dev).cuda_stream
-    sink = torch.empty(blocks * threads * 16, dtype=torch.uint8, device=dev)
+    sink = torch.empty(sms * 2048 * 16, dtype=torch.uint8, device=dev)
     peak, peak_kind = measured_peak()
     sampler = ClockSampler(dev.index, args.clocks_csv)
     sampler.start()
     lines = []
     mixes = PROBE_MIXES if not args.probe_mixes else [tuple(int(v) for v in m.split(":")) for m in args.probe_mixes.split(",")]
-    for r, w in mixes:
+    sizes = [float(v) for v in str(args.probe_mb).split(",")]
+    bpsms = [int(v) for v in str(args.probe_bpsm).split(",")]
+    for (r, w), mb, bpsm in [(m, mb, b) for m in mixes for mb in sizes for b in bpsms]:
+        blocks = sms * bpsm
         unit = 16 * (r + w)
-        n_units = int(args.probe_mb * 1e6) // unit
+        n_units = int(mb * 1e6) // unit
         per_set = n_units * unit
         n_sets = max(2, math.ceil(4 * l2 / per_set))
         sets = [(torch.empty(max(r, 1) * n_units * 16, dtype=torch.uint8, device=dev),
@@ -688,7 +690,8 @@ def main():
     ap.add_argument("--cpu-budget-s", type=float, default=10.0)
     ap.add_argument("--probe-mix", action="store_true",
                     help="time read:write bandwidth mixes (the verify's roofline) instead of the path")
-    ap.add_argument("--probe-mb", type=float, default=75.4, help="MB moved per probe launch")
+    ap.add_argument("--probe-mb", default="75.4", help="MB moved per probe launch (comma list)")
+    ap.add_argument("--probe-bpsm", default="8", help="probe blocks of 256 threads per SM (comma list)")
     ap.add_argument("--probe-mixes", default="", help="read:write mixes to time, e.g. 10:19,1:1 (default: all)")
     args = ap.parse_args()
     if args.warmup < 3:

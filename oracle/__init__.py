@@ -35,7 +35,7 @@ class _VerifyArgs(ctypes.Structure):
         ("cache_idx", c_vp), ("state_off", c_vp), ("weight", c_vp), ("bias", c_vp),
         ("window", c_vp), ("dedup", c_i32), ("w_seq", c_i64), ("w_step", c_i64), ("w_ch", c_i64),
         ("w_col", c_i64), ("status", c_vp), ("history", c_i32), ("recompute", c_i32), ("state_is_bf16", c_i32),
-        ("parent", c_vp),
+        ("parent", c_vp), ("cu_draft", c_vp), ("total_tokens", c_i32),
     ]
 
 
@@ -45,7 +45,7 @@ class _CommitArgs(ctypes.Structure):
         ("state", c_vp), ("n_slots", c_i32), ("st_slot", c_i64), ("st_ch", c_i64), ("cache_idx", c_vp),
         ("window", c_vp), ("dedup", c_i32), ("w_seq", c_i64), ("w_step", c_i64), ("w_ch", c_i64),
         ("w_col", c_i64), ("accept_len", c_vp), ("status", c_vp), ("recompute", c_i32), ("x", c_vp),
-        ("x_seq", c_i64), ("x_tok", c_i64),
+        ("x_seq", c_i64), ("x_tok", c_i64), ("cu_draft", c_vp), ("total_tokens", c_i32),
     ]
 
 
@@ -135,7 +135,7 @@ def window_strides(window: torch.Tensor, layout: str):
 
 
 def conv_verify(x, conv_state, weight, bias, out, window, *, layout, qk_channels, head_dim, l2_eps,
-                cache_idx=None, state_off=None, status=None, parent=None):
+                cache_idx=None, state_off=None, status=None, parent=None, cu_draft=None, T=None):
     """Run the oracle verify in place on CPU tensors (conv_state, out, window, status are written).
 
     x [n_seq, T, dim] (channel stride 1), conv_state [n_slots, dim, S] (column stride 1),
@@ -143,27 +143,43 @@ def conv_verify(x, conv_state, weight, bias, out, window, *, layout, qk_channels
     window dense [n_seq, T, dim, W-1] / dedup [n_seq, dim, T+W-2] / None for the history layout
     (the state row, S >= T+W-2 columns, receives the snapshot row) and the recompute layout
     (outputs only, state untouched); cache_idx, state_off, status int32 [n_seq] or None; parent
-    int32 [n_seq, T] contiguous (tree verify, dense layout only) or None (a chain)."""
+    int32 [n_seq, T] contiguous (tree verify, dense layout only) or None (a chain).
+
+    Packed ragged drafts: cu_draft int32 [n_seq + 1]; x and out are then [total_tokens, dim]
+    (sequence s owns rows cu_draft[s] .. cu_draft[s+1]-1) and T (required) is the largest draft
+    count, the T of the window buffer."""
     if parent is not None:
         assert layout == "dense" and parent.is_contiguous() and parent.dtype == torch.int32
     if layout not in ("dense", "dedup", "history", "recompute"):
         raise ValueError(f"unknown layout {layout!r}")
     if (layout in ("history", "recompute")) != (window is None):
         raise ValueError("the history and recompute layouts take no window buffer; the others need one")
-    n_seq, T, dim = x.shape
+    if cu_draft is not None:
+        assert cu_draft.dtype == torch.int32 and cu_draft.is_contiguous() and T is not None
+        assert parent is None, "packed ragged drafts are chains"
+        total, dim = x.shape
+        n_seq = cu_draft.shape[0] - 1
+        assert x.stride(1) == 1 and out.stride(1) == 1 and tuple(out.shape) == (total, dim)
+        x_seq, x_tok, o_seq, o_tok = 0, x.stride(0), 0, out.stride(0)
+    else:
+        n_seq, T, dim = x.shape
+        total = 0
+        assert x.stride(2) == 1 and out.stride(2) == 1
+        x_seq, x_tok, o_seq, o_tok = x.stride(0), x.stride(1), out.stride(0), out.stride(1)
     W = weight.shape[1]
-    assert x.stride(2) == 1 and out.stride(2) == 1 and conv_state.stride(2) == 1
+    assert conv_state.stride(2) == 1
     assert weight.is_contiguous()
     ws = window_strides(window, layout)
     a = _VerifyArgs(
         n_seq=n_seq, T=T, dim=dim, width=W, qk_channels=qk_channels, head_dim=head_dim, is_bf16=_is_bf16(x),
-        l2_eps=l2_eps, x=_ptr(x), x_seq=x.stride(0), x_tok=x.stride(1), out=_ptr(out),
-        out_seq=out.stride(0), out_tok=out.stride(1), state=_ptr(conv_state), n_slots=conv_state.shape[0],
+        l2_eps=l2_eps, x=_ptr(x), x_seq=x_seq, x_tok=x_tok, out=_ptr(out),
+        out_seq=o_seq, out_tok=o_tok, state=_ptr(conv_state), n_slots=conv_state.shape[0],
         state_cols=conv_state.shape[2], st_slot=conv_state.stride(0), st_ch=conv_state.stride(1),
         cache_idx=_ptr(cache_idx), state_off=_ptr(state_off), weight=_ptr(weight), bias=_ptr(bias),
         window=_ptr(window), dedup=1 if layout == "dedup" else 0, w_seq=ws[0], w_step=ws[1], w_ch=ws[2],
         w_col=ws[3], status=_ptr(status), history=1 if layout == "history" else 0,
-        recompute=1 if layout == "recompute" else 0, state_is_bf16=_is_bf16(conv_state), parent=_ptr(parent))
+        recompute=1 if layout == "recompute" else 0, state_is_bf16=_is_bf16(conv_state), parent=_ptr(parent),
+        cu_draft=_ptr(cu_draft), total_tokens=total)
     if window is not None and window.dtype != conv_state.dtype:
         raise TypeError("the window has the state's dtype")
     rc = _load().oracle_conv_verify(ctypes.byref(a))
@@ -171,15 +187,22 @@ def conv_verify(x, conv_state, weight, bias, out, window, *, layout, qk_channels
         raise RuntimeError(f"oracle_conv_verify returned {rc}")
 
 
-def conv_commit(conv_state, window, accept_len, *, layout, T, width, cache_idx=None, status=None, x=None):
+def conv_commit(conv_state, window, accept_len, *, layout, T, width, cache_idx=None, status=None, x=None,
+                cu_draft=None, total_tokens=0):
     """Run the oracle commit in place: state slot of seq s <- snapshot accept_len[s]-1.
 
     layout "recompute": window is None and x [n_seq, T, dim] (channel stride 1) is the verify's
-    input; the snapshot is rebuilt from the state's window and x."""
+    input; the snapshot is rebuilt from the state's window and x.  cu_draft int32 [n_seq + 1]: the
+    verify's packed ragged spans (accept_len then lies in 1..T_s, and x is [total_tokens, dim])."""
     if (layout == "recompute") != (x is not None and window is None):
         raise ValueError("the recompute commit takes x and no window; the others take a window")
-    if x is not None:
+    x_seq = x_tok = 0
+    if x is not None and cu_draft is not None:
+        assert x.stride(1) == 1
+        x_tok, total_tokens = x.stride(0), x.shape[0]
+    elif x is not None:
         assert x.stride(2) == 1
+        x_seq, x_tok = x.stride(0), x.stride(1)
     ws = window_strides(window, layout)
     n_seq = accept_len.shape[0]
     a = _CommitArgs(
@@ -188,7 +211,7 @@ def conv_commit(conv_state, window, accept_len, *, layout, T, width, cache_idx=N
         st_ch=conv_state.stride(1), cache_idx=_ptr(cache_idx), window=_ptr(window),
         dedup=1 if layout == "dedup" else 0, w_seq=ws[0], w_step=ws[1], w_ch=ws[2], w_col=ws[3],
         accept_len=_ptr(accept_len), status=_ptr(status), recompute=1 if layout == "recompute" else 0,
-        x=_ptr(x), x_seq=x.stride(0) if x is not None else 0, x_tok=x.stride(1) if x is not None else 0)
+        x=_ptr(x), x_seq=x_seq, x_tok=x_tok, cu_draft=_ptr(cu_draft), total_tokens=int(total_tokens))
     rc = _load().oracle_conv_commit(ctypes.byref(a))
     if rc != 0:
         raise RuntimeError(f"oracle_conv_commit returned {rc}")

@@ -78,6 +78,17 @@
  *     chain (p(t) = t-1) is the plain verify.  The state is left on window(T-1), as for a chain;
  *     the commit restores the window of the accepted path's last token (accept_len = its index + 1).
  *     Only the dense layout holds tree snapshots.  A parent outside [-1, t) flags the sequence (32).
+ *   - Packed ragged verify (sglang PR #46184, "Related upstream work": a packed variable-length
+ *     update, and target verify run on packed ragged tokens with the tile store covering the
+ *     packed rows).  Sequence s owns draft tokens [cu[s], cu[s+1]) of x and out, packed back to
+ *     back (row cu[s]+t holds its token t); its draft count T_s = cu[s+1]-cu[s] lies in [0, T],
+ *     where T is the call's maximum and sizes the window buffer.  Everything above holds with T_s
+ *     in place of T for that sequence: outputs for its T_s rows, snapshots t < T_s (snapshot steps
+ *     t >= T_s are not written, and in the deduplicated layout only columns [0, T_s+W-2), the ones
+ *     the per-token stores write, are), the state left on full[T_s .. T_s+W-2].  T_s = 0 writes no
+ *     output and no snapshot; the state then receives the committed window itself.  A span that
+ *     is reversed, leaves [0, total_tokens) or is longer than T flags the sequence (16).  The commit
+ *     accepts a in 1..T_s; a sequence with T_s = 0 has nothing to commit and is skipped.
  *   - Prefill (glm5next_kda mod.rs, the prefill path of the layer: the conv over all T prompt
  *     tokens with SiLU, then the L2 normalisation of q|k, which that code runs as a second launch;
  *     here the normalisation is applied to the fp32 SiLU values and rounded once, as in decode).
@@ -87,7 +98,8 @@
  *     the state is left holding the last W-1 entries of full.
  *
  * Status codes written per sequence (same meaning as the library's): 1 = cache slot out of range,
- * 2 = state offset out of range, 4 = accept count out of range, 16 = token span invalid (prefill),
+ * 2 = state offset out of range, 4 = accept count out of range, 16 = token span invalid (prefill,
+ * packed ragged verify),
  * 32 = a draft token's parent outside [-1, t) (tree verify).
  * A flagged sequence is untouched.
  */
@@ -119,6 +131,8 @@ typedef struct {
     int32_t recompute; /* 1: outputs only; no snapshots and the state is not written */
     int32_t state_is_bf16; /* dtype of state and window: 0 fp32, 1 bf16 (may differ from is_bf16) */
     const int32_t *parent; /* [n_seq][T] parent of each draft token (-1: the committed window) or NULL */
+    const int32_t *cu_draft; /* [n_seq + 1] packed draft rows of x and out, or NULL (T each) */
+    int32_t total_tokens;    /* rows of x and out when cu_draft is given */
 } oracle_verify_args;
 
 typedef struct {
@@ -135,6 +149,8 @@ typedef struct {
     int32_t recompute; /* 1: rebuild from the state's window and x (no window buffer) */
     const void *x;
     int64_t x_seq, x_tok;
+    const int32_t *cu_draft; /* [n_seq + 1] as in the verify, or NULL (T tokens each) */
+    int32_t total_tokens;
 } oracle_commit_args;
 
 /* ---- element access: raw bits, so copies keep NaN payloads and signed zeros ---- */
@@ -190,6 +206,7 @@ int oracle_conv_verify(const oracle_verify_args *a) {
     float fullf[1024];    /* the same inputs widened to fp32 (exact) */
     if (W < 1 || T < 1 || dim < 1 || W - 1 + T > 1024) return -1;
     if (a->history && T + W - 2 > a->state_cols) return -3;
+    if (a->cu_draft && a->parent) return -4; /* packed rows are chains only */
     /* y[t*dim + c]: post-SiLU fp32 values of one sequence, normalised in place below */
     float *y = (float *)malloc(sizeof(float) * (size_t)T * (size_t)dim);
     if (!y) return -2;
@@ -205,6 +222,17 @@ int oracle_conv_verify(const oracle_verify_args *a) {
                 const int par = a->parent[(int64_t)s * T + t];
                 if (par < -1 || par >= t) st |= 32;
             }
+        /* the sequence's draft rows: T rows at x[s] (sequence stride), or its packed span
+           [cu[s], cu[s+1]) of T_s rows (token stride only) */
+        int Ts = T;
+        int64_t xrow = (int64_t)s * a->x_seq, orow = (int64_t)s * a->out_seq;
+        if (a->cu_draft) {
+            const int b = a->cu_draft[s], e = a->cu_draft[s + 1];
+            if (slot >= 0 && (b < 0 || e < b || e > a->total_tokens || e - b > T)) st |= 16;
+            Ts = e - b;
+            xrow = (int64_t)b * a->x_tok;
+            orow = (int64_t)b * a->out_tok;
+        }
         if (a->status) a->status[s] = st;
         if (slot < 0 || st) continue;
 
@@ -228,7 +256,7 @@ int oracle_conv_verify(const oracle_verify_args *a) {
                 }
                 for (int t = 0; t < T; ++t) {
                     const int base = (a->parent[(int64_t)s * T + t] + 1) * R;
-                    const uint32_t xv = get_bits(a->x, bf, (int64_t)s * a->x_seq + (int64_t)t * a->x_tok + c);
+                    const uint32_t xv = get_bits(a->x, bf, xrow + (int64_t)t * a->x_tok + c);
                     const float xf = bits_to_float(xv, bf);
                     float acc = a->bias ? bits_to_float(get_bits(a->bias, bf, c), bf) : 0.0f;
                     for (int j = 0; j < W; ++j) {
@@ -257,13 +285,13 @@ int oracle_conv_verify(const oracle_verify_args *a) {
                 full[k] = get_bits(a->state, sbf, srow + o + k);
                 fullf[k] = bits_to_float(full[k], sbf);
             }
-            for (int t = 0; t < T; ++t) {
-                const uint32_t xv = get_bits(a->x, bf, (int64_t)s * a->x_seq + (int64_t)t * a->x_tok + c);
+            for (int t = 0; t < Ts; ++t) {
+                const uint32_t xv = get_bits(a->x, bf, xrow + (int64_t)t * a->x_tok + c);
                 full[W - 1 + t] = to_state_bits(xv, bf, sbf);
                 fullf[W - 1 + t] = bits_to_float(xv, bf);
             }
 
-            for (int t = 0; t < T; ++t) {
+            for (int t = 0; t < Ts; ++t) {
                 float acc = a->bias ? bits_to_float(get_bits(a->bias, bf, c), bf) : 0.0f;
                 for (int j = 0; j < W; ++j) {
                     const float wj = bits_to_float(get_bits(a->weight, bf, (int64_t)c * W + j), bf);
@@ -277,20 +305,20 @@ int oracle_conv_verify(const oracle_verify_args *a) {
 
             if (a->history) {
                 /* snapshot t into the state row itself, at columns t .. t+W-2 (after every read) */
-                for (int t = 0; t < T; ++t)
+                for (int t = 0; t < Ts; ++t)
                     for (int k = 0; k < W - 1; ++k) put_bits(a->state, sbf, srow + t + k, full[t + 1 + k]);
                 continue;
             }
 
             /* snapshot t = window after token t = full[t+1 .. t+W-1] */
-            for (int t = 0; t < T; ++t)
+            for (int t = 0; t < Ts; ++t)
                 for (int k = 0; k < W - 1; ++k) put_bits(a->window, sbf, win_index(a, s, t, c, k), full[t + 1 + k]);
 
             /* committed window after the last token, written after every read of this row */
-            for (int k = 0; k < W - 1; ++k) put_bits(a->state, sbf, srow + k, full[T + k]);
+            for (int k = 0; k < W - 1; ++k) put_bits(a->state, sbf, srow + k, full[Ts + k]);
         }
 
-        for (int t = 0; t < T; ++t) {
+        for (int t = 0; t < Ts; ++t) {
             float *yt = y + (int64_t)t * dim;
             if (a->qk_channels > 0) {
                 const int hd = a->head_dim;
@@ -305,7 +333,7 @@ int oracle_conv_verify(const oracle_verify_args *a) {
                 }
             }
             for (int c = 0; c < dim; ++c)
-                put_bits(a->out, bf, (int64_t)s * a->out_seq + (int64_t)t * a->out_tok + c, float_to_bits(yt[c], bf));
+                put_bits(a->out, bf, orow + (int64_t)t * a->out_tok + c, float_to_bits(yt[c], bf));
         }
     }
     free(y);
@@ -319,18 +347,28 @@ int oracle_conv_commit(const oracle_commit_args *a) {
         const int slot = a->cache_idx ? a->cache_idx[s] : s;
         int st = 0;
         if (slot >= 0 && slot >= a->n_slots) st |= 1;
+        /* draft count and rows as in the verify (packed span, or T rows at x[s]) */
+        int Ts = a->T;
+        int64_t xrow = (int64_t)s * a->x_seq;
+        if (a->cu_draft) {
+            const int b = a->cu_draft[s], e = a->cu_draft[s + 1];
+            if (slot >= 0 && (b < 0 || e < b || e > a->total_tokens || e - b > a->T)) st |= 16;
+            Ts = e - b;
+            xrow = (int64_t)b * a->x_tok;
+        }
         const int acc = a->accept_len[s];
-        if (slot >= 0 && (acc < 1 || acc > a->T)) st |= 4;
+        if (slot >= 0 && !(st & 16) && Ts > 0 && (acc < 1 || acc > Ts)) st |= 4;
         if (a->status) a->status[s] = st;
         if (slot < 0 || st) continue;
+        if (Ts == 0) continue; /* no draft token was verified: nothing to commit */
         const int t = acc - 1;
         if (a->recompute) {
             for (int c = 0; c < a->dim; ++c) {
                 const int64_t srow = (int64_t)slot * a->st_slot + (int64_t)c * a->st_ch;
-                uint32_t full[1024]; /* W-1 + T raw elements of one channel */
+                uint32_t full[1024]; /* W-1 + T_s raw elements of one channel */
                 for (int k = 0; k < W - 1; ++k) full[k] = get_bits(a->state, bf, srow + k);
-                for (int u = 0; u < a->T; ++u)
-                    full[W - 1 + u] = get_bits(a->x, bf, (int64_t)s * a->x_seq + (int64_t)u * a->x_tok + c);
+                for (int u = 0; u < Ts; ++u)
+                    full[W - 1 + u] = get_bits(a->x, bf, xrow + (int64_t)u * a->x_tok + c);
                 /* snapshot acc-1 = full[acc .. acc+W-2], written after the row's reads */
                 for (int k = 0; k < W - 1; ++k) put_bits(a->state, bf, srow + k, full[acc + k]);
             }

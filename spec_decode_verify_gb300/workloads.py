@@ -230,6 +230,145 @@ def algorithmic_bytes(w: VerifyWorkload, n_active: Optional[int] = None) -> dict
     return dict(verify=n * per_seq + shared, commit=commit, per_seq=per_seq)
 
 
+# ----------------------------------------------------------------------------- packed ragged verify
+
+@dataclasses.dataclass(frozen=True)
+class RaggedWorkload:
+    """Packed ragged verify: sequence s owns draft rows [cu[s], cu[s+1]) of x and out (T_s =
+    lengths[s] rows, 0..T), T is the largest draft count (the window buffer's T).  sglang PR
+    #46184, "Related upstream work": target verify on packed ragged tokens, the tile store covering
+    the packed rows."""
+    name: str
+    lengths: tuple  # draft tokens per sequence (0..T)
+    T: int
+    dim: int
+    width: int
+    qk_channels: int
+    head_dim: int
+    dtype: str
+    layout: str  # "dense", "dedup", "history" or "recompute"
+    bias: bool = False
+    l2_eps: float = 1e-6
+    pad: tuple = ()  # indices of padded sequences (cache index -1)
+    extra_slots: int = 0
+    state_offset: bool = False  # read the committed window at a per-sequence offset in 0..T-1
+    x_row_stride: Optional[int] = None
+    extra_rows: int = 0  # rows of x / out past the last span (never touched)
+    seed: int = 0
+
+    @property
+    def n_seq(self) -> int:
+        return len(self.lengths)
+
+    @property
+    def total_tokens(self) -> int:
+        return int(sum(self.lengths)) + self.extra_rows
+
+    @property
+    def n_slots(self) -> int:
+        return self.n_seq + self.extra_slots
+
+    @property
+    def n_pad(self) -> int:
+        return len(self.pad)
+
+    @property
+    def state_cols(self) -> int:
+        if self.layout == "history":
+            return self.T + self.width - 2
+        return self.width - 1 + (self.T - 1 if self.state_offset else 0)
+
+    @property
+    def torch_dtype(self):
+        return torch.float32 if self.dtype == "f32" else torch.bfloat16
+
+    state_torch_dtype = torch_dtype
+
+    @property
+    def esize(self) -> int:
+        return 4 if self.dtype == "f32" else 2
+
+    state_esize = esize
+
+    def replace(self, **kw) -> "RaggedWorkload":
+        return dataclasses.replace(self, **kw)
+
+
+def ragged_lengths(seed: int, n: int, lo: int, hi: int) -> tuple:
+    """n draft counts drawn uniformly from lo..hi (seeded)."""
+    rng = np.random.default_rng(seed)
+    return tuple(int(v) for v in rng.integers(lo, hi + 1, size=n))
+
+
+def make_ragged_inputs(w: RaggedWorkload, seed: Optional[int] = None) -> dict:
+    """CPU tensors for one packed ragged verify + commit: x [total_tokens, dim] (a view with token
+    stride x_row_stride when set), cu_draft int32 [n_seq+1], conv_state [n_slots, dim, state_cols],
+    weight, bias, cache_idx (-1 = padded), state_off (or None), accept_len in 1..T_s (1 where
+    T_s = 0), and sentinel-filled out [total_tokens, dim] and window (dense [n_seq, T, dim, W-1],
+    dedup [n_seq, dim, T+W-2], None for history and recompute)."""
+    rng = np.random.default_rng(w.seed if seed is None else seed)
+    dt = w.torch_dtype
+    total = w.total_tokens
+    row = w.x_row_stride or w.dim
+    x_wide = _to_dtype(rng.standard_normal((max(total, 1), row), dtype=np.float32), dt)
+    x = x_wide[:total, : w.dim]
+    state = _to_dtype(rng.standard_normal((w.n_slots, w.dim, w.state_cols), dtype=np.float32), dt)
+    weight = _to_dtype(rng.uniform(-0.5, 0.5, size=(w.dim, w.width)).astype(np.float32), dt)
+    bias = _to_dtype(rng.normal(0.0, 0.1, size=(w.dim,)).astype(np.float32), dt) if w.bias else None
+    perm = rng.permutation(w.n_slots)[: w.n_seq].astype(np.int32)
+    for i in w.pad:
+        perm[i] = -1
+    cu = np.zeros(w.n_seq + 1, dtype=np.int32)
+    cu[1:] = np.cumsum(np.asarray(w.lengths, dtype=np.int64))
+    accept = np.array([int(rng.integers(1, max(L, 1) + 1)) for L in w.lengths], dtype=np.int32)
+    state_off = None
+    if w.state_offset or w.layout == "history":
+        state_off = torch.from_numpy(rng.integers(0, w.T, size=w.n_seq).astype(np.int32))
+    out = sentinel_tensor((total, w.dim), dt)
+    window = None
+    if w.layout == "dense":
+        window = sentinel_tensor((w.n_seq, w.T, w.dim, w.width - 1), dt)
+    elif w.layout == "dedup":
+        window = sentinel_tensor((w.n_seq, w.dim, w.T + w.width - 2), dt)
+    return dict(x=x, x_base=x_wide, cu_draft=torch.from_numpy(cu), conv_state=state, weight=weight, bias=bias,
+                cache_idx=torch.from_numpy(perm.copy()), state_off=state_off, accept_len=torch.from_numpy(accept),
+                out=out, window=window)
+
+
+def ragged_algorithmic_bytes(w: RaggedWorkload) -> dict:
+    """Bytes a packed ragged verify and its commit must move: per active sequence with T_s draft
+    tokens, x T_s rows read and out T_s rows written, the committed window read and written, and the
+    snapshots written (dedup: T_s+W-2 columns when T_s >= 1; dense: T_s (W-1)-runs); weights, bias
+    and the index arrays once.  Commit: the window of snapshot a-1 read and the state written, for
+    sequences with T_s >= 1."""
+    e = w.esize
+    R = w.width - 1
+    act = [i for i in range(w.n_seq) if i not in w.pad]
+    shared = (w.dim * w.width + (w.dim if w.bias else 0)) * e + 4 * (2 * w.n_seq + 1)
+    verify = commit = 0
+    for i in act:
+        L = w.lengths[i]
+        snaps = (L + w.width - 2 if L > 0 else 0) if w.layout == "dedup" else L * R
+        verify += (2 * L + 2 * R + snaps) * w.dim * e
+        if L > 0:
+            commit += 2 * R * w.dim * e
+    return dict(verify=verify + shared, commit=commit + 8 * w.n_seq)
+
+
+RAGGED_WORKLOADS = {
+    w.name: w
+    for w in [
+        # the benchmark shape with ragged drafts: 128 sequences of 1..16 draft tokens (about 1100
+        # packed rows), 13 padded, dedup rows sized for T = 16
+        RaggedWorkload("ragged_n128_t1to16_dim10240_w4_bf16_dedup_pad13", lengths=ragged_lengths(31, 128, 1, 16),
+                       T=16, dim=10240, width=4, qk_channels=4096, head_dim=128, dtype="bf16", layout="dedup",
+                       pad=tuple(int(i) for i in np.random.default_rng(32).permutation(128)[:13]), extra_slots=16,
+                       seed=31),
+    ]
+}
+RAGGED_ORDER = list(RAGGED_WORKLOADS)
+
+
 # ----------------------------------------------------------------------------- prefill
 
 @dataclasses.dataclass(frozen=True)

@@ -11,6 +11,7 @@ import pytest
 import oracle
 import test_oracle_pins as pins
 import test_oracle_prefill_pins as ppins
+import test_oracle_varlen_pins as vpins
 
 SRC = os.path.join(os.path.dirname(oracle.__file__), "oracle.c")
 
@@ -36,7 +37,7 @@ MUTANTS = [
      lambda: pins.test_p3_one_hot_taps_and_constant_group()),
     ("snapshot_off_by_one", "win_index(a, s, t, c, k), full[t + 1 + k])", "win_index(a, s, t, c, k), full[t + k])",
      lambda: pins.test_p4_sequential_equals_batched_in_T("dense", "f32")),
-    ("state_write_lags", "put_bits(a->state, sbf, srow + k, full[T + k])", "put_bits(a->state, sbf, srow + k, full[T - 1 + k])",
+    ("state_write_lags", "put_bits(a->state, sbf, srow + k, full[Ts + k])", "put_bits(a->state, sbf, srow + k, full[Ts - 1 + k])",
      lambda: pins.test_p11_single_token_update()),
     ("offset_ignored", "full[k] = get_bits(a->state, sbf, srow + o + k);", "full[k] = get_bits(a->state, sbf, srow + k);",
      lambda: pins.test_p10_state_offset_equals_preshifted_state()),
@@ -50,14 +51,14 @@ MUTANTS = [
      lambda: pins.test_p6_dedup_view_equals_dense(4)),
     ("history_row_shifted", "srow + t + k, full[t + 1 + k])", "srow + t + k, full[t + k])",
      lambda: pins.test_h1_history_row_equals_dedup_row(3)),
-    ("history_row_last_window_only", "for (int t = 0; t < T; ++t)\n                    for (int k = 0; k < W - 1; ++k) put_bits(a->state",
-     "for (int t = T - 1; t < T; ++t)\n                    for (int k = 0; k < W - 1; ++k) put_bits(a->state",
+    ("history_row_last_window_only", "for (int t = 0; t < Ts; ++t)\n                    for (int k = 0; k < W - 1; ++k) put_bits(a->state",
+     "for (int t = Ts - 1; t < Ts; ++t)\n                    for (int k = 0; k < W - 1; ++k) put_bits(a->state",
      lambda: pins.test_h2_history_chain_equals_verify_commit_chain()),
     ("recompute_wrong_snapshot", "put_bits(a->state, bf, srow + k, full[acc + k]);",
      "put_bits(a->state, bf, srow + k, full[acc - 1 + k]);",
      lambda: pins.test_r3_recompute_commit_closed_form()),
     ("recompute_verify_writes_state", "if (a->recompute) continue; /* outputs only",
-     "if (a->recompute) { put_bits(a->state, bf, srow, full[T]); continue; } /* outputs only",
+     "if (a->recompute) { put_bits(a->state, bf, srow, full[Ts]); continue; } /* outputs only",
      lambda: pins.test_r1_recompute_verify_writes_outputs_only(3, "f32")),
     ("prefill_init_ignored", "full[k] = init ? get_bits(a->state, bf, srow + k) : 0u;",
      "full[k] = get_bits(a->state, bf, srow + k);", lambda: ppins.test_pf4_no_initial_state_is_a_zero_window()),
@@ -79,6 +80,20 @@ MUTANTS = [
     ("tree_state_one_token_short", "put_bits(a->state, sbf, srow + k, wbits[T * R + k]);",
      "put_bits(a->state, sbf, srow + k, wbits[(T - 1) * R + k]);",
      lambda: pins.test_tr1_chain_parents_equal_the_plain_verify(4, "f32")),
+    ("varlen_state_uses_T", "put_bits(a->state, sbf, srow + k, full[Ts + k]);",
+     "put_bits(a->state, sbf, srow + k, full[T + k]);",
+     lambda: vpins.test_v1_packed_equals_separate_verifies("dense", "f32")),
+    ("varlen_rows_shifted", "xrow = (int64_t)b * a->x_tok;", "xrow = (int64_t)(b > 0 ? b - 1 : 0) * a->x_tok;",
+     lambda: vpins.test_v3_matches_float64_conv1d(4)),
+    ("varlen_snapshots_past_Ts",
+     "for (int t = 0; t < Ts; ++t)\n                for (int k = 0; k < W - 1; ++k) put_bits(a->window",
+     "for (int t = 0; t < T; ++t)\n                for (int k = 0; k < W - 1; ++k) put_bits(a->window",
+     lambda: vpins.test_v5_untouched_regions()),
+    ("varlen_commit_accept_past_Ts", "(acc < 1 || acc > Ts)) st |= 4;", "(acc < 1 || acc > a->T)) st |= 4;",
+     lambda: vpins.test_v6_bad_spans_flagged_and_untouched()),
+    ("varlen_empty_commit_not_skipped", "if (Ts == 0) continue; /* no draft token was verified",
+     "/* mutated */ /* no draft token was verified",
+     lambda: vpins.test_v4_commit_equals_shorter_verify("dedup")),
     ("padded_row_written", "if (slot < 0 || st) continue;\n\n", "if (st) continue;\n        if (slot < 0) { if (a->out) put_bits(a->out, bf, (int64_t)s * a->out_seq, 0); continue; }\n\n",
      lambda: pins.test_p7_padded_rows_untouched()),
 ]
