@@ -248,7 +248,10 @@ def barrier(dist, device):
 def oracle_step_times(w, reps_max: int, budget_s: float):
     """Time oracle verify + commit on the whole workload (one core); returns per-step seconds."""
     import oracle
-    inp = wl.make_inputs(w)
+    ragged = isinstance(w, wl.RaggedWorkload)
+    inp = wl.make_ragged_inputs(w) if ragged else wl.make_inputs(w)
+    rag_kw = dict(cu_draft=inp["cu_draft"], T=w.T) if ragged else {}
+    commit_kw = dict(cu_draft=inp["cu_draft"], total_tokens=w.total_tokens) if ragged else {}
     times = []
     t_begin = time.perf_counter()
     for _ in range(reps_max):
@@ -258,10 +261,11 @@ def oracle_step_times(w, reps_max: int, budget_s: float):
         t0 = time.perf_counter()
         oracle.conv_verify(inp["x"], state, inp["weight"], inp["bias"], out, win, layout=w.layout,
                            qk_channels=w.qk_channels, head_dim=w.head_dim, l2_eps=w.l2_eps,
-                           cache_idx=inp["cache_idx"], state_off=inp["state_off"], parent=inp.get("parent"))
+                           cache_idx=inp["cache_idx"], state_off=inp["state_off"], parent=inp.get("parent"), **rag_kw)
         if w.layout != "history":
             oracle.conv_commit(state, win, inp["accept_len"], layout=w.layout, T=w.T, width=w.width,
-                               cache_idx=inp["cache_idx"], x=inp["x"] if w.layout == "recompute" else None)
+                               cache_idx=inp["cache_idx"], x=inp["x"] if w.layout == "recompute" else None,
+                               **commit_kw)
         times.append(time.perf_counter() - t0)
         if time.perf_counter() - t_begin > budget_s and len(times) >= 3:
             break
@@ -297,10 +301,14 @@ L2_RULE = "inputs larger than L2: every step uses the next of rotating buffer se
 
 
 def workload_config(w):
-    return {"workload": w.name, "n_seq": w.n_seq, "padded_seqs": w.n_pad, "T": w.T, "dim": w.dim, "width": w.width,
-            "qk_channels": w.qk_channels, "head_dim": w.head_dim, "layout": w.layout, "bias": w.bias,
-            "step": "cv_conv_verify" if w.layout == "history" else "cv_conv_verify + cv_conv_commit",
-            "l2": L2_RULE}
+    c = {"workload": w.name, "n_seq": w.n_seq, "padded_seqs": w.n_pad, "T": w.T, "dim": w.dim, "width": w.width,
+         "qk_channels": w.qk_channels, "head_dim": w.head_dim, "layout": w.layout, "bias": w.bias,
+         "step": "cv_conv_verify" if w.layout == "history" else "cv_conv_verify + cv_conv_commit",
+         "l2": L2_RULE}
+    if isinstance(w, wl.RaggedWorkload):
+        c.update(draft_tokens="packed ragged: T_s per sequence, T = the largest", total_tokens=w.total_tokens,
+                 active_draft_tokens=sum(L for i, L in enumerate(w.lengths) if i not in w.pad))
+    return c
 
 
 # ----------------------------------------------------------------------------- GPU arm
@@ -316,7 +324,8 @@ def run_ours(args, w, world, rank, local, dist):
     stream = torch.cuda.current_stream(dev)
     sp = stream.cuda_stream
 
-    inp = wl.make_inputs(w, seed=w.seed + 1009 * rank)
+    ragged = isinstance(w, wl.RaggedWorkload)
+    inp = (wl.make_ragged_inputs if ragged else wl.make_inputs)(w, seed=w.seed + 1009 * rank)
     props = torch.cuda.get_device_properties(dev)
     l2 = getattr(props, "L2_cache_size", 0) or 129 * 2 ** 20
     per_set = sum(inp[k].numel() * inp[k].element_size()
@@ -330,6 +339,9 @@ def run_ours(args, w, world, rank, local, dist):
     cache_idx = inp["cache_idx"].to(dev)
     state_off = inp["state_off"].to(dev) if inp["state_off"] is not None else None
     parent = inp["parent"].to(dev) if inp.get("parent") is not None else None
+    cu = inp["cu_draft"].to(dev) if ragged else None
+    rag_kw = dict(cu_draft=cu, T=w.T) if ragged else {}
+    commit_kw = dict(cu_draft=cu, total_tokens=w.total_tokens) if ragged else {}
     sets = []
     for i in range(n_sets):
         xb = inp["x_base"].to(dev)
@@ -339,11 +351,11 @@ def run_ours(args, w, world, rank, local, dist):
                  accept=inp["accept_len"].to(dev))
         s["va"] = cv.make_verify_args(x, s["conv_state"], weight, bias, s["out"], s["window"], layout=w.layout,
                                       qk_channels=w.qk_channels, head_dim=w.head_dim, l2_eps=w.l2_eps,
-                                      cache_idx=cache_idx, state_off=state_off, parent=parent)
+                                      cache_idx=cache_idx, state_off=state_off, parent=parent, **rag_kw)
         if has_commit:
             s["ca"] = cv.make_commit_args(s["conv_state"], s["window"], s["accept"], layout=w.layout, T=w.T,
                                           width=w.width, cache_idx=cache_idx,
-                                          x=x if w.layout == "recompute" else None)
+                                          x=x if w.layout == "recompute" else None, **commit_kw)
         sets.append(s)
     verify_fn, lib_commit = lib.cv_conv_verify, lib.cv_conv_commit
     vrefs = [ctypes.byref(s["va"]) for s in sets]
@@ -426,7 +438,7 @@ def run_ours(args, w, world, rank, local, dist):
     if rank != 0:
         return 0
 
-    nbytes = wl.algorithmic_bytes(w)
+    nbytes = wl.ragged_algorithmic_bytes(w) if ragged else wl.algorithmic_bytes(w)
     peak, peak_kind = measured_peak()
     achieved = nbytes["verify"] / (verify_us_max * 1e-6) / 1e9
     traffic, traffic_src = profile_traffic(w.name, kernel_kind)
@@ -682,7 +694,8 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default=wl.BENCH_WORKLOAD, choices=wl.WORKLOAD_ORDER + wl.PREFILL_ORDER)
+    ap.add_argument("--workload", default=wl.BENCH_WORKLOAD,
+                    choices=wl.WORKLOAD_ORDER + wl.RAGGED_ORDER + wl.PREFILL_ORDER)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--clocks-csv", default=None, help="keep the raw nvidia-smi clock samples in this file")
@@ -711,7 +724,7 @@ def main():
             if args.impl == "reference":
                 return run_reference_prefill(args, w, world, rank)
             return run_ours_prefill(args, w, world, rank, local, dist)
-        w = wl.WORKLOADS[args.workload]
+        w = wl.WORKLOADS[args.workload] if args.workload in wl.WORKLOADS else wl.RAGGED_WORKLOADS[args.workload]
         if args.impl == "reference":
             return run_reference(args, w, world, rank)
         return run_ours(args, w, world, rank, local, dist)

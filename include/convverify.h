@@ -51,7 +51,7 @@ extern "C" {
 #define CV_API
 #endif
 
-#define CV_ABI_VERSION 5
+#define CV_ABI_VERSION 6
 #define CV_MAX_T 128 /* draft tokens per verify call */
 
 typedef enum cv_dtype {
@@ -118,7 +118,8 @@ enum {
 #define CV_SEQ_BAD_ACCEPT 4 /* accept count outside 1..T (commit only) */
 #define CV_SEQ_TIMEOUT 8    /* a bounded wait for a bulk copy gave up: the sequence may be partly
                                written (every sequence whose data the block had not finished) */
-#define CV_SEQ_BAD_SPAN 16  /* prefill: token span invalid or longer than max_seqlen */
+#define CV_SEQ_BAD_SPAN 16  /* prefill: token span invalid or longer than max_seqlen; packed
+                               verify / commit: draft span invalid or longer than T */
 #define CV_SEQ_BAD_TREE 32  /* tree verify: a draft token's parent outside [-1, t) */
 
 /*
@@ -191,6 +192,22 @@ enum {
  *                      restores the accepted path's last node: accept_len = its index + 1.  Needs
  *                      the dense layout and one dtype; a parent outside [-1, t) flags
  *                      CV_SEQ_BAD_TREE.
+ *   cu_draft           int32 [n_seq + 1] device array or NULL: packed ragged drafts ([sglang-46184]
+ *                      "Related upstream work": target verify on packed ragged tokens, the tile
+ *                      store covering the packed rows).  Sequence s then owns rows
+ *                      [cu_draft[s], cu_draft[s+1]) of x and out -- row r at r*x_tok_stride and
+ *                      r*out_tok_stride; x_seq_stride and out_seq_stride are ignored -- and its T_s
+ *                      rows are verified exactly as a verify of T_s tokens: T_s outputs, snapshots
+ *                      t < T_s (dense steps >= T_s and dedup columns >= T_s+W-2 are not written),
+ *                      and the state left on full[T_s .. T_s+W-2].  T is the largest T_s and sizes
+ *                      the window buffer (dense [n_seq][T][dim][W-1], dedup [n_seq][dim][T+W-2],
+ *                      history rows >= T+W-2).  T_s = 0 writes no output and no snapshot (the
+ *                      state receives the committed window; in the history layout nothing is
+ *                      written).  A span that is reversed, leaves [0, total_tokens) or holds more
+ *                      than T rows flags CV_SEQ_BAD_SPAN and leaves the sequence untouched.  Chains
+ *                      only: cu_draft with parent is CV_ERR_LAYOUT.  With packed 16-byte-aligned
+ *                      buffers the pipelined kernel runs it (one dtype), otherwise the general one.
+ *   total_tokens       rows of x and out with cu_draft (>= 0); x and out may be NULL when it is 0
  * Preconditions the library cannot check: distinct sequences use distinct slots; out and window do
  * not overlap themselves, each other, x, conv_state or weight.
  * Returns CV_OK after the launch is queued, or a negative CV_ERR_* code with nothing launched.
@@ -217,6 +234,8 @@ typedef struct cv_verify_args {
     int32_t *err;
     int32_t state_dtype; /* CV_STATE_* */
     const int32_t *parent;
+    const int32_t *cu_draft; /* packed ragged drafts: int32 [n_seq + 1] device array, or NULL */
+    int32_t total_tokens;    /* rows of x and out when cu_draft is given */
 } cv_verify_args;
 
 CV_API int cv_conv_verify(const cv_verify_args *args, void *stream);
@@ -241,6 +260,10 @@ CV_API int cv_conv_verify(const cv_verify_args *args, void *stream);
  * pre-verify window in columns [0, W-1) (the verify leaves it alone in this layout).  With
  * full = [conv_state[slot][c][0 .. W-2], x[s][0][c] .. x[s][T-1][c]], the commit sets
  * conv_state[slot][c][k] = full[a+k] for k < W-1; each state row is read before it is written.
+ * With cu_draft (the matching verify's packed spans) the accept count of sequence s must lie in
+ * 1..T_s, an invalid span flags CV_SEQ_BAD_SPAN, and a sequence with T_s = 0 has nothing to commit
+ * (skipped, err 0); in the recompute layout its x rows start at row cu_draft[s] (x_tok_stride;
+ * total_tokens rows).
  * CV_WINDOW_HISTORY has nothing to commit and returns CV_ERR_LAYOUT.  dtype here is the dtype of
  * conv_state and window (with mixed dtypes, the state's); the recompute layout needs x in it too.
  */
@@ -261,6 +284,8 @@ typedef struct cv_commit_args {
     const void *x;
     int64_t x_seq_stride, x_tok_stride;
     int32_t wait_polls; /* limit of the bounded wait, as in cv_verify_args; 0 = the default */
+    const int32_t *cu_draft; /* the matching verify's packed draft spans, or NULL */
+    int32_t total_tokens;    /* rows of x (recompute layout) when cu_draft is given */
 } cv_commit_args;
 
 CV_API int cv_conv_commit(const cv_commit_args *args, void *stream);

@@ -42,7 +42,7 @@ class VerifyArgs(ctypes.Structure):
         ("cache_idx", c_vp), ("state_off", c_vp), ("weight", c_vp), ("bias", c_vp),
         ("window", c_vp), ("window_layout", c_i32), ("wait_polls", c_i32),
         ("win_seq_stride", c_i64), ("win_step_stride", c_i64), ("win_ch_stride", c_i64), ("win_col_stride", c_i64),
-        ("err", c_vp), ("state_dtype", c_i32), ("parent", c_vp),
+        ("err", c_vp), ("state_dtype", c_i32), ("parent", c_vp), ("cu_draft", c_vp), ("total_tokens", c_i32),
     ]
 
 
@@ -54,7 +54,7 @@ class CommitArgs(ctypes.Structure):
         ("state_cols", c_i32), ("window_layout", c_i32), ("cache_idx", c_vp), ("window", c_vp),
         ("win_seq_stride", c_i64), ("win_step_stride", c_i64), ("win_ch_stride", c_i64), ("win_col_stride", c_i64),
         ("accept_len", c_vp), ("err", c_vp), ("x", c_vp), ("x_seq_stride", c_i64), ("x_tok_stride", c_i64),
-        ("wait_polls", c_i32),
+        ("wait_polls", c_i32), ("cu_draft", c_vp), ("total_tokens", c_i32),
     ]
 
 
@@ -184,7 +184,7 @@ def _stream_ptr(stream) -> Optional[int]:
 
 def make_verify_args(x, conv_state, weight, bias, out, window, *, layout, qk_channels, head_dim,
                      l2_eps=1e-6, cache_idx=None, state_off=None, err=None, parent=None, wait_polls=0,
-                     check_device=True) -> VerifyArgs:
+                     cu_draft=None, T=None, check_device=True) -> VerifyArgs:
     """Build cv_verify_args from tensors.
 
     x [n_seq, T, dim] (channel stride 1, any seq/token strides), conv_state [n_slots, dim, S]
@@ -195,12 +195,28 @@ def make_verify_args(x, conv_state, weight, bias, out, window, *, layout, qk_cha
     row and the next call reads at state_off = accept_len - 1) or "recompute" (outputs only; the
     commit rebuilds the state from x), cache_idx / state_off / err int32 [n_seq] or None, parent int32
     [n_seq, T] contiguous (tree verify, dense layout) or None.  wait_polls: the limit of the
-    pipelined kernel's bounded waits (0 = the default; see cv_verify_args)."""
+    pipelined kernel's bounded waits (0 = the default; see cv_verify_args).
+
+    Packed ragged drafts: cu_draft int32 [n_seq + 1]; x and out are then [total_tokens, dim] (token
+    stride free, channel stride 1), sequence s owning rows cu_draft[s] .. cu_draft[s+1]-1, and T
+    (required) is the largest draft count, the T of the window buffer."""
     lay = _layout_code(layout)
     ptr = _dev_ptr if check_device else (lambda t, n, required=True: None if t is None else t.data_ptr())
-    if x.dim() != 3 or conv_state.dim() != 3 or weight.dim() != 2:
-        raise ValueError("x must be [n_seq, T, dim], conv_state [n_slots, dim, S] and weight [dim, W]")
-    n_seq, T, dim = x.shape
+    varlen = cu_draft is not None
+    if x.dim() != (2 if varlen else 3) or conv_state.dim() != 3 or weight.dim() != 2:
+        raise ValueError("x must be [n_seq, T, dim] ([total_tokens, dim] with cu_draft), conv_state "
+                         "[n_slots, dim, S] and weight [dim, W]")
+    if varlen:
+        if T is None:
+            raise ValueError("packed drafts need T, the largest draft count")
+        _need_int32(cu_draft, "cu_draft")
+        if cu_draft.dim() != 1 or cu_draft.shape[0] < 1:
+            raise ValueError("cu_draft must be [n_seq + 1]")
+        n_seq, (total, dim) = cu_draft.shape[0] - 1, x.shape
+        T = int(T)
+    else:
+        n_seq, T, dim = x.shape
+        total = 0
     W = weight.shape[1]
     _need_shape(out, "out", x.shape)
     _need_shape(weight, "weight", (dim, W))
@@ -214,15 +230,16 @@ def make_verify_args(x, conv_state, weight, bias, out, window, *, layout, qk_cha
     for t, name in ((cache_idx, "cache_idx"), (state_off, "state_off"), (err, "err")):
         _need_int32(t, name, n=n_seq)
     _need_int32(parent, "parent", shape=(n_seq, T))
-    if x.stride(2) != 1 or out.stride(2) != 1 or conv_state.stride(2) != 1:
+    if x.stride(-1) != 1 or out.stride(-1) != 1 or conv_state.stride(2) != 1:
         raise ValueError("x, out and conv_state need a unit innermost stride")
     if not weight.is_contiguous() or (bias is not None and not bias.is_contiguous()):
         raise ValueError("weight and bias must be contiguous")
     ws = _window_strides(window, lay)
     return VerifyArgs(
         n_seq=n_seq, T=T, dim=dim, width=W, qk_channels=qk_channels, head_dim=head_dim, dtype=_dtype_code(x),
-        l2_eps=l2_eps, x=ptr(x, "x"), x_seq_stride=x.stride(0), x_tok_stride=x.stride(1),
-        out=ptr(out, "out"), out_seq_stride=out.stride(0), out_tok_stride=out.stride(1),
+        l2_eps=l2_eps, x=ptr(x, "x", total > 0 or not varlen), x_seq_stride=0 if varlen else x.stride(0),
+        x_tok_stride=x.stride(-2), out=ptr(out, "out", total > 0 or not varlen),
+        out_seq_stride=0 if varlen else out.stride(0), out_tok_stride=out.stride(-2),
         conv_state=ptr(conv_state, "conv_state"), n_slots=conv_state.shape[0], state_cols=conv_state.shape[2],
         state_slot_stride=conv_state.stride(0), state_ch_stride=conv_state.stride(1),
         cache_idx=ptr(cache_idx, "cache_idx", False), state_off=ptr(state_off, "state_off", False),
@@ -231,11 +248,12 @@ def make_verify_args(x, conv_state, weight, bias, out, window, *, layout, qk_cha
         window_layout=lay, wait_polls=int(wait_polls), win_seq_stride=ws[0], win_step_stride=ws[1], win_ch_stride=ws[2],
         win_col_stride=ws[3], err=ptr(err, "err", False),
         state_dtype=0 if conv_state.dtype == x.dtype else _dtype_code(conv_state) + 1,
-        parent=ptr(parent, "parent", False))
+        parent=ptr(parent, "parent", False), cu_draft=ptr(cu_draft, "cu_draft", False), total_tokens=total)
 
 
 def conv_verify(x, conv_state, weight, bias, out, window, *, layout, qk_channels, head_dim, l2_eps=1e-6,
-                cache_idx=None, state_off=None, err=None, parent=None, wait_polls=0, stream=None) -> None:
+                cache_idx=None, state_off=None, err=None, parent=None, wait_polls=0, cu_draft=None, T=None,
+                stream=None) -> None:
     """Queue one batched verify on ``stream`` (default: torch's current stream).
 
     Writes out, window, conv_state (and err); raises CvError on an invalid argument.  With layout
@@ -250,18 +268,18 @@ def conv_verify(x, conv_state, weight, bias, out, window, *, layout, qk_channels
         raise TypeError("bias must have the dtype of x")
     a = make_verify_args(x, conv_state, weight, bias, out, window, layout=layout, qk_channels=qk_channels,
                          head_dim=head_dim, l2_eps=l2_eps, cache_idx=cache_idx, state_off=state_off, err=err,
-                         parent=parent, wait_polls=wait_polls)
+                         parent=parent, wait_polls=wait_polls, cu_draft=cu_draft, T=T)
     rc = load_library().cv_conv_verify(ctypes.byref(a), _stream_ptr(stream))
     if rc != 0:
         raise CvError(rc, "cv_conv_verify")
 
 
 def verify_plan(x, conv_state, weight, bias, out, window, *, layout, qk_channels, head_dim, l2_eps=1e-6,
-                cache_idx=None, state_off=None, err=None, parent=None) -> LaunchPlan:
+                cache_idx=None, state_off=None, err=None, parent=None, cu_draft=None, T=None) -> LaunchPlan:
     """The launch cv_conv_verify would make (validates without touching the GPU)."""
     a = make_verify_args(x, conv_state, weight, bias, out, window, layout=layout, qk_channels=qk_channels,
                          head_dim=head_dim, l2_eps=l2_eps, cache_idx=cache_idx, state_off=state_off, err=err,
-                         parent=parent, check_device=False)
+                         parent=parent, cu_draft=cu_draft, T=T, check_device=False)
     pl = LaunchPlan()
     rc = load_library().cv_verify_plan(ctypes.byref(a), ctypes.byref(pl))
     if rc != 0:
@@ -270,12 +288,18 @@ def verify_plan(x, conv_state, weight, bias, out, window, *, layout, qk_channels
 
 
 def make_commit_args(conv_state, window, accept_len, *, layout, T, width, cache_idx=None, err=None,
-                     x=None, wait_polls=0, check_device=True) -> CommitArgs:
+                     x=None, wait_polls=0, cu_draft=None, total_tokens=None, check_device=True) -> CommitArgs:
     """Build cv_commit_args.  Layout "recompute": window is None and x is the verify's input
-    [n_seq, T, dim] (channel stride 1)."""
+    [n_seq, T, dim] (channel stride 1).  cu_draft: the matching verify's packed draft spans (x is
+    then [total_tokens, dim]); accept_len[s] must lie in 1..T_s."""
     lay = _layout_code(layout)
-    if x is not None and x.stride(2) != 1:
+    if x is not None and x.stride(-1) != 1:
         raise ValueError("x needs a unit channel stride")
+    varlen = cu_draft is not None
+    if varlen:
+        _need_int32(cu_draft, "cu_draft", n=accept_len.shape[0] + 1)
+        if total_tokens is None:
+            total_tokens = x.shape[0] if x is not None else 0
     ptr = _dev_ptr if check_device else (lambda t, n, required=True: None if t is None else t.data_ptr())
     ws = _window_strides(window, lay)
     if conv_state.dim() != 3 or conv_state.stride(2) != 1:
@@ -290,6 +314,9 @@ def make_commit_args(conv_state, window, accept_len, *, layout, T, width, cache_
         _need_shape(window, "window", (n_seq, T, dim, width - 1))
     elif lay == DEDUP:
         _need_shape(window, "window", (n_seq, dim, T + width - 2))
+    elif varlen:
+        if x is None or x.dim() != 2 or x.shape[1] != dim or x.shape[0] != total_tokens:
+            raise ValueError(f"x must be [total_tokens, {dim}] with packed drafts")
     else:
         _need_shape(x, "x", (n_seq, T, dim))
     return CommitArgs(
@@ -299,20 +326,21 @@ def make_commit_args(conv_state, window, accept_len, *, layout, T, width, cache_
         state_cols=conv_state.shape[2], window_layout=lay, cache_idx=ptr(cache_idx, "cache_idx", False),
         window=ptr(window, "window", lay != RECOMPUTE), win_seq_stride=ws[0], win_step_stride=ws[1],
         win_ch_stride=ws[2], win_col_stride=ws[3], accept_len=ptr(accept_len, "accept_len"),
-        err=ptr(err, "err", False), x=ptr(x, "x", lay == RECOMPUTE),
-        x_seq_stride=x.stride(0) if x is not None else 0, x_tok_stride=x.stride(1) if x is not None else 0,
-        wait_polls=int(wait_polls))
+        err=ptr(err, "err", False), x=ptr(x, "x", lay == RECOMPUTE and not (varlen and total_tokens == 0)),
+        x_seq_stride=x.stride(0) if x is not None and not varlen else 0,
+        x_tok_stride=x.stride(-2) if x is not None else 0, wait_polls=int(wait_polls),
+        cu_draft=ptr(cu_draft, "cu_draft", False), total_tokens=int(total_tokens or 0))
 
 
 def conv_commit(conv_state, window, accept_len, *, layout, T, width, cache_idx=None, err=None, x=None,
-                wait_polls=0, stream=None) -> None:
+                wait_polls=0, cu_draft=None, total_tokens=None, stream=None) -> None:
     """Queue the commit: conv_state[slot] <- snapshot accept_len[s]-1 of sequence s (rebuilt from the
     kept window and x with layout "recompute")."""
     for t in (window, x):
         if t is not None and t.dtype != conv_state.dtype:
             raise TypeError("window / x and conv_state must share one dtype")
     a = make_commit_args(conv_state, window, accept_len, layout=layout, T=T, width=width, cache_idx=cache_idx,
-                         err=err, x=x, wait_polls=wait_polls)
+                         err=err, x=x, wait_polls=wait_polls, cu_draft=cu_draft, total_tokens=total_tokens)
     rc = load_library().cv_conv_commit(ctypes.byref(a), _stream_ptr(stream))
     if rc != 0:
         raise CvError(rc, "cv_conv_commit")

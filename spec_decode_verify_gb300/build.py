@@ -18,7 +18,8 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libconvverify.so")
 INCLUDE = os.path.join(ROOT, "include")
 # the verify library, then (last) the bandwidth probe of bench.py --probe-mix, linked on its own
-SOURCES = ["cv_abi.cu"] + [f"cv_inst_{d}_w{w}.cu" for d in ("bf16", "f32") for w in (2, 3, 4)] + ["cv_probe.cu"]
+SOURCES = (["cv_abi.cu"] + [f"cv_inst_{d}_w{w}.cu" for d in ("bf16", "f32") for w in (2, 3, 4)] +
+           [f"cv_inst_varlen_{d}_w{w}.cu" for d in ("bf16", "f32") for w in (2, 3, 4)] + ["cv_probe.cu"])
 PROBE_LIB = os.path.join(BUILD, "libcvprobe.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
@@ -57,7 +58,7 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
             sys.stderr.write(r.stdout + r.stderr)
         return obj
 
-    with cf.ThreadPoolExecutor(max_workers=min(8, len(SOURCES))) as ex:
+    with cf.ThreadPoolExecutor(max_workers=min(os.cpu_count() or 8, len(SOURCES))) as ex:
         objs = list(ex.map(compile_one, SOURCES))
     probe_obj = objs.pop()  # the bandwidth probe goes into its own library
     for lib, parts in ((LIB, objs), (PROBE_LIB, [probe_obj])):

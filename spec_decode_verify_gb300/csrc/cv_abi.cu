@@ -80,7 +80,10 @@ DeviceLimits device_limits() {
     return d;
 }
 
-bool pipe_compacts(const cv_verify_args *a) { return a->cache_idx != nullptr && a->n_seq <= kCompactMaxSeq; }
+// the list of active sequences (padded ones dropped; packed drafts ordered by draft count)
+bool pipe_compacts(const cv_verify_args *a) {
+    return (a->cache_idx != nullptr || a->cu_draft != nullptr) && a->n_seq <= kCompactMaxSeq;
+}
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool stride16(long long stride_elems, int esize) { return ((stride_elems * esize) & 15) == 0; }
@@ -95,6 +98,17 @@ const cvk::KernelSet &kernel_set(int dtype, int width) {
     if (width == 2) return cvk::kernels_f32_w2();
     if (width == 3) return cvk::kernels_f32_w3();
     return cvk::kernels_f32_w4();
+}
+
+const cvk::VarlenSet &varlen_set(int dtype, int width) {
+    if (dtype == CV_BF16) {
+        if (width == 2) return cvk::varlen_bf16_w2();
+        if (width == 3) return cvk::varlen_bf16_w3();
+        return cvk::varlen_bf16_w4();
+    }
+    if (width == 2) return cvk::varlen_f32_w2();
+    if (width == 3) return cvk::varlen_f32_w3();
+    return cvk::varlen_f32_w4();
 }
 
 int check_verify(const cv_verify_args *a) {
@@ -112,8 +126,10 @@ int check_verify(const cv_verify_args *a) {
     if (a->window_layout != CV_WINDOW_DENSE && a->window_layout != CV_WINDOW_DEDUP && !nowin) return CV_ERR_LAYOUT;
     if (a->window_layout == CV_WINDOW_DEDUP && a->win_step_stride != a->win_col_stride) return CV_ERR_LAYOUT;
     if (hist && a->state_cols < a->T + a->width - 2) return CV_ERR_SHAPE;
-    // tree verify: dense snapshots only, one dtype
+    // tree verify: dense snapshots only, one dtype; packed drafts are chains
     if (a->parent && a->window_layout != CV_WINDOW_DENSE) return CV_ERR_LAYOUT;
+    if (a->parent && a->cu_draft) return CV_ERR_LAYOUT;
+    if (a->cu_draft && a->total_tokens < 0) return CV_ERR_SHAPE;
     if (a->parent && a->state_dtype != CV_STATE_SAME && a->state_dtype - 1 != a->dtype) return CV_ERR_DTYPE;
     if (a->qk_channels < 0 || a->qk_channels > a->dim) return CV_ERR_HEAD_DIM;
     if (a->qk_channels > 0 && (!pow2(a->head_dim) || a->head_dim < 8 || a->head_dim > 256 ||
@@ -125,7 +141,9 @@ int check_verify(const cv_verify_args *a) {
     if (!nowin && (a->win_seq_stride < 0 || a->win_step_stride < 0 || a->win_ch_stride < 0 || a->win_col_stride < 0))
         return CV_ERR_STRIDE;
     if (a->dim > 1 && a->state_ch_stride < a->state_cols) return CV_ERR_STRIDE;
-    if (a->n_seq > 0 && (!a->x || !a->out || !a->conv_state || !a->weight || (!nowin && !a->window)))
+    // (packed drafts with no rows at all need no x or out)
+    const bool rows = !a->cu_draft || a->total_tokens > 0;
+    if (a->n_seq > 0 && ((rows && (!a->x || !a->out)) || !a->conv_state || !a->weight || (!nowin && !a->window)))
         return CV_ERR_NULL_POINTER;
     if (a->n_seq > 0) {
         const void *outs[2] = {a->out, nowin ? nullptr : a->window};
@@ -141,8 +159,11 @@ int check_verify(const cv_verify_args *a) {
 // x, out, taps and bias allow 16-byte vectors and bulk copies of whole channel blocks.
 bool io_packed(const cv_verify_args *a, int esize) {
     if (a->dim % 8 != 0) return false;
-    if (!aligned16(a->x) || !stride16(a->x_seq_stride, esize) || !stride16(a->x_tok_stride, esize)) return false;
-    if (!aligned16(a->out) || !stride16(a->out_seq_stride, esize) || !stride16(a->out_tok_stride, esize)) return false;
+    // (packed drafts ignore the sequence strides)
+    const bool vl = a->cu_draft != nullptr;
+    if (!aligned16(a->x) || !(vl || stride16(a->x_seq_stride, esize)) || !stride16(a->x_tok_stride, esize)) return false;
+    if (!aligned16(a->out) || !(vl || stride16(a->out_seq_stride, esize)) || !stride16(a->out_tok_stride, esize))
+        return false;
     return aligned16(a->weight) && (!a->bias || aligned16(a->bias));
 }
 
@@ -239,14 +260,15 @@ int plan_verify(const cv_verify_args *a, cv_launch_plan *pl) {
     // needs rows of exactly T+W-2 columns
     const bool rows_packed = aligned16(a->conv_state) && stride16(a->state_slot_stride, ssize) &&
                              a->state_ch_stride == a->state_cols;
-    // (mixed dtypes: compiled for T <= kMaxMixedT)
-    bool pipe_ok = (!mixed || a->T <= cvk::kMaxMixedT) && io_packed(a, esize) && a->T <= ks.max_static_t &&
-                   rows_packed && (hist ? a->state_cols == a->T + R - 1 : (recomp || fast));
+    const bool varlen = a->cu_draft != nullptr;
+    // (mixed dtypes: compiled for T <= kMaxMixedT; packed drafts: one dtype)
+    bool pipe_ok = (!mixed || a->T <= cvk::kMaxMixedT) && !(mixed && varlen) && io_packed(a, esize) &&
+                   a->T <= ks.max_static_t && rows_packed && (hist ? a->state_cols == a->T + R - 1 : (recomp || fast));
     const bool wide = !hist && a->state_cols != R;
     // (wide rows cost whole-row reads and element stores of the window; the pipeline pays that
     // back only when every block walks at least two units, otherwise the one-pass kernel wins)
     // (mixed dtypes have no one-pass kernel)
-    if (pipe_ok && wide && fast && !mixed && units_per_pipe_block(a, cpt, lim.sms) < 2.0) pipe_ok = false;
+    if (pipe_ok && wide && fast && !mixed && !varlen && units_per_pipe_block(a, cpt, lim.sms) < 2.0) pipe_ok = false;
     if (pipe_ok) {
         auto part = [](long long b) { return (b + 127) / 128 * 128; };
         int threads = kPipeThreads;
@@ -261,7 +283,8 @@ int plan_verify(const cv_verify_args *a, cv_launch_plan *pl) {
         const long long stage = part(a->T * bc * esize) + part((long long)a->state_cols * bc * ssize);
         long long image = (hist || recomp || wide) ? 0 : part(R * bc * ssize);
         if (a->window_layout == CV_WINDOW_DEDUP || hist) image += part(Q * bc * ssize);
-        const long long smem = 2 * stage + 2 * image + 32 + (pipe_compacts(a) ? 16 + 4LL * a->n_seq : 0);
+        const long long smem = 2 * stage + 2 * image + cvk::kPipeInfoBytes +
+                               (pipe_compacts(a) ? 4LL * cvk::pipe_aux_ints(varlen, a->T) + 4LL * a->n_seq : 0);
         int per_sm = (int)(lim.smem_per_sm / (smem + kSmemPerBlockReserved));
         if (per_sm > pipe_blocks_per_sm(cpt, a->T)) per_sm = pipe_blocks_per_sm(cpt, a->T);
         const int nst = (smem <= lim.smem_per_block && per_sm >= 1) ? 2 : 0;
@@ -282,7 +305,7 @@ int plan_verify(const cv_verify_args *a, cv_launch_plan *pl) {
             return CV_OK;
         }
     }
-    if (fast && !mixed) {
+    if (fast && !mixed && !varlen) {
         // 4 channels per thread (twice the threads of 8) unless an L2 group would span more than a warp
         int threads = kFastThreads;
         while (threads > 32 && cpt * (threads / 2) >= a->dim) threads /= 2;
@@ -388,6 +411,8 @@ int launch_verify(const cv_verify_args *a, const cv_launch_plan &pl, cudaStream_
     p.w_col = a->win_col_stride;
     p.err = a->err;
     p.wait_polls = a->wait_polls;
+    p.cu_draft = a->cu_draft;
+    p.total_tokens = a->total_tokens;
     p.n_seq = a->n_seq;
     p.T = a->T;
     p.dim = a->dim;
@@ -399,8 +424,9 @@ int launch_verify(const cv_verify_args *a, const cv_launch_plan &pl, cudaStream_
     const int ssize = state_dtype_of(a) == CV_BF16 ? 2 : 4;
     p.pitch = pl.channels_per_block + 16 / (mixed ? 4 : esize);
     p.eps = a->l2_eps;
-    p.x_vec = aligned16(a->x) && stride16(a->x_seq_stride, esize) && stride16(a->x_tok_stride, esize);
-    p.out_vec = aligned16(a->out) && stride16(a->out_seq_stride, esize) && stride16(a->out_tok_stride, esize);
+    const bool vl = a->cu_draft != nullptr;  // (packed drafts ignore the sequence strides)
+    p.x_vec = aligned16(a->x) && (vl || stride16(a->x_seq_stride, esize)) && stride16(a->x_tok_stride, esize);
+    p.out_vec = aligned16(a->out) && (vl || stride16(a->out_seq_stride, esize)) && stride16(a->out_tok_stride, esize);
     p.st_vec = state_packed(a->conv_state, a->state_slot_stride, a->state_ch_stride, a->width, ssize);
     p.w_vec = aligned16(a->weight);
     p.b_vec = a->bias ? aligned16(a->bias) : 0;
@@ -419,7 +445,9 @@ int launch_verify(const cv_verify_args *a, const cv_launch_plan &pl, cudaStream_
     cvk::VerifyKernel k = pl.path == 0   ? (mixed ? ks.generic_mixed : ks.generic)
                           : pl.path == 1 ? ks.fast[ci][a->T]
                           : pl.path == 2 ? ks.fast[ci][0]
-                          : pl.path == 3 ? (mixed ? ks.pipe_mixed[ci][a->T] : ks.pipe[ci][a->T])
+                          : pl.path == 3 ? (mixed ? ks.pipe_mixed[ci][a->T]
+                                            : a->cu_draft ? varlen_set(a->dtype, a->width).pipe[ci][a->T]
+                                                          : ks.pipe[ci][a->T])
                                          : ks.tree;
     if (ensure_smem(reinterpret_cast<const void *>(k), pl.smem_bytes) != cudaSuccess) return CV_ERR_LAUNCH;
     // the pipelined kernel ORs the per-sequence bits into err (several blocks share a sequence)
@@ -445,9 +473,11 @@ int check_commit(const cv_commit_args *a) {
     if (!recomp && (a->win_seq_stride < 0 || a->win_step_stride < 0 || a->win_ch_stride < 0 || a->win_col_stride < 0))
         return CV_ERR_STRIDE;
     if (recomp && (a->x_seq_stride < 0 || a->x_tok_stride < 0)) return CV_ERR_STRIDE;
+    if (a->cu_draft && a->total_tokens < 0) return CV_ERR_SHAPE;
     if (a->dim > 1 && a->state_ch_stride < a->state_cols) return CV_ERR_STRIDE;
     if (a->n_seq > 0 && (!a->conv_state || !a->accept_len)) return CV_ERR_NULL_POINTER;
-    if (a->n_seq > 0 && (recomp ? !a->x : !a->window)) return CV_ERR_NULL_POINTER;
+    if (a->n_seq > 0 && (recomp ? (!a->x && !(a->cu_draft && a->total_tokens == 0)) : !a->window))
+        return CV_ERR_NULL_POINTER;
     if (a->n_seq > 0 && (recomp ? a->conv_state == a->x : a->conv_state == a->window)) return CV_ERR_ALIAS;
     return CV_OK;
 }
@@ -470,6 +500,10 @@ int launch_commit(const cv_commit_args *a, cudaStream_t stream) {
     p.accept_len = a->accept_len;
     p.err = a->err;
     p.wait_polls = a->wait_polls;
+    p.cu_draft = a->cu_draft;
+    p.total_tokens = a->total_tokens;
+    p.cu_draft = a->cu_draft;
+    p.total_tokens = a->total_tokens;
     p.n_seq = a->n_seq;
     p.T = a->T;
     p.dim = a->dim;

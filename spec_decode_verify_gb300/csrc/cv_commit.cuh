@@ -23,6 +23,19 @@ namespace cvk {
 
 constexpr unsigned kCommitWaitPolls = 1u << 20;  // mbarrier polls before a block gives up
 
+// Status of sequence s for a commit: 1 = slot out of range, 16 = invalid packed draft span, 4 =
+// accept count a outside 1..T_s.  Sets ts to the sequence's draft count (T, or its packed span's
+// length) and row0 to its first packed row.  A sequence with ts = 0 has nothing to commit.
+__device__ __forceinline__ int commit_status(const CommitParams &p, int s, int slot, int a, int &ts, int &row0) {
+    ts = p.T;
+    row0 = 0;
+    if (slot < 0) return 0;
+    int st = slot >= p.n_slots ? 1 : 0;
+    if (p.cu_draft) st |= draft_span(p.cu_draft, s, p.T, p.total_tokens, ts, row0);
+    if (!(st & kSeqBadSpan) && ts > 0 && (a < 1 || a > ts)) st |= 4;
+    return st;
+}
+
 template <typename B, int W>
 __global__ void __launch_bounds__(128) commit_kernel(const __grid_constant__ CommitParams p) {
     grid_dep_wait();
@@ -36,13 +49,10 @@ __global__ void __launch_bounds__(128) commit_kernel(const __grid_constant__ Com
     const int NT = blockDim.x;
     const int slot = p.cache_idx ? __ldg(p.cache_idx + s) : s;
     const int a = __ldg(p.accept_len + s);
-    int status = 0;
-    if (slot >= 0) {
-        if (slot >= p.n_slots) status |= 1;
-        if (a < 1 || a > p.T) status |= 4;
-    }
+    int ts, row0;
+    const int status = commit_status(p, s, slot, a, ts, row0);
     if (p.err && blockIdx.x == 0 && tid == 0) p.err[s] = status;
-    if (slot < 0 || status) return;
+    if (slot < 0 || status || ts == 0) return;
 
     const int BC = 8 * NT;
     const int c0 = blockIdx.x * BC;
@@ -116,11 +126,8 @@ __global__ void __launch_bounds__(64) commit_rows(const __grid_constant__ Commit
     }
     const int slot = p.cache_idx ? __ldg(p.cache_idx + s) : s;
     const int a = __ldg(p.accept_len + s);
-    int status = 0;
-    if (slot >= 0) {
-        if (slot >= p.n_slots) status |= 1;
-        if (a < 1 || a > p.T) status |= 4;
-    }
+    int ts, row0;
+    const int status = commit_status(p, s, slot, a, ts, row0);
     if (p.err && blockIdx.x == 0 && tid == 0 && status) atomicOr(p.err + s, status);
     __syncthreads();  // the barrier's initialisation is visible to every waiting thread
     const unsigned polls = p.wait_polls == 0 ? kCommitWaitPolls : p.wait_polls < 0 ? 0u : (unsigned)p.wait_polls;
@@ -132,7 +139,7 @@ __global__ void __launch_bounds__(64) commit_rows(const __grid_constant__ Commit
         }
         return;
     }
-    if (slot < 0 || status) return;
+    if (slot < 0 || status || ts == 0) return;
     const B *sm = reinterpret_cast<const B *>(smem);
     B *d = reinterpret_cast<B *>(p.state) + (long long)slot * p.st_slot + (long long)c0 * R;
     const int col0 = a - 1;
@@ -169,17 +176,14 @@ __global__ void __launch_bounds__(128) commit_recompute(const __grid_constant__ 
     const int s = blockIdx.y;
     const int slot = p.cache_idx ? __ldg(p.cache_idx + s) : s;
     const int a = __ldg(p.accept_len + s);
-    int status = 0;
-    if (slot >= 0) {
-        if (slot >= p.n_slots) status |= 1;
-        if (a < 1 || a > p.T) status |= 4;
-    }
+    int ts, row0;
+    const int status = commit_status(p, s, slot, a, ts, row0);
     if (p.err && blockIdx.x == 0 && threadIdx.x == 0) p.err[s] = status;
-    if (slot < 0 || status) return;
+    if (slot < 0 || status || ts == 0) return;
     const int c = blockIdx.x * blockDim.x + threadIdx.x;
     if (c >= p.dim) return;
     B *row = reinterpret_cast<B *>(p.state) + (long long)slot * p.st_slot + (long long)c * p.st_ch;
-    const B *xs = reinterpret_cast<const B *>(p.x) + (long long)s * p.x_seq + c;
+    const B *xs = reinterpret_cast<const B *>(p.x) + (p.cu_draft ? (long long)row0 * p.x_tok : (long long)s * p.x_seq) + c;
     B v[R];
 #pragma unroll
     for (int k = 0; k < R; ++k) {
@@ -208,18 +212,15 @@ __global__ void __launch_bounds__(128) commit_recompute_vec(const __grid_constan
     const int s = blockIdx.y;
     const int slot = p.cache_idx ? __ldg(p.cache_idx + s) : s;
     const int a = __ldg(p.accept_len + s);
-    int status = 0;
-    if (slot >= 0) {
-        if (slot >= p.n_slots) status |= 1;
-        if (a < 1 || a > p.T) status |= 4;
-    }
+    int ts, row0;
+    const int status = commit_status(p, s, slot, a, ts, row0);
     if (p.err && blockIdx.x == 0 && threadIdx.x == 0) p.err[s] = status;
-    if (slot < 0 || status) return;
+    if (slot < 0 || status || ts == 0) return;
     const int c = 8 * (blockIdx.x * blockDim.x + threadIdx.x);
     if (c >= p.dim) return;  // dim % 8 == 0 on this path
     uint4 *run = reinterpret_cast<uint4 *>(reinterpret_cast<B *>(p.state) + (long long)slot * p.st_slot +
                                            (long long)c * R);
-    const B *xs = reinterpret_cast<const B *>(p.x) + (long long)s * p.x_seq + c;
+    const B *xs = reinterpret_cast<const B *>(p.x) + (p.cu_draft ? (long long)row0 * p.x_tok : (long long)s * p.x_seq) + c;
     union {
         uint4 v[NSV];
         U e[8 * R];

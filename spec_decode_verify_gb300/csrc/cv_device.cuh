@@ -34,7 +34,15 @@ struct VerifyParams {
     int x_vec, out_vec, st_vec, w_vec, b_vec;  // 16-byte vector access allowed (checked on the host)
     int st_packed;  // tree verify: the committed windows are packed, 16-byte-aligned [dim][W-1] rows
     int wait_polls;  // polls of the first bounded wait per unit: 0 = the default, < 0 = none (gives up at once)
+    const int *cu_draft;  // packed ragged drafts: [n_seq + 1] row offsets into x and out, or null
+    int total_tokens;     // rows of x and out when cu_draft is given
 };
+
+// Pipelined verify: shared memory after the stages and images holds 2 mbarriers, then 8 ints of
+// unit information (slots, state offsets, draft counts, first rows of the two units in flight),
+// then the compaction scratch (pipe_aux_ints of them) and the list of active sequences.
+constexpr int kPipeInfoBytes = 16 + 32;
+__host__ __device__ constexpr int pipe_aux_ints(bool varlen, int T) { return varlen ? 5 * (T + 2) : 4; }
 
 // Tree verify: channels per block, 8 per lane of a warp.
 constexpr int kTreeChannels = 256;
@@ -52,6 +60,8 @@ struct CommitParams {
     const void *x;  // mode 3: the verify's input
     long long x_seq, x_tok;
     int wait_polls;  // polls of the bounded wait for the staged rows: 0 = the default, < 0 = none
+    const int *cu_draft;  // packed ragged drafts of the matching verify, or null (T tokens each)
+    int total_tokens;
 };
 
 struct PrefillParams {
@@ -81,6 +91,22 @@ __device__ __forceinline__ int seq_status(int slot, int off, int n_slots, int st
         if (off < 0 || off > state_cols - R) st |= 2;
     }
     return st;
+}
+
+constexpr int kSeqBadSpan = 16;  // err bit: a packed draft span (or prefill span) is invalid
+
+// Packed ragged drafts (sglang PR #46184, "Related upstream work": target verify on packed ragged
+// tokens): sequence s owns rows [cu[s], cu[s+1]) of x and out.  Sets ts = its draft count and row0
+// = its first row; returns kSeqBadSpan when the span is reversed, leaves [0, total) or holds more
+// than T rows (the sequence is then left untouched).
+__device__ __forceinline__ int span_status(int b, int e, int T, int total) {
+    return (b < 0 || e < b || e > total || e - b > T) ? kSeqBadSpan : 0;
+}
+__device__ __forceinline__ int draft_span(const int *cu, int s, int T, int total, int &ts, int &row0) {
+    const int b = __ldg(cu + s), e = __ldg(cu + s + 1);
+    row0 = b;
+    ts = e - b;
+    return span_status(b, e, T, total);
 }
 
 template <typename B> __device__ __forceinline__ float widen(B b);

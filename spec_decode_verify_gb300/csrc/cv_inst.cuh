@@ -1,6 +1,29 @@
 // Builds the kernel table of one (element type, conv width); included once per instantiation unit
-// with CV_INST_B, CV_INST_W, CV_INST_MAXT and CV_INST_NAME defined.
+// with CV_INST_B, CV_INST_W, CV_INST_MAXT and CV_INST_NAME defined, and CV_INST_VARLEN defined for
+// the units that hold the packed-ragged-draft variants of the pipelined kernel (VarlenSet).
 #include <utility>
+
+#ifdef CV_INST_VARLEN
+#include "cv_launch.h"
+#include "cv_verify_pipe.cuh"
+
+namespace cvk {
+namespace {
+template <typename B, int W, int... Ts>
+VarlenSet make_varlen(std::integer_sequence<int, Ts...>) {
+    VarlenSet k{};
+    ((k.pipe[0][Ts + 1] = verify_pipe<B, W, Ts + 1, 4, B, true>), ...);
+    ((k.pipe[1][Ts + 1] = verify_pipe<B, W, Ts + 1, 8, B, true>), ...);
+    return k;
+}
+}  // namespace
+
+const VarlenSet &CV_INST_NAME() {
+    static const VarlenSet k = make_varlen<CV_INST_B, CV_INST_W>(std::make_integer_sequence<int, CV_INST_MAXT>{});
+    return k;
+}
+}  // namespace cvk
+#else
 
 #include "cv_commit.cuh"
 #include "cv_launch.h"
@@ -52,3 +75,4 @@ const KernelSet &CV_INST_NAME() {
     return k;
 }
 }  // namespace cvk
+#endif  // CV_INST_VARLEN

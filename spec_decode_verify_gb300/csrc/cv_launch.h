@@ -37,6 +37,19 @@ struct KernelSet {
     PrefillKernel prefill[2];
 };
 
+// The pipelined kernel for packed ragged drafts, pipe[c][T] as in KernelSet (T = the largest draft
+// count), compiled in translation units of their own.
+struct VarlenSet {
+    VerifyKernel pipe[2][kMaxStaticT + 1];
+};
+
+const VarlenSet &varlen_bf16_w2();
+const VarlenSet &varlen_bf16_w3();
+const VarlenSet &varlen_bf16_w4();
+const VarlenSet &varlen_f32_w2();
+const VarlenSet &varlen_f32_w3();
+const VarlenSet &varlen_f32_w4();
+
 const KernelSet &kernels_bf16_w2();
 const KernelSet &kernels_bf16_w3();
 const KernelSet &kernels_bf16_w4();

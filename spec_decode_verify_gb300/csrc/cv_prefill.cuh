@@ -24,7 +24,6 @@
 namespace cvk {
 
 constexpr int kPrefillBatch = 8;  // tokens per batch; the next batch's rows load during this one
-constexpr int kSeqBadSpan = 16;     // err bit: the sequence's token span is invalid
 
 template <typename B, int W, int CPT>
 __global__ void __launch_bounds__(128, CPT == 4 ? 4 : 2) prefill_conv(const __grid_constant__ PrefillParams p) {

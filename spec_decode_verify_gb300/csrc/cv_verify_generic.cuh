@@ -9,7 +9,9 @@
 // and every snapshot layout and the committed window are written from that tile in destination
 // order (channel-major runs, channel-stride-1 runs, or element by element).  The arithmetic is the
 // same as the fast path's: fp32, bias first, taps in order (conv_chain), SiLU, L2
-// over the head_dim group as an xor-shuffle over head_dim/8 lanes.
+// over the head_dim group as an xor-shuffle over head_dim/8 lanes.  Packed ragged drafts (p.cu_draft):
+// the sequence's T_s rows start at row cu[s] of x and out, and everything runs over T_s tokens
+// (snapshot steps and deduplicated columns past them stay untouched; T_s = 0 writes only the state).
 #pragma once
 
 #include <type_traits>
@@ -169,7 +171,9 @@ __global__ void __launch_bounds__(256) verify_generic(const __grid_constant__ Ve
 
     const int slot = p.cache_idx ? p.cache_idx[s] : s;
     const int off = p.state_off ? p.state_off[s] : 0;
-    const int status = seq_status(slot, off, p.n_slots, p.state_cols, R);
+    int status = seq_status(slot, off, p.n_slots, p.state_cols, R);
+    int Ts = T, row0 = 0;  // draft tokens of this sequence and (packed drafts) its first row
+    if (p.cu_draft && slot >= 0) status |= draft_span(p.cu_draft, s, T, p.total_tokens, Ts, row0);
     if (p.err && blockIdx.x == 0 && tid == 0) p.err[s] = status;
     if (slot < 0 || status) return;  // padded or rejected: touch nothing (uniform per block)
     if ((long long)(T + R) * pitch * (long long)sizeof(TT) > (long long)dynamic_smem_bytes()) return;  // launch mismatch
@@ -180,25 +184,25 @@ __global__ void __launch_bounds__(256) verify_generic(const __grid_constant__ Ve
     const bool full8 = (my == 8);
 
     // (1) x_0..x_{T-1} -> tile rows R..R+T-1 (asynchronous 16-byte copies, no registers)
-    const B *xs = reinterpret_cast<const B *>(p.x) + (long long)s * p.x_seq + c0;
+    const B *xs = reinterpret_cast<const B *>(p.x) + (p.cu_draft ? (long long)row0 * p.x_tok : (long long)s * p.x_seq) + c0;
     if (MIXED) {
-        for (int i = tid; i < T * nch; i += blockDim.x) {
+        for (int i = tid; i < Ts * nch; i += blockDim.x) {
             const int t = i / nch, c = i - t * nch;
             tile[(R + t) * pitch + c] = to_tile<TT>(xs[t * p.x_tok + c]);
         }
     } else if (p.x_vec) {
         if (full8) {
-            for (int t = 0; t < T; ++t) {
+            for (int t = 0; t < Ts; ++t) {
 #pragma unroll
                 for (int i = 0; i < Oct<B>::NV; ++i)
                     cp_async16(tile + (R + t) * pitch + cl + i * (16 / sizeof(B)), xs + t * p.x_tok + cl + i * (16 / sizeof(B)));
             }
         } else {
-            for (int t = 0; t < T; ++t)
+            for (int t = 0; t < Ts; ++t)
                 for (int e = 0; e < my; ++e) tile[(R + t) * pitch + cl + e] = to_tile<TT>(xs[t * p.x_tok + cl + e]);
         }
     } else {
-        for (int i = tid; i < T * nch; i += blockDim.x) {
+        for (int i = tid; i < Ts * nch; i += blockDim.x) {
             const int t = i / nch, c = i - t * nch;
             tile[(R + t) * pitch + c] = to_tile<TT>(xs[t * p.x_tok + c]);
         }
@@ -285,19 +289,21 @@ __global__ void __launch_bounds__(256) verify_generic(const __grid_constant__ Ve
     } else if (p.hist) {
         // history-row state: the snapshot row [full[1 .. W-2], x_0 .. x_{T-1}] replaces columns
         // [0, T+W-2) of the state row (every thread read its committed window before the barrier)
+        // (no draft token, no snapshot: a packed sequence with T_s = 0 writes nothing here)
         BS *sb = reinterpret_cast<BS *>(p.state) + (long long)slot * p.st_slot + (long long)c0 * p.st_ch;
-        write_view<TT, BS>(tile, pitch, 1, T + R - 1, sb, p.st_ch, 1, nch, R);
+        if (Ts > 0) write_view<TT, BS>(tile, pitch, 1, Ts + R - 1, sb, p.st_ch, 1, nch, R);
     } else {
         BS *wb = reinterpret_cast<BS *>(p.win) + (long long)s * p.w_seq;
         if (p.dedup) {
-            write_view<TT, BS>(tile, pitch, 1, T + R - 1, wb + (long long)c0 * p.w_ch, p.w_ch, p.w_col, nch, R);
+            if (Ts > 0)
+                write_view<TT, BS>(tile, pitch, 1, Ts + R - 1, wb + (long long)c0 * p.w_ch, p.w_ch, p.w_col, nch, R);
         } else {
-            for (int t = 0; t < T; ++t)
+            for (int t = 0; t < Ts; ++t)
                 write_view<TT, BS>(tile, pitch, t + 1, R, wb + t * p.w_step + (long long)c0 * p.w_ch, p.w_ch, p.w_col,
                                    nch, R);
         }
         BS *sb = reinterpret_cast<BS *>(p.state) + (long long)slot * p.st_slot + (long long)c0 * p.st_ch;
-        write_view<TT, BS>(tile, pitch, T, R, sb, p.st_ch, 1, nch, R);
+        write_view<TT, BS>(tile, pitch, Ts, R, sb, p.st_ch, 1, nch, R);
     }
 
     // (5) conv + SiLU (+ L2 over the head_dim group) for every token, outputs stored as vectors
@@ -305,8 +311,8 @@ __global__ void __launch_bounds__(256) verify_generic(const __grid_constant__ Ve
     const bool l2_block = (c0 < p.qk_channels);       // block-uniform
     const bool l2_mine = (c0 + cl) < p.qk_channels;   // whole 8-channel group is q|k or V
     const int lanes = p.head_dim >> 3;                // 1..32 threads per group
-    B *ob = reinterpret_cast<B *>(p.out) + (long long)s * p.out_seq + c0 + cl;
-    for (int t = 0; t < T; ++t) {
+    B *ob = reinterpret_cast<B *>(p.out) + (p.cu_draft ? (long long)row0 * p.out_tok : (long long)s * p.out_seq) + c0 + cl;
+    for (int t = 0; t < Ts; ++t) {
         float xv[8];
         if (full8) {
             Oct<TT> o;

@@ -34,6 +34,15 @@
 // bits, x elements enter them widened exactly (bf16 -> fp32) or rounded to the nearest bf16, and
 // the conv takes every input at its own precision with each product rounded (fp32 state values
 // make the products inexact).
+// Packed ragged drafts (VL; sglang PR #46184, "Related upstream work": target verify on packed ragged
+// tokens, the tile store covering the packed rows): sequence s owns rows [cu[s], cu[s+1]) of x and
+// out, T_s <= TS of them.  A unit copies only its T_s x rows; outputs, dense snapshot steps and
+// deduplicated columns past T_s are not written (a full row still leaves as one bulk copy; a shorter
+// one is copied out of the staged image by the whole block, word by word, with the columns past
+// T_s+W-2 skipped); the committed window full[T_s .. T_s+W-2] is gathered from the staged rows.
+// Units of long and short drafts differ in cost, so the list of active sequences is ordered by
+// draft count, longest first (a counting sort every block performs identically): consecutive
+// units of the round-robin walk then have similar cost and every block gets a similar mix.
 // Preconditions (checked on the host): those of the fast path, packed 16-byte-aligned state rows
 // (state_ch_stride == state_cols; exactly T+W-2 columns for the history layout), T <= 17 (bf16) /
 // 8 (fp32), head_dim / CPT <= 32.
@@ -53,11 +62,12 @@ __host__ __device__ constexpr int pipe_align(int bytes) { return bytes % 16 == 0
 // Bytes of one stage for a block of bc channels (x rows, windows, taps, bias), each part 128-aligned.
 __host__ __device__ constexpr long long pipe_part(long long b) { return (b + 127) / 128 * 128; }
 
-template <typename B, int W, int TS, int CPT, typename S = B>
+template <typename B, int W, int TS, int CPT, typename S = B, bool VL = false>
 __global__ void __launch_bounds__(128, (CPT == 4 && TS <= 8) ? 4 : 2) verify_pipe(const __grid_constant__ VerifyParams p) {
     grid_dep_wait();
     grid_dep_launch();
     static_assert(TS > 0, "the pipelined kernel needs a compile-time T");
+    static_assert(!VL || std::is_same_v<B, S>, "packed ragged drafts use one dtype");
     // (taps and bias are read from global memory, so W*CPT*ES need only be 8-byte aligned)
     constexpr int R = W - 1;
     constexpr int Q = TS + R - 1;  // dedup row columns
@@ -88,19 +98,22 @@ __global__ void __launch_bounds__(128, (CPT == 4 && TS <= 8) ? 4 : 2) verify_pip
 
     // shared memory: stage 0, stage 1 (x rows + committed windows, or whole history rows), image
     // buffers 0 and 1 (dedup row image + committed-window image, or the history row image alone),
-    // 2 mbarriers, 2 unit slots, 2 unit state offsets, then (when compacting) 4 warp counts and the
-    // list of active sequences
+    // 2 mbarriers and the unit information (kPipeInfoBytes), then (when compacting) the sort or warp
+    // counts (AUX ints) and the list of active sequences
     const long long xb = pipe_part((long long)TS * BC * ES);
     const long long stage_bytes = xb + pipe_part((long long)SC * BC * ESS);
     const long long rb = dense ? 0 : pipe_part((long long)Q * BC * ESS);
     const long long img_bytes = recomp ? 0 : rb + ((hist || wide) ? 0 : pipe_part((long long)R * BC * ESS));
     unsigned char *const img0 = smem + 2 * stage_bytes;
     uint64_t *const bar = reinterpret_cast<uint64_t *>(img0 + 2 * img_bytes);
-    volatile int *const info = reinterpret_cast<volatile int *>(bar + 2);  // [0, 2): slots, [2, 4): offsets
-    int *const wcount = reinterpret_cast<int *>(bar + 4);
-    int *const act = wcount + 4;
+    // [0, 2): slots, [2, 4): state offsets, [4, 6): draft counts, [6, 8): first rows (packed drafts)
+    volatile int *const info = reinterpret_cast<volatile int *>(bar + 2);
+    constexpr int AUX = pipe_aux_ints(VL, TS);
+    int *const wcount = reinterpret_cast<int *>(smem + 2 * stage_bytes + 2 * img_bytes + kPipeInfoBytes);
+    int *const act = wcount + AUX;
     const bool compact = p.compact != 0;
-    if (2 * stage_bytes + 2 * img_bytes + 32 + (compact ? 16 + 4LL * p.n_seq : 0) > (long long)dynamic_smem_bytes())
+    if (2 * stage_bytes + 2 * img_bytes + kPipeInfoBytes + (compact ? 4LL * AUX + 4LL * p.n_seq : 0) >
+        (long long)dynamic_smem_bytes())
         return;  // launch mismatch
 
     if (tid == 0) {
@@ -111,10 +124,65 @@ __global__ void __launch_bounds__(128, (CPT == 4 && TS <= 8) ? 4 : 2) verify_pip
     __syncthreads();
 
     // Units walk the active sequences only: the block lists the sequences whose cache slot is not
-    // negative (ascending), so padded sequences cost no unit and every block gets its fair share of
-    // real work.  Padded sequences' err entries are written here (0) by block 0.
+    // negative (ascending; packed drafts: by draft count), so padded sequences cost no unit and every
+    // block gets its fair share of real work.  (Padded sequences' err entries stay 0: the library
+    // clears err before the launch.)
     int n_act = p.n_seq;
-    if (compact) {
+    if (VL && compact) {
+        // the listed sequences (cache slot >= 0) ordered by key = TS - T_s (longest drafts first; a
+        // bad span counts as empty), ties in ascending sequence order: a stable counting sort whose
+        // counts come from warp ballots, so every block builds the same list
+        constexpr int NB = TS + 1;  // keys 0 .. TS
+        const int lane = tid & 31, warp = tid >> 5, nwarps = ((int)blockDim.x + 31) >> 5;
+        int *const bstart = wcount;       // [NB]: bucket sizes, then the next free position of each
+        int *const wc = wcount + NB + 1;  // [NB][4]: per-warp counts of the current chunk
+        auto key_of = [&](int i) -> int {
+            if (i >= p.n_seq || (p.cache_idx && __ldg(p.cache_idx + i) < 0)) return -1;
+            int ts, r0;
+            return draft_span(p.cu_draft, i, TS, p.total_tokens, ts, r0) ? TS : TS - ts;
+        };
+        for (int v = tid; v < NB; v += (int)blockDim.x) bstart[v] = 0;
+        __syncthreads();
+        for (int i0 = 0; i0 < p.n_seq; i0 += (int)blockDim.x) {
+            const int key = key_of(i0 + tid);
+            for (int v = 0; v < NB; ++v) {
+                const unsigned m = __ballot_sync(0xffffffffu, key == v);
+                if (lane == 0 && m) atomicAdd(bstart + v, __popc(m));
+            }
+        }
+        __syncthreads();
+        if (tid == 0) {
+            int run = 0;
+            for (int v = 0; v < NB; ++v) {
+                const int n = bstart[v];
+                bstart[v] = run;
+                run += n;
+            }
+            bstart[NB] = run;
+        }
+        __syncthreads();
+        n_act = bstart[NB];
+        for (int i0 = 0; i0 < p.n_seq; i0 += (int)blockDim.x) {
+            const int i = i0 + tid;
+            const int key = key_of(i);
+            unsigned mine = 0u;
+            for (int v = 0; v < NB; ++v) {
+                const unsigned m = __ballot_sync(0xffffffffu, key == v);
+                if (key == v) mine = m;
+                if (lane == 0) wc[v * 4 + warp] = __popc(m);
+            }
+            __syncthreads();
+            if (key >= 0) {
+                int before = 0;
+                for (int w = 0; w < warp; ++w) before += wc[key * 4 + w];
+                act[bstart[key] + before + __popc(mine & ((1u << lane) - 1u))] = i;
+            }
+            __syncthreads();
+            for (int v = tid; v < NB; v += (int)blockDim.x)
+                for (int w = 0; w < nwarps; ++w) bstart[v] += wc[v * 4 + w];
+            __syncthreads();
+        }
+    } else if (compact) {
         const int lane = tid & 31, warp = tid >> 5, nwarps = ((int)blockDim.x + 31) >> 5;
         n_act = 0;
         for (int i0 = 0; i0 < p.n_seq; i0 += (int)blockDim.x) {
@@ -139,9 +207,10 @@ __global__ void __launch_bounds__(128, (CPT == 4 && TS <= 8) ? 4 : 2) verify_pip
     const int iters = (int)blockIdx.x < n_units ? (n_units - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
 
     // thread 0: start the copies of iteration k into stage k & 1 (or only arrive, for padding).  The
-    // index data of the next unit (cache slot, state offset) is loaded one issue ahead, so no issue
-    // waits for a global-memory round trip; the first two units load theirs together at the start
-    // and send their x copies out before the indices arrive (the x rows do not depend on the slot).
+    // index data of the next unit (cache slot, state offset, packed row span) is loaded one issue
+    // ahead, so no issue waits for a global-memory round trip; the first two units load theirs
+    // together at the start and (whole-T batches) send their x copies out before the indices arrive
+    // (those x rows do not depend on the slot).
     auto unit_of = [&](int k, int &s, int &c0, int &nch) {
         const int u = (int)blockIdx.x + k * (int)gridDim.x;
         const int q = u / nblk;
@@ -149,34 +218,54 @@ __global__ void __launch_bounds__(128, (CPT == 4 && TS <= 8) ? 4 : 2) verify_pip
         c0 = (u - q * nblk) * BC;
         nch = min(BC, p.dim - c0);
     };
-    auto load_index = [&](int k, int &slot, int &off) {
+    // a unit's index data: cache slot, state offset and (packed drafts) its row span [b, e)
+    struct UnitIdx {
+        int slot, off, b, e;
+    };
+    auto load_index = [&](int k, UnitIdx &ix) {
         if (k >= iters) return;
         const int s = seq_at(((int)blockIdx.x + k * (int)gridDim.x) / nblk);
-        slot = p.cache_idx ? __ldg(p.cache_idx + s) : s;
-        off = p.state_off ? __ldg(p.state_off + s) : 0;
+        ix.slot = p.cache_idx ? __ldg(p.cache_idx + s) : s;
+        ix.off = p.state_off ? __ldg(p.state_off + s) : 0;
+        if constexpr (VL) {
+            ix.b = __ldg(p.cu_draft + s);
+            ix.e = __ldg(p.cu_draft + s + 1);
+        } else {
+            ix.b = s;  // (the rows of sequence s start at s * x_seq)
+            ix.e = s + TS;
+        }
     };
-    auto issue_x = [&](int k) {
+    // the unit's x rows: T_s rows from row b (packed drafts), or the TS rows of sequence s
+    auto issue_x = [&](int k, int b, int ts) {
         const int st = k & 1;
         int s, c0, nch;
         unit_of(k, s, c0, nch);
-        mbar_expect_tx(&bar[st], (unsigned)(TS * nch * ES));
-        const B *xs = reinterpret_cast<const B *>(p.x) + (long long)s * p.x_seq + c0;
-        for (int t = 0; t < TS; ++t)
+        mbar_expect_tx(&bar[st], (unsigned)(ts * nch * ES));
+        const B *xs = reinterpret_cast<const B *>(p.x) + (VL ? (long long)b * p.x_tok : (long long)s * p.x_seq) + c0;
+        for (int t = 0; t < ts; ++t)
             bulk_load(smem + st * stage_bytes + (long long)t * BC * ES, xs + (long long)t * p.x_tok,
                       (unsigned)(nch * ES), &bar[st]);
     };
     // the phase cannot complete before the single arrival at its end, so a late expect_tx is safe
-    auto issue = [&](int k, int slot, int off, bool x_sent) {
+    auto issue = [&](int k, const UnitIdx &ix, bool x_sent) {
         const int st = k & 1;
         int s, c0, nch;
         unit_of(k, s, c0, nch);
-        const int status = seq_status(slot, off, p.n_slots, p.state_cols, R);
+        const int slot = ix.slot, off = ix.off;
+        int status = seq_status(slot, off, p.n_slots, p.state_cols, R);
+        int ts = TS;
+        if constexpr (VL) {  // (the span was loaded with the indices, one issue ahead)
+            ts = ix.e - ix.b;
+            if (slot >= 0) status |= span_status(ix.b, ix.e, TS, p.total_tokens);
+        }
         if (p.err && c0 == 0 && status) atomicOr(p.err + s, status);
         const bool go = slot >= 0 && status == 0;
         info[st] = go ? slot : -1;
         info[2 + st] = off;
+        info[4 + st] = ts;
+        info[6 + st] = ix.b;
         if (go) {
-            if (!x_sent) issue_x(k);
+            if (!x_sent) issue_x(k, ix.b, ts);
             // packed state rows of SC columns: the committed windows, or whole rows
             mbar_expect_tx(&bar[st], (unsigned)(SC * nch * ESS));
             bulk_load(smem + st * stage_bytes + xb,
@@ -187,16 +276,18 @@ __global__ void __launch_bounds__(128, (CPT == 4 && TS <= 8) ? 4 : 2) verify_pip
     };
     // polls of each unit's first wait for its copies (the drain after a timeout uses kWaitPolls)
     const unsigned first_polls = p.wait_polls == 0 ? kWaitPolls : p.wait_polls < 0 ? 0u : (unsigned)p.wait_polls;
-    int pf_slot = 0, pf_off = 0;
+    UnitIdx pf{0, 0, 0, 0};
     if (tid == 0) {
-        int slot0 = 0, off0 = 0, slot1 = 0, off1 = 0;
-        load_index(0, slot0, off0);
-        load_index(1, slot1, off1);
-        if (iters > 0) issue_x(0);
-        if (iters > 1) issue_x(1);
-        if (iters > 0) issue(0, slot0, off0, true);
-        if (iters > 1) issue(1, slot1, off1, true);
-        load_index(2, pf_slot, pf_off);
+        UnitIdx i0{0, 0, 0, 0}, i1{0, 0, 0, 0};
+        load_index(0, i0);
+        load_index(1, i1);
+        if (!VL) {  // (x rows of a whole-T batch do not depend on the indices: send them first)
+            if (iters > 0) issue_x(0, 0, TS);
+            if (iters > 1) issue_x(1, 0, TS);
+        }
+        if (iters > 0) issue(0, i0, !VL);
+        if (iters > 1) issue(1, i1, !VL);
+        load_index(2, pf);
     }
 
     const int cl = tid * CPT;
@@ -248,13 +339,22 @@ __global__ void __launch_bounds__(128, (CPT == 4 && TS <= 8) ? 4 : 2) verify_pip
         const int slot = ok ? info[st] : -1;
         const int off = info[2 + st];
         const bool go = slot >= 0;
+        const int Ts = VL ? info[4 + st] : TS;           // draft tokens of this unit's sequence
+        const long long row0 = VL ? info[6 + st] : 0;    // its first packed row
 
         float fw[CPT][R + TS];  // inputs widened to fp32: [0, R) committed window, then x
         uint32_t xr[TS][NW];    // raw x rows
         uint32_t sw[R * NWS];   // raw committed window, channel-major [CPT][R]
         if (go && act) {
 #pragma unroll
-            for (int t = 0; t < TS; ++t) ldv<VX, NW>(xr[t], stg + ((long long)t * BC + cl) * ES);
+            for (int t = 0; t < TS; ++t) {
+                if (!VL || t < Ts) {
+                    ldv<VX, NW>(xr[t], stg + ((long long)t * BC + cl) * ES);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < NW; ++i) xr[t][i] = 0u;  // (no row: keep stale bits out)
+                }
+            }
             if (whole_rows) {
                 // the committed window sits at columns [off, off+W-1) of each staged row
                 using U = std::conditional_t<ESS == 2, unsigned short, unsigned>;
@@ -312,11 +412,50 @@ __global__ void __launch_bounds__(128, (CPT == 4 && TS <= 8) ? 4 : 2) verify_pip
                 S *wsq = reinterpret_cast<S *>(p.win) + (long long)s * p.w_seq + (long long)c * R;
 #pragma unroll
                 for (int t = 0; t < TS; ++t) {
+                    if (VL && t >= Ts) break;
                     uint32_t w[R * NWS];
 #pragma unroll
                     for (int i = 0; i < R * NWS; ++i) w[i] = run_word(i, R, t + 1);
                     stv<VS, R * NWS>(wsq + (long long)t * p.w_step, w);
                 }
+            }
+            // committed window = full[T_s .. T_s+W-2], channel-major [CPT][R] words
+            uint32_t fin[R * NWS];
+            if constexpr (VL) {
+                // column kk is x row T_s+kk-R when that is >= 0 (read back from the stage), else
+                // committed-window column T_s+kk (T_s < W-1)
+                uint32_t col[R][NW];
+#pragma unroll
+                for (int kk = 0; kk < R; ++kk) {
+                    const int j = Ts + kk;
+                    if (j >= R) {
+                        ldv<VX, NW>(col[kk], stg + ((long long)(j - R) * BC + cl) * ES);
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < NW; ++i) {
+                            uint32_t lo = 0u, hi = 0u;
+#pragma unroll
+                            for (int jj = 0; jj < R; ++jj) {
+                                if (jj != j) continue;
+                                lo = elem_raw<S>(sw, (EW * i) * R + jj);
+                                if (EW == 2) hi = elem_raw<S>(sw, (EW * i + 1) * R + jj);
+                            }
+                            col[kk][i] = EW == 2 ? pack_halves(lo, hi) : lo;
+                        }
+                    }
+                }
+#pragma unroll
+                for (int i = 0; i < R * NWS; ++i) {
+                    if (ES == 2) {
+                        const int a = 2 * i, b2 = 2 * i + 1;
+                        fin[i] = pack_halves(elem_raw<S>(col[a % R], a / R), elem_raw<S>(col[b2 % R], b2 / R));
+                    } else {
+                        fin[i] = col[i % R][i / R];
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int i = 0; i < R * NWS; ++i) fin[i] = run_word(i, R, TS);
             }
             if (wide && !recomp) {
                 // committed window -> columns [0, W-1) of the wide rows, stored directly (the rows'
@@ -325,11 +464,8 @@ __global__ void __launch_bounds__(128, (CPT == 4 && TS <= 8) ? 4 : 2) verify_pip
 #pragma unroll
                 for (int e = 0; e < CPT; ++e)
 #pragma unroll
-                    for (int kk = 0; kk < R; ++kk) srow[(long long)e * SC + kk] = (S)elem_bits(e, TS + kk);
+                    for (int kk = 0; kk < R; ++kk) srow[(long long)e * SC + kk] = (S)elem_raw<S>(fin, e * R + kk);
             } else if (!hist && !recomp) {
-                uint32_t fin[R * NWS];
-#pragma unroll
-                for (int i = 0; i < R * NWS; ++i) fin[i] = run_word(i, R, TS);
                 stv<VS, R * NWS>(stimg + (long long)tid * CPT * R * ESS, fin);
             }
         }
@@ -355,25 +491,45 @@ __global__ void __launch_bounds__(128, (CPT == 4 && TS <= 8) ? 4 : 2) verify_pip
             }
             return;
         }
+        // the row image (dedup row, or history row): whole rows leave as one bulk copy; a packed
+        // sequence with fewer than TS drafts writes only columns [0, T_s+W-2) of each channel's row
+        const bool full_row = !VL || Ts == TS;
+        S *const row_dst = hist ? reinterpret_cast<S *>(p.state) + (long long)slot * p.st_slot + (long long)c0 * Q
+                                : reinterpret_cast<S *>(p.win) + (long long)s * p.w_seq + (long long)c0 * Q;
         if (tid == 0) {
             if (go && !recomp) {
-                if (hist) {
-                    // the row image replaces columns [0, T+W-2) of the (packed) history rows
-                    bulk_store(reinterpret_cast<S *>(p.state) + (long long)slot * p.st_slot + (long long)c0 * Q, img,
-                               (unsigned)(nch * Q * ESS));
-                } else {
-                    if (!dense)
-                        bulk_store(reinterpret_cast<S *>(p.win) + (long long)s * p.w_seq + (long long)c0 * Q, img,
-                                   (unsigned)(nch * Q * ESS));
-                    if (!wide)
-                        bulk_store(reinterpret_cast<S *>(p.state) + (long long)slot * p.st_slot + (long long)c0 * R,
-                                   stimg, (unsigned)(nch * R * ESS));
-                }
+                if (!dense && full_row) bulk_store(row_dst, img, (unsigned)(nch * Q * ESS));
+                if (!hist && !wide)
+                    bulk_store(reinterpret_cast<S *>(p.state) + (long long)slot * p.st_slot + (long long)c0 * R, stimg,
+                               (unsigned)(nch * R * ESS));
                 asm volatile("cp.async.bulk.commit_group;\n" ::: "memory");
             }
             if (k + 2 < iters) {
-                issue(k + 2, pf_slot, pf_off, false);
-                load_index(k + 3, pf_slot, pf_off);
+                issue(k + 2, pf, false);
+                load_index(k + 3, pf);
+            }
+        }
+        if (VL && go && !recomp && !dense && !full_row && Ts > 0) {
+            // word w of the staged image holds elements 2w, 2w+1 (bf16) or w (fp32) of the block's
+            // [nch][Q] run; an element in column q >= T_s+W-2 is skipped
+            const int ncols = Ts + R - 1;
+            const unsigned *iw = reinterpret_cast<const unsigned *>(img);
+            unsigned *dw = reinterpret_cast<unsigned *>(row_dst);
+            const int nwords = nch * Q * ESS / 4;
+            for (int w = tid; w < nwords; w += (int)blockDim.x) {
+                const unsigned v = iw[w];
+                if (ESS == 4) {
+                    if (w % Q < ncols) dw[w] = v;
+                } else {
+                    const bool lo = (2 * w) % Q < ncols, hi = (2 * w + 1) % Q < ncols;
+                    if (lo && hi) {
+                        dw[w] = v;
+                    } else if (lo) {
+                        reinterpret_cast<unsigned short *>(dw)[2 * w] = (unsigned short)(v & 0xffffu);
+                    } else if (hi) {
+                        reinterpret_cast<unsigned short *>(dw)[2 * w + 1] = (unsigned short)(v >> 16);
+                    }
+                }
             }
         }
         if (go) {
@@ -432,9 +588,10 @@ __global__ void __launch_bounds__(128, (CPT == 4 && TS <= 8) ? 4 : 2) verify_pip
                 }
             }
             if (act) {
-                B *os = reinterpret_cast<B *>(p.out) + (long long)s * p.out_seq + c;
+                B *os = reinterpret_cast<B *>(p.out) + (VL ? row0 * p.out_tok : (long long)s * p.out_seq) + c;
 #pragma unroll
                 for (int t = 0; t < TS; ++t) {
+                    if (VL && t >= Ts) break;
                     uint32_t ow[NW];
                     if (ES == 2) {
 #pragma unroll

@@ -67,10 +67,12 @@ def _plan(lib, a):
 W3 = wl.WORKLOADS["n128_t8_dim10240_w4_bf16_dedup_pad13"]
 
 
-def _pipe_smem(stage, image, n_seq):
-    """The pipelined kernel's shared memory: two stages, two image buffers, 32 bytes of barriers,
-    slots and offsets, and 16 + 4 * n_seq bytes for the list of active sequences."""
-    return 2 * stage + 2 * image + 32 + 16 + 4 * n_seq
+def _pipe_smem(stage, image, n_seq, varlen_T=None):
+    """The pipelined kernel's shared memory: two stages, two image buffers, 48 bytes of barriers and
+    unit information (slots, offsets, draft counts, first rows), then the compaction scratch (4
+    ints; 5 * (T + 2) for packed drafts) and 4 * n_seq bytes for the list of active sequences."""
+    aux = 4 if varlen_T is None else 5 * (varlen_T + 2)
+    return 2 * stage + 2 * image + 48 + 4 * aux + 4 * n_seq
 
 
 def test_plan_for_benchmark_workload(lib):
@@ -486,3 +488,60 @@ def test_struct_layouts_match_header(tmp_path):
         assert c_side[(cname, "size")] == ctypes.sizeof(py), f"{cname}: sizeof differs"
         for fname, _ in py._fields_:
             assert c_side[(cname, fname)] == getattr(py, fname).offset, f"{cname}.{fname}: offset differs"
+
+
+RAG = wl.RAGGED_WORKLOADS["ragged_n128_t1to16_dim10240_w4_bf16_dedup_pad13"]
+
+
+def _ragged_args(w, **over):
+    inp = wl.make_ragged_inputs(w)
+    a = cv.make_verify_args(inp["x"], inp["conv_state"], inp["weight"], inp["bias"], inp["out"], inp["window"],
+                            layout=w.layout, qk_channels=w.qk_channels, head_dim=w.head_dim,
+                            cache_idx=inp["cache_idx"], state_off=inp["state_off"], cu_draft=inp["cu_draft"], T=w.T,
+                            check_device=False)
+    _ragged_args.keep = inp
+    for k, v in over.items():
+        setattr(a, k, v)
+    return a
+
+
+def test_plan_packed_drafts_pipelined(lib):
+    """Packed ragged drafts at the benchmark shape take the pipelined kernel, whose shared memory
+    holds the sort scratch of 5 * (T + 2) ints and the list of sequences."""
+    a = _ragged_args(RAG)
+    rc, pl = _plan(lib, a)
+    assert rc == 0 and pl.path == 3
+    R, Q, bc = RAG.width - 1, RAG.T + RAG.width - 2, 512
+
+    def part(b):
+        return (b + 127) // 128 * 128
+    stage = part(RAG.T * bc * 2) + part(R * bc * 2)
+    image = part(Q * bc * 2) + part(R * bc * 2)
+    assert pl.smem_bytes == _pipe_smem(stage, image, RAG.n_seq, varlen_T=RAG.T)
+
+
+def test_packed_drafts_argument_checks(lib):
+    """cu_draft with a tree is a layout error, a negative total_tokens a shape error; with no rows
+    at all x and out may be NULL; unaligned x falls back to the general kernel."""
+    rc, _ = _plan(lib, _ragged_args(RAG, parent=_ragged_args.keep["cache_idx"].data_ptr()))
+    assert rc == -8
+    rc, _ = _plan(lib, _ragged_args(RAG, total_tokens=-1))
+    assert rc == -3
+    w0 = RAG.replace(lengths=(0,) * 4, pad=(), extra_rows=0)
+    a = _ragged_args(w0, x=None, out=None)
+    rc, pl = _plan(lib, a)
+    assert rc == 0
+    a = _ragged_args(RAG)
+    a.x = a.x + 2  # one bf16 element off 16-byte alignment
+    rc, pl = _plan(lib, a)
+    assert rc == 0 and pl.path == 0
+
+
+def test_packed_commit_argument_checks(lib):
+    inp = wl.make_ragged_inputs(RAG)
+    ca = cv.make_commit_args(inp["conv_state"], inp["window"], inp["accept_len"], layout=RAG.layout, T=RAG.T,
+                             width=RAG.width, cache_idx=inp["cache_idx"], cu_draft=inp["cu_draft"],
+                             total_tokens=RAG.total_tokens, check_device=False)
+    assert ca.total_tokens == RAG.total_tokens and ca.cu_draft == inp["cu_draft"].data_ptr()
+    ca.total_tokens = -1
+    assert lib.cv_conv_commit(ctypes.byref(ca), None) == -3
