@@ -346,8 +346,11 @@ def run_ours(args, w, world, rank, local, dist):
     for i in range(n_sets):
         xb = inp["x_base"].to(dev)
         x = xb.as_strided(inp["x"].shape, inp["x"].stride(), inp["x"].storage_offset())
-        s = dict(x_base=xb, x=x, conv_state=inp["conv_state"].to(dev), out=inp["out"].to(dev),
-                 window=inp["window"].to(dev) if inp["window"] is not None else None,
+        win = None
+        if inp["window"] is not None:  # (keeping its strides: a transposed row stays transposed)
+            win = torch.empty_strided(inp["window"].shape, inp["window"].stride(), dtype=inp["window"].dtype, device=dev)
+            win.copy_(inp["window"])
+        s = dict(x_base=xb, x=x, conv_state=inp["conv_state"].to(dev), out=inp["out"].to(dev), window=win,
                  accept=inp["accept_len"].to(dev))
         s["va"] = cv.make_verify_args(x, s["conv_state"], weight, bias, s["out"], s["window"], layout=w.layout,
                                       qk_channels=w.qk_channels, head_dim=w.head_dim, l2_eps=w.l2_eps,

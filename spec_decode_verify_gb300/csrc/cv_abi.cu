@@ -37,9 +37,12 @@ constexpr int kTreeBlocksPerSM = 10;  // tree verify: resident blocks per SM at 
 constexpr int kCommitDenseThreads = 64;      // packed dense snapshot -> packed state (16-byte copies)
 constexpr int kCommitElementThreads = 32;    // element by element
 constexpr int kCommitRecomputeThreads = 64;  // recompute rollback
-// dedup commit: 256 channels per block (small blocks fit beside the verify's resident blocks, so
-// more of them start, under programmatic dependent launch, while the verify drains)
-constexpr int kCommitRowThreads = 32;
+// dedup commit: one thread per 8 channels; 1024 channels per block keep the batch in one wave, and
+// the per-thread row slices stay within the default 48 KB of dynamic shared memory (longer rows
+// take the element kernel)
+constexpr int kCommitRowThreads = 128;
+constexpr long long kCommitRowSmem = 48 * 1024;
+constexpr int kCommitColThreads = 128;  // transposed dedup rows: 1024 channels per block
 // the pipelined kernel lists the active sequences in shared memory up to this batch size
 constexpr int kCompactMaxSeq = 1024;
 constexpr int kPrefillMaxChunk = 256;  // tokens per prefill block, at most / at least (multiples of
@@ -178,6 +181,14 @@ bool fast_eligible(const cv_verify_args *a, int esize, int ssize, int max_static
     return a->win_ch_stride == R && stride16(a->win_step_stride, ssize);
 }
 
+// Deduplicated rows laid out transposed (channel stride 1, every column a 16-byte-aligned run of
+// channels), which only the pipelined kernel stores by bulk copies (one per column).
+bool dedup_transposed_ok(const cv_verify_args *a, int ssize, int max_static_t) {
+    return a->window_layout == CV_WINDOW_DEDUP && a->dim % 8 == 0 && a->win_ch_stride == 1 &&
+           a->win_col_stride >= a->dim && aligned16(a->window) && stride16(a->win_seq_stride, ssize) &&
+           stride16(a->win_col_stride, ssize) && a->T <= max_static_t;
+}
+
 // Halve a block (down to 32 threads) while the launch would have fewer than two blocks per SM and
 // the smaller block still holds whole L2 groups: small batches then still fill the GPU.
 int shrink_for_parallelism(int threads, int cpt, const cv_verify_args *a, int sms) {
@@ -262,8 +273,10 @@ int plan_verify(const cv_verify_args *a, cv_launch_plan *pl) {
                              a->state_ch_stride == a->state_cols;
     const bool varlen = a->cu_draft != nullptr;
     // (mixed dtypes: compiled for T <= kMaxMixedT; packed drafts: one dtype)
+    const bool dedup_t = dedup_transposed_ok(a, ssize, ks.max_static_t);
     bool pipe_ok = (!mixed || a->T <= cvk::kMaxMixedT) && !(mixed && varlen) && io_packed(a, esize) &&
-                   a->T <= ks.max_static_t && rows_packed && (hist ? a->state_cols == a->T + R - 1 : (recomp || fast));
+                   a->T <= ks.max_static_t && rows_packed &&
+                   (hist ? a->state_cols == a->T + R - 1 : (recomp || fast || dedup_t));
     const bool wide = !hist && a->state_cols != R;
     // (wide rows cost whole-row reads and element stores of the window; the pipeline pays that
     // back only when every block walks at least two units, otherwise the one-pass kernel wins)
@@ -400,6 +413,8 @@ int launch_verify(const cv_verify_args *a, const cv_launch_plan &pl, cudaStream_
     p.bias = a->bias;
     p.win = a->window;
     p.dedup = a->window_layout == CV_WINDOW_DEDUP;
+    p.dedup_t = pl.path == 3 && dedup_transposed_ok(a, state_dtype_of(a) == CV_BF16 ? 2 : 4,
+                                                    kernel_set(a->dtype, a->width).max_static_t);
     p.hist = a->window_layout == CV_WINDOW_HISTORY;
     p.recomp = a->window_layout == CV_WINDOW_RECOMPUTE;
     p.parent = a->parent;
@@ -499,9 +514,6 @@ int launch_commit(const cv_commit_args *a, cudaStream_t stream) {
     p.w_col = a->win_col_stride;
     p.accept_len = a->accept_len;
     p.err = a->err;
-    p.wait_polls = a->wait_polls;
-    p.cu_draft = a->cu_draft;
-    p.total_tokens = a->total_tokens;
     p.cu_draft = a->cu_draft;
     p.total_tokens = a->total_tokens;
     p.n_seq = a->n_seq;
@@ -518,7 +530,8 @@ int launch_commit(const cv_commit_args *a, cudaStream_t stream) {
         // 8 channels per thread with 16-byte vectors when the rows and x allow it
         const bool vec = a->dim % 8 == 0 &&
                          state_packed(a->conv_state, a->state_slot_stride, a->state_ch_stride, a->width, esize) &&
-                         aligned16(a->x) && stride16(a->x_seq_stride, esize) && stride16(a->x_tok_stride, esize);
+                         aligned16(a->x) && (a->cu_draft || stride16(a->x_seq_stride, esize)) &&
+                         stride16(a->x_tok_stride, esize);
         const int threads = kCommitRecomputeThreads;
         const int per_block = vec ? 8 * threads : threads;
         auto kr = vec ? kernel_set(a->dtype, a->width).commit_recompute_vec : kernel_set(a->dtype, a->width).commit_recompute;
@@ -528,25 +541,31 @@ int launch_commit(const cv_commit_args *a, cudaStream_t stream) {
     }
 
     const bool packed_state = state_packed(a->conv_state, a->state_slot_stride, a->state_ch_stride, a->width, esize);
-    const bool win_ok = a->dim % 8 == 0 && aligned16(a->window) && stride16(a->win_seq_stride, esize) &&
-                        a->win_col_stride == 1;
+    const bool win_base = a->dim % 8 == 0 && aligned16(a->window) && stride16(a->win_seq_stride, esize);
+    const bool win_ok = win_base && a->win_col_stride == 1;
+    const bool dedup = a->window_layout == CV_WINDOW_DEDUP;
     int smem = 0;
     if (packed_state && win_ok && a->window_layout == CV_WINDOW_DENSE && a->win_ch_stride == R &&
         stride16(a->win_step_stride, esize)) {
         p.mode = 1;
-    } else if (packed_state && win_ok && a->window_layout == CV_WINDOW_DEDUP && a->win_ch_stride == Q) {
-        // one block of 8*kCommitRowThreads channels per sequence, its rows staged by one bulk copy
+    } else if (packed_state && win_base && dedup && a->win_ch_stride == 1 && stride16(a->win_col_stride, esize)) {
+        // transposed rows: each thread reads its W-1 accepted column pieces
+        p.mode = 4;
+        const int threads = kCommitColThreads;
+        auto kr = kernel_set(a->dtype, a->width).commit_cols;
+        if (launch_pdl(kr, dim3((a->dim + 8 * threads - 1) / (8 * threads), a->n_seq), threads, 0, stream, p) !=
+            cudaSuccess)
+            return CV_ERR_LAUNCH;
+        return cudaGetLastError() == cudaSuccess ? CV_OK : CV_ERR_LAUNCH;
+    } else if (packed_state && win_ok && dedup && a->win_ch_stride == Q) {
+        // one thread per 8 channels, each with its own shared-memory slice of 8 rows
         int rt = kCommitRowThreads;
         while (rt > kMinThreads && 8 * (rt / 2) >= a->dim) rt /= 2;
-        const long long sm = (8LL * rt * Q * esize + 127) / 128 * 128 + 8;
-        if (sm <= device_limits().smem_per_block) {
+        const long long sm = (long long)rt * Q * 8 * esize;
+        if (sm <= kCommitRowSmem) {
             p.mode = 2;
             const int bc = 8 * rt;
             auto kr = kernel_set(a->dtype, a->width).commit_rows;
-            if (ensure_smem(reinterpret_cast<const void *>(kr), (int)sm) != cudaSuccess) return CV_ERR_LAUNCH;
-            // commit_rows ORs its bits into err
-            if (a->err && cudaMemsetAsync(a->err, 0, sizeof(int32_t) * (size_t)a->n_seq, stream) != cudaSuccess)
-                return CV_ERR_LAUNCH;
             if (launch_pdl(kr, dim3((a->dim + bc - 1) / bc, a->n_seq), rt, (int)sm, stream, p) != cudaSuccess)
                 return CV_ERR_LAUNCH;
             return cudaGetLastError() == cudaSuccess ? CV_OK : CV_ERR_LAUNCH;

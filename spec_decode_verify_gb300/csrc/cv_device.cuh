@@ -27,6 +27,7 @@ struct VerifyParams {
     int qk_channels, head_dim, pitch;      // pitch: elements per shared-memory row (generic kernel)
     float eps;
     int dedup;
+    int dedup_t;  // dedup rows laid out transposed: channel stride 1, one contiguous run per column
     int hist;     // history-row state: the snapshot row goes into the state row (no window buffer)
     int compact;  // pipelined kernel: walk only the sequences with a cache slot >= 0 (list in shared memory)
     int recomp;   // recompute rollback: outputs only (no snapshots, state not written)
@@ -56,10 +57,11 @@ struct CommitParams {
     const int *accept_len;
     int *err;
     int n_seq, T, dim, n_slots;
-    int mode;  // 0: element by element, 1: packed dense snapshot -> packed state, 2: packed dedup row -> packed state, 3: recompute from x
+    // 0: element by element, 1: packed dense snapshot -> packed state, 2: packed dedup row -> packed
+    // state, 3: recompute from x, 4: packed transposed dedup row (channel stride 1) -> packed state
+    int mode;
     const void *x;  // mode 3: the verify's input
     long long x_seq, x_tok;
-    int wait_polls;  // polls of the bounded wait for the staged rows: 0 = the default, < 0 = none
     const int *cu_draft;  // packed ragged drafts of the matching verify, or null (T tokens each)
     int total_tokens;
 };

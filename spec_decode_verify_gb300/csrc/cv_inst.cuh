@@ -62,6 +62,7 @@ KernelSet make_set(std::integer_sequence<int, Ts...>) {
     k.generic_mixed = verify_generic<B, W, OtherT<B>>;
     k.commit = commit_kernel<B, W>;
     k.commit_rows = commit_rows<B, W>;
+    k.commit_cols = commit_cols<B, W>;
     k.commit_recompute = commit_recompute<B, W>;
     k.commit_recompute_vec = commit_recompute_vec<B, W>;
     k.prefill[0] = prefill_conv<B, W, 4>;

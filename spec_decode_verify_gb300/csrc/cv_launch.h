@@ -31,6 +31,7 @@ struct KernelSet {
     VerifyKernel generic_mixed;  // state and snapshots in the other dtype (bf16 <-> fp32)
     CommitKernel commit;
     CommitKernel commit_rows;
+    CommitKernel commit_cols;
     CommitKernel commit_recompute;
     CommitKernel commit_recompute_vec;
     // prefill[c]: c = 0 for 4 channels per thread, 1 for 8

@@ -23,6 +23,10 @@
 // limit, so nothing lands in shared memory after the block has left) and returns.  The limit of
 // that first wait per unit is p.wait_polls (0: the default; negative: no poll at all, a wait
 // that gives up at once).  Every err bit is ORed in; the library zeroes err before the launch.
+// Deduplicated rows laid out transposed ([n_seq][T+W-2][dim] seen as [n_seq][dim][T+W-2], channel
+// stride 1: sglang PR #46184, "Modifications", test coverage: MambaPool's axis-0 window layout seen
+// transposed): the image is staged column by column, [T+W-2][channels], and leaves as one bulk copy
+// per column, each a contiguous run of the block's channels.
 // History-row state (no window buffer): the stage holds each channel's whole [T+W-2] state row,
 // the committed window is taken from columns [off, off+W-1) of it, and the row image is stored
 // back over the state row instead of into a window buffer; there is no separate committed-window
@@ -89,6 +93,7 @@ __global__ void __launch_bounds__(128, (CPT == 4 && TS <= 8) ? 4 : 2) verify_pip
     const bool hist = p.hist != 0;        // history-row state: no window buffer
     const bool recomp = p.recomp != 0;    // recompute rollback: outputs only
     const bool dense = !p.dedup && !hist;  // dense window (or none): no row image
+    const bool dedup_t = p.dedup_t != 0;     // dedup rows stored column by column
     const bool has_bias = p.bias != nullptr;
     // state columns staged per channel: the committed windows of packed [dim][W-1] rows, or whole
     // rows when they are wider (history rows, or rows read at a state offset)
@@ -403,6 +408,22 @@ __global__ void __launch_bounds__(128, (CPT == 4 && TS <= 8) ? 4 : 2) verify_pip
             };
             if (recomp) {
                 // outputs only: no snapshots, and the state keeps the pre-verify window
+            } else if (dedup_t) {
+                // column q (input q+1) of the thread's CPT channels, in the state's type, at image
+                // position [q][cl]
+#pragma unroll
+                for (int q = 0; q < Q; ++q) {
+                    const int j = q + 1;
+                    uint32_t w[NWS];
+#pragma unroll
+                    for (int i = 0; i < NWS; ++i) {
+                        if (ESS == 2)
+                            w[i] = pack_halves(elem_bits(2 * i, j), elem_bits(2 * i + 1, j));
+                        else
+                            w[i] = elem_bits(i, j);
+                    }
+                    stv<pipe_align(CPT * ESS), NWS>(img + ((long long)q * BC + cl) * ESS, w);
+                }
             } else if (!dense) {
                 uint32_t im[Q * NWS];  // CPT channels x Q columns; column q holds input q+1
 #pragma unroll
@@ -498,7 +519,15 @@ __global__ void __launch_bounds__(128, (CPT == 4 && TS <= 8) ? 4 : 2) verify_pip
                                 : reinterpret_cast<S *>(p.win) + (long long)s * p.w_seq + (long long)c0 * Q;
         if (tid == 0) {
             if (go && !recomp) {
-                if (!dense && full_row) bulk_store(row_dst, img, (unsigned)(nch * Q * ESS));
+                if (dedup_t) {
+                    // one bulk copy per column (columns past T_s+W-2 of a packed draft are skipped)
+                    const int ncols = full_row ? Q : (Ts > 0 ? Ts + R - 1 : 0);
+                    S *const colb = reinterpret_cast<S *>(p.win) + (long long)s * p.w_seq + c0;
+                    for (int q = 0; q < ncols; ++q)
+                        bulk_store(colb + (long long)q * p.w_col, img + (long long)q * BC * ESS, (unsigned)(nch * ESS));
+                } else if (!dense && full_row) {
+                    bulk_store(row_dst, img, (unsigned)(nch * Q * ESS));
+                }
                 if (!hist && !wide)
                     bulk_store(reinterpret_cast<S *>(p.state) + (long long)slot * p.st_slot + (long long)c0 * R, stimg,
                                (unsigned)(nch * R * ESS));
@@ -509,7 +538,7 @@ __global__ void __launch_bounds__(128, (CPT == 4 && TS <= 8) ? 4 : 2) verify_pip
                 load_index(k + 3, pf);
             }
         }
-        if (VL && go && !recomp && !dense && !full_row && Ts > 0) {
+        if (VL && go && !recomp && !dense && !dedup_t && !full_row && Ts > 0) {
             // word w of the staged image holds elements 2w, 2w+1 (bf16) or w (fp32) of the block's
             // [nch][Q] run; an element in column q >= T_s+W-2 is skipped
             const int ncols = Ts + R - 1;

@@ -61,6 +61,9 @@ class VerifyWorkload:
     state_offset: bool = False  # per-sequence offset = accept_len - 1 into a wider state row
     state_dtype: Optional[str] = None  # dtype of state and window when it differs from x ("f32"/"bf16")
     tree: bool = False  # draft tokens form a tree: a random earlier parent (or -1) per token
+    # dedup rows stored column by column ([n_seq, T+W-2, dim] seen as [n_seq, dim, T+W-2]: MambaPool's
+    # axis-0 window layout seen transposed, sglang PR #46184 "Modifications", test coverage)
+    window_transposed: bool = False
     seed: int = 0
 
     @property
@@ -124,6 +127,9 @@ WORKLOADS = {
         VerifyWorkload("n128_t8_dim10240_w4_bf16_history_pad13", n_seq=128, T=8, dim=10240, width=4,
                        qk_channels=4096, head_dim=128, dtype="bf16", layout="history", n_pad=13,
                        extra_slots=16, state_offset=True, seed=5),
+        VerifyWorkload("n128_t8_dim10240_w4_bf16_dedupT_pad13", n_seq=128, T=8, dim=10240, width=4,
+                       qk_channels=4096, head_dim=128, dtype="bf16", layout="dedup", n_pad=13,
+                       extra_slots=16, window_transposed=True, seed=9),
     ]
 }
 WORKLOAD_ORDER = list(WORKLOADS)
@@ -181,6 +187,8 @@ def make_inputs(w: VerifyWorkload, seed: Optional[int] = None) -> dict:
     state_off = (accept - 1).to(torch.int32) if w.state_offset else None
     out = sentinel_tensor((w.n_seq, w.T, w.dim), dt)
     window = None if w.layout in ("history", "recompute") else sentinel_tensor(window_shape(w), w.state_torch_dtype)
+    if window is not None and w.window_transposed:
+        window = sentinel_tensor((w.n_seq, w.T + w.width - 2, w.dim), w.state_torch_dtype).transpose(1, 2)
     r = dict(x=x, x_base=x_wide, conv_state=state, weight=weight, bias=bias, cache_idx=cache_idx,
              state_off=state_off, accept_len=accept, out=out, window=window)
     if w.tree:

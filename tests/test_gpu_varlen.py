@@ -46,7 +46,8 @@ def to_dev(inp, x_shift=0):
         base = xb.to("cuda")
     x = inp["x"]
     d["x_base"] = base
-    d["x"] = base.as_strided(x.shape, x.stride(), x.storage_offset())
+    # (as_strided takes an offset into the whole storage, which starts x_shift elements earlier)
+    d["x"] = base.as_strided(x.shape, x.stride(), base.storage_offset() + x.storage_offset())
     return d
 
 
