@@ -183,7 +183,8 @@ def test_plan_sequence_list_only_with_cache_indices(lib):
 
 
 def test_plan_general_path_cases(lib):
-    """Odd dims, long dedup rows and transposed rows take the general kernel."""
+    """Odd dims, long dedup rows and transposed rows with unaligned columns take the general kernel;
+    transposed rows with 16-byte-aligned columns take the pipelined one (a bulk copy per column)."""
     assert _plan(lib, _args(W3.replace(dim=10236, qk_channels=4096)))[1].path == 0
     assert _plan(lib, _args(W3.replace(T=18)))[1].path == 0
     assert _plan(lib, _args(W3.replace(T=9, dtype="f32")))[1].path == 0
@@ -202,6 +203,8 @@ def test_plan_general_path_cases(lib):
     assert _plan(lib, _args(W3.replace(T=12)))[1].path == 3
     a = _args(W3)
     a.win_ch_stride, a.win_col_stride, a.win_step_stride = 1, W3.dim, W3.dim
+    assert _plan(lib, a)[1].path == 3
+    a.win_col_stride = a.win_step_stride = W3.dim + 4  # columns 8 bytes off 16-byte alignment
     assert _plan(lib, a)[1].path == 0
     a = _args(W3)
     a.x_tok_stride = W3.dim + 1
