@@ -249,9 +249,12 @@ CV_API int cv_conv_verify(const cv_verify_args *args, void *stream);
  * read on the device (no host round trip), 1 <= a <= T:
  *     conv_state[slot][c][k] = snapshot (s, a-1, c, k)      for every c < dim, k < W-1
  * a = T rewrites the state with the value it already holds.  A sequence whose a is out of range
- * gets CV_SEQ_BAD_ACCEPT in err[s] and is untouched.  No commit kernel waits on another thread or
- * on a bulk copy: packed deduplicated rows are read by each thread's own asynchronous copies, and
- * rows laid out transposed (win_ch_stride = 1) by plain loads of the accepted columns only.  The window must be the one the matching
+ * gets CV_SEQ_BAD_ACCEPT in err[s] and is untouched.  Packed deduplicated rows are staged by a
+ * bulk copy per block with a bounded wait (wait_polls, as in cv_verify_args; a timeout flags
+ * CV_SEQ_TIMEOUT and leaves the block's channels unwritten); that kernel ORs its bits into err,
+ * which the library clears first with an asynchronous memset on `stream`.  Rows laid out
+ * transposed (win_ch_stride = 1, 16-byte-aligned columns) are read by plain loads of the accepted
+ * columns alone.  The window must be the one the matching
  * cv_conv_verify wrote (same layout and strides).
  *
  * CV_WINDOW_RECOMPUTE: there is no window; x (with x_seq_stride, x_tok_stride, channel stride 1)
@@ -284,6 +287,7 @@ typedef struct cv_commit_args {
     int64_t x_seq_stride, x_tok_stride;
     const int32_t *cu_draft; /* the matching verify's packed draft spans, or NULL */
     int32_t total_tokens;    /* rows of x (recompute layout) when cu_draft is given */
+    int32_t wait_polls;      /* limit of the packed-dedup commit's bounded wait, as in cv_verify_args */
 } cv_commit_args;
 
 CV_API int cv_conv_commit(const cv_commit_args *args, void *stream);

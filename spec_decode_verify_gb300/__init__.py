@@ -54,7 +54,7 @@ class CommitArgs(ctypes.Structure):
         ("state_cols", c_i32), ("window_layout", c_i32), ("cache_idx", c_vp), ("window", c_vp),
         ("win_seq_stride", c_i64), ("win_step_stride", c_i64), ("win_ch_stride", c_i64), ("win_col_stride", c_i64),
         ("accept_len", c_vp), ("err", c_vp), ("x", c_vp), ("x_seq_stride", c_i64), ("x_tok_stride", c_i64),
-        ("cu_draft", c_vp), ("total_tokens", c_i32),
+        ("cu_draft", c_vp), ("total_tokens", c_i32), ("wait_polls", c_i32),
     ]
 
 
@@ -288,7 +288,7 @@ def verify_plan(x, conv_state, weight, bias, out, window, *, layout, qk_channels
 
 
 def make_commit_args(conv_state, window, accept_len, *, layout, T, width, cache_idx=None, err=None,
-                     x=None, cu_draft=None, total_tokens=None, check_device=True) -> CommitArgs:
+                     x=None, cu_draft=None, total_tokens=None, wait_polls=0, check_device=True) -> CommitArgs:
     """Build cv_commit_args.  Layout "recompute": window is None and x is the verify's input
     [n_seq, T, dim] (channel stride 1).  cu_draft: the matching verify's packed draft spans (x is
     then [total_tokens, dim]); accept_len[s] must lie in 1..T_s."""
@@ -329,18 +329,18 @@ def make_commit_args(conv_state, window, accept_len, *, layout, T, width, cache_
         err=ptr(err, "err", False), x=ptr(x, "x", lay == RECOMPUTE and not (varlen and total_tokens == 0)),
         x_seq_stride=x.stride(0) if x is not None and not varlen else 0,
         x_tok_stride=x.stride(-2) if x is not None else 0,
-        cu_draft=ptr(cu_draft, "cu_draft", False), total_tokens=int(total_tokens or 0))
+        cu_draft=ptr(cu_draft, "cu_draft", False), total_tokens=int(total_tokens or 0), wait_polls=int(wait_polls))
 
 
 def conv_commit(conv_state, window, accept_len, *, layout, T, width, cache_idx=None, err=None, x=None,
-                cu_draft=None, total_tokens=None, stream=None) -> None:
+                cu_draft=None, total_tokens=None, wait_polls=0, stream=None) -> None:
     """Queue the commit: conv_state[slot] <- snapshot accept_len[s]-1 of sequence s (rebuilt from the
     kept window and x with layout "recompute")."""
     for t in (window, x):
         if t is not None and t.dtype != conv_state.dtype:
             raise TypeError("window / x and conv_state must share one dtype")
     a = make_commit_args(conv_state, window, accept_len, layout=layout, T=T, width=width, cache_idx=cache_idx,
-                         err=err, x=x, cu_draft=cu_draft, total_tokens=total_tokens)
+                         err=err, x=x, cu_draft=cu_draft, total_tokens=total_tokens, wait_polls=wait_polls)
     rc = load_library().cv_conv_commit(ctypes.byref(a), _stream_ptr(stream))
     if rc != 0:
         raise CvError(rc, "cv_conv_commit")

@@ -37,14 +37,13 @@ constexpr int kTreeBlocksPerSM = 10;  // tree verify: resident blocks per SM at 
 constexpr int kCommitDenseThreads = 64;      // packed dense snapshot -> packed state (16-byte copies)
 constexpr int kCommitElementThreads = 32;    // element by element
 constexpr int kCommitRecomputeThreads = 64;  // recompute rollback
-// dedup commit: one thread per 8 channels; 1024 channels per block keep the batch in one wave, and
-// the per-thread row slices stay within the default 48 KB of dynamic shared memory (longer rows
-// take the element kernel)
-constexpr int kCommitRowThreads = 128;
-constexpr long long kCommitRowSmem = 48 * 1024;
+// dedup commit: 256 channels per block (small blocks fit beside the verify's resident blocks, so
+// more of them start, under programmatic dependent launch, while the verify drains)
+constexpr int kCommitRowThreads = 32;
 constexpr int kCommitColThreads = 128;  // transposed dedup rows: 1024 channels per block
-// the pipelined kernel lists the active sequences in shared memory up to this batch size
-constexpr int kCompactMaxSeq = 1024;
+// the pipelined kernel lists the active sequences (or packed drafts' chunks) in shared memory up to
+// this many entries
+constexpr int kCompactMaxEntries = 1024;
 constexpr int kPrefillMaxChunk = 256;  // tokens per prefill block, at most / at least (multiples of
 constexpr int kPrefillMinChunk = 32;   // the kernel's 8-token batch, and >= W-1)
 
@@ -83,9 +82,20 @@ DeviceLimits device_limits() {
     return d;
 }
 
-// the list of active sequences (padded ones dropped; packed drafts ordered by draft count)
+// Tokens per unit of the pipelined kernel for packed drafts: the whole draft when T <= 8, else
+// chunks of 8 (so any T runs with the registers of an 8-token unit); T otherwise.
+constexpr int kVarlenChunk = 8;
+int pipe_tokens(const cv_verify_args *a) {
+    return a->cu_draft && a->T > kVarlenChunk ? kVarlenChunk : a->T;
+}
+// entries of the pipelined kernel's work list: sequences, or (packed drafts) chunks of them
+long long pipe_list_len(const cv_verify_args *a) {
+    const int ts = pipe_tokens(a);
+    return (long long)a->n_seq * ((a->T + ts - 1) / ts);
+}
+// the list of active sequences (padded ones dropped; packed drafts as chunks ordered by size)
 bool pipe_compacts(const cv_verify_args *a) {
-    return (a->cache_idx != nullptr || a->cu_draft != nullptr) && a->n_seq <= kCompactMaxSeq;
+    return (a->cache_idx != nullptr || a->cu_draft != nullptr) && pipe_list_len(a) <= kCompactMaxEntries;
 }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -171,13 +181,13 @@ bool io_packed(const cv_verify_args *a, int esize) {
 }
 
 // (esize: bytes of an x element; ssize: of a state and snapshot element)
-bool fast_eligible(const cv_verify_args *a, int esize, int ssize, int max_static_t) {
+bool fast_eligible(const cv_verify_args *a, int esize, int ssize, int max_static_t, int tokens) {
     const int R = a->width - 1;
     const long long Q = a->T + R - 1;
     if (a->window_layout == CV_WINDOW_HISTORY || a->window_layout == CV_WINDOW_RECOMPUTE || !io_packed(a, esize))
         return false;
     if (!aligned16(a->window) || !stride16(a->win_seq_stride, ssize) || a->win_col_stride != 1) return false;
-    if (a->window_layout == CV_WINDOW_DEDUP) return a->win_ch_stride == Q && a->T <= max_static_t;
+    if (a->window_layout == CV_WINDOW_DEDUP) return a->win_ch_stride == Q && tokens <= max_static_t;
     return a->win_ch_stride == R && stride16(a->win_step_stride, ssize);
 }
 
@@ -186,7 +196,7 @@ bool fast_eligible(const cv_verify_args *a, int esize, int ssize, int max_static
 bool dedup_transposed_ok(const cv_verify_args *a, int ssize, int max_static_t) {
     return a->window_layout == CV_WINDOW_DEDUP && a->dim % 8 == 0 && a->win_ch_stride == 1 &&
            a->win_col_stride >= a->dim && aligned16(a->window) && stride16(a->win_seq_stride, ssize) &&
-           stride16(a->win_col_stride, ssize) && a->T <= max_static_t;
+           stride16(a->win_col_stride, ssize) && pipe_tokens(a) <= max_static_t;
 }
 
 // Halve a block (down to 32 threads) while the launch would have fewer than two blocks per SM and
@@ -208,7 +218,7 @@ double units_per_pipe_block(const cv_verify_args *a, int cpt, int sms) {
     const long long bc = (long long)cpt * threads;
     const long long nblk = (a->dim + bc - 1) / bc;
     const long long units = (long long)a->n_seq * nblk;
-    long long g = (long long)sms * pipe_blocks_per_sm(cpt, a->T);
+    long long g = (long long)sms * pipe_blocks_per_sm(cpt, pipe_tokens(a));
     if (g >= nblk) g = g / nblk * nblk;
     if (g > units) g = units;
     return g > 0 ? (double)units / (double)g : 0.0;
@@ -264,7 +274,7 @@ int plan_verify(const cv_verify_args *a, cv_launch_plan *pl) {
     const bool hist = a->window_layout == CV_WINDOW_HISTORY;
     const bool recomp = a->window_layout == CV_WINDOW_RECOMPUTE;
     const int ssize = state_dtype_of(a) == CV_BF16 ? 2 : 4;
-    const bool fast = fast_eligible(a, esize, ssize, ks.max_static_t);
+    const bool fast = fast_eligible(a, esize, ssize, ks.max_static_t, pipe_tokens(a));
     const int cpt = (a->qk_channels > 0 && a->head_dim / 4 > 32) ? 8 : 4;
     // the pipelined kernel stages packed state rows whole (state_ch_stride == state_cols): the
     // committed windows of [dim][W-1] rows, or wider rows read at an offset; the history layout
@@ -272,11 +282,15 @@ int plan_verify(const cv_verify_args *a, cv_launch_plan *pl) {
     const bool rows_packed = aligned16(a->conv_state) && stride16(a->state_slot_stride, ssize) &&
                              a->state_ch_stride == a->state_cols;
     const bool varlen = a->cu_draft != nullptr;
-    // (mixed dtypes: compiled for T <= kMaxMixedT; packed drafts: one dtype)
+    const int ts = pipe_tokens(a);             // tokens per unit
+    const bool chunked = varlen && a->T > ts;  // packed drafts cut into chunks
     const bool dedup_t = dedup_transposed_ok(a, ssize, ks.max_static_t);
+    // (mixed dtypes: compiled for T <= kMaxMixedT; packed drafts: one dtype, and the chunks of a
+    // longer draft need the work list and no history rows)
     bool pipe_ok = (!mixed || a->T <= cvk::kMaxMixedT) && !(mixed && varlen) && io_packed(a, esize) &&
-                   a->T <= ks.max_static_t && rows_packed &&
-                   (hist ? a->state_cols == a->T + R - 1 : (recomp || fast || dedup_t));
+                   ts <= ks.max_static_t && rows_packed &&
+                   (hist ? a->state_cols == a->T + R - 1 : (recomp || fast || dedup_t)) &&
+                   !(chunked && (hist || !pipe_compacts(a)));
     const bool wide = !hist && a->state_cols != R;
     // (wide rows cost whole-row reads and element stores of the window; the pipeline pays that
     // back only when every block walks at least two units, otherwise the one-pass kernel wins)
@@ -289,17 +303,19 @@ int plan_verify(const cv_verify_args *a, cv_launch_plan *pl) {
         while (a->qk_channels > 0 && cpt * threads < a->head_dim) threads *= 2;
         threads = shrink_for_parallelism(threads, cpt, a, lim.sms);
         const long long bc = (long long)cpt * threads;
-        const long long Q = a->T + R - 1;
-        // two stages (x rows + committed windows, or whole history rows) and two image buffers
-        // (dedup row + committed windows, or the history row alone; none for the recompute
-        // rollback), the state parts in the state's dtype; 2 mbarriers, 2 slots, 2 offsets
-        const long long stage = part(a->T * bc * esize) + part((long long)a->state_cols * bc * ssize);
+        const long long Q = ts + R - 1;
+        // two stages (x rows -- with a halo or tail of W-1 more for chunks of packed drafts --
+        // + committed windows, or whole history rows) and two image buffers (dedup row + committed
+        // windows, or the history row alone; none for the recompute rollback), the state parts in
+        // the state's dtype; 2 mbarriers, 2 slots, 2 offsets
+        const long long stage = part((long long)(ts + (chunked ? R : 0)) * bc * esize) +
+                                part((long long)a->state_cols * bc * ssize);
         long long image = (hist || recomp || wide) ? 0 : part(R * bc * ssize);
         if (a->window_layout == CV_WINDOW_DEDUP || hist) image += part(Q * bc * ssize);
         const long long smem = 2 * stage + 2 * image + cvk::kPipeInfoBytes +
-                               (pipe_compacts(a) ? 4LL * cvk::pipe_aux_ints(varlen, a->T) + 4LL * a->n_seq : 0);
+                               (pipe_compacts(a) ? 4LL * cvk::pipe_aux_ints(varlen, ts) + 4LL * pipe_list_len(a) : 0);
         int per_sm = (int)(lim.smem_per_sm / (smem + kSmemPerBlockReserved));
-        if (per_sm > pipe_blocks_per_sm(cpt, a->T)) per_sm = pipe_blocks_per_sm(cpt, a->T);
+        if (per_sm > pipe_blocks_per_sm(cpt, ts)) per_sm = pipe_blocks_per_sm(cpt, ts);
         const int nst = (smem <= lim.smem_per_block && per_sm >= 1) ? 2 : 0;
         if (nst > 0) {
             const long long nblk = (a->dim + bc - 1) / bc;
@@ -461,7 +477,7 @@ int launch_verify(const cv_verify_args *a, const cv_launch_plan &pl, cudaStream_
                           : pl.path == 1 ? ks.fast[ci][a->T]
                           : pl.path == 2 ? ks.fast[ci][0]
                           : pl.path == 3 ? (mixed ? ks.pipe_mixed[ci][a->T]
-                                            : a->cu_draft ? varlen_set(a->dtype, a->width).pipe[ci][a->T]
+                                            : a->cu_draft ? varlen_set(a->dtype, a->width).pipe[ci][pipe_tokens(a)]
                                                           : ks.pipe[ci][a->T])
                                          : ks.tree;
     if (ensure_smem(reinterpret_cast<const void *>(k), pl.smem_bytes) != cudaSuccess) return CV_ERR_LAUNCH;
@@ -514,6 +530,7 @@ int launch_commit(const cv_commit_args *a, cudaStream_t stream) {
     p.w_col = a->win_col_stride;
     p.accept_len = a->accept_len;
     p.err = a->err;
+    p.wait_polls = a->wait_polls;
     p.cu_draft = a->cu_draft;
     p.total_tokens = a->total_tokens;
     p.n_seq = a->n_seq;
@@ -558,14 +575,18 @@ int launch_commit(const cv_commit_args *a, cudaStream_t stream) {
             return CV_ERR_LAUNCH;
         return cudaGetLastError() == cudaSuccess ? CV_OK : CV_ERR_LAUNCH;
     } else if (packed_state && win_ok && dedup && a->win_ch_stride == Q) {
-        // one thread per 8 channels, each with its own shared-memory slice of 8 rows
+        // one block of 8*kCommitRowThreads channels per sequence, its rows staged by one bulk copy
         int rt = kCommitRowThreads;
         while (rt > kMinThreads && 8 * (rt / 2) >= a->dim) rt /= 2;
-        const long long sm = (long long)rt * Q * 8 * esize;
-        if (sm <= kCommitRowSmem) {
+        const long long sm = (8LL * rt * Q * esize + 127) / 128 * 128 + 8;
+        if (sm <= device_limits().smem_per_block) {
             p.mode = 2;
             const int bc = 8 * rt;
             auto kr = kernel_set(a->dtype, a->width).commit_rows;
+            if (ensure_smem(reinterpret_cast<const void *>(kr), (int)sm) != cudaSuccess) return CV_ERR_LAUNCH;
+            // commit_rows ORs its bits into err
+            if (a->err && cudaMemsetAsync(a->err, 0, sizeof(int32_t) * (size_t)a->n_seq, stream) != cudaSuccess)
+                return CV_ERR_LAUNCH;
             if (launch_pdl(kr, dim3((a->dim + bc - 1) / bc, a->n_seq), rt, (int)sm, stream, p) != cudaSuccess)
                 return CV_ERR_LAUNCH;
             return cudaGetLastError() == cudaSuccess ? CV_OK : CV_ERR_LAUNCH;

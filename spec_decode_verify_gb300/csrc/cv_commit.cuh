@@ -21,6 +21,8 @@
 
 namespace cvk {
 
+constexpr unsigned kCommitWaitPolls = 1u << 20;  // mbarrier polls before a block gives up
+
 // Status of sequence s for a commit: 1 = slot out of range, 16 = invalid packed draft span, 4 =
 // accept count a outside 1..T_s.  Sets ts to the sequence's draft count (T, or its packed span's
 // length) and row0 to its first packed row.  A sequence with ts = 0 has nothing to commit.
@@ -87,54 +89,73 @@ __global__ void __launch_bounds__(128) commit_kernel(const __grid_constant__ Com
     }
 }
 
-// Commit of packed deduplicated rows into packed state rows (mode 2): one thread per 8 channels of
-// one sequence, one wave of blocks.  The rows do not depend on the cache slot or the accept count,
-// so each thread first starts 16-byte asynchronous copies (cp.async) of its 8 channels' rows -- one
-// contiguous run of 8*(T+W-2) elements -- into its own slice of shared memory, then reads the slot
-// and the accept count while they are in flight: a single round trip, and no thread waits on
-// another (nothing but the thread's own copies is waited for, so there is no barrier and no spin).
-// The state run [c][k] = row[c][a-1+k] of its channels is then gathered from the slice and written
-// as 16-byte stores.  (Right after the verify the rows are still in L2; reading the whole rows in
-// parallel with the indices beats reading the slot first and then only the needed columns.)
+// Commit of packed deduplicated rows into packed state rows (mode 2): one block per (block of
+// 8*threads channels, sequence), a single wave of small blocks.  The row address does not depend
+// on the cache slot, so thread 0 starts the bulk copy (TMA, cp.async.bulk) of the block's rows --
+// one contiguous run of channels*(T+W-2) elements -- before anything else, and the slot and the
+// accept count are read while it is in flight; no dependent load precedes the data.  (Right after
+// the verify the rows are in L2: reading them whole in parallel with the indices beats reading the
+// slot first and then only the needed columns; the rows of padded sequences are read too.)  The
+// state run [c][k] = row[c][a-1+k] is then gathered from shared memory and written with 16-byte
+// coalesced stores.  A padded or rejected sequence still waits for its copy (the shared memory must
+// outlive it) and writes nothing.  The wait is bounded (p.wait_polls polls, 0 = the default,
+// negative = none): a timeout sets CV_SEQ_TIMEOUT in err, and the copy is then drained with the
+// default limit before the block leaves.  Every err bit is ORed in; the library clears err before
+// the launch.
 template <typename B, int W>
-__global__ void __launch_bounds__(128) commit_rows(const __grid_constant__ CommitParams p) {
+__global__ void __launch_bounds__(64) commit_rows(const __grid_constant__ CommitParams p) {
     grid_dep_wait();
     grid_dep_launch();
     constexpr int R = W - 1;
     constexpr int ES = (int)sizeof(B);
-    constexpr int VE = 16 / ES;  // elements per 16-byte vector
-    extern __shared__ __align__(16) unsigned char smem[];
+    constexpr int VE = 16 / ES;
+    extern __shared__ __align__(128) unsigned char smem[];
+    const int tid = threadIdx.x;
     const int s = blockIdx.y;
-    const int c = 8 * (blockIdx.x * blockDim.x + threadIdx.x);  // first of this thread's 8 channels
+    const int BC = 8 * blockDim.x;
+    const int c0 = blockIdx.x * BC;
+    const int nch = min(BC, p.dim - c0);
     const int Q = p.T + R - 1;
-    const int nv = Q * 8 * ES / 16;  // 16-byte vectors of the 8 rows
-    if ((long long)blockDim.x * nv * 16 > (long long)dynamic_smem_bytes()) return;  // launch mismatch
-    B *const mine = reinterpret_cast<B *>(smem + (long long)threadIdx.x * nv * 16);
-    const bool has = c < p.dim;  // (dim % 8 == 0 on this path)
-    if (has) {
-        const B *src = reinterpret_cast<const B *>(p.win) + (long long)s * p.w_seq + (long long)c * Q;
-        for (int i = 0; i < nv; ++i) cp_async16(mine + i * VE, src + i * VE);
+    const long long row_bytes = ((long long)BC * Q * ES + 127) / 128 * 128;
+    uint64_t *const bar = reinterpret_cast<uint64_t *>(smem + row_bytes);
+    if (row_bytes + 8 > (long long)dynamic_smem_bytes()) return;  // launch mismatch
+    if (tid == 0) {
+        mbar_init(bar, 1);
+        mbar_init_fence();
+        mbar_arrive_expect_tx(bar, (unsigned)(nch * Q * ES));
+        bulk_load(smem, reinterpret_cast<const B *>(p.win) + (long long)s * p.w_seq + (long long)c0 * Q,
+                  (unsigned)(nch * Q * ES), bar);
     }
-    asm volatile("cp.async.commit_group;\n" ::: "memory");
     const int slot = p.cache_idx ? __ldg(p.cache_idx + s) : s;
     const int a = __ldg(p.accept_len + s);
     int ts, row0;
     const int status = commit_status(p, s, slot, a, ts, row0);
-    if (p.err && blockIdx.x == 0 && threadIdx.x == 0) p.err[s] = status;
-    asm volatile("cp.async.wait_group 0;\n" ::: "memory");  // (this thread's own copies)
-    if (!has || slot < 0 || status || ts == 0) return;
-    B *d = reinterpret_cast<B *>(p.state) + (long long)slot * p.st_slot + (long long)c * R;
+    if (p.err && blockIdx.x == 0 && tid == 0 && status) atomicOr(p.err + s, status);
+    __syncthreads();  // the barrier's initialisation is visible to every waiting thread
+    const unsigned polls = p.wait_polls == 0 ? kCommitWaitPolls : p.wait_polls < 0 ? 0u : (unsigned)p.wait_polls;
+    const bool ok = mbar_wait_bounded(bar, 0u, polls);
+    if (__syncthreads_or(!ok)) {  // every thread agrees before anyone leaves
+        if (tid == 0) {
+            if (p.err && slot >= 0) atomicOr(p.err + s, kSeqTimeout);
+            mbar_wait_bounded(bar, 0u, kCommitWaitPolls);  // drain the copy (bounded)
+        }
+        return;
+    }
+    if (slot < 0 || status || ts == 0) return;
+    const B *sm = reinterpret_cast<const B *>(smem);
+    B *d = reinterpret_cast<B *>(p.state) + (long long)slot * p.st_slot + (long long)c0 * R;
     const int col0 = a - 1;
-#pragma unroll
-    for (int m = 0; m < 8 * R / VE; ++m) {
+    const int nd = nch * R / VE;
+    for (int m = tid; m < nd; m += blockDim.x) {
         uint32_t wv[4];
 #pragma unroll
         for (int h = 0; h < 4; ++h) {
             uint32_t bits[2] = {0u, 0u};
 #pragma unroll
             for (int z = 0; z < 4 / ES; ++z) {
-                const int pos = m * VE + h * (4 / ES) + z;  // element (channel pos / R, column pos % R)
-                bits[z] = (uint32_t)mine[(pos / R) * Q + col0 + pos % R];
+                const int pos = m * VE + h * (4 / ES) + z;
+                const int cc = pos / R, kk = pos - cc * R;
+                bits[z] = (uint32_t)sm[cc * Q + col0 + kk];
             }
             wv[h] = (ES == 2) ? pack_halves(bits[0], bits[1]) : bits[0];
         }

@@ -41,9 +41,13 @@ struct VerifyParams {
 
 // Pipelined verify: shared memory after the stages and images holds 2 mbarriers, then 8 ints of
 // unit information (slots, state offsets, draft counts, first rows of the two units in flight),
-// then the compaction scratch (pipe_aux_ints of them) and the list of active sequences.
+// then the listing scratch (pipe_aux_ints of them: 4 warp counts, or list_chunks' counts) and the
+// list of active sequences (or of chunks).
 constexpr int kPipeInfoBytes = 16 + 32;
-__host__ __device__ constexpr int pipe_aux_ints(bool varlen, int T) { return varlen ? 5 * (T + 2) : 4; }
+__host__ __device__ constexpr int pipe_aux_ints(bool varlen, int TS) { return varlen ? 5 * (TS + 2) : 4; }
+
+constexpr int kSeqTimeout = 8;  // err bit: a bounded wait for a bulk copy gave up
+__host__ __device__ constexpr int pipe_align(int bytes) { return bytes % 16 == 0 ? 16 : 8; }
 
 // Tree verify: channels per block, 8 per lane of a warp.
 constexpr int kTreeChannels = 256;
@@ -64,6 +68,7 @@ struct CommitParams {
     long long x_seq, x_tok;
     const int *cu_draft;  // packed ragged drafts of the matching verify, or null (T tokens each)
     int total_tokens;
+    int wait_polls;  // polls of the bounded wait for the staged rows: 0 = the default, < 0 = none
 };
 
 struct PrefillParams {
@@ -109,6 +114,71 @@ __device__ __forceinline__ int draft_span(const int *cu, int s, int T, int total
     row0 = b;
     ts = e - b;
     return span_status(b, e, T, total);
+}
+
+// The work list of a persistent verify kernel over packed ragged drafts, built identically by every
+// block (block-wide: every thread of a block of at most 4 warps calls it).  A sequence with a cache
+// slot >= 0 contributes one entry per chunk of at most TS of its T_s draft tokens (one entry when
+// T_s = 0 or its span is bad), encoded (chunk << 16) | sequence.  Entries are ordered by the number
+// of tokens they hold, most first, so that units of similar cost come together in the round-robin
+// walk; ties are ordered by chunk, then sequence.  A stable counting sort: a shared-memory
+// histogram of the keys (TS - tokens), its prefix sums, then each entry's place from its key's
+// start, the counts of earlier warps in the chunk of sequences and its rank among its warp's lanes
+// of the same key (__match_any_sync).  scratch holds pipe_aux_ints(true, TS) ints of counts, then
+// the list.  Returns its length.
+__device__ __forceinline__ int list_chunks(const VerifyParams &p, int *scratch, int TS) {
+    const int NB = TS + 1;             // keys 0 .. TS
+    int *const cnt = scratch;          // [NB + 1]: bucket sizes, then each bucket's next position
+    int *const wc = scratch + NB + 1;  // [NB][4]: per-warp counts of the current chunk of sequences
+    int *const list = scratch + pipe_aux_ints(true, TS);
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nt = blockDim.x;
+    const int C = (p.T + TS - 1) / TS;  // chunks of the longest draft
+    // the key of sequence i's chunk c, or -1 when it has none
+    auto key_of = [&](int i, int c) -> int {
+        if (i >= p.n_seq || (p.cache_idx && __ldg(p.cache_idx + i) < 0)) return -1;
+        int ts, r0;
+        if (draft_span(p.cu_draft, i, p.T, p.total_tokens, ts, r0)) return c == 0 ? TS : -1;
+        if (c > 0 && c * TS >= ts) return -1;
+        return TS - min(TS, ts - c * TS);
+    };
+    for (int v = tid; v <= NB; v += nt) cnt[v] = 0;
+    __syncthreads();
+    for (int c = 0; c < C; ++c)
+        for (int i0 = 0; i0 < p.n_seq; i0 += nt) {
+            const int key = key_of(i0 + tid, c);
+            if (key >= 0) atomicAdd(cnt + key, 1);
+        }
+    __syncthreads();
+    if (tid == 0) {
+        int run = 0;
+        for (int v = 0; v < NB; ++v) {
+            const int n = cnt[v];
+            cnt[v] = run;
+            run += n;
+        }
+        cnt[NB] = run;
+    }
+    __syncthreads();
+    const int n_list = cnt[NB];
+    for (int c = 0; c < C; ++c)
+        for (int i0 = 0; i0 < p.n_seq; i0 += nt) {
+            const int i = i0 + tid;
+            const int key = key_of(i, c);
+            for (int v = tid; v < 4 * NB; v += nt) wc[v] = 0;
+            __syncthreads();
+            const unsigned m = __match_any_sync(0xffffffffu, key);
+            if (key >= 0 && lane == __ffs(m) - 1) wc[key * 4 + warp] = __popc(m);
+            __syncthreads();
+            if (key >= 0) {
+                int before = 0;
+                for (int w = 0; w < warp; ++w) before += wc[key * 4 + w];
+                list[cnt[key] + before + __popc(m & ((1u << lane) - 1u))] = (c << 16) | i;
+            }
+            __syncthreads();
+            for (int v = tid; v < NB; v += nt) cnt[v] += wc[v * 4] + wc[v * 4 + 1] + wc[v * 4 + 2] + wc[v * 4 + 3];
+            __syncthreads();
+        }
+    return n_list;
 }
 
 template <typename B> __device__ __forceinline__ float widen(B b);

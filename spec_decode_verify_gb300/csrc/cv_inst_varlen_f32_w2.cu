@@ -1,4 +1,4 @@
-// Packed-ragged-draft variants of the pipelined verify kernel for f32 elements, conv width 2.
+// Packed-ragged-draft variants of the pipelined verify kernel for f32 elements, conv width 2 (units of at most 8 tokens).
 #define CV_INST_VARLEN
 #define CV_INST_B uint32_t
 #define CV_INST_W 2

@@ -40,13 +40,18 @@
 // make the products inexact).
 // Packed ragged drafts (VL; sglang PR #46184, "Related upstream work": target verify on packed ragged
 // tokens, the tile store covering the packed rows): sequence s owns rows [cu[s], cu[s+1]) of x and
-// out, T_s <= TS of them.  A unit copies only its T_s x rows; outputs, dense snapshot steps and
-// deduplicated columns past T_s are not written (a full row still leaves as one bulk copy; a shorter
-// one is copied out of the staged image by the whole block, word by word, with the columns past
-// T_s+W-2 skipped); the committed window full[T_s .. T_s+W-2] is gathered from the staged rows.
-// Units of long and short drafts differ in cost, so the list of active sequences is ordered by
-// draft count, longest first (a counting sort every block performs identically): consecutive
-// units of the round-robin walk then have similar cost and every block gets a similar mix.
+// out, T_s <= p.T of them, cut into chunks of at most TS tokens (TS = p.T when p.T <= 8, else 8):
+// a unit is (sequence, chunk, channel block), so a draft of any length runs with the registers of
+// an 8-token unit.  Chunk c holds tokens [8c, 8c + n); its first W-1 inputs are the committed
+// window (c = 0) or the 3 x rows before it (the halo, staged after the chunk's rows), and it writes
+// its outputs, its dense snapshot steps and its columns of the snapshot row: a full row leaves as
+// one bulk copy, a transposed row as one bulk copy per column, anything shorter is copied out of
+// the staged image by the block element by element (columns past T_s+W-2 are never written).  The
+// committed window full[T_s .. T_s+W-2] is written by chunk 0 alone -- from its own rows, or from
+// the last W-1 rows of the draft, which it stages as a tail -- so no other block's chunk writes a
+// state row that chunk 0 reads.  Units of long and short chunks differ in cost, so the list of
+// units is ordered by tokens per chunk, most first (list_chunks, identical in every block):
+// consecutive units of the round-robin walk then cost about the same.
 // Preconditions (checked on the host): those of the fast path, packed 16-byte-aligned state rows
 // (state_ch_stride == state_cols; exactly T+W-2 columns for the history layout), T <= 17 (bf16) /
 // 8 (fp32), head_dim / CPT <= 32.
@@ -59,9 +64,6 @@
 namespace cvk {
 
 constexpr unsigned kWaitPolls = 1u << 20;  // mbarrier polls before a block gives up
-constexpr int kSeqTimeout = 8;             // err bit: a bulk copy did not complete in time
-
-__host__ __device__ constexpr int pipe_align(int bytes) { return bytes % 16 == 0 ? 16 : 8; }
 
 // Bytes of one stage for a block of bc channels (x rows, windows, taps, bias), each part 128-aligned.
 __host__ __device__ constexpr long long pipe_part(long long b) { return (b + 127) / 128 * 128; }
@@ -101,11 +103,16 @@ __global__ void __launch_bounds__(128, (CPT == 4 && TS <= 8) ? 4 : 2) verify_pip
     const bool whole_rows = SC != R;
     const bool wide = whole_rows && !hist;  // wider rows, not history: the window is stored directly
 
+    // packed drafts longer than a chunk: W-1 more staged x rows per unit (a halo or a tail)
+    const bool chunked = VL && p.T > TS;
+    const int XR = TS + (chunked ? R : 0);
+    const int Qrow = p.T + R - 1;  // columns of the snapshot row in global memory (Q: of the staged image)
+
     // shared memory: stage 0, stage 1 (x rows + committed windows, or whole history rows), image
     // buffers 0 and 1 (dedup row image + committed-window image, or the history row image alone),
     // 2 mbarriers and the unit information (kPipeInfoBytes), then (when compacting) the sort or warp
-    // counts (AUX ints) and the list of active sequences
-    const long long xb = pipe_part((long long)TS * BC * ES);
+    // counts (AUX ints) and the list of active sequences (of chunks, for packed drafts)
+    const long long xb = pipe_part((long long)XR * BC * ES);
     const long long stage_bytes = xb + pipe_part((long long)SC * BC * ESS);
     const long long rb = dense ? 0 : pipe_part((long long)Q * BC * ESS);
     const long long img_bytes = recomp ? 0 : rb + ((hist || wide) ? 0 : pipe_part((long long)R * BC * ESS));
@@ -117,7 +124,8 @@ __global__ void __launch_bounds__(128, (CPT == 4 && TS <= 8) ? 4 : 2) verify_pip
     int *const wcount = reinterpret_cast<int *>(smem + 2 * stage_bytes + 2 * img_bytes + kPipeInfoBytes);
     int *const act = wcount + AUX;
     const bool compact = p.compact != 0;
-    if (2 * stage_bytes + 2 * img_bytes + kPipeInfoBytes + (compact ? 4LL * AUX + 4LL * p.n_seq : 0) >
+    const long long list_len = VL ? (long long)p.n_seq * ((p.T + TS - 1) / TS) : p.n_seq;
+    if (2 * stage_bytes + 2 * img_bytes + kPipeInfoBytes + (compact ? 4LL * AUX + 4LL * list_len : 0) >
         (long long)dynamic_smem_bytes())
         return;  // launch mismatch
 
@@ -134,59 +142,7 @@ __global__ void __launch_bounds__(128, (CPT == 4 && TS <= 8) ? 4 : 2) verify_pip
     // clears err before the launch.)
     int n_act = p.n_seq;
     if (VL && compact) {
-        // the listed sequences (cache slot >= 0) ordered by key = TS - T_s (longest drafts first; a
-        // bad span counts as empty), ties in ascending sequence order: a stable counting sort whose
-        // counts come from warp ballots, so every block builds the same list
-        constexpr int NB = TS + 1;  // keys 0 .. TS
-        const int lane = tid & 31, warp = tid >> 5, nwarps = ((int)blockDim.x + 31) >> 5;
-        int *const bstart = wcount;       // [NB]: bucket sizes, then the next free position of each
-        int *const wc = wcount + NB + 1;  // [NB][4]: per-warp counts of the current chunk
-        auto key_of = [&](int i) -> int {
-            if (i >= p.n_seq || (p.cache_idx && __ldg(p.cache_idx + i) < 0)) return -1;
-            int ts, r0;
-            return draft_span(p.cu_draft, i, TS, p.total_tokens, ts, r0) ? TS : TS - ts;
-        };
-        for (int v = tid; v < NB; v += (int)blockDim.x) bstart[v] = 0;
-        __syncthreads();
-        for (int i0 = 0; i0 < p.n_seq; i0 += (int)blockDim.x) {
-            const int key = key_of(i0 + tid);
-            for (int v = 0; v < NB; ++v) {
-                const unsigned m = __ballot_sync(0xffffffffu, key == v);
-                if (lane == 0 && m) atomicAdd(bstart + v, __popc(m));
-            }
-        }
-        __syncthreads();
-        if (tid == 0) {
-            int run = 0;
-            for (int v = 0; v < NB; ++v) {
-                const int n = bstart[v];
-                bstart[v] = run;
-                run += n;
-            }
-            bstart[NB] = run;
-        }
-        __syncthreads();
-        n_act = bstart[NB];
-        for (int i0 = 0; i0 < p.n_seq; i0 += (int)blockDim.x) {
-            const int i = i0 + tid;
-            const int key = key_of(i);
-            unsigned mine = 0u;
-            for (int v = 0; v < NB; ++v) {
-                const unsigned m = __ballot_sync(0xffffffffu, key == v);
-                if (key == v) mine = m;
-                if (lane == 0) wc[v * 4 + warp] = __popc(m);
-            }
-            __syncthreads();
-            if (key >= 0) {
-                int before = 0;
-                for (int w = 0; w < warp; ++w) before += wc[key * 4 + w];
-                act[bstart[key] + before + __popc(mine & ((1u << lane) - 1u))] = i;
-            }
-            __syncthreads();
-            for (int v = tid; v < NB; v += (int)blockDim.x)
-                for (int w = 0; w < nwarps; ++w) bstart[v] += wc[v * 4 + w];
-            __syncthreads();
-        }
+        n_act = list_chunks(p, wcount, TS);
     } else if (compact) {
         const int lane = tid & 31, warp = tid >> 5, nwarps = ((int)blockDim.x + 31) >> 5;
         n_act = 0;
@@ -198,15 +154,16 @@ __global__ void __launch_bounds__(128, (CPT == 4 && TS <= 8) ? 4 : 2) verify_pip
             __syncthreads();
             int before = 0, total = 0;
             for (int w = 0; w < nwarps; ++w) {
-                const int c = wcount[w];
-                before += w < warp ? c : 0;
-                total += c;
+                const int cw = wcount[w];
+                before += w < warp ? cw : 0;
+                total += cw;
             }
             if (a) act[n_act + before + __popc(m & ((1u << lane) - 1u))] = i;
             n_act += total;
             __syncthreads();
         }
     }
+    // list entry q: (chunk << 16) | sequence (chunk 0 without packed drafts)
     auto seq_at = [&](int q) { return compact ? act[q] : q; };
     const int n_units = n_act * nblk;
     const int iters = (int)blockIdx.x < n_units ? (n_units - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
@@ -219,17 +176,18 @@ __global__ void __launch_bounds__(128, (CPT == 4 && TS <= 8) ? 4 : 2) verify_pip
     auto unit_of = [&](int k, int &s, int &c0, int &nch) {
         const int u = (int)blockIdx.x + k * (int)gridDim.x;
         const int q = u / nblk;
-        s = seq_at(q);
+        s = seq_at(q) & 0xffff;
         c0 = (u - q * nblk) * BC;
         nch = min(BC, p.dim - c0);
     };
+    auto chunk_of = [&](int k) { return VL ? seq_at(((int)blockIdx.x + k * (int)gridDim.x) / nblk) >> 16 : 0; };
     // a unit's index data: cache slot, state offset and (packed drafts) its row span [b, e)
     struct UnitIdx {
         int slot, off, b, e;
     };
     auto load_index = [&](int k, UnitIdx &ix) {
         if (k >= iters) return;
-        const int s = seq_at(((int)blockIdx.x + k * (int)gridDim.x) / nblk);
+        const int s = seq_at(((int)blockIdx.x + k * (int)gridDim.x) / nblk) & 0xffff;
         ix.slot = p.cache_idx ? __ldg(p.cache_idx + s) : s;
         ix.off = p.state_off ? __ldg(p.state_off + s) : 0;
         if constexpr (VL) {
@@ -240,15 +198,28 @@ __global__ void __launch_bounds__(128, (CPT == 4 && TS <= 8) ? 4 : 2) verify_pip
             ix.e = s + TS;
         }
     };
-    // the unit's x rows: T_s rows from row b (packed drafts), or the TS rows of sequence s
-    auto issue_x = [&](int k, int b, int ts) {
+    // the unit's x rows: n rows from row b (packed drafts: the chunk's rows), or the TS rows of
+    // sequence s, into stage rows 0 .. n-1
+    auto issue_x = [&](int k, int b, int n) {
         const int st = k & 1;
         int s, c0, nch;
         unit_of(k, s, c0, nch);
-        mbar_expect_tx(&bar[st], (unsigned)(ts * nch * ES));
+        mbar_expect_tx(&bar[st], (unsigned)(n * nch * ES));
         const B *xs = reinterpret_cast<const B *>(p.x) + (VL ? (long long)b * p.x_tok : (long long)s * p.x_seq) + c0;
-        for (int t = 0; t < ts; ++t)
+        for (int t = 0; t < n; ++t)
             bulk_load(smem + st * stage_bytes + (long long)t * BC * ES, xs + (long long)t * p.x_tok,
+                      (unsigned)(nch * ES), &bar[st]);
+    };
+    // (packed drafts) W-1 x rows from row b into stage rows TS .. TS+W-2: a later chunk's halo, or
+    // chunk 0's tail (the draft's last W-1 rows, which hold the committed window)
+    auto issue_extra = [&](int k, int b) {
+        const int st = k & 1;
+        int s, c0, nch;
+        unit_of(k, s, c0, nch);
+        mbar_expect_tx(&bar[st], (unsigned)(R * nch * ES));
+        const B *xs = reinterpret_cast<const B *>(p.x) + (long long)b * p.x_tok + c0;
+        for (int j = 0; j < R; ++j)
+            bulk_load(smem + st * stage_bytes + (long long)(TS + j) * BC * ES, xs + (long long)j * p.x_tok,
                       (unsigned)(nch * ES), &bar[st]);
     };
     // the phase cannot complete before the single arrival at its end, so a late expect_tx is safe
@@ -259,23 +230,31 @@ __global__ void __launch_bounds__(128, (CPT == 4 && TS <= 8) ? 4 : 2) verify_pip
         const int slot = ix.slot, off = ix.off;
         int status = seq_status(slot, off, p.n_slots, p.state_cols, R);
         int ts = TS;
+        const int ch = chunk_of(k);
         if constexpr (VL) {  // (the span was loaded with the indices, one issue ahead)
             ts = ix.e - ix.b;
-            if (slot >= 0) status |= span_status(ix.b, ix.e, TS, p.total_tokens);
+            if (slot >= 0) status |= span_status(ix.b, ix.e, p.T, p.total_tokens);
         }
-        if (p.err && c0 == 0 && status) atomicOr(p.err + s, status);
+        if (p.err && c0 == 0 && ch == 0 && status) atomicOr(p.err + s, status);
         const bool go = slot >= 0 && status == 0;
         info[st] = go ? slot : -1;
         info[2 + st] = off;
-        info[4 + st] = ts;
+        info[4 + st] = (ch << 16) | ts;
         info[6 + st] = ix.b;
         if (go) {
-            if (!x_sent) issue_x(k, ix.b, ts);
-            // packed state rows of SC columns: the committed windows, or whole rows
-            mbar_expect_tx(&bar[st], (unsigned)(SC * nch * ESS));
-            bulk_load(smem + st * stage_bytes + xb,
-                      reinterpret_cast<const S *>(p.state) + (long long)slot * p.st_slot + (long long)c0 * SC,
-                      (unsigned)(nch * SC * ESS), &bar[st]);
+            const int t0 = ch * TS;
+            const int n = VL ? min(TS, ts - t0) : TS;
+            if (!x_sent) issue_x(k, ix.b + t0, n);
+            if (ch > 0) {
+                issue_extra(k, ix.b + t0 - R);  // the halo: the W-1 rows before the chunk
+            } else {
+                if (chunked && ts > TS) issue_extra(k, ix.b + ts - R);  // the tail: the draft's last W-1 rows
+                // packed state rows of SC columns: the committed windows, or whole rows
+                mbar_expect_tx(&bar[st], (unsigned)(SC * nch * ESS));
+                bulk_load(smem + st * stage_bytes + xb,
+                          reinterpret_cast<const S *>(p.state) + (long long)slot * p.st_slot + (long long)c0 * SC,
+                          (unsigned)(nch * SC * ESS), &bar[st]);
+            }
         }
         mbar_arrive(&bar[st]);
     };
@@ -308,7 +287,7 @@ __global__ void __launch_bounds__(128, (CPT == 4 && TS <= 8) ? 4 : 2) verify_pip
     int wcb = -1;
     for (int k = 0; k < iters; ++k) {
         const int st = k & 1;
-        const int s = seq_at(q);
+        const int s = seq_at(q) & 0xffff;  // (a list entry of packed drafts also holds the chunk)
         const unsigned char *stg = smem + st * stage_bytes;
         unsigned char *const img = img0 + (k & 1) * img_bytes;
         unsigned char *const stimg = img + rb;
@@ -344,8 +323,13 @@ __global__ void __launch_bounds__(128, (CPT == 4 && TS <= 8) ? 4 : 2) verify_pip
         const int slot = ok ? info[st] : -1;
         const int off = info[2 + st];
         const bool go = slot >= 0;
-        const int Ts = VL ? info[4 + st] : TS;           // draft tokens of this unit's sequence
-        const long long row0 = VL ? info[6 + st] : 0;    // its first packed row
+        const int Ts = VL ? (info[4 + st] & 0xffff) : TS;   // draft tokens of this unit's sequence
+        const int chunk = VL ? (info[4 + st] >> 16) : 0;    // which chunk of them
+        const int t0 = chunk * TS;                          // its first token
+        const int nt = VL ? max(0, min(TS, Ts - t0)) : TS;  // its token count
+        const bool first = chunk == 0;                      // (reads and writes the state)
+        const bool tail = chunked && first && Ts > TS;      // (its committed window is in the tail rows)
+        const long long row0 = VL ? info[6 + st] : 0;       // the sequence's first packed row
 
         float fw[CPT][R + TS];  // inputs widened to fp32: [0, R) committed window, then x
         uint32_t xr[TS][NW];    // raw x rows
@@ -353,14 +337,28 @@ __global__ void __launch_bounds__(128, (CPT == 4 && TS <= 8) ? 4 : 2) verify_pip
         if (go && act) {
 #pragma unroll
             for (int t = 0; t < TS; ++t) {
-                if (!VL || t < Ts) {
+                if (!VL || t < nt) {
                     ldv<VX, NW>(xr[t], stg + ((long long)t * BC + cl) * ES);
                 } else {
 #pragma unroll
                     for (int i = 0; i < NW; ++i) xr[t][i] = 0u;  // (no row: keep stale bits out)
                 }
             }
-            if (whole_rows) {
+            if (VL && !first) {
+                // a later chunk: its first W-1 inputs are the halo rows (the x rows before it)
+                uint32_t hr[R][NW];
+#pragma unroll
+                for (int j = 0; j < R; ++j) ldv<VX, NW>(hr[j], stg + ((long long)(TS + j) * BC + cl) * ES);
+#pragma unroll
+                for (int i = 0; i < R * NWS; ++i) {
+                    if (ESS == 2) {
+                        const int a = 2 * i, b2 = 2 * i + 1;  // elements (channel a / R, input a % R)
+                        sw[i] = pack_halves(elem_raw<S>(hr[a % R], a / R), elem_raw<S>(hr[b2 % R], b2 / R));
+                    } else {
+                        sw[i] = hr[i % R][i / R];
+                    }
+                }
+            } else if (whole_rows) {
                 // the committed window sits at columns [off, off+W-1) of each staged row
                 using U = std::conditional_t<ESS == 2, unsigned short, unsigned>;
                 const U *row = reinterpret_cast<const U *>(stg + xb) + (long long)cl * SC + off;
@@ -433,23 +431,30 @@ __global__ void __launch_bounds__(128, (CPT == 4 && TS <= 8) ? 4 : 2) verify_pip
                 S *wsq = reinterpret_cast<S *>(p.win) + (long long)s * p.w_seq + (long long)c * R;
 #pragma unroll
                 for (int t = 0; t < TS; ++t) {
-                    if (VL && t >= Ts) break;
+                    if (VL && t >= nt) break;
                     uint32_t w[R * NWS];
 #pragma unroll
                     for (int i = 0; i < R * NWS; ++i) w[i] = run_word(i, R, t + 1);
-                    stv<VS, R * NWS>(wsq + (long long)t * p.w_step, w);
+                    stv<VS, R * NWS>(wsq + (long long)(t0 + t) * p.w_step, w);
                 }
             }
             // committed window = full[T_s .. T_s+W-2], channel-major [CPT][R] words
             uint32_t fin[R * NWS];
-            if constexpr (VL) {
-                // column kk is x row T_s+kk-R when that is >= 0 (read back from the stage), else
+#pragma unroll
+            for (int i = 0; i < R * NWS; ++i) fin[i] = 0u;
+            if (VL && !first) {
+                // a later chunk writes no committed window (chunk 0 does)
+            } else if constexpr (VL) {
+                // column kk is x row T_s+kk-R when that is >= 0 (read back from the stage: from the
+                // chunk's rows, or from the tail rows when the draft is longer than a chunk), else
                 // committed-window column T_s+kk (T_s < W-1)
                 uint32_t col[R][NW];
 #pragma unroll
                 for (int kk = 0; kk < R; ++kk) {
                     const int j = Ts + kk;
-                    if (j >= R) {
+                    if (tail) {
+                        ldv<VX, NW>(col[kk], stg + ((long long)(TS + kk) * BC + cl) * ES);
+                    } else if (j >= R) {
                         ldv<VX, NW>(col[kk], stg + ((long long)(j - R) * BC + cl) * ES);
                     } else {
 #pragma unroll
@@ -478,14 +483,17 @@ __global__ void __launch_bounds__(128, (CPT == 4 && TS <= 8) ? 4 : 2) verify_pip
 #pragma unroll
                 for (int i = 0; i < R * NWS; ++i) fin[i] = run_word(i, R, TS);
             }
-            if (wide && !recomp) {
+            if (wide) {
                 // committed window -> columns [0, W-1) of the wide rows, stored directly (the rows'
-                // other columns are not this call's to rewrite); this thread alone owns them
-                S *srow = reinterpret_cast<S *>(p.state) + (long long)slot * p.st_slot + (long long)c * SC;
+                // other columns are not this call's to rewrite); this thread alone owns them.  (Wide
+                // rows have no committed-window image; only chunk 0 of a packed draft writes.)
+                if (!recomp && first) {
+                    S *srow = reinterpret_cast<S *>(p.state) + (long long)slot * p.st_slot + (long long)c * SC;
 #pragma unroll
-                for (int e = 0; e < CPT; ++e)
+                    for (int e = 0; e < CPT; ++e)
 #pragma unroll
-                    for (int kk = 0; kk < R; ++kk) srow[(long long)e * SC + kk] = (S)elem_raw<S>(fin, e * R + kk);
+                        for (int kk = 0; kk < R; ++kk) srow[(long long)e * SC + kk] = (S)elem_raw<S>(fin, e * R + kk);
+                }
             } else if (!hist && !recomp) {
                 stv<VS, R * NWS>(stimg + (long long)tid * CPT * R * ESS, fin);
             }
@@ -512,23 +520,27 @@ __global__ void __launch_bounds__(128, (CPT == 4 && TS <= 8) ? 4 : 2) verify_pip
             }
             return;
         }
-        // the row image (dedup row, or history row): whole rows leave as one bulk copy; a packed
-        // sequence with fewer than TS drafts writes only columns [0, T_s+W-2) of each channel's row
-        const bool full_row = !VL || Ts == TS;
-        S *const row_dst = hist ? reinterpret_cast<S *>(p.state) + (long long)slot * p.st_slot + (long long)c0 * Q
-                                : reinterpret_cast<S *>(p.win) + (long long)s * p.w_seq + (long long)c0 * Q;
+        // the row image (dedup row, or history row): whole rows leave as one bulk copy.  A packed
+        // draft's unit writes columns [qd, qd + cnt) of each channel's row from image columns
+        // [qs, qs + cnt): its own inputs only (chunk 0 also the window's columns 1 .. W-2)
+        const bool full_row = !VL || (!chunked && Ts == TS);
+        const int qs = first ? 0 : R - 1, qd = first ? 0 : t0 + R - 1;
+        const int cnt = first ? (nt > 0 ? nt + R - 1 : 0) : nt;
+        S *const row_dst = hist ? reinterpret_cast<S *>(p.state) + (long long)slot * p.st_slot + (long long)c0 * Qrow
+                                : reinterpret_cast<S *>(p.win) + (long long)s * p.w_seq + (long long)c0 * Qrow;
         if (tid == 0) {
             if (go && !recomp) {
                 if (dedup_t) {
-                    // one bulk copy per column (columns past T_s+W-2 of a packed draft are skipped)
-                    const int ncols = full_row ? Q : (Ts > 0 ? Ts + R - 1 : 0);
+                    // one bulk copy per column
+                    const int ncols = full_row ? Q : cnt;
                     S *const colb = reinterpret_cast<S *>(p.win) + (long long)s * p.w_seq + c0;
-                    for (int q = 0; q < ncols; ++q)
-                        bulk_store(colb + (long long)q * p.w_col, img + (long long)q * BC * ESS, (unsigned)(nch * ESS));
+                    for (int q2 = 0; q2 < ncols; ++q2)
+                        bulk_store(colb + (long long)(qd + q2) * p.w_col, img + (long long)(qs + q2) * BC * ESS,
+                                   (unsigned)(nch * ESS));
                 } else if (!dense && full_row) {
                     bulk_store(row_dst, img, (unsigned)(nch * Q * ESS));
                 }
-                if (!hist && !wide)
+                if (!hist && !wide && first)
                     bulk_store(reinterpret_cast<S *>(p.state) + (long long)slot * p.st_slot + (long long)c0 * R, stimg,
                                (unsigned)(nch * R * ESS));
                 asm volatile("cp.async.bulk.commit_group;\n" ::: "memory");
@@ -538,26 +550,36 @@ __global__ void __launch_bounds__(128, (CPT == 4 && TS <= 8) ? 4 : 2) verify_pip
                 load_index(k + 3, pf);
             }
         }
-        if (VL && go && !recomp && !dense && !dedup_t && !full_row && Ts > 0) {
-            // word w of the staged image holds elements 2w, 2w+1 (bf16) or w (fp32) of the block's
-            // [nch][Q] run; an element in column q >= T_s+W-2 is skipped
-            const int ncols = Ts + R - 1;
-            const unsigned *iw = reinterpret_cast<const unsigned *>(img);
-            unsigned *dw = reinterpret_cast<unsigned *>(row_dst);
-            const int nwords = nch * Q * ESS / 4;
-            for (int w = tid; w < nwords; w += (int)blockDim.x) {
-                const unsigned v = iw[w];
-                if (ESS == 4) {
-                    if (w % Q < ncols) dw[w] = v;
-                } else {
-                    const bool lo = (2 * w) % Q < ncols, hi = (2 * w + 1) % Q < ncols;
-                    if (lo && hi) {
-                        dw[w] = v;
-                    } else if (lo) {
-                        reinterpret_cast<unsigned short *>(dw)[2 * w] = (unsigned short)(v & 0xffffu);
-                    } else if (hi) {
-                        reinterpret_cast<unsigned short *>(dw)[2 * w + 1] = (unsigned short)(v >> 16);
+        if (VL && go && !recomp && !dense && !dedup_t && !full_row && cnt > 0) {
+            if (!chunked) {
+                // one chunk, columns [0, T_s+W-2): word w of the staged image holds elements 2w,
+                // 2w+1 (bf16) or w (fp32) of the block's [nch][Q] run, Q = the row's width
+                const unsigned *iw = reinterpret_cast<const unsigned *>(img);
+                unsigned *dw = reinterpret_cast<unsigned *>(row_dst);
+                const int nwords = nch * Q * ESS / 4;
+                for (int w = tid; w < nwords; w += (int)blockDim.x) {
+                    const unsigned v = iw[w];
+                    if (ESS == 4) {
+                        if (w % Q < cnt) dw[w] = v;
+                    } else {
+                        const bool lo = (2 * w) % Q < cnt, hi = (2 * w + 1) % Q < cnt;
+                        if (lo && hi) {
+                            dw[w] = v;
+                        } else if (lo) {
+                            reinterpret_cast<unsigned short *>(dw)[2 * w] = (unsigned short)(v & 0xffffu);
+                        } else if (hi) {
+                            reinterpret_cast<unsigned short *>(dw)[2 * w + 1] = (unsigned short)(v >> 16);
+                        }
                     }
+                }
+            } else {
+                // a chunk of a longer draft: element by element, channel-major
+                using U = std::conditional_t<ESS == 2, unsigned short, unsigned>;
+                const U *ie = reinterpret_cast<const U *>(img);
+                U *de = reinterpret_cast<U *>(row_dst);
+                for (int i = tid; i < nch * cnt; i += (int)blockDim.x) {
+                    const int cc = i / cnt, q2 = i - cc * cnt;
+                    de[(long long)cc * Qrow + qd + q2] = ie[cc * Q + qs + q2];
                 }
             }
         }
@@ -617,10 +639,10 @@ __global__ void __launch_bounds__(128, (CPT == 4 && TS <= 8) ? 4 : 2) verify_pip
                 }
             }
             if (act) {
-                B *os = reinterpret_cast<B *>(p.out) + (VL ? row0 * p.out_tok : (long long)s * p.out_seq) + c;
+                B *os = reinterpret_cast<B *>(p.out) + (VL ? (row0 + t0) * p.out_tok : (long long)s * p.out_seq) + c;
 #pragma unroll
                 for (int t = 0; t < TS; ++t) {
-                    if (VL && t >= Ts) break;
+                    if (VL && t >= nt) break;
                     uint32_t ow[NW];
                     if (ES == 2) {
 #pragma unroll

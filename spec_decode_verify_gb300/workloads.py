@@ -262,6 +262,7 @@ class RaggedWorkload:
     state_offset: bool = False  # read the committed window at a per-sequence offset in 0..T-1
     x_row_stride: Optional[int] = None
     extra_rows: int = 0  # rows of x / out past the last span (never touched)
+    window_transposed: bool = False  # dedup rows stored column by column ([n_seq, T+W-2, dim])
     seed: int = 0
 
     @property
@@ -336,6 +337,8 @@ def make_ragged_inputs(w: RaggedWorkload, seed: Optional[int] = None) -> dict:
     window = None
     if w.layout == "dense":
         window = sentinel_tensor((w.n_seq, w.T, w.dim, w.width - 1), dt)
+    elif w.layout == "dedup" and w.window_transposed:
+        window = sentinel_tensor((w.n_seq, w.T + w.width - 2, w.dim), dt).transpose(1, 2)
     elif w.layout == "dedup":
         window = sentinel_tensor((w.n_seq, w.dim, w.T + w.width - 2), dt)
     return dict(x=x, x_base=x_wide, cu_draft=torch.from_numpy(cu), conv_state=state, weight=weight, bias=bias,

@@ -69,10 +69,13 @@ W3 = wl.WORKLOADS["n128_t8_dim10240_w4_bf16_dedup_pad13"]
 
 def _pipe_smem(stage, image, n_seq, varlen_T=None):
     """The pipelined kernel's shared memory: two stages, two image buffers, 48 bytes of barriers and
-    unit information (slots, offsets, draft counts, first rows), then the compaction scratch (4
-    ints; 5 * (T + 2) for packed drafts) and 4 * n_seq bytes for the list of active sequences."""
-    aux = 4 if varlen_T is None else 5 * (varlen_T + 2)
-    return 2 * stage + 2 * image + 48 + 4 * aux + 4 * n_seq
+    unit information (slots, offsets, draft counts, first rows), then the listing scratch (4 warp
+    counts; for packed drafts 5 * (TS + 2) sort counts, TS = min(T, 8) tokens per unit) and 4 bytes
+    per list entry (a sequence; for packed drafts a chunk of TS tokens of one)."""
+    if varlen_T is None:
+        return 2 * stage + 2 * image + 48 + 4 * 4 + 4 * n_seq
+    ts = min(varlen_T, 8)
+    return 2 * stage + 2 * image + 48 + 4 * 5 * (ts + 2) + 4 * n_seq * ((varlen_T + ts - 1) // ts)
 
 
 def test_plan_for_benchmark_workload(lib):
@@ -509,18 +512,25 @@ def _ragged_args(w, **over):
 
 
 def test_plan_packed_drafts_pipelined(lib):
-    """Packed ragged drafts at the benchmark shape take the pipelined kernel, whose shared memory
-    holds the sort scratch of 5 * (T + 2) ints and the list of sequences."""
+    """Packed ragged drafts of up to 16 tokens at the benchmark shape take the pipelined kernel in
+    units of 8-token chunks: stages of 8 + 3 x rows (the chunk, then its halo or the draft's tail)
+    and the committed windows, images of 8 + 2 columns, the sort scratch and a list of 2 chunks per
+    sequence."""
     a = _ragged_args(RAG)
     rc, pl = _plan(lib, a)
     assert rc == 0 and pl.path == 3
-    R, Q, bc = RAG.width - 1, RAG.T + RAG.width - 2, 512
+    R, bc = RAG.width - 1, 512
+    Q = 8 + R - 1
 
     def part(b):
         return (b + 127) // 128 * 128
-    stage = part(RAG.T * bc * 2) + part(R * bc * 2)
+    stage = part((8 + R) * bc * 2) + part(R * bc * 2)
     image = part(Q * bc * 2) + part(R * bc * 2)
     assert pl.smem_bytes == _pipe_smem(stage, image, RAG.n_seq, varlen_T=RAG.T)
+    # longer drafts (T = 40: 5 chunks per sequence) still fit the list; history rows do not chunk
+    assert _plan(lib, _ragged_args(RAG.replace(T=40)))[1].path == 3
+    assert _plan(lib, _ragged_args(RAG.replace(layout="history", T=8)))[1].path == 3
+    assert _plan(lib, _ragged_args(RAG.replace(layout="history", T=16)))[1].path == 0
 
 
 def test_packed_drafts_argument_checks(lib):

@@ -1,14 +1,16 @@
-"""The bounded-wait failure path of the pipelined verify, on the GPU, without a fault: the limit of each unit's first wait for its bulk copies is set so low that the wait runs out
+"""The bounded-wait failure path of the pipelined verify and the dedup commit, on the GPU, without a
+fault: the limit of each unit's first wait for its bulk copies is set so low that the wait runs out
 on an ordinary copy (wait_polls < 0: no poll at all; 1: a single poll).  The call must return, flag
 CV_SEQ_TIMEOUT on every sequence it did not finish, leave every other sequence exactly as the oracle
 computes it, and leave the context usable: the next call with the default limit is exact."""
 from __future__ import annotations
 
+import numpy as np
 import pytest
 import torch
 
 from gpu_helpers import to_device
-from helpers import assert_bits_equal, assert_out_close, run_oracle_verify
+from helpers import assert_bits_equal, assert_out_close, bits, run_oracle_commit, run_oracle_verify
 from spec_decode_verify_gb300 import workloads as wl
 
 pytestmark = pytest.mark.gpu
@@ -92,3 +94,28 @@ def test_verify_short_wait_others_exact(cuda_lib, polls):
     ref = run_oracle_verify(W3, inp)
     got = gpu_verify(cuda_lib, W3, inp, wait_polls=polls)
     check_unflagged(W3, inp, ref, got)
+
+
+def test_commit_wait_gives_up_at_once(cuda_lib):
+    """The dedup commit with no poll: every active sequence is flagged and its state keeps the
+    verify's committed window; the default limit then commits exactly."""
+    w = W3
+    inp = wl.make_inputs(w)
+    ref = run_oracle_verify(w, inp)
+    got = gpu_verify(cuda_lib, w, inp, wait_polls=0)
+    before = got["conv_state"].clone()
+    e = torch.full((w.n_seq,), -7, dtype=torch.int32, device="cuda")
+    cuda_lib.conv_commit(got["conv_state"], got["window"], got["accept_len"], layout=w.layout, T=w.T, width=w.width,
+                         cache_idx=got["cache_idx"], err=e, wait_polls=-1)
+    torch.cuda.synchronize()
+    cache = inp["cache_idx"].numpy()
+    want = np.where(cache >= 0, 8, 0).astype(np.uint32)
+    assert np.array_equal(bits(e.cpu()), want)
+    assert_bits_equal(got["conv_state"].cpu(), before.cpu(), "state after a commit that gave up")
+    st_ref = run_oracle_commit(w, ref)
+    e2 = torch.full((w.n_seq,), -7, dtype=torch.int32, device="cuda")
+    cuda_lib.conv_commit(got["conv_state"], got["window"], got["accept_len"], layout=w.layout, T=w.T, width=w.width,
+                         cache_idx=got["cache_idx"], err=e2)
+    torch.cuda.synchronize()
+    assert_bits_equal(e2.cpu(), st_ref, "commit err")
+    assert_bits_equal(got["conv_state"].cpu(), ref["conv_state"], "committed state")

@@ -35,8 +35,12 @@ def oracle_commit(w, r, accept=None):
 
 
 def to_dev(inp, x_shift=0):
-    """Copy to the GPU; x_shift > 0 places x that many elements past a 16-byte boundary."""
+    """Copy to the GPU (a transposed window keeps its strides); x_shift > 0 places x that many
+    elements past a 16-byte boundary."""
     d = {k: (v.to("cuda") if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    if inp.get("window") is not None and not inp["window"].is_contiguous():
+        w = inp["window"]
+        d["window"] = torch.empty_strided(w.shape, w.stride(), dtype=w.dtype, device="cuda").copy_(w)
     xb = inp["x_base"]
     if x_shift:
         flat = torch.zeros(xb.numel() + x_shift, dtype=xb.dtype, device="cuda")
@@ -162,3 +166,20 @@ def test_ragged_bad_spans_on_gpu(cuda_lib):
     inp["cu_draft"][2] = 1
     inp["accept_len"] = torch.tensor([3, 1, 1, 1, 1], dtype=torch.int32)
     check(cuda_lib, w, inp)
+
+
+@pytest.mark.parametrize("layout", ["dense", "dedup", "dedupT", "recompute"])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("T", [24, 40])
+def test_ragged_chunked_on_pipelined_kernel(cuda_lib, layout, dtype, T):
+    """Drafts longer than 8 tokens run on the pipelined kernel in 8-token chunks (each later chunk
+    reads its first inputs from the x rows before it, chunk 0 writes the committed window from the
+    draft's last rows): every layout, both dtypes, draft counts 0..T including exact multiples of
+    8, padded sequences, state offsets, against the oracle."""
+    rng = np.random.default_rng(23000 + T)
+    lengths = tuple(int(v) for v in rng.integers(0, T + 1, size=30)) + (0, 1, 8, 16, T)
+    w = wl.RaggedWorkload(f"chunks{T}", lengths=lengths, T=T, dim=1024, width=4, qk_channels=512, head_dim=128,
+                          dtype=dtype, layout="dedup" if layout == "dedupT" else layout, bias=True,
+                          pad=(2, 11), extra_slots=3, state_offset=layout != "recompute", extra_rows=2,
+                          window_transposed=layout == "dedupT", seed=T)
+    check(cuda_lib, w, wl.make_ragged_inputs(w), path=3)
