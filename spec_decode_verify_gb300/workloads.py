@@ -375,6 +375,12 @@ RAGGED_WORKLOADS = {
                        T=16, dim=10240, width=4, qk_channels=4096, head_dim=128, dtype="bf16", layout="dedup",
                        pad=tuple(int(i) for i in np.random.default_rng(32).permutation(128)[:13]), extra_slots=16,
                        seed=31),
+        # the same drafts with the rows stored column by column (MambaPool's axis-0 layout): every
+        # chunk's columns are whole contiguous runs
+        RaggedWorkload("ragged_n128_t1to16_dim10240_w4_bf16_dedupT_pad13", lengths=ragged_lengths(31, 128, 1, 16),
+                       T=16, dim=10240, width=4, qk_channels=4096, head_dim=128, dtype="bf16", layout="dedup",
+                       pad=tuple(int(i) for i in np.random.default_rng(32).permutation(128)[:13]), extra_slots=16,
+                       window_transposed=True, seed=31),
     ]
 }
 RAGGED_ORDER = list(RAGGED_WORKLOADS)
