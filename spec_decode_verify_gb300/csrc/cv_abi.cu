@@ -82,31 +82,20 @@ DeviceLimits device_limits() {
     return d;
 }
 
-// The pipelined kernel cuts drafts into chunks of at most 8 tokens -- units of (sequence, chunk,
-// channel block) with the registers of an 8-token unit -- for packed ragged drafts, and for a
-// uniform batch of more than 8 tokens (one dtype, no history rows: a chunk of a history row could
-// overwrite the columns another block's chunk 0 reads).
+// Tokens per unit of the pipelined kernel for packed drafts: the whole draft when T <= 8, else
+// chunks of 8 (so any T runs with the registers of an 8-token unit); T otherwise.
 constexpr int kVarlenChunk = 8;
-bool state_mixed(const cv_verify_args *a) {
-    return a->state_dtype != CV_STATE_SAME && a->state_dtype - 1 != a->dtype;
-}
-bool chunks_uniform(const cv_verify_args *a) {
-    return !a->cu_draft && !a->parent && !state_mixed(a) && a->T > kVarlenChunk &&
-           a->window_layout != CV_WINDOW_HISTORY;
-}
-bool chunked_kernel(const cv_verify_args *a) { return a->cu_draft != nullptr || chunks_uniform(a); }
-// tokens per unit of the pipelined kernel
 int pipe_tokens(const cv_verify_args *a) {
-    return chunked_kernel(a) && a->T > kVarlenChunk ? kVarlenChunk : a->T;
+    return a->cu_draft && a->T > kVarlenChunk ? kVarlenChunk : a->T;
 }
 // entries of the pipelined kernel's work list: sequences, or (packed drafts) chunks of them
 long long pipe_list_len(const cv_verify_args *a) {
     const int ts = pipe_tokens(a);
     return (long long)a->n_seq * ((a->T + ts - 1) / ts);
 }
-// the list of active sequences (padded ones dropped; chunks ordered by size)
+// the list of active sequences (padded ones dropped; packed drafts as chunks ordered by size)
 bool pipe_compacts(const cv_verify_args *a) {
-    return (a->cache_idx != nullptr || chunked_kernel(a)) && pipe_list_len(a) <= kCompactMaxEntries;
+    return (a->cache_idx != nullptr || a->cu_draft != nullptr) && pipe_list_len(a) <= kCompactMaxEntries;
 }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -292,9 +281,9 @@ int plan_verify(const cv_verify_args *a, cv_launch_plan *pl) {
     // needs rows of exactly T+W-2 columns
     const bool rows_packed = aligned16(a->conv_state) && stride16(a->state_slot_stride, ssize) &&
                              a->state_ch_stride == a->state_cols;
-    const bool varlen = chunked_kernel(a);     // the chunk kernel (packed drafts, or T > 8 uniform)
+    const bool varlen = a->cu_draft != nullptr;
     const int ts = pipe_tokens(a);             // tokens per unit
-    const bool chunked = varlen && a->T > ts;  // drafts cut into several chunks
+    const bool chunked = varlen && a->T > ts;  // packed drafts cut into chunks
     const bool dedup_t = dedup_transposed_ok(a, ssize, ks.max_static_t);
     // (mixed dtypes: compiled for T <= kMaxMixedT; packed drafts: one dtype, and the chunks of a
     // longer draft need the work list and no history rows)
@@ -488,7 +477,7 @@ int launch_verify(const cv_verify_args *a, const cv_launch_plan &pl, cudaStream_
                           : pl.path == 1 ? ks.fast[ci][a->T]
                           : pl.path == 2 ? ks.fast[ci][0]
                           : pl.path == 3 ? (mixed ? ks.pipe_mixed[ci][a->T]
-                                            : chunked_kernel(a) ? varlen_set(a->dtype, a->width).pipe[ci][pipe_tokens(a)]
+                                            : a->cu_draft ? varlen_set(a->dtype, a->width).pipe[ci][pipe_tokens(a)]
                                                           : ks.pipe[ci][a->T])
                                          : ks.tree;
     if (ensure_smem(reinterpret_cast<const void *>(k), pl.smem_bytes) != cudaSuccess) return CV_ERR_LAUNCH;

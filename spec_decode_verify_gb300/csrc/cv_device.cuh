@@ -116,11 +116,10 @@ __device__ __forceinline__ int draft_span(const int *cu, int s, int T, int total
     return span_status(b, e, T, total);
 }
 
-// The work list of a persistent verify kernel over chunks of drafts -- packed ragged drafts, or a
-// uniform batch of T tokens each cut into chunks -- built identically by every block (block-wide:
-// every thread of a block of at most 4 warps calls it).  A sequence with a cache slot >= 0
-// contributes one entry per chunk of at most TS of its T_s draft tokens (one entry when T_s = 0 or
-// its span is bad), encoded (chunk << 16) | sequence.  Entries are ordered by the number
+// The work list of a persistent verify kernel over packed ragged drafts, built identically by every
+// block (block-wide: every thread of a block of at most 4 warps calls it).  A sequence with a cache
+// slot >= 0 contributes one entry per chunk of at most TS of its T_s draft tokens (one entry when
+// T_s = 0 or its span is bad), encoded (chunk << 16) | sequence.  Entries are ordered by the number
 // of tokens they hold, most first, so that units of similar cost come together in the round-robin
 // walk; ties are ordered by chunk, then sequence.  A stable counting sort: a shared-memory
 // histogram of the keys (TS - tokens), its prefix sums, then each entry's place from its key's
@@ -137,8 +136,8 @@ __device__ __forceinline__ int list_chunks(const VerifyParams &p, int *scratch, 
     // the key of sequence i's chunk c, or -1 when it has none
     auto key_of = [&](int i, int c) -> int {
         if (i >= p.n_seq || (p.cache_idx && __ldg(p.cache_idx + i) < 0)) return -1;
-        int ts = p.T, r0;  // (a uniform batch: T tokens each)
-        if (p.cu_draft && draft_span(p.cu_draft, i, p.T, p.total_tokens, ts, r0)) return c == 0 ? TS : -1;
+        int ts, r0;
+        if (draft_span(p.cu_draft, i, p.T, p.total_tokens, ts, r0)) return c == 0 ? TS : -1;
         if (c > 0 && c * TS >= ts) return -1;
         return TS - min(TS, ts - c * TS);
     };

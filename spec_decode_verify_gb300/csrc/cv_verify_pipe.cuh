@@ -103,10 +103,7 @@ __global__ void __launch_bounds__(128, (CPT == 4 && TS <= 8) ? 4 : 2) verify_pip
     const bool whole_rows = SC != R;
     const bool wide = whole_rows && !hist;  // wider rows, not history: the window is stored directly
 
-    // VL: units are chunks of at most TS tokens -- of packed ragged drafts (p.cu_draft), or of a
-    // uniform batch of T tokens each (sequence and token strides, as without VL)
-    const bool packed = VL && p.cu_draft != nullptr;
-    // drafts longer than a chunk: W-1 more staged x rows per unit (a halo or a tail)
+    // packed drafts longer than a chunk: W-1 more staged x rows per unit (a halo or a tail)
     const bool chunked = VL && p.T > TS;
     const int XR = TS + (chunked ? R : 0);
     const int Qrow = p.T + R - 1;  // columns of the snapshot row in global memory (Q: of the staged image)
@@ -193,42 +190,34 @@ __global__ void __launch_bounds__(128, (CPT == 4 && TS <= 8) ? 4 : 2) verify_pip
         const int s = seq_at(((int)blockIdx.x + k * (int)gridDim.x) / nblk) & 0xffff;
         ix.slot = p.cache_idx ? __ldg(p.cache_idx + s) : s;
         ix.off = p.state_off ? __ldg(p.state_off + s) : 0;
-        if (packed) {
+        if constexpr (VL) {
             ix.b = __ldg(p.cu_draft + s);
             ix.e = __ldg(p.cu_draft + s + 1);
-        } else if (VL) {
-            ix.b = 0;  // (a uniform batch: T tokens at the sequence's rows)
-            ix.e = p.T;
         } else {
             ix.b = s;  // (the rows of sequence s start at s * x_seq)
             ix.e = s + TS;
         }
     };
-    // x row t of sequence s whose packed rows start at row b: the unit's channel block
-    auto x_row = [&](int s, int b, int t, int c0) -> const B * {
-        return reinterpret_cast<const B *>(p.x) +
-               (packed ? (long long)(b + t) * p.x_tok : (long long)s * p.x_seq + (long long)t * p.x_tok) + c0;
-    };
-    // the unit's x rows: n rows from token t (the chunk's rows; the TS rows of the sequence without
-    // VL), into stage rows 0 .. n-1
-    auto issue_x = [&](int k, int b, int t, int n) {
+    // the unit's x rows: n rows from row b (packed drafts: the chunk's rows), or the TS rows of
+    // sequence s, into stage rows 0 .. n-1
+    auto issue_x = [&](int k, int b, int n) {
         const int st = k & 1;
         int s, c0, nch;
         unit_of(k, s, c0, nch);
         mbar_expect_tx(&bar[st], (unsigned)(n * nch * ES));
-        const B *xs = x_row(s, b, t, c0);
-        for (int u = 0; u < n; ++u)
-            bulk_load(smem + st * stage_bytes + (long long)u * BC * ES, xs + (long long)u * p.x_tok,
+        const B *xs = reinterpret_cast<const B *>(p.x) + (VL ? (long long)b * p.x_tok : (long long)s * p.x_seq) + c0;
+        for (int t = 0; t < n; ++t)
+            bulk_load(smem + st * stage_bytes + (long long)t * BC * ES, xs + (long long)t * p.x_tok,
                       (unsigned)(nch * ES), &bar[st]);
     };
-    // (chunks) W-1 x rows from token t into stage rows TS .. TS+W-2: a later chunk's halo, or chunk
-    // 0's tail (the draft's last W-1 rows, which hold the committed window)
-    auto issue_extra = [&](int k, int b, int t) {
+    // (packed drafts) W-1 x rows from row b into stage rows TS .. TS+W-2: a later chunk's halo, or
+    // chunk 0's tail (the draft's last W-1 rows, which hold the committed window)
+    auto issue_extra = [&](int k, int b) {
         const int st = k & 1;
         int s, c0, nch;
         unit_of(k, s, c0, nch);
         mbar_expect_tx(&bar[st], (unsigned)(R * nch * ES));
-        const B *xs = x_row(s, b, t, c0);
+        const B *xs = reinterpret_cast<const B *>(p.x) + (long long)b * p.x_tok + c0;
         for (int j = 0; j < R; ++j)
             bulk_load(smem + st * stage_bytes + (long long)(TS + j) * BC * ES, xs + (long long)j * p.x_tok,
                       (unsigned)(nch * ES), &bar[st]);
@@ -244,7 +233,7 @@ __global__ void __launch_bounds__(128, (CPT == 4 && TS <= 8) ? 4 : 2) verify_pip
         const int ch = chunk_of(k);
         if constexpr (VL) {  // (the span was loaded with the indices, one issue ahead)
             ts = ix.e - ix.b;
-            if (slot >= 0 && packed) status |= span_status(ix.b, ix.e, p.T, p.total_tokens);
+            if (slot >= 0) status |= span_status(ix.b, ix.e, p.T, p.total_tokens);
         }
         if (p.err && c0 == 0 && ch == 0 && status) atomicOr(p.err + s, status);
         const bool go = slot >= 0 && status == 0;
@@ -255,11 +244,11 @@ __global__ void __launch_bounds__(128, (CPT == 4 && TS <= 8) ? 4 : 2) verify_pip
         if (go) {
             const int t0 = ch * TS;
             const int n = VL ? min(TS, ts - t0) : TS;
-            if (!x_sent) issue_x(k, ix.b, t0, n);
+            if (!x_sent) issue_x(k, ix.b + t0, n);
             if (ch > 0) {
-                issue_extra(k, ix.b, t0 - R);  // the halo: the W-1 rows before the chunk
+                issue_extra(k, ix.b + t0 - R);  // the halo: the W-1 rows before the chunk
             } else {
-                if (chunked && ts > TS) issue_extra(k, ix.b, ts - R);  // the tail: the draft's last W-1 rows
+                if (chunked && ts > TS) issue_extra(k, ix.b + ts - R);  // the tail: the draft's last W-1 rows
                 // packed state rows of SC columns: the committed windows, or whole rows
                 mbar_expect_tx(&bar[st], (unsigned)(SC * nch * ESS));
                 bulk_load(smem + st * stage_bytes + xb,
@@ -277,8 +266,8 @@ __global__ void __launch_bounds__(128, (CPT == 4 && TS <= 8) ? 4 : 2) verify_pip
         load_index(0, i0);
         load_index(1, i1);
         if (!VL) {  // (x rows of a whole-T batch do not depend on the indices: send them first)
-            if (iters > 0) issue_x(0, 0, 0, TS);
-            if (iters > 1) issue_x(1, 0, 0, TS);
+            if (iters > 0) issue_x(0, 0, TS);
+            if (iters > 1) issue_x(1, 0, TS);
         }
         if (iters > 0) issue(0, i0, !VL);
         if (iters > 1) issue(1, i1, !VL);
@@ -650,8 +639,7 @@ __global__ void __launch_bounds__(128, (CPT == 4 && TS <= 8) ? 4 : 2) verify_pip
                 }
             }
             if (act) {
-                B *os = reinterpret_cast<B *>(p.out) + c +
-                        (packed ? (row0 + t0) * p.out_tok : (long long)s * p.out_seq + (long long)t0 * p.out_tok);
+                B *os = reinterpret_cast<B *>(p.out) + (VL ? (row0 + t0) * p.out_tok : (long long)s * p.out_seq) + c;
 #pragma unroll
                 for (int t = 0; t < TS; ++t) {
                     if (VL && t >= nt) break;

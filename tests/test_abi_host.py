@@ -186,12 +186,11 @@ def test_plan_sequence_list_only_with_cache_indices(lib):
 
 
 def test_plan_general_path_cases(lib):
-    """Odd dims and transposed rows with unaligned columns take the general kernel; transposed rows
-    with 16-byte-aligned columns take the pipelined one (a bulk copy per column), and so do drafts
-    longer than 8 tokens, in chunks of 8."""
+    """Odd dims, long dedup rows and transposed rows with unaligned columns take the general kernel;
+    transposed rows with 16-byte-aligned columns take the pipelined one (a bulk copy per column)."""
     assert _plan(lib, _args(W3.replace(dim=10236, qk_channels=4096)))[1].path == 0
-    assert _plan(lib, _args(W3.replace(T=18)))[1].path == 3
-    assert _plan(lib, _args(W3.replace(T=9, dtype="f32")))[1].path == 3
+    assert _plan(lib, _args(W3.replace(T=18)))[1].path == 0
+    assert _plan(lib, _args(W3.replace(T=9, dtype="f32")))[1].path == 0
     assert _plan(lib, _args(W3.replace(T=8, dtype="f32")))[1].path == 3
     pl = _plan(lib, _args(W3.replace(head_dim=256, qk_channels=4096)))[1]
     assert pl.path == 3 and pl.channels_per_block == 8 * pl.threads  # a 256-channel group needs 8 per thread
@@ -257,10 +256,10 @@ def test_zero_sequences_is_ok_without_gpu(lib):
 @pytest.mark.parametrize("T,dtype,threads", [(18, "bf16", 128), (32, "bf16", 128), (64, "f32", 32),
                                              (128, "f32", 32), (128, "bf16", 32)])
 def test_general_plan_fits_shared_memory(lib, T, dtype, threads):
-    """General kernel (x rows off 16-byte alignment keep the pipelined kernel out): the tile (T+W-1
-    rows of 8*threads channels plus 16 bytes) shrinks the block until it fits."""
+    """General kernel: the tile (T+W-1 rows of 8*threads channels plus 16 bytes) shrinks the block
+    until it fits."""
     w = W3.replace(T=T, dtype=dtype, n_seq=2, n_pad=0, extra_slots=0)
-    rc, pl = _plan(lib, _args(w, x_tok_stride=w.dim + 1))
+    rc, pl = _plan(lib, _args(w))
     esize = 2 if dtype == "bf16" else 4
     assert rc == 0 and pl.path == 0 and pl.threads == threads
     assert pl.smem_bytes == (T + 3) * (8 * threads * esize + 16)
