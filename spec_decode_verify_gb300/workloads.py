@@ -127,6 +127,12 @@ WORKLOADS = {
         VerifyWorkload("n128_t8_dim10240_w4_bf16_history_pad13", n_seq=128, T=8, dim=10240, width=4,
                        qk_channels=4096, head_dim=128, dtype="bf16", layout="history", n_pad=13,
                        extra_slots=16, state_offset=True, seed=5),
+        # the rows of the pages' kernel-time table (bs 128, T 8 and T 16, dim 10240, width 4, bf16,
+        # deduplicated rows), with no padded rows, as that table has none
+        VerifyWorkload("n128_t8_dim10240_w4_bf16_dedup_nopad", n_seq=128, T=8, dim=10240, width=4,
+                       qk_channels=4096, head_dim=128, dtype="bf16", layout="dedup", seed=10),
+        VerifyWorkload("n128_t16_dim10240_w4_bf16_dedup_nopad", n_seq=128, T=16, dim=10240, width=4,
+                       qk_channels=4096, head_dim=128, dtype="bf16", layout="dedup", seed=11),
         VerifyWorkload("n128_t8_dim10240_w4_bf16_dedupT_pad13", n_seq=128, T=8, dim=10240, width=4,
                        qk_channels=4096, head_dim=128, dtype="bf16", layout="dedup", n_pad=13,
                        extra_slots=16, window_transposed=True, seed=9),
