@@ -292,10 +292,14 @@ int plan_verify(const cv_verify_args *a, cv_launch_plan *pl) {
                    (hist ? a->state_cols == a->T + R - 1 : (recomp || fast || dedup_t)) &&
                    !(chunked && (hist || !pipe_compacts(a)));
     const bool wide = !hist && a->state_cols != R;
-    // (wide rows cost whole-row reads and element stores of the window; the pipeline pays that
-    // back only when every block walks at least two units, otherwise the one-pass kernel wins)
-    // (mixed dtypes have no one-pass kernel)
-    if (pipe_ok && wide && fast && !mixed && !varlen && units_per_pipe_block(a, cpt, lim.sms) < 2.0) pipe_ok = false;
+    // The pipeline pays for its prologue only when every block walks several units; with fewer the
+    // one-pass kernel wins (measured: 8 x 17 tokens x 8192 channels, 2 units per block, 6.8 us
+    // one-pass against 9.4 pipelined; 4 x 4 x 4096, 1 unit per block, 4.0 against 4.0 and a shorter
+    // step), from 3 units per block the pipeline does (the 128 x 8 x 10240 benchmark: 3.8).  Wide
+    // rows cost the one-pass kernel whole-row reads and element stores of the window, so for them
+    // the pipeline wins from 2 units per block.  (Mixed dtypes have no one-pass kernel.)
+    if (pipe_ok && fast && !mixed && !varlen && units_per_pipe_block(a, cpt, lim.sms) < (wide ? 2.0 : 3.0))
+        pipe_ok = false;
     if (pipe_ok) {
         auto part = [](long long b) { return (b + 127) / 128 * 128; };
         int threads = kPipeThreads;

@@ -131,8 +131,8 @@ def test_history_validation_and_paths(lib):
 
 
 @pytest.mark.parametrize("name,path", [
-    ("n1_t2_dim512_w4_f32_dense", 3), ("n4_t4_dim4096_w4_bf16_dedup_bias", 3),
-    ("n8_t17_dim8192_w4_bf16_dense_qkvsplit_xstride12288", 3), ("n64_t8_dim6144_w3_bf16_dense_nol2_stateoff", 1),
+    ("n1_t2_dim512_w4_f32_dense", 1), ("n4_t4_dim4096_w4_bf16_dedup_bias", 1),
+    ("n8_t17_dim8192_w4_bf16_dense_qkvsplit_xstride12288", 1), ("n64_t8_dim6144_w3_bf16_dense_nol2_stateoff", 1),
     ("n128_t8_dim10240_w4_bf16_history_pad13", 3), ("n128_t8_dim10240_w4_bf16_recompute_pad13", 3),
     ("n128_t8_dim10240_w4_bf16_tree_dense_pad13", 5), ("n128_t8_dim10240_w4_bf16x_f32state_dedup_pad13", 3)])
 def test_plan_paths_of_named_workloads(lib, name, path):

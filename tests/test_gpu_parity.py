@@ -271,8 +271,8 @@ def test_all_paths_bit_identical(cuda_lib, layout, dtype):
     wider, staged whole), the static-T kernel (rows with a gap between them, element stores) and
     the general kernel (x shifted off 16-byte alignment) give bit-identical outputs, snapshots and
     committed windows -- and match the oracle."""
-    # 420 sequences x 3 channel blocks: enough units per block for wide rows to be pipelined
-    w = wl.VerifyWorkload("paths", n_seq=420, T=6, dim=1536, width=4, qk_channels=512, head_dim=128, dtype=dtype,
+    # 640 sequences x 3 channel blocks: enough units per block (3.2) for the pipelined kernel
+    w = wl.VerifyWorkload("paths", n_seq=640, T=6, dim=1536, width=4, qk_channels=512, head_dim=128, dtype=dtype,
                           layout=layout, bias=True, n_pad=7, extra_slots=2, seed=31)
     inp = wl.make_inputs(w)
     ref = run_oracle_verify(w, inp)
