@@ -362,7 +362,7 @@ def test_wide_state_rows_pipelined(cuda_lib, layout, T, width):
     kernel when every block walks several units: it stages the rows whole and stores the committed
     window into their first W-1 columns directly; every offset 0..T-1 appears and the result equals
     the oracle's."""
-    w = wl.VerifyWorkload("wide", n_seq=140 + T, T=T, dim=4096 + 512, width=width, qk_channels=1024, head_dim=128,
+    w = wl.VerifyWorkload("wide", n_seq=300 + T, T=T, dim=4096 + 512, width=width, qk_channels=1024, head_dim=128,
                           dtype="bf16", layout=layout, bias=True, n_pad=1, extra_slots=3, state_offset=True,
                           seed=50 * T + width)
     inp = wl.make_inputs(w)
