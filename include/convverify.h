@@ -140,7 +140,9 @@ enum {
  *                    2 ulp in bf16, and are identical for every launch path and batch split)
  *     snapshot (s, t, c, k) = full[t+1+k], k < W-1      raw bit copy, dense or dedup layout
  * and finally conv_state[slot][c][0 .. W-2] = full[T .. T+W-2] (the committed window, equal to
- * snapshot T-1); state columns >= W-1 are not touched.  In the CV_WINDOW_HISTORY layout the
+ * snapshot T-1); state columns >= W-1 keep their values (packed rows wider than the window may be
+ * written back whole with those columns' own bits, so nothing else may write them during the
+ * call).  In the CV_WINDOW_HISTORY layout the
  * snapshots go into the state row instead (columns [0, T+W-2), see the layout) and no window
  * buffer is written; in the CV_WINDOW_RECOMPUTE layout neither snapshots nor the state are
  * written.  A sequence with slot < 0 is padding: its

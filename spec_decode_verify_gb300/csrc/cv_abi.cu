@@ -25,6 +25,7 @@ namespace {
 
 constexpr int kFastThreads = 128;
 constexpr int kPipeThreads = 128;
+constexpr long long kFastRowsMaxBytes = 64 * 1024;  // staged wide state rows of a one-pass block
 // blocks per SM the pipelined kernel's launch bounds provide registers for
 constexpr int pipe_blocks_per_sm(int cpt, int T) { return (cpt == 4 && T <= 8) ? 4 : 2; }
 constexpr int kSmemPerBlockReserved = 1024;
@@ -228,6 +229,15 @@ bool state_packed(const void *state, long long slot_stride, long long ch_stride,
     return aligned16(state) && stride16(slot_stride, esize) && ch_stride == width - 1;
 }
 
+// Packed state rows wider than the window (read at a state offset): [dim][state_cols] per slot,
+// 16-byte aligned.  The one-pass kernel then stages a block's rows whole in shared memory and
+// stores them back whole, when they take at most kFastRowsMaxBytes.
+bool fast_rows_staged(const cv_verify_args *a, int ssize, long long bc) {
+    return !state_packed(a->conv_state, a->state_slot_stride, a->state_ch_stride, a->width, ssize) &&
+           aligned16(a->conv_state) && stride16(a->state_slot_stride, ssize) && a->state_ch_stride == a->state_cols &&
+           bc * a->state_cols * ssize <= kFastRowsMaxBytes;
+}
+
 // Validates verify arguments; on success fills the launch plan.
 // dtype of conv_state and the snapshots
 int state_dtype_of(const cv_verify_args *a) { return a->state_dtype == CV_STATE_SAME ? a->dtype : a->state_dtype - 1; }
@@ -314,7 +324,7 @@ int plan_verify(const cv_verify_args *a, cv_launch_plan *pl) {
         // the state's dtype; 2 mbarriers, 2 slots, 2 offsets
         const long long stage = part((long long)(ts + (chunked ? R : 0)) * bc * esize) +
                                 part((long long)a->state_cols * bc * ssize);
-        long long image = (hist || recomp || wide) ? 0 : part(R * bc * ssize);
+        long long image = (hist || recomp) ? 0 : part((wide ? a->state_cols : R) * bc * ssize);
         if (a->window_layout == CV_WINDOW_DEDUP || hist) image += part(Q * bc * ssize);
         const long long smem = 2 * stage + 2 * image + cvk::kPipeInfoBytes +
                                (pipe_compacts(a) ? 4LL * cvk::pipe_aux_ints(varlen, ts) + 4LL * pipe_list_len(a) : 0);
@@ -345,7 +355,8 @@ int plan_verify(const cv_verify_args *a, cv_launch_plan *pl) {
         while (a->qk_channels > 0 && cpt * threads < a->head_dim) threads *= 2;
         threads = shrink_for_parallelism(threads, cpt, a, lim.sms);
         const long long bc = (long long)cpt * threads;
-        long long smem = bc * R * esize;  // committed-window image
+        // committed-window image, or the staged wide rows
+        long long smem = bc * (fast_rows_staged(a, ssize, bc) ? a->state_cols : R) * esize;
         if (a->window_layout == CV_WINDOW_DEDUP) smem += bc * (a->T + R - 1) * esize;
         pl->threads = threads;
         pl->channels_per_block = (int)bc;
@@ -463,6 +474,7 @@ int launch_verify(const cv_verify_args *a, const cv_launch_plan &pl, cudaStream_
     p.x_vec = aligned16(a->x) && (vl || stride16(a->x_seq_stride, esize)) && stride16(a->x_tok_stride, esize);
     p.out_vec = aligned16(a->out) && (vl || stride16(a->out_seq_stride, esize)) && stride16(a->out_tok_stride, esize);
     p.st_vec = state_packed(a->conv_state, a->state_slot_stride, a->state_ch_stride, a->width, ssize);
+    p.st_rows = (pl.path == 1 || pl.path == 2) && fast_rows_staged(a, ssize, pl.channels_per_block);
     p.w_vec = aligned16(a->weight);
     p.b_vec = a->bias ? aligned16(a->bias) : 0;
     if (pl.path == 5) {

@@ -34,6 +34,8 @@ struct VerifyParams {
     const int *parent;  // tree verify: [n_seq][T] parent of each draft token, or null (a chain)
     int x_vec, out_vec, st_vec, w_vec, b_vec;  // 16-byte vector access allowed (checked on the host)
     int st_packed;  // tree verify: the committed windows are packed, 16-byte-aligned [dim][W-1] rows
+    int st_rows;    // one-pass verify: packed state rows wider than the window, staged whole (16-byte
+                    // aligned [dim][state_cols] runs per slot)
     int wait_polls;  // polls of the first bounded wait per unit: 0 = the default, < 0 = none (gives up at once)
     const int *cu_draft;  // packed ragged drafts: [n_seq + 1] row offsets into x and out, or null
     int total_tokens;     // rows of x and out when cu_draft is given

@@ -15,7 +15,11 @@
 //          instead of W-1 scattered stores per token;
 //        - dense snapshots: the thread's CPT x (W-1) run per token as vector stores;
 //        - committed window (= snapshot T-1) -> state columns [0, W-1), staged and bulk-copied
-//          when the state rows are packed;
+//          when the state rows are packed.  Rows wider than the window (read at a state offset),
+//          when packed, are staged whole in shared memory (cp.async, 16-byte pieces) at the start
+//          and leave whole by one bulk copy with the window in their first W-1 columns (the other
+//          columns go back with their own bits): one contiguous run per block instead of 2-byte
+//          loads and stores at the row pitch;
 //   3. conv (fp32, bias first, taps in order, see conv_chain), SiLU, and for
 //      q|k channels the L2 normalisation over the head_dim group as an xor-shuffle over
 //      head_dim/CPT lanes (glm5next_kda mod.rs: SiLU after the conv, then L2 on q and k alone,
@@ -66,6 +70,21 @@ __global__ void __launch_bounds__(256) verify_fast(const __grid_constant__ Verif
     const int c = c0 + cl;
     const int T = TS > 0 ? TS : p.T;
     const bool dense = !p.dedup;
+    // shared memory: [dedup image: BC x (TS+W-2)] then the state part: the committed-window image
+    // (BC x (W-1)) or, for staged wide rows, the rows themselves (BC x state_cols)
+    const bool rows = p.st_rows;  // block-uniform
+    const int SC = p.state_cols;
+    const long long img_bytes = (TS > 0 && !dense) ? (long long)BC * (TS + R - 1) * ES : 0;
+    if (img_bytes + (long long)BC * (rows ? SC : R) * ES > (long long)dynamic_smem_bytes()) return;  // launch mismatch
+    unsigned char *st_img = smem + img_bytes;
+    B *const st_blk = reinterpret_cast<B *>(p.state) + (long long)slot * p.st_slot + (long long)c0 * SC;
+    if (rows) {
+        // the block's [nch][SC] rows: contiguous, 16-byte aligned, a multiple of 16 bytes (host-checked)
+        const int nbytes = nch * SC * ES;
+        for (int o = tid * 16; o < nbytes; o += (int)blockDim.x * 16)
+            cp_async16(st_img + o, reinterpret_cast<const unsigned char *>(st_blk) + o);
+        asm volatile("cp.async.commit_group;\n" ::: "memory");
+    }
 
     // ---- 1. loads.  fw[e][j] = input j of channel e widened to fp32 (j < R: committed window).
     float fw[CPT][R + TC];
@@ -76,7 +95,7 @@ __global__ void __launch_bounds__(256) verify_fast(const __grid_constant__ Verif
     for (int e = 0; e < CPT; ++e)
 #pragma unroll
         for (int k = 0; k < R; ++k) fw[e][k] = 0.0f;
-    if (act) {
+    if (act && !rows) {
         if (p.st_vec) {  // packed [dim][R] rows (then the offset is 0)
             uint32_t sw[R * NW];
             ldv<VS, R * NW>(sw, st_row);
@@ -122,6 +141,17 @@ __global__ void __launch_bounds__(256) verify_fast(const __grid_constant__ Verif
             ldv<VX, NW>(bw, reinterpret_cast<const B *>(p.bias) + c);
 #pragma unroll
             for (int e = 0; e < CPT; ++e) bs[e] = elem_f<B>(bw, e);
+        }
+    }
+    const B *const srow_img = reinterpret_cast<const B *>(st_img) + (size_t)cl * SC;  // staged rows
+    if (rows) {
+        cp_async_wait_all();
+        __syncthreads();
+        if (act) {
+#pragma unroll
+            for (int e = 0; e < CPT; ++e)
+#pragma unroll
+                for (int k = 0; k < R; ++k) fw[e][k] = widen<B>(srow_img[e * SC + off + k]);
         }
     }
 
@@ -203,9 +233,16 @@ __global__ void __launch_bounds__(256) verify_fast(const __grid_constant__ Verif
         }
         stv<VX, NW>(os + (long long)t * p.out_tok, ow);
     };
-    auto stage_state = [&](unsigned char *st_img, const uint32_t *fin) {
+    auto stage_state = [&](const uint32_t *fin) {
         if (p.st_vec) {
             stv<VS, R * NW>(st_img + (size_t)tid * CPT * R * ES, fin);
+        } else if (rows) {
+            // into the staged rows, in place: this thread's own channels, read above
+            B *const rr = reinterpret_cast<B *>(st_img) + (size_t)cl * SC;
+#pragma unroll
+            for (int e = 0; e < CPT; ++e)
+#pragma unroll
+                for (int k = 0; k < R; ++k) rr[e * SC + k] = (B)elem_raw<B>(fin, e * R + k);
         } else {
 #pragma unroll
             for (int e = 0; e < CPT; ++e)
@@ -217,10 +254,8 @@ __global__ void __launch_bounds__(256) verify_fast(const __grid_constant__ Verif
     bool bulk = false;
     if constexpr (TS > 0) {
         constexpr int Q = TS + R - 1;  // dedup row columns
-        if ((long long)BC * ((dense ? 0 : Q) + R) * ES > (long long)dynamic_smem_bytes()) return;  // launch mismatch
         constexpr int VI = chunk_align(CPT * Q * ES);
         // ---- 2. input-only outputs
-        unsigned char *st_img = dense ? smem : smem + (size_t)BC * Q * ES;
         if (act) {
             if (!dense) {
                 uint32_t img[Q * NW];  // the thread's CPT x Q image, channel-major
@@ -241,17 +276,15 @@ __global__ void __launch_bounds__(256) verify_fast(const __grid_constant__ Verif
             }
             uint32_t fin[R * NW];
             window_words(TS, fin);
-            stage_state(st_img, fin);
+            stage_state(fin);
         }
-        bulk = !dense || p.st_vec;
+        bulk = !dense || p.st_vec || rows;
         if (bulk) {
             fence_smem_to_async();
             __syncthreads();
             if (tid == 0) {
                 if (!dense) bulk_store(wseq + (long long)c0 * Q, smem, (unsigned)(nch * Q * ES));
-                if (p.st_vec)
-                    bulk_store(reinterpret_cast<B *>(p.state) + (long long)slot * p.st_slot + (long long)c0 * R, st_img,
-                               (unsigned)(nch * R * ES));
+                if (p.st_vec || rows) bulk_store(st_blk, st_img, (unsigned)(nch * SC * ES));
                 asm volatile("cp.async.bulk.commit_group;\n" ::: "memory");
             }
         }
@@ -263,7 +296,6 @@ __global__ void __launch_bounds__(256) verify_fast(const __grid_constant__ Verif
 #pragma unroll
         for (int u = 0; u < TS; ++u) store_token(u, y[u]);
     } else {
-        if ((long long)BC * R * ES > (long long)dynamic_smem_bytes()) return;  // launch mismatch
         // chunked: any T, dense window
         uint32_t fin[R * NW];
 #pragma unroll
@@ -290,14 +322,13 @@ __global__ void __launch_bounds__(256) verify_fast(const __grid_constant__ Verif
 #pragma unroll
                 for (int k = 0; k < R; ++k) fw[e][k] = fw[e][TC + k];
         }
-        if (act) stage_state(smem, fin);
-        bulk = p.st_vec;
+        if (act) stage_state(fin);
+        bulk = p.st_vec || rows;
         if (bulk) {
             fence_smem_to_async();
             __syncthreads();
             if (tid == 0) {
-                bulk_store(reinterpret_cast<B *>(p.state) + (long long)slot * p.st_slot + (long long)c0 * R, smem,
-                           (unsigned)(nch * R * ES));
+                bulk_store(st_blk, st_img, (unsigned)(nch * SC * ES));
                 asm volatile("cp.async.bulk.commit_group;\n" ::: "memory");
             }
         }

@@ -31,8 +31,10 @@
 // the committed window is taken from columns [off, off+W-1) of it, and the row image is stored
 // back over the state row instead of into a window buffer; there is no separate committed-window
 // image.  Recompute rollback: outputs only; nothing is staged for storing and no bulk store runs.
-// State rows wider than the window (read at a state offset) are staged whole too; the committed
-// window then goes to their first W-1 columns by direct stores.
+// State rows wider than the window (read at a state offset) are staged whole too; each thread
+// copies its channels' staged rows into the state image with the committed window over their first
+// W-1 columns, and the image leaves whole by one bulk copy (the other columns go back with their
+// own bits): one contiguous run per unit instead of element stores at the row pitch.
 // Mixed dtypes (S, the type of the state and the snapshots, differs from B, the type of x, out, taps
 // and bias): the stages and the images hold each part in its own type; state columns keep their
 // bits, x elements enter them widened exactly (bf16 -> fp32) or rounded to the nearest bf16, and
@@ -109,13 +111,14 @@ __global__ void __launch_bounds__(128, (CPT == 4 && TS <= 8) ? 4 : 2) verify_pip
     const int Qrow = p.T + R - 1;  // columns of the snapshot row in global memory (Q: of the staged image)
 
     // shared memory: stage 0, stage 1 (x rows + committed windows, or whole history rows), image
-    // buffers 0 and 1 (dedup row image + committed-window image, or the history row image alone),
+    // buffers 0 and 1 (dedup row image + committed-window image -- whole rows when they are wider
+    // -- or the history row image alone),
     // 2 mbarriers and the unit information (kPipeInfoBytes), then (when compacting) the sort or warp
     // counts (AUX ints) and the list of active sequences (of chunks, for packed drafts)
     const long long xb = pipe_part((long long)XR * BC * ES);
     const long long stage_bytes = xb + pipe_part((long long)SC * BC * ESS);
     const long long rb = dense ? 0 : pipe_part((long long)Q * BC * ESS);
-    const long long img_bytes = recomp ? 0 : rb + ((hist || wide) ? 0 : pipe_part((long long)R * BC * ESS));
+    const long long img_bytes = recomp ? 0 : rb + (hist ? 0 : pipe_part((long long)(wide ? SC : R) * BC * ESS));
     unsigned char *const img0 = smem + 2 * stage_bytes;
     uint64_t *const bar = reinterpret_cast<uint64_t *>(img0 + 2 * img_bytes);
     // [0, 2): slots, [2, 4): state offsets, [4, 6): draft counts, [6, 8): first rows (packed drafts)
@@ -484,15 +487,19 @@ __global__ void __launch_bounds__(128, (CPT == 4 && TS <= 8) ? 4 : 2) verify_pip
                 for (int i = 0; i < R * NWS; ++i) fin[i] = run_word(i, R, TS);
             }
             if (wide) {
-                // committed window -> columns [0, W-1) of the wide rows, stored directly (the rows'
-                // other columns are not this call's to rewrite); this thread alone owns them.  (Wide
-                // rows have no committed-window image; only chunk 0 of a packed draft writes.)
+                // the thread's CPT staged rows (CPT * SC contiguous elements, a whole number of
+                // words) into the state image, the committed window over columns [0, W-1).  (Only
+                // chunk 0 of a packed draft writes the state.)
                 if (!recomp && first) {
-                    S *srow = reinterpret_cast<S *>(p.state) + (long long)slot * p.st_slot + (long long)c * SC;
+                    const int nwords = CPT * SC * ESS / 4;
+                    const unsigned *src = reinterpret_cast<const unsigned *>(stg + xb) + (long long)tid * nwords;
+                    unsigned *dst = reinterpret_cast<unsigned *>(stimg) + (long long)tid * nwords;
+                    for (int i = 0; i < nwords; ++i) dst[i] = src[i];
+                    S *const drow = reinterpret_cast<S *>(stimg) + (long long)cl * SC;
 #pragma unroll
                     for (int e = 0; e < CPT; ++e)
 #pragma unroll
-                        for (int kk = 0; kk < R; ++kk) srow[(long long)e * SC + kk] = (S)elem_raw<S>(fin, e * R + kk);
+                        for (int kk = 0; kk < R; ++kk) drow[e * SC + kk] = (S)elem_raw<S>(fin, e * R + kk);
                 }
             } else if (!hist && !recomp) {
                 stv<VS, R * NWS>(stimg + (long long)tid * CPT * R * ESS, fin);
@@ -540,9 +547,9 @@ __global__ void __launch_bounds__(128, (CPT == 4 && TS <= 8) ? 4 : 2) verify_pip
                 } else if (!dense && full_row) {
                     bulk_store(row_dst, img, (unsigned)(nch * Q * ESS));
                 }
-                if (!hist && !wide && first)
-                    bulk_store(reinterpret_cast<S *>(p.state) + (long long)slot * p.st_slot + (long long)c0 * R, stimg,
-                               (unsigned)(nch * R * ESS));
+                if (!hist && first)  // (SC == W-1 unless the rows are wide)
+                    bulk_store(reinterpret_cast<S *>(p.state) + (long long)slot * p.st_slot + (long long)c0 * SC, stimg,
+                               (unsigned)(nch * SC * ESS));
                 asm volatile("cp.async.bulk.commit_group;\n" ::: "memory");
             }
             if (k + 2 < iters) {

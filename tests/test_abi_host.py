@@ -197,9 +197,12 @@ def test_plan_general_path_cases(lib):
     a = _args(W3)
     a.state_ch_stride = 4  # packed rows wider than the window: staged whole (4+ units per block)
     a.state_cols = 4
-    assert _plan(lib, a)[1].path == 3
-    a.n_seq = 32  # too few units per block for wide rows: the one-pass kernel
-    assert _plan(lib, a)[1].path == 1
+    pl = _plan(lib, a)[1]
+    # stages of 8 x rows + 4 state columns; images of the 10-column dedup row + the 4-column rows
+    assert pl.path == 3 and pl.smem_bytes == _pipe_smem((8 + 4) * 512 * 2, (10 + 4) * 512 * 2, 128)
+    a.n_seq = 32  # too few units per block for wide rows: the one-pass kernel, the rows staged whole
+    pl = _plan(lib, a)[1]
+    assert pl.path == 1 and pl.smem_bytes == pl.channels_per_block * (10 + 4) * 2
     a.n_seq = 128
     a.state_ch_stride = 8  # rows with a gap between them: no bulk copy of the state
     assert _plan(lib, a)[1].path == 1

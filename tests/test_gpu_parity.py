@@ -375,6 +375,56 @@ def test_wide_state_rows_pipelined(cuda_lib, layout, T, width):
     check_verify_and_commit(cuda_lib, w, inp)
 
 
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("layout,T,width", [("dense", 3, 2), ("dense", 8, 3), ("dedup", 4, 4), ("dedup", 8, 4),
+                                            ("dense", 17, 3), ("dense", 24, 4)])
+def test_wide_state_rows_one_pass(cuda_lib, dtype, layout, T, width):
+    """Packed state rows wider than the window on the one-pass kernel (a small batch): each block
+    stages its rows whole and stores them back whole, with the committed window over the first W-1
+    columns; every offset 0..T-1 appears, dim 1000 leaves a partial last block, and the columns
+    past the window must come back with their own bits (compared bitwise, like everything else)."""
+    w = wl.VerifyWorkload("wide1", n_seq=6, T=T, dim=1000, width=width, qk_channels=512, head_dim=128,
+                          dtype=dtype, layout=layout, bias=True, n_pad=1, extra_slots=2, state_offset=True,
+                          seed=70 * T + width)
+    inp = wl.make_inputs(w)
+    inp["state_off"] = (torch.arange(w.n_seq, dtype=torch.int32) % T).contiguous()
+    d = {k: (v.to("cuda") if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    pl = cuda_lib.verify_plan(d["x"], d["conv_state"], d["weight"], d["bias"], d["out"], d["window"], layout=layout,
+                              qk_channels=w.qk_channels, head_dim=w.head_dim, cache_idx=d["cache_idx"],
+                              state_off=d["state_off"])
+    assert pl.path in (1, 2)
+    check_verify_and_commit(cuda_lib, w, inp)
+
+
+@pytest.mark.parametrize("layout,T", [("dense", 8), ("dedup", 5), ("dense", 20)])
+def test_wide_state_rows_unaligned(cuda_lib, layout, T):
+    """Wide state rows whose base is not 16-byte aligned cannot be staged by 16-byte copies: the
+    one-pass kernel reads and writes them element by element instead, with the same results."""
+    w = wl.VerifyWorkload("wideu", n_seq=5, T=T, dim=1000, width=4, qk_channels=512, head_dim=128, dtype="bf16",
+                          layout=layout, bias=True, n_pad=1, extra_slots=2, state_offset=True, seed=90 + T)
+    inp = wl.make_inputs(w)
+    inp["state_off"] = (torch.arange(w.n_seq, dtype=torch.int32) % T).contiguous()
+    ref = run_oracle_verify(w, inp)
+    d = to_device(inp)
+    st = d["conv_state"]
+    buf = torch.empty(st.numel() + 8, dtype=st.dtype, device="cuda")
+    d["conv_state"] = buf[1:1 + st.numel()].view(st.shape)  # 2 bytes past a 16-byte boundary
+    d["conv_state"].copy_(st)
+    err = torch.full((w.n_seq,), -7, dtype=torch.int32, device="cuda")
+    pl = cuda_lib.verify_plan(d["x"], d["conv_state"], d["weight"], d["bias"], d["out"], d["window"], layout=layout,
+                              qk_channels=w.qk_channels, head_dim=w.head_dim, cache_idx=d["cache_idx"],
+                              state_off=d["state_off"])
+    assert pl.path in (1, 2)
+    cuda_lib.conv_verify(d["x"], d["conv_state"], d["weight"], d["bias"], d["out"], d["window"], layout=layout,
+                         qk_channels=w.qk_channels, head_dim=w.head_dim, l2_eps=w.l2_eps, cache_idx=d["cache_idx"],
+                         state_off=d["state_off"], err=err)
+    torch.cuda.synchronize()
+    assert_bits_equal(err.cpu(), ref["status"], "err")
+    assert_bits_equal(d["window"].cpu(), ref["window"], "window")
+    assert_bits_equal(d["conv_state"].cpu(), ref["conv_state"], "state")
+    assert_out_close(d["out"].cpu(), ref["out"], "out")
+
+
 def test_maximum_batch_on_gpu(cuda_lib):
     """The largest batch the ABI accepts (65535 sequences; the pipelined kernel then walks every
     sequence without a shared-memory list), with padded sequences and a pool of unused slots."""
