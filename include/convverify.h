@@ -51,7 +51,7 @@ extern "C" {
 #define CV_API
 #endif
 
-#define CV_ABI_VERSION 6
+#define CV_ABI_VERSION 7
 #define CV_MAX_T 128 /* draft tokens per verify call */
 
 typedef enum cv_dtype {
@@ -80,7 +80,10 @@ typedef enum cv_window_layout {
        call passes state_off[s] = accept_len[s] - 1 and no commit runs (a reading of the
        [sglang-46184] slot row together with its accepted-token state offset).  Needs
        state_cols >= T+W-2; columns at and above T+W-2 are not touched.  cv_conv_commit rejects
-       this layout. */
+       this layout.  Only this layout accepts column-major state rows (state_col_stride != 1:
+       [n_slots, state_cols, dim] storage seen as [n_slots, dim, state_cols], like the pool's
+       axis-0 window layout of [sglang-46184]), with which the call reads W-1 columns and writes
+       T+W-2 columns, each a contiguous run of channels. */
     CV_WINDOW_HISTORY = 3,
     /* recompute rollback ([memra-engine] ssm_conv_ring_rebuild_dc): no window buffer (window may
        be NULL; the win_* strides are ignored).  The verify writes the outputs only -- no
@@ -102,10 +105,12 @@ enum {
     CV_ERR_DTYPE = -6,        /* dtype not a cv_dtype */
     CV_ERR_HEAD_DIM = -7,     /* qk_channels > 0 and head_dim not a power of two in 8..256, or
                                  qk_channels not a multiple of head_dim, or qk_channels > dim */
-    CV_ERR_LAYOUT = -8,       /* unknown layout, DEDUP with win_step_stride != win_col_stride, or
-                                 HISTORY passed to cv_conv_commit */
+    CV_ERR_LAYOUT = -8,       /* unknown layout, DEDUP with win_step_stride != win_col_stride,
+                                 HISTORY passed to cv_conv_commit, or column-major state rows
+                                 outside HISTORY */
     CV_ERR_STRIDE = -9,       /* a negative stride, or state rows that overlap (state_ch_stride <
-                                 state_cols with dim > 1) */
+                                 state_cols with dim > 1; column-major rows: state_ch_stride != 1
+                                 or state_col_stride < dim) */
     CV_ERR_ALIAS = -10,       /* out or window has the same base address as x, conv_state or weight,
                                  or out and window share a base address */
     CV_ERR_LAUNCH = -11,      /* the CUDA launch failed (cudaGetLastError after the launch) */
@@ -160,7 +165,11 @@ enum {
  *                      (x may be a strided slice of a wider projection output)
  *   out                [n_seq][T][dim] write-only; (s,t,c) at s*out_seq_stride + t*out_tok_stride + c
  *   conv_state         [n_slots][dim][state_cols] read-modify-write in place;
- *                      (slot,c,k) at slot*state_slot_stride + c*state_ch_stride + k
+ *                      (slot,c,k) at slot*state_slot_stride + c*state_ch_stride + k*state_col_stride
+ *                      (state_col_stride 0 or 1: columns contiguous, state_ch_stride >= state_cols;
+ *                      else only in CV_WINDOW_HISTORY, with state_ch_stride == 1 and
+ *                      state_col_stride >= dim: column-major rows, else CV_ERR_STRIDE /
+ *                      CV_ERR_LAYOUT)
  *   cache_idx          int32 [n_seq] device array or NULL (slot = s); negative = padded sequence
  *   state_off          int32 [n_seq] device array or NULL (0): column where the committed window is
  *                      read, the num_accept_tokens offset of [sglang-46184]
@@ -238,6 +247,7 @@ typedef struct cv_verify_args {
     const int32_t *parent;
     const int32_t *cu_draft; /* packed ragged drafts: int32 [n_seq + 1] device array, or NULL */
     int32_t total_tokens;    /* rows of x and out when cu_draft is given */
+    int64_t state_col_stride; /* conv_state column stride; 0 or 1 = columns contiguous */
 } cv_verify_args;
 
 CV_API int cv_conv_verify(const cv_verify_args *args, void *stream);

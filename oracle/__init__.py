@@ -138,8 +138,9 @@ def conv_verify(x, conv_state, weight, bias, out, window, *, layout, qk_channels
                 cache_idx=None, state_off=None, status=None, parent=None, cu_draft=None, T=None):
     """Run the oracle verify in place on CPU tensors (conv_state, out, window, status are written).
 
-    x [n_seq, T, dim] (channel stride 1), conv_state [n_slots, dim, S] (column stride 1),
-    weight [dim, W] contiguous, bias [dim] or None, out [n_seq, T, dim] (channel stride 1),
+    x [n_seq, T, dim] (channel stride 1), conv_state [n_slots, dim, S] (any strides: a state whose
+    columns are not contiguous is run on a contiguous copy, written back afterwards), weight
+    [dim, W] contiguous, bias [dim] or None, out [n_seq, T, dim] (channel stride 1),
     window dense [n_seq, T, dim, W-1] / dedup [n_seq, dim, T+W-2] / None for the history layout
     (the state row, S >= T+W-2 columns, receives the snapshot row) and the recompute layout
     (outputs only, state untouched); cache_idx, state_off, status int32 [n_seq] or None; parent
@@ -167,7 +168,9 @@ def conv_verify(x, conv_state, weight, bias, out, window, *, layout, qk_channels
         assert x.stride(2) == 1 and out.stride(2) == 1
         x_seq, x_tok, o_seq, o_tok = x.stride(0), x.stride(1), out.stride(0), out.stride(1)
     W = weight.shape[1]
-    assert conv_state.stride(2) == 1
+    state_arg = conv_state  # (the storage order of the state rows is not part of the arithmetic)
+    if conv_state.stride(2) != 1:
+        conv_state = conv_state.contiguous()
     assert weight.is_contiguous()
     ws = window_strides(window, layout)
     a = _VerifyArgs(
@@ -185,6 +188,8 @@ def conv_verify(x, conv_state, weight, bias, out, window, *, layout, qk_channels
     rc = _load().oracle_conv_verify(ctypes.byref(a))
     if rc != 0:
         raise RuntimeError(f"oracle_conv_verify returned {rc}")
+    if conv_state is not state_arg:
+        state_arg.copy_(conv_state)
 
 
 def conv_commit(conv_state, window, accept_len, *, layout, T, width, cache_idx=None, status=None, x=None,

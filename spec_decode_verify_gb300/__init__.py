@@ -43,6 +43,7 @@ class VerifyArgs(ctypes.Structure):
         ("window", c_vp), ("window_layout", c_i32), ("wait_polls", c_i32),
         ("win_seq_stride", c_i64), ("win_step_stride", c_i64), ("win_ch_stride", c_i64), ("win_col_stride", c_i64),
         ("err", c_vp), ("state_dtype", c_i32), ("parent", c_vp), ("cu_draft", c_vp), ("total_tokens", c_i32),
+        ("state_col_stride", c_i64),
     ]
 
 
@@ -230,8 +231,11 @@ def make_verify_args(x, conv_state, weight, bias, out, window, *, layout, qk_cha
     for t, name in ((cache_idx, "cache_idx"), (state_off, "state_off"), (err, "err")):
         _need_int32(t, name, n=n_seq)
     _need_int32(parent, "parent", shape=(n_seq, T))
-    if x.stride(-1) != 1 or out.stride(-1) != 1 or conv_state.stride(2) != 1:
-        raise ValueError("x, out and conv_state need a unit innermost stride")
+    if x.stride(-1) != 1 or out.stride(-1) != 1:
+        raise ValueError("x and out need a unit innermost stride")
+    # conv_state: columns contiguous, or (history layout) column-major rows [n_slots, S, dim] seen
+    # as [n_slots, dim, S]; the library checks which strides it accepts
+    st_col = 1 if conv_state.shape[2] == 1 else conv_state.stride(2)
     if not weight.is_contiguous() or (bias is not None and not bias.is_contiguous()):
         raise ValueError("weight and bias must be contiguous")
     ws = _window_strides(window, lay)
@@ -248,7 +252,8 @@ def make_verify_args(x, conv_state, weight, bias, out, window, *, layout, qk_cha
         window_layout=lay, wait_polls=int(wait_polls), win_seq_stride=ws[0], win_step_stride=ws[1], win_ch_stride=ws[2],
         win_col_stride=ws[3], err=ptr(err, "err", False),
         state_dtype=0 if conv_state.dtype == x.dtype else _dtype_code(conv_state) + 1,
-        parent=ptr(parent, "parent", False), cu_draft=ptr(cu_draft, "cu_draft", False), total_tokens=total)
+        parent=ptr(parent, "parent", False), cu_draft=ptr(cu_draft, "cu_draft", False), total_tokens=total,
+        state_col_stride=st_col)
 
 
 def conv_verify(x, conv_state, weight, bias, out, window, *, layout, qk_channels, head_dim, l2_eps=1e-6,

@@ -125,6 +125,9 @@ const cvk::VarlenSet &varlen_set(int dtype, int width) {
     return cvk::varlen_f32_w4();
 }
 
+// State columns not contiguous (state_col_stride other than 0 or 1).
+bool state_col_major(const cv_verify_args *a) { return a->state_col_stride > 1; }
+
 int check_verify(const cv_verify_args *a) {
     if (!a) return CV_ERR_NULL_ARGS;
     if (a->dtype != CV_F32 && a->dtype != CV_BF16) return CV_ERR_DTYPE;
@@ -154,7 +157,14 @@ int check_verify(const cv_verify_args *a) {
         return CV_ERR_STRIDE;
     if (!nowin && (a->win_seq_stride < 0 || a->win_step_stride < 0 || a->win_ch_stride < 0 || a->win_col_stride < 0))
         return CV_ERR_STRIDE;
-    if (a->dim > 1 && a->state_ch_stride < a->state_cols) return CV_ERR_STRIDE;
+    if (a->state_col_stride < 0) return CV_ERR_STRIDE;
+    if (state_col_major(a)) {
+        // column-major rows: the commit-free history layout only
+        if (!hist) return CV_ERR_LAYOUT;
+        if (a->state_ch_stride != 1 || a->state_col_stride < a->dim) return CV_ERR_STRIDE;
+    } else if (a->dim > 1 && a->state_ch_stride < a->state_cols) {
+        return CV_ERR_STRIDE;
+    }
     // (packed drafts with no rows at all need no x or out)
     const bool rows = !a->cu_draft || a->total_tokens > 0;
     if (a->n_seq > 0 && ((rows && (!a->x || !a->out)) || !a->conv_state || !a->weight || (!nowin && !a->window)))
@@ -289,8 +299,11 @@ int plan_verify(const cv_verify_args *a, cv_launch_plan *pl) {
     // the pipelined kernel stages packed state rows whole (state_ch_stride == state_cols): the
     // committed windows of [dim][W-1] rows, or wider rows read at an offset; the history layout
     // needs rows of exactly T+W-2 columns
-    const bool rows_packed = aligned16(a->conv_state) && stride16(a->state_slot_stride, ssize) &&
-                             a->state_ch_stride == a->state_cols;
+    const bool hist_t = hist && state_col_major(a);  // column-major history rows
+    const bool rows_packed = hist_t ? a->dim % 8 == 0 && aligned16(a->conv_state) &&
+                                          stride16(a->state_slot_stride, ssize) && stride16(a->state_col_stride, ssize)
+                                    : aligned16(a->conv_state) && stride16(a->state_slot_stride, ssize) &&
+                                          a->state_ch_stride == a->state_cols;
     const bool varlen = a->cu_draft != nullptr;
     const int ts = pipe_tokens(a);             // tokens per unit
     const bool chunked = varlen && a->T > ts;  // packed drafts cut into chunks
@@ -299,7 +312,7 @@ int plan_verify(const cv_verify_args *a, cv_launch_plan *pl) {
     // longer draft need the work list and no history rows)
     bool pipe_ok = (!mixed || a->T <= cvk::kMaxMixedT) && !(mixed && varlen) && io_packed(a, esize) &&
                    ts <= ks.max_static_t && rows_packed &&
-                   (hist ? a->state_cols == a->T + R - 1 : (recomp || fast || dedup_t)) &&
+                   (hist ? (hist_t || a->state_cols == a->T + R - 1) : (recomp || fast || dedup_t)) &&
                    !(chunked && (hist || !pipe_compacts(a)));
     const bool wide = !hist && a->state_cols != R;
     // The pipeline pays for its prologue only when every block walks several units; with fewer the
@@ -323,7 +336,7 @@ int plan_verify(const cv_verify_args *a, cv_launch_plan *pl) {
         // windows, or the history row alone; none for the recompute rollback), the state parts in
         // the state's dtype; 2 mbarriers, 2 slots, 2 offsets
         const long long stage = part((long long)(ts + (chunked ? R : 0)) * bc * esize) +
-                                part((long long)a->state_cols * bc * ssize);
+                                part((long long)(hist_t ? R : a->state_cols) * bc * ssize);
         long long image = (hist || recomp) ? 0 : part((wide ? a->state_cols : R) * bc * ssize);
         if (a->window_layout == CV_WINDOW_DEDUP || hist) image += part(Q * bc * ssize);
         const long long smem = 2 * stage + 2 * image + cvk::kPipeInfoBytes +
@@ -438,6 +451,7 @@ int launch_verify(const cv_verify_args *a, const cv_launch_plan &pl, cudaStream_
     p.state = a->conv_state;
     p.st_slot = a->state_slot_stride;
     p.st_ch = a->state_ch_stride;
+    p.st_col = state_col_major(a) ? a->state_col_stride : 1;
     p.cache_idx = a->cache_idx;
     p.state_off = a->state_off;
     p.weight = a->weight;
@@ -473,7 +487,8 @@ int launch_verify(const cv_verify_args *a, const cv_launch_plan &pl, cudaStream_
     const bool vl = a->cu_draft != nullptr;  // (packed drafts ignore the sequence strides)
     p.x_vec = aligned16(a->x) && (vl || stride16(a->x_seq_stride, esize)) && stride16(a->x_tok_stride, esize);
     p.out_vec = aligned16(a->out) && (vl || stride16(a->out_seq_stride, esize)) && stride16(a->out_tok_stride, esize);
-    p.st_vec = state_packed(a->conv_state, a->state_slot_stride, a->state_ch_stride, a->width, ssize);
+    p.st_vec = !state_col_major(a) &&
+               state_packed(a->conv_state, a->state_slot_stride, a->state_ch_stride, a->width, ssize);
     p.st_rows = (pl.path == 1 || pl.path == 2) && fast_rows_staged(a, ssize, pl.channels_per_block);
     p.w_vec = aligned16(a->weight);
     p.b_vec = a->bias ? aligned16(a->bias) : 0;

@@ -16,6 +16,7 @@ struct VerifyParams {
     long long out_seq, out_tok;
     void *state;
     long long st_slot, st_ch;
+    long long st_col;  // state column stride: 1, or (history rows only) column-major rows with st_ch == 1
     const int *cache_idx;
     const int *state_off;
     const void *weight;

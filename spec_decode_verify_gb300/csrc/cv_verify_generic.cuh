@@ -212,7 +212,8 @@ __global__ void __launch_bounds__(256) verify_generic(const __grid_constant__ Ve
     float win[R][8];
     {
         BS raw[R][8];
-        BS *sp = reinterpret_cast<BS *>(p.state) + (long long)slot * p.st_slot + (long long)(c0 + cl) * p.st_ch + off;
+        BS *sp = reinterpret_cast<BS *>(p.state) + (long long)slot * p.st_slot + (long long)(c0 + cl) * p.st_ch +
+                 (long long)off * p.st_col;
         if (full8 && p.st_vec && off == 0) {
             // 8 channels x R columns are contiguous: R 16-byte vectors (2R for fp32)
             Oct<BS> o[R];
@@ -229,7 +230,7 @@ __global__ void __launch_bounds__(256) verify_generic(const __grid_constant__ Ve
 #pragma unroll
             for (int e = 0; e < 8; ++e)
 #pragma unroll
-                for (int k = 0; k < R; ++k) raw[k][e] = (e < my) ? sp[e * p.st_ch + k] : (BS)0;
+                for (int k = 0; k < R; ++k) raw[k][e] = (e < my) ? sp[e * p.st_ch + k * p.st_col] : (BS)0;
         }
 #pragma unroll
         for (int k = 0; k < R; ++k) {
@@ -291,7 +292,7 @@ __global__ void __launch_bounds__(256) verify_generic(const __grid_constant__ Ve
         // [0, T+W-2) of the state row (every thread read its committed window before the barrier)
         // (no draft token, no snapshot: a packed sequence with T_s = 0 writes nothing here)
         BS *sb = reinterpret_cast<BS *>(p.state) + (long long)slot * p.st_slot + (long long)c0 * p.st_ch;
-        if (Ts > 0) write_view<TT, BS>(tile, pitch, 1, Ts + R - 1, sb, p.st_ch, 1, nch, R);
+        if (Ts > 0) write_view<TT, BS>(tile, pitch, 1, Ts + R - 1, sb, p.st_ch, p.st_col, nch, R);
     } else {
         BS *wb = reinterpret_cast<BS *>(p.win) + (long long)s * p.w_seq;
         if (p.dedup) {

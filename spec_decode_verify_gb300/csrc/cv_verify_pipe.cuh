@@ -30,7 +30,10 @@
 // History-row state (no window buffer): the stage holds each channel's whole [T+W-2] state row,
 // the committed window is taken from columns [off, off+W-1) of it, and the row image is stored
 // back over the state row instead of into a window buffer; there is no separate committed-window
-// image.  Recompute rollback: outputs only; nothing is staged for storing and no bulk store runs.
+// image.  Column-major history rows (the state row stored column by column, channel stride 1): the
+// stage holds only the W-1 columns at the offset, one bulk copy each, and the row image is staged
+// column by column like a transposed dedup row and stored as one bulk copy per column, so the
+// commit-free step moves exactly the bytes the method reads and writes.  Recompute rollback: outputs only; nothing is staged for storing and no bulk store runs.
 // State rows wider than the window (read at a state offset) are staged whole too; each thread
 // copies its channels' staged rows into the state image with the committed window over their first
 // W-1 columns, and the image leaves whole by one bulk copy (the other columns go back with their
@@ -102,8 +105,10 @@ __global__ void __launch_bounds__(128, (CPT == 4 && TS <= 8) ? 4 : 2) verify_pip
     // state columns staged per channel: the committed windows of packed [dim][W-1] rows, or whole
     // rows when they are wider (history rows, or rows read at a state offset)
     const int SC = p.state_cols;
-    const bool whole_rows = SC != R;
-    const bool wide = whole_rows && !hist;  // wider rows, not history: the window is stored directly
+    const bool hist_t = hist && p.st_col != 1;  // column-major history rows: W-1 columns staged
+    const int SCS = hist_t ? R : SC;            // state columns per staged channel (or staged columns)
+    const bool whole_rows = !hist_t && SC != R;
+    const bool wide = whole_rows && !hist;  // wider rows, not history: staged whole, stored whole
 
     // packed drafts longer than a chunk: W-1 more staged x rows per unit (a halo or a tail)
     const bool chunked = VL && p.T > TS;
@@ -116,7 +121,7 @@ __global__ void __launch_bounds__(128, (CPT == 4 && TS <= 8) ? 4 : 2) verify_pip
     // 2 mbarriers and the unit information (kPipeInfoBytes), then (when compacting) the sort or warp
     // counts (AUX ints) and the list of active sequences (of chunks, for packed drafts)
     const long long xb = pipe_part((long long)XR * BC * ES);
-    const long long stage_bytes = xb + pipe_part((long long)SC * BC * ESS);
+    const long long stage_bytes = xb + pipe_part((long long)SCS * BC * ESS);
     const long long rb = dense ? 0 : pipe_part((long long)Q * BC * ESS);
     const long long img_bytes = recomp ? 0 : rb + (hist ? 0 : pipe_part((long long)(wide ? SC : R) * BC * ESS));
     unsigned char *const img0 = smem + 2 * stage_bytes;
@@ -252,11 +257,22 @@ __global__ void __launch_bounds__(128, (CPT == 4 && TS <= 8) ? 4 : 2) verify_pip
                 issue_extra(k, ix.b + t0 - R);  // the halo: the W-1 rows before the chunk
             } else {
                 if (chunked && ts > TS) issue_extra(k, ix.b + ts - R);  // the tail: the draft's last W-1 rows
-                // packed state rows of SC columns: the committed windows, or whole rows
-                mbar_expect_tx(&bar[st], (unsigned)(SC * nch * ESS));
-                bulk_load(smem + st * stage_bytes + xb,
-                          reinterpret_cast<const S *>(p.state) + (long long)slot * p.st_slot + (long long)c0 * SC,
-                          (unsigned)(nch * SC * ESS), &bar[st]);
+                if (hist_t) {
+                    // column-major history rows: columns [off, off+W-1), each a run of nch channels,
+                    // into stage columns [0, W-1) of BC channels each
+                    mbar_expect_tx(&bar[st], (unsigned)(R * nch * ESS));
+                    const S *col0 = reinterpret_cast<const S *>(p.state) + (long long)slot * p.st_slot +
+                                    (long long)off * p.st_col + c0;
+                    for (int kk = 0; kk < R; ++kk)
+                        bulk_load(smem + st * stage_bytes + xb + (long long)kk * BC * ESS, col0 + (long long)kk * p.st_col,
+                                  (unsigned)(nch * ESS), &bar[st]);
+                } else {
+                    // packed state rows of SC columns: the committed windows, or whole rows
+                    mbar_expect_tx(&bar[st], (unsigned)(SC * nch * ESS));
+                    bulk_load(smem + st * stage_bytes + xb,
+                              reinterpret_cast<const S *>(p.state) + (long long)slot * p.st_slot + (long long)c0 * SC,
+                              (unsigned)(nch * SC * ESS), &bar[st]);
+                }
             }
         }
         mbar_arrive(&bar[st]);
@@ -361,6 +377,21 @@ __global__ void __launch_bounds__(128, (CPT == 4 && TS <= 8) ? 4 : 2) verify_pip
                         sw[i] = hr[i % R][i / R];
                     }
                 }
+            } else if (hist_t) {
+                // staged column kk holds the committed window's column kk of all BC channels
+                uint32_t cw[R][NWS];
+#pragma unroll
+                for (int kk = 0; kk < R; ++kk)
+                    ldv<pipe_align(CPT * ESS), NWS>(cw[kk], stg + xb + ((long long)kk * BC + cl) * ESS);
+#pragma unroll
+                for (int i = 0; i < R * NWS; ++i) {
+                    if (ESS == 2) {
+                        const int a = 2 * i, b2 = 2 * i + 1;  // elements (channel a / R, column a % R)
+                        sw[i] = pack_halves(elem_raw<S>(cw[a % R], a / R), elem_raw<S>(cw[b2 % R], b2 / R));
+                    } else {
+                        sw[i] = cw[i % R][i / R];
+                    }
+                }
             } else if (whole_rows) {
                 // the committed window sits at columns [off, off+W-1) of each staged row
                 using U = std::conditional_t<ESS == 2, unsigned short, unsigned>;
@@ -409,7 +440,7 @@ __global__ void __launch_bounds__(128, (CPT == 4 && TS <= 8) ? 4 : 2) verify_pip
             };
             if (recomp) {
                 // outputs only: no snapshots, and the state keeps the pre-verify window
-            } else if (dedup_t) {
+            } else if (dedup_t || hist_t) {
                 // column q (input q+1) of the thread's CPT channels, in the state's type, at image
                 // position [q][cl]
 #pragma unroll
@@ -537,12 +568,14 @@ __global__ void __launch_bounds__(128, (CPT == 4 && TS <= 8) ? 4 : 2) verify_pip
                                 : reinterpret_cast<S *>(p.win) + (long long)s * p.w_seq + (long long)c0 * Qrow;
         if (tid == 0) {
             if (go && !recomp) {
-                if (dedup_t) {
-                    // one bulk copy per column
+                if (dedup_t || hist_t) {
+                    // one bulk copy per column (of the window row, or of the column-major state row)
                     const int ncols = full_row ? Q : cnt;
-                    S *const colb = reinterpret_cast<S *>(p.win) + (long long)s * p.w_seq + c0;
+                    S *const colb = hist_t ? reinterpret_cast<S *>(p.state) + (long long)slot * p.st_slot + c0
+                                           : reinterpret_cast<S *>(p.win) + (long long)s * p.w_seq + c0;
+                    const long long cstride = hist_t ? p.st_col : p.w_col;
                     for (int q2 = 0; q2 < ncols; ++q2)
-                        bulk_store(colb + (long long)(qd + q2) * p.w_col, img + (long long)(qs + q2) * BC * ESS,
+                        bulk_store(colb + (long long)(qd + q2) * cstride, img + (long long)(qs + q2) * BC * ESS,
                                    (unsigned)(nch * ESS));
                 } else if (!dense && full_row) {
                     bulk_store(row_dst, img, (unsigned)(nch * Q * ESS));
@@ -557,7 +590,7 @@ __global__ void __launch_bounds__(128, (CPT == 4 && TS <= 8) ? 4 : 2) verify_pip
                 load_index(k + 3, pf);
             }
         }
-        if (VL && go && !recomp && !dense && !dedup_t && !full_row && cnt > 0) {
+        if (VL && go && !recomp && !dense && !dedup_t && !hist_t && !full_row && cnt > 0) {
             if (!chunked) {
                 // one chunk, columns [0, T_s+W-2): word w of the staged image holds elements 2w,
                 // 2w+1 (bf16) or w (fp32) of the block's [nch][Q] run, Q = the row's width

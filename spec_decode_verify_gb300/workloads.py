@@ -64,6 +64,9 @@ class VerifyWorkload:
     # dedup rows stored column by column ([n_seq, T+W-2, dim] seen as [n_seq, dim, T+W-2]: MambaPool's
     # axis-0 window layout seen transposed, sglang PR #46184 "Modifications", test coverage)
     window_transposed: bool = False
+    # state rows stored column by column ([n_slots, state_cols, dim] seen as [n_slots, dim, state_cols]);
+    # the history layout only: the commit-free step then reads W-1 and writes T+W-2 channel runs
+    state_transposed: bool = False
     seed: int = 0
 
     @property
@@ -136,6 +139,10 @@ WORKLOADS = {
         VerifyWorkload("n128_t8_dim10240_w4_bf16_dedupT_pad13", n_seq=128, T=8, dim=10240, width=4,
                        qk_channels=4096, head_dim=128, dtype="bf16", layout="dedup", n_pad=13,
                        extra_slots=16, window_transposed=True, seed=9),
+        # the commit-free step with the state rows stored column by column
+        VerifyWorkload("n128_t8_dim10240_w4_bf16_historyT_pad13", n_seq=128, T=8, dim=10240, width=4,
+                       qk_channels=4096, head_dim=128, dtype="bf16", layout="history", n_pad=13,
+                       extra_slots=16, state_offset=True, state_transposed=True, seed=12),
     ]
 }
 WORKLOAD_ORDER = list(WORKLOADS)
@@ -165,7 +172,7 @@ def make_inputs(w: VerifyWorkload, seed: Optional[int] = None) -> dict:
     """CPU tensors for one verify + commit of workload ``w``.
 
     Returns x [n_seq, T, dim] (a view with token stride ``x_row_stride`` when set), conv_state
-    [n_slots, dim, state_cols], weight [dim, W], bias [dim] or None, cache_idx int32 [n_seq]
+    [n_slots, dim, state_cols] (column-major when ``state_transposed``), weight [dim, W], bias [dim] or None, cache_idx int32 [n_seq]
     (-1 = padded), state_off int32 [n_seq] or None, accept_len int32 [n_seq] in 1..T, and
     sentinel-filled out [n_seq, T, dim] and window buffers (dense [n_seq, T, dim, W-1], dedup
     [n_seq, dim, T+W-2], None for the history and recompute layouts).
@@ -177,6 +184,10 @@ def make_inputs(w: VerifyWorkload, seed: Optional[int] = None) -> dict:
     x_wide = _to_dtype(xw, dt)
     x = x_wide.view(w.n_seq, w.T, row)[:, :, : w.dim]
     state = _to_dtype(rng.standard_normal((w.n_slots, w.dim, w.state_cols), dtype=np.float32), w.state_torch_dtype)
+    if w.state_transposed:  # the same values, stored column-major
+        st = torch.empty((w.n_slots, w.state_cols, w.dim), dtype=state.dtype).transpose(1, 2)
+        st.copy_(state)
+        state = st
     if w.qkv_split:
         parts = [rng.uniform(-0.5, 0.5, size=(n, 1, w.width)).astype(np.float32) for n in w.qkv_split]
         weight = _to_dtype(np.concatenate(parts, axis=0), dt).squeeze(1)

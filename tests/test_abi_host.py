@@ -108,6 +108,58 @@ def test_plan_for_history_workload(lib):
     assert (pl.grid_x, pl.grid_y) == (440, 1)
 
 
+HISTT = wl.WORKLOADS["n128_t8_dim10240_w4_bf16_historyT_pad13"]
+
+
+def test_plan_for_column_major_history(lib):
+    """Column-major history rows: the stages hold 8 x rows and only the W-1 = 3 staged columns of
+    the state, the image the 10-column row (stored column by column); 4 blocks fit an SM."""
+    a = _args(HISTT)
+    assert (a.state_ch_stride, a.state_col_stride, a.state_slot_stride) == (1, 10240, 10 * 10240)
+    rc, pl = _plan(lib, a)
+    assert rc == 0
+    smem = _pipe_smem((8 + 3) * 512 * 2, 10 * 512 * 2, 128)
+    assert (pl.threads, pl.channels_per_block, pl.path, pl.smem_bytes, pl.stages) == (128, 512, 3, smem, 2)
+    assert (pl.grid_x, pl.grid_y) == (600, 1)
+    # rows wider than T+W-2 stay pipelined (only W-1 columns are staged)
+    b = _args(HISTT.replace(n_seq=64, n_pad=0, extra_slots=0))
+    b.state_cols = 12
+    b.state_slot_stride = 12 * 10240
+    assert _plan(lib, b)[1].path == 3
+
+
+def test_column_major_state_validation(lib):
+    """A column stride other than 0/1 needs the history layout (else CV_ERR_LAYOUT), a channel
+    stride of 1 and a column stride of at least dim (else CV_ERR_STRIDE); negative is
+    CV_ERR_STRIDE; column strides that are not 16-byte multiples, or dims that are not multiples
+    of 8, take the general kernel."""
+    a = _args(HISTT)
+    a.state_col_stride = -1
+    assert _plan(lib, a)[0] == -9
+    a = _args(HISTT)
+    a.state_col_stride = 10239
+    assert _plan(lib, a)[0] == -9
+    a = _args(HISTT)
+    a.state_ch_stride = 2
+    a.state_col_stride = 2 * 10240
+    assert _plan(lib, a)[0] == -9
+    a = _args(HISTT)
+    a.state_col_stride = 10248  # a 16-byte multiple (bf16): still pipelined
+    a.state_slot_stride = 10 * 10248
+    assert _plan(lib, a)[1].path == 3
+    a.state_col_stride = 10241
+    a.state_slot_stride = 10 * 10241
+    assert _plan(lib, a)[1].path == 0
+    w = W3.replace(n_seq=4, n_pad=0, extra_slots=0)
+    a = _args(w)
+    a.state_ch_stride, a.state_col_stride = 1, w.dim
+    assert _plan(lib, a)[0] == -8
+    a = _args(HISTT.replace(dim=10232, qk_channels=4096, n_seq=8, n_pad=0, extra_slots=0))
+    assert _plan(lib, a)[1].path == 3
+    a = _args(HISTT.replace(dim=10236, qk_channels=4096, n_seq=8, n_pad=0, extra_slots=0))
+    assert _plan(lib, a)[1].path == 0
+
+
 def test_history_validation_and_paths(lib):
     # rows narrower than T+W-2 are rejected
     a = _args(HIST)

@@ -183,3 +183,23 @@ def test_ragged_chunked_on_pipelined_kernel(cuda_lib, layout, dtype, T):
                           pad=(2, 11), extra_slots=3, state_offset=layout != "recompute", extra_rows=2,
                           window_transposed=layout == "dedupT", seed=T)
     check(cuda_lib, w, wl.make_ragged_inputs(w), path=3)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("T", [5, 8, 12])
+def test_ragged_column_major_history(cuda_lib, dtype, T):
+    """Packed drafts (0..T tokens each) on column-major history rows: the pipelined kernel for
+    T <= 8 (a sequence writes columns [0, T_s+W-2) of its row, one bulk copy each; T_s = 0 writes
+    nothing), the general kernel beyond (history rows are not chunked)."""
+    rng = np.random.default_rng(900 + T)
+    n = 41
+    lengths = tuple(int(v) for v in rng.integers(0, T + 1, size=n))
+    w = wl.RaggedWorkload(f"ragHT{T}", lengths=lengths, T=T, dim=1024, width=4, qk_channels=512, head_dim=128,
+                          dtype=dtype, layout="history", bias=True, pad=(3, 17), extra_slots=2, state_offset=True,
+                          seed=T)
+    inp = wl.make_ragged_inputs(w)
+    st = inp["conv_state"]
+    cm = torch.empty((st.shape[0], st.shape[2], st.shape[1]), dtype=st.dtype).transpose(1, 2)
+    cm.copy_(st)
+    inp["conv_state"] = cm
+    check(cuda_lib, w, inp, path=3 if T <= 8 else 0)

@@ -393,6 +393,23 @@ def test_h3_history_sequential_single_tokens():
         assert_bits_equal(st[slot], whole["conv_state"][slot, :, T - 1:T - 1 + R], f"seq {s} final window")
 
 
+def test_h4_column_major_rows_are_storage_only():
+    """The state rows' storage order is not part of the method: the oracle run on column-major
+    rows ([n_slots, S, dim] seen transposed) writes the same values as on row-major rows, and
+    leaves the column-major storage column-major."""
+    w = small(n_seq=4, T=5, width=4, dtype="bf16", layout="history", state_offset=True)
+    inp = wl.make_inputs(w)
+    ref = run_oracle_verify(w, inp)
+    cm = clone_inputs(inp)
+    st = torch.empty((w.n_slots, w.state_cols, w.dim), dtype=w.torch_dtype).transpose(1, 2)
+    st.copy_(inp["conv_state"])
+    cm["conv_state"] = st
+    got = run_oracle_verify(w, cm)
+    assert got["conv_state"].stride(1) == 1
+    assert_bits_equal(got["conv_state"], ref["conv_state"], "state rows")
+    assert_bits_equal(got["out"], ref["out"], "out")
+
+
 @pytest.mark.parametrize("width", [2, 3, 4])
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 def test_r1_recompute_verify_writes_outputs_only(width, dtype):
