@@ -613,13 +613,23 @@ __global__ void __launch_bounds__(128, (CPT == 4 && TS <= 8) ? 4 : 2) verify_pip
                     }
                 }
             } else {
-                // a chunk of a longer draft: element by element, channel-major
+                // a chunk of a longer draft: element by element, channel-major, consecutive threads
+                // on consecutive elements; element i = (channel i / cnt, column i % cnt), stepped
+                // by the block size without a division per element
                 using U = std::conditional_t<ESS == 2, unsigned short, unsigned>;
                 const U *ie = reinterpret_cast<const U *>(img);
                 U *de = reinterpret_cast<U *>(row_dst);
-                for (int i = tid; i < nch * cnt; i += (int)blockDim.x) {
-                    const int cc = i / cnt, q2 = i - cc * cnt;
+                const int nthr = (int)blockDim.x;
+                const int dcc = nthr / cnt, dq = nthr - dcc * cnt;
+                int cc = tid / cnt, q2 = tid - cc * cnt;
+                for (int i = tid; i < nch * cnt; i += nthr) {
                     de[(long long)cc * Qrow + qd + q2] = ie[cc * Q + qs + q2];
+                    cc += dcc;
+                    q2 += dq;
+                    if (q2 >= cnt) {
+                        q2 -= cnt;
+                        ++cc;
+                    }
                 }
             }
         }
