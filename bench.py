@@ -691,6 +691,56 @@ def run_probe_mix(args):
     return 0
 
 
+def run_probe_link(args):
+    """Host-link rate of the end-to-end copies: the benchmark workload's upload (x) and download (out)
+    sizes between pinned host buffers and the device, by the copy engines as the end-to-end loop
+    issues them, each direction alone and both at once on two streams, K copies back to back between
+    two CUDA events.  Prints one JSON line per case."""
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    w = wl.WORKLOADS[wl.BENCH_WORKLOAD]
+    n = w.n_seq * w.T * w.dim * w.esize  # x rows up, out rows down
+    hs = [torch.empty(n, dtype=torch.uint8).pin_memory() for _ in range(2)]
+    ho = [torch.empty(n, dtype=torch.uint8).pin_memory() for _ in range(2)]
+    ds = [torch.empty(n, dtype=torch.uint8, device=dev) for _ in range(2)]
+    do = [torch.empty(n, dtype=torch.uint8, device=dev) for _ in range(2)]
+    up, down = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+
+    def h2d(i):
+        with torch.cuda.stream(up):
+            ds[i % 2].copy_(hs[i % 2], non_blocking=True)
+
+    def d2h(i):
+        with torch.cuda.stream(down):
+            ho[i % 2].copy_(do[i % 2], non_blocking=True)
+
+    def both(i):
+        h2d(i)
+        d2h(i)
+
+    for name, fn, dirs in (("h2d", h2d, 1), ("d2h", d2h, 1), ("both", both, 2)):
+        for i in range(max(args.warmup, 3)):
+            fn(i)
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        cur = torch.cuda.current_stream(dev)
+        e0.record(cur)
+        up.wait_event(e0)
+        down.wait_event(e0)
+        for i in range(args.steps):
+            fn(i)
+        for st in (up, down):
+            ev = torch.cuda.Event()
+            ev.record(st)
+            cur.wait_event(ev)
+        e1.record(cur)
+        torch.cuda.synchronize(dev)
+        us = e0.elapsed_time(e1) * 1e3 / args.steps
+        print(json.dumps({"probe": "link", "copies": name, "bytes_per_direction": n, "us_per_step": round(us, 2),
+                          "gbs_per_direction": round(n / us / 1e3, 1), "steps": args.steps}), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -709,11 +759,15 @@ def main():
     ap.add_argument("--probe-mb", default="75.4", help="MB moved per probe launch (comma list)")
     ap.add_argument("--probe-bpsm", default="8", help="probe blocks of 256 threads per SM (comma list)")
     ap.add_argument("--probe-mixes", default="", help="read:write mixes to time, e.g. 10:19,1:1 (default: all)")
+    ap.add_argument("--probe-link", action="store_true",
+                    help="time the end-to-end copies' host-link rate (the e2e number's ceiling) instead of the path")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     if args.probe_mix:
         return run_probe_mix(args)
+    if args.probe_link:
+        return run_probe_link(args)
     if args.gpus < 1:
         ap.error("--gpus must be at least 1")
     if "WORLD_SIZE" not in os.environ and args.gpus > 1:
