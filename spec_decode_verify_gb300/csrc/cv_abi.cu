@@ -340,7 +340,7 @@ int plan_verify(const cv_verify_args *a, cv_launch_plan *pl) {
         long long image = (hist || recomp) ? 0 : part((wide ? a->state_cols : R) * bc * ssize);
         if (a->window_layout == CV_WINDOW_DEDUP || hist) image += part(Q * bc * ssize);
         const long long smem = 2 * stage + 2 * image + cvk::kPipeInfoBytes +
-                               (pipe_compacts(a) ? 4LL * cvk::pipe_aux_ints(varlen, ts) + 4LL * pipe_list_len(a) : 0);
+                               (pipe_compacts(a) ? 4LL * cvk::pipe_aux_ints(varlen, ts) + (varlen ? 4LL : 12LL) * pipe_list_len(a) : 0);
         int per_sm = (int)(lim.smem_per_sm / (smem + kSmemPerBlockReserved));
         if (per_sm > pipe_blocks_per_sm(cpt, ts)) per_sm = pipe_blocks_per_sm(cpt, ts);
         const int nst = (smem <= lim.smem_per_block && per_sm >= 1) ? 2 : 0;

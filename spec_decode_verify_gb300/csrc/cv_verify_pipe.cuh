@@ -133,7 +133,10 @@ __global__ void __launch_bounds__(128, (CPT == 4 && TS <= 8) ? 4 : 2) verify_pip
     int *const act = wcount + AUX;
     const bool compact = p.compact != 0;
     const long long list_len = VL ? (long long)p.n_seq * ((p.T + TS - 1) / TS) : p.n_seq;
-    if (2 * stage_bytes + 2 * img_bytes + kPipeInfoBytes + (compact ? 4LL * AUX + 4LL * list_len : 0) >
+    // (whole batches: each listed sequence's cache slot and state offset, read while listing)
+    int *const act_slot = act + list_len;
+    int *const act_off = act_slot + list_len;
+    if (2 * stage_bytes + 2 * img_bytes + kPipeInfoBytes + (compact ? 4LL * AUX + (VL ? 4 : 12) * list_len : 0) >
         (long long)dynamic_smem_bytes())
         return;  // launch mismatch
 
@@ -156,7 +159,9 @@ __global__ void __launch_bounds__(128, (CPT == 4 && TS <= 8) ? 4 : 2) verify_pip
         n_act = 0;
         for (int i0 = 0; i0 < p.n_seq; i0 += (int)blockDim.x) {
             const int i = i0 + tid;
-            const bool a = i < p.n_seq && __ldg(p.cache_idx + i) >= 0;
+            const int sl = i < p.n_seq ? __ldg(p.cache_idx + i) : -1;
+            const int of = (i < p.n_seq && p.state_off) ? __ldg(p.state_off + i) : 0;
+            const bool a = sl >= 0;
             const unsigned m = __ballot_sync(0xffffffffu, a);
             if (lane == 0) wcount[warp] = __popc(m);
             __syncthreads();
@@ -166,7 +171,12 @@ __global__ void __launch_bounds__(128, (CPT == 4 && TS <= 8) ? 4 : 2) verify_pip
                 before += w < warp ? cw : 0;
                 total += cw;
             }
-            if (a) act[n_act + before + __popc(m & ((1u << lane) - 1u))] = i;
+            if (a) {
+                const int pos = n_act + before + __popc(m & ((1u << lane) - 1u));
+                act[pos] = i;
+                act_slot[pos] = sl;
+                act_off[pos] = of;
+            }
             n_act += total;
             __syncthreads();
         }
@@ -195,9 +205,15 @@ __global__ void __launch_bounds__(128, (CPT == 4 && TS <= 8) ? 4 : 2) verify_pip
     };
     auto load_index = [&](int k, UnitIdx &ix) {
         if (k >= iters) return;
-        const int s = seq_at(((int)blockIdx.x + k * (int)gridDim.x) / nblk) & 0xffff;
-        ix.slot = p.cache_idx ? __ldg(p.cache_idx + s) : s;
-        ix.off = p.state_off ? __ldg(p.state_off + s) : 0;
+        const int q = ((int)blockIdx.x + k * (int)gridDim.x) / nblk;
+        const int s = seq_at(q) & 0xffff;
+        if (!VL && compact) {  // (read while listing)
+            ix.slot = act_slot[q];
+            ix.off = act_off[q];
+        } else {
+            ix.slot = p.cache_idx ? __ldg(p.cache_idx + s) : s;
+            ix.off = p.state_off ? __ldg(p.state_off + s) : 0;
+        }
         if constexpr (VL) {
             ix.b = __ldg(p.cu_draft + s);
             ix.e = __ldg(p.cu_draft + s + 1);

@@ -70,10 +70,11 @@ W3 = wl.WORKLOADS["n128_t8_dim10240_w4_bf16_dedup_pad13"]
 def _pipe_smem(stage, image, n_seq, varlen_T=None):
     """The pipelined kernel's shared memory: two stages, two image buffers, 48 bytes of barriers and
     unit information (slots, offsets, draft counts, first rows), then the listing scratch (4 warp
-    counts; for packed drafts 5 * (TS + 2) sort counts, TS = min(T, 8) tokens per unit) and 4 bytes
-    per list entry (a sequence; for packed drafts a chunk of TS tokens of one)."""
+    counts; for packed drafts 5 * (TS + 2) sort counts, TS = min(T, 8) tokens per unit) and the list:
+    12 bytes per sequence (its index, cache slot and state offset), or for packed drafts 4 bytes per
+    chunk of TS tokens."""
     if varlen_T is None:
-        return 2 * stage + 2 * image + 48 + 4 * 4 + 4 * n_seq
+        return 2 * stage + 2 * image + 48 + 4 * 4 + 12 * n_seq
     ts = min(varlen_T, 8)
     return 2 * stage + 2 * image + 48 + 4 * 5 * (ts + 2) + 4 * n_seq * ((varlen_T + ts - 1) // ts)
 
@@ -231,10 +232,10 @@ def test_plan_sequence_list_only_with_cache_indices(lib):
     base = _plan(lib, a)[1]
     a.cache_idx = None
     pl = _plan(lib, a)[1]
-    assert pl.stages == base.stages and pl.smem_bytes == base.smem_bytes - 16 - 4 * 128
+    assert pl.stages == base.stages and pl.smem_bytes == base.smem_bytes - 16 - 12 * 128
     a = _args(W3.replace(n_seq=1025, n_pad=0))
     pl = _plan(lib, a)[1]
-    assert pl.path == 3 and pl.stages == base.stages and pl.smem_bytes == base.smem_bytes - 16 - 4 * 128
+    assert pl.path == 3 and pl.stages == base.stages and pl.smem_bytes == base.smem_bytes - 16 - 12 * 128
 
 
 def test_plan_general_path_cases(lib):
