@@ -409,6 +409,11 @@ __device__ __forceinline__ void bulk_load(void *sdst, const void *gsrc, unsigned
                  : "memory");
 }
 
+// L2 prefetch hint of `bytes` (a multiple of 16) from a 16-byte-aligned global address.
+__device__ __forceinline__ void bulk_prefetch_l2(const void *gsrc, unsigned bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;\n" ::"l"(gsrc), "r"(bytes) : "memory");
+}
+
 __device__ __forceinline__ void cp_async16(void *smem, const void *gmem) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(smem_u32(smem)), "l"(gmem) : "memory");
 }

@@ -75,8 +75,7 @@ __host__ __device__ constexpr long long pipe_part(long long b) { return (b + 127
 
 template <typename B, int W, int TS, int CPT, typename S = B, bool VL = false>
 __global__ void __launch_bounds__(128, (CPT == 4 && TS <= 8) ? 4 : 2) verify_pipe(const __grid_constant__ VerifyParams p) {
-    grid_dep_wait();
-    grid_dep_launch();
+    // (griddepcontrol.wait comes after the L2 prefetch hints below: nothing before it reads data)
     static_assert(TS > 0, "the pipelined kernel needs a compile-time T");
     static_assert(!VL || std::is_same_v<B, S>, "packed ragged drafts use one dtype");
     // (taps and bias are read from global memory, so W*CPT*ES need only be 8-byte aligned)
@@ -139,6 +138,28 @@ __global__ void __launch_bounds__(128, (CPT == 4 && TS <= 8) ? 4 : 2) verify_pip
     if (2 * stage_bytes + 2 * img_bytes + kPipeInfoBytes + (compact ? 4LL * AUX + (VL ? 4 : 12) * list_len : 0) >
         (long long)dynamic_smem_bytes())
         return;  // launch mismatch
+
+    // Before waiting for the previous grid: L2 prefetch hints for the x rows and state rows of the
+    // block's first two units, taking unit u as sequence u / nblk (as if no sequence were padded).
+    // The cache slot is read through L2 only (never cached in L1), and only to form a hint's
+    // address, which stays inside the state buffer; all data is read after the wait, so a hint that
+    // is stale or misses costs only its bandwidth.
+    if (!VL && tid == 0) {
+        for (int k = 0; k < 2; ++k) {
+            const long long u = (long long)blockIdx.x + (long long)k * gridDim.x;
+            if (u >= (long long)p.n_seq * nblk) break;
+            const int s = (int)(u / nblk), c0 = (int)(u - (long long)s * nblk) * BC;
+            const int nch = min(BC, p.dim - c0);
+            const B *xs = reinterpret_cast<const B *>(p.x) + (long long)s * p.x_seq + c0;
+            for (int t = 0; t < TS; ++t) bulk_prefetch_l2(xs + (long long)t * p.x_tok, (unsigned)(nch * ES));
+            const int slot = p.cache_idx ? __ldcg(p.cache_idx + s) : s;
+            if (slot >= 0 && slot < p.n_slots && !hist_t)
+                bulk_prefetch_l2(reinterpret_cast<const S *>(p.state) + (long long)slot * p.st_slot + (long long)c0 * SC,
+                                 (unsigned)(nch * SC * ESS));
+        }
+    }
+    grid_dep_wait();
+    grid_dep_launch();
 
     if (tid == 0) {
         mbar_init(&bar[0], 1);
