@@ -413,6 +413,13 @@ __device__ __forceinline__ void bulk_load(void *sdst, const void *gsrc, unsigned
 __device__ __forceinline__ void bulk_prefetch_l2(const void *gsrc, unsigned bytes) {
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;\n" ::"l"(gsrc), "r"(bytes) : "memory");
 }
+// L2 prefetch hints for n runs of `bytes` bytes, `stride` bytes apart, from `base`, when every run
+// starts on a 16-byte boundary and is a multiple of 16 bytes (else nothing: hints only).
+__device__ __forceinline__ void prefetch_runs_l2(const void *base, long long stride, int n, long long bytes) {
+    if ((reinterpret_cast<uintptr_t>(base) & 15u) || (stride & 15) || (bytes & 15) || bytes <= 0) return;
+    const unsigned char *b = reinterpret_cast<const unsigned char *>(base);
+    for (int i = 0; i < n; ++i) bulk_prefetch_l2(b + (long long)i * stride, (unsigned)bytes);
+}
 
 __device__ __forceinline__ void cp_async16(void *smem, const void *gmem) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(smem_u32(smem)), "l"(gmem) : "memory");

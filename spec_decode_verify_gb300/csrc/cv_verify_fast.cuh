@@ -42,6 +42,19 @@ __host__ __device__ constexpr int chunk_align(int bytes) { return bytes % 16 == 
 
 template <typename B, int W, int TS, int CPT>
 __global__ void __launch_bounds__(256) verify_fast(const __grid_constant__ VerifyParams p) {
+    // Before waiting for the previous grid: L2 prefetch hints for the block's x rows and state run.
+    // The cache slot is read through L2 only and only to form a hint's address (inside the state
+    // buffer); all data is read after the wait.
+    if (threadIdx.x == 0) {
+        const int bc = CPT * (int)blockDim.x, cb0 = (int)blockIdx.x * bc, sq = (int)blockIdx.y;
+        const int n = min(bc, p.dim - cb0), es = (int)sizeof(B);
+        prefetch_runs_l2(reinterpret_cast<const B *>(p.x) + (long long)sq * p.x_seq + cb0, p.x_tok * es,
+                         TS > 0 ? TS : p.T, (long long)n * es);
+        const int sl = p.cache_idx ? __ldcg(p.cache_idx + sq) : sq;
+        if (sl >= 0 && sl < p.n_slots && (p.st_vec || p.st_rows))
+            prefetch_runs_l2(reinterpret_cast<const B *>(p.state) + (long long)sl * p.st_slot + (long long)cb0 * p.state_cols,
+                             0, 1, (long long)n * p.state_cols * es);
+    }
     grid_dep_wait();
     grid_dep_launch();
     constexpr int R = W - 1;                  // committed window columns
