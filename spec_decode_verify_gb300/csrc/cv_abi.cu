@@ -41,7 +41,7 @@ constexpr int kCommitRecomputeThreads = 64;  // recompute rollback
 // dedup commit: 256 channels per block (small blocks fit beside the verify's resident blocks, so
 // more of them start, under programmatic dependent launch, while the verify drains)
 constexpr int kCommitRowThreads = 32;
-constexpr int kCommitColThreads = 128;  // transposed dedup rows: 1024 channels per block
+constexpr int kCommitColThreads = 64;  // transposed dedup rows: 512 channels per block (measured: 4.4 us alone against 5.1 with 128)
 // the pipelined kernel lists the active sequences (or packed drafts' chunks) in shared memory up to
 // this many entries
 constexpr int kCompactMaxEntries = 1024;
