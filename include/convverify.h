@@ -51,7 +51,7 @@ extern "C" {
 #define CV_API
 #endif
 
-#define CV_ABI_VERSION 7
+#define CV_ABI_VERSION 8
 #define CV_MAX_T 128 /* draft tokens per verify call */
 
 typedef enum cv_dtype {
@@ -370,6 +370,7 @@ CV_API int cv_conv_prefill(const cv_prefill_args *args, void *stream);
 typedef struct cv_launch_plan {
     int32_t grid_x, grid_y, threads, smem_bytes, channels_per_block, path;
     int32_t stages; /* paths 3 and 5: unit buffers per block (loads in flight); 0 otherwise */
+    int32_t token_groups; /* path 2: thread groups splitting the draft tokens (the block's y size); 1 otherwise */
 } cv_launch_plan;
 
 CV_API int cv_verify_plan(const cv_verify_args *args, cv_launch_plan *plan);

@@ -74,7 +74,7 @@ class PrefillArgs(ctypes.Structure):
 class LaunchPlan(ctypes.Structure):
     """Mirror of cv_launch_plan."""
     _fields_ = [("grid_x", c_i32), ("grid_y", c_i32), ("threads", c_i32), ("smem_bytes", c_i32),
-                ("channels_per_block", c_i32), ("path", c_i32), ("stages", c_i32)]
+                ("channels_per_block", c_i32), ("path", c_i32), ("stages", c_i32), ("token_groups", c_i32)]
 
 
 class CvError(RuntimeError):

@@ -24,6 +24,9 @@
 namespace {
 
 constexpr int kFastThreads = 128;
+constexpr int kFastThreadsMax = 256;   // the one-pass kernel's launch bound (threads x token groups)
+constexpr int kMaxTokenGroups = 4;     // token groups of the chunked one-pass kernel, at most
+constexpr int kFastMinWarpsPerSM = 8;  // below this the chunked one-pass kernel splits the tokens
 constexpr int kPipeThreads = 128;
 constexpr long long kFastRowsMaxBytes = 64 * 1024;  // staged wide state rows of a one-pass block
 // blocks per SM the pipelined kernel's launch bounds provide registers for
@@ -261,6 +264,7 @@ int plan_verify(const cv_verify_args *a, cv_launch_plan *pl) {
     const int R = a->width - 1;
     const DeviceLimits lim = device_limits();
     std::memset(pl, 0, sizeof *pl);
+    pl->token_groups = 1;
     if (a->parent) {
         // tree verify: its own persistent kernel of kTreeWarps-warp blocks walking (sequence,
         // kTreeChannels channels) units; two unit buffers (the next unit loads while this one
@@ -290,6 +294,7 @@ int plan_verify(const cv_verify_args *a, cv_launch_plan *pl) {
         (a->qk_channels > 0 && a->head_dim / 8 > kMinThreads) ? a->head_dim / 8 : kMinThreads;
     const cvk::KernelSet &ks = kernel_set(a->dtype, a->width);
     std::memset(pl, 0, sizeof *pl);
+    pl->token_groups = 1;
 
     const bool hist = a->window_layout == CV_WINDOW_HISTORY;
     const bool recomp = a->window_layout == CV_WINDOW_RECOMPUTE;
@@ -371,10 +376,21 @@ int plan_verify(const cv_verify_args *a, cv_launch_plan *pl) {
         // committed-window image, or the staged wide rows
         long long smem = bc * (fast_rows_staged(a, ssize, bc) ? a->state_cols : R) * esize;
         if (a->window_layout == CV_WINDOW_DEDUP) smem += bc * (a->T + R - 1) * esize;
+        // Small dense batches: split the draft tokens among thread groups (the chunked kernel, the
+        // block's y dimension) while the launch would hold fewer than kFastMinWarpsPerSM warps per
+        // SM, each group keeping at least W-1 tokens (its first W-1 inputs are the x rows before it)
+        int groups = 1;
+        if (a->window_layout == CV_WINDOW_DENSE) {
+            const long long warps = (long long)a->n_seq * ((a->dim + bc - 1) / bc) * ((threads + 31) / 32);
+            while (groups < kMaxTokenGroups && threads * groups * 2 <= kFastThreadsMax &&
+                   warps * groups < (long long)kFastMinWarpsPerSM * lim.sms && (a->T + 2 * groups - 1) / (2 * groups) >= R)
+                groups *= 2;
+        }
         pl->threads = threads;
         pl->channels_per_block = (int)bc;
         pl->smem_bytes = (int)smem;
-        pl->path = a->T <= ks.max_static_t ? 1 : 2;
+        pl->path = (a->T <= ks.max_static_t && groups == 1) ? 1 : 2;
+        pl->token_groups = groups;
     } else {
         // (with mixed dtypes the tile holds fp32 bits)
         const int tsize = mixed ? 4 : esize;
@@ -402,11 +418,11 @@ int plan_verify(const cv_verify_args *a, cv_launch_plan *pl) {
 // grid in the stream finishes; every kernel waits (griddepcontrol.wait) for that grid's completion
 // before its first global-memory access, so the order of the stream's work is kept.
 template <typename P>
-cudaError_t launch_pdl(void (*kernel)(P), dim3 grid, int threads, int smem, cudaStream_t stream, const P &p) {
+cudaError_t launch_pdl(void (*kernel)(P), dim3 grid, dim3 block, int smem, cudaStream_t stream, const P &p) {
     cudaLaunchConfig_t cfg;
     std::memset(&cfg, 0, sizeof cfg);
     cfg.gridDim = grid;
-    cfg.blockDim = dim3(threads);
+    cfg.blockDim = block;
     cfg.dynamicSmemBytes = (size_t)smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
@@ -515,7 +531,8 @@ int launch_verify(const cv_verify_args *a, const cv_launch_plan &pl, cudaStream_
     // the pipelined kernel ORs the per-sequence bits into err (several blocks share a sequence)
     if (pl.path == 3 && a->err && cudaMemsetAsync(a->err, 0, sizeof(int32_t) * (size_t)a->n_seq, stream) != cudaSuccess)
         return CV_ERR_LAUNCH;
-    if (launch_pdl(k, dim3(pl.grid_x, pl.grid_y), pl.threads, pl.smem_bytes, stream, p) != cudaSuccess)
+    if (launch_pdl(k, dim3(pl.grid_x, pl.grid_y), dim3(pl.threads, pl.token_groups > 1 ? pl.token_groups : 1),
+                   pl.smem_bytes, stream, p) != cudaSuccess)
         return CV_ERR_LAUNCH;
     return cudaGetLastError() == cudaSuccess ? CV_OK : CV_ERR_LAUNCH;
 }

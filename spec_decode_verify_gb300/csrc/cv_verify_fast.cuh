@@ -25,7 +25,12 @@
 //      head_dim/CPT lanes (glm5next_kda mod.rs: SiLU after the conv, then L2 on q and k alone,
 //      eps inside the root); one rounding to the output type; vector stores.
 // T is a template parameter for T <= 17 (bf16) / 8 (fp32), which unrolls the token loop and makes
-// the row permutation static; TS = 0 runs any T with a dense window in unrolled chunks of 4.
+// the row permutation static; TS = 0 runs any T with a dense window in unrolled chunks of 4, and
+// may split the tokens among blockDim.y thread groups (small batches, where one group per block
+// would leave the SMs with too few warps): group g takes tokens [g*TH, min(T, (g+1)*TH)), TH =
+// ceil(T / groups), starting from the W-1 x rows before them (group 0: the committed window); the
+// group holding token T-1 writes the committed window.  Each warp stays within one group, so the
+// L2 shuffles see one token's channels.
 // Preconditions (checked on the host): dim % 8 == 0; x, out, weight, bias, window 16-byte aligned
 // with 16-byte-multiple strides; window packed (dense [.., T, dim, W-1] or dedup [.., dim, T+W-2]
 // with unit column stride); TS = 0 only with the dense layout; head_dim / CPT <= 32.
@@ -45,7 +50,7 @@ __global__ void __launch_bounds__(256) verify_fast(const __grid_constant__ Verif
     // Before waiting for the previous grid: L2 prefetch hints for the block's x rows and state run.
     // The cache slot is read through L2 only and only to form a hint's address (inside the state
     // buffer); all data is read after the wait.
-    if (threadIdx.x == 0) {
+    if (threadIdx.x == 0 && threadIdx.y == 0) {
         const int bc = CPT * (int)blockDim.x, cb0 = (int)blockIdx.x * bc, sq = (int)blockIdx.y;
         const int n = min(bc, p.dim - cb0), es = (int)sizeof(B);
         prefetch_runs_l2(reinterpret_cast<const B *>(p.x) + (long long)sq * p.x_seq + cb0, p.x_tok * es,
@@ -69,12 +74,13 @@ __global__ void __launch_bounds__(256) verify_fast(const __grid_constant__ Verif
 
     const int s = blockIdx.y;
     const int tid = threadIdx.x;
+    const bool lead = threadIdx.x == 0 && threadIdx.y == 0;  // issues the block's bulk copies
     const int BC = CPT * blockDim.x;
     const int c0 = blockIdx.x * BC;
     const int slot = p.cache_idx ? __ldg(p.cache_idx + s) : s;
     const int off = p.state_off ? __ldg(p.state_off + s) : 0;
     const int status = seq_status(slot, off, p.n_slots, p.state_cols, R);
-    if (p.err && blockIdx.x == 0 && tid == 0) p.err[s] = status;
+    if (p.err && blockIdx.x == 0 && lead) p.err[s] = status;
     if (slot < 0 || status) return;  // padded or rejected: nothing is written (block-uniform)
 
     const int nch = min(BC, p.dim - c0);  // a multiple of 8 on this path
@@ -83,6 +89,11 @@ __global__ void __launch_bounds__(256) verify_fast(const __grid_constant__ Verif
     const int c = c0 + cl;
     const int T = TS > 0 ? TS : p.T;
     const bool dense = !p.dedup;
+    // token groups (TS = 0 only): this thread's group takes tokens [tb, te)
+    const int G = TS > 0 ? 1 : (int)blockDim.y, g = TS > 0 ? 0 : (int)threadIdx.y;
+    const int TH = (T + G - 1) / G;
+    const int tb = min(T, g * TH), te = min(T, tb + TH);
+    const bool last_group = tb < te && te == T;  // holds token T-1: writes the committed window
     // shared memory: [dedup image: BC x (TS+W-2)] then the state part: the committed-window image
     // (BC x (W-1)) or, for staged wide rows, the rows themselves (BC x state_cols)
     const bool rows = p.st_rows;  // block-uniform
@@ -91,7 +102,7 @@ __global__ void __launch_bounds__(256) verify_fast(const __grid_constant__ Verif
     if (img_bytes + (long long)BC * (rows ? SC : R) * ES > (long long)dynamic_smem_bytes()) return;  // launch mismatch
     unsigned char *st_img = smem + img_bytes;
     B *const st_blk = reinterpret_cast<B *>(p.state) + (long long)slot * p.st_slot + (long long)c0 * SC;
-    if (rows) {
+    if (rows && g == 0) {
         // the block's [nch][SC] rows: contiguous, 16-byte aligned, a multiple of 16 bytes (host-checked)
         const int nbytes = nch * SC * ES;
         for (int o = tid * 16; o < nbytes; o += (int)blockDim.x * 16)
@@ -108,7 +119,16 @@ __global__ void __launch_bounds__(256) verify_fast(const __grid_constant__ Verif
     for (int e = 0; e < CPT; ++e)
 #pragma unroll
         for (int k = 0; k < R; ++k) fw[e][k] = 0.0f;
-    if (act && !rows) {
+    if (act && g > 0) {
+        // a later token group starts from the W-1 x rows before its first token (tb >= W-1, host)
+#pragma unroll
+        for (int k = 0; k < R; ++k) {
+            uint32_t hw[NW];
+            ldv<VX, NW>(hw, xs + (long long)(tb - R + k) * p.x_tok);
+#pragma unroll
+            for (int e = 0; e < CPT; ++e) fw[e][k] = elem_f<B>(hw, e);
+        }
+    } else if (act && !rows) {
         if (p.st_vec) {  // packed [dim][R] rows (then the offset is 0)
             uint32_t sw[R * NW];
             ldv<VS, R * NW>(sw, st_row);
@@ -129,10 +149,10 @@ __global__ void __launch_bounds__(256) verify_fast(const __grid_constant__ Verif
         for (int u = 0; u < TC; ++u) {
 #pragma unroll
             for (int i = 0; i < NW; ++i) xr[u][i] = 0u;
-            if (act && (TS > 0 || t0 + u < T)) ldv<VX, NW>(xr[u], xs + (long long)(t0 + u) * p.x_tok);
+            if (act && (TS > 0 || t0 + u < te)) ldv<VX, NW>(xr[u], xs + (long long)(t0 + u) * p.x_tok);
         }
     };
-    load_chunk(0);
+    load_chunk(tb);
 
     float wt[CPT][W];
     float bs[CPT];
@@ -160,12 +180,14 @@ __global__ void __launch_bounds__(256) verify_fast(const __grid_constant__ Verif
     if (rows) {
         cp_async_wait_all();
         __syncthreads();
-        if (act) {
+        if (act && g == 0) {
 #pragma unroll
             for (int e = 0; e < CPT; ++e)
 #pragma unroll
                 for (int k = 0; k < R; ++k) fw[e][k] = widen<B>(srow_img[e * SC + off + k]);
         }
+        // (the last group writes the new window over the rows' first columns later)
+        if (G > 1) __syncthreads();
     }
 
     B *wseq = reinterpret_cast<B *>(p.win) + (long long)s * p.w_seq;
@@ -295,7 +317,7 @@ __global__ void __launch_bounds__(256) verify_fast(const __grid_constant__ Verif
         if (bulk) {
             fence_smem_to_async();
             __syncthreads();
-            if (tid == 0) {
+            if (lead) {
                 if (!dense) bulk_store(wseq + (long long)c0 * Q, smem, (unsigned)(nch * Q * ES));
                 if (p.st_vec || rows) bulk_store(st_blk, st_img, (unsigned)(nch * SC * ES));
                 asm volatile("cp.async.bulk.commit_group;\n" ::: "memory");
@@ -309,15 +331,15 @@ __global__ void __launch_bounds__(256) verify_fast(const __grid_constant__ Verif
 #pragma unroll
         for (int u = 0; u < TS; ++u) store_token(u, y[u]);
     } else {
-        // chunked: any T, dense window
+        // chunked: any T, dense window; this group's tokens [tb, te)
         uint32_t fin[R * NW];
 #pragma unroll
         for (int i = 0; i < R * NW; ++i) fin[i] = 0u;
-        for (int t0 = 0; t0 < T; t0 += TC) {
-            if (t0 > 0) load_chunk(t0);
+        for (int t0 = tb; t0 < te; t0 += TC) {
+            if (t0 > tb) load_chunk(t0);
 #pragma unroll
             for (int u = 0; u < TC; ++u) {
-                if (t0 + u < T) {
+                if (t0 + u < te) {
                     if (act) write_snapshot(t0 + u, u + 1);
                     if (t0 + u == T - 1) window_words(u + 1, fin);
                 }
@@ -325,29 +347,29 @@ __global__ void __launch_bounds__(256) verify_fast(const __grid_constant__ Verif
             float y[TC][CPT];
 #pragma unroll
             for (int u = 0; u < TC; ++u)
-                if (t0 + u < T) conv_token(u, y[u]);
+                if (t0 + u < te) conv_token(u, y[u]);
             l2_tokens(y, std::integral_constant<int, TC>{});
 #pragma unroll
             for (int u = 0; u < TC; ++u)
-                if (t0 + u < T) store_token(t0 + u, y[u]);
+                if (t0 + u < te) store_token(t0 + u, y[u]);
 #pragma unroll
             for (int e = 0; e < CPT; ++e)
 #pragma unroll
                 for (int k = 0; k < R; ++k) fw[e][k] = fw[e][TC + k];
         }
-        if (act) stage_state(fin);
+        if (act && last_group) stage_state(fin);
         bulk = p.st_vec || rows;
         if (bulk) {
             fence_smem_to_async();
             __syncthreads();
-            if (tid == 0) {
+            if (lead) {
                 bulk_store(st_blk, st_img, (unsigned)(nch * SC * ES));
                 asm volatile("cp.async.bulk.commit_group;\n" ::: "memory");
             }
         }
     }
     // the issuing thread keeps the block's shared memory alive until the bulk copies have read it
-    if (bulk && tid == 0) asm volatile("cp.async.bulk.wait_group.read 0;\n" ::: "memory");
+    if (bulk && lead) asm volatile("cp.async.bulk.wait_group.read 0;\n" ::: "memory");
 }
 
 }  // namespace cvk

@@ -185,7 +185,7 @@ def test_history_validation_and_paths(lib):
 
 @pytest.mark.parametrize("name,path", [
     ("n1_t2_dim512_w4_f32_dense", 1), ("n4_t4_dim4096_w4_bf16_dedup_bias", 1),
-    ("n8_t17_dim8192_w4_bf16_dense_qkvsplit_xstride12288", 1), ("n64_t8_dim6144_w3_bf16_dense_nol2_stateoff", 1),
+    ("n8_t17_dim8192_w4_bf16_dense_qkvsplit_xstride12288", 2), ("n64_t8_dim6144_w3_bf16_dense_nol2_stateoff", 1),
     ("n128_t8_dim10240_w4_bf16_history_pad13", 3), ("n128_t8_dim10240_w4_bf16_recompute_pad13", 3),
     ("n128_t8_dim10240_w4_bf16_tree_dense_pad13", 5), ("n128_t8_dim10240_w4_bf16x_f32state_dedup_pad13", 3)])
 def test_plan_paths_of_named_workloads(lib, name, path):
@@ -409,6 +409,26 @@ def test_mixed_dtypes_plan_and_validation(lib):
     rc, pl3 = _plan(lib, _args(w3))
     assert rc == 0 and pl3.path == 0
     assert pl3.smem_bytes == (9 + 3) * (8 * pl3.threads + 4) * 4
+
+
+def test_plan_token_groups(lib):
+    """Small dense batches split the draft tokens among thread groups of the chunked one-pass kernel
+    (path 2) while fewer than 8 warps per SM would run, each group keeping at least W-1 tokens and
+    a block at most 256 threads; other layouts and large batches keep one group."""
+    w4 = wl.WORKLOADS["n8_t17_dim8192_w4_bf16_dense_qkvsplit_xstride12288"]
+    rc, pl = _plan(lib, _args(w4))
+    # 8 x 64 blocks of one warp = 512 warps < 8 x 152: 4 groups of ceil(17 / 4) = 5 tokens
+    assert rc == 0 and (pl.path, pl.threads, pl.token_groups) == (2, 32, 4)
+    rc, pl = _plan(lib, _args(w4.replace(T=5)))
+    assert (pl.path, pl.token_groups) == (2, 2)  # groups of 3 and 2 tokens (4 would hold 2 each)
+    rc, pl = _plan(lib, _args(w4.replace(T=4)))
+    assert (pl.path, pl.token_groups) == (1, 1)  # 2 groups would hold 2 tokens each
+    rc, pl = _plan(lib, _args(w4.replace(layout="dedup")))
+    assert pl.token_groups == 1
+    rc, pl = _plan(lib, _args(W3))
+    assert pl.token_groups == 1
+    rc, pl = _plan(lib, _args(wl.WORKLOADS["n64_t8_dim6144_w3_bf16_dense_nol2_stateoff"]))
+    assert (pl.path, pl.token_groups) == (1, 1)  # 64 x 12 blocks of 4 warps are enough
 
 
 def test_tree_plan_and_validation(lib):

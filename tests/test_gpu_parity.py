@@ -425,6 +425,28 @@ def test_wide_state_rows_unaligned(cuda_lib, layout, T):
     assert_out_close(d["out"].cpu(), ref["out"], "out")
 
 
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("T,width", [(5, 4), (6, 3), (9, 2), (17, 4), (24, 4), (40, 3), (128, 4)])
+@pytest.mark.parametrize("offset", [False, True])
+def test_token_groups_one_pass(cuda_lib, dtype, T, width, offset):
+    """Small dense batches on the chunked one-pass kernel with the draft tokens split among thread
+    groups: a later group starts from the x rows before its first token, only the group holding
+    token T-1 writes the state; wide rows read at per-sequence offsets, padded rows, a partial last
+    channel block, L2 groups of 64 channels."""
+    w = wl.VerifyWorkload("tgroups", n_seq=3, T=T, dim=1000, width=width, qk_channels=512, head_dim=64,
+                          dtype=dtype, layout="dense", bias=True, n_pad=1, extra_slots=2, state_offset=offset,
+                          seed=7 * T + width + (100 if offset else 0))
+    inp = wl.make_inputs(w)
+    if offset:
+        inp["state_off"] = (torch.arange(w.n_seq, dtype=torch.int32) % T).contiguous()
+    d = {k: (v.to("cuda") if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    pl = cuda_lib.verify_plan(d["x"], d["conv_state"], d["weight"], d["bias"], d["out"], d["window"], layout="dense",
+                              qk_channels=w.qk_channels, head_dim=w.head_dim, cache_idx=d["cache_idx"],
+                              state_off=d["state_off"])
+    assert pl.path == 2 and pl.token_groups > 1
+    check_verify_and_commit(cuda_lib, w, inp)
+
+
 def test_maximum_batch_on_gpu(cuda_lib):
     """The largest batch the ABI accepts (65535 sequences; the pipelined kernel then walks every
     sequence without a shared-memory list), with padded sequences and a pool of unused slots."""
