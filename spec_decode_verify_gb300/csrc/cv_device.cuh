@@ -236,6 +236,34 @@ __device__ __forceinline__ uint32_t halves(uint32_t a, int h0, uint32_t b, int h
 // Two raw 16-bit values -> one word (lo in the low half).  For fp32 only lo is used.
 __device__ __forceinline__ uint32_t pack_halves(uint32_t lo, uint32_t hi) { return __byte_perm(lo, hi, 0x5410); }
 
+// Two fp32 lanes in one 64-bit register.  The paired fp32 instructions (fma / mul / add .f32x2,
+// sm_100 and later) compute each lane exactly as the scalar instruction does (IEEE fp32, round to
+// nearest even) in one issue slot, so paired arithmetic gives the scalar results bit for bit.
+using f2 = unsigned long long;
+__device__ __forceinline__ f2 f2_pack(float lo, float hi) {
+    f2 r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void f2_unpack(f2 v, float &lo, float &hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ f2 f2_fma(f2 a, f2 b, f2 c) {
+    f2 d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ f2 f2_mul(f2 a, f2 b) {
+    f2 d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ f2 f2_add(f2 a, f2 b) {
+    f2 d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
 // SiLU(a) = a / (1 + exp(-a)).  silu_fast evaluates exp(-a) = 2^(-a * log2 e) with the
 // ex2.approx instruction and the quotient as a * rcp.approx(1 + exp(-a)); relative error a few
 // fp32 ulp.  Both instructions flush subnormals, which matters only below a = -87
@@ -249,6 +277,18 @@ __device__ __forceinline__ float silu_fast(float a) {
     return a * r;
 }
 __device__ __forceinline__ float silu_exact(float a) { return a / (1.0f + expf(-a)); }
+// silu_fast of two values in paired lanes: the same operations per lane, so the same bits.
+__device__ __forceinline__ f2 silu_fast2(f2 a) {
+    float t0, t1, e0, e1, r0, r1;
+    f2_unpack(f2_mul(a, f2_pack(-1.4426950408889634f, -1.4426950408889634f)), t0, t1);
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e0) : "f"(t0));
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e1) : "f"(t1));
+    float s0, s1;
+    f2_unpack(f2_add(f2_pack(1.0f, 1.0f), f2_pack(e0, e1)), s0, s1);
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r0) : "f"(s0));
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r1) : "f"(s1));
+    return f2_mul(a, f2_pack(r0, r1));
+}
 
 // SiLU of n values with one range check for the run (a branch realistic inputs never take); in
 // that branch only the values below -80 switch to the exact form, so the result equals silu()
@@ -287,6 +327,14 @@ template <typename B, int W>
 __device__ __forceinline__ float conv_chain(float acc, const float *w, const float *in) {
 #pragma unroll
     for (int j = 0; j < W; ++j) acc = sizeof(B) == 2 ? fmaf(w[j], in[j], acc) : __fadd_rn(acc, __fmul_rn(w[j], in[j]));
+    return acc;
+}
+
+// conv_chain for two channels at once (paired lanes), each lane bit for bit the scalar chain.
+template <typename B, int W>
+__device__ __forceinline__ f2 conv_chain2(f2 acc, const f2 *w, const f2 *in) {
+#pragma unroll
+    for (int j = 0; j < W; ++j) acc = sizeof(B) == 2 ? f2_fma(w[j], in[j], acc) : f2_add(acc, f2_mul(w[j], in[j]));
     return acc;
 }
 

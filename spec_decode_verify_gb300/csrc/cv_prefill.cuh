@@ -123,6 +123,17 @@ __global__ void __launch_bounds__(128, CPT == 4 ? 4 : 2) prefill_conv(const __gr
             }
         }
     };
+    // channels in pairs (paired fp32 lanes: the same operations per lane, half the instructions)
+    constexpr int P = CPT / 2;
+    f2 win2[P][R], wt2[P][W], bs2[P];
+#pragma unroll
+    for (int q = 0; q < P; ++q) {
+        bs2[q] = f2_pack(bs[2 * q], bs[2 * q + 1]);
+#pragma unroll
+        for (int k = 0; k < W; ++k) wt2[q][k] = f2_pack(wt[2 * q][k], wt[2 * q + 1][k]);
+#pragma unroll
+        for (int k = 0; k < R; ++k) win2[q][k] = f2_pack(win[2 * q][k], win[2 * q + 1][k]);
+    }
     uint32_t xn[U][NW];  // the next batch, in flight while this one is computed
     if (t0 < t1) load_batch(xn, t0);
     for (int tb = t0; tb < t1; tb += U) {
@@ -133,21 +144,37 @@ __global__ void __launch_bounds__(128, CPT == 4 ? 4 : 2) prefill_conv(const __gr
             for (int i = 0; i < NW; ++i) xr[u][i] = xn[u][i];
         if (tb + U < t1) load_batch(xn, tb + U);
         float y[U][CPT];
-        float acc[U][CPT];
+        f2 acc2[U][P];
+        float lo = 0.0f;
 #pragma unroll
         for (int u = 0; u < U; ++u)
 #pragma unroll
-            for (int j = 0; j < CPT; ++j) {
-                float in[W];
+            for (int q = 0; q < P; ++q) {
+                f2 in[W];
 #pragma unroll
-                for (int k = 0; k < R; ++k) in[k] = win[j][k];
-                in[R] = elem_f<B>(xr[u], j);
-                acc[u][j] = conv_chain<B, W>(bs[j], wt[j], in);
+                for (int k = 0; k < R; ++k) in[k] = win2[q][k];
+                in[R] = f2_pack(elem_f<B>(xr[u], 2 * q), elem_f<B>(xr[u], 2 * q + 1));
+                acc2[u][q] = conv_chain2<B, W>(bs2[q], wt2[q], in);
 #pragma unroll
-                for (int k = 0; k + 1 < R; ++k) win[j][k] = win[j][k + 1];
-                win[j][R - 1] = in[R];
+                for (int k = 0; k + 1 < R; ++k) win2[q][k] = win2[q][k + 1];
+                win2[q][R - 1] = in[R];
+                float a0, a1;
+                f2_unpack(acc2[u][q], a0, a1);
+                lo = fminf(lo, fminf(a0, a1));
+                f2_unpack(silu_fast2(acc2[u][q]), y[u][2 * q], y[u][2 * q + 1]);
             }
-        silu_run<U * CPT>(&acc[0][0], &y[0][0]);
+        if (lo < -80.0f) {
+            // only the values below -80 take the exact form (the same bits as silu())
+#pragma unroll
+            for (int u = 0; u < U; ++u)
+#pragma unroll
+                for (int q = 0; q < P; ++q) {
+                    float a0, a1;
+                    f2_unpack(acc2[u][q], a0, a1);
+                    if (a0 < -80.0f) y[u][2 * q] = silu_exact(a0);
+                    if (a1 < -80.0f) y[u][2 * q + 1] = silu_exact(a1);
+                }
+        }
         if (l2_block) {
             float ss[U];
 #pragma unroll
@@ -164,8 +191,10 @@ __global__ void __launch_bounds__(128, CPT == 4 ? 4 : 2) prefill_conv(const __gr
 #pragma unroll
                 for (int u = 0; u < U; ++u) {
                     const float r = rsqrtf(ss[u] + p.eps);
+                    const f2 r2 = f2_pack(r, r);
 #pragma unroll
-                    for (int j = 0; j < CPT; ++j) y[u][j] *= r;
+                    for (int q = 0; q < P; ++q)
+                        f2_unpack(f2_mul(f2_pack(y[u][2 * q], y[u][2 * q + 1]), r2), y[u][2 * q], y[u][2 * q + 1]);
                 }
             }
         }
