@@ -330,12 +330,30 @@ __device__ __forceinline__ float conv_chain(float acc, const float *w, const flo
     return acc;
 }
 
-// conv_chain for two channels at once (paired lanes), each lane bit for bit the scalar chain.
+// conv_chain for two channels at once (paired lanes), each lane bit for bit the scalar chain.  The
+// bf16 chain is paired fused multiply-adds.  The fp32 chain rounds each product before its add, so
+// it stays scalar: a paired multiply feeding a paired add may be contracted into a fused one by the
+// compiler (measured: the results then differed from the scalar chain), which the scalar .rn forms
+// rule out.
 template <typename B, int W>
 __device__ __forceinline__ f2 conv_chain2(f2 acc, const f2 *w, const f2 *in) {
+    if constexpr (sizeof(B) == 2) {
 #pragma unroll
-    for (int j = 0; j < W; ++j) acc = sizeof(B) == 2 ? f2_fma(w[j], in[j], acc) : f2_add(acc, f2_mul(w[j], in[j]));
-    return acc;
+        for (int j = 0; j < W; ++j) acc = f2_fma(w[j], in[j], acc);
+        return acc;
+    } else {
+        float a0, a1;
+        f2_unpack(acc, a0, a1);
+#pragma unroll
+        for (int j = 0; j < W; ++j) {
+            float w0, w1, x0, x1;
+            f2_unpack(w[j], w0, w1);
+            f2_unpack(in[j], x0, x1);
+            a0 = __fadd_rn(a0, __fmul_rn(w0, x0));
+            a1 = __fadd_rn(a1, __fmul_rn(w1, x1));
+        }
+        return f2_pack(a0, a1);
+    }
 }
 
 // Sum of squares of a thread's CPT (4 or 8) values in one fixed order: a chain over each run of 4

@@ -339,8 +339,11 @@ __global__ void __launch_bounds__(128, (CPT == 4 && TS <= 8) ? 4 : 2) verify_pip
     int q = (int)blockIdx.x / nblk, cb = (int)blockIdx.x - q * nblk;  // q: index into the sequence list
     constexpr int LOG_CPT = CPT == 4 ? 2 : 3;
     const int lanes = p.head_dim >> LOG_CPT;  // threads per L2 group
-    float wt[CPT][W];                         // taps and bias of the current channel block
-    float bs[CPT];
+    // taps and bias of the current channel block, channels in pairs (paired fp32 lanes: the same
+    // operations per lane as scalar code, half the instructions)
+    constexpr int P = CPT / 2;
+    f2 wt2[P][W];
+    f2 bs2[P];
     int wcb = -1;
     for (int k = 0; k < iters; ++k) {
         const int st = k & 1;
@@ -354,6 +357,7 @@ __global__ void __launch_bounds__(128, (CPT == 4 && TS <= 8) ? 4 : 2) verify_pip
         const int c = c0 + cl;
         if (cb != wcb) {  // once per block when the grid is a multiple of the channel-block count
             wcb = cb;
+            float wt[CPT][W], bs[CPT];
 #pragma unroll
             for (int e = 0; e < CPT; ++e) {
                 bs[e] = 0.0f;
@@ -374,6 +378,12 @@ __global__ void __launch_bounds__(128, (CPT == 4 && TS <= 8) ? 4 : 2) verify_pip
                     for (int e = 0; e < CPT; ++e) bs[e] = elem_f<B>(bw, e);
                 }
             }
+#pragma unroll
+            for (int q = 0; q < P; ++q) {
+                bs2[q] = f2_pack(bs[2 * q], bs[2 * q + 1]);
+#pragma unroll
+                for (int j = 0; j < W; ++j) wt2[q][j] = f2_pack(wt[2 * q][j], wt[2 * q + 1][j]);
+            }
         }
 
         const bool ok = mbar_wait_bounded(&bar[st], (unsigned)((k >> 1) & 1), first_polls);
@@ -388,7 +398,7 @@ __global__ void __launch_bounds__(128, (CPT == 4 && TS <= 8) ? 4 : 2) verify_pip
         const bool tail = chunked && first && Ts > TS;      // (its committed window is in the tail rows)
         const long long row0 = VL ? info[6 + st] : 0;       // the sequence's first packed row
 
-        float fw[CPT][R + TS];  // inputs widened to fp32: [0, R) committed window, then x
+        f2 fw2[P][R + TS];  // inputs widened to fp32, channel pairs: [0, R) committed window, then x
         uint32_t xr[TS][NW];    // raw x rows
         uint32_t sw[R * NWS];   // raw committed window, channel-major [CPT][R]
         if (go && act) {
@@ -448,7 +458,9 @@ __global__ void __launch_bounds__(128, (CPT == 4 && TS <= 8) ? 4 : 2) verify_pip
 #pragma unroll
             for (int e = 0; e < CPT; ++e)
 #pragma unroll
-                for (int kk = 0; kk < R; ++kk) fw[e][kk] = elem_f<S>(sw, e * R + kk);
+                for (int kk = 0; kk < R; ++kk) {
+                    if (e % 2 == 0) fw2[e / 2][kk] = f2_pack(elem_f<S>(sw, e * R + kk), elem_f<S>(sw, (e + 1) * R + kk));
+                }
 
             // word and half holding input j of channel e (j < R: committed window, else x_{j-R})
             auto word_of = [&](int e, int j) -> uint32_t { return j < R ? sw[(e * R + j) / EW] : xr[j - R][e / EW]; };
@@ -681,12 +693,14 @@ __global__ void __launch_bounds__(128, (CPT == 4 && TS <= 8) ? 4 : 2) verify_pip
 #pragma unroll
                 for (int t = 0; t < TS; ++t) {
 #pragma unroll
-                    for (int e = 0; e < CPT; ++e) fw[e][R + t] = elem_f<B>(xr[t], e);
+                    for (int q = 0; q < P; ++q) fw2[q][R + t] = f2_pack(elem_f<B>(xr[t], 2 * q), elem_f<B>(xr[t], 2 * q + 1));
 #pragma unroll
-                    for (int e = 0; e < CPT; ++e) {
-                        const float acc = conv_chain<CB, W>(bs[e], wt[e], &fw[e][t]);
-                        y[t][e] = silu_fast(acc);
-                        lo = fminf(lo, acc);
+                    for (int q = 0; q < P; ++q) {
+                        const f2 acc = conv_chain2<CB, W>(bs2[q], wt2[q], &fw2[q][t]);
+                        f2_unpack(silu_fast2(acc), y[t][2 * q], y[t][2 * q + 1]);
+                        float a0, a1;
+                        f2_unpack(acc, a0, a1);
+                        lo = fminf(lo, fminf(a0, a1));
                     }
                 }
                 if (lo < -80.0f) {
@@ -694,9 +708,11 @@ __global__ void __launch_bounds__(128, (CPT == 4 && TS <= 8) ? 4 : 2) verify_pip
 #pragma unroll
                     for (int t = 0; t < TS; ++t)
 #pragma unroll
-                        for (int e = 0; e < CPT; ++e) {
-                            const float acc = conv_chain<CB, W>(bs[e], wt[e], &fw[e][t]);
-                            if (acc < -80.0f) y[t][e] = silu_exact(acc);
+                        for (int q = 0; q < P; ++q) {
+                            float a0, a1;
+                            f2_unpack(conv_chain2<CB, W>(bs2[q], wt2[q], &fw2[q][t]), a0, a1);
+                            if (a0 < -80.0f) y[t][2 * q] = silu_exact(a0);
+                            if (a1 < -80.0f) y[t][2 * q + 1] = silu_exact(a1);
                         }
                 }
             } else {
@@ -721,8 +737,10 @@ __global__ void __launch_bounds__(128, (CPT == 4 && TS <= 8) ? 4 : 2) verify_pip
 #pragma unroll
                     for (int t = 0; t < TS; ++t) {
                         const float r = rsqrtf(ss[t] + p.eps);
+                        const f2 r2 = f2_pack(r, r);
 #pragma unroll
-                        for (int e = 0; e < CPT; ++e) y[t][e] *= r;
+                        for (int q = 0; q < P; ++q)
+                            f2_unpack(f2_mul(f2_pack(y[t][2 * q], y[t][2 * q + 1]), r2), y[t][2 * q], y[t][2 * q + 1]);
                     }
                 }
             }

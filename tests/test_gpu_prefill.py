@@ -98,13 +98,15 @@ def test_prefill_bad_spans_and_short_max_seqlen(cuda_lib):
     assert_out_close(got["out"].cpu(), ref["out"], "out")
 
 
-def test_prefill_equals_gpu_verify_bitwise(cuda_lib):
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_prefill_equals_gpu_verify_bitwise(cuda_lib, dtype):
     """A prompt of T tokens with an initial state gives, on the GPU, the outputs and final state of
-    a verify over the same T tokens (dense window), bit for bit."""
+    a verify over the same T tokens (dense window), bit for bit, in both dtypes (the fp32 conv rounds
+    every product, the bf16 one fuses exact products)."""
     import spec_decode_verify_gb300 as cv
-    T = 17
+    T = 17 if dtype == "bf16" else 8
     w = wl.PrefillWorkload("pv", lengths=(T, T, T), dim=4096, width=4, qk_channels=2048, head_dim=128,
-                           dtype="bf16", bias=True, seed=11)
+                           dtype=dtype, bias=True, seed=11)
     inp = wl.make_prefill_inputs(w)
     got = run_gpu(cuda_lib, w, inp)
     dev = torch.device("cuda")
