@@ -646,7 +646,7 @@ int launch_commit(const cv_commit_args *a, cudaStream_t stream) {
     int threads = p.mode == 1 ? kCommitDenseThreads : kCommitElementThreads;
     while (threads > kMinThreads && 8 * (threads / 2) >= a->dim) threads /= 2;
     const int bc = 8 * threads;
-    auto k = kernel_set(a->dtype, a->width).commit;
+    auto k = p.mode == 1 ? kernel_set(a->dtype, a->width).commit_packed : kernel_set(a->dtype, a->width).commit;
     if (ensure_smem(reinterpret_cast<const void *>(k), smem) != cudaSuccess) return CV_ERR_LAUNCH;
     if (launch_pdl(k, dim3((a->dim + bc - 1) / bc, a->n_seq), threads, smem, stream, p) != cudaSuccess)
         return CV_ERR_LAUNCH;

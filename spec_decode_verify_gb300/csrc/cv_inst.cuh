@@ -60,7 +60,8 @@ KernelSet make_set(std::integer_sequence<int, Ts...>) {
     k.tree = verify_tree<B, W>;
     // mixed dtypes: the state and the snapshots in the other dtype
     k.generic_mixed = verify_generic<B, W, OtherT<B>>;
-    k.commit = commit_kernel<B, W>;
+    k.commit = commit_kernel<B, W, false>;
+    k.commit_packed = commit_kernel<B, W, true>;
     k.commit_rows = commit_rows<B, W>;
     k.commit_cols = commit_cols<B, W>;
     k.commit_recompute = commit_recompute<B, W>;

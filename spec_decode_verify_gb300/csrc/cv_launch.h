@@ -29,7 +29,8 @@ struct KernelSet {
     VerifyKernel generic;
     VerifyKernel tree;  // draft tokens with parents (dense snapshots)
     VerifyKernel generic_mixed;  // state and snapshots in the other dtype (bf16 <-> fp32)
-    CommitKernel commit;
+    CommitKernel commit;         // element by element (mode 0)
+    CommitKernel commit_packed;  // packed dense snapshots into packed state rows (mode 1)
     CommitKernel commit_rows;
     CommitKernel commit_cols;
     CommitKernel commit_recompute;
