@@ -40,6 +40,7 @@ constexpr int kTreeBlocksPerSM = 10;  // tree verify: resident blocks per SM at 
 // verify's resident blocks while it drains
 constexpr int kCommitDenseThreads = 64;      // packed dense snapshot -> packed state (16-byte copies)
 constexpr int kCommitElementThreads = 32;    // element by element
+constexpr int kCommitWideThreads = 32;       // packed dense snapshot -> packed rows wider than the window
 constexpr int kCommitRecomputeThreads = 64;  // recompute rollback
 // dedup commit: 256 channels per block (small blocks fit beside the verify's resident blocks, so
 // more of them start, under programmatic dependent launch, while the verify drains)
@@ -613,6 +614,20 @@ int launch_commit(const cv_commit_args *a, cudaStream_t stream) {
     if (packed_state && win_ok && a->window_layout == CV_WINDOW_DENSE && a->win_ch_stride == R &&
         stride16(a->win_step_stride, esize)) {
         p.mode = 1;
+    } else if (!packed_state && win_ok && a->window_layout == CV_WINDOW_DENSE && a->win_ch_stride == R &&
+               stride16(a->win_step_stride, esize) && aligned16(a->conv_state) &&
+               stride16(a->state_slot_stride, esize) && a->state_ch_stride == a->state_cols &&
+               8LL * kCommitWideThreads * a->state_cols * esize <= device_limits().smem_per_block) {
+        // rows wider than the window: staged whole, the new window written over their first columns
+        p.mode = 5;
+        int wt = kCommitWideThreads;
+        while (wt > kMinThreads && 8 * (wt / 2) >= a->dim) wt /= 2;
+        const int sm = 8 * wt * a->state_cols * esize;
+        auto kr = kernel_set(a->dtype, a->width).commit_wide;
+        if (ensure_smem(reinterpret_cast<const void *>(kr), sm) != cudaSuccess) return CV_ERR_LAUNCH;
+        if (launch_pdl(kr, dim3((a->dim + 8 * wt - 1) / (8 * wt), a->n_seq), wt, sm, stream, p) != cudaSuccess)
+            return CV_ERR_LAUNCH;
+        return cudaGetLastError() == cudaSuccess ? CV_OK : CV_ERR_LAUNCH;
     } else if (packed_state && win_base && dedup && a->win_ch_stride == 1 && stride16(a->win_col_stride, esize)) {
         // transposed rows: each thread reads its W-1 accepted column pieces
         p.mode = 4;

@@ -12,7 +12,8 @@
 //   otherwise (mode 0), anything else: element by element.
 // They are separate kernels so that the element path's registers do not cut the packed path's
 // residency.
-// commit_rows (below) handles packed deduplicated rows with packed state rows, commit_cols the same
+// commit_wide (below) handles packed dense snapshots with packed state rows wider than the window,
+// commit_rows packed deduplicated rows with packed state rows, commit_cols the same
 // rows laid out transposed (column-major), and commit_recompute the recompute rollback (no
 // snapshots: the state is rebuilt from its kept window and the verify's inputs).
 #pragma once
@@ -101,6 +102,67 @@ __global__ void __launch_bounds__(128) commit_kernel(const __grid_constant__ Com
             }
         }
     }
+}
+
+// Commit of packed dense snapshots into packed state rows wider than the window (mode 5): the rows
+// [dim][S] per slot with S > W-1, the layout whose window the verify reads at a state offset
+// ([kda-mod] binding).  One block per (8*threads channels, sequence).  The block's rows are one
+// contiguous run: they are copied into shared memory by 16-byte cp.async copies while each thread
+// loads its 16-byte pieces of snapshot a-1 (one contiguous run as well); the new window then goes
+// over the rows' first W-1 columns in shared memory, and the rows go back whole as coalesced 16-byte
+// stores.  So every access is a 16-byte vector, every store fills whole sectors, the data costs one
+// round trip, and the other columns are written back with their own bits.
+template <typename B, int W>
+__global__ void __launch_bounds__(128) commit_wide(const __grid_constant__ CommitParams p) {
+    grid_dep_wait();
+    grid_dep_launch();
+    constexpr int R = W - 1;
+    constexpr int ES = (int)sizeof(B);
+    constexpr int VE = 16 / ES;
+    constexpr int UV = 8 * R / VE;  // 16-byte snapshot vectors per thread
+    using U = std::conditional_t<ES == 2, unsigned short, unsigned>;
+    extern __shared__ __align__(128) unsigned char smem[];
+    const int s = blockIdx.y;
+    const int tid = threadIdx.x;
+    const int NT = blockDim.x;
+    const int slot = p.cache_idx ? __ldg(p.cache_idx + s) : s;
+    const int a = __ldg(p.accept_len + s);
+    int ts, row0;
+    const int status = commit_status(p, s, slot, a, ts, row0);
+    if (p.err && blockIdx.x == 0 && tid == 0) p.err[s] = status;
+    if (slot < 0 || status || ts == 0) return;
+
+    const int c0 = blockIdx.x * 8 * NT;
+    const int nch = min(8 * NT, p.dim - c0);  // a multiple of 8 (dim % 8 == 0 on this path)
+    const int S = (int)p.st_ch;               // the row width (host: st_ch == state_cols)
+    const int nbytes = nch * S * ES;          // a multiple of 16
+    unsigned char *rows =
+        reinterpret_cast<unsigned char *>(reinterpret_cast<B *>(p.state) + (long long)slot * p.st_slot + (long long)c0 * S);
+    for (int o = tid * 16; o < nbytes; o += NT * 16) cp_async16(smem + o, rows + o);
+    const B *src = reinterpret_cast<const B *>(p.win) + (long long)s * p.w_seq + (long long)(a - 1) * p.w_step +
+                   (long long)c0 * R;
+    const int nv = nch * R / VE;
+    union {
+        uint4 v[UV];
+        U e[UV * VE];
+    } sn;
+#pragma unroll
+    for (int u = 0; u < UV; ++u)
+        if (tid + u * NT < nv) sn.v[u] = ld16(src + (tid + u * NT) * VE);
+    cp_async_wait_all();
+    __syncthreads();
+    U *img = reinterpret_cast<U *>(smem);
+#pragma unroll
+    for (int u = 0; u < UV; ++u) {
+        if (tid + u * NT < nv) {
+            const int i0 = (tid + u * NT) * VE;  // element of the snapshot run: channel i / R, column i % R
+#pragma unroll
+            for (int z = 0; z < VE; ++z) img[((i0 + z) / R) * S + (i0 + z) % R] = sn.e[u * VE + z];
+        }
+    }
+    __syncthreads();
+    for (int o = tid * 16; o < nbytes; o += NT * 16)
+        st16(rows + o, *reinterpret_cast<const uint4 *>(smem + o));
 }
 
 // Commit of packed deduplicated rows into packed state rows (mode 2): one block per (block of

@@ -62,6 +62,7 @@ KernelSet make_set(std::integer_sequence<int, Ts...>) {
     k.generic_mixed = verify_generic<B, W, OtherT<B>>;
     k.commit = commit_kernel<B, W, false>;
     k.commit_packed = commit_kernel<B, W, true>;
+    k.commit_wide = commit_wide<B, W>;
     k.commit_rows = commit_rows<B, W>;
     k.commit_cols = commit_cols<B, W>;
     k.commit_recompute = commit_recompute<B, W>;

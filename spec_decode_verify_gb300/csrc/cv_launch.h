@@ -31,6 +31,7 @@ struct KernelSet {
     VerifyKernel generic_mixed;  // state and snapshots in the other dtype (bf16 <-> fp32)
     CommitKernel commit;         // element by element (mode 0)
     CommitKernel commit_packed;  // packed dense snapshots into packed state rows (mode 1)
+    CommitKernel commit_wide;    // packed dense snapshots into packed rows wider than the window (mode 5)
     CommitKernel commit_rows;
     CommitKernel commit_cols;
     CommitKernel commit_recompute;

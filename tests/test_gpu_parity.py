@@ -447,6 +447,24 @@ def test_token_groups_one_pass(cuda_lib, dtype, T, width, offset):
     check_verify_and_commit(cuda_lib, w, inp)
 
 
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("width", [2, 3, 4])
+@pytest.mark.parametrize("T,dim", [(2, 8), (3, 520), (8, 1000), (17, 264), (128, 256)])
+def test_commit_wide_rows(cuda_lib, dtype, width, T, dim):
+    """Dense snapshots committed into packed state rows wider than the window (the rows a verify
+    reads at a state offset): the rows are staged whole and written back whole, so besides the new
+    window in the first W-1 columns every other column must keep its bits.  Partial last channel
+    blocks, padded sequences, a pool of unused slots, every accept count; rows of up to 130 fp32
+    columns."""
+    w = wl.VerifyWorkload("widecommit", n_seq=6, T=T, dim=dim, width=width, qk_channels=0, head_dim=8, dtype=dtype,
+                          layout="dense", bias=True, n_pad=1, extra_slots=3, state_offset=True,
+                          seed=1000 * width + 10 * T + dim)
+    inp = wl.make_inputs(w)
+    inp["accept_len"] = (torch.arange(w.n_seq, dtype=torch.int32) % T + 1).contiguous()
+    inp["state_off"] = (inp["accept_len"] - 1).contiguous()
+    check_verify_and_commit(cuda_lib, w, inp)
+
+
 def test_maximum_batch_on_gpu(cuda_lib):
     """The largest batch the ABI accepts (65535 sequences; the pipelined kernel then walks every
     sequence without a shared-memory list), with padded sequences and a pool of unused slots."""
