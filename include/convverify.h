@@ -260,7 +260,9 @@ CV_API int cv_conv_verify(const cv_verify_args *args, void *stream);
  * For every sequence s with slot = cache_idx ? cache_idx[s] : s, slot >= 0, and a = accept_len[s]
  * read on the device (no host round trip), 1 <= a <= T:
  *     conv_state[slot][c][k] = snapshot (s, a-1, c, k)      for every c < dim, k < W-1
- * a = T rewrites the state with the value it already holds.  A sequence whose a is out of range
+ * a = T rewrites the state with the value it already holds.  State columns >= W-1 keep their
+ * values (packed rows wider than the window may be written back whole with those columns' own
+ * bits, so nothing else may write them during the call).  A sequence whose a is out of range
  * gets CV_SEQ_BAD_ACCEPT in err[s] and is untouched.  Packed deduplicated rows are staged by a
  * bulk copy per block with a bounded wait (wait_polls, as in cv_verify_args; a timeout flags
  * CV_SEQ_TIMEOUT and leaves the block's channels unwritten); that kernel ORs its bits into err,
