@@ -108,6 +108,12 @@ __global__ void __launch_bounds__(128, (CPT == 4 && TS <= 8) ? 4 : 2) verify_pip
     const int SCS = hist_t ? R : SC;            // state columns per staged channel (or staged columns)
     const bool whole_rows = !hist_t && SC != R;
     const bool wide = whole_rows && !hist;  // wider rows, not history: staged whole, stored whole
+    // mixed dtypes: each thread stores its committed-window run straight to the packed state rows
+    // (coalesced vectors) instead of through a shared-memory image and a bulk copy, so that the
+    // larger fp32 images leave room for a third block per SM (measured, bf16 x with fp32 state and
+    // rows, 128 x 8 x 10240: 23.1 us against 24.2 with two blocks per SM; storing the dedup rows
+    // from registers too, for four blocks per SM, took 27.5 us)
+    const bool direct_state = MIXED && !wide && !hist && !recomp;
 
     // packed drafts longer than a chunk: W-1 more staged x rows per unit (a halo or a tail)
     const bool chunked = VL && p.T > TS;
@@ -122,7 +128,8 @@ __global__ void __launch_bounds__(128, (CPT == 4 && TS <= 8) ? 4 : 2) verify_pip
     const long long xb = pipe_part((long long)XR * BC * ES);
     const long long stage_bytes = xb + pipe_part((long long)SCS * BC * ESS);
     const long long rb = dense ? 0 : pipe_part((long long)Q * BC * ESS);
-    const long long img_bytes = recomp ? 0 : rb + (hist ? 0 : pipe_part((long long)(wide ? SC : R) * BC * ESS));
+    const long long img_bytes =
+        recomp ? 0 : rb + ((hist || direct_state) ? 0 : pipe_part((long long)(wide ? SC : R) * BC * ESS));
     unsigned char *const img0 = smem + 2 * stage_bytes;
     uint64_t *const bar = reinterpret_cast<uint64_t *>(img0 + 2 * img_bytes);
     // [0, 2): slots, [2, 4): state offsets, [4, 6): draft counts, [6, 8): first rows (packed drafts)
@@ -582,6 +589,8 @@ __global__ void __launch_bounds__(128, (CPT == 4 && TS <= 8) ? 4 : 2) verify_pip
 #pragma unroll
                         for (int kk = 0; kk < R; ++kk) drow[e * SC + kk] = (S)elem_raw<S>(fin, e * R + kk);
                 }
+            } else if (direct_state) {
+                stv<VS, R * NWS>(reinterpret_cast<S *>(p.state) + (long long)slot * p.st_slot + (long long)c * R, fin);
             } else if (!hist && !recomp) {
                 stv<VS, R * NWS>(stimg + (long long)tid * CPT * R * ESS, fin);
             }
@@ -630,7 +639,7 @@ __global__ void __launch_bounds__(128, (CPT == 4 && TS <= 8) ? 4 : 2) verify_pip
                 } else if (!dense && full_row) {
                     bulk_store(row_dst, img, (unsigned)(nch * Q * ESS));
                 }
-                if (!hist && first)  // (SC == W-1 unless the rows are wide)
+                if (!hist && first && !direct_state)  // (SC == W-1 unless the rows are wide)
                     bulk_store(reinterpret_cast<S *>(p.state) + (long long)slot * p.st_slot + (long long)c0 * SC, stimg,
                                (unsigned)(nch * SC * ESS));
                 asm volatile("cp.async.bulk.commit_group;\n" ::: "memory");

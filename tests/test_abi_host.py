@@ -384,7 +384,8 @@ def test_prefill_aliasing_and_empty(lib):
 
 def test_mixed_dtypes_plan_and_validation(lib):
     """bf16 x with an fp32 state (and the reverse) plan the pipelined kernel for T <= 8, its stage
-    and image parts sized in each part's own dtype, and the general kernel with an fp32 tile above
+    and image parts sized in each part's own dtype (no committed-window image: mixed dtypes store
+    those runs from registers), and the general kernel with an fp32 tile above
     that; unknown state dtypes are rejected."""
     part = lambda b: (b + 127) // 128 * 128
     w = W3.replace(state_dtype="f32", n_seq=4, n_pad=0, extra_slots=0)
@@ -394,7 +395,7 @@ def test_mixed_dtypes_plan_and_validation(lib):
     assert rc == 0 and pl.path == 3 and pl.stages == 2
     bc = pl.channels_per_block
     stage = part(8 * bc * 2) + part(3 * bc * 4)  # bf16 x rows, fp32 committed windows
-    image = part(10 * bc * 4) + part(3 * bc * 4)  # fp32 dedup row, fp32 committed window
+    image = part(10 * bc * 4)  # fp32 dedup row (the committed windows go straight to the state)
     assert pl.smem_bytes == _pipe_smem(stage, image, 4)
     a.state_dtype = 3
     assert _plan(lib, a)[0] == -6
@@ -403,7 +404,7 @@ def test_mixed_dtypes_plan_and_validation(lib):
     rc, pl2 = _plan(lib, a2)
     assert a2.state_dtype == 2 and rc == 0 and pl2.path == 3
     bc = pl2.channels_per_block
-    assert pl2.smem_bytes == _pipe_smem(part(8 * bc * 4) + part(3 * bc * 2), part(10 * bc * 2) + part(3 * bc * 2), 4)
+    assert pl2.smem_bytes == _pipe_smem(part(8 * bc * 4) + part(3 * bc * 2), part(10 * bc * 2), 4)
     # T = 9: no mixed pipelined kernel; the general kernel's tile holds fp32 bits
     w3 = W3.replace(state_dtype="f32", T=9, n_seq=4, n_pad=0, extra_slots=0)
     rc, pl3 = _plan(lib, _args(w3))
