@@ -108,12 +108,14 @@ __global__ void __launch_bounds__(128, (CPT == 4 && TS <= 8) ? 4 : 2) verify_pip
     const int SCS = hist_t ? R : SC;            // state columns per staged channel (or staged columns)
     const bool whole_rows = !hist_t && SC != R;
     const bool wide = whole_rows && !hist;  // wider rows, not history: staged whole, stored whole
-    // mixed dtypes: each thread stores its committed-window run straight to the packed state rows
-    // (coalesced vectors) instead of through a shared-memory image and a bulk copy, so that the
-    // larger fp32 images leave room for a third block per SM (measured, bf16 x with fp32 state and
-    // rows, 128 x 8 x 10240: 23.1 us against 24.2 with two blocks per SM; storing the dedup rows
-    // from registers too, for four blocks per SM, took 27.5 us)
-    const bool direct_state = MIXED && !wide && !hist && !recomp;
+    // Each thread stores its committed-window run straight to the packed state rows (coalesced
+    // vectors) instead of through a shared-memory image and a bulk copy: with mixed dtypes, so that
+    // the larger fp32 images leave room for a third block per SM (measured, bf16 x with fp32 state
+    // and rows, 128 x 8 x 10240: 23.1 us against 24.2 with two blocks per SM; storing the dedup rows
+    // from registers too, for four blocks per SM, took 27.5 us); with transposed rows and packed
+    // drafts, where it measured faster (step 19.18 against 19.46 us, and 31.9 against 32.0), but
+    // not with row-major rows (19.64 against 19.47).
+    const bool direct_state = (MIXED || dedup_t || VL) && !wide && !hist && !recomp;
 
     // packed drafts longer than a chunk: W-1 more staged x rows per unit (a halo or a tail)
     const bool chunked = VL && p.T > TS;
@@ -590,7 +592,8 @@ __global__ void __launch_bounds__(128, (CPT == 4 && TS <= 8) ? 4 : 2) verify_pip
                         for (int kk = 0; kk < R; ++kk) drow[e * SC + kk] = (S)elem_raw<S>(fin, e * R + kk);
                 }
             } else if (direct_state) {
-                stv<VS, R * NWS>(reinterpret_cast<S *>(p.state) + (long long)slot * p.st_slot + (long long)c * R, fin);
+                if (first)  // (chunk 0 of a packed draft writes the state)
+                    stv<VS, R * NWS>(reinterpret_cast<S *>(p.state) + (long long)slot * p.st_slot + (long long)c * R, fin);
             } else if (!hist && !recomp) {
                 stv<VS, R * NWS>(stimg + (long long)tid * CPT * R * ESS, fin);
             }

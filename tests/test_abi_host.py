@@ -262,7 +262,9 @@ def test_plan_general_path_cases(lib):
     assert _plan(lib, _args(W3.replace(T=12)))[1].path == 3
     a = _args(W3)
     a.win_ch_stride, a.win_col_stride, a.win_step_stride = 1, W3.dim, W3.dim
-    assert _plan(lib, a)[1].path == 3
+    pl = _plan(lib, a)[1]
+    # the transposed row image, and no committed-window image (those runs go out from registers)
+    assert pl.path == 3 and pl.smem_bytes == _pipe_smem((8 + 3) * 512 * 2, 10 * 512 * 2, 128)
     a.win_col_stride = a.win_step_stride = W3.dim + 4  # columns 8 bytes off 16-byte alignment
     assert _plan(lib, a)[1].path == 0
     a = _args(W3)
@@ -591,8 +593,8 @@ def _ragged_args(w, **over):
 def test_plan_packed_drafts_pipelined(lib):
     """Packed ragged drafts of up to 16 tokens at the benchmark shape take the pipelined kernel in
     units of 8-token chunks: stages of 8 + 3 x rows (the chunk, then its halo or the draft's tail)
-    and the committed windows, images of 8 + 2 columns, the sort scratch and a list of 2 chunks per
-    sequence."""
+    and the committed windows, row images of 8 + 2 columns (no committed-window image), the sort
+    scratch and a list of 2 chunks per sequence."""
     a = _ragged_args(RAG)
     rc, pl = _plan(lib, a)
     assert rc == 0 and pl.path == 3
@@ -602,7 +604,7 @@ def test_plan_packed_drafts_pipelined(lib):
     def part(b):
         return (b + 127) // 128 * 128
     stage = part((8 + R) * bc * 2) + part(R * bc * 2)
-    image = part(Q * bc * 2) + part(R * bc * 2)
+    image = part(Q * bc * 2)  # (the committed windows go straight from registers to the state)
     assert pl.smem_bytes == _pipe_smem(stage, image, RAG.n_seq, varlen_T=RAG.T)
     # longer drafts (T = 40: 5 chunks per sequence) still fit the list; history rows do not chunk
     assert _plan(lib, _ragged_args(RAG.replace(T=40)))[1].path == 3
