@@ -346,10 +346,10 @@ int plan_verify(const cv_verify_args *a, cv_launch_plan *pl) {
         // the state's dtype; 2 mbarriers, 2 slots, 2 offsets
         const long long stage = part((long long)(ts + (chunked ? R : 0)) * bc * esize) +
                                 part((long long)(hist_t ? R : a->state_cols) * bc * ssize);
-        // (mixed dtypes, transposed rows and packed drafts store the committed windows straight from
-        // registers: no state image)
+        // (mixed dtypes and packed drafts store the committed windows straight from registers: no
+        // state image)
         long long image =
-            (hist || recomp || ((mixed || dedup_t || varlen) && !wide)) ? 0 : part((wide ? a->state_cols : R) * bc * ssize);
+            (hist || recomp || ((mixed || varlen) && !wide)) ? 0 : part((wide ? a->state_cols : R) * bc * ssize);
         if (a->window_layout == CV_WINDOW_DEDUP || hist) image += part(Q * bc * ssize);
         const long long smem = 2 * stage + 2 * image + cvk::kPipeInfoBytes +
                                (pipe_compacts(a) ? 4LL * cvk::pipe_aux_ints(varlen, ts) + (varlen ? 4LL : 12LL) * pipe_list_len(a) : 0);

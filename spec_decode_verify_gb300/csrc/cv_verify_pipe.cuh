@@ -112,10 +112,11 @@ __global__ void __launch_bounds__(128, (CPT == 4 && TS <= 8) ? 4 : 2) verify_pip
     // vectors) instead of through a shared-memory image and a bulk copy: with mixed dtypes, so that
     // the larger fp32 images leave room for a third block per SM (measured, bf16 x with fp32 state
     // and rows, 128 x 8 x 10240: 23.1 us against 24.2 with two blocks per SM; storing the dedup rows
-    // from registers too, for four blocks per SM, took 27.5 us); with transposed rows and packed
-    // drafts, where it measured faster (step 19.18 against 19.46 us, and 31.9 against 32.0), but
-    // not with row-major rows (19.64 against 19.47).
-    const bool direct_state = (MIXED || dedup_t || VL) && !wide && !hist && !recomp;
+    // from registers too, for four blocks per SM, took 27.5 us), and with packed drafts (ragged
+    // step 31.9 against 32.0 us).  Only where the kernel's type parameters decide it: as a runtime
+    // choice (for transposed rows, where it measured 19.18 against 19.46 us) the extra branch cost
+    // the row-major rows 0.1 us.
+    const bool direct_state = (MIXED || VL) && !wide && !hist && !recomp;
 
     // packed drafts longer than a chunk: W-1 more staged x rows per unit (a halo or a tail)
     const bool chunked = VL && p.T > TS;

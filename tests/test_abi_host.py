@@ -263,8 +263,8 @@ def test_plan_general_path_cases(lib):
     a = _args(W3)
     a.win_ch_stride, a.win_col_stride, a.win_step_stride = 1, W3.dim, W3.dim
     pl = _plan(lib, a)[1]
-    # the transposed row image, and no committed-window image (those runs go out from registers)
-    assert pl.path == 3 and pl.smem_bytes == _pipe_smem((8 + 3) * 512 * 2, 10 * 512 * 2, 128)
+    # the transposed row image and the committed-window image
+    assert pl.path == 3 and pl.smem_bytes == _pipe_smem((8 + 3) * 512 * 2, (10 + 3) * 512 * 2, 128)
     a.win_col_stride = a.win_step_stride = W3.dim + 4  # columns 8 bytes off 16-byte alignment
     assert _plan(lib, a)[1].path == 0
     a = _args(W3)
