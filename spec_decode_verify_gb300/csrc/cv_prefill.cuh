@@ -24,6 +24,19 @@
 namespace cvk {
 
 constexpr int kPrefillBatch = 8;  // tokens per batch; the next batch's rows load during this one
+constexpr int kPrefillRing = 3;   // batches of x rows staged in shared memory: 2 in flight, 1 in use
+
+// cp.async of BYTES (8 or 16) into shared memory, zero-filled past src_bytes (0: nothing is read)
+template <int BYTES>
+__device__ __forceinline__ void prefill_cp_async(void *dst, const void *src, unsigned src_bytes) {
+    if constexpr (BYTES == 16)
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(smem_u32(dst)), "l"(src), "r"(src_bytes)
+                     : "memory");
+    else
+        asm volatile("cp.async.ca.shared.global [%0], [%1], %2, %3;\n" ::"r"(smem_u32(dst)), "l"(src), "n"(BYTES),
+                     "r"(src_bytes)
+                     : "memory");
+}
 
 template <typename B, int W, int CPT>
 __global__ void __launch_bounds__(128, CPT == 4 ? 4 : 2) prefill_conv(const __grid_constant__ PrefillParams p) {
@@ -134,15 +147,8 @@ __global__ void __launch_bounds__(128, CPT == 4 ? 4 : 2) prefill_conv(const __gr
 #pragma unroll
         for (int k = 0; k < R; ++k) win2[q][k] = f2_pack(win[2 * q][k], win[2 * q + 1][k]);
     }
-    uint32_t xn[U][NW];  // the next batch, in flight while this one is computed
-    if (t0 < t1) load_batch(xn, t0);
-    for (int tb = t0; tb < t1; tb += U) {
-        uint32_t xr[U][NW];
-#pragma unroll
-        for (int u = 0; u < U; ++u)
-#pragma unroll
-            for (int i = 0; i < NW; ++i) xr[u][i] = xn[u][i];
-        if (tb + U < t1) load_batch(xn, tb + U);
+    // conv + SiLU + L2 + stores of the batch of rows xr starting at token tb
+    auto run_batch = [&](const uint32_t (*xr)[NW], int tb) {
         float y[U][CPT];
         f2 acc2[U][P];
         float lo = 0.0f;
@@ -219,6 +225,62 @@ __global__ void __launch_bounds__(128, CPT == 4 ? 4 : 2) prefill_conv(const __gr
                 for (int j = 0; j < CPT; ++j)
                     if (j < my) dst[j] = narrow<B>(y[u][j]);
             }
+        }
+    };
+
+    extern __shared__ __align__(16) unsigned char ring[];
+    const int NT = blockDim.x;
+    constexpr int RB = CPT * ES;  // bytes of a thread's piece of one x row: 8, 16 or 32
+    if (p.x_vec && dynamic_smem_bytes() >= (unsigned)(kPrefillRing * U * NT * RB)) {
+        // aligned rows: each thread stages its own RB-byte pieces of the next batches in shared
+        // memory by cp.async ([batch][row][thread] cells, conflict-free), kPrefillRing - 1 batches
+        // ahead, so no register holds data in flight.  With x_vec a thread has all CPT channels or
+        // none (dim % 8 == 0); one with none, and rows past the chunk, get zeros and read nothing
+        // (their source address is the row base, inside the buffer).
+        constexpr int D = kPrefillRing;
+        auto cell = [&](int slot, int u) { return ring + ((size_t)(slot * U + u) * NT + tid) * RB; };
+        auto issue = [&](int k, int nb) {
+            if (k < nb) {
+                const int tb = t0 + k * U;
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const bool ok = my > 0 && tb + u < t1;
+                    const B *src = ok ? xq + ((long long)b + tb + u) * p.x_tok : reinterpret_cast<const B *>(p.x);
+                    if constexpr (RB == 8) {
+                        prefill_cp_async<8>(cell(k % D, u), src, ok ? 8u : 0u);
+                    } else {
+#pragma unroll
+                        for (int h = 0; h < RB / 16; ++h)
+                            prefill_cp_async<16>(cell(k % D, u) + 16 * h, reinterpret_cast<const unsigned char *>(src) + (ok ? 16 * h : 0),
+                                                 ok ? 16u : 0u);
+                    }
+                }
+            }
+            asm volatile("cp.async.commit_group;\n" ::: "memory");  // (an empty group past the end)
+        };
+        const int nb = (t1 - t0 + U - 1) / U;
+#pragma unroll
+        for (int k = 0; k < D - 1; ++k) issue(k, nb);
+        for (int k = 0; k < nb; ++k) {
+            issue(k + D - 1, nb);  // into the cell batch k - 1 was read from
+            asm volatile("cp.async.wait_group %0;\n" ::"n"(D - 1) : "memory");  // batch k has landed
+            uint32_t xr[U][NW];
+#pragma unroll
+            for (int u = 0; u < U; ++u) ldv<VX, NW>(xr[u], cell(k % D, u));
+            run_batch(xr, t0 + k * U);
+        }
+        asm volatile("cp.async.wait_group 0;\n" ::: "memory");
+    } else {
+        uint32_t xn[U][NW];  // the next batch, in flight while this one is computed
+        if (t0 < t1) load_batch(xn, t0);
+        for (int tb = t0; tb < t1; tb += U) {
+            uint32_t xr[U][NW];
+#pragma unroll
+            for (int u = 0; u < U; ++u)
+#pragma unroll
+                for (int i = 0; i < NW; ++i) xr[u][i] = xn[u][i];
+            if (tb + U < t1) load_batch(xn, tb + U);
+            run_batch(xr, tb);
         }
     }
 
