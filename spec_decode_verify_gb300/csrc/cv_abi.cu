@@ -54,7 +54,7 @@ constexpr int kCommitColThreadsPacked = 32;
 constexpr int kCompactMaxEntries = 1024;
 constexpr int kPrefillMaxChunk = 128;  // tokens per prefill block, at most / at least (multiples of
 constexpr int kPrefillMinChunk = 32;   // the kernel's 8-token batch, and >= W-1)
-constexpr int kPrefillRing = 3;        // batches of staged x rows per prefill thread (as the kernel's)
+constexpr int kPrefillRing = 4;        // batches of staged x rows per prefill thread (as the kernel's)
 
 // The device the launch plans size for: SM count (the persistent grids), shared memory per SM
 // (residency) and per block (opt-in maximum), queried once per device and cached.  Without a

@@ -8,13 +8,16 @@
 //
 // The conv needs only the W-1 inputs before each token, so the work is a stencil in time: block
 // (channel block, chunk, sequence) covers a chunk of tokens of one sequence (the host picks its
-// length, 32..256) for CPT*threads channels.  Its halo is the sequence's initial window (the cached state, or zeros without one)
+// length, 32..128) for CPT*threads channels.  Its halo is the sequence's initial window (the cached state, or zeros without one)
 // for the first chunk and the W-1 x rows before the chunk otherwise (a chunk is at least W-1
 // tokens long).  Each thread keeps its channels' window in registers and walks the chunk 8 tokens
-// at a time: the next batch's 8 x rows are loaded (vector loads when aligned) while this batch's
-// conv + SiLU, batched L2 shuffle trees, rounding and stores run.  The launch bounds hold a
-// thread to 128 registers (4 blocks, 16 warps per SM), which beat more registers with fewer
-// warps, smaller batches with more warps, and a bulk-copy ring of staged rows when timed.  The first chunk's block also writes the
+// at a time.  With aligned rows it stages its own pieces of the next x rows in a shared-memory ring
+// by cp.async, 3 batches ahead, while this batch's conv + SiLU, batched L2 shuffle trees, rounding
+// and stores run (otherwise the next batch's rows are loaded into registers).  The launch bounds
+// hold a thread to 128 registers (4 blocks, 16 warps per SM), which beat more registers with fewer
+// warps, fewer registers with more warps, smaller batches with more warps, and a bulk-copy ring of
+// staged rows when timed; ring depths of 2 / 3 / 4 batches measured 262.1 / 262.9 / 260.8 us on
+// 30,822 tokens at dim 10240, against 267.1 with registers only.  The first chunk's block also writes the
 // final window -- the last W-1 entries of [initial window, x] -- into the state: it is the only
 // block that reads the initial window, so no other block races with that write.
 #pragma once
@@ -24,7 +27,7 @@
 namespace cvk {
 
 constexpr int kPrefillBatch = 8;  // tokens per batch; the next batch's rows load during this one
-constexpr int kPrefillRing = 3;   // batches of x rows staged in shared memory: 2 in flight, 1 in use
+constexpr int kPrefillRing = 4;   // batches of x rows staged in shared memory: 3 in flight, 1 in use
 
 // cp.async of BYTES (8 or 16) into shared memory, zero-filled past src_bytes (0: nothing is read)
 template <int BYTES>
