@@ -57,16 +57,17 @@ def test_named_prefill_workloads(cuda_lib, name):
 
 @pytest.mark.parametrize("case", range(24))
 def test_prefill_random_sweep(cuda_lib, case):
-    """Random batches: W 2..4, fp32/bf16, head_dim 8..256, ragged dims, lengths around the 256-token
-    chunk (0, 1, 255, 256, 257, ...), padded sequences, missing initial states, x rows with an odd
-    stride (scalar path)."""
+    """Random batches: W 2..4, fp32/bf16, head_dim 8..256, ragged dims, lengths around the chunk
+    boundaries (0, 1, 127, 128, 129, 255, 256, 257, ...), padded sequences, missing initial states,
+    x rows with an odd stride or an odd dim (the register path) and aligned rows (the shared-memory
+    ring, 8-, 16- and 32-byte pieces per thread and row)."""
     rng = np.random.default_rng(9000 + case)
     W = int(rng.integers(2, 5))
     hd = int(rng.choice([8, 16, 32, 64, 128, 256]))
     groups = int(rng.integers(0, 4))
     dim = groups * hd + int(rng.integers(1, 300)) if case % 2 else groups * hd + 8 * int(rng.integers(1, 40))
     n = int(rng.integers(1, 6))
-    lengths = tuple(int(rng.choice([0, 1, 2, 7, 255, 256, 257, 300, 513, 1000])) for _ in range(n))
+    lengths = tuple(int(rng.choice([0, 1, 2, 7, 127, 128, 129, 255, 256, 257, 300, 513, 1000])) for _ in range(n))
     pad = tuple(i for i in range(n) if rng.random() < 0.2)
     no_init = tuple(i for i in range(n) if rng.random() < 0.4)
     w = wl.PrefillWorkload("rand", lengths=lengths, dim=dim, width=W, qk_channels=groups * hd, head_dim=hd,
