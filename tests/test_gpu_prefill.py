@@ -77,6 +77,19 @@ def test_prefill_random_sweep(cuda_lib, case):
     check(cuda_lib, w, wl.make_prefill_inputs(w))
 
 
+@pytest.mark.parametrize("dtype,hd", [("bf16", 128), ("bf16", 256), ("f32", 128), ("f32", 256)])
+def test_prefill_ring_pieces(cuda_lib, dtype, hd):
+    """Aligned rows take the shared-memory ring of staged x rows: each thread's piece of a row is 8
+    bytes (bf16, 4 channels), 16 (bf16, 8 channels for a 256-channel group; fp32, 4 channels) or
+    32 (fp32, 8 channels).  Lengths end inside, at and just past the 128-token chunks, with prompts
+    without a state, a padded prompt and a partly filled channel block."""
+    dim = 2 * hd + 8 * 9
+    w = wl.PrefillWorkload("ring", lengths=(1, 128, 129, 300, 1000, 7), dim=dim, width=4, qk_channels=2 * hd,
+                           head_dim=hd, dtype=dtype, bias=True, pad=(5,), no_init=(0, 3), extra_slots=2,
+                           seed=hd + (1 if dtype == "f32" else 0))
+    check(cuda_lib, w, wl.make_prefill_inputs(w))
+
+
 def test_prefill_bad_spans_and_short_max_seqlen(cuda_lib):
     """Reversed or out-of-range spans, and a span longer than max_seqlen, are flagged (16) and
     touch nothing; the other sequences are processed."""
